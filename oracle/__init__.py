@@ -1,0 +1,364 @@
+"""CPU oracle for the entropy-coded weight path -- TEST INFRASTRUCTURE ONLY.
+
+The library under lossless_entropy_coded_gb300/ never imports this package.
+Only tests/, ``__graft_entry__.smoke()`` and the CPU-baseline leg of bench.py
+use it.  The arithmetic lives in ``oracle.c`` (plain C, FP64 sums in index
+order); this module only marshals arrays through ctypes.
+
+Functions and the passages they follow (page titles and sections):
+  entropy, cross_entropy        DFloat11 Eq.(2); MINE sec. 4.2 "Compressed Size Prediction"
+  huffman_textbook              DFloat11 sec. "entropy coding" (Huffman's merge rule)
+  package_merge                 Larmore & Hirschberg's optimal length-limited code
+  canonical_codes               consistent with DFloat11 Fig. 13
+  flat_lut / hier_luts          DFloat11 appendix, Fig. 13 and Fig. 14
+  DF11 (encode/decode)          DFloat11 sec. "Dynamic-Length Float", "two-phase kernel", Algorithm 1
+  Rans (encode/decode)          EntroPack sec. 3.6 and appendix C.3; Duda's rANS
+  gemv_bf16 / gemv_rans         y = W x with FP64 accumulation
+
+Every function is pinned by tests in tests/test_oracle_*.py against the pages'
+worked examples, closed forms, invariants or brute force.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so next to its source (plain gcc)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                               "-Wall", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _L():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB)
+    vp, i64, i32, f64, u16 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_uint16
+    sig = {
+        "orc_bf16_to_f64": ([u16], f64),
+        "orc_f16_to_f32": ([u16], ctypes.c_float),
+        "orc_f32_to_bf16_rne": ([ctypes.c_float], u16),
+        "orc_entropy": ([vp, i32], f64),
+        "orc_cross_entropy": ([vp, vp, i32, i32], f64),
+        "orc_huffman_textbook": ([vp, vp], i32),
+        "orc_package_merge": ([vp, i32, vp], i32),
+        "orc_code_lengths": ([vp, i32, vp], i32),
+        "orc_canonical_codes": ([vp, vp], None),
+        "orc_flat_lut": ([vp, vp, i32, vp], i32),
+        "orc_hier_luts": ([vp, vp, i32, vp, i32], i32),
+        "orc_df11_encode": ([vp, i64, i32, i32, i32], vp),
+        "orc_df11_decode": ([vp, vp], i32),
+        "orc_df11_free": ([vp], None),
+        "orc_df11_info": ([vp, vp], i64),
+        "orc_df11_lengths": ([vp], vp),
+        "orc_df11_codes": ([vp], vp),
+        "orc_df11_counts": ([vp], vp),
+        "orc_df11_stream": ([vp], vp),
+        "orc_df11_gaps": ([vp], vp),
+        "orc_df11_block_pos": ([vp], vp),
+        "orc_df11_luts": ([vp], vp),
+        "orc_df11_sm_mut": ([vp], vp),
+        "orc_df11_stream_mut": ([vp], vp),
+        "orc_rans_freqs": ([vp, i32, vp], i32),
+        "orc_rans_encode": ([vp, i64, i32, i32], vp),
+        "orc_rans_decode": ([vp, vp, vp], i32),
+        "orc_rans_free": ([vp], None),
+        "orc_rans_info": ([vp, vp], i64),
+        "orc_rans_freqs_of": ([vp], vp),
+        "orc_rans_counts_of": ([vp], vp),
+        "orc_rans_states": ([vp], vp),
+        "orc_rans_offsets": ([vp], vp),
+        "orc_rans_payload_mut": ([vp], vp),
+        "orc_rans_dequant_bf16": ([vp, vp, i64, i64, i32, vp], None),
+        "orc_gemv_bf16": ([vp, i64, i64, vp, i32, vp, i64, vp, vp], None),
+        "orc_gemv_rans": ([vp, vp, i64, i64, i32, vp, i32, vp, i64, vp, vp], None),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _p(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"], "arrays passed to the oracle must be C-contiguous"
+    return a.ctypes.data
+
+
+def _view(addr: int, dtype, n: int) -> np.ndarray:
+    if n == 0:
+        return np.empty(0, dtype=dtype)
+    buf = (ctypes.c_char * (n * np.dtype(dtype).itemsize)).from_address(addr)
+    return np.frombuffer(buf, dtype=dtype, count=n).copy()
+
+
+# --------------------------------------------------------------------------- scalars
+def bf16_to_f64(h: int) -> float:
+    return float(_L().orc_bf16_to_f64(h))
+
+
+def f16_to_f32(h: int) -> float:
+    return float(_L().orc_f16_to_f32(h))
+
+
+def f32_to_bf16_rne(f: float) -> int:
+    return int(_L().orc_f32_to_bf16_rne(f))
+
+
+# --------------------------------------------------------------------------- entropy
+def entropy(counts) -> float:
+    c = np.ascontiguousarray(counts, dtype=np.uint64)
+    return float(_L().orc_entropy(_p(c), len(c)))
+
+
+def cross_entropy(counts, freqs, prob_bits: int) -> float:
+    c = np.ascontiguousarray(counts, dtype=np.uint64)
+    f = np.ascontiguousarray(freqs, dtype=np.uint32)
+    return float(_L().orc_cross_entropy(_p(c), _p(f), len(c), prob_bits))
+
+
+# --------------------------------------------------------------------------- Huffman
+def _counts256(counts) -> np.ndarray:
+    c = np.zeros(256, dtype=np.uint64)
+    cc = np.asarray(counts, dtype=np.uint64)
+    c[: len(cc)] = cc
+    return c
+
+
+def huffman_textbook(counts) -> np.ndarray:
+    c = _counts256(counts)
+    out = np.zeros(256, dtype=np.uint8)
+    _L().orc_huffman_textbook(_p(c), _p(out))
+    return out
+
+
+def package_merge(counts, max_len: int) -> np.ndarray:
+    c = _counts256(counts)
+    out = np.zeros(256, dtype=np.uint8)
+    if _L().orc_package_merge(_p(c), max_len, _p(out)) < 0:
+        raise ValueError("no prefix code with that length limit")
+    return out
+
+
+def code_lengths(counts, max_len: int = 24) -> np.ndarray:
+    c = _counts256(counts)
+    out = np.zeros(256, dtype=np.uint8)
+    if _L().orc_code_lengths(_p(c), max_len, _p(out)) < 0:
+        raise ValueError("no prefix code with that length limit")
+    return out
+
+
+def canonical_codes(lengths) -> np.ndarray:
+    ln = np.zeros(256, dtype=np.uint8)
+    ln[: len(lengths)] = lengths
+    out = np.zeros(256, dtype=np.uint32)
+    _L().orc_canonical_codes(_p(ln), _p(out))
+    return out
+
+
+def flat_lut(lengths, codes, L: int) -> np.ndarray:
+    ln = np.zeros(256, dtype=np.uint8)
+    ln[: len(lengths)] = lengths
+    cd = np.zeros(256, dtype=np.uint32)
+    cd[: len(codes)] = codes
+    out = np.zeros(1 << L, dtype=np.int16)
+    if _L().orc_flat_lut(_p(ln), _p(cd), L, _p(out)) < 0:
+        raise ValueError("flat LUT needs L >= the longest code")
+    return out
+
+
+def hier_luts(lengths, codes, b: int, max_tables: int = 4096) -> np.ndarray:
+    """Returns [k, 2^b] int16: 0..255 symbol, 256+t pointer to table t, -1 unused."""
+    ln = np.zeros(256, dtype=np.uint8)
+    ln[: len(lengths)] = lengths
+    cd = np.zeros(256, dtype=np.uint32)
+    cd[: len(codes)] = codes
+    buf = np.zeros(max_tables * (1 << b), dtype=np.int16)
+    k = _L().orc_hier_luts(_p(ln), _p(cd), b, _p(buf), max_tables)
+    if k < 0:
+        raise ValueError("too many tables")
+    return buf[: k * (1 << b)].reshape(k, 1 << b)
+
+
+# --------------------------------------------------------------------------- DF11 codec
+class DF11:
+    """DFloat11-format encoding of a BF16 array (EncodedExponent, PackedSignMantissa,
+    Gaps, BlockOutputPos, hierarchical LUTs with b = 8)."""
+
+    def __init__(self, w_bf16: np.ndarray, max_len: int = 24, n_bytes: int = 8, threads: int = 256):
+        w = np.ascontiguousarray(w_bf16, dtype=np.uint16).ravel()
+        self._w_keepalive = w
+        h = _L().orc_df11_encode(_p(w), w.size, max_len, n_bytes, threads)
+        if not h:
+            raise ValueError("DF11 encode failed")
+        self._h = h
+        info = np.zeros(8, dtype=np.int64)
+        _L().orc_df11_info(h, _p(info))
+        (self.n, self.n_bytes, self.threads, self.n_chunks, self.n_blocks, self.stream_bytes,
+         self.payload_bits, self.n_luts) = (int(v) for v in info)
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            _L().orc_df11_free(self._h)
+            self._h = None
+
+    @property
+    def lengths(self):
+        return _view(_L().orc_df11_lengths(self._h), np.uint8, 256)
+
+    @property
+    def codes(self):
+        return _view(_L().orc_df11_codes(self._h), np.uint32, 256)
+
+    @property
+    def counts(self):
+        return _view(_L().orc_df11_counts(self._h), np.uint64, 256)
+
+    @property
+    def stream(self):
+        return _view(_L().orc_df11_stream(self._h), np.uint8, self.stream_bytes)
+
+    @property
+    def gaps(self):
+        return _view(_L().orc_df11_gaps(self._h), np.uint16, self.n_chunks)
+
+    @property
+    def block_pos(self):
+        return _view(_L().orc_df11_block_pos(self._h), np.uint64, self.n_blocks + 1)
+
+    @property
+    def luts(self):
+        return _view(_L().orc_df11_luts(self._h), np.int16, self.n_luts * 256).reshape(self.n_luts, 256)
+
+    def flip_stream_bit(self, bit: int) -> None:
+        addr = _L().orc_df11_stream_mut(self._h)
+        b = ctypes.c_uint8.from_address(addr + bit // 8)
+        b.value ^= 0x80 >> (bit % 8)
+
+    def decode(self) -> np.ndarray:
+        out = np.zeros(self.n, dtype=np.uint16)
+        if _L().orc_df11_decode(self._h, _p(out) if self.n else 0) != 0:
+            raise ValueError("DF11 decode hit an invalid table entry")
+        return out
+
+
+# --------------------------------------------------------------------------- rANS codec
+def rans_freqs(counts, prob_bits: int = 12) -> np.ndarray:
+    c = np.zeros(16, dtype=np.uint64)
+    c[: len(counts)] = counts
+    out = np.zeros(16, dtype=np.uint32)
+    if _L().orc_rans_freqs(_p(c), prob_bits, _p(out)) < 0:
+        raise ValueError("cannot normalise")
+    return out
+
+
+class Rans:
+    """Independent-tile interleaved rANS encoding of 4-bit codes (-8..7)."""
+
+    def __init__(self, codes: np.ndarray, prob_bits: int = 12, tile: int = 4096):
+        c = np.ascontiguousarray(codes, dtype=np.int8).ravel()
+        self._c = c
+        h = _L().orc_rans_encode(_p(c) if c.size else 0, c.size, prob_bits, tile)
+        if not h:
+            raise ValueError("rANS encode failed")
+        self._h = h
+        self.prob_bits = prob_bits
+        info = np.zeros(4, dtype=np.int64)
+        _L().orc_rans_info(h, _p(info))
+        self.n, self.n_tiles, self.payload_words, self.tile = (int(v) for v in info)
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            _L().orc_rans_free(self._h)
+            self._h = None
+
+    @property
+    def freqs(self):
+        return _view(_L().orc_rans_freqs_of(self._h), np.uint32, 16)
+
+    @property
+    def counts(self):
+        return _view(_L().orc_rans_counts_of(self._h), np.uint64, 16)
+
+    @property
+    def states(self):
+        return _view(_L().orc_rans_states(self._h), np.uint32, 32 * self.n_tiles).reshape(self.n_tiles, 32)
+
+    @property
+    def offsets(self):
+        return _view(_L().orc_rans_offsets(self._h), np.uint32, self.n_tiles + 1)
+
+    def flip_payload_bit(self, word: int, bit: int) -> None:
+        addr = _L().orc_rans_payload_mut(self._h)
+        w = ctypes.c_uint16.from_address(addr + 2 * word)
+        w.value ^= 1 << bit
+
+    def decode(self, strict: bool = True):
+        out = np.zeros(self.n, dtype=np.int8)
+        fin = np.zeros(max(1, 32 * self.n_tiles), dtype=np.uint32)
+        rc = _L().orc_rans_decode(self._h, _p(out) if self.n else 0, _p(fin))
+        if rc == -1 or (strict and rc != 0):
+            raise ValueError(f"rANS decode failed ({rc})")
+        return out, fin[: 32 * self.n_tiles].reshape(self.n_tiles, 32), rc
+
+
+def rans_dequant_bf16(codes: np.ndarray, scales: np.ndarray, group: int = 128) -> np.ndarray:
+    c = np.ascontiguousarray(codes, dtype=np.int8)
+    s = np.ascontiguousarray(scales, dtype=np.uint16)
+    n, k = c.shape
+    out = np.zeros((n, k), dtype=np.uint16)
+    _L().orc_rans_dequant_bf16(_p(c), _p(s), n, k, group, _p(out))
+    return out
+
+
+# --------------------------------------------------------------------------- GEMV
+def _rows_arg(rows):
+    if rows is None:
+        return None, 0
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    return r, r.size
+
+
+def gemv_bf16(w: np.ndarray, x: np.ndarray, rows=None):
+    """FP64 y[b, i] and a[b, i] = sum |w x| for BF16 W [N, K] and x [batch, K]."""
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.uint16)
+    n, k = w.shape
+    batch = x.shape[0]
+    r, nsel = _rows_arg(rows)
+    nr = nsel if r is not None else n
+    y = np.zeros((batch, nr), dtype=np.float64)
+    a = np.zeros((batch, nr), dtype=np.float64)
+    _L().orc_gemv_bf16(_p(w), n, k, _p(x), batch, _p(r) if r is not None else None, nsel, _p(y), _p(a))
+    return y, a
+
+
+def gemv_rans(codes: np.ndarray, scales: np.ndarray, x: np.ndarray, group: int = 128, rows=None):
+    c = np.ascontiguousarray(codes, dtype=np.int8)
+    s = np.ascontiguousarray(scales, dtype=np.uint16)
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.uint16)
+    n, k = c.shape
+    batch = x.shape[0]
+    r, nsel = _rows_arg(rows)
+    nr = nsel if r is not None else n
+    y = np.zeros((batch, nr), dtype=np.float64)
+    a = np.zeros((batch, nr), dtype=np.float64)
+    _L().orc_gemv_rans(_p(c), _p(s), n, k, group, _p(x), batch, _p(r) if r is not None else None, nsel,
+                       _p(y), _p(a))
+    return y, a

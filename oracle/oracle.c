@@ -1,0 +1,789 @@
+/*
+ * oracle.c -- plain, slow CPU reference for the entropy-coded weight path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the library (lossless_entropy_coded_gb300)
+ * includes, links or calls this file; only tests/, the smoke check and the
+ * benchmark's CPU-baseline leg load it.  It shares no code, header, table or
+ * constant generator with the CUDA path.
+ *
+ * What it follows (sources are the pages' titles and sections):
+ *  - DFloat11, "70% Size, 100% Accuracy: Lossless LLM Compression for Efficient
+ *    GPU Inference via Dynamic-Length Float": Eq.(1) BF16 field split; Eq.(2)
+ *    Shannon entropy; the Huffman exponent coding with sign and mantissa kept as
+ *    a raw byte (section "Dynamic-Length Float", Fig. 3); the flat LUT plus
+ *    CodeLengths (appendix "two lookup tables", Fig. 13); hierarchical compact
+ *    LUTs of b bits each (appendix, Fig. 14); per-thread byte chunks with Gaps
+ *    and BlockOutputPos (section "two-phase kernel", Fig. 5); the two-phase
+ *    decompression of Algorithm 1.
+ *  - EntroPack (arXiv 2609.34185), section 3.6 and appendix C.3: independent
+ *    rANS tiles, 32 terminal states plus a 32-bit payload offset per tile,
+ *    32-bit states, 16-bit payload words, at most one word per symbol.
+ *  - rANS itself: Duda, "Asymmetric numeral systems" (2013), cited by MINE
+ *    section 3.
+ *
+ * Readings of points the pages leave open are marked "reading:" below.
+ * Floating point: every sum is an FP64 sum in index order.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ===========================================================================
+ * Storage-type helpers (IEEE definitions written out).
+ * ========================================================================= */
+
+/* BF16 bit pattern -> value: the top 16 bits of an FP32 (DFloat11 Eq. (1)). */
+double orc_bf16_to_f64(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/* FP16 bit pattern -> FP32 value, from the binary16 definition. */
+float orc_f16_to_f32(uint16_t h) {
+    const int s = (h >> 15) & 1, e = (h >> 10) & 0x1F, m = h & 0x3FF;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24); /* subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp(1024.0 + m, e - 25); /* (1 + m/1024) * 2^(e-15) */
+    return (float)(s ? -v : v);
+}
+
+/* FP32 -> BF16 with round-to-nearest, ties to even (NaN stays NaN). */
+uint16_t orc_f32_to_bf16_rne(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if (isnan(f)) return (uint16_t)((u >> 16) | 0x40);
+    const uint32_t lower = u & 0xFFFFu, upper = u >> 16;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) return (uint16_t)(upper + 1u);
+    return (uint16_t)upper;
+}
+
+/* ===========================================================================
+ * Entropy (DFloat11 Eq. (2); MINE section 3: H(P) lower-bounds the size).
+ * ========================================================================= */
+double orc_entropy(const uint64_t* counts, int n_symbols) {
+    double total = 0.0, h = 0.0;
+    for (int s = 0; s < n_symbols; ++s) total += (double)counts[s];
+    if (total <= 0.0) return 0.0;
+    for (int s = 0; s < n_symbols; ++s) {
+        if (!counts[s]) continue;
+        const double p = (double)counts[s] / total;
+        h -= p * log2(p);
+    }
+    return h;
+}
+
+/* Cross-entropy (bits/symbol) of empirical counts under model q_s = f_s / 2^prob_bits
+ * (MINE section 4.2 "Compressed Size Prediction"). Returns INFINITY if a present
+ * symbol has f_s = 0. */
+double orc_cross_entropy(const uint64_t* counts, const uint32_t* freqs, int n_symbols, int prob_bits) {
+    double total = 0.0, h = 0.0;
+    for (int s = 0; s < n_symbols; ++s) total += (double)counts[s];
+    if (total <= 0.0) return 0.0;
+    for (int s = 0; s < n_symbols; ++s) {
+        if (!counts[s]) continue;
+        if (!freqs[s]) return INFINITY;
+        h -= (double)counts[s] / total * (log2((double)freqs[s]) - prob_bits);
+    }
+    return h;
+}
+
+/* ===========================================================================
+ * Huffman code lengths.
+ * ========================================================================= */
+
+/* Textbook Huffman (DFloat11 section "entropy coding": repeatedly merge the two
+ * least frequent nodes).  reading: ties are broken by (weight, smallest symbol in
+ * the subtree).  One present symbol gets length 1.  Returns the number of
+ * present symbols; lengths of absent symbols are 0. */
+int orc_huffman_textbook(const uint64_t counts[256], uint8_t lengths[256]) {
+    uint64_t w[511];
+    int minsym[511], parent[511], alive[511];
+    int n = 0, leaf_of[256];
+    memset(lengths, 0, 256);
+    for (int s = 0; s < 256; ++s) {
+        leaf_of[s] = -1;
+        if (!counts[s]) continue;
+        w[n] = counts[s];
+        minsym[n] = s;
+        parent[n] = -1;
+        alive[n] = 1;
+        leaf_of[s] = n++;
+    }
+    if (n == 0) return 0;
+    if (n == 1) {
+        for (int s = 0; s < 256; ++s)
+            if (leaf_of[s] >= 0) lengths[s] = 1;
+        return 1;
+    }
+    int total = n;
+    for (int merges = 0; merges < n - 1; ++merges) {
+        int a = -1, b = -1;
+        for (int i = 0; i < total; ++i) {
+            if (!alive[i]) continue;
+            if (a < 0 || w[i] < w[a] || (w[i] == w[a] && minsym[i] < minsym[a])) {
+                b = a;
+                a = i;
+            } else if (b < 0 || w[i] < w[b] || (w[i] == w[b] && minsym[i] < minsym[b])) {
+                b = i;
+            }
+        }
+        w[total] = w[a] + w[b];
+        minsym[total] = minsym[a] < minsym[b] ? minsym[a] : minsym[b];
+        parent[total] = -1;
+        alive[total] = 1;
+        alive[a] = alive[b] = 0;
+        parent[a] = parent[b] = total;
+        ++total;
+    }
+    for (int s = 0; s < 256; ++s) {
+        if (leaf_of[s] < 0) continue;
+        int d = 0;
+        for (int v = leaf_of[s]; parent[v] >= 0; v = parent[v]) ++d;
+        lengths[s] = (uint8_t)d;
+    }
+    return n;
+}
+
+/* Package-merge (Larmore & Hirschberg 1990), the optimal length-limited prefix
+ * code, in its "coin collector" form.  Items are leaves (one per present symbol,
+ * sorted by (weight, symbol)) and packages (adjacent pairs of the previous list).
+ * reading: on equal weight a leaf precedes a package when merging.
+ * The list for denomination 2^-1 keeps its first 2(n-1) items; a symbol's length
+ * is the number of times its leaf occurs inside them.  Returns n, or -1 if
+ * 2^max_len < n. */
+typedef struct {
+    uint64_t w;
+    int leaf;      /* symbol, or -1 for a package */
+    int child[2];  /* indices into the previous level's list */
+} pm_item;
+
+static void pm_count(pm_item* const* lists, int level, int idx, int* cnt) {
+    const pm_item* it = &lists[level][idx];
+    if (it->leaf >= 0) {
+        cnt[it->leaf]++;
+        return;
+    }
+    pm_count(lists, level - 1, it->child[0], cnt);
+    pm_count(lists, level - 1, it->child[1], cnt);
+}
+
+int orc_package_merge(const uint64_t counts[256], int max_len, uint8_t lengths[256]) {
+    int syms[256], n = 0;
+    memset(lengths, 0, 256);
+    for (int s = 0; s < 256; ++s)
+        if (counts[s]) syms[n++] = s;
+    if (n == 0) return 0;
+    if (n == 1) {
+        lengths[syms[0]] = 1;
+        return 1;
+    }
+    if (max_len < 1 || max_len > 30 || (1LL << max_len) < n) return -1;
+    /* leaves sorted by (weight, symbol): insertion sort */
+    for (int i = 1; i < n; ++i) {
+        int s = syms[i], j = i - 1;
+        while (j >= 0 && (counts[syms[j]] > counts[s] || (counts[syms[j]] == counts[s] && syms[j] > s))) {
+            syms[j + 1] = syms[j];
+            --j;
+        }
+        syms[j + 1] = s;
+    }
+    /* lists[0] is denomination 2^-max_len (leaves only); lists[d] is 2^-(max_len-d). */
+    pm_item** lists = (pm_item**)calloc((size_t)max_len, sizeof(pm_item*));
+    int* sizes = (int*)calloc((size_t)max_len, sizeof(int));
+    for (int d = 0; d < max_len; ++d) lists[d] = (pm_item*)malloc(sizeof(pm_item) * (size_t)(2 * n));
+    for (int i = 0; i < n; ++i) {
+        lists[0][i].w = counts[syms[i]];
+        lists[0][i].leaf = syms[i];
+    }
+    sizes[0] = n;
+    for (int d = 1; d < max_len; ++d) {
+        const pm_item* prev = lists[d - 1];
+        const int np = sizes[d - 1] / 2; /* packages: pairs (0,1), (2,3), ... */
+        int li = 0, pi = 0, k = 0;
+        while (li < n || pi < np) {
+            const uint64_t pw = pi < np ? prev[2 * pi].w + prev[2 * pi + 1].w : 0;
+            if (li < n && (pi >= np || counts[syms[li]] <= pw)) {
+                lists[d][k].w = counts[syms[li]];
+                lists[d][k].leaf = syms[li];
+                ++li;
+            } else {
+                lists[d][k].w = pw;
+                lists[d][k].leaf = -1;
+                lists[d][k].child[0] = 2 * pi;
+                lists[d][k].child[1] = 2 * pi + 1;
+                ++pi;
+            }
+            ++k;
+        }
+        sizes[d] = k;
+    }
+    int cnt[256] = {0};
+    for (int i = 0; i < 2 * (n - 1); ++i) pm_count(lists, max_len - 1, i, cnt);
+    for (int s = 0; s < 256; ++s) lengths[s] = (uint8_t)cnt[s];
+    for (int d = 0; d < max_len; ++d) free(lists[d]);
+    free(lists);
+    free(sizes);
+    return n;
+}
+
+/* Lengths used by the codec: textbook Huffman if its longest code fits max_len,
+ * else package-merge (reading: DFloat11 leaves the limit open; 24 is the
+ * workload's stated maximum). */
+int orc_code_lengths(const uint64_t counts[256], int max_len, uint8_t lengths[256]) {
+    int n = orc_huffman_textbook(counts, lengths);
+    int longest = 0;
+    for (int s = 0; s < 256; ++s)
+        if (lengths[s] > longest) longest = lengths[s];
+    if (longest <= max_len) return n;
+    return orc_package_merge(counts, max_len, lengths);
+}
+
+/* Canonical codewords: symbols sorted by (length, symbol) get consecutive
+ * values, shifted left whenever the length grows.  This reproduces DFloat11
+ * Fig. 13 (A=0, B=100, C=101, D=110, E=1110, F=1111). */
+void orc_canonical_codes(const uint8_t lengths[256], uint32_t codes[256]) {
+    uint32_t code = 0;
+    int prev_len = 0, first = 1;
+    memset(codes, 0, 256 * sizeof(uint32_t));
+    for (int l = 1; l <= 32; ++l) {
+        for (int s = 0; s < 256; ++s) {
+            if (lengths[s] != l) continue;
+            if (first) {
+                code = 0;
+                first = 0;
+            } else {
+                code = (code + 1) << (l - prev_len);
+            }
+            prev_len = l;
+            codes[s] = code;
+        }
+    }
+}
+
+/* ===========================================================================
+ * Lookup tables.
+ * ========================================================================= */
+
+/* Flat LUT of 2^L entries (DFloat11 appendix, Fig. 13): entry i holds the symbol
+ * whose codeword is a prefix of the L-bit string i; -1 if none. */
+int orc_flat_lut(const uint8_t lengths[256], const uint32_t codes[256], int L, int16_t* lut) {
+    if (L < 1 || L > 24) return -1;
+    for (int64_t i = 0; i < (1 << L); ++i) lut[i] = -1;
+    for (int s = 0; s < 256; ++s) {
+        const int l = lengths[s];
+        if (!l) continue;
+        if (l > L) return -1;
+        const uint32_t lo = codes[s] << (L - l), hi = (codes[s] + 1) << (L - l);
+        for (uint32_t i = lo; i < hi; ++i) lut[i] = (int16_t)s;
+    }
+    return 0;
+}
+
+/* Hierarchical LUTs, b bits per table (DFloat11 appendix "decomposing the LUT",
+ * Fig. 4 and Fig. 14).  Table t has 2^b entries.  reading: an entry is a
+ * 16-bit value -- 0..255 is a decoded exponent, 256+j points at table j, -1 is
+ * unused -- so all 256 exponent values stay legal (the pages reserve 240..255 as
+ * pointers, which cannot represent exponents 240..255).  Tables are numbered in
+ * breadth-first order of their prefixes, children in index order.
+ * Returns the number of tables, or -1 if more than max_tables are needed. */
+int orc_hier_luts(const uint8_t lengths[256], const uint32_t codes[256], int b, int16_t* luts,
+                  int max_tables) {
+    if (b < 1 || b > 12) return -1;
+    uint32_t prefix[4096];
+    int depth[4096];
+    int n_tables = 1, head = 0;
+    prefix[0] = 0;
+    depth[0] = 0;
+    const int size = 1 << b;
+    while (head < n_tables) {
+        const int t = head++;
+        const int d = depth[t];
+        for (int v = 0; v < size; ++v) {
+            /* bit string P.v of length d + b, compared with every codeword */
+            const uint64_t pv = ((uint64_t)prefix[t] << b) | (uint64_t)v;
+            const int dl = d + b;
+            int16_t entry = -1;
+            int needs_child = 0;
+            for (int s = 0; s < 256; ++s) {
+                const int l = lengths[s];
+                if (!l) continue;
+                if (l <= dl) {
+                    if ((pv >> (dl - l)) == codes[s] && l > d) {
+                        entry = (int16_t)s;
+                        break;
+                    }
+                } else if (((uint64_t)codes[s] >> (l - dl)) == pv) {
+                    needs_child = 1;
+                }
+            }
+            if (entry < 0 && needs_child) {
+                if (n_tables >= max_tables || n_tables >= 4096) return -1;
+                prefix[n_tables] = (uint32_t)pv;
+                depth[n_tables] = dl;
+                entry = (int16_t)(256 + n_tables);
+                ++n_tables;
+            }
+            luts[(size_t)t * size + v] = entry;
+        }
+    }
+    return n_tables;
+}
+
+/* ===========================================================================
+ * DFloat11 format: EncodedExponent, PackedSignMantissa, Gaps, BlockOutputPos.
+ * ========================================================================= */
+typedef struct {
+    int64_t n;              /* number of weights */
+    int n_bytes;            /* bytes per thread chunk (the pages' n) */
+    int threads;            /* threads per block (the pages' T) */
+    int64_t n_chunks, n_blocks;
+    int64_t stream_bytes;   /* EncodedExponent length incl. padding */
+    uint8_t* stream;        /* EncodedExponent, MSB-first */
+    uint8_t* sm;            /* PackedSignMantissa: (sign << 7) | mantissa */
+    uint16_t* gaps;         /* one per chunk, bit offset of its first codeword */
+    uint64_t* block_pos64;  /* BlockOutputPos, n_blocks + 1 entries */
+    uint8_t lengths[256];
+    uint32_t codes[256];
+    uint64_t counts[256];
+    int16_t* luts;          /* hierarchical, b = 8 */
+    int n_luts;
+    int64_t payload_bits;   /* sum of codeword lengths */
+} orc_df11;
+
+void orc_df11_free(orc_df11* d) {
+    if (!d) return;
+    free(d->stream);
+    free(d->sm);
+    free(d->gaps);
+    free(d->block_pos64);
+    free(d->luts);
+    free(d);
+}
+
+/* Encoder (DFloat11 section "Dynamic-Length Float" and Fig. 3/5).
+ * Step 1: split w into the exponent byte e = (w >> 7) & 0xFF and the raw byte
+ *         sm = ((w >> 8) & 0x80) | (w & 0x7F); count e over the whole matrix.
+ * Step 2: code lengths (max_len), canonical codewords.
+ * Step 3: concatenate codewords MSB-first into EncodedExponent.
+ * Step 4: cut the stream into chunks of n_bytes; gap = offset of the first
+ *         codeword starting in the chunk; BlockOutputPos[b] = index of the first
+ *         element whose codeword starts in block b, BlockOutputPos[B] = n.
+ * reading: the stream is padded with zero bytes to whole blocks plus 4 bytes, so
+ * a 4-byte read at any chunk offset stays inside it. */
+orc_df11* orc_df11_encode(const uint16_t* w, int64_t n, int max_len, int n_bytes, int threads) {
+    if (n < 0 || n_bytes < 1 || threads < 1 || max_len < 1 || max_len > 24) return NULL;
+    orc_df11* d = (orc_df11*)calloc(1, sizeof(orc_df11));
+    d->n = n;
+    d->n_bytes = n_bytes;
+    d->threads = threads;
+    for (int64_t p = 0; p < n; ++p) d->counts[(w[p] >> 7) & 0xFF]++;
+    if (orc_code_lengths(d->counts, max_len, d->lengths) < 0) {
+        orc_df11_free(d);
+        return NULL;
+    }
+    orc_canonical_codes(d->lengths, d->codes);
+    d->luts = (int16_t*)malloc(sizeof(int16_t) * 256 * 4096);
+    d->n_luts = orc_hier_luts(d->lengths, d->codes, 8, d->luts, 4096);
+
+    int64_t bits = 0;
+    for (int64_t p = 0; p < n; ++p) bits += d->lengths[(w[p] >> 7) & 0xFF];
+    d->payload_bits = bits;
+    const int64_t block_bytes = (int64_t)n_bytes * threads;
+    int64_t nbytes = (bits + 7) / 8;
+    d->n_blocks = (nbytes + block_bytes - 1) / block_bytes;
+    if (d->n_blocks == 0) d->n_blocks = 1;
+    d->n_chunks = d->n_blocks * threads;
+    d->stream_bytes = d->n_blocks * block_bytes + 4;
+    d->stream = (uint8_t*)calloc((size_t)d->stream_bytes, 1);
+    d->sm = (uint8_t*)malloc((size_t)(n > 0 ? n : 1));
+    d->gaps = (uint16_t*)calloc((size_t)d->n_chunks, sizeof(uint16_t));
+    d->block_pos64 = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)(d->n_blocks + 1));
+    for (int64_t b = 0; b <= d->n_blocks; ++b) d->block_pos64[b] = (uint64_t)n;
+
+    /* Codewords MSB-first.  Elements are visited in increasing start bit, so the
+     * first element starting at or after chunk c's first bit is the current one
+     * for every chunk c not yet assigned whose first bit is <= its start. */
+    const int64_t chunk_bits = 8 * (int64_t)n_bytes;
+    int64_t bitpos = 0, next_chunk = 0;
+    for (int64_t p = 0; p < n; ++p) {
+        const int e = (w[p] >> 7) & 0xFF;
+        d->sm[p] = (uint8_t)(((w[p] >> 8) & 0x80) | (w[p] & 0x7F));
+        while (next_chunk < d->n_chunks && next_chunk * chunk_bits <= bitpos) {
+            const int64_t off = bitpos - next_chunk * chunk_bits;
+            /* reading: a chunk in which no codeword starts gets gap = 8n (decodes nothing) */
+            d->gaps[next_chunk] = (uint16_t)(off < chunk_bits ? off : chunk_bits);
+            if (next_chunk % threads == 0) d->block_pos64[next_chunk / threads] = (uint64_t)p;
+            ++next_chunk;
+        }
+        const int l = d->lengths[e];
+        const uint32_t c = d->codes[e];
+        for (int k = l - 1; k >= 0; --k) {
+            if ((c >> k) & 1u) d->stream[bitpos >> 3] |= (uint8_t)(0x80u >> (bitpos & 7));
+            ++bitpos;
+        }
+    }
+    /* Chunks after the last codeword start hold only padding: gap 0, and their
+     * blocks start at n (already set); whatever they decode is dropped. */
+    for (; next_chunk < d->n_chunks; ++next_chunk) d->gaps[next_chunk] = 0;
+    return d;
+}
+
+/* Read the 32-bit MSB-first window starting at absolute bit `bit`. */
+static uint32_t window32(const uint8_t* s, int64_t bit) {
+    const int64_t byte = bit >> 3;
+    const int sh = (int)(bit & 7);
+    uint64_t v = 0;
+    for (int i = 0; i < 5; ++i) v = (v << 8) | s[byte + i];
+    return (uint32_t)(v >> (8 - sh));
+}
+
+/* Decoder: Algorithm 1 of DFloat11 ("DF11ToBF16"), both phases.
+ * For block b and thread t: BitOffset starts at Gaps[bT+t]; while BitOffset < 8n,
+ * read the 4 bytes of the window at BitOffset, look up LUT_1[Byte_1] and follow
+ * pointers through Byte_2.. while the entry is a pointer, then advance by
+ * CodeLengths[Exponent].  Phase 1 counts, an exclusive prefix sum over the
+ * block's threads gives ThreadOutputPos, phase 2 decodes again and writes
+ * (Sign << 8) | (Exponent << 7) | Mantissa into the block's write buffer, which is
+ * copied to Outputs[BlockOutputPos[b] .. BlockOutputPos[b+1]).
+ * reading: elements whose index reaches BlockOutputPos[b+1] are dropped (they
+ * are padding bits of the last block).  Returns 0, or -1 on a bad table walk. */
+int orc_df11_decode(const orc_df11* d, uint16_t* out) {
+    if (d->n == 0) return 0; /* no elements, no code */
+    const int T = d->threads, n = d->n_bytes;
+    int64_t* num = (int64_t*)malloc(sizeof(int64_t) * (size_t)T);
+    int64_t* pos = (int64_t*)malloc(sizeof(int64_t) * (size_t)T);
+    uint16_t* wbuf = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(8 * n * T + 1));
+    int rc = 0;
+    for (int64_t b = 0; b < d->n_blocks && rc == 0; ++b) {
+        const int64_t b_lo = (int64_t)d->block_pos64[b], b_hi = (int64_t)d->block_pos64[b + 1];
+        for (int phase = 1; phase <= 2 && rc == 0; ++phase) {
+            for (int t = 0; t < T && rc == 0; ++t) {
+                const int64_t chunk = b * T + t;
+                const int64_t base = chunk * 8 * (int64_t)n;
+                int64_t off = d->gaps[chunk];
+                if (phase == 1) num[t] = 0;
+                while (off < 8 * (int64_t)n) {
+                    const uint32_t win = window32(d->stream, base + off);
+                    int i = 0;
+                    int v = d->luts[(win >> 24) & 0xFF];
+                    while (v >= 256) {
+                        ++i;
+                        if (i > 3) {
+                            rc = -1;
+                            break;
+                        }
+                        v = d->luts[(size_t)(v - 256) * 256 + ((win >> (24 - 8 * i)) & 0xFF)];
+                    }
+                    if (rc || v < 0) {
+                        rc = -1;
+                        break;
+                    }
+                    if (phase == 1) {
+                        num[t]++;
+                    } else {
+                        if (pos[t] < b_hi) {
+                            const uint8_t smb = d->sm[pos[t]];
+                            wbuf[pos[t] - b_lo] =
+                                (uint16_t)(((smb & 0x80u) << 8) | ((uint32_t)v << 7) | (smb & 0x7Fu));
+                        }
+                        pos[t]++;
+                    }
+                    off += d->lengths[v];
+                }
+            }
+            if (phase == 1) { /* exclusive prefix sum over the block's threads */
+                int64_t acc = b_lo;
+                for (int t = 0; t < T; ++t) {
+                    pos[t] = acc;
+                    acc += num[t];
+                }
+            }
+        }
+        for (int64_t p = b_lo; p < b_hi && rc == 0; ++p) out[p] = wbuf[p - b_lo];
+    }
+    free(num);
+    free(pos);
+    free(wbuf);
+    return rc;
+}
+
+/* Accessors for tests. */
+int64_t orc_df11_info(const orc_df11* d, int64_t* out /* 8 */) {
+    out[0] = d->n;
+    out[1] = d->n_bytes;
+    out[2] = d->threads;
+    out[3] = d->n_chunks;
+    out[4] = d->n_blocks;
+    out[5] = d->stream_bytes;
+    out[6] = d->payload_bits;
+    out[7] = d->n_luts;
+    return 0;
+}
+const uint8_t* orc_df11_lengths(const orc_df11* d) { return d->lengths; }
+const uint32_t* orc_df11_codes(const orc_df11* d) { return d->codes; }
+const uint64_t* orc_df11_counts(const orc_df11* d) { return d->counts; }
+const uint8_t* orc_df11_stream(const orc_df11* d) { return d->stream; }
+const uint16_t* orc_df11_gaps(const orc_df11* d) { return d->gaps; }
+const uint64_t* orc_df11_block_pos(const orc_df11* d) { return d->block_pos64; }
+const int16_t* orc_df11_luts(const orc_df11* d) { return d->luts; }
+uint8_t* orc_df11_sm_mut(orc_df11* d) { return d->sm; }
+uint8_t* orc_df11_stream_mut(orc_df11* d) { return d->stream; }
+
+/* ===========================================================================
+ * rANS tile codec (EntroPack section 3.6, appendix C.3; rANS after Duda 2013).
+ *
+ * Alphabet: 4-bit codes -8..7 as symbols 0..15.  One frequency table per matrix
+ * with sum 2^prob_bits.  The matrix is flattened row-major and cut into tiles of
+ * `tile` symbols (the last may be short).  Inside a tile, position q = 32*j + l
+ * belongs to lane l, step j.  State x lives in [2^16, 2^32); payload words are
+ * 16 bits; the encoder starts every lane at x = 2^16.
+ * ========================================================================= */
+
+/* reading: f_s = max(1, floor(M*c_s/n)) for present s; while the sum is short,
+ * add 1 to the present symbol with the largest remainder M*c_s - f_s*n (ties to
+ * the lower symbol); while it is over, take 1 from the present symbol with f_s > 1
+ * and the smallest remainder (ties to the lower symbol).  Absent symbols get 0. */
+int orc_rans_freqs(const uint64_t counts[16], int prob_bits, uint32_t freqs[16]) {
+    const int64_t M = (int64_t)1 << prob_bits;
+    uint64_t n = 0;
+    int present = 0;
+    for (int s = 0; s < 16; ++s) {
+        n += counts[s];
+        present += counts[s] != 0;
+    }
+    memset(freqs, 0, 16 * sizeof(uint32_t));
+    if (n == 0) return 0;
+    if (present > M) return -1;
+    __int128 rem[16];
+    int64_t sum = 0;
+    for (int s = 0; s < 16; ++s) {
+        if (!counts[s]) continue;
+        int64_t f = (int64_t)(((unsigned __int128)M * counts[s]) / n);
+        if (f < 1) f = 1;
+        freqs[s] = (uint32_t)f;
+        rem[s] = (__int128)M * (__int128)counts[s] - (__int128)f * (__int128)n;
+        sum += f;
+    }
+    while (sum < M) {
+        int best = -1;
+        for (int s = 0; s < 16; ++s)
+            if (counts[s] && (best < 0 || rem[s] > rem[best])) best = s;
+        freqs[best]++;
+        rem[best] -= (__int128)n;
+        ++sum;
+    }
+    while (sum > M) {
+        int best = -1;
+        for (int s = 0; s < 16; ++s)
+            if (counts[s] && freqs[s] > 1 && (best < 0 || rem[s] < rem[best])) best = s;
+        if (best < 0) return -1;
+        freqs[best]--;
+        rem[best] += (__int128)n;
+        --sum;
+    }
+    return present;
+}
+
+typedef struct {
+    int64_t n;            /* symbols */
+    int prob_bits, tile;
+    int64_t n_tiles;
+    uint32_t freqs[16], cum[16];
+    uint64_t counts[16];
+    uint32_t* states;     /* n_tiles * 32: the decoder's initial (encoder's final) states */
+    uint32_t* offsets;    /* n_tiles + 1: start of each tile's payload, in 16-bit words */
+    uint16_t* payload;
+    int64_t payload_words;
+} orc_rans;
+
+void orc_rans_free(orc_rans* r) {
+    if (!r) return;
+    free(r->states);
+    free(r->offsets);
+    free(r->payload);
+    free(r);
+}
+
+static int64_t lane_steps(int64_t n_t, int l) { return n_t > l ? (n_t - l + 31) / 32 : 0; }
+
+/* Encoder: each lane is encoded in reverse (last step first); within a step the
+ * lanes go 31 -> 0.  Before encoding s into x: while x >= f_s * 2^(32-prob_bits),
+ * emit the low 16 bits and shift x right by 16 (with 2^16 <= x < 2^32 this is the
+ * renormalisation bound ((2^16 >> b) << 16) * f_s).  Then
+ * x = floor(x / f_s) * 2^b + (x mod f_s) + c_s.  Emitted words go on a stack; the
+ * tile's payload is the stack read from the top, which is the order in which the
+ * decoder asks for them. */
+orc_rans* orc_rans_encode(const int8_t* codes, int64_t n, int prob_bits, int tile) {
+    if (n < 0 || prob_bits < 5 || prob_bits > 15 || tile < 32 || tile % 32) return NULL;
+    orc_rans* r = (orc_rans*)calloc(1, sizeof(orc_rans));
+    r->n = n;
+    r->prob_bits = prob_bits;
+    r->tile = tile;
+    for (int64_t i = 0; i < n; ++i) {
+        if (codes[i] < -8 || codes[i] > 7) {
+            orc_rans_free(r);
+            return NULL;
+        }
+        r->counts[codes[i] + 8]++;
+    }
+    if (orc_rans_freqs(r->counts, prob_bits, r->freqs) < 0) {
+        orc_rans_free(r);
+        return NULL;
+    }
+    for (int s = 0, c = 0; s < 16; ++s) {
+        r->cum[s] = (uint32_t)c;
+        c += (int)r->freqs[s];
+    }
+    r->n_tiles = (n + tile - 1) / tile;
+    r->states = (uint32_t*)malloc(sizeof(uint32_t) * 32 * (size_t)(r->n_tiles > 0 ? r->n_tiles : 1));
+    r->offsets = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)(r->n_tiles + 1));
+    r->payload = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(n > 0 ? n : 1)); /* <= 1 word per symbol */
+    uint16_t* stack = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(tile));
+    const uint64_t renorm_unit = (uint64_t)1 << (32 - prob_bits);
+    int64_t words = 0;
+    for (int64_t t = 0; t < r->n_tiles; ++t) {
+        const int64_t base = t * tile;
+        const int64_t n_t = (n - base < tile) ? n - base : tile;
+        uint64_t x[32];
+        for (int l = 0; l < 32; ++l) x[l] = 1u << 16;
+        int64_t sp = 0;
+        const int64_t steps = (n_t + 31) / 32;
+        for (int64_t j = steps - 1; j >= 0; --j) {
+            for (int l = 31; l >= 0; --l) {
+                if (j >= lane_steps(n_t, l)) continue;
+                const int s = codes[base + 32 * j + l] + 8;
+                const uint64_t f = r->freqs[s];
+                while (x[l] >= f * renorm_unit) {
+                    stack[sp++] = (uint16_t)(x[l] & 0xFFFF);
+                    x[l] >>= 16;
+                }
+                x[l] = (x[l] / f << prob_bits) + (x[l] % f) + r->cum[s];
+            }
+        }
+        for (int l = 0; l < 32; ++l) r->states[t * 32 + l] = (uint32_t)x[l];
+        r->offsets[t] = (uint32_t)words;
+        while (sp > 0) r->payload[words++] = stack[--sp];
+    }
+    r->offsets[r->n_tiles] = (uint32_t)words;
+    r->payload_words = words;
+    free(stack);
+    return r;
+}
+
+/* Decoder: for step j = 0.., lanes ascending: slot = x mod 2^b, s = the symbol with
+ * c_s <= slot < c_s + f_s, x = f_s * (x >> b) + slot - c_s; if x < 2^16 then
+ * x = (x << 16) | next payload word.  Writes codes; also reports the lanes' final
+ * states (each must be 2^16) and the words consumed (must be the tile's count).
+ * Returns 0, -1 on a corrupt stream, -2 if a final state or word count is off. */
+int orc_rans_decode(const orc_rans* r, int8_t* out, uint32_t* final_states /* n_tiles*32 or NULL */) {
+    const uint32_t M = 1u << r->prob_bits;
+    int rc = 0;
+    for (int64_t t = 0; t < r->n_tiles; ++t) {
+        const int64_t base = t * r->tile;
+        const int64_t n_t = (r->n - base < r->tile) ? r->n - base : r->tile;
+        uint64_t x[32];
+        for (int l = 0; l < 32; ++l) x[l] = r->states[t * 32 + l];
+        int64_t wp = r->offsets[t];
+        const int64_t wend = r->offsets[t + 1];
+        const int64_t steps = (n_t + 31) / 32;
+        for (int64_t j = 0; j < steps; ++j) {
+            for (int l = 0; l < 32; ++l) {
+                if (j >= lane_steps(n_t, l)) continue;
+                const uint32_t slot = (uint32_t)(x[l] & (M - 1));
+                int s = -1;
+                for (int k = 0; k < 16; ++k)
+                    if (r->freqs[k] && slot >= r->cum[k] && slot < r->cum[k] + r->freqs[k]) s = k;
+                if (s < 0) return -1;
+                x[l] = (uint64_t)r->freqs[s] * (x[l] >> r->prob_bits) + slot - r->cum[s];
+                if (x[l] < (1u << 16)) {
+                    if (wp >= wend) return -1;
+                    x[l] = (x[l] << 16) | r->payload[wp++];
+                }
+                out[base + 32 * j + l] = (int8_t)(s - 8);
+            }
+        }
+        for (int l = 0; l < 32; ++l) {
+            if (final_states) final_states[t * 32 + l] = (uint32_t)x[l];
+            if (x[l] != (1u << 16)) rc = -2;
+        }
+        if (wp != wend) rc = -2;
+    }
+    return rc;
+}
+
+int64_t orc_rans_info(const orc_rans* r, int64_t* out /* 4 */) {
+    out[0] = r->n;
+    out[1] = r->n_tiles;
+    out[2] = r->payload_words;
+    out[3] = r->tile;
+    return 0;
+}
+const uint32_t* orc_rans_freqs_of(const orc_rans* r) { return r->freqs; }
+const uint64_t* orc_rans_counts_of(const orc_rans* r) { return r->counts; }
+const uint32_t* orc_rans_states(const orc_rans* r) { return r->states; }
+const uint32_t* orc_rans_offsets(const orc_rans* r) { return r->offsets; }
+uint16_t* orc_rans_payload_mut(orc_rans* r) { return r->payload; }
+
+/* Dequantised weight w = code * scale in FP32 (exact: a 4-bit integer times an
+ * 11-bit significand), scale from group floor(j / group) of row i. */
+static float rans_weight(int8_t code, const uint16_t* scales, int64_t i, int64_t j, int64_t k_cols, int group) {
+    const int64_t groups = (k_cols + group - 1) / group;
+    return (float)code * orc_f16_to_f32(scales[i * groups + j / group]);
+}
+
+/* BF16 (RNE) of the dequantised weights, the dense output of a decode. */
+void orc_rans_dequant_bf16(const int8_t* codes, const uint16_t* scales, int64_t n_rows, int64_t k_cols,
+                           int group, uint16_t* out) {
+    for (int64_t i = 0; i < n_rows; ++i)
+        for (int64_t j = 0; j < k_cols; ++j)
+            out[i * k_cols + j] = orc_f32_to_bf16_rne(rans_weight(codes[i * k_cols + j], scales, i, j, k_cols, group));
+}
+
+/* ===========================================================================
+ * GEMV in FP64: y[b,i] = sum_j w_ij * x_bj, summed in order j = 0..K-1, and
+ * a[b,i] = sum_j |w_ij * x_bj| (the per-element error scale).
+ * `rows` selects output rows (NULL = all); y and a are [batch, n_sel].
+ * ========================================================================= */
+void orc_gemv_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols, const uint16_t* x, int batch,
+                   const int64_t* rows, int64_t n_sel, double* y, double* a) {
+    const int64_t nr = rows ? n_sel : n_rows;
+    for (int b = 0; b < batch; ++b) {
+        for (int64_t r = 0; r < nr; ++r) {
+            const int64_t i = rows ? rows[r] : r;
+            double acc = 0.0, mag = 0.0;
+            for (int64_t j = 0; j < k_cols; ++j) {
+                const double p = orc_bf16_to_f64(w[i * k_cols + j]) * orc_bf16_to_f64(x[(int64_t)b * k_cols + j]);
+                acc += p;
+                mag += fabs(p);
+            }
+            y[(int64_t)b * nr + r] = acc;
+            a[(int64_t)b * nr + r] = mag;
+        }
+    }
+}
+
+void orc_gemv_rans(const int8_t* codes, const uint16_t* scales, int64_t n_rows, int64_t k_cols, int group,
+                   const uint16_t* x, int batch, const int64_t* rows, int64_t n_sel, double* y, double* a) {
+    const int64_t nr = rows ? n_sel : n_rows;
+    for (int b = 0; b < batch; ++b) {
+        for (int64_t r = 0; r < nr; ++r) {
+            const int64_t i = rows ? rows[r] : r;
+            double acc = 0.0, mag = 0.0;
+            for (int64_t j = 0; j < k_cols; ++j) {
+                const double wv = (double)rans_weight(codes[i * k_cols + j], scales, i, j, k_cols, group);
+                const double p = wv * orc_bf16_to_f64(x[(int64_t)b * k_cols + j]);
+                acc += p;
+                mag += fabs(p);
+            }
+            y[(int64_t)b * nr + r] = acc;
+            a[(int64_t)b * nr + r] = mag;
+        }
+    }
+}

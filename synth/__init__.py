@@ -1,0 +1,183 @@
+"""Seeded synthetic inputs shared by the oracle tests, the GPU tests and the benchmark.
+
+Only random-number drawing and storage-type rounding live here (FP32 -> BF16
+round-to-nearest-even, integer codes, FP64 -> FP16 scales).  None of the
+entropy-coding or GEMV arithmetic does: both sides get these arrays as inputs.
+
+Workload recipes (shapes and distributions of the Llama-3.1-8B / 70B linear
+layers and the 4-bit rANS case) are in ``WORKLOADS`` and the ``make_*``
+functions below.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "synth.c")
+_LIB = os.path.join(_HERE, "libsynth.so")
+_lib = None
+
+NTHREADS = max(1, min(64, os.cpu_count() or 1))
+
+
+def build(force: bool = False) -> str:
+    """Compile libsynth.so next to its source (plain gcc, no CUDA)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                               "-Wall", "-o", tmp, _SRC, "-lm", "-lpthread"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _L():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        u64, i64, i32, f64, vp = ctypes.c_uint64, ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
+        lib.synth_sm64.argtypes = [u64, u64]
+        lib.synth_sm64.restype = u64
+        lib.synth_subseed.argtypes = [u64, u64]
+        lib.synth_subseed.restype = u64
+        lib.synth_normal_f64.argtypes = [u64, u64, i64, vp, i32]
+        lib.synth_uniform_f64.argtypes = [u64, u64, i64, vp, i32]
+        lib.synth_gauss_bf16.argtypes = [u64, i64, f64, vp, i32]
+        lib.synth_llama_bf16.argtypes = [u64, i64, i64, f64, f64, f64, f64, vp, vp, i32]
+        lib.synth_llama_bf16.restype = i64
+        lib.synth_codes_i8.argtypes = [u64, i64, f64, i32, i32, vp, i32]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def sm64(seed: int, n: int) -> int:
+    """Output number n of the SplitMix64 stream seeded with `seed`."""
+    return int(_L().synth_sm64(seed & (2**64 - 1), n))
+
+
+def normal_f64(seed: int, n: int, offset: int = 0) -> np.ndarray:
+    out = np.empty(n, dtype=np.float64)
+    _L().synth_normal_f64(seed, offset, n, _ptr(out), NTHREADS)
+    return out
+
+
+def uniform_f64(seed: int, n: int, offset: int = 0) -> np.ndarray:
+    out = np.empty(n, dtype=np.float64)
+    _L().synth_uniform_f64(seed, offset, n, _ptr(out), NTHREADS)
+    return out
+
+
+def gauss_bf16(seed: int, shape, std: float) -> np.ndarray:
+    """bf16(float(std * z)) as uint16 bit patterns."""
+    n = int(np.prod(shape)) if len(shape) else 1
+    out = np.empty(n, dtype=np.uint16)
+    _L().synth_gauss_bf16(seed, n, float(std), _ptr(out), NTHREADS)
+    return out.reshape(shape)
+
+
+def llama_bf16(seed: int, n_rows: int, k_cols: int, base_std: float = 0.02, ln_sigma: float = 0.5,
+               outlier_frac: float = 0.001, outlier_std: float = 0.5, return_positions: bool = False):
+    """Row-scaled Gaussian weights with a fixed count of outliers, as BF16 bit patterns.
+
+    s_i = base_std * exp(ln_sigma * z_i) (a LogNormal(0, ln_sigma) factor), w_ij ~ N(0, s_i^2),
+    then round(outlier_frac * N * K) distinct positions get N(0, outlier_std^2).
+    """
+    out = np.empty((n_rows, k_cols), dtype=np.uint16)
+    m = int(round(outlier_frac * n_rows * k_cols))
+    pos = np.empty(max(m, 1), dtype=np.int64)
+    got = _L().synth_llama_bf16(seed, n_rows, k_cols, base_std, ln_sigma, outlier_frac, outlier_std,
+                                _ptr(out), _ptr(pos), NTHREADS)
+    if got < 0:
+        raise MemoryError("synth_llama_bf16 failed")
+    return (out, pos[:got]) if return_positions else out
+
+
+def codes_i8(seed: int, shape, std: float = 1.1, lo: int = -8, hi: int = 7) -> np.ndarray:
+    """clip(round_half_even(std * z), lo, hi) as int8."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.int8)
+    _L().synth_codes_i8(seed, n, float(std), lo, hi, _ptr(out), NTHREADS)
+    return out.reshape(shape)
+
+
+def scales_f16(seed: int, shape, lo: float = 0.005, hi: float = 0.03) -> np.ndarray:
+    """FP16 (round-to-nearest-even from FP64) draws of U(lo, hi), as uint16 bit patterns."""
+    n = int(np.prod(shape))
+    u = uniform_f64(seed, n)
+    return (lo + (hi - lo) * u).astype(np.float16).view(np.uint16).reshape(shape)
+
+
+def bf16_to_f32(a: np.ndarray) -> np.ndarray:
+    return (a.astype(np.uint32) << 16).view(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# Workloads: Llama-3.1-8B decoder-layer linears (q, k, v, o, gate, up, down),
+# Llama-3.3-70B-shaped block, 1024x1024 single matrix, 4-bit rANS shapes.
+# ---------------------------------------------------------------------------
+LAYER_8B = [("q", 4096, 4096), ("k", 1024, 4096), ("v", 1024, 4096), ("o", 4096, 4096),
+            ("gate", 14336, 4096), ("up", 14336, 4096), ("down", 4096, 14336)]
+BLOCK_70B = [("q", 8192, 8192), ("k", 1024, 8192), ("v", 1024, 8192), ("o", 8192, 8192),
+             ("gate", 28672, 8192), ("up", 28672, 8192), ("down", 8192, 28672)]
+RANS_SHAPES = [(14336, 4096), (4096, 14336)]
+N_LAYERS_8B = 32
+
+
+@dataclass(frozen=True)
+class MatrixSpec:
+    name: str
+    n_rows: int
+    k_cols: int
+    seed: int
+    kind: str  # "gauss" | "llama"
+
+
+def single_1024() -> MatrixSpec:
+    return MatrixSpec("w1024", 1024, 1024, 1001, "gauss")
+
+
+def layer_8b(layer: int | None = None) -> list[MatrixSpec]:
+    """One 8B layer set; layer=None is the stand-alone set (seeds 2000+i), else layer l of the stack."""
+    out = []
+    for i, (nm, n, k) in enumerate(LAYER_8B):
+        seed = 2000 + i if layer is None else 3000 + 16 * layer + i
+        out.append(MatrixSpec(nm if layer is None else f"L{layer}.{nm}", n, k, seed, "llama"))
+    return out
+
+
+def block_70b() -> list[MatrixSpec]:
+    return [MatrixSpec(nm, n, k, 5000 + i, "llama") for i, (nm, n, k) in enumerate(BLOCK_70B)]
+
+
+def make_weights(spec: MatrixSpec) -> np.ndarray:
+    if spec.kind == "gauss":
+        return gauss_bf16(spec.seed, (spec.n_rows, spec.k_cols), 0.02)
+    return llama_bf16(spec.seed, spec.n_rows, spec.k_cols)
+
+
+def make_x(seed: int, batch: int, k_cols: int) -> np.ndarray:
+    """Activations x ~ N(0, 1) as BF16 bit patterns, stream seed + 7."""
+    return gauss_bf16(seed + 7, (batch, k_cols), 1.0)
+
+
+def make_rans_case(shape_index: int, n_rows: int | None = None, k_cols: int | None = None, group: int = 128):
+    """4-bit codes ~ clip(rne(N(0, 1.1^2)), -8, 7) and FP16 scales ~ U(0.005, 0.03) per `group` weights."""
+    n, k = RANS_SHAPES[shape_index] if n_rows is None else (n_rows, k_cols)
+    seed = 4000 + shape_index
+    codes = codes_i8(seed, (n, k))
+    scales = scales_f16(synth_subseed(seed, 9), (n, (k + group - 1) // group))
+    return codes, scales
+
+
+def synth_subseed(seed: int, tag: int) -> int:
+    return int(_L().synth_subseed(seed, tag))
