@@ -1,0 +1,178 @@
+/*
+ * ec.h -- C ABI of the entropy-coded weight library (GB300, sm_103a).
+ *
+ * The library stores LLM weight matrices losslessly entropy-coded in GPU memory
+ * and decodes them on the fly: either to dense BF16 (ec_decode) or fused into a
+ * matrix-vector product y = W x (ec_gemv), so the dense weights never travel
+ * through HBM.
+ *
+ * Two codecs:
+ *  - Huffman over the BF16 exponent byte, sign and mantissa kept as one raw
+ *    byte per weight.  Source: DFloat11, "70% Size, 100% Accuracy: Lossless LLM
+ *    Compression for Efficient GPU Inference via Dynamic-Length Float", section
+ *    "Dynamic-Length Float" (Fig. 3), decoding through hierarchical lookup
+ *    tables (appendix, Fig. 13/14) with per-thread start offsets (section
+ *    "two-phase kernel", Fig. 5, Algorithm 1).
+ *  - Interleaved rANS in independent tiles for 4-bit codes with FP16 group
+ *    scales.  Source: EntroPack (arXiv 2609.34185), section 3.6 and appendix
+ *    C.3 (32 terminal states and a payload offset per tile, 32-bit states,
+ *    16-bit payload words).
+ * The fused decode + multiply-accumulate follows MINE ("Entropy-coded
+ * Memory-efficient Inference for LLMs"), section 4 "Fused mvm" (Fig. 2).
+ *
+ * Conventions (all entry points):
+ *  - Return EC_OK (0) or a negative EC_ERR_* code; no exception crosses the ABI.
+ *  - Shapes are checked with overflow-safe 64-bit arithmetic before anything is
+ *    allocated.
+ *  - Device pointers are plain CUDA device addresses on the matrix's device;
+ *    x and y must be 16-byte aligned.  The caller owns x, y, out and the stream.
+ *  - Calls that take a stream are asynchronous on it.  Encoders synchronise
+ *    their own upload before returning.
+ *  - Corruption that only the GPU can see (payload bits) never faults or hangs
+ *    a kernel: loops are bounded, reads are clamped to the matrix's buffer, and
+ *    a device status word records EC_ERR_CORRUPT; ec_status() returns it.
+ */
+#ifndef EC_H_
+#define EC_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#ifndef __DRIVER_TYPES_H__
+typedef struct CUstream_st* cudaStream_t; /* same type as CUDA's cudaStream_t */
+#endif
+
+enum {
+    EC_OK = 0,
+    EC_ERR_INVALID_ARG = -1, /* null / misaligned pointer, bad parameter value */
+    EC_ERR_SHAPE = -2,       /* negative or inconsistent dimensions */
+    EC_ERR_OVERFLOW = -3,    /* a size computation would overflow */
+    EC_ERR_UNSUPPORTED = -4, /* valid request the library does not implement (e.g. batch > 16) */
+    EC_ERR_CORRUPT = -5,     /* the compressed data is inconsistent */
+    EC_ERR_CUDA = -6,        /* a CUDA runtime call failed */
+    EC_ERR_OOM = -7          /* host or device allocation failed */
+};
+
+#define EC_MAX_BATCH 16
+#define EC_MAX_GROUP 8
+#define EC_MAX_DECODE_BATCH 64
+
+typedef struct ec_matrix ec_matrix; /* opaque: host descriptor + one device blob */
+
+/* Huffman-exponent codec parameters (NULL = defaults).
+ *  max_code_len  longest codeword, 1..24 (default 24, the workloads' limit); the
+ *                code is textbook Huffman when it fits, otherwise the optimal
+ *                length-limited code (package-merge).
+ *  tile_steps    symbols per lane in one tile of 32 lanes; 32, 64 or 128 (default
+ *                128, i.e. 4096-weight tiles). */
+typedef struct {
+    int32_t max_code_len;
+    int32_t tile_steps;
+    int32_t reserved[2];
+} ec_huff_params;
+
+/* rANS codec parameters (NULL = defaults).
+ *  prob_bits  frequency precision b, 9..15 (default 12)
+ *  tile_syms  symbols per independent tile, a multiple of 32 (default 4096)
+ *  group      weights per FP16 scale along a row (only 128 is supported) */
+typedef struct {
+    int32_t prob_bits;
+    int32_t tile_syms;
+    int32_t group;
+    int32_t reserved;
+} ec_rans_params;
+
+enum { EC_KIND_HUFFMAN_BF16 = 1, EC_KIND_RANS_INT4 = 2 };
+
+/* Sizes and rates of one encoded matrix (ec_stats). */
+typedef struct {
+    int32_t kind;
+    int32_t max_code_len;      /* longest codeword in use (Huffman) or prob_bits (rANS) */
+    int64_t n_rows, k_cols;
+    int64_t k_pad;             /* row length in the coded layout (zero padding at the row end) */
+    int64_t n_tiles;
+    int64_t payload_bits;      /* entropy-coded bits (exponent codewords or rANS words) */
+    int64_t raw_bytes;         /* sign/mantissa bytes (Huffman) or 0 */
+    int64_t aux_bytes;         /* per-tile offsets, lane starts, states, padding */
+    int64_t table_bytes;       /* decode tables, group scales */
+    int64_t device_bytes;      /* whole device blob */
+    double bits_per_weight;    /* device_bytes * 8 / (n_rows * k_cols) */
+    double entropy_bits;       /* H of the coded symbol (exponent byte or 4-bit code), Eq.(2) */
+    double coded_bits_per_symbol; /* payload_bits / coded symbols */
+} ec_stats_t;
+
+/* Encode a row-major BF16 matrix [n_rows, k_cols] (host memory, bit patterns) with
+ * the Huffman-exponent codec and upload it to `device`.  Every one of the 65536
+ * BF16 patterns round-trips exactly.  On success *out owns a device blob; free it
+ * with ec_free.  device < 0 keeps the blob in host memory (no CUDA call is made;
+ * such a matrix can be serialised and inspected but not decoded on a GPU). */
+int ec_encode_bf16(const uint16_t* w_host, int64_t n_rows, int64_t k_cols, const ec_huff_params* params,
+                   int device, ec_matrix** out);
+
+/* Encode 4-bit codes [n_rows, k_cols] (int8 values in [-8, 7], host) with FP16 scales
+ * [n_rows, ceil(k_cols / group)] (host, bit patterns) as rANS tiles and upload them.
+ * The represented weight is w = code * scale (exact in FP32). */
+int ec_encode_rans(const int8_t* codes_host, const uint16_t* scales_f16_host, int64_t n_rows, int64_t k_cols,
+                   const ec_rans_params* params, int device, ec_matrix** out);
+
+/* Decode W to dense row-major BF16 [n_rows, k_cols] in device memory out_bf16.
+ * Huffman: the original bit patterns.  rANS: BF16 round-to-nearest-even of
+ * code * scale. */
+int ec_decode(const ec_matrix* W, uint16_t* out_bf16, cudaStream_t stream);
+
+/* Decode `count` matrices (1..EC_MAX_DECODE_BATCH) in one launch, the way
+ * DFloat11 decompresses a whole transformer block at once (section
+ * "Transformer-block-level decompression").  outs[m] is [n_rows(m), k_cols(m)]. */
+int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs, int count, cudaStream_t stream);
+
+/* y[b, i] = sum_j W[i, j] * x[b, j] for b < batch (1..EC_MAX_BATCH), with the weights
+ * decoded in registers / shared memory and FP32 accumulation.  x: BF16 [batch,
+ * k_cols] device; y: FP32 [batch, n_rows] device, overwritten. */
+int ec_gemv(const ec_matrix* W, const uint16_t* x_bf16, float* y, int batch, cudaStream_t stream);
+
+/* Several GEMVs over the same input x in one launch (MINE section 4.2 "Launch":
+ * q/k/v, gate/up).  All matrices must have the same kind and k_cols; count <=
+ * EC_MAX_GROUP; ys[m] is [batch, n_rows(m)]. */
+int ec_gemv_group(const ec_matrix* const* Ws, int count, const uint16_t* x_bf16, float* const* ys, int batch,
+                  cudaStream_t stream);
+
+/* Uncompressed comparator: y = W x for a dense BF16 W [n_rows, k_cols] in device
+ * memory, FP32 accumulation, same x / y conventions as ec_gemv. */
+int ec_bf16_gemv(const uint16_t* w_bf16, int64_t n_rows, int64_t k_cols, const uint16_t* x_bf16, float* y,
+                 int batch, cudaStream_t stream);
+
+/* Sizes and rates (host only). */
+int ec_stats(const ec_matrix* W, ec_stats_t* out);
+
+/* Code length of each exponent value (Huffman matrices; 0 = absent). */
+int ec_code_lengths(const ec_matrix* W, uint8_t lengths[256]);
+
+/* Synchronise `stream`, then return and clear the device status word of the
+ * current device: EC_OK, or EC_ERR_CORRUPT if a kernel met inconsistent data. */
+int ec_status(cudaStream_t stream);
+
+/* Serialise W into host memory: a fixed metadata block followed by the device blob
+ * (copied back from the GPU).  With dst == NULL only *size_out is set.  Fails with
+ * EC_ERR_INVALID_ARG if capacity < *size_out. */
+int ec_serialize(const ec_matrix* W, void* dst, int64_t capacity, int64_t* size_out);
+
+/* Rebuild a matrix from ec_serialize output.  The bytes are untrusted: the
+ * metadata, every section offset, every tile offset and every decode-table entry
+ * are validated before anything is allocated or uploaded (EC_ERR_CORRUPT on any
+ * inconsistency).  device < 0 keeps the blob in host memory (inspection only;
+ * ec_decode / ec_gemv reject such a matrix). */
+int ec_deserialize(const void* src, int64_t size, int device, ec_matrix** out);
+
+/* Free a matrix (host descriptor and device blob). NULL is ignored. */
+void ec_free(ec_matrix* W);
+
+/* Human-readable text for an EC_* code. */
+const char* ec_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EC_H_ */

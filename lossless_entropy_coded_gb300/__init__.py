@@ -1,0 +1,19 @@
+"""Entropy-coded LLM weights on GB300: lossless Huffman-exponent BF16 and rANS
+4-bit codecs with fused decode + GEMV kernels for sm_103a.
+
+The work happens in libec.so (include/ec.h); this package only marshals arguments.
+The library is loaded on first use of any attribute below; if libec.so has not been
+built the access raises ImportError (there is no fallback path).
+"""
+_API = ("EC_KIND_HUFFMAN_BF16", "EC_KIND_RANS_INT4", "EC_MAX_BATCH", "EC_MAX_GROUP", "EcError", "Matrix",
+        "bf16_gemv", "decode", "decode_batch", "deserialize", "encode_bf16", "encode_rans", "gemv", "gemv_group", "lib",
+        "status", "strerror", "LIB_PATH", "EXPORTS")
+
+__all__ = list(_API)
+
+
+def __getattr__(name):
+    if name in _API:
+        from . import _ec
+        return getattr(_ec, name)
+    raise AttributeError(name)

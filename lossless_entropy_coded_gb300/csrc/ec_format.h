@@ -1,0 +1,81 @@
+/*
+ * ec_format.h -- device layout of an encoded matrix (shared by the host encoder
+ * and the CUDA kernels of this library; nothing outside the library uses it).
+ *
+ * One contiguous device blob per matrix:
+ *
+ *   [ec_blob_header, 256 B]
+ *   [decode table]            Huffman: level-1 table of 2^EC_L1_BITS u32 entries,
+ *                             then 256-entry sub-tables (8 more bits each).
+ *                             rANS:    2^prob_bits u32 slot entries.
+ *   [group scales]            rANS only: FP16 [n_rows, k_pad / 128].
+ *   [tile offsets]            u32 [n_tiles + 1], record start in 16-byte units.
+ *   [tile records]            16-byte aligned, variable length.
+ *
+ * Coded layout of the weights.  The matrix is padded at the end of every row to
+ * k_pad columns (a multiple of EC_HUFF_ROW_ALIGN / EC_RANS_ROW_ALIGN) with zero
+ * weights, flattened row-major, and cut into tiles of 32 * steps positions (the
+ * last tile may be shorter, always a multiple of the row alignment).  Inside a
+ * tile, position q = 32 * i + l is symbol i of lane l: lane l of the decoding warp
+ * owns positions l, l + 32, l + 64, ...
+ *
+ * Huffman tile record (DFloat11's EncodedExponent / PackedSignMantissa /
+ * per-thread start offsets, re-cut so every lane owns a fixed number of symbols):
+ *   u16 lane_start[32]        byte offset of lane l's codewords in the code area
+ *   u8  raw[n_t]              (sign << 7) | mantissa, natural position order,
+ *                             padded to 16 bytes
+ *   u32 code[]                the code area: lane 0's codewords, then lane 1's, ...
+ *                             each lane starting on a byte boundary; bit b of the
+ *                             area is bit 31 - (b % 32) of word b / 32 (MSB first);
+ *                             followed by >= 8 zero bytes, padded to 16 bytes.
+ *
+ * rANS tile record (EntroPack appendix C.3):
+ *   u32 state[32]             the decoder's initial states (the encoder's final ones)
+ *   u16 word[]                16-bit payload words in decoder order, padded to 16 B.
+ */
+#ifndef EC_FORMAT_H_
+#define EC_FORMAT_H_
+
+#include <stdint.h>
+
+#define EC_BLOB_MAGIC 0x31434345u /* "ECC1" */
+#define EC_BLOB_VERSION 1u
+
+#define EC_L1_BITS 12            /* level-1 Huffman window */
+#define EC_SUB_BITS 8            /* bits per sub-table level */
+#define EC_HUFF_ROW_ALIGN 256    /* k_pad multiple for the Huffman layout */
+#define EC_RANS_ROW_ALIGN 128    /* k_pad multiple for the rANS layout (= scale group) */
+#define EC_MAX_CODE_LEN 24
+
+/* Huffman table entry (u32):
+ *   symbol:  bits 0..15 = exponent << 7 (the BF16 exponent field), bits 16..20 =
+ *            total code length, bits 21..31 = 0
+ *   pointer: bit 31 = 1, bits 0..15 = sub-table index, bits 16..20 = bits already
+ *            consumed before the sub-table
+ *   invalid: bit 30 = 1 (a window no codeword matches; only reachable from corrupt
+ *            data or the padding of a one-symbol code). */
+#define EC_ENT_PTR 0x80000000u
+#define EC_ENT_BAD 0x40000000u
+
+/* rANS slot entry (u32): bits 0..3 = symbol (code + 8), bits 4..15 = slot - cum[s],
+ * bits 16..28 = freq[s]. */
+
+typedef struct {
+    uint32_t magic, version;
+    int32_t kind;             /* EC_KIND_* */
+    int32_t steps;            /* symbols per lane per tile */
+    int64_t n_rows, k_cols, k_pad;
+    int64_t n_tiles;
+    int64_t table_off, table_words;   /* byte offset, u32 count */
+    int64_t scales_off;               /* rANS: byte offset of FP16 scales */
+    int64_t tile_off_off;             /* byte offset of u32 tile offsets */
+    int64_t records_off;              /* byte offset of the first record */
+    int64_t blob_bytes;
+    int32_t max_code_bytes;           /* Huffman: largest code area of any tile (bytes) */
+    int32_t prob_bits;                /* rANS */
+    int32_t max_words;                /* rANS: largest payload of any tile (u16 words) */
+    int32_t max_len;                  /* Huffman: longest codeword in use */
+    uint8_t pad[256 - 4 * 4 - 8 * 10 - 4 * 4];
+} ec_blob_header;
+
+#endif /* EC_FORMAT_H_ */

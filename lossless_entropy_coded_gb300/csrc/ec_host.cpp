@@ -1,0 +1,846 @@
+/*
+ * ec_host.cpp -- host side of the library: the two encoders, the device blob, and
+ * the bookkeeping entry points (ec_stats, ec_code_lengths, ec_free, ec_strerror).
+ *
+ * Huffman-exponent codec (DFloat11, "70% Size, 100% Accuracy", section
+ * "Dynamic-Length Float" and Fig. 3): the exponent byte of every BF16 weight is
+ * Huffman coded, one code per matrix; sign and mantissa stay one raw byte.
+ * Codeword lengths come from Huffman's merge rule, or from package-merge when the
+ * Huffman tree is deeper than the length limit; codewords are canonical.
+ *
+ * rANS codec (EntroPack section 3.6 / appendix C.3): 4-bit codes in independent
+ * tiles decoded by one warp, 32 interleaved lanes, 32-bit states in [2^16, 2^32),
+ * 16-bit renormalisation words.
+ *
+ * Sizes are computed with checked 64-bit arithmetic before any allocation
+ * (loading-time rule from "M8.9 Quantized Artifacts and Runtime Integration",
+ * section "Parse Before Allocation").
+ */
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <array>
+#include <atomic>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <queue>
+#include <thread>
+#include <vector>
+
+#include "ec_internal.h"
+
+static_assert(sizeof(ec_blob_header) == 256, "blob header must be 256 bytes");
+
+namespace {
+
+/* ------------------------------------------------------------------ utilities */
+bool mul_ok(int64_t a, int64_t b, int64_t* r) {
+    if (a < 0 || b < 0) return false;
+    if (a != 0 && b > INT64_MAX / a) return false;
+    *r = a * b;
+    return true;
+}
+bool add_ok(int64_t a, int64_t b, int64_t* r) {
+    if (a < 0 || b < 0 || a > INT64_MAX - b) return false;
+    *r = a + b;
+    return true;
+}
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+/* Values at padded positions [base, base + n) of a row-major [rows, K] matrix laid
+ * out with rows of KP >= K entries (the tail of each row reads as zero). */
+template <class T>
+void gather_padded(const T* src, int64_t K, int64_t KP, int64_t base, int64_t n, T* out) {
+    int64_t r = base / KP, c = base - r * KP;
+    for (int64_t q = 0; q < n;) {
+        const int64_t run = std::min(n - q, KP - c);
+        const T* row = src + r * K;
+        for (int64_t k = 0; k < run; ++k) out[q + k] = (c + k < K) ? row[c + k] : T(0);
+        q += run;
+        c = 0;
+        ++r;
+    }
+}
+
+int host_threads() {
+    unsigned n = std::thread::hardware_concurrency();
+    if (n == 0) n = 4;
+    return (int)std::min(n, 64u);
+}
+
+/* Run fn(lo, hi) over [0, n) split across threads. */
+template <class F>
+void parallel_for(int64_t n, F fn, int64_t min_chunk = 1) {
+    int nt = host_threads();
+    if (n / std::max<int64_t>(min_chunk, 1) < nt) nt = (int)std::max<int64_t>(1, n / std::max<int64_t>(min_chunk, 1));
+    if (nt <= 1) {
+        fn((int64_t)0, n);
+        return;
+    }
+    std::vector<std::thread> th;
+    th.reserve(nt);
+    for (int t = 0; t < nt; ++t) th.emplace_back([=] { fn(n * t / nt, n * (t + 1) / nt); });
+    for (auto& x : th) x.join();
+}
+
+/* --------------------------------------------------------- Huffman code lengths */
+
+/* Huffman's merge rule with a priority queue; ties go to the node whose subtree
+ * holds the smallest symbol.  Returns the number of present symbols. */
+int huffman_lengths(const uint64_t counts[256], uint8_t len[256]) {
+    struct Node {
+        uint64_t w;
+        int minsym, id;
+    };
+    auto later = [](const Node& a, const Node& b) { return a.w != b.w ? a.w > b.w : a.minsym > b.minsym; };
+    std::priority_queue<Node, std::vector<Node>, decltype(later)> pq(later);
+    std::vector<int> parent;
+    std::vector<int> leaf(256, -1);
+    for (int s = 0; s < 256; ++s) {
+        if (!counts[s]) continue;
+        leaf[s] = (int)parent.size();
+        pq.push({counts[s], s, (int)parent.size()});
+        parent.push_back(-1);
+    }
+    std::memset(len, 0, 256);
+    const int n = (int)parent.size();
+    if (n == 1) {
+        for (int s = 0; s < 256; ++s)
+            if (leaf[s] >= 0) len[s] = 1;
+    }
+    if (n <= 1) return n;
+    while (pq.size() > 1) {
+        Node a = pq.top();
+        pq.pop();
+        Node b = pq.top();
+        pq.pop();
+        const int id = (int)parent.size();
+        parent.push_back(-1);
+        parent[a.id] = parent[b.id] = id;
+        pq.push({a.w + b.w, std::min(a.minsym, b.minsym), id});
+    }
+    for (int s = 0; s < 256; ++s) {
+        if (leaf[s] < 0) continue;
+        int d = 0;
+        for (int v = leaf[s]; parent[v] >= 0; v = parent[v]) ++d;
+        len[s] = (uint8_t)d;
+    }
+    return n;
+}
+
+/* Optimal code with lengths <= L: package-merge over L denominations.  Leaves are
+ * ordered by (count, symbol); a package is the sum of two adjacent items of the
+ * finer list; equal weights put the leaf first.  The coarsest list keeps 2(n-1)
+ * items and a symbol's length is how often its leaf is inside them (tracked as a
+ * per-item vector of leaf multiplicities, accumulated level by level). */
+bool package_merge_lengths(const uint64_t counts[256], int L, uint8_t len[256]) {
+    std::vector<int> sym;
+    for (int s = 0; s < 256; ++s)
+        if (counts[s]) sym.push_back(s);
+    std::memset(len, 0, 256);
+    const int n = (int)sym.size();
+    if (n <= 1) {
+        if (n == 1) len[sym[0]] = 1;
+        return true;
+    }
+    if (L < 1 || L > 30 || (int64_t(1) << L) < n) return false;
+    std::stable_sort(sym.begin(), sym.end(), [&](int a, int b) { return counts[a] < counts[b]; });
+    /* An item is described by how many times each leaf (by rank) occurs in it. */
+    struct Item {
+        uint64_t w;
+        std::vector<uint8_t> mult;
+    };
+    std::vector<Item> cur;
+    for (int i = 0; i < n; ++i) {
+        Item it{counts[sym[i]], std::vector<uint8_t>(n, 0)};
+        it.mult[i] = 1;
+        cur.push_back(std::move(it));
+    }
+    for (int level = 1; level < L; ++level) {
+        std::vector<Item> next;
+        next.reserve(2 * n);
+        size_t li = 0, pi = 0;
+        const size_t np = cur.size() / 2;
+        while (li < (size_t)n || pi < np) {
+            uint64_t pw = pi < np ? cur[2 * pi].w + cur[2 * pi + 1].w : 0;
+            if (li < (size_t)n && (pi >= np || counts[sym[li]] <= pw)) {
+                Item it{counts[sym[li]], std::vector<uint8_t>(n, 0)};
+                it.mult[li] = 1;
+                next.push_back(std::move(it));
+                ++li;
+            } else {
+                Item it{pw, cur[2 * pi].mult};
+                for (int k = 0; k < n; ++k) it.mult[k] = (uint8_t)(it.mult[k] + cur[2 * pi + 1].mult[k]);
+                next.push_back(std::move(it));
+                ++pi;
+            }
+        }
+        cur.swap(next);
+    }
+    std::vector<int> total(n, 0);
+    for (int i = 0; i < 2 * (n - 1); ++i)
+        for (int k = 0; k < n; ++k) total[k] += cur[i].mult[k];
+    for (int k = 0; k < n; ++k) len[sym[k]] = (uint8_t)total[k];
+    return true;
+}
+
+/* Canonical codewords: ascending (length, symbol), consecutive values. */
+void canonical(const uint8_t len[256], uint32_t code[256]) {
+    std::vector<int> order;
+    for (int s = 0; s < 256; ++s)
+        if (len[s]) order.push_back(s);
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return len[a] < len[b]; });
+    std::memset(code, 0, 256 * sizeof(uint32_t));
+    uint32_t c = 0;
+    for (size_t i = 0; i < order.size(); ++i) {
+        if (i) c = (c + 1) << (len[order[i]] - len[order[i - 1]]);
+        code[order[i]] = c;
+    }
+}
+
+/* Hierarchical decode table: a 2^EC_L1_BITS level-1 table, then 256-entry tables
+ * for every prefix that leads to longer codewords (the decomposition of
+ * DFloat11's appendix, Fig. 4 / Fig. 14, with a wider first level). */
+std::vector<uint32_t> build_huff_table(const uint8_t len[256], const uint32_t code[256]) {
+    struct Tab {
+        uint32_t prefix;
+        int depth, width;
+        size_t base;
+    };
+    std::vector<uint32_t> t(1u << EC_L1_BITS, EC_ENT_BAD);
+    std::vector<Tab> tabs{{0, 0, EC_L1_BITS, 0}};
+    for (size_t k = 0; k < tabs.size(); ++k) {
+        const Tab tb = tabs[k];
+        for (int s = 0; s < 256; ++s) {
+            const int l = len[s];
+            if (l <= tb.depth) continue;
+            if (tb.depth && (code[s] >> (l - tb.depth)) != tb.prefix) continue;
+            const int rem = l - tb.depth;
+            const uint32_t tail = code[s] & ((1u << rem) - 1);
+            if (rem <= tb.width) {
+                const uint32_t lo = tail << (tb.width - rem), hi = (tail + 1) << (tb.width - rem);
+                for (uint32_t i = lo; i < hi; ++i) t[tb.base + i] = ((uint32_t)s << 7) | ((uint32_t)l << 16);
+            } else {
+                const uint32_t idx = tail >> (rem - tb.width);
+                uint32_t& e = t[tb.base + idx];
+                if (!(e & EC_ENT_PTR)) {
+                    const size_t sub = tabs.size();
+                    tabs.push_back({(tb.prefix << tb.width) | idx, tb.depth + tb.width, EC_SUB_BITS,
+                                    t.size()});
+                    t.resize(t.size() + (1u << EC_SUB_BITS), EC_ENT_BAD);
+                    t[tb.base + idx] = EC_ENT_PTR | (uint32_t)(sub - 1) | ((uint32_t)(tb.depth + tb.width) << 16);
+                }
+            }
+        }
+    }
+    return t;
+}
+
+/* ------------------------------------------------------------ rANS frequencies */
+
+/* f_s = max(1, floor(M c_s / n)) for present s; while the sum is short add one to
+ * the present symbol with the largest remainder M c_s - f_s n, while it is over
+ * take one from the present symbol with f_s > 1 and the smallest remainder (ties
+ * to the lower symbol in both cases). */
+bool rans_normalise(const uint64_t counts[16], int prob_bits, uint32_t f[16]) {
+    const int64_t M = int64_t(1) << prob_bits;
+    unsigned __int128 n = 0;
+    for (int s = 0; s < 16; ++s) n += counts[s];
+    std::memset(f, 0, 16 * sizeof(uint32_t));
+    if (n == 0) return true;
+    __int128 rem[16] = {};
+    int64_t sum = 0;
+    for (int s = 0; s < 16; ++s) {
+        if (!counts[s]) continue;
+        int64_t v = (int64_t)((unsigned __int128)M * counts[s] / n);
+        v = std::max<int64_t>(v, 1);
+        f[s] = (uint32_t)v;
+        rem[s] = (__int128)M * counts[s] - (__int128)v * (__int128)n;
+        sum += v;
+    }
+    for (; sum < M; ++sum) {
+        int b = -1;
+        for (int s = 0; s < 16; ++s)
+            if (counts[s] && (b < 0 || rem[s] > rem[b])) b = s;
+        f[b]++;
+        rem[b] -= (__int128)n;
+    }
+    for (; sum > M; --sum) {
+        int b = -1;
+        for (int s = 0; s < 16; ++s)
+            if (counts[s] && f[s] > 1 && (b < 0 || rem[s] < rem[b])) b = s;
+        if (b < 0) return false;
+        f[b]--;
+        rem[b] += (__int128)n;
+    }
+    return true;
+}
+
+double entropy_bits(const uint64_t* c, int n) {
+    double tot = 0, h = 0;
+    for (int i = 0; i < n; ++i) tot += (double)c[i];
+    if (tot <= 0) return 0;
+    for (int i = 0; i < n; ++i)
+        if (c[i]) {
+            const double p = (double)c[i] / tot;
+            h -= p * std::log2(p);
+        }
+    return h;
+}
+
+/* ------------------------------------------------------------------ device blob */
+int upload(ec_matrix* m, const std::vector<uint8_t>& blob, int device) {
+    if (device < 0) { /* host-only matrix: inspection and serialisation, no kernels */
+        m->h_blob = (uint8_t*)std::malloc(std::max<size_t>(blob.size(), 1));
+        if (!m->h_blob) return EC_ERR_OOM;
+        std::memcpy(m->h_blob, blob.data(), blob.size());
+        return EC_OK;
+    }
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess) return EC_ERR_CUDA;
+    if (cudaSetDevice(device) != cudaSuccess) return EC_ERR_INVALID_ARG;
+    void* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, std::max<size_t>(blob.size(), 256));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        cudaSetDevice(prev);
+        return e == cudaErrorMemoryAllocation ? EC_ERR_OOM : EC_ERR_CUDA;
+    }
+    e = cudaMemcpy(p, blob.data(), blob.size(), cudaMemcpyHostToDevice);
+    cudaSetDevice(prev);
+    if (e != cudaSuccess) {
+        cudaFree(p);
+        return EC_ERR_CUDA;
+    }
+    m->d_blob = (uint8_t*)p;
+    return EC_OK;
+}
+
+ec_matrix* new_matrix() {
+    ec_matrix* m = new (std::nothrow) ec_matrix;
+    if (m) std::memset((void*)m, 0, sizeof(ec_matrix));
+    return m;
+}
+
+/* Encoder body under a try block: std::bad_alloc becomes EC_ERR_OOM. */
+template <class F>
+int guarded(F fn) {
+    try {
+        return fn();
+    } catch (const std::bad_alloc&) {
+        return EC_ERR_OOM;
+    } catch (...) {
+        return EC_ERR_INVALID_ARG;
+    }
+}
+
+}  // namespace
+
+/* ============================================================ Huffman encoder */
+extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols, const ec_huff_params* params,
+                              int device, ec_matrix** out) {
+    if (!out) return EC_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (n_rows < 0 || k_cols < 0) return EC_ERR_SHAPE;
+    const int max_len = params ? params->max_code_len : EC_MAX_CODE_LEN;
+    const int steps = params ? params->tile_steps : 128;
+    if (max_len < 1 || max_len > EC_MAX_CODE_LEN) return EC_ERR_INVALID_ARG;
+    if (steps != 32 && steps != 64 && steps != 128) return EC_ERR_INVALID_ARG;
+    int64_t nk = 0, k_pad = round_up(k_cols, EC_HUFF_ROW_ALIGN), n_pad = 0, tmp = 0;
+    if (k_cols > INT64_MAX - EC_HUFF_ROW_ALIGN) return EC_ERR_OVERFLOW;
+    if (!mul_ok(n_rows, k_cols, &nk) || !mul_ok(n_rows, k_pad, &n_pad) || !mul_ok(n_pad, 4, &tmp))
+        return EC_ERR_OVERFLOW;
+    if (nk > 0 && !w) return EC_ERR_INVALID_ARG;
+
+    return guarded([&]() -> int {
+        const int64_t T = 32 * (int64_t)steps;
+        const int64_t n_tiles = (n_pad + T - 1) / T;
+        const int64_t K = k_cols, KP = k_pad;
+
+        /* exponent histogram over the padded layout */
+        const int nth = host_threads();
+        std::vector<std::vector<uint64_t>> part(nth, std::vector<uint64_t>(256, 0));
+        std::atomic<int> slot{0};
+        parallel_for(
+            n_rows,
+            [&](int64_t lo, int64_t hi) {
+                std::vector<uint64_t>& h = part[slot++ % nth];
+                for (int64_t r = lo; r < hi; ++r) {
+                    const uint16_t* row = w + r * K;
+                    for (int64_t c = 0; c < K; ++c) h[(row[c] >> 7) & 0xFF]++;
+                }
+            },
+            16);
+        ec_matrix* m = new_matrix();
+        if (!m) return EC_ERR_OOM;
+        for (auto& h : part)
+            for (int s = 0; s < 256; ++s) m->counts[s] += h[s];
+        m->counts[0] += (uint64_t)(n_rows * (KP - K));
+
+        if (huffman_lengths(m->counts, m->lengths) > 1) {
+            int longest = *std::max_element(m->lengths, m->lengths + 256);
+            if (longest > max_len && !package_merge_lengths(m->counts, max_len, m->lengths)) {
+                delete m;
+                return EC_ERR_INVALID_ARG;
+            }
+        }
+        uint32_t code[256];
+        canonical(m->lengths, code);
+        std::vector<uint32_t> table = build_huff_table(m->lengths, code);
+
+        /* pass 1: per-tile record sizes */
+        std::vector<int64_t> rec_bytes(n_tiles + 1, 0), code_bytes(n_tiles, 0);
+        parallel_for(n_tiles, [&](int64_t lo, int64_t hi) {
+            std::vector<uint16_t> v(T);
+            for (int64_t t = lo; t < hi; ++t) {
+                const int64_t base = t * T, n_t = std::min(T, n_pad - base);
+                gather_padded(w, K, KP, base, n_t, v.data());
+                int64_t bits[32] = {0};
+                for (int64_t q = 0; q < n_t; ++q) bits[q & 31] += m->lengths[(v[q] >> 7) & 0xFF];
+                int64_t bytes = 0;
+                for (int l = 0; l < 32; ++l) bytes += (bits[l] + 7) / 8;
+                code_bytes[t] = round_up(bytes + 8, 16);
+                rec_bytes[t] = 64 + round_up(n_t, 16) + code_bytes[t];
+            }
+        });
+        std::vector<uint32_t> tile_off(n_tiles + 1, 0);
+        int64_t total = 0, max_code = 0, payload = 0;
+        for (int64_t t = 0; t < n_tiles; ++t) {
+            tile_off[t] = (uint32_t)(total / 16);
+            if (!add_ok(total, rec_bytes[t], &total)) {
+                delete m;
+                return EC_ERR_OVERFLOW;
+            }
+            max_code = std::max(max_code, code_bytes[t]);
+        }
+        if (total / 16 > (int64_t)UINT32_MAX) {
+            delete m;
+            return EC_ERR_OVERFLOW;
+        }
+        tile_off[n_tiles] = (uint32_t)(total / 16);
+
+        ec_blob_header h{};
+        h.magic = EC_BLOB_MAGIC;
+        h.version = EC_BLOB_VERSION;
+        h.kind = EC_KIND_HUFFMAN_BF16;
+        h.steps = steps;
+        h.n_rows = n_rows;
+        h.k_cols = k_cols;
+        h.k_pad = KP;
+        h.n_tiles = n_tiles;
+        h.table_off = sizeof(ec_blob_header);
+        h.table_words = (int64_t)table.size();
+        h.scales_off = 0;
+        h.tile_off_off = round_up(h.table_off + 4 * h.table_words, 16);
+        h.records_off = round_up(h.tile_off_off + 4 * (n_tiles + 1), 16);
+        h.blob_bytes = h.records_off + total;
+        h.max_code_bytes = (int32_t)max_code;
+        h.max_len = *std::max_element(m->lengths, m->lengths + 256);
+
+        std::vector<uint8_t> blob((size_t)h.blob_bytes, 0);
+        std::memcpy(blob.data(), &h, sizeof h);
+        std::memcpy(blob.data() + h.table_off, table.data(), 4 * table.size());
+        std::memcpy(blob.data() + h.tile_off_off, tile_off.data(), 4 * tile_off.size());
+
+        /* pass 2: records */
+        parallel_for(n_tiles, [&](int64_t lo, int64_t hi) {
+            std::vector<uint16_t> v(T);
+            for (int64_t t = lo; t < hi; ++t) {
+                uint8_t* rec = blob.data() + h.records_off + (int64_t)tile_off[t] * 16;
+                const int64_t base = t * T, n_t = std::min(T, n_pad - base), S = n_t / 32;
+                gather_padded(w, K, KP, base, n_t, v.data());
+                uint16_t* start = (uint16_t*)rec;
+                uint8_t* raw = rec + 64;
+                uint32_t* area = (uint32_t*)(rec + 64 + round_up(n_t, 16));
+                for (int64_t q = 0; q < n_t; ++q) raw[q] = (uint8_t)(((v[q] >> 8) & 0x80) | (v[q] & 0x7F));
+                int64_t bitpos = 0;
+                for (int l = 0; l < 32; ++l) {
+                    bitpos = round_up(bitpos, 8);
+                    start[l] = (uint16_t)(bitpos / 8);
+                    for (int64_t i = 0; i < S; ++i) {
+                        const int e = (v[32 * i + l] >> 7) & 0xFF;
+                        const int L = m->lengths[e];
+                        const uint32_t c = code[e];
+                        const int64_t wi = bitpos >> 5;
+                        const int o = (int)(bitpos & 31);
+                        if (o + L <= 32) {
+                            area[wi] |= c << (32 - o - L);
+                        } else {
+                            area[wi] |= c >> (o + L - 32);
+                            area[wi + 1] |= c << (64 - o - L);
+                        }
+                        bitpos += L;
+                    }
+                }
+            }
+        });
+        for (int s = 0; s < 256; ++s) payload += (int64_t)m->counts[s] * m->lengths[s];
+
+        m->kind = EC_KIND_HUFFMAN_BF16;
+        m->device = device;
+        m->hdr = h;
+        m->payload_bits = payload;
+        m->raw_bytes = n_pad;
+        m->table_bytes = 4 * (int64_t)table.size();
+        m->aux_bytes = h.blob_bytes - m->table_bytes - n_pad - (payload + 7) / 8;
+        m->entropy = entropy_bits(m->counts, 256);
+        int rc = upload(m, blob, device);
+        if (rc != EC_OK) {
+            delete m;
+            return rc;
+        }
+        *out = m;
+        return EC_OK;
+    });
+}
+
+/* =============================================================== rANS encoder */
+extern "C" int ec_encode_rans(const int8_t* codes, const uint16_t* scales, int64_t n_rows, int64_t k_cols,
+                              const ec_rans_params* params, int device, ec_matrix** out) {
+    if (!out) return EC_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (n_rows < 0 || k_cols < 0) return EC_ERR_SHAPE;
+    const int b = params ? params->prob_bits : 12;
+    const int T = params ? params->tile_syms : 4096;
+    const int group = params ? params->group : 128;
+    if (b < 9 || b > 15 || T < 32 || T % EC_RANS_ROW_ALIGN || T > 65536) return EC_ERR_INVALID_ARG;
+    if (group != 128) return EC_ERR_UNSUPPORTED;
+    if (k_cols > INT64_MAX - EC_RANS_ROW_ALIGN) return EC_ERR_OVERFLOW;
+    const int64_t KP = round_up(k_cols, EC_RANS_ROW_ALIGN), G = KP / 128;
+    int64_t nk = 0, n_pad = 0, ns = 0, tmp = 0;
+    if (!mul_ok(n_rows, k_cols, &nk) || !mul_ok(n_rows, KP, &n_pad) || !mul_ok(n_rows, G, &ns) ||
+        !mul_ok(n_pad, 4, &tmp))
+        return EC_ERR_OVERFLOW;
+    if (nk > 0 && (!codes || !scales)) return EC_ERR_INVALID_ARG;
+
+    return guarded([&]() -> int {
+        const int64_t K = k_cols;
+        for (int64_t i = 0; i < nk; ++i)
+            if (codes[i] < -8 || codes[i] > 7) return EC_ERR_INVALID_ARG;
+        ec_matrix* m = new_matrix();
+        if (!m) return EC_ERR_OOM;
+        for (int64_t i = 0; i < nk; ++i) m->counts[codes[i] + 8]++;
+        m->counts[8] += (uint64_t)(n_rows * (KP - K));
+        if (!rans_normalise(m->counts, b, m->freqs)) {
+            delete m;
+            return EC_ERR_INVALID_ARG;
+        }
+        const uint32_t M = 1u << b;
+        uint32_t cum[16];
+        for (int s = 0, c = 0; s < 16; ++s) {
+            cum[s] = (uint32_t)c;
+            c += (int)m->freqs[s];
+        }
+        std::vector<uint32_t> table(M, 0);
+        for (int s = 0; s < 16; ++s)
+            for (uint32_t k = 0; k < m->freqs[s]; ++k)
+                table[cum[s] + k] = (uint32_t)s | (k << 4) | (m->freqs[s] << 16);
+
+        const int64_t n_tiles = (n_pad + T - 1) / T;
+        std::vector<std::vector<uint16_t>> words(n_tiles);
+        std::vector<std::array<uint32_t, 32>> states(n_tiles);
+        const uint64_t unit = uint64_t(1) << (32 - b);
+        parallel_for(n_tiles, [&](int64_t lo, int64_t hi) {
+            std::vector<uint16_t> stack;
+            std::vector<int8_t> v(T);
+            for (int64_t t = lo; t < hi; ++t) {
+                const int64_t base = t * T, n_t = std::min<int64_t>(T, n_pad - base), S = n_t / 32;
+                gather_padded(codes, K, KP, base, n_t, v.data());
+                uint64_t x[32];
+                for (int l = 0; l < 32; ++l) x[l] = 1u << 16;
+                stack.clear();
+                for (int64_t j = S - 1; j >= 0; --j)
+                    for (int l = 31; l >= 0; --l) {
+                        const int s = v[32 * j + l] + 8;
+                        const uint64_t f = m->freqs[s];
+                        if (x[l] >= f * unit) {
+                            stack.push_back((uint16_t)x[l]);
+                            x[l] >>= 16;
+                        }
+                        x[l] = ((x[l] / f) << b) + x[l] % f + cum[s];
+                    }
+                for (int l = 0; l < 32; ++l) states[t][l] = (uint32_t)x[l];
+                words[t].assign(stack.rbegin(), stack.rend());
+            }
+        });
+        std::vector<uint32_t> tile_off(n_tiles + 1, 0);
+        int64_t total = 0, max_words = 0, payload = 0;
+        for (int64_t t = 0; t < n_tiles; ++t) {
+            tile_off[t] = (uint32_t)(total / 16);
+            total += 128 + round_up(2 * (int64_t)words[t].size(), 16);
+            max_words = std::max<int64_t>(max_words, (int64_t)words[t].size());
+            payload += 16 * (int64_t)words[t].size();
+        }
+        if (total / 16 > (int64_t)UINT32_MAX) {
+            delete m;
+            return EC_ERR_OVERFLOW;
+        }
+        tile_off[n_tiles] = (uint32_t)(total / 16);
+
+        ec_blob_header h{};
+        h.magic = EC_BLOB_MAGIC;
+        h.version = EC_BLOB_VERSION;
+        h.kind = EC_KIND_RANS_INT4;
+        h.steps = T / 32;
+        h.n_rows = n_rows;
+        h.k_cols = k_cols;
+        h.k_pad = KP;
+        h.n_tiles = n_tiles;
+        h.table_off = sizeof(ec_blob_header);
+        h.table_words = M;
+        h.scales_off = round_up(h.table_off + 4 * (int64_t)M, 16);
+        h.tile_off_off = round_up(h.scales_off + 2 * ns, 16);
+        h.records_off = round_up(h.tile_off_off + 4 * (n_tiles + 1), 16);
+        h.blob_bytes = h.records_off + total;
+        h.prob_bits = b;
+        h.max_words = (int32_t)max_words;
+
+        std::vector<uint8_t> blob((size_t)h.blob_bytes, 0);
+        std::memcpy(blob.data(), &h, sizeof h);
+        std::memcpy(blob.data() + h.table_off, table.data(), 4 * table.size());
+        if (ns) std::memcpy(blob.data() + h.scales_off, scales, 2 * (size_t)ns);
+        std::memcpy(blob.data() + h.tile_off_off, tile_off.data(), 4 * tile_off.size());
+        parallel_for(n_tiles, [&](int64_t lo, int64_t hi) {
+            for (int64_t t = lo; t < hi; ++t) {
+                uint8_t* rec = blob.data() + h.records_off + (int64_t)tile_off[t] * 16;
+                std::memcpy(rec, states[t].data(), 128);
+                if (!words[t].empty()) std::memcpy(rec + 128, words[t].data(), 2 * words[t].size());
+            }
+        });
+        m->kind = EC_KIND_RANS_INT4;
+        m->device = device;
+        m->hdr = h;
+        m->payload_bits = payload;
+        m->raw_bytes = 0;
+        m->table_bytes = 4 * (int64_t)M + 2 * ns;
+        m->aux_bytes = h.blob_bytes - m->table_bytes - payload / 8;
+        m->entropy = entropy_bits(m->counts, 16);
+        int rc = upload(m, blob, device);
+        if (rc != EC_OK) {
+            delete m;
+            return rc;
+        }
+        *out = m;
+        return EC_OK;
+    });
+}
+
+/* ======================================================= bookkeeping entry points */
+extern "C" int ec_stats(const ec_matrix* m, ec_stats_t* s) {
+    if (!m || !s) return EC_ERR_INVALID_ARG;
+    std::memset(s, 0, sizeof *s);
+    s->kind = m->kind;
+    s->max_code_len = m->kind == EC_KIND_HUFFMAN_BF16 ? m->hdr.max_len : m->hdr.prob_bits;
+    s->n_rows = m->hdr.n_rows;
+    s->k_cols = m->hdr.k_cols;
+    s->k_pad = m->hdr.k_pad;
+    s->n_tiles = m->hdr.n_tiles;
+    s->payload_bits = m->payload_bits;
+    s->raw_bytes = m->raw_bytes;
+    s->aux_bytes = m->aux_bytes;
+    s->table_bytes = m->table_bytes;
+    s->device_bytes = m->hdr.blob_bytes;
+    const double n = (double)m->hdr.n_rows * (double)m->hdr.k_cols;
+    s->bits_per_weight = n > 0 ? 8.0 * (double)m->hdr.blob_bytes / n : 0.0;
+    s->entropy_bits = m->entropy;
+    const double coded = (double)m->hdr.n_rows * (double)m->hdr.k_pad;
+    s->coded_bits_per_symbol = coded > 0 ? (double)m->payload_bits / coded : 0.0;
+    return EC_OK;
+}
+
+extern "C" int ec_code_lengths(const ec_matrix* m, uint8_t lengths[256]) {
+    if (!m || !lengths) return EC_ERR_INVALID_ARG;
+    if (m->kind != EC_KIND_HUFFMAN_BF16) return EC_ERR_UNSUPPORTED;
+    std::memcpy(lengths, m->lengths, 256);
+    return EC_OK;
+}
+
+extern "C" void ec_free(ec_matrix* m) {
+    if (!m) return;
+    std::free(m->h_blob);
+    if (m->d_blob) {
+        int prev = 0;
+        cudaGetDevice(&prev);
+        cudaSetDevice(m->device);
+        cudaFree(m->d_blob);
+        cudaSetDevice(prev);
+    }
+    delete m;
+}
+
+extern "C" const char* ec_strerror(int code) {
+    switch (code) {
+        case EC_OK: return "ok";
+        case EC_ERR_INVALID_ARG: return "invalid argument";
+        case EC_ERR_SHAPE: return "invalid shape";
+        case EC_ERR_OVERFLOW: return "size overflow";
+        case EC_ERR_UNSUPPORTED: return "unsupported request";
+        case EC_ERR_CORRUPT: return "corrupt compressed data";
+        case EC_ERR_CUDA: return "CUDA runtime error";
+        case EC_ERR_OOM: return "out of memory";
+        default: return "unknown error";
+    }
+}
+
+/* ============================================================ serialisation */
+namespace {
+
+struct SerialMeta {
+    char magic[8];          /* "ECSER001" */
+    int32_t kind, reserved;
+    int64_t blob_bytes;
+    uint64_t counts[256];
+    uint8_t lengths[256];
+    uint32_t freqs[16];
+    int64_t payload_bits, raw_bytes, aux_bytes, table_bytes;
+    double entropy;
+};
+const char kSerialMagic[8] = {'E', 'C', 'S', 'E', 'R', '0', '0', '1'};
+
+/* Structural validation of a device blob held in host memory: every field and
+ * offset is checked with overflow-safe arithmetic before anything trusts it
+ * ("M8.9 Quantized Artifacts and Runtime Integration", sections "Parse Before
+ * Allocation" and "Container Gates").  Payload bits are not checked here; the
+ * kernels bound every read and report EC_ERR_CORRUPT through ec_status. */
+int validate_blob(const uint8_t* b, int64_t bytes) {
+    if (bytes < (int64_t)sizeof(ec_blob_header)) return EC_ERR_CORRUPT;
+    ec_blob_header h;
+    std::memcpy(&h, b, sizeof h);
+    if (h.magic != EC_BLOB_MAGIC || h.version != EC_BLOB_VERSION) return EC_ERR_CORRUPT;
+    if (h.blob_bytes != bytes) return EC_ERR_CORRUPT;
+    if (h.kind != EC_KIND_HUFFMAN_BF16 && h.kind != EC_KIND_RANS_INT4) return EC_ERR_CORRUPT;
+    if (h.n_rows < 0 || h.k_cols < 0 || h.k_cols > INT64_MAX / 2) return EC_ERR_CORRUPT;
+    const bool huff = h.kind == EC_KIND_HUFFMAN_BF16;
+    const int64_t align = huff ? EC_HUFF_ROW_ALIGN : EC_RANS_ROW_ALIGN;
+    if (h.k_pad != round_up(h.k_cols, align)) return EC_ERR_CORRUPT;
+    if (huff ? (h.steps != 32 && h.steps != 64 && h.steps != 128) : (h.steps < 1 || (32 * h.steps) % align))
+        return EC_ERR_CORRUPT;
+    int64_t n_pad = 0;
+    if (!mul_ok(h.n_rows, h.k_pad, &n_pad)) return EC_ERR_CORRUPT;
+    const int64_t T = 32 * (int64_t)h.steps;
+    if (h.n_tiles != (n_pad + T - 1) / T) return EC_ERR_CORRUPT;
+    if (h.table_off != (int64_t)sizeof(ec_blob_header)) return EC_ERR_CORRUPT;
+    int64_t end = 0, t4 = 0;
+    if (huff) {
+        if (h.table_words < (1 << EC_L1_BITS) || (h.table_words - (1 << EC_L1_BITS)) % 256) return EC_ERR_CORRUPT;
+        if (h.max_len < 0 || h.max_len > EC_MAX_CODE_LEN || h.max_code_bytes < 0) return EC_ERR_CORRUPT;
+    } else {
+        if (h.prob_bits < 9 || h.prob_bits > 15 || h.table_words != (int64_t(1) << h.prob_bits) || h.max_words < 0)
+            return EC_ERR_CORRUPT;
+    }
+    if (!mul_ok(h.table_words, 4, &t4) || !add_ok(h.table_off, t4, &end)) return EC_ERR_CORRUPT;
+    if (!huff) {
+        int64_t ns = 0, s2 = 0;
+        if (!mul_ok(h.n_rows, h.k_pad / 128, &ns) || !mul_ok(ns, 2, &s2)) return EC_ERR_CORRUPT;
+        if (h.scales_off < end || h.scales_off % 16 || !add_ok(h.scales_off, s2, &end)) return EC_ERR_CORRUPT;
+    }
+    int64_t to4 = 0;
+    if (h.tile_off_off < end || h.tile_off_off % 16 || !mul_ok(h.n_tiles + 1, 4, &to4) ||
+        !add_ok(h.tile_off_off, to4, &end))
+        return EC_ERR_CORRUPT;
+    if (h.records_off < end || h.records_off % 16 || h.records_off > bytes) return EC_ERR_CORRUPT;
+    const uint32_t* off = (const uint32_t*)(b + h.tile_off_off);
+    if (off[0] != 0 || (int64_t)off[h.n_tiles] * 16 != bytes - h.records_off) return EC_ERR_CORRUPT;
+    for (int64_t t = 0; t < h.n_tiles; ++t) {
+        if (off[t + 1] < off[t]) return EC_ERR_CORRUPT;
+        const int64_t rb = ((int64_t)off[t + 1] - off[t]) * 16;
+        const int64_t n_t = std::min(T, n_pad - t * T);
+        if (huff) {
+            const int64_t area = rb - 64 - round_up(n_t, 16);
+            if (area < 16 || area > h.max_code_bytes) return EC_ERR_CORRUPT;
+            const uint16_t* start = (const uint16_t*)(b + h.records_off + (int64_t)off[t] * 16);
+            for (int l = 0; l < 32; ++l)
+                if (start[l] > area || (l && start[l] < start[l - 1])) return EC_ERR_CORRUPT;
+        } else {
+            if (rb < 128 || (rb - 128) / 2 > round_up(h.max_words, 8)) return EC_ERR_CORRUPT;
+        }
+    }
+    const uint32_t* tab = (const uint32_t*)(b + h.table_off);
+    if (huff) {
+        const int64_t n_sub = (h.table_words - (1 << EC_L1_BITS)) / 256;
+        for (int64_t i = 0; i < h.table_words; ++i)
+            if ((tab[i] & EC_ENT_PTR) && (int64_t)(tab[i] & 0xFFFFu) >= n_sub) return EC_ERR_CORRUPT;
+    } else {
+        for (int64_t i = 0; i < h.table_words; ++i) {
+            const uint32_t f = tab[i] >> 16, k = (tab[i] >> 4) & 0xFFF;
+            if (f == 0 || f > (1u << h.prob_bits) || k >= f) return EC_ERR_CORRUPT;
+        }
+    }
+    return EC_OK;
+}
+
+}  // namespace
+
+extern "C" int ec_serialize(const ec_matrix* m, void* dst, int64_t capacity, int64_t* size_out) {
+    if (!m || !size_out) return EC_ERR_INVALID_ARG;
+    const int64_t need = (int64_t)sizeof(SerialMeta) + m->hdr.blob_bytes;
+    *size_out = need;
+    if (!dst) return EC_OK;
+    if (capacity < need) return EC_ERR_INVALID_ARG;
+    SerialMeta s{};
+    std::memcpy(s.magic, kSerialMagic, 8);
+    s.kind = m->kind;
+    s.blob_bytes = m->hdr.blob_bytes;
+    std::memcpy(s.counts, m->counts, sizeof s.counts);
+    std::memcpy(s.lengths, m->lengths, sizeof s.lengths);
+    std::memcpy(s.freqs, m->freqs, sizeof s.freqs);
+    s.payload_bits = m->payload_bits;
+    s.raw_bytes = m->raw_bytes;
+    s.aux_bytes = m->aux_bytes;
+    s.table_bytes = m->table_bytes;
+    s.entropy = m->entropy;
+    std::memcpy(dst, &s, sizeof s);
+    uint8_t* out = (uint8_t*)dst + sizeof s;
+    if (m->h_blob) {
+        std::memcpy(out, m->h_blob, (size_t)m->hdr.blob_bytes);
+        return EC_OK;
+    }
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess) return EC_ERR_CUDA;
+    cudaSetDevice(m->device);
+    const cudaError_t e = cudaMemcpy(out, m->d_blob, (size_t)m->hdr.blob_bytes, cudaMemcpyDeviceToHost);
+    cudaSetDevice(prev);
+    return e == cudaSuccess ? EC_OK : EC_ERR_CUDA;
+}
+
+extern "C" int ec_deserialize(const void* src, int64_t size, int device, ec_matrix** out) {
+    if (!src || !out) return EC_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (size < (int64_t)sizeof(SerialMeta)) return EC_ERR_CORRUPT;
+    SerialMeta s;
+    std::memcpy(&s, src, sizeof s);
+    if (std::memcmp(s.magic, kSerialMagic, 8) != 0) return EC_ERR_CORRUPT;
+    if (s.blob_bytes < 0 || s.blob_bytes != size - (int64_t)sizeof s) return EC_ERR_CORRUPT;
+    const uint8_t* blob = (const uint8_t*)src + sizeof s;
+    int rc = validate_blob(blob, s.blob_bytes);
+    if (rc != EC_OK) return rc;
+    return guarded([&]() -> int {
+        ec_matrix* m = new_matrix();
+        if (!m) return EC_ERR_OOM;
+        std::memcpy(&m->hdr, blob, sizeof m->hdr);
+        if (s.kind != m->hdr.kind) {
+            delete m;
+            return EC_ERR_CORRUPT;
+        }
+        m->kind = s.kind;
+        m->device = device;
+        std::memcpy(m->counts, s.counts, sizeof s.counts);
+        std::memcpy(m->lengths, s.lengths, sizeof s.lengths);
+        std::memcpy(m->freqs, s.freqs, sizeof s.freqs);
+        m->payload_bits = s.payload_bits;
+        m->raw_bytes = s.raw_bytes;
+        m->aux_bytes = s.aux_bytes;
+        m->table_bytes = s.table_bytes;
+        m->entropy = s.entropy;
+        std::vector<uint8_t> copy(blob, blob + s.blob_bytes);
+        const int r = upload(m, copy, device);
+        if (r != EC_OK) {
+            delete m;
+            return r;
+        }
+        *out = m;
+        return EC_OK;
+    });
+}

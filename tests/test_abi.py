@@ -1,0 +1,235 @@
+"""CPU-only tests of the C ABI: exported symbols, argument validation, the host
+encoders (through host-only matrices and their serialised form), the untrusted-
+input validator, and agreement of the library's code lengths / rANS frequencies
+with the oracle's (same tie rules, independent implementations)."""
+import ctypes
+import os
+import re
+import struct
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ec():
+    from lossless_entropy_coded_gb300 import build
+    build.build()
+    import lossless_entropy_coded_gb300 as ec
+    return ec
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "ec.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ec_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(ec):
+    names = declared_functions()
+    assert len(names) >= 14
+    lib = ctypes.CDLL(ec.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ec.h but not exported"
+    assert set(ec.EXPORTS) == set(names)
+
+
+def test_strerror_codes(ec):
+    for c in range(-7, 1):
+        assert ec.strerror(c) and ec.strerror(c) != "unknown error"
+    assert ec.strerror(-99) == "unknown error"
+
+
+def rc_of(fn, *a):
+    from lossless_entropy_coded_gb300 import _ec
+    h = ctypes.c_void_p()
+    return fn(*a, ctypes.byref(h)), h
+
+
+def test_argument_validation(ec):
+    from lossless_entropy_coded_gb300 import _ec
+    lib = ec.lib
+    w = np.zeros(16, np.uint16)
+    bad = [(-1, 4, None, _ec.EC_ERR_SHAPE), (4, -1, None, _ec.EC_ERR_SHAPE),
+           (2 ** 62, 1024, None, _ec.EC_ERR_OVERFLOW),
+           (4, 4, _ec.HuffParams(0, 128), _ec.EC_ERR_INVALID_ARG),
+           (4, 4, _ec.HuffParams(25, 128), _ec.EC_ERR_INVALID_ARG),
+           (4, 4, _ec.HuffParams(24, 100), _ec.EC_ERR_INVALID_ARG)]
+    for n, k, prm, want in bad:
+        h = ctypes.c_void_p()
+        rc = lib.ec_encode_bf16(w.ctypes.data, n, k, ctypes.byref(prm) if prm else None, -1, ctypes.byref(h))
+        assert rc == want, (n, k, rc)
+        assert not h.value
+    assert lib.ec_encode_bf16(None, 4, 4, None, -1, ctypes.byref(ctypes.c_void_p())) == _ec.EC_ERR_INVALID_ARG
+    assert lib.ec_encode_bf16(w.ctypes.data, 4, 4, None, -1, None) == _ec.EC_ERR_INVALID_ARG
+    codes = np.array([[0, 8]], np.int8)
+    sc = np.zeros((1, 1), np.uint16)
+    h = ctypes.c_void_p()
+    assert lib.ec_encode_rans(codes.ctypes.data, sc.ctypes.data, 1, 2, None, -1, ctypes.byref(h)) == _ec.EC_ERR_INVALID_ARG
+    assert lib.ec_encode_rans(codes.ctypes.data, sc.ctypes.data, 1, 2, ctypes.byref(_ec.RansParams(12, 4096, 64, 0)),
+                              -1, ctypes.byref(h)) == _ec.EC_ERR_UNSUPPORTED
+    assert lib.ec_encode_rans(codes.ctypes.data, sc.ctypes.data, 1, 2, ctypes.byref(_ec.RansParams(8, 4096, 128, 0)),
+                              -1, ctypes.byref(h)) == _ec.EC_ERR_INVALID_ARG
+    # host-only matrices are rejected by the device entry points
+    W = ec.encode_bf16(synth.gauss_bf16(1, (4, 8), 0.02), device=-1)
+    assert lib.ec_gemv(W.handle, None, None, 1, None) == _ec.EC_ERR_INVALID_ARG
+    assert lib.ec_gemv(W.handle, None, None, 0, None) == _ec.EC_ERR_INVALID_ARG
+    assert lib.ec_gemv(W.handle, None, None, 17, None) == _ec.EC_ERR_UNSUPPORTED
+
+
+# --------------------------------------------------------------- blob reader
+HDR = struct.Struct("<IIii" + "q" * 10 + "iiii")
+
+
+def parse(blob: bytes):
+    meta_size = 8 + 8 + 8 + 256 * 8 + 256 + 16 * 4 + 4 * 8 + 8
+    dev = blob[meta_size:]
+    f = HDR.unpack_from(dev, 0)
+    keys = ["magic", "version", "kind", "steps", "n_rows", "k_cols", "k_pad", "n_tiles", "table_off",
+            "table_words", "scales_off", "tile_off_off", "records_off", "blob_bytes", "max_code_bytes",
+            "prob_bits", "max_words", "max_len"]
+    h = dict(zip(keys, f))
+    return h, dev
+
+
+def read_huffman(blob: bytes, lengths: np.ndarray) -> np.ndarray:
+    """Reconstruct the BF16 matrix from a Huffman blob with a bit-by-bit reader."""
+    h, dev = parse(blob)
+    codes = O.canonical_codes(lengths)
+    table = {(int(lengths[s]), int(codes[s])): s for s in range(256) if lengths[s]}
+    n, k, kp, steps = h["n_rows"], h["k_cols"], h["k_pad"], h["steps"]
+    T = 32 * steps
+    toff = np.frombuffer(dev, np.uint32, h["n_tiles"] + 1, h["tile_off_off"])
+    flat = np.zeros(n * kp, np.uint16)
+    for t in range(h["n_tiles"]):
+        rec = h["records_off"] + int(toff[t]) * 16
+        n_t = min(T, n * kp - t * T)
+        start = np.frombuffer(dev, np.uint16, 32, rec)
+        raw = np.frombuffer(dev, np.uint8, n_t, rec + 64)
+        area_off = rec + 64 + (n_t + 15) // 16 * 16
+        area_end = h["records_off"] + int(toff[t + 1]) * 16
+        words = np.frombuffer(dev, np.uint32, (area_end - area_off) // 4, area_off)
+        bits = "".join(format(int(x), "032b") for x in words)
+        for l in range(32):
+            pos = 8 * int(start[l])
+            for i in range(n_t // 32):
+                L, c = 0, 0
+                while (L, c) not in table:
+                    c = (c << 1) | (bits[pos] == "1")
+                    L += 1
+                    pos += 1
+                    assert L <= 24
+                e = table[(L, c)]
+                q = 32 * i + l
+                r = int(raw[q])
+                flat[t * T + q] = ((r & 0x80) << 8) | (e << 7) | (r & 0x7F)
+    return flat.reshape(n, kp)[:, :k]
+
+
+@pytest.mark.parametrize("shape,steps", [((7, 13), 128), ((3, 300), 32), ((40, 1024), 64), ((2, 4097), 128)])
+def test_huffman_blob_reads_back(ec, shape, steps):
+    w = synth.llama_bf16(2007, *shape)
+    W = ec.encode_bf16(w, tile_steps=steps, device=-1)
+    got = read_huffman(W.serialize(), W.code_lengths())
+    assert np.array_equal(got, w)
+
+
+def test_all_bf16_patterns_blob_reads_back(ec):
+    w = np.arange(65536, dtype=np.uint16).reshape(256, 256)
+    W = ec.encode_bf16(w, device=-1)
+    assert (W.code_lengths() == 8).all()
+    assert np.array_equal(read_huffman(W.serialize(), W.code_lengths()), w)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_code_lengths_match_oracle(ec, seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(2, 60))
+    exps = rng.choice(np.arange(80, 140), n, replace=False)
+    counts = np.floor(2.0 ** rng.uniform(0, 15, n)).astype(np.int64) + 1  # skewed, deep trees
+    e = np.repeat(exps, counts)
+    w = (e.astype(np.uint16) << 7) | (np.arange(e.size) % 128).astype(np.uint16)
+    k = 256
+    rows = (w.size + k - 1) // k
+    pad = rows * k - w.size
+    # pad with an exponent already present so the histogram matches the oracle's
+    w = np.concatenate([w, np.full(pad, int(exps[0]) << 7, np.uint16)]).reshape(rows, k)
+    for L in (24, 12, 9):
+        if 2 ** L < n:
+            continue
+        W = ec.encode_bf16(w, max_code_len=L, device=-1)
+        cnt = np.bincount(((w >> 7) & 0xFF).ravel(), minlength=256)
+        assert np.array_equal(W.code_lengths(), O.code_lengths(cnt, L)), L
+
+
+def test_rans_frequencies_match_oracle(ec):
+    for seed in range(5):
+        codes, scales = synth.make_rans_case(0, 64, 512)
+        codes = np.clip(codes + seed - 2, -8, 7).astype(np.int8)
+        W = ec.encode_rans(codes, scales, device=-1)
+        h, dev = parse(W.serialize())
+        tab = np.frombuffer(dev, np.uint32, h["table_words"], h["table_off"])
+        sym = tab & 15
+        freq_lib = np.bincount(sym, minlength=16)
+        want = O.rans_freqs(np.bincount(codes.ravel().astype(np.int64) + 8, minlength=16))
+        assert np.array_equal(freq_lib, want)
+        assert ((tab >> 16) == want[sym]).all()
+
+
+def corruptions(blob: bytes):
+    h, dev = parse(blob)
+    meta = len(blob) - len(dev)
+    b = bytearray(blob)
+    yield "truncated", bytes(b[:-16])
+    x = bytearray(b); x[meta] ^= 1
+    yield "magic", bytes(x)
+    x = bytearray(b); struct.pack_into("<q", x, meta + 16 + 8 * 3, h["n_tiles"] + 1)
+    yield "n_tiles", bytes(x)
+    toff = meta + h["tile_off_off"]
+    x = bytearray(b); struct.pack_into("<I", x, toff + 4, 0xFFFFFF)
+    yield "tile offset", bytes(x)
+    rec = meta + h["records_off"]
+    if h["kind"] == 1:
+        x = bytearray(b); struct.pack_into("<H", x, rec + 2 * 31, 0xFFFF)
+        yield "lane start", bytes(x)
+        x = bytearray(b); struct.pack_into("<I", x, meta + h["table_off"], 0x80000000 | 0x7FFF)
+        yield "table pointer", bytes(x)
+    else:
+        x = bytearray(b); struct.pack_into("<I", x, meta + h["table_off"], 0)
+        yield "slot entry", bytes(x)
+
+
+@pytest.mark.parametrize("kind", ["huffman", "rans"])
+def test_deserialize_rejects_structural_corruption(ec, kind):
+    if kind == "huffman":
+        W = ec.encode_bf16(synth.llama_bf16(2008, 20, 1000), device=-1)
+    else:
+        W = ec.encode_rans(*synth.make_rans_case(0, 20, 1000), device=-1)
+    blob = W.serialize()
+    W2 = ec.deserialize(blob, device=-1)
+    assert W2.stats() == W.stats()
+    for name, bad in corruptions(blob):
+        with pytest.raises(ec.EcError) as e:
+            ec.deserialize(bad, device=-1)
+        assert e.value.code == -5, name
+
+
+def test_stats_accounting(ec):
+    w = synth.llama_bf16(2001, 1024, 4096)
+    W = ec.encode_bf16(w, device=-1)
+    s = W.stats()
+    n = w.size
+    assert s["k_pad"] == 4096 and s["n_tiles"] == n // 4096
+    cnt = np.bincount(((w >> 7) & 0xFF).ravel(), minlength=256)
+    assert s["entropy_bits"] == pytest.approx(O.entropy(cnt), rel=1e-12)
+    assert s["payload_bits"] == int((cnt * W.code_lengths()).sum())
+    assert s["raw_bytes"] == n
+    assert s["device_bytes"] * 8 / n == pytest.approx(s["bits_per_weight"])
+    # aux (lane starts, byte alignment, 16-byte record padding, offsets) well under 0.25 bit per weight
+    assert s["aux_bytes"] * 8 / n < 0.25
+    assert 10.5 < s["bits_per_weight"] < 11.3

@@ -1,0 +1,175 @@
+"""GPU parity of the Huffman-exponent path against the oracle, through the C ABI.
+
+Decoded weights must be bit-exact with the input (the oracle's DFloat11 decode
+returns the input too, checked alongside); GEMV outputs must match the oracle's
+FP64 GEMV within relative L2 <= 1e-3 and |err| <= 2e-3 * sum|w x| per element."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from parity import check_gemv
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ec():
+    import lossless_entropy_coded_gb300 as ec
+    return ec
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def decode_gpu(ec, W, n, k):
+    out = torch.full((n, k), 0xFFFF, dtype=torch.int16, device="cuda")
+    ec.decode(W, out)
+    assert ec.status() == 0
+    return out.cpu().numpy().view(np.uint16)
+
+
+def gemv_gpu(ec, W, x, n):
+    b = x.shape[0]
+    y = torch.full((b, n), float("nan"), dtype=torch.float32, device="cuda")
+    ec.gemv(W, dev(x.view(np.int16)), y, batch=b)
+    assert ec.status() == 0
+    return y.cpu().numpy()
+
+
+def fib_weights(n_sym=30, rows=None):
+    """A histogram with Fibonacci counts: the unconstrained code is 29 deep, so the
+    24-bit limit binds and sub-table walks are exercised."""
+    fib = [1, 1]
+    while len(fib) < n_sym:
+        fib.append(fib[-1] + fib[-2])
+    e = np.concatenate([np.full(f, 100 + i) for i, f in enumerate(fib)])
+    rng = np.random.default_rng(0)
+    rng.shuffle(e)
+    m = (rng.integers(0, 256, e.size)).astype(np.uint16)
+    w = (e.astype(np.uint16) << 7) | (m & 0x7F) | ((m & 0x80) << 8)
+    k = 4096
+    r = w.size // k
+    return w[: r * k].reshape(r, k)
+
+
+def test_all_65536_patterns_round_trip(ec):
+    w = np.arange(65536, dtype=np.uint16).reshape(256, 256)
+    W = ec.encode_bf16(w)
+    assert np.array_equal(decode_gpu(ec, W, 256, 256), w)
+
+
+@pytest.mark.parametrize("shape", [(1, 1), (7, 13), (1, 4096), (4096, 1), (3, 300), (5, 1000), (33, 2049)])
+@pytest.mark.parametrize("steps", [32, 128])
+def test_round_trip_ragged_shapes(ec, shape, steps):
+    w = synth.llama_bf16(2100 + shape[0], *shape)
+    W = ec.encode_bf16(w, tile_steps=steps)
+    assert np.array_equal(decode_gpu(ec, W, *shape), w)
+
+
+def test_round_trip_config1_and_oracle_agrees(ec):
+    spec = synth.single_1024()
+    w = synth.make_weights(spec)
+    W = ec.encode_bf16(w)
+    got = decode_gpu(ec, W, 1024, 1024)
+    assert np.array_equal(got, w)
+    assert np.array_equal(O.DF11(w).decode(), w.ravel())
+    assert W.stats()["max_code_len"] == int(O.DF11(w).lengths.max())
+
+
+@pytest.mark.parametrize("max_len", [24, 12, 9])
+def test_long_codes_and_length_limit(ec, max_len):
+    w = fib_weights()
+    W = ec.encode_bf16(w, max_code_len=max_len)
+    assert W.code_lengths().max() == min(max_len, 24)
+    assert np.array_equal(decode_gpu(ec, W, *w.shape), w)
+    x = synth.make_x(77, 2, w.shape[1])
+    y_ref, a_ref = O.gemv_bf16(w, x)
+    check_gemv(gemv_gpu(ec, W, x, w.shape[0]), y_ref, a_ref, f"fib L={max_len}")
+
+
+@pytest.mark.parametrize("shape", [(1024, 1024), (256, 4096), (96, 14336), (7, 13), (1, 1), (300, 1000)])
+@pytest.mark.parametrize("batch", [1, 3, 16])
+def test_gemv_parity(ec, shape, batch):
+    w = synth.llama_bf16(2200 + shape[1], *shape)
+    x = synth.make_x(2200, batch, shape[1])
+    W = ec.encode_bf16(w)
+    y_ref, a_ref = O.gemv_bf16(w, x)
+    check_gemv(gemv_gpu(ec, W, x, shape[0]), y_ref, a_ref, f"{shape} b={batch}")
+
+
+def test_gemv_group_matches_individual(ec):
+    shapes = [(512, 1024), (128, 1024), (128, 1024)]
+    ws = [synth.llama_bf16(2300 + i, *s) for i, s in enumerate(shapes)]
+    Ws = [ec.encode_bf16(w) for w in ws]
+    x = synth.make_x(2300, 2, 1024)
+    ys = [torch.full((2, s[0]), float("nan"), dtype=torch.float32, device="cuda") for s in shapes]
+    ec.gemv_group(Ws, dev(x.view(np.int16)), ys, batch=2)
+    assert ec.status() == 0
+    for w, y in zip(ws, ys):
+        y_ref, a_ref = O.gemv_bf16(w, x)
+        check_gemv(y.cpu().numpy(), y_ref, a_ref, "group")
+
+
+def test_decode_batch(ec):
+    shapes = [(256, 1024), (64, 1024), (100, 700), (256, 3584)]
+    ws = [synth.llama_bf16(2400 + i, *s) for i, s in enumerate(shapes)]
+    Ws = [ec.encode_bf16(w) for w in ws]
+    outs = [torch.zeros(s, dtype=torch.int16, device="cuda") for s in shapes]
+    ec.decode_batch(Ws, outs)
+    assert ec.status() == 0
+    for w, o in zip(ws, outs):
+        assert np.array_equal(o.cpu().numpy().view(np.uint16), w)
+
+
+def test_full_size_8b_layer(ec):
+    """All seven Llama-3.1-8B layer matrices at full size: bit-exact decode and the
+    batch-1 GEMV against the oracle's FP64 GEMV (all rows)."""
+    for spec in synth.layer_8b():
+        w = synth.make_weights(spec)
+        W = ec.encode_bf16(w)
+        out = torch.empty((spec.n_rows, spec.k_cols), dtype=torch.int16, device="cuda")
+        ec.decode(W, out)
+        assert ec.status() == 0
+        assert torch.equal(out, torch.from_numpy(w.view(np.int16)).cuda()), spec.name
+        del out
+        x = synth.make_x(spec.seed, 1, spec.k_cols)
+        y_ref, a_ref = O.gemv_bf16(w, x)
+        check_gemv(gemv_gpu(ec, W, x, spec.n_rows), y_ref, a_ref, spec.name)
+        s = W.stats()
+        assert s["aux_bytes"] * 8 / w.size < 0.25
+        W.free()
+
+
+def test_payload_corruption_is_reported_not_faulted(ec):
+    w = synth.llama_bf16(2500, 64, 4096)
+    W = ec.encode_bf16(w)
+    blob = bytearray(W.serialize())
+    from test_abi import parse
+    h, devb = parse(bytes(blob))
+    meta = len(blob) - len(devb)
+    rec = meta + h["records_off"]
+    # flip bits inside the first tile's code area (after 64 B of lane starts + 4096 raw bytes)
+    for off in (64 + 4096 + 3, 64 + 4096 + 200, 64 + 4096 + 900):
+        blob[rec + off] ^= 0x5A
+    Wc = ec.deserialize(bytes(blob), device=0)
+    out = torch.zeros((64, 4096), dtype=torch.int16, device="cuda")
+    ec.decode(Wc, out)
+    st = ec.status()
+    got = out.cpu().numpy().view(np.uint16)
+    assert st == -5 or not np.array_equal(got, w)
+    # the context is still healthy and the clean matrix still decodes exactly
+    assert np.array_equal(decode_gpu(ec, W, 64, 4096), w)
+
+
+def test_empty_and_zero_k(ec):
+    W = ec.encode_bf16(np.zeros((5, 0), np.uint16))
+    y = torch.full((1, 5), 7.0, device="cuda")
+    ec.gemv(W, torch.zeros(8, dtype=torch.int16, device="cuda"), y, batch=1)
+    assert ec.status() == 0
+    assert (y == 0).all()
+    W0 = ec.encode_bf16(np.zeros((0, 64), np.uint16))
+    ec.decode(W0, torch.zeros(8, dtype=torch.int16, device="cuda"))
+    assert ec.status() == 0
