@@ -1,0 +1,503 @@
+"""Benchmark: fused entropy decode + GEMV per token on the Llama-3.1-8B-shaped linear stack.
+
+One step = one token of single-stream decoding through all 224 linear layers of a
+32-layer Llama-3.1-8B-shaped stack (q, k, v, o, gate, up, down per layer), batch 1,
+Huffman-exponent coded weights, four grouped launches per layer (q/k/v, o,
+gate/up, down) captured in one CUDA graph.  Weights are synthetic (seeded,
+Llama-shaped distributions); the compressed stack (~9.4 GB) is far larger than L2,
+so every step streams it from HBM.
+
+Printed: one JSON line (rank 0).  `value` is microseconds per token (lower is
+better); `roofline` is the fused GEMV kernel's achieved compressed-stream GB/s
+against the measured HBM copy peak; `e2e` adds the host<->device copies of the
+step's activations and outputs; `cpu_baseline` is the CPU oracle on a bounded
+sample.  `--impl reference` times the CPU oracle instead (the reference arm).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--no-extras]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused decode+GEMV us/token & compressed-stream HBM GB/s (% of GB300 peak)"
+WORKLOAD = "llama-3.1-8b linear stack, 32 layers x (q,k,v,o,gate,up,down), batch 1, Huffman-exponent BF16"
+KERNEL_SRC = os.path.join(ROOT, "lossless_entropy_coded_gb300", "csrc", "ec_kernels.cu")
+PROFILE = os.path.join(ROOT, "profiles", "huff_gemv_8b_stack.md")
+
+
+# ------------------------------------------------------------------ helpers
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes of the fused GEMV kernel from the committed ncu summary,
+    only if it was taken on the current kernel source."""
+    if not os.path.exists(PROFILE):
+        return None
+    txt = open(PROFILE).read()
+    m = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
+    t = re.search(r"dram_bytes_per_token:\s*([0-9.eE+]+)", txt)
+    if not m or not t or m.group(1) != kernel_hash():
+        return None
+    return float(t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu, self.rows, self.proc = gpu, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in self.rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------------ the stack
+class Stack:
+    """Per-layer compressed matrices, activations and outputs of the 8B stack."""
+
+    GROUPS = [("qkv", ["q", "k", "v"]), ("o", ["o"]), ("gu", ["gate", "up"]), ("down", ["down"])]
+
+    def __init__(self, n_layers: int, keep_bf16: bool, device: int):
+        import torch
+
+        import lossless_entropy_coded_gb300 as ec
+        import synth
+        self.ec, self.torch = ec, torch
+        self.n_layers = n_layers
+        self.mats, self.bf16, self.specs = [], [], []
+        self.x_host, self.y_dev = [], []
+        x_parts, y_sizes = [], []
+        self.compressed_bytes = 0
+        self.weights = 0
+        t0 = time.time()
+        for l in range(n_layers):
+            specs = {s.name.split(".")[1]: s for s in synth.layer_8b(l)}
+            layer, layer_bf16 = {}, {}
+            for nm, s in specs.items():
+                w = synth.make_weights(s)
+                W = ec.encode_bf16(w, device=device)
+                layer[nm] = W
+                self.compressed_bytes += W.stats()["device_bytes"]
+                self.weights += w.size
+                if keep_bf16:
+                    layer_bf16[nm] = torch.from_numpy(w.view(np.int16)).to(f"cuda:{device}")
+                del w
+            self.mats.append(layer)
+            self.bf16.append(layer_bf16)
+            self.specs.append(specs)
+            for g, names in self.GROUPS:
+                k = specs[names[0]].k_cols
+                x_parts.append(synth.make_x(specs[names[0]].seed, 1, k).ravel())
+                y_sizes.extend(specs[n].n_rows for n in names)
+        self.encode_s = time.time() - t0
+        # one contiguous activation buffer and one output buffer (for the e2e copies)
+        xs = np.concatenate(x_parts)
+        self.x_pinned = torch.from_numpy(xs.view(np.int16)).pin_memory()
+        self.x_dev = self.x_pinned.to(f"cuda:{device}")
+        self.y_total = int(sum(y_sizes))
+        self.y_dev_all = torch.zeros(self.y_total, dtype=torch.float32, device=f"cuda:{device}")
+        self.y_pinned = torch.zeros(self.y_total, dtype=torch.float32).pin_memory()
+        # views per launch
+        self.calls = []
+        xo = yo = 0
+        for l in range(n_layers):
+            for g, names in self.GROUPS:
+                k = self.specs[l][names[0]].k_cols
+                xv = self.x_dev[xo:xo + k]
+                xo += k
+                ys = []
+                for n in names:
+                    r = self.specs[l][n].n_rows
+                    ys.append(self.y_dev_all[yo:yo + r])
+                    yo += r
+                self.calls.append(([self.mats[l][n] for n in names], xv, ys, [self.bf16[l].get(n) for n in names]))
+        self.algo_bytes = self.compressed_bytes + 2 * xs.size + 4 * self.y_total
+
+    def run_ec(self, batch_x=None):
+        for Ws, x, ys, _ in self.calls:
+            self.ec.gemv_group(Ws, x, ys, batch=1)
+
+    def run_bf16_own(self):
+        for Ws, x, ys, ws in self.calls:
+            for w, y in zip(ws, ys):
+                self.ec.bf16_gemv(w, x, y, batch=1)
+
+    def run_cublas(self):
+        F = self.torch.nn.functional
+        bf = self.torch.bfloat16
+        for Ws, x, ys, ws in self.calls:
+            xb = x.view(bf).view(1, -1)
+            for w, y in zip(ws, ys):
+                y.copy_(F.linear(xb, w.view(bf)).view(-1))
+
+
+def capture(torch, fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # first call outside capture: one-time attribute setup
+    stream.synchronize()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+        fn()
+    return g
+
+
+def time_graph(torch, g, stream, steps, warmup, pre=None, post=None):
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            if pre:
+                pre()
+            g.replay()
+            if post:
+                post()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            if pre:
+                pre()
+            g.replay()
+            if post:
+                post()
+        e1.record(stream)
+        stream.synchronize()
+    return e0.elapsed_time(e1) / steps * 1e3  # us per step
+
+
+def per_launch_us(torch, stack, stream, reps=3):
+    """Average device duration of each fused GEMV launch: the launches of one token
+    are queued behind a sleep kernel so they run back to back, with an event between
+    every two launches."""
+    n = len(stack.calls)
+    tot = np.zeros(n)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+            torch.cuda._sleep(100_000_000)
+            for i, (Ws, x, ys, _) in enumerate(stack.calls):
+                evs[i].record(stream)
+                stack.ec.gemv_group(Ws, x, ys, batch=1)
+            evs[n].record(stream)
+            stream.synchronize()
+            tot += np.array([evs[i].elapsed_time(evs[i + 1]) * 1e3 for i in range(n)])
+    return tot / reps
+
+
+# ------------------------------------------------------------------ CPU oracle sample
+class OracleSample:
+    """CPU oracle (DFloat11 two-phase decode + FP64 GEMV, single thread) on the first
+    half of the rows of each of the seven layer-0 matrices, scaled to one token
+    (224 matrices).  Encoding is done once, outside the timed part."""
+
+    FRAC = 0.5
+
+    def __init__(self):
+        import oracle as O
+        import synth
+        self.O = O
+        self.items = []
+        self.weights = 0
+        specs = synth.layer_8b(0)
+        for s in specs:
+            rows = max(1, int(s.n_rows * self.FRAC))
+            w = np.ascontiguousarray(synth.make_weights(s)[:rows])
+            x = synth.make_x(s.seed, 1, s.k_cols)
+            self.items.append((O.DF11(w), w.shape, x))
+            self.weights += w.size
+        self.token_weights = sum(s.n_rows * s.k_cols for s in specs) * synth.N_LAYERS_8B
+
+    def run(self):
+        """One timed pass; returns (us_per_token, seconds)."""
+        t0 = time.perf_counter()
+        for d, shape, x in self.items:
+            wd = d.decode().reshape(shape)
+            self.O.gemv_bf16(wd, x)
+        dt = time.perf_counter() - t0
+        return dt / self.weights * self.token_weights * 1e6, dt
+
+    def describe(self, dt):
+        return (f"single-thread oracle: DF11 decode + FP64 GEMV of the first half of the rows of each of the 7 "
+                f"layer-0 matrices ({self.weights} weights, {dt:.1f} s), scaled x{self.token_weights / self.weights:.1f} "
+                f"to the {self.token_weights} weights of one token")
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    t0 = time.time()
+    sample = OracleSample()
+    vals, dts = [], []
+    for _ in range(max(1, min(args.steps, 3))):
+        v, dt = sample.run()
+        vals.append(v)
+        dts.append(dt)
+    value = float(np.median(vals))
+    desc = sample.describe(float(np.median(dts)))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "us/token", "n_gpus": args.gpus,
+            "steps": len(vals), "warmup": 0, "ms_per_step": value / 1e3, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": 1, "matrices": 224},
+            "cpu_baseline": {"value": value, "unit": "us/token", "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "us/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(time.time() - t0, 1)}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ extras
+def extras(torch, ec, stream, device):
+    """Secondary measurements: config 1 latency, rANS shapes, 70B-block decode."""
+    import synth
+    out = {}
+    dev = f"cuda:{device}"
+
+    def t_loop(fn, iters=50, warm=5):
+        with torch.cuda.stream(stream):
+            for _ in range(warm):
+                fn()
+            stream.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(iters):
+                fn()
+            b.record(stream)
+            stream.synchronize()
+        return a.elapsed_time(b) / iters * 1e3
+
+    # config 1: 1024x1024, latency-bound
+    spec = synth.single_1024()
+    w = synth.make_weights(spec)
+    W = ec.encode_bf16(w, device=device)
+    x = torch.from_numpy(synth.make_x(spec.seed, 1, 1024).view(np.int16)).to(dev)
+    y = torch.empty((1, 1024), device=dev)
+    g = capture(torch, lambda: ec.gemv(W, x, y), stream)
+    out["w1024_gemv_us"] = round(t_loop(g.replay, 200), 2)
+    dw = torch.empty((1024, 1024), dtype=torch.int16, device=dev)
+    g2 = capture(torch, lambda: ec.decode(W, dw), stream)
+    out["w1024_decode_us"] = round(t_loop(g2.replay, 200), 2)
+    out["w1024_bpw"] = round(W.stats()["bits_per_weight"], 3)
+
+    # rANS 4-bit tiles, both shapes (rotate 8 copies to stay out of L2)
+    for idx, (n, k) in enumerate(synth.RANS_SHAPES):
+        codes, scales = synth.make_rans_case(idx)
+        blob = ec.encode_rans(codes, scales, device=-1).serialize()
+        Rs = [ec.deserialize(blob, device=device) for _ in range(8)]
+        xr = torch.from_numpy(synth.make_x(4000 + idx, 1, k).view(np.int16)).to(dev)
+        yr = torch.empty((1, n), device=dev)
+        st = Rs[0].stats()
+
+        def rg():
+            for R in Rs:
+                ec.gemv(R, xr, yr)
+        gr = capture(torch, rg, stream)
+        us = t_loop(gr.replay, 20) / len(Rs)
+        out[f"rans_{n}x{k}_gemv_us"] = round(us, 2)
+        out[f"rans_{n}x{k}_bpw"] = round(st["bits_per_weight"], 3)
+        out[f"rans_{n}x{k}_gbs"] = round(st["device_bytes"] / us / 1e3, 1)
+        del Rs
+
+    # 70B-shaped block: one batched decode of all seven matrices to BF16
+    Ws, outs, comp, nw = [], [], 0, 0
+    for s in synth.block_70b():
+        w = synth.make_weights(s)
+        Wm = ec.encode_bf16(w, device=device)
+        Ws.append(Wm)
+        comp += Wm.stats()["device_bytes"]
+        nw += w.size
+        outs.append(torch.empty((s.n_rows, s.k_cols), dtype=torch.int16, device=dev))
+        del w
+    gd = capture(torch, lambda: ec.decode_batch(Ws, outs), stream)
+    us = t_loop(gd.replay, 10, 2)
+    out["block70b_decode_us"] = round(us, 1)
+    out["block70b_decode_in_gbs"] = round(comp / us / 1e3, 1)
+    out["block70b_decode_weights_per_s"] = float(f"{nw / us * 1e6:.4g}")
+    out["block70b_decode_hbm_gbs"] = round((comp + 2 * nw) / us / 1e3, 1)
+    assert ec.status() == 0
+    return out
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    args.warmup_ref = 0
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    import lossless_entropy_coded_gb300 as ec
+
+    t_setup = time.time()
+    stack = Stack(args.layers, keep_bf16=True, device=local)
+    stream = torch.cuda.Stream()
+    g_ec = capture(torch, stack.run_ec, stream)
+    g_bf = capture(torch, stack.run_bf16_own, stream)
+    g_cb = capture(torch, stack.run_cublas, stream)
+    assert ec.status(stream) == 0
+    setup_s = time.time() - t_setup
+
+    # correctness guard on a few outputs of the timed graph (against the BF16 path)
+    g_ec.replay()
+    stream.synchronize()
+    y_ec = stack.y_dev_all.clone()
+    g_bf.replay()
+    stream.synchronize()
+    rel = float(torch.linalg.norm(y_ec - stack.y_dev_all) / torch.linalg.norm(stack.y_dev_all))
+    assert rel < 1e-4, f"fused GEMV disagrees with the BF16 GEMV (rel {rel})"
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        us_ec = time_graph(torch, g_ec, stream, args.steps, args.warmup)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+    clocks = clk.summary()
+    us_bf = time_graph(torch, g_bf, stream, max(20, args.steps // 4), args.warmup)
+    us_cb = time_graph(torch, g_cb, stream, max(20, args.steps // 4), args.warmup)
+    # end to end: pinned host activations in, outputs back to pinned host memory
+    us_e2e = time_graph(torch, g_ec, stream, max(20, args.steps // 4), args.warmup,
+                        pre=lambda: stack.x_dev.copy_(stack.x_pinned, non_blocking=True),
+                        post=lambda: stack.y_pinned.copy_(stack.y_dev_all, non_blocking=True))
+    launches = per_launch_us(torch, stack, stream)
+    assert ec.status(stream) == 0
+
+    t_max = torch.tensor([us_ec], device="cuda")
+    if world > 1:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    us_step = float(t_max.item())
+    value = us_step / world  # replicas: `world` tokens per step
+
+    peak, peak_kind = peaks()
+    per_launch_bytes = stack.algo_bytes / len(stack.calls)
+    achieved = per_launch_bytes / (float(launches.mean()) * 1e-6) / 1e9
+    traffic = profiled_traffic()
+    ex = {}
+    if rank == 0 and not args.no_extras:
+        ex = extras(torch, ec, stream, local)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        sample = OracleSample()
+        v, dt = sample.run()
+        cpu = {"value": round(v, 1), "unit": "us/token", "cores": 1, "kind": "oracle", "sample": sample.describe(dt)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "us/token", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us_step / 1e3, 4),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": 1, "matrices": 224, "weights": stack.weights,
+                       "compressed_bytes": stack.compressed_bytes,
+                       "l2": "inputs larger than L2 (compressed stack >> 129 MB), no flush",
+                       "launches_per_step": len(stack.calls), "cuda_graph": True},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "kernel": "huff_gemv_kernel<1>", "peak_kind": peak_kind,
+                         "bytes_per_launch": round(per_launch_bytes), "launch_us_mean": round(float(launches.mean()), 3)},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(us_e2e / world, 2), "unit": "us/token",
+                    "h2d_bytes_per_step": int(stack.x_pinned.numel() * 2),
+                    "d2h_bytes_per_step": int(stack.y_total * 4)},
+            "gpu_launches": len(stack.calls) * args.steps,
+            "clocks": clocks,
+            "detail": {
+                "bf16_gemv_own_us_per_token": round(us_bf, 2),
+                "bf16_cublas_us_per_token": round(us_cb, 2),
+                "speedup_vs_own_bf16": round(us_bf / us_step, 3),
+                "speedup_vs_cublas": round(us_cb / us_step, 3),
+                "step_compressed_gbs": round(stack.compressed_bytes / us_step / 1e3, 1),
+                "step_frac_of_peak": round(stack.compressed_bytes / us_step / 1e3 / peak, 4),
+                "step_frac_of_8tbs": round(stack.compressed_bytes / us_step / 1e3 / 8000.0, 4),
+                "bits_per_weight": round(8 * stack.compressed_bytes / stack.weights, 3),
+                "effective_weights_per_s": float(f"{stack.weights / us_step * 1e6:.4g}"),
+                "setup_s": round(setup_s, 1), "encode_s": round(stack.encode_s, 1),
+                **ex,
+            },
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

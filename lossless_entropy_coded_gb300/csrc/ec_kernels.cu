@@ -652,11 +652,32 @@ int current_device(int* dev) { return cudaGetDevice(dev) == cudaSuccess ? EC_OK 
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+/* Raise a kernel's dynamic shared-memory limit once per (device, kernel); later
+ * calls that need no more than the recorded value skip the runtime call. */
 template <class K>
 int set_smem(K kernel, size_t bytes) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) == cudaSuccess
-               ? EC_OK
-               : EC_ERR_CUDA;
+    struct Entry {
+        int dev;
+        const void* fn;
+        size_t bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> done;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(mu);
+    for (Entry& e : done)
+        if (e.dev == dev && e.fn == (const void*)kernel) {
+            if (bytes <= e.bytes) return EC_OK;
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+                return EC_ERR_CUDA;
+            e.bytes = bytes;
+            return EC_OK;
+        }
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+        return EC_ERR_CUDA;
+    done.push_back({dev, (const void*)kernel, bytes});
+    return EC_OK;
 }
 
 int launch_result() {
@@ -915,23 +936,31 @@ extern "C" int ec_bf16_gemv(const uint16_t* w, int64_t n_rows, int64_t k_cols, c
     int rc = device_info(dev, &d);
     if (rc != EC_OK) return rc;
     const int64_t kp = (k_cols + 255) / 256 * 256;
-    if ((size_t)4 * batch * kp > d->smem_optin) return EC_ERR_UNSUPPORTED;
-    const size_t smem = (size_t)4 * batch * kp;
+    const int per_pass = rows_per_pass(kp, batch, d->smem_optin);
+    if (per_pass < 1) return EC_ERR_UNSUPPORTED;
     const int64_t groups = (n_rows + kRowsPerWarp - 1) / kRowsPerWarp;
-    const int ctas = std::max(1, std::min(4, (int)(d->smem_optin / (smem + 1024))));
-    const int grid = grid_for(*d, groups, ctas);
-#define EC_BF16_LAUNCH(BB)                                                                              \
-    do {                                                                                                \
-        if (set_smem(bf16_gemv_kernel<BB>, std::max<size_t>(smem, 16)) != EC_OK) return EC_ERR_CUDA;    \
-        bf16_gemv_kernel<BB><<<grid, kWarps * 32, std::max<size_t>(smem, 16), stream>>>(w, n_rows, k_cols, x, y, batch); \
+    for (int b0 = 0; b0 < batch; b0 += per_pass) {
+        const int nb = std::min(per_pass, batch - b0);
+        const size_t smem = std::max<size_t>((size_t)4 * nb * kp, 16);
+        const int ctas = std::max(1, std::min(4, (int)(d->smem_optin / (smem + 1024))));
+        const int grid = grid_for(*d, groups, ctas);
+        const uint16_t* xb = x + (int64_t)b0 * k_cols;
+        float* yb = y + (int64_t)b0 * n_rows;
+#define EC_BF16_LAUNCH(BB)                                                                      \
+    do {                                                                                        \
+        if (set_smem(bf16_gemv_kernel<BB>, smem) != EC_OK) return EC_ERR_CUDA;                  \
+        bf16_gemv_kernel<BB><<<grid, kWarps * 32, smem, stream>>>(w, n_rows, k_cols, xb, yb, nb); \
     } while (0)
-    if (batch <= 1) EC_BF16_LAUNCH(1);
-    else if (batch <= 2) EC_BF16_LAUNCH(2);
-    else if (batch <= 4) EC_BF16_LAUNCH(4);
-    else if (batch <= 8) EC_BF16_LAUNCH(8);
-    else EC_BF16_LAUNCH(16);
+        if (nb <= 1) EC_BF16_LAUNCH(1);
+        else if (nb <= 2) EC_BF16_LAUNCH(2);
+        else if (nb <= 4) EC_BF16_LAUNCH(4);
+        else if (nb <= 8) EC_BF16_LAUNCH(8);
+        else EC_BF16_LAUNCH(16);
 #undef EC_BF16_LAUNCH
-    return launch_result();
+        const int rc = launch_result();
+        if (rc != EC_OK) return rc;
+    }
+    return EC_OK;
 }
 
 extern "C" int ec_status(cudaStream_t stream) {

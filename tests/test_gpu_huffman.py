@@ -25,7 +25,7 @@ def dev(a):
 
 
 def decode_gpu(ec, W, n, k):
-    out = torch.full((n, k), 0xFFFF, dtype=torch.int16, device="cuda")
+    out = torch.full((n, k), -1, dtype=torch.int16, device="cuda")
     ec.decode(W, out)
     assert ec.status() == 0
     return out.cpu().numpy().view(np.uint16)
