@@ -5,8 +5,8 @@
  * One contiguous device blob per matrix:
  *
  *   [ec_blob_header, 256 B]
- *   [decode table]            Huffman: level-1 table of 2^EC_L1_BITS u32 entries,
- *                             then 256-entry sub-tables (8 more bits each).
+ *   [decode table]            Huffman: multi-symbol level-1 table, then the
+ *                             hierarchical table (level 1 + 256-entry sub-tables).
  *                             rANS:    2^prob_bits u32 slot entries.
  *   [group scales]            rANS only: FP16 [n_rows, k_pad / 128].
  *   [tile offsets]            u32 [n_tiles + 1], record start in 16-byte units.
@@ -22,8 +22,11 @@
  * Huffman tile record (DFloat11's EncodedExponent / PackedSignMantissa /
  * per-thread start offsets, re-cut so every lane owns a fixed number of symbols):
  *   u16 lane_start[32]        byte offset of lane l's codewords in the code area
- *   u8  raw[n_t]              (sign << 7) | mantissa, natural position order,
- *                             padded to 16 bytes
+ *   u8  raw[32 * S16]         (sign << 7) | mantissa, lane-transposed in 16-byte
+ *                             chunks: chunk j of lane l (bytes (32 j + l) * 16 ..
+ *                             + 15) holds lane l's symbols 16 j .. 16 j + 15, so a
+ *                             warp reading chunk j reads 512 contiguous bytes;
+ *                             S16 = steps rounded up to 16, the tail zero
  *   u32 code[]                the code area: lane 0's codewords, then lane 1's, ...
  *                             each lane starting on a byte boundary; bit b of the
  *                             area is bit 31 - (b % 32) of word b / 32 (MSB first);
@@ -41,11 +44,32 @@
 #define EC_BLOB_MAGIC 0x31434345u /* "ECC1" */
 #define EC_BLOB_VERSION 1u
 
-#define EC_L1_BITS 12            /* level-1 Huffman window */
+#define EC_L1_BITS 11            /* level-1 Huffman window */
 #define EC_SUB_BITS 8            /* bits per sub-table level */
+#define EC_MULTI_MAX 3           /* exponents decoded by one level-1 lookup */
+#define EC_MULTI_QINC 2          /* stage bytes per decoded exponent field */
+#define EC_MULTI_WORDS (4 << EC_L1_BITS) /* u32 words of the multi-symbol level-1 table */
 #define EC_HUFF_ROW_ALIGN 256    /* k_pad multiple for the Huffman layout */
 #define EC_RANS_ROW_ALIGN 128    /* k_pad multiple for the rANS layout (= scale group) */
 #define EC_MAX_CODE_LEN 24
+
+/* bytes of the raw sign/mantissa section of a tile with `steps` symbols per lane */
+#define EC_RAW_BYTES(steps) (32 * (((steps) + 15) / 16) * 16)
+
+/* Huffman decode tables, in this order inside the table section:
+ *
+ * 1. multi-symbol level-1 table, 2^EC_L1_BITS entries of 4 u32 (16 bytes), indexed
+ *    by the next EC_L1_BITS bits of the stream.  Decodes up to EC_MULTI_MAX whole
+ *    codewords at once:
+ *      word 0 = f0 | (EC_MULTI_QINC * n) << 16, word 1 = f1, word 2 = f2,
+ *      word 3 = total bits
+ *    where f_k = exponent_k << 7 (0 for unused slots) and n >= 1 is the number of
+ *    codewords decoded (EC_MULTI_QINC = bytes per exponent field in the decoder's
+ *    lane-private stage).
+ *    When the first codeword is longer than EC_L1_BITS, word 3 holds the level-1
+ *    entry of table 2 (a pointer, bit 31 set) and words 0..2 are 0.
+ * 2. hierarchical table (u32 entries, below): a 2^EC_L1_BITS level-1 table then
+ *    256-entry sub-tables (DFloat11 appendix, Fig. 4 / Fig. 14). */
 
 /* Huffman table entry (u32):
  *   symbol:  bits 0..15 = exponent << 7 (the BF16 exponent field), bits 16..20 =

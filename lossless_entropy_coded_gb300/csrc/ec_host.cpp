@@ -238,6 +238,38 @@ std::vector<uint32_t> build_huff_table(const uint8_t len[256], const uint32_t co
     return t;
 }
 
+/* Multi-symbol level-1 table: for every EC_L1_BITS-bit window, the codewords that
+ * lie entirely inside it, read greedily from the top, at most EC_MULTI_MAX.  Built
+ * from the hierarchical level-1 table: the window shifted left by the bits already
+ * used, zero-filled, names the next codeword, which counts only if it ends inside
+ * the window. */
+std::vector<uint32_t> build_multi_table(const std::vector<uint32_t>& h) {
+    const uint32_t W = EC_L1_BITS, mask = (1u << W) - 1;
+    std::vector<uint32_t> t(EC_MULTI_WORDS, 0);
+    for (uint32_t v = 0; v <= mask; ++v) {
+        uint32_t* e = &t[4 * v];
+        const uint32_t first = h[v];
+        if (first & (EC_ENT_PTR | EC_ENT_BAD)) {
+            e[3] = (first & EC_ENT_BAD) ? (EC_ENT_PTR | EC_ENT_BAD) : first;
+            continue;
+        }
+        uint32_t used = 0, n = 0, f[EC_MULTI_MAX] = {0, 0, 0};
+        while (n < EC_MULTI_MAX && used < W) {
+            const uint32_t ent = h[(v << used) & mask];
+            if (ent & (EC_ENT_PTR | EC_ENT_BAD)) break;
+            const uint32_t len = (ent >> 16) & 31;
+            if (used + len > W) break;
+            f[n++] = ent & 0xFFFFu;
+            used += len;
+        }
+        e[0] = f[0] | ((EC_MULTI_QINC * n) << 16);
+        e[1] = f[1];
+        e[2] = f[2];
+        e[3] = used;
+    }
+    return t;
+}
+
 /* ------------------------------------------------------------ rANS frequencies */
 
 /* f_s = max(1, floor(M c_s / n)) for present s; while the sum is short add one to
@@ -388,7 +420,11 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
         }
         uint32_t code[256];
         canonical(m->lengths, code);
-        std::vector<uint32_t> table = build_huff_table(m->lengths, code);
+        std::vector<uint32_t> table = build_multi_table(build_huff_table(m->lengths, code));
+        {
+            const std::vector<uint32_t> hier = build_huff_table(m->lengths, code);
+            table.insert(table.end(), hier.begin(), hier.end());
+        }
 
         /* pass 1: per-tile record sizes */
         std::vector<int64_t> rec_bytes(n_tiles + 1, 0), code_bytes(n_tiles, 0);
@@ -402,7 +438,7 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
                 int64_t bytes = 0;
                 for (int l = 0; l < 32; ++l) bytes += (bits[l] + 7) / 8;
                 code_bytes[t] = round_up(bytes + 8, 16);
-                rec_bytes[t] = 64 + round_up(n_t, 16) + code_bytes[t];
+                rec_bytes[t] = 64 + EC_RAW_BYTES(n_t / 32) + code_bytes[t];
             }
         });
         std::vector<uint32_t> tile_off(n_tiles + 1, 0);
@@ -453,8 +489,11 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
                 gather_padded(w, K, KP, base, n_t, v.data());
                 uint16_t* start = (uint16_t*)rec;
                 uint8_t* raw = rec + 64;
-                uint32_t* area = (uint32_t*)(rec + 64 + round_up(n_t, 16));
-                for (int64_t q = 0; q < n_t; ++q) raw[q] = (uint8_t)(((v[q] >> 8) & 0x80) | (v[q] & 0x7F));
+                uint32_t* area = (uint32_t*)(rec + 64 + EC_RAW_BYTES(S));
+                for (int64_t q = 0; q < n_t; ++q) {
+                    const int64_t l = q & 31, i = q >> 5; /* lane l, symbol i */
+                    raw[((i >> 4) * 32 + l) * 16 + (i & 15)] = (uint8_t)(((v[q] >> 8) & 0x80) | (v[q] & 0x7F));
+                }
                 int64_t bitpos = 0;
                 for (int l = 0; l < 32; ++l) {
                     bitpos = round_up(bitpos, 8);
@@ -724,7 +763,9 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
     if (h.table_off != (int64_t)sizeof(ec_blob_header)) return EC_ERR_CORRUPT;
     int64_t end = 0, t4 = 0;
     if (huff) {
-        if (h.table_words < (1 << EC_L1_BITS) || (h.table_words - (1 << EC_L1_BITS)) % 256) return EC_ERR_CORRUPT;
+        if (h.table_words < EC_MULTI_WORDS + (1 << EC_L1_BITS) ||
+            (h.table_words - EC_MULTI_WORDS - (1 << EC_L1_BITS)) % 256)
+            return EC_ERR_CORRUPT;
         if (h.max_len < 0 || h.max_len > EC_MAX_CODE_LEN || h.max_code_bytes < 0) return EC_ERR_CORRUPT;
     } else {
         if (h.prob_bits < 9 || h.prob_bits > 15 || h.table_words != (int64_t(1) << h.prob_bits) || h.max_words < 0)
@@ -748,7 +789,7 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
         const int64_t rb = ((int64_t)off[t + 1] - off[t]) * 16;
         const int64_t n_t = std::min(T, n_pad - t * T);
         if (huff) {
-            const int64_t area = rb - 64 - round_up(n_t, 16);
+            const int64_t area = rb - 64 - EC_RAW_BYTES(n_t / 32);
             if (area < 16 || area > h.max_code_bytes) return EC_ERR_CORRUPT;
             const uint16_t* start = (const uint16_t*)(b + h.records_off + (int64_t)off[t] * 16);
             for (int l = 0; l < 32; ++l)
@@ -759,8 +800,18 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
     }
     const uint32_t* tab = (const uint32_t*)(b + h.table_off);
     if (huff) {
-        const int64_t n_sub = (h.table_words - (1 << EC_L1_BITS)) / 256;
-        for (int64_t i = 0; i < h.table_words; ++i)
+        const int64_t n_sub = (h.table_words - EC_MULTI_WORDS - (1 << EC_L1_BITS)) / 256;
+        for (int64_t i = 0; i < (1 << EC_L1_BITS); ++i) { /* multi-symbol entries */
+            const uint32_t* e = tab + 4 * i;
+            if (e[3] & EC_ENT_PTR) {
+                if (!(e[3] & EC_ENT_BAD) && (int64_t)(e[3] & 0xFFFFu) >= n_sub) return EC_ERR_CORRUPT;
+            } else {
+                const uint32_t n = (e[0] >> 16) / EC_MULTI_QINC;
+                if (n < 1 || n > EC_MULTI_MAX || (e[0] >> 16) % EC_MULTI_QINC || e[3] < n || e[3] > EC_L1_BITS)
+                    return EC_ERR_CORRUPT;
+            }
+        }
+        for (int64_t i = EC_MULTI_WORDS; i < h.table_words; ++i)
             if ((tab[i] & EC_ENT_PTR) && (int64_t)(tab[i] & 0xFFFFu) >= n_sub) return EC_ERR_CORRUPT;
     } else {
         for (int64_t i = 0; i < h.table_words; ++i) {

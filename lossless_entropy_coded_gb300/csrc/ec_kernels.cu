@@ -30,6 +30,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -38,9 +39,7 @@
 
 namespace {
 
-constexpr int kWarps = 8;          /* warps per CTA */
-constexpr int kChunk = 32;         /* steps decoded before each multiply-accumulate pass */
-constexpr int kStage = (kChunk + 4) * 32 * 2; /* per-warp exponent stage (bytes), with slack */
+constexpr int kWarps = 8;          /* warps per CTA (rANS and BF16 kernels) */
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kMaxDecodeBatch = EC_MAX_DECODE_BATCH;
 
@@ -113,75 +112,6 @@ __device__ __forceinline__ int owner(const Args& a, int64_t g) {
     return k;
 }
 
-/* Sub-table walk for codewords longer than the level-1 window. */
-__device__ __noinline__ uint32_t walk_subtables(uint32_t ent, uint32_t win, const uint32_t* __restrict__ table,
-                                                int64_t table_words, int* status) {
-#pragma unroll 1
-    for (int lvl = 0; lvl < 3 && (ent & EC_ENT_PTR); ++lvl) {
-        const int used = (int)((ent >> 16) & 31);
-        const int64_t at = (int64_t(1) << EC_L1_BITS) + (int64_t)(ent & 0xFFFFu) * 256 + ((win << used) >> 24);
-        if (used > 24 || at >= table_words) {
-            ent = EC_ENT_BAD;
-            break;
-        }
-        ent = __ldg(table + at);
-    }
-    if (ent & (EC_ENT_PTR | EC_ENT_BAD)) {
-        flag_corrupt(status);
-        ent = 1u << 16; /* length 1, exponent 0: keeps the lane moving */
-    }
-    return ent;
-}
-
-/* Decode `n` codewords of one lane into stage[i * 32 + lane] (16-bit exponent
- * fields).  (hi, lo) is the 64-bit window, pos the bits already consumed in hi. */
-struct LaneDecoder {
-    uint32_t hi, lo;
-    int pos, widx;
-};
-
-__device__ __forceinline__ void lane_init(LaneDecoder& d, const uint32_t* area, int area_words, int start_byte) {
-    const int w = start_byte >> 2;
-    d.pos = (start_byte & 3) * 8;
-    d.hi = w < area_words ? area[w] : 0u;
-    d.lo = w + 1 < area_words ? area[w + 1] : 0u;
-    d.widx = w + 2;
-}
-
-__device__ __forceinline__ void lane_decode(LaneDecoder& d, int n, const uint32_t* __restrict__ l1, const uint32_t* area,
-                                            int area_words, uint16_t* stage, int lane,
-                                            const uint32_t* __restrict__ table, int64_t table_words, int* status) {
-#pragma unroll 4
-    for (int i = 0; i < n; ++i) {
-        const uint32_t win = __funnelshift_l(d.lo, d.hi, d.pos);
-        uint32_t ent = l1[win >> (32 - EC_L1_BITS)];
-        if (ent & (EC_ENT_PTR | EC_ENT_BAD)) ent = walk_subtables(ent, win, table, table_words, status);
-        stage[i * 32 + lane] = (uint16_t)ent;
-        d.pos += (int)((ent >> 16) & 31);
-        if (d.pos >= 32) {
-            d.hi = d.lo;
-            d.lo = d.widx < area_words ? area[d.widx] : 0u;
-            d.widx++;
-            d.pos -= 32;
-        }
-    }
-}
-
-/* Merge two exponent fields (e0, e1 in the low / high half of e) with raw bytes
- * r0 = byte a, r1 = byte a+1 of r into two BF16 values [w1 | w0]. */
-__device__ __forceinline__ uint32_t merge_pair(uint32_t e, uint32_t r, uint32_t sel) {
-    const uint32_t dup = __byte_perm(r, 0, sel); /* [r1 r1 r0 r0] */
-    return e | (dup & 0x807F807Fu);
-}
-
-/* Eight BF16 weights for 8 consecutive positions: stage fields e8, raw bytes r8. */
-__device__ __forceinline__ void merge8(const uint4& e8, const uint2& r8, uint32_t (&p)[4]) {
-    p[0] = merge_pair(e8.x, r8.x, 0x1100);
-    p[1] = merge_pair(e8.y, r8.x, 0x3322);
-    p[2] = merge_pair(e8.z, r8.y, 0x1100);
-    p[3] = merge_pair(e8.w, r8.y, 0x3322);
-}
-
 /* Start and length (bytes) of tile t's record; a range outside the records region
  * (only possible with a corrupted offset table) yields an empty record. */
 __device__ __forceinline__ int64_t record_span(const uint32_t* __restrict__ tile_off, int64_t t, int64_t records_bytes,
@@ -210,214 +140,419 @@ __device__ __forceinline__ int64_t tile_row(int64_t t, int64_t T, int64_t kp, in
     return (int64_t)(a / b);
 }
 
+/* ============================================================ Huffman path */
+/*
+ * Work layout.  One warp decodes one tile at a time; lane l owns the tile's
+ * symbols i = 0 .. S-1 at positions 32 i + l and, unlike a DFloat11 thread that
+ * hands its output to a block-wide write buffer, lane l also multiplies them:
+ * exponent fields go to a lane-private stage in shared memory (two buffers of
+ * kC fields + spill), the matching raw bytes arrive lane-transposed with one
+ * 16-byte load per 16 symbols, and x is kept transposed in shared memory
+ * (xs_t[l][j] = x[32 j + l]) so lane l finds x for its symbols contiguously.
+ * Decoding chunk c + 1 is interleaved with the multiply-accumulate of chunk c.
+ */
+constexpr int kHW = 24;                        /* max warps per CTA */
+constexpr int kC = 32;                         /* symbols per lane per chunk */
+constexpr int kSpill = 2 * EC_MULTI_MAX - 1;   /* symbols two lookups may write past a chunk */
+constexpr int kLane = 40;                      /* fields per lane per stage buffer (>= kC + kSpill, x8) */
+constexpr int kStageBytes = 2 * 32 * kLane * 2; /* two buffers */
+constexpr int kSlackPairs = 32;                /* zero pairs after the code area (even) */
+constexpr uint32_t kMultiBytes = 16u << EC_L1_BITS;
+static_assert(kLane >= kC + kSpill && kLane % 8 == 0, "stage lane stride");
+static_assert(EC_MULTI_QINC == 2, "stage fields are 16-bit and lane-contiguous");
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts16(uint32_t a, uint32_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"((unsigned short)v) : "memory");
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+/* Codeword longer than the level-1 window (rare): walk the 8-bit sub-tables of the
+ * hierarchical table in global memory; returns a one-symbol multi entry.  Corrupt
+ * data (no codeword matches) yields exponent 0 of length 1 and sets the status. */
+__device__ __forceinline__ uint4 long_codeword(uint32_t w3, uint32_t win, const uint32_t* __restrict__ hier,
+                                               int64_t hier_words, int* status) {
+    uint32_t ent = w3;
+#pragma unroll 1
+    for (int lvl = 0; lvl < 3 && (ent & EC_ENT_PTR) && !(ent & EC_ENT_BAD); ++lvl) {
+        const int used = (int)((ent >> 16) & 31);
+        const int64_t at = (int64_t(1) << EC_L1_BITS) + (int64_t)(ent & 0xFFFFu) * 256 + ((win << used) >> 24);
+        if (used > 24 || at >= hier_words) {
+            ent = EC_ENT_BAD;
+            break;
+        }
+        ent = __ldg(hier + at);
+    }
+    if (ent & (EC_ENT_PTR | EC_ENT_BAD)) {
+        flag_corrupt(status);
+        ent = 1u << 16;
+    }
+    return make_uint4((ent & 0xFFFFu) | ((uint32_t)EC_MULTI_QINC << 16), 0u, 0u, (ent >> 16) & 31);
+}
+
+/* Copy a tile's code area (nw words, global) into shared memory as overlapping
+ * word pairs pairs[k] = (area[k], area[k + 1]), so the 64-bit window at any word is
+ * one aligned 8-byte load, followed by kSlackPairs zero pairs. */
+__device__ __forceinline__ void stage_pairs(uint2* pairs, const uint32_t* __restrict__ area, int nw, int lane) {
+    const uint4* a4 = (const uint4*)area;
+    for (int g = lane; 4 * g < nw; g += 32) {
+        const uint4 a = __ldg(a4 + g);
+        const uint32_t nx = 4 * g + 4 < nw ? __ldg(area + 4 * g + 4) : 0u;
+        uint4* d = (uint4*)(pairs + 4 * g);
+        d[0] = make_uint4(a.x, a.y, a.y, a.z);
+        d[1] = make_uint4(a.z, a.w, a.w, nx);
+    }
+    for (int k = lane; k < kSlackPairs; k += 32) pairs[nw + k] = make_uint2(0u, 0u);
+}
+
+/* One lane's decoder: bit position p in the staged code area and the shared
+ * address q of its next exponent field. */
+struct HuffLane {
+    uint32_t p, q;
+};
+
+/* One multi-symbol lookup: write three exponent fields at q, q+2, q+4 and advance by
+ * the codewords the entry holds (word 0 bits 16.. = 2 * count, word 3 = bits). */
+__device__ __forceinline__ void huff_step(HuffLane& L, uint32_t l1s, uint32_t ps, const uint32_t* __restrict__ hier,
+                                          int64_t hier_words, int* status) {
+    const uint2 wp = lds64(ps + ((L.p >> 5) << 3));
+    const uint32_t win = __funnelshift_l(wp.y, wp.x, L.p);
+    uint4 e = lds128(l1s + ((win >> (32 - EC_L1_BITS)) << 4));
+    if (__builtin_expect((int)e.w < 0, 0)) e = long_codeword(e.w, win, hier, hier_words, status);
+    sts16(L.q, e.x);
+    sts16(L.q + 2, e.y);
+    sts16(L.q + 4, e.z);
+    L.p += e.w;
+    L.q += e.x >> 16;
+}
+
+/* Merge two exponent fields e = [f1 | f0] with raw bytes a, a+1 of r into two BF16
+ * bit patterns [w1 | w0]:  w = (sign << 15) | (exponent << 7) | mantissa. */
+__device__ __forceinline__ uint32_t merge_pair(uint32_t e, uint32_t r, uint32_t sel) {
+    const uint32_t dup = __byte_perm(r, 0, sel); /* [r1 r1 r0 r0] */
+    return e | (dup & 0x807F807Fu);
+}
+
+__device__ __forceinline__ void merge8(const uint4& e8, uint32_t r0, uint32_t r1, uint32_t (&w)[4]) {
+    w[0] = merge_pair(e8.x, r0, 0x1100);
+    w[1] = merge_pair(e8.y, r0, 0x3322);
+    w[2] = merge_pair(e8.z, r1, 0x1100);
+    w[3] = merge_pair(e8.w, r1, 0x3322);
+}
+
+/* acc += w0 * x0 + w1 * x1 for BF16 pairs w = [w1|w0], x = [x1|x0]; the products are
+ * exact and the sums are FP32 (round to nearest). */
+__device__ __forceinline__ float fma2_bf16(uint32_t w, uint32_t x, float acc) {
+    asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+        "mov.b32 {wl, wh}, %1;\n\t"
+        "mov.b32 {xl, xh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
+        "fma.rn.f32.bf16 %0, wh, xh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w), "r"(x));
+    return acc;
+}
+
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+/* Per-warp shared memory: stage (2 x 32 lanes x kLane fields) | code pairs + slack.
+ * Multiples of 16 bytes, so 16-byte loads and stores stay aligned. */
+__host__ __device__ constexpr size_t huff_warp_bytes(int code_bytes) {
+    return (size_t)kStageBytes + 2 * (size_t)((code_bytes + 15) & ~15) + 8 * (size_t)kSlackPairs;
+}
+static_assert(kStageBytes % 16 == 0 && (8 * kSlackPairs) % 16 == 0 && kMultiBytes % 16 == 0, "alignment");
+static_assert(huff_warp_bytes(16) % 16 == 0 && huff_warp_bytes(4112) % 16 == 0, "per-warp block alignment");
+
+/* x for the GEMV, transposed per batch row: xs_t[b][l][j] = x[b][32 j + l], lane
+ * stride kp / 32 + 8 entries (the +8 spreads the lanes of a quarter-warp over
+ * distinct banks for 16-byte loads). */
+__host__ __device__ constexpr uint32_t xs_lane_stride(uint32_t kp) { return kp / 32 + 8; }
+__host__ __device__ constexpr size_t xs_row_bytes(uint32_t kp) { return (size_t)2 * 32 * xs_lane_stride(kp); }
+
+/* Resolve tile t of matrix M.  Returns false for a record whose offsets are
+ * inconsistent (status flagged, tile skipped). */
+struct TileView {
+    const uint8_t* raw;
+    const uint32_t* area;
+    int nw, S;
+    int64_t row;
+    uint32_t col0;
+};
+
+template <class Args>
+__device__ __forceinline__ bool tile_view(const Args& a, const HuffMat& M, int64_t t, int lane, TileView& v) {
+    const int64_t kp = M.k_pad;
+    const int64_t T = 32 * (int64_t)M.steps;
+    const int64_t base = t * T;
+    const int64_t n_t = min(T, M.n_rows * kp - base);
+    int64_t rec_bytes = 0;
+    const uint8_t* rec = M.records + record_span(M.tile_off, t, M.records_bytes, &rec_bytes, a.status, lane);
+    const int S = (int)(n_t / 32);
+    const int raw_bytes = EC_RAW_BYTES(S);
+    int64_t area_bytes = rec_bytes - 64 - raw_bytes;
+    if (area_bytes < 16 || area_bytes > a.code_bytes) {
+        if (lane == 0) flag_corrupt(a.status);
+        return false;
+    }
+    v.raw = rec + 64;
+    v.area = (const uint32_t*)(rec + 64 + raw_bytes);
+    v.nw = (int)(area_bytes / 4);
+    v.S = S;
+    v.row = tile_row(t, T, kp, EC_HUFF_ROW_ALIGN);
+    v.col0 = (uint32_t)(base - v.row * kp);
+    return true;
+}
+
+/* Lane start in bits, clamped to the code area (a corrupt start cannot move the
+ * window reads past the zero slack). */
+__device__ __forceinline__ uint32_t lane_start_bits(const TileView& v, int lane) {
+    const uint32_t s = __ldg((const uint16_t*)(v.raw - 64) + lane);
+    return 8u * min(s, (uint32_t)(4 * v.nw));
+}
+
+/* Raw bytes of lane `lane`, symbols 16 j .. 16 j + 15 (one coalesced 16-byte load). */
+__device__ __forceinline__ uint4 raw16(const TileView& v, int j, int lane) {
+    return __ldg((const uint4*)v.raw + (32 * j + lane));
+}
+
+/* Decode the lane's next chunk (target symbols) into stage buffer Y, interleaving
+ * up to four multiply-accumulate sub-steps `fma(k)` of the previous chunk. */
+template <class Fma>
+__device__ __forceinline__ void huff_chunk(HuffLane& L, uint32_t q_end, int subs, uint32_t l1s, uint32_t ps,
+                                           const uint32_t* __restrict__ hier, int64_t hier_words, int* status,
+                                           Fma&& fma) {
+#pragma unroll
+    for (int k = 0; k < kC / 8; ++k) {
+        if (L.q < q_end) {
+            huff_step(L, l1s, ps, hier, hier_words, status);
+            huff_step(L, l1s, ps, hier, hier_words, status);
+        }
+        if (k < subs) fma(k);
+    }
+#pragma unroll 1
+    while (L.q < q_end) {
+        huff_step(L, l1s, ps, hier, hier_words, status);
+        huff_step(L, l1s, ps, hier, hier_words, status);
+    }
+}
+
+/* Walk one tile: prologue decodes chunk 0; iteration c moves chunk c's spill to the
+ * other buffer, decodes chunk c + 1 there while `consume(c, k, fields)` handles
+ * sub-step k (8 symbols) of chunk c. */
+template <class Consume>
+__device__ __forceinline__ void huff_tile(const TileView& v, uint32_t l1s, uint32_t ps, uint32_t stage_lane,
+                                          const uint32_t* __restrict__ hier, int64_t hier_words, int* status,
+                                          int lane, Consume&& consume) {
+    const uint32_t bufb = 32 * kLane * 2; /* byte distance between the two buffers */
+    const uint32_t pmax = 32u * v.nw;
+    HuffLane L{lane_start_bits(v, lane), stage_lane};
+    const int nch = (v.S + kC - 1) / kC;
+    /* chunk 0 into buffer 0 */
+    huff_chunk(L, stage_lane + 2u * min(kC, v.S), 0, l1s, ps, hier, hier_words, status, [](int) {});
+    for (int c = 0; c < nch; ++c) {
+        const uint32_t X = stage_lane + (c & 1) * bufb, Y = stage_lane + ((c + 1) & 1) * bufb;
+        const int rows_c = min(kC, v.S - c * kC);
+        /* spill of chunk c (fields kC .. kC + 7 of X) becomes the start of buffer Y */
+        sts128(Y, lds128(X + 2 * kC));
+        L.q = L.q - X - 2 * kC + Y;
+        L.p = min(L.p, pmax);
+        const int next = min(kC, v.S - (c + 1) * kC); /* symbols of chunk c + 1 (<= 0: none) */
+        const uint32_t q_end = next > 0 ? Y + 2u * next : 0u;
+        huff_chunk(L, q_end, rows_c / 8, l1s, ps, hier, hier_words, status,
+                   [&](int k) { consume(c, k, lds128(X + 16 * k)); });
+    }
+}
+
 /* ======================================================== Huffman GEMV kernel */
 template <int B>
-__global__ void __launch_bounds__(kWarps * 32) huff_gemv_kernel(const __grid_constant__ HuffGemvArgs a) {
+__global__ void __launch_bounds__(kHW * 32, 1) huff_gemv_kernel(const __grid_constant__ HuffGemvArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t kp = a.m[0].k_pad;
-    const int batch = a.batch;
-
-    /* shared: level-1 tables | x (fp32, [batch, k_pad]) | per warp: code buffer + stage */
-    uint32_t* l1s = (uint32_t*)smem;
-    float* xs = (float*)(smem + (size_t)a.count * (4u << EC_L1_BITS));
-    uint8_t* wbase = (uint8_t*)(xs + (size_t)batch * kp) + (size_t)warp * (a.code_bytes + kStage);
-    uint32_t* code = (uint32_t*)wbase;
-    uint16_t* stage = (uint16_t*)(wbase + a.code_bytes);
-
-    for (int k = 0; k < a.count; ++k)
-        for (int i = threadIdx.x; i < (1 << EC_L1_BITS); i += blockDim.x) l1s[(k << EC_L1_BITS) + i] = __ldg(a.m[k].table + i);
+    const uint32_t kp = (uint32_t)a.m[0].k_pad;
     const int64_t K = a.m[0].k_cols;
+    const int batch = a.batch;
+    const uint32_t lx = xs_lane_stride(kp);
+
+    /* shared: multi-symbol level-1 tables | x transposed [batch][32][lx] | per warp: stage, pairs */
+    uint4* l1g = (uint4*)smem;
+    uint16_t* xs = (uint16_t*)(smem + (size_t)a.count * kMultiBytes);
+    uint8_t* wbase = (uint8_t*)xs + (size_t)batch * xs_row_bytes(kp) + (size_t)warp * huff_warp_bytes(a.code_bytes);
+    const uint32_t stage_lane = smem_u32(wbase) + lane * (kLane * 2);
+    uint2* pairs = (uint2*)(wbase + kStageBytes);
+    const uint32_t pairs_s = smem_u32(pairs);
+    const uint32_t xs_lane = smem_u32(xs) + lane * lx * 2;
+
+    for (int k = 0; k < a.count; ++k) {
+        const uint4* src = (const uint4*)a.m[k].table;
+        for (int i = threadIdx.x; i < (1 << EC_L1_BITS); i += blockDim.x) l1g[(k << EC_L1_BITS) + i] = __ldg(src + i);
+    }
+    grid_dep_launch();
+    grid_dep_wait(); /* x and y belong to the preceding kernel in the stream from here on */
     for (int b = 0; b < batch; ++b)
-        for (int64_t c = threadIdx.x; c < kp; c += blockDim.x) {
-            float v = 0.f;
-            if (c < K) v = __uint_as_float((uint32_t)a.x[(int64_t)b * K + c] << 16);
-            xs[(int64_t)b * kp + c] = v;
-        }
+        for (uint32_t c = threadIdx.x; c < kp; c += blockDim.x)
+            xs[(size_t)b * 32 * lx + (c & 31) * lx + (c >> 5)] = c < K ? a.x[(int64_t)b * K + c] : (uint16_t)0;
     __syncthreads();
 
-    const int64_t gw = (int64_t)blockIdx.x * kWarps + warp, nw = (int64_t)gridDim.x * kWarps;
+    const int nwarp = blockDim.x >> 5;
+    const int64_t gw = (int64_t)blockIdx.x * nwarp + warp, nw = (int64_t)gridDim.x * nwarp;
     for (int64_t g = gw; g < a.total_tiles; g += nw) {
         const int mi = owner(a, g);
         const HuffMat& M = a.m[mi];
-        const int64_t t = g - M.tile_begin;
-        const int64_t T = 32 * (int64_t)M.steps;
-        const int64_t base = t * T;
-        const int64_t n_t = min(T, M.n_rows * kp - base);
-        const int S = (int)(n_t / 32);
-        int64_t rec_bytes = 0;
-        const uint8_t* rec = M.records + record_span(M.tile_off, t, M.records_bytes, &rec_bytes, a.status, lane);
-        const int raw_bytes = (int)((n_t + 15) & ~15);
-        if (rec_bytes < 64 + raw_bytes) { /* corrupt offsets: skip the tile */
-            if (lane == 0) flag_corrupt(a.status);
-            continue;
-        }
-        int area_bytes = (int)(rec_bytes - 64 - raw_bytes);
-        if (area_bytes < 0 || area_bytes > a.code_bytes) {
-            if (lane == 0) flag_corrupt(a.status);
-            area_bytes = max(0, min(area_bytes, a.code_bytes));
-        }
-        const int area_words = area_bytes / 4;
-        const uint16_t start = __ldg((const uint16_t*)rec + lane);
-        const uint8_t* raw = rec + 64;
-        warp_copy16(code, rec + 64 + raw_bytes, area_bytes, lane);
+        TileView v;
+        if (!tile_view(a, M, g - M.tile_begin, lane, v)) continue;
         __syncwarp();
-        const uint32_t* l1 = l1s + (mi << EC_L1_BITS);
-
-        LaneDecoder dec;
-        lane_init(dec, code, area_words, start);
-        int64_t row = tile_row(t, T, kp, EC_HUFF_ROW_ALIGN);
-        int64_t col0 = base - row * kp;
-        float acc[B];
+        stage_pairs(pairs, v.area, v.nw, lane);
+        __syncwarp();
+        const uint32_t l1s = smem_u32(l1g + (mi << EC_L1_BITS));
+        int64_t row = v.row;
+        uint32_t jc = v.col0 / 32; /* x column block of the current sub-step */
+        const uint32_t jrow = kp / 32;
+        float acc[B][2];
 #pragma unroll
-        for (int b = 0; b < B; ++b) acc[b] = 0.f;
+        for (int b = 0; b < B; ++b) acc[b][0] = acc[b][1] = 0.f;
+        uint4 rw[2] = {raw16(v, 0, lane), v.S > 16 ? raw16(v, 1, lane) : make_uint4(0, 0, 0, 0)};
+        uint4 rn[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
 
         auto flush = [&](int64_t r) {
 #pragma unroll
             for (int b = 0; b < B; ++b) {
                 if (b >= batch) break;
-                const float v = warp_sum(acc[b]);
+                const float s = warp_sum(acc[b][0] + acc[b][1]);
                 if (lane == 0) {
                     float* dst = M.y + (int64_t)b * M.n_rows + r;
-                    if (M.atomic_y) atomicAdd(dst, v);
-                    else *dst = v;
+                    if (M.atomic_y) atomicAdd(dst, s);
+                    else *dst = s;
                 }
-                acc[b] = 0.f;
+                acc[b][0] = acc[b][1] = 0.f;
             }
         };
 
-        for (int c0 = 0; c0 < S; c0 += kChunk) {
-            const int n = min(kChunk, S - c0);
-            const int subs = n / 8;
-            uint2 r8[kChunk / 8];
+        huff_tile(v, l1s, pairs_s, stage_lane, M.table + EC_MULTI_WORDS, M.table_words - EC_MULTI_WORDS, a.status,
+                  lane, [&](int c, int k, const uint4& e8) {
+                      if (k == 0) { /* prefetch the next chunk's raw bytes */
+                          const int j = 2 * (c + 1);
+                          rn[0] = 16 * j < v.S ? raw16(v, j, lane) : make_uint4(0, 0, 0, 0);
+                          rn[1] = 16 * (j + 1) < v.S ? raw16(v, j + 1, lane) : make_uint4(0, 0, 0, 0);
+                      }
+                      if (jc >= jrow) {
+                          flush(row);
+                          jc -= jrow;
+                          ++row;
+                      }
+                      const uint4& r = rw[k >> 1];
+                      uint32_t w[4];
+                      merge8(e8, (k & 1) ? r.z : r.x, (k & 1) ? r.w : r.y, w);
+                      const uint32_t xa = xs_lane + 2 * jc;
 #pragma unroll
-            for (int k = 0; k < kChunk / 8; ++k)
-                if (k < subs) r8[k] = __ldg((const uint2*)(raw + (int64_t)c0 * 32 + k * 256) + lane);
-            lane_decode(dec, n, l1, code, area_words, stage, lane, M.table, M.table_words, a.status);
-            __syncwarp();
-#pragma unroll
-            for (int k = 0; k < kChunk / 8; ++k) {
-                if (k >= subs) break;
-                if (col0 >= kp) {
-                    flush(row);
-                    col0 -= kp;
-                    ++row;
-                }
-                const uint4 e8 = *(const uint4*)(stage + k * 256 + 8 * lane);
-                uint32_t p[4];
-                merge8(e8, r8[k], p);
-                float w[8];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    w[2 * j] = __uint_as_float(p[j] << 16);
-                    w[2 * j + 1] = __uint_as_float(p[j] & 0xFFFF0000u);
-                }
-                const int64_t col = col0 + 8 * lane;
-#pragma unroll
-                for (int b = 0; b < B; ++b) {
-                    if (b >= batch) break;
-                    const float4 xa = *(const float4*)(xs + (int64_t)b * kp + col);
-                    const float4 xb = *(const float4*)(xs + (int64_t)b * kp + col + 4);
-                    float s = acc[b];
-                    s = fmaf(w[0], xa.x, s);
-                    s = fmaf(w[1], xa.y, s);
-                    s = fmaf(w[2], xa.z, s);
-                    s = fmaf(w[3], xa.w, s);
-                    s = fmaf(w[4], xb.x, s);
-                    s = fmaf(w[5], xb.y, s);
-                    s = fmaf(w[6], xb.z, s);
-                    s = fmaf(w[7], xb.w, s);
-                    acc[b] = s;
-                }
-                col0 += 256;
-            }
-            __syncwarp();
-        }
+                      for (int b = 0; b < B; ++b) {
+                          if (b >= batch) break;
+                          const uint4 xv = lds128(xa + (uint32_t)(b * xs_row_bytes(kp)));
+                          acc[b][0] = fma2_bf16(w[0], xv.x, acc[b][0]);
+                          acc[b][1] = fma2_bf16(w[1], xv.y, acc[b][1]);
+                          acc[b][0] = fma2_bf16(w[2], xv.z, acc[b][0]);
+                          acc[b][1] = fma2_bf16(w[3], xv.w, acc[b][1]);
+                      }
+                      jc += 8;
+                      if (k == kC / 8 - 1) {
+                          rw[0] = rn[0];
+                          rw[1] = rn[1];
+                      }
+                  });
         flush(row);
     }
 }
 
 /* ====================================================== Huffman decode kernel */
-__global__ void __launch_bounds__(kWarps * 32) huff_decode_kernel(const __grid_constant__ HuffDecodeArgs a) {
+/* Each CTA owns a contiguous range of the launch's tiles; it walks the range one
+ * matrix segment at a time, with that matrix's level-1 table in shared memory.
+ * Lanes merge their own symbols, then the warp transposes 256 outputs through a
+ * small shared buffer so the stores to out are coalesced 16-byte writes. */
+__host__ __device__ constexpr size_t decode_warp_bytes(int code_bytes) { return huff_warp_bytes(code_bytes) + 512; }
+
+__global__ void __launch_bounds__(kHW * 32, 1) huff_decode_kernel(const __grid_constant__ HuffDecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint8_t* wbase = smem + (size_t)warp * (a.code_bytes + kStage + (4u << EC_L1_BITS));
-    uint32_t* l1w = (uint32_t*)wbase; /* per-warp copy: matrices differ between warps */
-    uint32_t* code = (uint32_t*)(wbase + (4u << EC_L1_BITS));
-    uint16_t* stage = (uint16_t*)(wbase + (4u << EC_L1_BITS) + a.code_bytes);
-    int loaded = -1;
+    uint4* l1 = (uint4*)smem;
+    uint8_t* wbase = smem + kMultiBytes + (size_t)warp * decode_warp_bytes(a.code_bytes);
+    const uint32_t stage_lane = smem_u32(wbase) + lane * (kLane * 2);
+    uint2* pairs = (uint2*)(wbase + kStageBytes);
+    const uint32_t pairs_s = smem_u32(pairs), l1s = smem_u32(l1);
+    const uint32_t tbuf = smem_u32(wbase + huff_warp_bytes(a.code_bytes)); /* 256 outputs */
+    grid_dep_launch();
+    grid_dep_wait();
 
-    const int64_t gw = (int64_t)blockIdx.x * kWarps + warp, nw = (int64_t)gridDim.x * kWarps;
-    for (int64_t g = gw; g < a.total_tiles; g += nw) {
-        const int mi = owner(a, g);
+    const int64_t lo = a.total_tiles * blockIdx.x / gridDim.x, hi = a.total_tiles * (blockIdx.x + 1) / gridDim.x;
+    for (int64_t cur = lo; cur < hi;) {
+        const int mi = owner(a, cur);
         const HuffMat& M = a.m[mi];
-        if (mi != loaded) {
-            __syncwarp();
-            for (int i = lane; i < (1 << EC_L1_BITS); i += 32) l1w[i] = __ldg(M.table + i);
-            loaded = mi;
-            __syncwarp();
-        }
+        const int64_t mend = min(hi, M.tile_begin + M.n_tiles);
+        __syncthreads();
+        const uint4* src = (const uint4*)M.table;
+        for (int i = threadIdx.x; i < (1 << EC_L1_BITS); i += blockDim.x) l1[i] = __ldg(src + i);
+        __syncthreads();
         const int64_t kp = M.k_pad, K = M.k_cols;
-        const int64_t t = g - M.tile_begin;
-        const int64_t T = 32 * (int64_t)M.steps;
-        const int64_t base = t * T;
-        const int64_t n_t = min(T, M.n_rows * kp - base);
-        const int S = (int)(n_t / 32);
-        int64_t rec_bytes = 0;
-        const uint8_t* rec = M.records + record_span(M.tile_off, t, M.records_bytes, &rec_bytes, a.status, lane);
-        const int raw_bytes = (int)((n_t + 15) & ~15);
-        if (rec_bytes < 64 + raw_bytes) { /* corrupt offsets: skip the tile */
-            if (lane == 0) flag_corrupt(a.status);
-            continue;
-        }
-        int area_bytes = (int)(rec_bytes - 64 - raw_bytes);
-        if (area_bytes < 0 || area_bytes > a.code_bytes) {
-            if (lane == 0) flag_corrupt(a.status);
-            area_bytes = max(0, min(area_bytes, a.code_bytes));
-        }
-        const int area_words = area_bytes / 4;
-        const uint16_t start = __ldg((const uint16_t*)rec + lane);
-        const uint8_t* raw = rec + 64;
-        warp_copy16(code, rec + 64 + raw_bytes, area_bytes, lane);
-        __syncwarp();
-
-        LaneDecoder dec;
-        lane_init(dec, code, area_words, start);
-        int64_t row = tile_row(t, T, kp, EC_HUFF_ROW_ALIGN);
-        int64_t col0 = base - row * kp;
         const bool vec = (K % 8) == 0;
-        for (int c0 = 0; c0 < S; c0 += kChunk) {
-            const int n = min(kChunk, S - c0);
-            const int subs = n / 8;
-            uint2 r8[kChunk / 8];
-#pragma unroll
-            for (int k = 0; k < kChunk / 8; ++k)
-                if (k < subs) r8[k] = __ldg((const uint2*)(raw + (int64_t)c0 * 32 + k * 256) + lane);
-            lane_decode(dec, n, l1w, code, area_words, stage, lane, M.table, M.table_words, a.status);
+        for (int64_t g = cur + warp; g < mend; g += (blockDim.x >> 5)) {
+            TileView v;
+            if (!tile_view(a, M, g - M.tile_begin, lane, v)) continue;
             __syncwarp();
-#pragma unroll
-            for (int k = 0; k < kChunk / 8; ++k) {
-                if (k >= subs) break;
-                if (col0 >= kp) {
-                    col0 -= kp;
-                    ++row;
-                }
-                const uint4 e8 = *(const uint4*)(stage + k * 256 + 8 * lane);
-                uint32_t p[4];
-                merge8(e8, r8[k], p);
-                const int64_t col = col0 + 8 * lane;
-                uint16_t* dst = M.out + row * K + col;
-                if (vec) {
-                    if (col < K) *(uint4*)dst = make_uint4(p[0], p[1], p[2], p[3]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        if (col + j < K) dst[j] = (uint16_t)(p[j >> 1] >> (16 * (j & 1)));
-                }
-                col0 += 256;
-            }
+            stage_pairs(pairs, v.area, v.nw, lane);
             __syncwarp();
+            int64_t row = v.row;
+            int64_t col0 = v.col0;
+            uint4 rw[2] = {raw16(v, 0, lane), v.S > 16 ? raw16(v, 1, lane) : make_uint4(0, 0, 0, 0)};
+            uint4 rn[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+            huff_tile(v, l1s, pairs_s, stage_lane, M.table + EC_MULTI_WORDS, M.table_words - EC_MULTI_WORDS,
+                      a.status, lane, [&](int c, int k, const uint4& e8) {
+                          if (k == 0) {
+                              const int j = 2 * (c + 1);
+                              rn[0] = 16 * j < v.S ? raw16(v, j, lane) : make_uint4(0, 0, 0, 0);
+                              rn[1] = 16 * (j + 1) < v.S ? raw16(v, j + 1, lane) : make_uint4(0, 0, 0, 0);
+                          }
+                          if (col0 >= kp) {
+                              col0 -= kp;
+                              ++row;
+                          }
+                          const uint4& r = rw[k >> 1];
+                          uint32_t w[4];
+                          merge8(e8, (k & 1) ? r.z : r.x, (k & 1) ? r.w : r.y, w);
+                          /* lane's 8 outputs are positions 32 i + lane, i = 8k'..8k'+7: transpose */
+                          __syncwarp();
+#pragma unroll
+                          for (int j = 0; j < 8; ++j) sts16(tbuf + 64 * j + 2 * lane, w[j >> 1] >> (16 * (j & 1)));
+                          __syncwarp();
+                          const uint4 o = lds128(tbuf + 16 * lane);
+                          const int64_t col = col0 + 8 * lane;
+                          uint16_t* dst = M.out + row * K + col;
+                          if (vec) {
+                              if (col < K) *(uint4*)dst = o;
+                          } else {
+                              const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                              for (int j = 0; j < 8; ++j)
+                                  if (col + j < K) dst[j] = (uint16_t)(ow[j >> 1] >> (16 * (j & 1)));
+                          }
+                          col0 += 256;
+                          if (k == kC / 8 - 1) {
+                              rw[0] = rn[0];
+                              rw[1] = rn[1];
+                          }
+                      });
         }
+        cur = mend;
     }
 }
 
@@ -685,6 +820,33 @@ int launch_result() {
     return e == cudaSuccess ? EC_OK : EC_ERR_CUDA;
 }
 
+/* Programmatic dependent launch: a kernel may start its prologue (tables into
+ * shared memory) while the previous kernel in the stream drains; it waits for
+ * that kernel (griddepcontrol.wait) before it reads x or writes outputs.
+ * EC_NO_PDL=1 in the environment turns it off. */
+bool use_pdl() {
+    static const bool on = [] {
+        const char* e = std::getenv("EC_NO_PDL");
+        return !(e && e[0] == '1');
+    }();
+    return on;
+}
+
+template <class... KArgs, class... Args>
+int launch_ex(void (*kernel)(KArgs...), int grid, int block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = use_pdl() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? EC_OK : EC_ERR_CUDA;
+}
+
 HuffMat huff_desc(const ec_matrix* W) {
     HuffMat m{};
     const ec_blob_header& h = W->hdr;
@@ -737,18 +899,17 @@ int grid_for(const DeviceInfo& d, int64_t work_items, int ctas_per_sm) {
 }
 
 template <int B>
-int launch_huff_gemv_b(const HuffGemvArgs& a, size_t smem, int grid, cudaStream_t s) {
+int launch_huff_gemv_b(const HuffGemvArgs& a, size_t smem, int grid, int block, cudaStream_t s) {
     if (set_smem(huff_gemv_kernel<B>, smem) != EC_OK) return EC_ERR_CUDA;
-    huff_gemv_kernel<B><<<grid, kWarps * 32, smem, s>>>(a);
-    return launch_result();
+    return launch_ex(huff_gemv_kernel<B>, grid, block, smem, s, a);
 }
 
-int launch_huff_gemv(const HuffGemvArgs& a, size_t smem, int grid, cudaStream_t s) {
-    if (a.batch <= 1) return launch_huff_gemv_b<1>(a, smem, grid, s);
-    if (a.batch <= 2) return launch_huff_gemv_b<2>(a, smem, grid, s);
-    if (a.batch <= 4) return launch_huff_gemv_b<4>(a, smem, grid, s);
-    if (a.batch <= 8) return launch_huff_gemv_b<8>(a, smem, grid, s);
-    return launch_huff_gemv_b<16>(a, smem, grid, s);
+int launch_huff_gemv(const HuffGemvArgs& a, size_t smem, int grid, int block, cudaStream_t s) {
+    if (a.batch <= 1) return launch_huff_gemv_b<1>(a, smem, grid, block, s);
+    if (a.batch <= 2) return launch_huff_gemv_b<2>(a, smem, grid, block, s);
+    if (a.batch <= 4) return launch_huff_gemv_b<4>(a, smem, grid, block, s);
+    if (a.batch <= 8) return launch_huff_gemv_b<8>(a, smem, grid, block, s);
+    return launch_huff_gemv_b<16>(a, smem, grid, block, s);
 }
 
 template <bool G, int B>
@@ -767,10 +928,10 @@ int launch_rans(bool gemv, const RansArgs& a, size_t smem, int grid, cudaStream_
     return launch_rans_b<true, 16>(a, smem, grid, s);
 }
 
-/* Batch rows whose FP32 copy of x fits in `budget` bytes of shared memory. */
-int rows_per_pass(int64_t k_pad, int batch, size_t budget) {
+/* Batch rows whose copy of x (elem bytes per value) fits in `budget` bytes of shared memory. */
+int rows_per_pass(int64_t k_pad, int batch, size_t budget, int elem = 4) {
     if (k_pad == 0) return batch;
-    const int64_t per = 4 * k_pad;
+    const int64_t per = elem * k_pad;
     return (int)std::max<int64_t>(0, std::min<int64_t>(batch, (int64_t)budget / per));
 }
 
@@ -798,19 +959,22 @@ int huff_gemv(const ec_matrix* const* Ws, int count, const uint16_t* x, float* c
     a.status = d->status;
     a.code_bytes = code_bytes;
     if (total == 0) return EC_OK;
-    const size_t fixed = (size_t)count * (4u << EC_L1_BITS) + (size_t)kWarps * (code_bytes + kStage);
-    if (fixed > d->smem_optin) return EC_ERR_UNSUPPORTED;
-    int per_pass = rows_per_pass(kp, batch, d->smem_optin - fixed);
+    /* warps per CTA: as many as fit next to the tables and one batch row of x (>= 4) */
+    const size_t tables = (size_t)count * kMultiBytes, per_warp = huff_warp_bytes(code_bytes);
+    const size_t xrow = xs_row_bytes((uint32_t)kp);
+    if (tables + xrow + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED;
+    const int warps = (int)std::min<size_t>(kHW, (d->smem_optin - tables - xrow) / per_warp);
+    const size_t fixed = tables + (size_t)warps * per_warp;
+    const int per_pass = (int)std::min<size_t>(batch, (d->smem_optin - fixed) / xrow);
     if (per_pass < 1) return EC_ERR_UNSUPPORTED;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(d->sms, (total + warps - 1) / warps));
     for (int b0 = 0; b0 < batch; b0 += per_pass) {
         const int nb = std::min(per_pass, batch - b0);
         a.batch = nb;
         a.x = x + (int64_t)b0 * K;
         for (int k = 0; k < count; ++k) a.m[k].y = ys[k] + (int64_t)b0 * Ws[k]->hdr.n_rows;
-        const size_t smem = fixed + (size_t)4 * nb * kp;
-        const int ctas = std::max(1, (int)(d->smem_optin / (smem + 1024)));
-        const int grid = grid_for(*d, total, std::min(ctas, 2));
-        const int rc = launch_huff_gemv(a, smem, grid, s);
+        const size_t smem = fixed + xrow * nb;
+        const int rc = launch_huff_gemv(a, smem, grid, warps * 32, s);
         if (rc != EC_OK) return rc;
     }
     return EC_OK;
@@ -911,12 +1075,13 @@ extern "C" int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs
     a.total_tiles = total;
     a.status = d->status;
     a.code_bytes = code_bytes;
-    const size_t smem = (size_t)kWarps * (code_bytes + kStage + (4u << EC_L1_BITS));
-    if (smem > d->smem_optin) return EC_ERR_UNSUPPORTED;
+    const size_t per_warp = decode_warp_bytes(code_bytes);
+    if (kMultiBytes + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED;
+    const int warps = (int)std::min<size_t>(kHW, (d->smem_optin - kMultiBytes) / per_warp);
+    const size_t smem = kMultiBytes + (size_t)warps * per_warp;
     if (set_smem(huff_decode_kernel, smem) != EC_OK) return EC_ERR_CUDA;
-    const int ctas = std::max(1, std::min(2, (int)(d->smem_optin / (smem + 1024))));
-    huff_decode_kernel<<<grid_for(*d, total, ctas), kWarps * 32, smem, stream>>>(a);
-    return launch_result();
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(d->sms, (total + warps - 1) / warps));
+    return launch_ex(huff_decode_kernel, grid, warps * 32, smem, stream, a);
 }
 
 extern "C" int ec_decode(const ec_matrix* W, uint16_t* out, cudaStream_t stream) {

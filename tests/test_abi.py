@@ -110,8 +110,12 @@ def read_huffman(blob: bytes, lengths: np.ndarray) -> np.ndarray:
         rec = h["records_off"] + int(toff[t]) * 16
         n_t = min(T, n * kp - t * T)
         start = np.frombuffer(dev, np.uint16, 32, rec)
-        raw = np.frombuffer(dev, np.uint8, n_t, rec + 64)
-        area_off = rec + 64 + (n_t + 15) // 16 * 16
+        S = n_t // 32
+        S16 = (S + 15) // 16 * 16
+        raw_t = np.frombuffer(dev, np.uint8, 32 * S16, rec + 64)
+        # lane-transposed 16-byte chunks: chunk j of lane l holds symbols 16j..16j+15
+        raw = raw_t.reshape(S16 // 16, 32, 16).transpose(0, 2, 1).reshape(S16, 32)[:S].ravel()
+        area_off = rec + 64 + 32 * S16
         area_end = h["records_off"] + int(toff[t + 1]) * 16
         words = np.frombuffer(dev, np.uint32, (area_end - area_off) // 4, area_off)
         bits = "".join(format(int(x), "032b") for x in words)
