@@ -139,6 +139,27 @@ int ec_gemv(const ec_matrix* W, const uint16_t* x_bf16, float* y, int batch, cud
 int ec_gemv_group(const ec_matrix* const* Ws, int count, const uint16_t* x_bf16, float* const* ys, int batch,
                   cudaStream_t stream);
 
+/* Allocation-free GEMV.  Same result contract as ec_gemv (Huffman-coded matrices,
+ * batch 1..EC_MAX_BATCH, y overwritten), for callers that must not allocate device
+ * memory while serving: a cudaMalloc can stall the whole device and can fail at an
+ * arbitrary point, and some processes hand all device memory to one allocator (for
+ * example a framework's caching allocator) or reserve a fixed budget up front.
+ * This call allocates nothing, on the device or the host.  Its working memory is a
+ * fixed 4 MiB array built into the library (every GPU that loads the library keeps
+ * it until the process exits): a status word plus one partial sum per (batch row,
+ * output row, tile covering that row); the tiles' partial sums are added in tile
+ * order by a second small kernel, so repeated calls give identical y.
+ * Limits: batch * n_rows * (ceil(k_pad / tile) + 1) partial sums must fit in that
+ * array (about 1M floats), otherwise EC_ERR_UNSUPPORTED; rANS matrices also return
+ * EC_ERR_UNSUPPORTED.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) and the device's limits once; make that first call
+ * before any stream capture.  All calls share the one array: calls whose work
+ * overlaps on the GPU (other streams, other threads) race and corrupt each other's
+ * partial sums, so serialise them.  Corruption found in the payload is recorded in
+ * the array's status word, not in the word ec_status() reads.  The pages have no
+ * counterpart to this entry point. */
+int ec_gemv_static(const ec_matrix* W, const uint16_t* x_bf16, float* y, int batch, cudaStream_t stream);
+
 /* Uncompressed comparator: y = W x for a dense BF16 W [n_rows, k_cols] in device
  * memory, FP32 accumulation, same x / y conventions as ec_gemv. */
 int ec_bf16_gemv(const uint16_t* w_bf16, int64_t n_rows, int64_t k_cols, const uint16_t* x_bf16, float* y,

@@ -36,7 +36,7 @@ EC_KIND_RANS_INT4 = 2
 
 EXPORTS = ["ec_encode_bf16", "ec_encode_rans", "ec_decode", "ec_decode_batch", "ec_gemv", "ec_gemv_group",
            "ec_bf16_gemv", "ec_stats", "ec_code_lengths", "ec_serialize", "ec_deserialize", "ec_status", "ec_free",
-           "ec_strerror"]
+           "ec_strerror", "ec_gemv_static"]
 
 
 class HuffParams(ctypes.Structure):
@@ -69,6 +69,7 @@ _sig = {
     "ec_gemv": ([_vp, _vp, _vp, _i32, _vp], _i32),
     "ec_gemv_group": ([_vp, _i32, _vp, _vp, _i32, _vp], _i32),
     "ec_bf16_gemv": ([_vp, _i64, _i64, _vp, _vp, _i32, _vp], _i32),
+    "ec_gemv_static": ([_vp, _vp, _vp, _i32, _vp], _i32),
     "ec_stats": ([_vp, ctypes.POINTER(Stats)], _i32),
     "ec_code_lengths": ([_vp, _vp], _i32),
     "ec_serialize": ([_vp, _vp, _i64, ctypes.POINTER(_i64)], _i32),
@@ -208,6 +209,12 @@ def decode_batch(Ws, outs, stream=None) -> None:
 
 def gemv(W: Matrix, x, y, batch: int = 1, stream=None) -> None:
     _check(lib.ec_gemv(W.handle, _dev_ptr(x), _dev_ptr(y), batch, _stream_ptr(stream)), "ec_gemv")
+
+
+def gemv_static(W: Matrix, x, y, batch: int = 1, stream=None) -> None:
+    """ec_gemv_static: the GEMV with no device or host allocation (fixed built-in
+    scratch; serialise calls that could overlap on the GPU)."""
+    _check(lib.ec_gemv_static(W.handle, _dev_ptr(x), _dev_ptr(y), batch, _stream_ptr(stream)), "ec_gemv_static")
 
 
 def gemv_group(Ws, x, ys, batch: int = 1, stream=None) -> None:

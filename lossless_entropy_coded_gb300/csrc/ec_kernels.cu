@@ -65,6 +65,8 @@ struct HuffGemvArgs {
     int64_t total_tiles;
     int* status;
     int code_bytes;             /* per-warp code buffer */
+    float* part;                /* allocation-free variant: per (row, tile) partial sums */
+    int part_slots;             /* partial-sum slots per row */
 };
 
 struct HuffDecodeArgs {
@@ -377,7 +379,10 @@ __device__ __forceinline__ void huff_tile(const TileView& v, uint32_t l1s, uint3
 }
 
 /* ======================================================== Huffman GEMV kernel */
-template <int B>
+/* kPart = false: row sums go to y (stored, or added atomically when a row spans
+ * tiles).  kPart = true (allocation-free entry point): every row segment a tile
+ * produces goes to its own slot of a.part, summed into y by part_reduce_kernel. */
+template <int B, bool kPart = false>
 __global__ void __launch_bounds__(kHW * 32, 1) huff_gemv_kernel(const __grid_constant__ HuffGemvArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -426,15 +431,23 @@ __global__ void __launch_bounds__(kHW * 32, 1) huff_gemv_kernel(const __grid_con
         uint4 rw[2] = {raw16(v, 0, lane), v.S > 16 ? raw16(v, 1, lane) : make_uint4(0, 0, 0, 0)};
         uint4 rn[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
 
+        const int64_t t_cur = g - M.tile_begin;
         auto flush = [&](int64_t r) {
+            int64_t slot = 0;
+            if (kPart) /* tiles before this one that also cover row r */
+                slot = t_cur - (r * M.k_pad) / (32 * (int64_t)M.steps);
 #pragma unroll
             for (int b = 0; b < B; ++b) {
                 if (b >= batch) break;
                 const float s = warp_sum(acc[b][0] + acc[b][1]);
                 if (lane == 0) {
-                    float* dst = M.y + (int64_t)b * M.n_rows + r;
-                    if (M.atomic_y) atomicAdd(dst, s);
-                    else *dst = s;
+                    if (kPart) {
+                        a.part[((int64_t)b * M.n_rows + r) * a.part_slots + slot] = s;
+                    } else {
+                        float* dst = M.y + (int64_t)b * M.n_rows + r;
+                        if (M.atomic_y) atomicAdd(dst, s);
+                        else *dst = s;
+                    }
                 }
                 acc[b][0] = acc[b][1] = 0.f;
             }
@@ -1013,6 +1026,77 @@ int rans_run(const ec_matrix* W, const uint16_t* x, float* y, uint16_t* out, int
     return EC_OK;
 }
 
+/* ====================================================== allocation-free GEMV */
+/* Scratch for ec_gemv_static: one file-scope device array that every GPU loading
+ * this library holds until exit.  Word 0 is the status word of those calls; the
+ * partial row sums start after a 256-byte header. */
+constexpr size_t kStaticScratchBytes = size_t(4) << 20; /* 4 MiB */
+constexpr int64_t kStaticHeaderFloats = 64;
+constexpr int64_t kStaticPartFloats = (int64_t)(kStaticScratchBytes / sizeof(float)) - kStaticHeaderFloats;
+static __device__ __align__(256) float g_ec_static_scratch[kStaticScratchBytes / sizeof(float)];
+
+/* y[b, r] = sum of the row's partial sums, one per tile that covers row r, added in
+ * tile order (so the result is the same on every call). */
+__global__ void part_reduce_kernel(const float* __restrict__ part, int slots, int64_t n_rows, int64_t k_pad, int64_t T,
+                                   int batch, float* __restrict__ y) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)batch * n_rows) return;
+    const int64_t r = i % n_rows;
+    const int64_t first = (r * k_pad) / T, last = ((r + 1) * k_pad - 1) / T;
+    const float* src = part + i * slots;
+    float s = 0.f;
+    for (int64_t k = 0; k <= last - first && k < slots; ++k) s += src[k];
+    y[i] = s;
+}
+
+/* Per-device set-up of the allocation-free path, in a fixed table (no allocation):
+ * SM count, shared-memory limit and the device address of the scratch array. */
+struct StaticDevice {
+    int ready;
+    int sms;
+    size_t smem_optin;
+    float* scratch;
+};
+constexpr int kMaxStaticDevices = 64;
+StaticDevice g_static_dev[kMaxStaticDevices];
+std::mutex g_static_mu;
+
+int static_device(int dev, StaticDevice** out) {
+    if (dev < 0 || dev >= kMaxStaticDevices) return EC_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    StaticDevice& s = g_static_dev[dev];
+    if (!s.ready) {
+        int sms = 0, optin = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return EC_ERR_CUDA;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_ec_static_scratch) != cudaSuccess || !p) return EC_ERR_CUDA;
+        s.sms = sms;
+        s.smem_optin = (size_t)optin;
+        s.scratch = (float*)p;
+        s.ready = 1;
+    }
+    *out = &s;
+    return EC_OK;
+}
+
+template <int B>
+int launch_huff_gemv_part_b(const HuffGemvArgs& a, size_t smem, int grid, int block, cudaStream_t s) {
+    if (cudaFuncSetAttribute(huff_gemv_kernel<B, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return EC_ERR_CUDA;
+    return launch_ex(huff_gemv_kernel<B, true>, grid, block, smem, s, a);
+}
+
+int launch_huff_gemv_part(const HuffGemvArgs& a, size_t smem, int grid, int block, cudaStream_t s) {
+    if (a.batch <= 1) return launch_huff_gemv_part_b<1>(a, smem, grid, block, s);
+    if (a.batch <= 2) return launch_huff_gemv_part_b<2>(a, smem, grid, block, s);
+    if (a.batch <= 4) return launch_huff_gemv_part_b<4>(a, smem, grid, block, s);
+    if (a.batch <= 8) return launch_huff_gemv_part_b<8>(a, smem, grid, block, s);
+    return launch_huff_gemv_part_b<16>(a, smem, grid, block, s);
+}
+
 }  // namespace
 
 /* ================================================================ C ABI */
@@ -1139,4 +1223,54 @@ extern "C" int ec_status(cudaStream_t stream) {
     if (cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return EC_ERR_CUDA;
     if (v && cudaMemset(d->status, 0, sizeof(int)) != cudaSuccess) return EC_ERR_CUDA;
     return v ? EC_ERR_CORRUPT : EC_OK;
+}
+
+/* Allocation-free GEMV (declared in ec.h, where its contract is described). */
+extern "C" int ec_gemv_static(const ec_matrix* W, const uint16_t* x, float* y, int batch, cudaStream_t stream) {
+    if (!W || !W->d_blob) return EC_ERR_INVALID_ARG;
+    if (batch < 1) return EC_ERR_INVALID_ARG;
+    if (batch > EC_MAX_BATCH || W->kind != EC_KIND_HUFFMAN_BF16) return EC_ERR_UNSUPPORTED;
+    if (!y || !aligned16(y) || (W->hdr.k_cols > 0 && (!x || !aligned16(x)))) return EC_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return EC_ERR_CUDA;
+    if (check_matrix(W, dev) != EC_OK) return EC_ERR_INVALID_ARG;
+    StaticDevice* d = nullptr;
+    int rc = static_device(dev, &d);
+    if (rc != EC_OK) return rc;
+    const ec_blob_header& h = W->hdr;
+    const int64_t T = 32 * (int64_t)h.steps;
+    const int64_t slots = (h.k_pad + T - 1) / T + 1;
+    if (h.n_rows > 0 && (int64_t)batch * slots > kStaticPartFloats / h.n_rows) return EC_ERR_UNSUPPORTED;
+    if (h.n_tiles == 0)
+        return cudaMemsetAsync(y, 0, sizeof(float) * (size_t)batch * (size_t)h.n_rows, stream) == cudaSuccess
+                   ? EC_OK
+                   : EC_ERR_CUDA;
+    HuffGemvArgs a{};
+    a.m[0] = huff_desc(W);
+    a.count = 1;
+    a.total_tiles = h.n_tiles;
+    a.status = (int*)d->scratch;
+    a.code_bytes = ((int)h.max_code_bytes + 15) & ~15;
+    a.part = d->scratch + kStaticHeaderFloats;
+    a.part_slots = (int)slots;
+    if (a.code_bytes < 16) a.code_bytes = 16;
+    if (cudaMemsetAsync(d->scratch, 0, sizeof(int), stream) != cudaSuccess) return EC_ERR_CUDA;
+    const size_t tables = kMultiBytes, per_warp = huff_warp_bytes(a.code_bytes);
+    const size_t xrow = xs_row_bytes((uint32_t)h.k_pad);
+    if (tables + xrow + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED;
+    const int warps = (int)std::min<size_t>(kHW, (d->smem_optin - tables - xrow) / per_warp);
+    const size_t fixed = tables + (size_t)warps * per_warp;
+    const int per_pass = (int)std::min<size_t>(batch, (d->smem_optin - fixed) / xrow);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(d->sms, (h.n_tiles + warps - 1) / warps));
+    for (int b0 = 0; b0 < batch; b0 += per_pass) {
+        const int nb = std::min(per_pass, batch - b0);
+        a.batch = nb;
+        a.x = x + (int64_t)b0 * h.k_cols;
+        if ((rc = launch_huff_gemv_part(a, fixed + xrow * nb, grid, warps * 32, stream)) != EC_OK) return rc;
+        const int64_t n = (int64_t)nb * h.n_rows;
+        part_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(a.part, a.part_slots, h.n_rows, h.k_pad,
+                                                                           T, nb, y + (int64_t)b0 * h.n_rows);
+        if ((rc = launch_result()) != EC_OK) return rc;
+    }
+    return EC_OK;
 }
