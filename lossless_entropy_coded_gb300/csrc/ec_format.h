@@ -44,11 +44,10 @@
 #define EC_BLOB_MAGIC 0x31434345u /* "ECC1" */
 #define EC_BLOB_VERSION 1u
 
-#define EC_L1_BITS 11            /* level-1 Huffman window */
+#define EC_L1_BITS 12            /* level-1 Huffman window */
 #define EC_SUB_BITS 8            /* bits per sub-table level */
 #define EC_MULTI_MAX 3           /* exponents decoded by one level-1 lookup */
-#define EC_MULTI_QINC 2          /* stage bytes per decoded exponent field */
-#define EC_MULTI_WORDS (4 << EC_L1_BITS) /* u32 words of the multi-symbol level-1 table */
+#define EC_MULTI_WORDS (1 << EC_L1_BITS) /* u32 words of the multi-symbol level-1 table */
 #define EC_HUFF_ROW_ALIGN 256    /* k_pad multiple for the Huffman layout */
 #define EC_RANS_ROW_ALIGN 128    /* k_pad multiple for the rANS layout (= scale group) */
 #define EC_MAX_CODE_LEN 24
@@ -58,16 +57,12 @@
 
 /* Huffman decode tables, in this order inside the table section:
  *
- * 1. multi-symbol level-1 table, 2^EC_L1_BITS entries of 4 u32 (16 bytes), indexed
- *    by the next EC_L1_BITS bits of the stream.  Decodes up to EC_MULTI_MAX whole
- *    codewords at once:
- *      word 0 = f0 | (EC_MULTI_QINC * n) << 16, word 1 = f1, word 2 = f2,
- *      word 3 = total bits
- *    where f_k = exponent_k << 7 (0 for unused slots) and n >= 1 is the number of
- *    codewords decoded (EC_MULTI_QINC = bytes per exponent field in the decoder's
- *    lane-private stage).
- *    When the first codeword is longer than EC_L1_BITS, word 3 holds the level-1
- *    entry of table 2 (a pointer, bit 31 set) and words 0..2 are 0.
+ * 1. multi-symbol level-1 table, 2^EC_L1_BITS u32 entries indexed by the next
+ *    EC_L1_BITS bits of the stream; it decodes up to EC_MULTI_MAX whole codewords
+ *    at once:  bits 0..7, 8..15, 16..23 = exponents of codewords 1..3 (0 when
+ *    unused), bits 24..25 = their count n >= 1, bits 28..31 = their total length.
+ *    An entry of 0 means the first codeword is longer than EC_L1_BITS (or no
+ *    codeword matches): the decoder then walks table 2.
  * 2. hierarchical table (u32 entries, below): a 2^EC_L1_BITS level-1 table then
  *    256-entry sub-tables (DFloat11 appendix, Fig. 4 / Fig. 14). */
 

@@ -247,25 +247,18 @@ std::vector<uint32_t> build_multi_table(const std::vector<uint32_t>& h) {
     const uint32_t W = EC_L1_BITS, mask = (1u << W) - 1;
     std::vector<uint32_t> t(EC_MULTI_WORDS, 0);
     for (uint32_t v = 0; v <= mask; ++v) {
-        uint32_t* e = &t[4 * v];
-        const uint32_t first = h[v];
-        if (first & (EC_ENT_PTR | EC_ENT_BAD)) {
-            e[3] = (first & EC_ENT_BAD) ? (EC_ENT_PTR | EC_ENT_BAD) : first;
-            continue;
-        }
-        uint32_t used = 0, n = 0, f[EC_MULTI_MAX] = {0, 0, 0};
+        if (h[v] & (EC_ENT_PTR | EC_ENT_BAD)) continue; /* 0: long codeword or no match */
+        uint32_t used = 0, n = 0, e = 0;
         while (n < EC_MULTI_MAX && used < W) {
             const uint32_t ent = h[(v << used) & mask];
             if (ent & (EC_ENT_PTR | EC_ENT_BAD)) break;
             const uint32_t len = (ent >> 16) & 31;
             if (used + len > W) break;
-            f[n++] = ent & 0xFFFFu;
+            e |= ((ent & 0xFFFFu) >> 7) << (8 * n);
+            ++n;
             used += len;
         }
-        e[0] = f[0] | ((EC_MULTI_QINC * n) << 16);
-        e[1] = f[1];
-        e[2] = f[2];
-        e[3] = used;
+        t[v] = e | (n << 24) | (used << 28);
     }
     return t;
 }
@@ -801,15 +794,10 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
     const uint32_t* tab = (const uint32_t*)(b + h.table_off);
     if (huff) {
         const int64_t n_sub = (h.table_words - EC_MULTI_WORDS - (1 << EC_L1_BITS)) / 256;
-        for (int64_t i = 0; i < (1 << EC_L1_BITS); ++i) { /* multi-symbol entries */
-            const uint32_t* e = tab + 4 * i;
-            if (e[3] & EC_ENT_PTR) {
-                if (!(e[3] & EC_ENT_BAD) && (int64_t)(e[3] & 0xFFFFu) >= n_sub) return EC_ERR_CORRUPT;
-            } else {
-                const uint32_t n = (e[0] >> 16) / EC_MULTI_QINC;
-                if (n < 1 || n > EC_MULTI_MAX || (e[0] >> 16) % EC_MULTI_QINC || e[3] < n || e[3] > EC_L1_BITS)
-                    return EC_ERR_CORRUPT;
-            }
+        for (int64_t i = 0; i < EC_MULTI_WORDS; ++i) { /* multi-symbol entries */
+            const uint32_t e = tab[i], n = (e >> 24) & 3u, len = e >> 28;
+            if (e == 0) continue;
+            if (n < 1 || len < n || len > EC_L1_BITS || (e & 0x0C000000u)) return EC_ERR_CORRUPT;
         }
         for (int64_t i = EC_MULTI_WORDS; i < h.table_words; ++i)
             if ((tab[i] & EC_ENT_PTR) && (int64_t)(tab[i] & 0xFFFFu) >= n_sub) return EC_ERR_CORRUPT;

@@ -147,21 +147,22 @@ __device__ __forceinline__ int64_t tile_row(int64_t t, int64_t T, int64_t kp, in
  * Work layout.  One warp decodes one tile at a time; lane l owns the tile's
  * symbols i = 0 .. S-1 at positions 32 i + l and, unlike a DFloat11 thread that
  * hands its output to a block-wide write buffer, lane l also multiplies them:
- * exponent fields go to a lane-private stage in shared memory (two buffers of
- * kC fields + spill), the matching raw bytes arrive lane-transposed with one
- * 16-byte load per 16 symbols, and x is kept transposed in shared memory
- * (xs_t[l][j] = x[32 j + l]) so lane l finds x for its symbols contiguously.
- * Decoding chunk c + 1 is interleaved with the multiply-accumulate of chunk c.
+ * exponents go to a lane-private byte stage in shared memory (two buffers of
+ * kC symbols + spill, lane stride kLane = 11 words so the 32 lanes' stores and
+ * 4-byte reads fall in distinct banks), the matching raw bytes arrive
+ * lane-transposed with one 16-byte load per 16 symbols, and x is kept transposed
+ * in shared memory (xs_t[l][j] = x[32 j + l]) so lane l finds x for its symbols
+ * contiguously.  Decoding chunk c + 1 is interleaved with the multiply-accumulate
+ * of chunk c.
  */
 constexpr int kHW = 24;                        /* max warps per CTA */
 constexpr int kC = 32;                         /* symbols per lane per chunk */
-constexpr int kSpill = 2 * EC_MULTI_MAX - 1;   /* symbols two lookups may write past a chunk */
-constexpr int kLane = 40;                      /* fields per lane per stage buffer (>= kC + kSpill, x8) */
-constexpr int kStageBytes = 2 * 32 * kLane * 2; /* two buffers */
+constexpr int kLane = 44;                      /* stage bytes per lane per buffer (11 words) */
+constexpr int kStageBuf = 32 * kLane;          /* one buffer of the warp */
+constexpr int kStageBytes = 2 * kStageBuf;     /* two buffers */
 constexpr int kSlackPairs = 32;                /* zero pairs after the code area (even) */
-constexpr uint32_t kMultiBytes = 16u << EC_L1_BITS;
-static_assert(kLane >= kC + kSpill && kLane % 8 == 0, "stage lane stride");
-static_assert(EC_MULTI_QINC == 2, "stage fields are 16-bit and lane-contiguous");
+constexpr uint32_t kMultiBytes = 4u * EC_MULTI_WORDS;
+static_assert(kLane >= kC + 8 && kLane % 4 == 0 && (kLane / 4) % 2 == 1, "stage lane stride");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 __device__ __forceinline__ uint2 lds64(uint32_t a) {
@@ -169,24 +170,34 @@ __device__ __forceinline__ uint2 lds64(uint32_t a) {
     asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
     return v;
 }
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
     return v;
 }
+__device__ __forceinline__ void sts8(uint32_t a, uint32_t v) {
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
 __device__ __forceinline__ void sts16(uint32_t a, uint32_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"((unsigned short)v) : "memory");
 }
-__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+__device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
-/* Codeword longer than the level-1 window (rare): walk the 8-bit sub-tables of the
- * hierarchical table in global memory; returns a one-symbol multi entry.  Corrupt
+/* Codeword longer than the level-1 window (rare): walk the hierarchical table in
+ * global memory from its level-1 entry for this window.  Returns the exponent with
+ * a count of 1 in the multi-entry layout (.x) and the codeword length (.y, up to
+ * 24 bits, which the 4-bit length field of a multi entry cannot hold).  Corrupt
  * data (no codeword matches) yields exponent 0 of length 1 and sets the status. */
-__device__ __forceinline__ uint4 long_codeword(uint32_t w3, uint32_t win, const uint32_t* __restrict__ hier,
-                                               int64_t hier_words, int* status) {
-    uint32_t ent = w3;
+__device__ __noinline__ uint2 long_codeword(uint32_t win, const uint32_t* __restrict__ hier, int64_t hier_words,
+                                            int* status) {
+    uint32_t ent = __ldg(hier + (win >> (32 - EC_L1_BITS)));
 #pragma unroll 1
     for (int lvl = 0; lvl < 3 && (ent & EC_ENT_PTR) && !(ent & EC_ENT_BAD); ++lvl) {
         const int used = (int)((ent >> 16) & 31);
@@ -201,7 +212,7 @@ __device__ __forceinline__ uint4 long_codeword(uint32_t w3, uint32_t win, const 
         flag_corrupt(status);
         ent = 1u << 16;
     }
-    return make_uint4((ent & 0xFFFFu) | ((uint32_t)EC_MULTI_QINC << 16), 0u, 0u, (ent >> 16) & 31);
+    return make_uint2(((ent & 0xFFFFu) >> 7) | (1u << 24), (ent >> 16) & 31);
 }
 
 /* Copy a tile's code area (nw words, global) into shared memory as overlapping
@@ -220,38 +231,46 @@ __device__ __forceinline__ void stage_pairs(uint2* pairs, const uint32_t* __rest
 }
 
 /* One lane's decoder: bit position p in the staged code area and the shared
- * address q of its next exponent field. */
+ * address q of its next exponent byte. */
 struct HuffLane {
     uint32_t p, q;
 };
 
-/* One multi-symbol lookup: write three exponent fields at q, q+2, q+4 and advance by
- * the codewords the entry holds (word 0 bits 16.. = 2 * count, word 3 = bits). */
+/* One multi-symbol lookup: store the entry's three exponent bytes at q, q+1, q+2 and
+ * advance by the codewords it holds. */
 __device__ __forceinline__ void huff_step(HuffLane& L, uint32_t l1s, uint32_t ps, const uint32_t* __restrict__ hier,
                                           int64_t hier_words, int* status) {
     const uint2 wp = lds64(ps + ((L.p >> 5) << 3));
     const uint32_t win = __funnelshift_l(wp.y, wp.x, L.p);
-    uint4 e = lds128(l1s + ((win >> (32 - EC_L1_BITS)) << 4));
-    if (__builtin_expect((int)e.w < 0, 0)) e = long_codeword(e.w, win, hier, hier_words, status);
-    sts16(L.q, e.x);
-    sts16(L.q + 2, e.y);
-    sts16(L.q + 4, e.z);
-    L.p += e.w;
-    L.q += e.x >> 16;
+    uint32_t e = lds32(l1s + ((win >> (32 - EC_L1_BITS)) << 2));
+    uint32_t adv = e >> 28;
+    if (__builtin_expect(e < (1u << 28), 0)) {
+        const uint2 lc = long_codeword(win, hier, hier_words, status);
+        e = lc.x;
+        adv = lc.y;
+    }
+    sts8(L.q, e);
+    sts8(L.q + 1, e >> 8);
+    sts8(L.q + 2, e >> 16);
+    L.p += adv;
+    L.q += (e >> 24) & 3u;
 }
 
-/* Merge two exponent fields e = [f1 | f0] with raw bytes a, a+1 of r into two BF16
- * bit patterns [w1 | w0]:  w = (sign << 15) | (exponent << 7) | mantissa. */
-__device__ __forceinline__ uint32_t merge_pair(uint32_t e, uint32_t r, uint32_t sel) {
-    const uint32_t dup = __byte_perm(r, 0, sel); /* [r1 r1 r0 r0] */
-    return e | (dup & 0x807F807Fu);
+/* Two BF16 weights [w1 | w0] from exponent bytes (a, a+1 of e, spread by esel) and
+ * raw bytes (a, a+1 of r, duplicated by rsel):
+ *     w = (sign << 15) | (exponent << 7) | mantissa. */
+__device__ __forceinline__ uint32_t merge_pair(uint32_t e, uint32_t esel, uint32_t r, uint32_t rsel) {
+    const uint32_t spread = __byte_perm(e, 0, esel); /* [0 e1 0 e0] */
+    const uint32_t dup = __byte_perm(r, 0, rsel);    /* [r1 r1 r0 r0] */
+    return spread * 128u + (dup & 0x807F807Fu);      /* fields do not overlap: + is | */
 }
 
-__device__ __forceinline__ void merge8(const uint4& e8, uint32_t r0, uint32_t r1, uint32_t (&w)[4]) {
-    w[0] = merge_pair(e8.x, r0, 0x1100);
-    w[1] = merge_pair(e8.y, r0, 0x3322);
-    w[2] = merge_pair(e8.z, r1, 0x1100);
-    w[3] = merge_pair(e8.w, r1, 0x3322);
+/* Eight weights: exponent bytes e = (e0..e3, e4..e7), raw bytes r0 (4), r1 (4). */
+__device__ __forceinline__ void merge8(uint2 e, uint32_t r0, uint32_t r1, uint32_t (&w)[4]) {
+    w[0] = merge_pair(e.x, 0x4140, r0, 0x1100);
+    w[1] = merge_pair(e.x, 0x4342, r0, 0x3322);
+    w[2] = merge_pair(e.y, 0x4140, r1, 0x1100);
+    w[3] = merge_pair(e.y, 0x4342, r1, 0x3322);
 }
 
 /* acc += w0 * x0 + w1 * x1 for BF16 pairs w = [w1|w0], x = [x1|x0]; the products are
@@ -270,8 +289,8 @@ __device__ __forceinline__ float fma2_bf16(uint32_t w, uint32_t x, float acc) {
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
 
-/* Per-warp shared memory: stage (2 x 32 lanes x kLane fields) | code pairs + slack.
- * Multiples of 16 bytes, so 16-byte loads and stores stay aligned. */
+/* Per-warp shared memory: stage (2 buffers x 32 lanes x kLane bytes) | code pairs +
+ * slack.  Multiples of 16 bytes, so 16-byte loads and stores stay aligned. */
 __host__ __device__ constexpr size_t huff_warp_bytes(int code_bytes) {
     return (size_t)kStageBytes + 2 * (size_t)((code_bytes + 15) & ~15) + 8 * (size_t)kSlackPairs;
 }
@@ -330,8 +349,8 @@ __device__ __forceinline__ uint4 raw16(const TileView& v, int j, int lane) {
     return __ldg((const uint4*)v.raw + (32 * j + lane));
 }
 
-/* Decode the lane's next chunk (target symbols) into stage buffer Y, interleaving
- * up to four multiply-accumulate sub-steps `fma(k)` of the previous chunk. */
+/* Decode the lane's next chunk (until q reaches q_end) interleaving up to four
+ * multiply-accumulate sub-steps `fma(k)` of the previous chunk. */
 template <class Fma>
 __device__ __forceinline__ void huff_chunk(HuffLane& L, uint32_t q_end, int subs, uint32_t l1s, uint32_t ps,
                                            const uint32_t* __restrict__ hier, int64_t hier_words, int* status,
@@ -351,30 +370,29 @@ __device__ __forceinline__ void huff_chunk(HuffLane& L, uint32_t q_end, int subs
     }
 }
 
-/* Walk one tile: prologue decodes chunk 0; iteration c moves chunk c's spill to the
- * other buffer, decodes chunk c + 1 there while `consume(c, k, fields)` handles
+/* Walk one tile: the prologue decodes chunk 0; iteration c moves chunk c's spill to
+ * the other buffer and decodes chunk c + 1 there while `consume(c, k, exps)` handles
  * sub-step k (8 symbols) of chunk c. */
 template <class Consume>
 __device__ __forceinline__ void huff_tile(const TileView& v, uint32_t l1s, uint32_t ps, uint32_t stage_lane,
                                           const uint32_t* __restrict__ hier, int64_t hier_words, int* status,
                                           int lane, Consume&& consume) {
-    const uint32_t bufb = 32 * kLane * 2; /* byte distance between the two buffers */
     const uint32_t pmax = 32u * v.nw;
     HuffLane L{lane_start_bits(v, lane), stage_lane};
     const int nch = (v.S + kC - 1) / kC;
-    /* chunk 0 into buffer 0 */
-    huff_chunk(L, stage_lane + 2u * min(kC, v.S), 0, l1s, ps, hier, hier_words, status, [](int) {});
+    huff_chunk(L, stage_lane + (uint32_t)min(kC, v.S), 0, l1s, ps, hier, hier_words, status, [](int) {});
     for (int c = 0; c < nch; ++c) {
-        const uint32_t X = stage_lane + (c & 1) * bufb, Y = stage_lane + ((c + 1) & 1) * bufb;
+        const uint32_t X = stage_lane + (c & 1) * kStageBuf, Y = stage_lane + ((c + 1) & 1) * kStageBuf;
         const int rows_c = min(kC, v.S - c * kC);
-        /* spill of chunk c (fields kC .. kC + 7 of X) becomes the start of buffer Y */
-        sts128(Y, lds128(X + 2 * kC));
-        L.q = L.q - X - 2 * kC + Y;
+        /* spill of chunk c (bytes kC .. kC + 7 of X) becomes the start of buffer Y */
+        sts32(Y, lds32(X + kC));
+        sts32(Y + 4, lds32(X + kC + 4));
+        L.q = L.q - X - kC + Y;
         L.p = min(L.p, pmax);
         const int next = min(kC, v.S - (c + 1) * kC); /* symbols of chunk c + 1 (<= 0: none) */
-        const uint32_t q_end = next > 0 ? Y + 2u * next : 0u;
+        const uint32_t q_end = next > 0 ? Y + (uint32_t)next : 0u;
         huff_chunk(L, q_end, rows_c / 8, l1s, ps, hier, hier_words, status,
-                   [&](int k) { consume(c, k, lds128(X + 16 * k)); });
+                   [&](int k) { consume(c, k, make_uint2(lds32(X + 8 * k), lds32(X + 8 * k + 4))); });
     }
 }
 
@@ -395,14 +413,14 @@ __global__ void __launch_bounds__(kHW * 32, 1) huff_gemv_kernel(const __grid_con
     uint4* l1g = (uint4*)smem;
     uint16_t* xs = (uint16_t*)(smem + (size_t)a.count * kMultiBytes);
     uint8_t* wbase = (uint8_t*)xs + (size_t)batch * xs_row_bytes(kp) + (size_t)warp * huff_warp_bytes(a.code_bytes);
-    const uint32_t stage_lane = smem_u32(wbase) + lane * (kLane * 2);
+    const uint32_t stage_lane = smem_u32(wbase) + lane * kLane;
     uint2* pairs = (uint2*)(wbase + kStageBytes);
     const uint32_t pairs_s = smem_u32(pairs);
     const uint32_t xs_lane = smem_u32(xs) + lane * lx * 2;
 
     for (int k = 0; k < a.count; ++k) {
         const uint4* src = (const uint4*)a.m[k].table;
-        for (int i = threadIdx.x; i < (1 << EC_L1_BITS); i += blockDim.x) l1g[(k << EC_L1_BITS) + i] = __ldg(src + i);
+        for (int i = threadIdx.x; i < EC_MULTI_WORDS / 4; i += blockDim.x) l1g[k * (EC_MULTI_WORDS / 4) + i] = __ldg(src + i);
     }
     grid_dep_launch();
     grid_dep_wait(); /* x and y belong to the preceding kernel in the stream from here on */
@@ -421,7 +439,7 @@ __global__ void __launch_bounds__(kHW * 32, 1) huff_gemv_kernel(const __grid_con
         __syncwarp();
         stage_pairs(pairs, v.area, v.nw, lane);
         __syncwarp();
-        const uint32_t l1s = smem_u32(l1g + (mi << EC_L1_BITS));
+        const uint32_t l1s = smem_u32(l1g + mi * (EC_MULTI_WORDS / 4));
         int64_t row = v.row;
         uint32_t jc = v.col0 / 32; /* x column block of the current sub-step */
         const uint32_t jrow = kp / 32;
@@ -454,7 +472,7 @@ __global__ void __launch_bounds__(kHW * 32, 1) huff_gemv_kernel(const __grid_con
         };
 
         huff_tile(v, l1s, pairs_s, stage_lane, M.table + EC_MULTI_WORDS, M.table_words - EC_MULTI_WORDS, a.status,
-                  lane, [&](int c, int k, const uint4& e8) {
+                  lane, [&](int c, int k, const uint2& e8) {
                       if (k == 0) { /* prefetch the next chunk's raw bytes */
                           const int j = 2 * (c + 1);
                           rn[0] = 16 * j < v.S ? raw16(v, j, lane) : make_uint4(0, 0, 0, 0);
@@ -500,7 +518,7 @@ __global__ void __launch_bounds__(kHW * 32, 1) huff_decode_kernel(const __grid_c
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint4* l1 = (uint4*)smem;
     uint8_t* wbase = smem + kMultiBytes + (size_t)warp * decode_warp_bytes(a.code_bytes);
-    const uint32_t stage_lane = smem_u32(wbase) + lane * (kLane * 2);
+    const uint32_t stage_lane = smem_u32(wbase) + lane * kLane;
     uint2* pairs = (uint2*)(wbase + kStageBytes);
     const uint32_t pairs_s = smem_u32(pairs), l1s = smem_u32(l1);
     const uint32_t tbuf = smem_u32(wbase + huff_warp_bytes(a.code_bytes)); /* 256 outputs */
@@ -514,7 +532,7 @@ __global__ void __launch_bounds__(kHW * 32, 1) huff_decode_kernel(const __grid_c
         const int64_t mend = min(hi, M.tile_begin + M.n_tiles);
         __syncthreads();
         const uint4* src = (const uint4*)M.table;
-        for (int i = threadIdx.x; i < (1 << EC_L1_BITS); i += blockDim.x) l1[i] = __ldg(src + i);
+        for (int i = threadIdx.x; i < EC_MULTI_WORDS / 4; i += blockDim.x) l1[i] = __ldg(src + i);
         __syncthreads();
         const int64_t kp = M.k_pad, K = M.k_cols;
         const bool vec = (K % 8) == 0;
@@ -529,7 +547,7 @@ __global__ void __launch_bounds__(kHW * 32, 1) huff_decode_kernel(const __grid_c
             uint4 rw[2] = {raw16(v, 0, lane), v.S > 16 ? raw16(v, 1, lane) : make_uint4(0, 0, 0, 0)};
             uint4 rn[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
             huff_tile(v, l1s, pairs_s, stage_lane, M.table + EC_MULTI_WORDS, M.table_words - EC_MULTI_WORDS,
-                      a.status, lane, [&](int c, int k, const uint4& e8) {
+                      a.status, lane, [&](int c, int k, const uint2& e8) {
                           if (k == 0) {
                               const int j = 2 * (c + 1);
                               rn[0] = 16 * j < v.S ? raw16(v, j, lane) : make_uint4(0, 0, 0, 0);
