@@ -57,15 +57,20 @@ enum {
 };
 
 #define EC_MAX_BATCH 16
+#define EC_DEFAULT_MAX_CODE_LEN 12
 #define EC_MAX_GROUP 8
 #define EC_MAX_DECODE_BATCH 64
 
 typedef struct ec_matrix ec_matrix; /* opaque: host descriptor + one device blob */
 
 /* Huffman-exponent codec parameters (NULL = defaults).
- *  max_code_len  longest codeword, 1..24 (default 24, the workloads' limit); the
- *                code is textbook Huffman when it fits, otherwise the optimal
- *                length-limited code (package-merge).
+ *  max_code_len  longest codeword, 1..24 (default EC_DEFAULT_MAX_CODE_LEN = 12);
+ *                the code is textbook Huffman when it fits, otherwise the
+ *                optimal length-limited code (package-merge).  At 12 every
+ *                codeword fits the decoder's first table lookup; on LLM
+ *                weights the limit costs about 0.004 bits per exponent over
+ *                the unconstrained code.  Longer limits decode through a
+ *                hierarchical table in global memory, more slowly.
  *  tile_steps    symbols per lane in one tile of 32 lanes; 32, 64 or 128 (default
  *                128, i.e. 4096-weight tiles). */
 typedef struct {

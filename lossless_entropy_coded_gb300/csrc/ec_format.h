@@ -5,8 +5,8 @@
  * One contiguous device blob per matrix:
  *
  *   [ec_blob_header, 256 B]
- *   [decode table]            Huffman: multi-symbol level-1 table, then the
- *                             hierarchical table (level 1 + 256-entry sub-tables).
+ *   [decode table]            Huffman: pair table, then the hierarchical table
+ *                             (level 1 + 256-entry sub-tables).
  *                             rANS:    2^prob_bits u32 slot entries.
  *   [group scales]            rANS only: FP16 [n_rows, k_pad / 128].
  *   [tile offsets]            u32 [n_tiles + 1], record start in 16-byte units.
@@ -42,13 +42,12 @@
 #include <stdint.h>
 
 #define EC_BLOB_MAGIC 0x31434345u /* "ECC1" */
-#define EC_BLOB_VERSION 1u
+#define EC_BLOB_VERSION 3u
 
 #define EC_L1_BITS 12            /* level-1 Huffman window */
 #define EC_SUB_BITS 8            /* bits per sub-table level */
-#define EC_MULTI_MAX 3           /* exponents decoded by one level-1 lookup */
-#define EC_MULTI_WORDS (1 << EC_L1_BITS) /* u32 words of the multi-symbol level-1 table */
-#define EC_HUFF_ROW_ALIGN 256    /* k_pad multiple for the Huffman layout */
+#define EC_PAIR_WORDS (1 << EC_L1_BITS) /* u32 words of the pair table */
+#define EC_HUFF_ROW_ALIGN 512    /* k_pad multiple for the Huffman layout (16 symbols x 32 lanes) */
 #define EC_RANS_ROW_ALIGN 128    /* k_pad multiple for the rANS layout (= scale group) */
 #define EC_MAX_CODE_LEN 24
 
@@ -57,14 +56,23 @@
 
 /* Huffman decode tables, in this order inside the table section:
  *
- * 1. multi-symbol level-1 table, 2^EC_L1_BITS u32 entries indexed by the next
- *    EC_L1_BITS bits of the stream; it decodes up to EC_MULTI_MAX whole codewords
- *    at once:  bits 0..7, 8..15, 16..23 = exponents of codewords 1..3 (0 when
- *    unused), bits 24..25 = their count n >= 1, bits 28..31 = their total length.
- *    An entry of 0 means the first codeword is longer than EC_L1_BITS (or no
- *    codeword matches): the decoder then walks table 2.
+ * 1. pair table, 2^EC_L1_BITS u32 entries indexed by the next EC_L1_BITS bits of
+ *    a lane's stream.  Entry layout (fields chosen so that the entry is already
+ *    the exponent half of two BF16 weights [w(i+1) | w(i)]):
+ *      bits  7..14  exponent of the first codeword in the window
+ *      bits 23..30  exponent of the second codeword (pairs only)
+ *      bits  0..3   total length of the two codewords when both end inside the
+ *                   window, else 0
+ *      bits 16..19  length of the first codeword when it ends inside the window,
+ *                   else 0 (longer than the window, or no codeword matches)
+ *      all other bits 0.
+ *    The decoder reads bits 0..3 to advance; 0 sends it to a second lookup for
+ *    the second codeword and, when bits 16..19 are 0 too, to table 2.
  * 2. hierarchical table (u32 entries, below): a 2^EC_L1_BITS level-1 table then
  *    256-entry sub-tables (DFloat11 appendix, Fig. 4 / Fig. 14). */
+#define EC_PAIR_LEN_MASK 0x0000000Fu
+#define EC_PAIR_FIRST_SHIFT 16
+#define EC_PAIR_FIELDS 0x7F8F7F8Fu /* every bit a valid entry may set */
 
 /* Huffman table entry (u32):
  *   symbol:  bits 0..15 = exponent << 7 (the BF16 exponent field), bits 16..20 =

@@ -238,27 +238,27 @@ std::vector<uint32_t> build_huff_table(const uint8_t len[256], const uint32_t co
     return t;
 }
 
-/* Multi-symbol level-1 table: for every EC_L1_BITS-bit window, the codewords that
- * lie entirely inside it, read greedily from the top, at most EC_MULTI_MAX.  Built
- * from the hierarchical level-1 table: the window shifted left by the bits already
- * used, zero-filled, names the next codeword, which counts only if it ends inside
- * the window. */
-std::vector<uint32_t> build_multi_table(const std::vector<uint32_t>& h) {
+/* Pair table: for every EC_L1_BITS-bit window, the first codeword (when it ends
+ * inside the window) and the second one (when it ends inside it too), with their
+ * exponents placed in the BF16 exponent fields of two weights.  Built from the
+ * hierarchical level-1 table: the window shifted left by the first codeword's
+ * length, zero-filled, names the second codeword, which counts only if it ends
+ * inside the window. */
+std::vector<uint32_t> build_pair_table(const std::vector<uint32_t>& h) {
     const uint32_t W = EC_L1_BITS, mask = (1u << W) - 1;
-    std::vector<uint32_t> t(EC_MULTI_WORDS, 0);
+    std::vector<uint32_t> t(EC_PAIR_WORDS, 0);
     for (uint32_t v = 0; v <= mask; ++v) {
-        if (h[v] & (EC_ENT_PTR | EC_ENT_BAD)) continue; /* 0: long codeword or no match */
-        uint32_t used = 0, n = 0, e = 0;
-        while (n < EC_MULTI_MAX && used < W) {
-            const uint32_t ent = h[(v << used) & mask];
-            if (ent & (EC_ENT_PTR | EC_ENT_BAD)) break;
-            const uint32_t len = (ent >> 16) & 31;
-            if (used + len > W) break;
-            e |= ((ent & 0xFFFFu) >> 7) << (8 * n);
-            ++n;
-            used += len;
+        const uint32_t a = h[v];
+        if (a & (EC_ENT_PTR | EC_ENT_BAD)) continue; /* 0: long codeword or no match */
+        const uint32_t l0 = (a >> 16) & 31, e0 = (a & 0xFFFFu) >> 7;
+        uint32_t ent = (e0 << 7) | (l0 << EC_PAIR_FIRST_SHIFT);
+        if (l0 < W) {
+            const uint32_t b = h[(v << l0) & mask];
+            const uint32_t l1 = (b >> 16) & 31;
+            if (!(b & (EC_ENT_PTR | EC_ENT_BAD)) && l0 + l1 <= W)
+                ent |= (((b & 0xFFFFu) >> 7) << 23) | (l0 + l1);
         }
-        t[v] = e | (n << 24) | (used << 28);
+        t[v] = ent;
     }
     return t;
 }
@@ -369,7 +369,7 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
     if (!out) return EC_ERR_INVALID_ARG;
     *out = nullptr;
     if (n_rows < 0 || k_cols < 0) return EC_ERR_SHAPE;
-    const int max_len = params ? params->max_code_len : EC_MAX_CODE_LEN;
+    const int max_len = params ? params->max_code_len : EC_DEFAULT_MAX_CODE_LEN;
     const int steps = params ? params->tile_steps : 128;
     if (max_len < 1 || max_len > EC_MAX_CODE_LEN) return EC_ERR_INVALID_ARG;
     if (steps != 32 && steps != 64 && steps != 128) return EC_ERR_INVALID_ARG;
@@ -413,7 +413,7 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
         }
         uint32_t code[256];
         canonical(m->lengths, code);
-        std::vector<uint32_t> table = build_multi_table(build_huff_table(m->lengths, code));
+        std::vector<uint32_t> table = build_pair_table(build_huff_table(m->lengths, code));
         {
             const std::vector<uint32_t> hier = build_huff_table(m->lengths, code);
             table.insert(table.end(), hier.begin(), hier.end());
@@ -756,8 +756,8 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
     if (h.table_off != (int64_t)sizeof(ec_blob_header)) return EC_ERR_CORRUPT;
     int64_t end = 0, t4 = 0;
     if (huff) {
-        if (h.table_words < EC_MULTI_WORDS + (1 << EC_L1_BITS) ||
-            (h.table_words - EC_MULTI_WORDS - (1 << EC_L1_BITS)) % 256)
+        if (h.table_words < EC_PAIR_WORDS + (1 << EC_L1_BITS) ||
+            (h.table_words - EC_PAIR_WORDS - (1 << EC_L1_BITS)) % 256)
             return EC_ERR_CORRUPT;
         if (h.max_len < 0 || h.max_len > EC_MAX_CODE_LEN || h.max_code_bytes < 0) return EC_ERR_CORRUPT;
     } else {
@@ -793,13 +793,13 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
     }
     const uint32_t* tab = (const uint32_t*)(b + h.table_off);
     if (huff) {
-        const int64_t n_sub = (h.table_words - EC_MULTI_WORDS - (1 << EC_L1_BITS)) / 256;
-        for (int64_t i = 0; i < EC_MULTI_WORDS; ++i) { /* multi-symbol entries */
-            const uint32_t e = tab[i], n = (e >> 24) & 3u, len = e >> 28;
-            if (e == 0) continue;
-            if (n < 1 || len < n || len > EC_L1_BITS || (e & 0x0C000000u)) return EC_ERR_CORRUPT;
+        const int64_t n_sub = (h.table_words - EC_PAIR_WORDS - (1 << EC_L1_BITS)) / 256;
+        for (int64_t i = 0; i < EC_PAIR_WORDS; ++i) { /* pair entries */
+            const uint32_t e = tab[i], n = e & EC_PAIR_LEN_MASK, l0 = (e >> EC_PAIR_FIRST_SHIFT) & 15u;
+            if ((e & ~EC_PAIR_FIELDS) || l0 > EC_L1_BITS || n > EC_L1_BITS) return EC_ERR_CORRUPT;
+            if (n ? (l0 == 0 || n <= l0) : (e >> 23) != 0) return EC_ERR_CORRUPT;
         }
-        for (int64_t i = EC_MULTI_WORDS; i < h.table_words; ++i)
+        for (int64_t i = EC_PAIR_WORDS; i < h.table_words; ++i)
             if ((tab[i] & EC_ENT_PTR) && (int64_t)(tab[i] & 0xFFFFu) >= n_sub) return EC_ERR_CORRUPT;
     } else {
         for (int64_t i = 0; i < h.table_words; ++i) {

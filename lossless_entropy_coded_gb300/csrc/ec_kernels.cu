@@ -145,34 +145,42 @@ __device__ __forceinline__ int64_t tile_row(int64_t t, int64_t T, int64_t kp, in
 /* ============================================================ Huffman path */
 /*
  * Work layout.  One warp decodes one tile at a time; lane l owns the tile's
- * symbols i = 0 .. S-1 at positions 32 i + l and, unlike a DFloat11 thread that
- * hands its output to a block-wide write buffer, lane l also multiplies them:
- * exponents go to a lane-private byte stage in shared memory (two buffers of
- * kC symbols + spill, lane stride kLane = 11 words so the 32 lanes' stores and
- * 4-byte reads fall in distinct banks), the matching raw bytes arrive
- * lane-transposed with one 16-byte load per 16 symbols, and x is kept transposed
- * in shared memory (xs_t[l][j] = x[32 j + l]) so lane l finds x for its symbols
- * contiguously.  Decoding chunk c + 1 is interleaved with the multiply-accumulate
- * of chunk c.
+ * symbols i = 0 .. S-1 at positions 32 i + l.  Each lookup of the pair table
+ * (shared memory, indexed by the next EC_L1_BITS bits of the lane's stream)
+ * yields exactly two exponents, already sitting in the BF16 exponent fields of a
+ * 32-bit word [w(i+1) | w(i)].  With a fixed two symbols per lookup the decoded
+ * exponents stay in registers at compile-time positions: one byte permute and one
+ * bitwise select merge them with the raw sign/mantissa bytes
+ *     bf16 = (sign << 15) | (exponent << 7) | mantissa     (DFloat11 Algorithm 1)
+ * and the pair goes straight into the FP32 multiply-accumulate (GEMV) or to the
+ * output (decode).  A window whose two codewords do not both fit takes a second
+ * lookup for the second one (about 0.5% of lookups for LLM exponent statistics),
+ * and a codeword longer than the window walks the hierarchical table in global
+ * memory.
+ *
+ * Streams per warp: the lane starts and code area of the warp's next tile are
+ * copied with cp.async into the second of two shared-memory buffers while the
+ * current tile is decoded from the first; the raw bytes arrive with one
+ * coalesced 16-byte load per lane per 16 symbols, two blocks ahead of use and
+ * continuing into the next tile; x sits transposed in shared memory
+ * (xs_t[l][j] = x[32 j + l]) so lane l finds x for its symbols contiguously.
  */
-constexpr int kHW = 24;                        /* max warps per CTA */
-constexpr int kC = 32;                         /* symbols per lane per chunk */
-constexpr int kLane = 44;                      /* stage bytes per lane per buffer (11 words) */
-constexpr int kStageBuf = 32 * kLane;          /* one buffer of the warp */
-constexpr int kStageBytes = 2 * kStageBuf;     /* two buffers */
-constexpr int kSlackPairs = 32;                /* zero pairs after the code area (even) */
-constexpr uint32_t kMultiBytes = 4u * EC_MULTI_WORDS;
-static_assert(kLane >= kC + 8 && kLane % 4 == 0 && (kLane / 4) % 2 == 1, "stage lane stride");
+constexpr int kMaxHW = 32;                     /* max warps per CTA */
+constexpr int kSlackBytes = 64;                /* after a code area: reads run <= 8 steps x 48 bits + 8 bytes past it */
+constexpr uint32_t kPairTabBytes = 4u * EC_PAIR_WORDS;
+constexpr uint32_t kSignMant = 0x807F807Fu;    /* sign and mantissa bits of two BF16 */
+
+__host__ __device__ constexpr int huff_max_warps(int b) { return b <= 2 ? 32 : (b <= 4 ? 24 : 16); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ uint2 lds64(uint32_t a) {
-    uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
-    return v;
-}
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
     uint32_t v;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
     return v;
 }
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
@@ -180,21 +188,19 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
     return v;
 }
-__device__ __forceinline__ void sts8(uint32_t a, uint32_t v) {
-    asm volatile("st.shared.u8 [%0], %1;" ::"r"(a), "r"(v) : "memory");
-}
 __device__ __forceinline__ void sts16(uint32_t a, uint32_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"((unsigned short)v) : "memory");
 }
-__device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
-    asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-/* Codeword longer than the level-1 window (rare): walk the hierarchical table in
- * global memory from its level-1 entry for this window.  Returns the exponent with
- * a count of 1 in the multi-entry layout (.x) and the codeword length (.y, up to
- * 24 bits, which the 4-bit length field of a multi entry cannot hold).  Corrupt
- * data (no codeword matches) yields exponent 0 of length 1 and sets the status. */
+/* Codeword longer than the pair-table window (rare): walk the hierarchical table
+ * in global memory from its level-1 entry for this window.  Returns the exponent
+ * (.x) and the codeword length (.y, up to 24 bits).  Corrupt data (no codeword
+ * matches) yields exponent 0 of length 1 and sets the status. */
 __device__ __noinline__ uint2 long_codeword(uint32_t win, const uint32_t* __restrict__ hier, int64_t hier_words,
                                             int* status) {
     uint32_t ent = __ldg(hier + (win >> (32 - EC_L1_BITS)));
@@ -212,65 +218,76 @@ __device__ __noinline__ uint2 long_codeword(uint32_t win, const uint32_t* __rest
         flag_corrupt(status);
         ent = 1u << 16;
     }
-    return make_uint2(((ent & 0xFFFFu) >> 7) | (1u << 24), (ent >> 16) & 31);
+    return make_uint2((ent & 0xFFFFu) >> 7, min((ent >> 16) & 31, (uint32_t)EC_MAX_CODE_LEN));
 }
 
-/* Copy a tile's code area (nw words, global) into shared memory as overlapping
- * word pairs pairs[k] = (area[k], area[k + 1]), so the 64-bit window at any word is
- * one aligned 8-byte load, followed by kSlackPairs zero pairs. */
-__device__ __forceinline__ void stage_pairs(uint2* pairs, const uint32_t* __restrict__ area, int nw, int lane) {
-    const uint4* a4 = (const uint4*)area;
-    for (int g = lane; 4 * g < nw; g += 32) {
-        const uint4 a = __ldg(a4 + g);
-        const uint32_t nx = 4 * g + 4 < nw ? __ldg(area + 4 * g + 4) : 0u;
-        uint4* d = (uint4*)(pairs + 4 * g);
-        d[0] = make_uint4(a.x, a.y, a.y, a.z);
-        d[1] = make_uint4(a.z, a.w, a.w, nx);
-    }
-    for (int k = lane; k < kSlackPairs; k += 32) pairs[nw + k] = make_uint2(0u, 0u);
-}
-
-/* One lane's decoder: bit position p in the staged code area and the shared
- * address q of its next exponent byte. */
-struct HuffLane {
-    uint32_t p, q;
+/* Per-warp decoding context: shared addresses of the pair table and the staged
+ * code area, and the launch matrix whose hierarchical table backs them up. */
+struct PairCtx {
+    uint32_t tab, area;
+    int mi;
 };
 
-/* One multi-symbol lookup: store the entry's three exponent bytes at q, q+1, q+2 and
- * advance by the codewords it holds. */
-__device__ __forceinline__ void huff_step(HuffLane& L, uint32_t l1s, uint32_t ps, const uint32_t* __restrict__ hier,
-                                          int64_t hier_words, int* status) {
-    const uint2 wp = lds64(ps + ((L.p >> 5) << 3));
-    const uint32_t win = __funnelshift_l(wp.y, wp.x, L.p);
-    uint32_t e = lds32(l1s + ((win >> (32 - EC_L1_BITS)) << 2));
-    uint32_t adv = e >> 28;
-    if (__builtin_expect(e < (1u << 28), 0)) {
-        const uint2 lc = long_codeword(win, hier, hier_words, status);
-        e = lc.x;
-        adv = lc.y;
+/* The 32 stream bits starting at bit p of the staged code area (MSB first). */
+__device__ __forceinline__ uint32_t window(uint32_t area, uint32_t p) {
+    const uint32_t a = area + ((p >> 5) << 2);
+    return __funnelshift_l(lds32(a + 4), lds32(a), p);
+}
+
+/* Decode the lane's next two symbols: returns their exponents in BF16 position
+ * [e(i+1) << 23 | e(i) << 7] (other bits unspecified) and advances p.  A window
+ * whose two codewords do not both fit takes a second lookup at the end of the
+ * first; with kLong (a launch holding codewords longer than the window) a first
+ * or second codeword the window cannot hold walks the hierarchical table.  A
+ * window no codeword matches (corrupt data) advances one bit and marks `bad`. */
+template <bool kLong, class Args>
+__device__ __forceinline__ uint32_t pair_step(uint32_t& p, uint32_t& bad, const PairCtx& c, const Args& a) {
+    const uint32_t win = window(c.area, p);
+    uint32_t e = lds32(c.tab + ((win >> (32 - EC_L1_BITS)) << 2));
+    uint32_t adv = e & EC_PAIR_LEN_MASK;
+    if (__builtin_expect(adv == 0, 0)) {
+        uint32_t l0 = (e >> EC_PAIR_FIRST_SHIFT) & 15u, x0 = (e >> 7) & 0xFFu;
+        if (kLong && l0 == 0) {
+            const HuffMat& M = a.m[c.mi];
+            const uint2 lc = long_codeword(win, M.table + EC_PAIR_WORDS, M.table_words - EC_PAIR_WORDS, a.status);
+            x0 = lc.x;
+            l0 = lc.y;
+        }
+        bad |= l0 == 0;
+        l0 = max(l0, 1u);
+        const uint32_t w1 = window(c.area, p + l0);
+        const uint32_t f = lds32(c.tab + ((w1 >> (32 - EC_L1_BITS)) << 2));
+        uint32_t l1 = (f >> EC_PAIR_FIRST_SHIFT) & 15u, x1 = (f >> 7) & 0xFFu;
+        if (kLong && l1 == 0) {
+            const HuffMat& M = a.m[c.mi];
+            const uint2 lc = long_codeword(w1, M.table + EC_PAIR_WORDS, M.table_words - EC_PAIR_WORDS, a.status);
+            x1 = lc.x;
+            l1 = lc.y;
+        }
+        bad |= l1 == 0;
+        l1 = max(l1, 1u);
+        e = (x0 << 7) | (x1 << 23);
+        adv = l0 + l1;
     }
-    sts8(L.q, e);
-    sts8(L.q + 1, e >> 8);
-    sts8(L.q + 2, e >> 16);
-    L.p += adv;
-    L.q += (e >> 24) & 3u;
+    p += adv;
+    return e;
 }
 
-/* Two BF16 weights [w1 | w0] from exponent bytes (a, a+1 of e, spread by esel) and
- * raw bytes (a, a+1 of r, duplicated by rsel):
- *     w = (sign << 15) | (exponent << 7) | mantissa. */
-__device__ __forceinline__ uint32_t merge_pair(uint32_t e, uint32_t esel, uint32_t r, uint32_t rsel) {
-    const uint32_t spread = __byte_perm(e, 0, esel); /* [0 e1 0 e0] */
-    const uint32_t dup = __byte_perm(r, 0, rsel);    /* [r1 r1 r0 r0] */
-    return spread * 128u + (dup & 0x807F807Fu);      /* fields do not overlap: + is | */
+/* Two BF16 weights [w(i+1) | w(i)]: exponents from a pair entry, sign and
+ * mantissa from raw bytes a and a + 1 of r (duplicated into both bytes of each
+ * half by sel). */
+__device__ __forceinline__ uint32_t merge2(uint32_t e, uint32_t r, uint32_t sel) {
+    return (__byte_perm(r, 0, sel) & kSignMant) | (e & ~kSignMant);
 }
 
-/* Eight weights: exponent bytes e = (e0..e3, e4..e7), raw bytes r0 (4), r1 (4). */
-__device__ __forceinline__ void merge8(uint2 e, uint32_t r0, uint32_t r1, uint32_t (&w)[4]) {
-    w[0] = merge_pair(e.x, 0x4140, r0, 0x1100);
-    w[1] = merge_pair(e.x, 0x4342, r0, 0x3322);
-    w[2] = merge_pair(e.y, 0x4140, r1, 0x1100);
-    w[3] = merge_pair(e.y, 0x4342, r1, 0x3322);
+/* Eight symbols of the lane (raw bytes r0 = symbols 0..3, r1 = 4..7). */
+template <bool kLong, class Args>
+__device__ __forceinline__ void decode8(uint32_t& p, uint32_t& bad, const PairCtx& c, const Args& a, uint32_t r0,
+                                        uint32_t r1, uint32_t (&w)[4]) {
+    w[0] = merge2(pair_step<kLong>(p, bad, c, a), r0, 0x1100);
+    w[1] = merge2(pair_step<kLong>(p, bad, c, a), r0, 0x3322);
+    w[2] = merge2(pair_step<kLong>(p, bad, c, a), r1, 0x1100);
+    w[3] = merge2(pair_step<kLong>(p, bad, c, a), r1, 0x3322);
 }
 
 /* acc += w0 * x0 + w1 * x1 for BF16 pairs w = [w1|w0], x = [x1|x0]; the products are
@@ -289,12 +306,11 @@ __device__ __forceinline__ float fma2_bf16(uint32_t w, uint32_t x, float acc) {
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
 
-/* Per-warp shared memory: stage (2 buffers x 32 lanes x kLane bytes) | code pairs +
- * slack.  Multiples of 16 bytes, so 16-byte loads and stores stay aligned. */
-__host__ __device__ constexpr size_t huff_warp_bytes(int code_bytes) {
-    return (size_t)kStageBytes + 2 * (size_t)((code_bytes + 15) & ~15) + 8 * (size_t)kSlackPairs;
-}
-static_assert(kStageBytes % 16 == 0 && (8 * kSlackPairs) % 16 == 0 && kMultiBytes % 16 == 0, "alignment");
+/* Per-warp shared memory: two tile buffers, each the 64 bytes of lane starts, the
+ * code area and slack.  Multiples of 16 bytes when code_bytes is. */
+__host__ __device__ constexpr size_t tile_buf_bytes(int code_bytes) { return 64 + (size_t)code_bytes + kSlackBytes; }
+__host__ __device__ constexpr size_t huff_warp_bytes(int code_bytes) { return 2 * tile_buf_bytes(code_bytes); }
+static_assert(kSlackBytes % 16 == 0 && kSlackBytes >= 8 * 48 / 8 + 16 && kPairTabBytes % 16 == 0, "alignment");
 static_assert(huff_warp_bytes(16) % 16 == 0 && huff_warp_bytes(4112) % 16 == 0, "per-warp block alignment");
 
 /* x for the GEMV, transposed per batch row: xs_t[b][l][j] = x[b][32 j + l], lane
@@ -303,96 +319,127 @@ static_assert(huff_warp_bytes(16) % 16 == 0 && huff_warp_bytes(4112) % 16 == 0, 
 __host__ __device__ constexpr uint32_t xs_lane_stride(uint32_t kp) { return kp / 32 + 8; }
 __host__ __device__ constexpr size_t xs_row_bytes(uint32_t kp) { return (size_t)2 * 32 * xs_lane_stride(kp); }
 
-/* Resolve tile t of matrix M.  Returns false for a record whose offsets are
- * inconsistent (status flagged, tile skipped). */
-struct TileView {
-    const uint8_t* raw;
-    const uint32_t* area;
-    int nw, S;
-    int64_t row;
-    uint32_t col0;
+/* A resolved tile record (all lanes hold the same values). */
+struct TileRef {
+    const uint8_t* rec; /* lane starts | raw | code area */
+    int64_t t;          /* tile index within its matrix */
+    int mi;             /* matrix of the launch */
+    int S;              /* symbols per lane */
+    int area;           /* code area bytes; 0 = corrupt record (skipped) */
 };
 
 template <class Args>
-__device__ __forceinline__ bool tile_view(const Args& a, const HuffMat& M, int64_t t, int lane, TileView& v) {
-    const int64_t kp = M.k_pad;
+__device__ __forceinline__ uint2 tile_offsets(const Args& a, int64_t g) {
+    const HuffMat& M = a.m[owner(a, g)];
+    const int64_t t = g - M.tile_begin;
+    return make_uint2(__ldg(M.tile_off + t), __ldg(M.tile_off + t + 1));
+}
+
+/* Resolve combined tile g from its record offsets (16-byte units); a record whose
+ * extent is inconsistent gets area 0. */
+template <class Args>
+__device__ __forceinline__ TileRef tile_ref(const Args& a, int64_t g, uint2 off) {
+    TileRef r;
+    r.mi = owner(a, g);
+    const HuffMat& M = a.m[r.mi];
+    r.t = g - M.tile_begin;
     const int64_t T = 32 * (int64_t)M.steps;
-    const int64_t base = t * T;
-    const int64_t n_t = min(T, M.n_rows * kp - base);
-    int64_t rec_bytes = 0;
-    const uint8_t* rec = M.records + record_span(M.tile_off, t, M.records_bytes, &rec_bytes, a.status, lane);
-    const int S = (int)(n_t / 32);
-    const int raw_bytes = EC_RAW_BYTES(S);
-    int64_t area_bytes = rec_bytes - 64 - raw_bytes;
-    if (area_bytes < 16 || area_bytes > a.code_bytes) {
-        if (lane == 0) flag_corrupt(a.status);
-        return false;
+    r.S = (int)(min(T, M.n_rows * M.k_pad - r.t * T) / 32);
+    const int64_t lo = (int64_t)off.x * 16, hi = (int64_t)off.y * 16;
+    const int64_t area = hi - lo - 64 - EC_RAW_BYTES(r.S);
+    const bool ok = lo <= hi && hi <= M.records_bytes && area >= 16 && area <= a.code_bytes;
+    r.rec = M.records + (ok ? lo : 0);
+    r.area = ok ? (int)area : 0;
+    return r;
+}
+
+/* Start the copy of a tile's lane starts and code area into a tile buffer. */
+__device__ __forceinline__ void prefetch_code(uint32_t buf, const TileRef& r, int lane) {
+    if (r.area > 0) {
+        const uint8_t* area = r.rec + 64 + EC_RAW_BYTES(r.S);
+        if (lane < 4) cp_async16(buf + 16 * lane, r.rec + 16 * lane);
+        for (int i = lane; i < r.area / 16; i += 32) cp_async16(buf + 64 + 16 * i, area + 16 * i);
     }
-    v.raw = rec + 64;
-    v.area = (const uint32_t*)(rec + 64 + raw_bytes);
-    v.nw = (int)(area_bytes / 4);
-    v.S = S;
-    v.row = tile_row(t, T, kp, EC_HUFF_ROW_ALIGN);
-    v.col0 = (uint32_t)(base - v.row * kp);
-    return true;
+    cp_async_commit();
 }
 
-/* Lane start in bits, clamped to the code area (a corrupt start cannot move the
- * window reads past the zero slack). */
-__device__ __forceinline__ uint32_t lane_start_bits(const TileView& v, int lane) {
-    const uint32_t s = __ldg((const uint16_t*)(v.raw - 64) + lane);
-    return 8u * min(s, (uint32_t)(4 * v.nw));
-}
-
-/* Raw bytes of lane `lane`, symbols 16 j .. 16 j + 15 (one coalesced 16-byte load). */
-__device__ __forceinline__ uint4 raw16(const TileView& v, int j, int lane) {
-    return __ldg((const uint4*)v.raw + (32 * j + lane));
-}
-
-/* Decode the lane's next chunk (until q reaches q_end) interleaving up to four
- * multiply-accumulate sub-steps `fma(k)` of the previous chunk. */
-template <class Fma>
-__device__ __forceinline__ void huff_chunk(HuffLane& L, uint32_t q_end, int subs, uint32_t l1s, uint32_t ps,
-                                           const uint32_t* __restrict__ hier, int64_t hier_words, int* status,
-                                           Fma&& fma) {
-#pragma unroll
-    for (int k = 0; k < kC / 8; ++k) {
-        if (L.q < q_end) {
-            huff_step(L, l1s, ps, hier, hier_words, status);
-            huff_step(L, l1s, ps, hier, hier_words, status);
+/* Walk combined tiles g0, g0 + stride, ... < g_end.  The first tile's copy must
+ * already be in flight (prefetch_code).  For every tile with a sound record:
+ * begin(tile) once; then, for each block of 16 symbols of the lane, block() and
+ * two calls half(w) for its two 8-symbol halves in order (w = four words
+ * [w(i+1) | w(i)]); then end().  Rows start on block boundaries (k_pad is a
+ * multiple of 16 * 32 positions).  The raw bytes of block b + 2 are loaded right
+ * after block b is decoded, into the ring slot it frees; blocks 0 and 1 of the
+ * next tile are loaded the same way at the end of the current one. */
+template <bool kLong, class Args, class TabOf, class Begin, class Block, class Half, class End>
+__device__ __forceinline__ void huff_walk(const Args& a, int64_t g0, int64_t stride, int64_t g_end, TileRef cur,
+                                          uint32_t bufs, uint32_t buf_bytes, int lane, TabOf&& tab_of,
+                                          Begin&& begin, Block&& block, Half&& half, End&& end) {
+    uint2 off_next = g0 + stride < g_end ? tile_offsets(a, g0 + stride) : make_uint2(0u, 0u);
+    uint4 rr[2] = {};
+    bool raw_ready = false;
+    uint32_t cb = bufs; /* buffer of the current tile */
+    for (int64_t g = g0; g < g_end; g += stride) {
+        cp_async_wait_all();
+        __syncwarp(); /* the current tile's copy is visible; every lane is done with the other buffer */
+        const uint32_t nb_buf = cb == bufs ? bufs + buf_bytes : bufs; /* the next tile's buffer */
+        const bool has_next = g + stride < g_end;
+        TileRef nxt{};
+        if (has_next) {
+            nxt = tile_ref(a, g + stride, off_next);
+            prefetch_code(nb_buf, nxt, lane);
+            if (g + 2 * stride < g_end) off_next = tile_offsets(a, g + 2 * stride);
         }
-        if (k < subs) fma(k);
-    }
-#pragma unroll 1
-    while (L.q < q_end) {
-        huff_step(L, l1s, ps, hier, hier_words, status);
-        huff_step(L, l1s, ps, hier, hier_words, status);
-    }
-}
-
-/* Walk one tile: the prologue decodes chunk 0; iteration c moves chunk c's spill to
- * the other buffer and decodes chunk c + 1 there while `consume(c, k, exps)` handles
- * sub-step k (8 symbols) of chunk c. */
-template <class Consume>
-__device__ __forceinline__ void huff_tile(const TileView& v, uint32_t l1s, uint32_t ps, uint32_t stage_lane,
-                                          const uint32_t* __restrict__ hier, int64_t hier_words, int* status,
-                                          int lane, Consume&& consume) {
-    const uint32_t pmax = 32u * v.nw;
-    HuffLane L{lane_start_bits(v, lane), stage_lane};
-    const int nch = (v.S + kC - 1) / kC;
-    huff_chunk(L, stage_lane + (uint32_t)min(kC, v.S), 0, l1s, ps, hier, hier_words, status, [](int) {});
-    for (int c = 0; c < nch; ++c) {
-        const uint32_t X = stage_lane + (c & 1) * kStageBuf, Y = stage_lane + ((c + 1) & 1) * kStageBuf;
-        const int rows_c = min(kC, v.S - c * kC);
-        /* spill of chunk c (bytes kC .. kC + 7 of X) becomes the start of buffer Y */
-        sts32(Y, lds32(X + kC));
-        sts32(Y + 4, lds32(X + kC + 4));
-        L.q = L.q - X - kC + Y;
-        L.p = min(L.p, pmax);
-        const int next = min(kC, v.S - (c + 1) * kC); /* symbols of chunk c + 1 (<= 0: none) */
-        const uint32_t q_end = next > 0 ? Y + (uint32_t)next : 0u;
-        huff_chunk(L, q_end, rows_c / 8, l1s, ps, hier, hier_words, status,
-                   [&](int k) { consume(c, k, make_uint2(lds32(X + 8 * k), lds32(X + 8 * k + 4))); });
+        if (cur.area == 0) {
+            if (lane == 0) flag_corrupt(a.status);
+            raw_ready = false;
+            cur = nxt;
+            cb = nb_buf;
+            continue;
+        }
+        const uint32_t s0 = lds16(cb + 2 * lane);
+        const uint32_t s1 = lane < 31 ? lds16(cb + 2 * lane + 2) : 0u;
+        const PairCtx c{tab_of(cur.mi), cb + 64, cur.mi};
+        const uint4* raw4 = (const uint4*)(cur.rec + 64) + lane;
+        const int nb = cur.S / 16;
+        const uint32_t pmax = 8u * (uint32_t)cur.area;
+        uint32_t p = 8u * min(s0, (uint32_t)cur.area), bad = 0;
+        if (!raw_ready) {
+            rr[0] = __ldg(raw4);
+            if (nb > 1) rr[1] = __ldg(raw4 + 32);
+        }
+        /* blocks 0 and 1 of the next tile land in ring slots 0 and 1 when this
+         * tile's block count is even */
+        const bool chain = has_next && nxt.area > 0 && (nb & 1) == 0;
+        const uint4* nraw4 = (const uint4*)((chain ? nxt.rec : cur.rec) + 64) + lane;
+        const int lim = nb + (chain ? min(2, nxt.S / 16) : 0);
+        begin(cur);
+        for (int b0 = 0; b0 < nb; b0 += 2) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int blk = b0 + u;
+                if (u == 0 || blk < nb) {
+                    block();
+                    p = min(p, pmax);
+                    uint32_t w[4];
+                    decode8<kLong>(p, bad, c, a, rr[u].x, rr[u].y, w);
+                    half(w);
+                    decode8<kLong>(p, bad, c, a, rr[u].z, rr[u].w, w);
+                    half(w);
+                    const int pf = blk + 2;
+                    const uint4* src = pf < nb ? raw4 + 32 * pf : nraw4 + 32 * (pf - nb);
+                    if (pf < lim) rr[u] = __ldg(src);
+                }
+            }
+        }
+        raw_ready = chain;
+        /* every lane's codewords end in the last byte before the next lane's start
+         * (the last lane: before the >= 8 zero bytes closing the area) */
+        bad |= lane < 31 ? (p > 8u * s1 || p + 8u <= 8u * s1) : (p + 64u > pmax);
+        if (__any_sync(kFull, bad) && lane == 0) flag_corrupt(a.status);
+        end();
+        cur = nxt;
+        cb = nb_buf;
     }
 }
 
@@ -400,8 +447,8 @@ __device__ __forceinline__ void huff_tile(const TileView& v, uint32_t l1s, uint3
 /* kPart = false: row sums go to y (stored, or added atomically when a row spans
  * tiles).  kPart = true (allocation-free entry point): every row segment a tile
  * produces goes to its own slot of a.part, summed into y by part_reduce_kernel. */
-template <int B, bool kPart = false>
-__global__ void __launch_bounds__(kHW * 32, 1) huff_gemv_kernel(const __grid_constant__ HuffGemvArgs a) {
+template <int B, bool kPart, bool kLong>
+__global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(const __grid_constant__ HuffGemvArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t kp = (uint32_t)a.m[0].k_pad;
@@ -409,18 +456,23 @@ __global__ void __launch_bounds__(kHW * 32, 1) huff_gemv_kernel(const __grid_con
     const int batch = a.batch;
     const uint32_t lx = xs_lane_stride(kp);
 
-    /* shared: multi-symbol level-1 tables | x transposed [batch][32][lx] | per warp: stage, pairs */
-    uint4* l1g = (uint4*)smem;
-    uint16_t* xs = (uint16_t*)(smem + (size_t)a.count * kMultiBytes);
+    /* shared: pair tables | x transposed [batch][32][lx] | per warp: two tile buffers */
+    uint4* tabs = (uint4*)smem;
+    uint16_t* xs = (uint16_t*)(smem + (size_t)a.count * kPairTabBytes);
     uint8_t* wbase = (uint8_t*)xs + (size_t)batch * xs_row_bytes(kp) + (size_t)warp * huff_warp_bytes(a.code_bytes);
-    const uint32_t stage_lane = smem_u32(wbase) + lane * kLane;
-    uint2* pairs = (uint2*)(wbase + kStageBytes);
-    const uint32_t pairs_s = smem_u32(pairs);
-    const uint32_t xs_lane = smem_u32(xs) + lane * lx * 2;
+    const uint32_t bufs = smem_u32(wbase), buf_bytes = (uint32_t)tile_buf_bytes(a.code_bytes);
+    const uint32_t xs_lane = smem_u32(xs) + lane * lx * 2, tabs_s = smem_u32(tabs);
 
+    const int nwarp = blockDim.x >> 5;
+    const int64_t gw = (int64_t)blockIdx.x * nwarp + warp, nw = (int64_t)gridDim.x * nwarp;
+    TileRef first{};
+    if (gw < a.total_tiles) {
+        first = tile_ref(a, gw, tile_offsets(a, gw));
+        prefetch_code(bufs, first, lane);
+    }
     for (int k = 0; k < a.count; ++k) {
         const uint4* src = (const uint4*)a.m[k].table;
-        for (int i = threadIdx.x; i < EC_MULTI_WORDS / 4; i += blockDim.x) l1g[k * (EC_MULTI_WORDS / 4) + i] = __ldg(src + i);
+        for (int i = threadIdx.x; i < EC_PAIR_WORDS / 4; i += blockDim.x) tabs[k * (EC_PAIR_WORDS / 4) + i] = __ldg(src + i);
     }
     grid_dep_launch();
     grid_dep_wait(); /* x and y belong to the preceding kernel in the stream from here on */
@@ -428,100 +480,83 @@ __global__ void __launch_bounds__(kHW * 32, 1) huff_gemv_kernel(const __grid_con
         for (uint32_t c = threadIdx.x; c < kp; c += blockDim.x)
             xs[(size_t)b * 32 * lx + (c & 31) * lx + (c >> 5)] = c < K ? a.x[(int64_t)b * K + c] : (uint16_t)0;
     __syncthreads();
+    if (gw >= a.total_tiles) return;
 
-    const int nwarp = blockDim.x >> 5;
-    const int64_t gw = (int64_t)blockIdx.x * nwarp + warp, nw = (int64_t)gridDim.x * nwarp;
-    for (int64_t g = gw; g < a.total_tiles; g += nw) {
-        const int mi = owner(a, g);
-        const HuffMat& M = a.m[mi];
-        TileView v;
-        if (!tile_view(a, M, g - M.tile_begin, lane, v)) continue;
-        __syncwarp();
-        stage_pairs(pairs, v.area, v.nw, lane);
-        __syncwarp();
-        const uint32_t l1s = smem_u32(l1g + mi * (EC_MULTI_WORDS / 4));
-        int64_t row = v.row;
-        uint32_t jc = v.col0 / 32; /* x column block of the current sub-step */
-        const uint32_t jrow = kp / 32;
-        float acc[B][2];
+    const uint32_t jrow = kp / 32;
+    float acc[B][2];
+    int64_t row = 0, t_cur = 0;
+    uint32_t jc = 0; /* x column block of the current 8 symbols */
+    const HuffMat* Mp = &a.m[0];
+    auto flush = [&](int64_t r) {
+        const HuffMat& M = *Mp;
+        int64_t slot = 0;
+        if (kPart) /* tiles before this one that also cover row r */
+            slot = t_cur - (r * M.k_pad) / (32 * (int64_t)M.steps);
 #pragma unroll
-        for (int b = 0; b < B; ++b) acc[b][0] = acc[b][1] = 0.f;
-        uint4 rw[2] = {raw16(v, 0, lane), v.S > 16 ? raw16(v, 1, lane) : make_uint4(0, 0, 0, 0)};
-        uint4 rn[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-
-        const int64_t t_cur = g - M.tile_begin;
-        auto flush = [&](int64_t r) {
-            int64_t slot = 0;
-            if (kPart) /* tiles before this one that also cover row r */
-                slot = t_cur - (r * M.k_pad) / (32 * (int64_t)M.steps);
+        for (int b = 0; b < B; ++b) {
+            if (B > 1 && b >= batch) break;
+            const float s = warp_sum(acc[b][0] + acc[b][1]);
+            if (lane == 0) {
+                if (kPart) {
+                    a.part[((int64_t)b * M.n_rows + r) * a.part_slots + slot] = s;
+                } else {
+                    float* dst = M.y + (int64_t)b * M.n_rows + r;
+                    if (M.atomic_y) atomicAdd(dst, s);
+                    else *dst = s;
+                }
+            }
+            acc[b][0] = acc[b][1] = 0.f;
+        }
+    };
+    huff_walk<kLong>(
+        a, gw, nw, a.total_tiles, first, bufs, buf_bytes, lane, [&](int mi) { return tabs_s + mi * kPairTabBytes; },
+        [&](const TileRef& r) {
+            Mp = &a.m[r.mi];
+            t_cur = r.t;
+            const int64_t T = 32 * (int64_t)Mp->steps;
+            row = tile_row(r.t, T, kp, EC_HUFF_ROW_ALIGN);
+            jc = (uint32_t)(r.t * T - row * (int64_t)kp) / 32;
+#pragma unroll
+            for (int b = 0; b < B; ++b) acc[b][0] = acc[b][1] = 0.f;
+        },
+        [&]() {
+            if (jc >= jrow) {
+                flush(row);
+                jc -= jrow;
+                ++row;
+            }
+        },
+        [&](const uint32_t (&w)[4]) {
+            const uint32_t xa = xs_lane + 2 * jc;
 #pragma unroll
             for (int b = 0; b < B; ++b) {
-                if (b >= batch) break;
-                const float s = warp_sum(acc[b][0] + acc[b][1]);
-                if (lane == 0) {
-                    if (kPart) {
-                        a.part[((int64_t)b * M.n_rows + r) * a.part_slots + slot] = s;
-                    } else {
-                        float* dst = M.y + (int64_t)b * M.n_rows + r;
-                        if (M.atomic_y) atomicAdd(dst, s);
-                        else *dst = s;
-                    }
-                }
-                acc[b][0] = acc[b][1] = 0.f;
+                if (B > 1 && b >= batch) break;
+                const uint4 xv = lds128(xa + (uint32_t)(b * xs_row_bytes(kp)));
+                acc[b][0] = fma2_bf16(w[0], xv.x, acc[b][0]);
+                acc[b][1] = fma2_bf16(w[1], xv.y, acc[b][1]);
+                acc[b][0] = fma2_bf16(w[2], xv.z, acc[b][0]);
+                acc[b][1] = fma2_bf16(w[3], xv.w, acc[b][1]);
             }
-        };
-
-        huff_tile(v, l1s, pairs_s, stage_lane, M.table + EC_MULTI_WORDS, M.table_words - EC_MULTI_WORDS, a.status,
-                  lane, [&](int c, int k, const uint2& e8) {
-                      if (k == 0) { /* prefetch the next chunk's raw bytes */
-                          const int j = 2 * (c + 1);
-                          rn[0] = 16 * j < v.S ? raw16(v, j, lane) : make_uint4(0, 0, 0, 0);
-                          rn[1] = 16 * (j + 1) < v.S ? raw16(v, j + 1, lane) : make_uint4(0, 0, 0, 0);
-                      }
-                      if (jc >= jrow) {
-                          flush(row);
-                          jc -= jrow;
-                          ++row;
-                      }
-                      const uint4& r = rw[k >> 1];
-                      uint32_t w[4];
-                      merge8(e8, (k & 1) ? r.z : r.x, (k & 1) ? r.w : r.y, w);
-                      const uint32_t xa = xs_lane + 2 * jc;
-#pragma unroll
-                      for (int b = 0; b < B; ++b) {
-                          if (b >= batch) break;
-                          const uint4 xv = lds128(xa + (uint32_t)(b * xs_row_bytes(kp)));
-                          acc[b][0] = fma2_bf16(w[0], xv.x, acc[b][0]);
-                          acc[b][1] = fma2_bf16(w[1], xv.y, acc[b][1]);
-                          acc[b][0] = fma2_bf16(w[2], xv.z, acc[b][0]);
-                          acc[b][1] = fma2_bf16(w[3], xv.w, acc[b][1]);
-                      }
-                      jc += 8;
-                      if (k == kC / 8 - 1) {
-                          rw[0] = rn[0];
-                          rw[1] = rn[1];
-                      }
-                  });
-        flush(row);
-    }
+            jc += 8;
+        },
+        [&]() { flush(row); });
 }
 
 /* ====================================================== Huffman decode kernel */
 /* Each CTA owns a contiguous range of the launch's tiles; it walks the range one
- * matrix segment at a time, with that matrix's level-1 table in shared memory.
- * Lanes merge their own symbols, then the warp transposes 256 outputs through a
- * small shared buffer so the stores to out are coalesced 16-byte writes. */
+ * matrix segment at a time, with that matrix's pair table in shared memory.  The
+ * warp transposes each 256 outputs (8 symbols of 32 lanes) through a small shared
+ * buffer so the stores to out are coalesced 16-byte writes. */
 __host__ __device__ constexpr size_t decode_warp_bytes(int code_bytes) { return huff_warp_bytes(code_bytes) + 512; }
 
-__global__ void __launch_bounds__(kHW * 32, 1) huff_decode_kernel(const __grid_constant__ HuffDecodeArgs a) {
+template <bool kLong>
+__global__ void __launch_bounds__(kMaxHW * 32, 1) huff_decode_kernel(const __grid_constant__ HuffDecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint4* l1 = (uint4*)smem;
-    uint8_t* wbase = smem + kMultiBytes + (size_t)warp * decode_warp_bytes(a.code_bytes);
-    const uint32_t stage_lane = smem_u32(wbase) + lane * kLane;
-    uint2* pairs = (uint2*)(wbase + kStageBytes);
-    const uint32_t pairs_s = smem_u32(pairs), l1s = smem_u32(l1);
-    const uint32_t tbuf = smem_u32(wbase + huff_warp_bytes(a.code_bytes)); /* 256 outputs */
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+    uint4* tab = (uint4*)smem;
+    uint8_t* wbase = smem + kPairTabBytes + (size_t)warp * decode_warp_bytes(a.code_bytes);
+    const uint32_t bufs = smem_u32(wbase), buf_bytes = (uint32_t)tile_buf_bytes(a.code_bytes);
+    const uint32_t tbuf = bufs + (uint32_t)huff_warp_bytes(a.code_bytes), tab_s = smem_u32(tab);
     grid_dep_launch();
     grid_dep_wait();
 
@@ -530,59 +565,53 @@ __global__ void __launch_bounds__(kHW * 32, 1) huff_decode_kernel(const __grid_c
         const int mi = owner(a, cur);
         const HuffMat& M = a.m[mi];
         const int64_t mend = min(hi, M.tile_begin + M.n_tiles);
+        const int64_t g0 = cur + warp;
+        TileRef first{};
+        if (g0 < mend) {
+            first = tile_ref(a, g0, tile_offsets(a, g0));
+            prefetch_code(bufs, first, lane);
+        }
         __syncthreads();
         const uint4* src = (const uint4*)M.table;
-        for (int i = threadIdx.x; i < EC_MULTI_WORDS / 4; i += blockDim.x) l1[i] = __ldg(src + i);
+        for (int i = threadIdx.x; i < EC_PAIR_WORDS / 4; i += blockDim.x) tab[i] = __ldg(src + i);
         __syncthreads();
         const int64_t kp = M.k_pad, K = M.k_cols;
         const bool vec = (K % 8) == 0;
-        for (int64_t g = cur + warp; g < mend; g += (blockDim.x >> 5)) {
-            TileView v;
-            if (!tile_view(a, M, g - M.tile_begin, lane, v)) continue;
-            __syncwarp();
-            stage_pairs(pairs, v.area, v.nw, lane);
-            __syncwarp();
-            int64_t row = v.row;
-            int64_t col0 = v.col0;
-            uint4 rw[2] = {raw16(v, 0, lane), v.S > 16 ? raw16(v, 1, lane) : make_uint4(0, 0, 0, 0)};
-            uint4 rn[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-            huff_tile(v, l1s, pairs_s, stage_lane, M.table + EC_MULTI_WORDS, M.table_words - EC_MULTI_WORDS,
-                      a.status, lane, [&](int c, int k, const uint2& e8) {
-                          if (k == 0) {
-                              const int j = 2 * (c + 1);
-                              rn[0] = 16 * j < v.S ? raw16(v, j, lane) : make_uint4(0, 0, 0, 0);
-                              rn[1] = 16 * (j + 1) < v.S ? raw16(v, j + 1, lane) : make_uint4(0, 0, 0, 0);
-                          }
-                          if (col0 >= kp) {
-                              col0 -= kp;
-                              ++row;
-                          }
-                          const uint4& r = rw[k >> 1];
-                          uint32_t w[4];
-                          merge8(e8, (k & 1) ? r.z : r.x, (k & 1) ? r.w : r.y, w);
-                          /* lane's 8 outputs are positions 32 i + lane, i = 8k'..8k'+7: transpose */
-                          __syncwarp();
+        int64_t row = 0, col0 = 0;
+        if (g0 < mend)
+            huff_walk<kLong>(
+                a, g0, nwarp, mend, first, bufs, buf_bytes, lane, [&](int) { return tab_s; },
+                [&](const TileRef& r) {
+                    const int64_t T = 32 * (int64_t)M.steps;
+                    row = tile_row(r.t, T, kp, EC_HUFF_ROW_ALIGN);
+                    col0 = r.t * T - row * kp;
+                },
+                [&]() {
+                    if (col0 >= kp) {
+                        col0 -= kp;
+                        ++row;
+                    }
+                },
+                [&](const uint32_t (&w)[4]) {
+                    /* lane's 8 outputs are positions 32 i + lane, i = 8k'..8k'+7: transpose */
+                    __syncwarp();
 #pragma unroll
-                          for (int j = 0; j < 8; ++j) sts16(tbuf + 64 * j + 2 * lane, w[j >> 1] >> (16 * (j & 1)));
-                          __syncwarp();
-                          const uint4 o = lds128(tbuf + 16 * lane);
-                          const int64_t col = col0 + 8 * lane;
-                          uint16_t* dst = M.out + row * K + col;
-                          if (vec) {
-                              if (col < K) *(uint4*)dst = o;
-                          } else {
-                              const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+                    for (int j = 0; j < 8; ++j) sts16(tbuf + 64 * j + 2 * lane, w[j >> 1] >> (16 * (j & 1)));
+                    __syncwarp();
+                    const uint4 o = lds128(tbuf + 16 * lane);
+                    const int64_t col = col0 + 8 * lane;
+                    uint16_t* dst = M.out + row * K + col;
+                    if (vec) {
+                        if (col < K) *(uint4*)dst = o;
+                    } else {
+                        const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
-                              for (int j = 0; j < 8; ++j)
-                                  if (col + j < K) dst[j] = (uint16_t)(ow[j >> 1] >> (16 * (j & 1)));
-                          }
-                          col0 += 256;
-                          if (k == kC / 8 - 1) {
-                              rw[0] = rn[0];
-                              rw[1] = rn[1];
-                          }
-                      });
-        }
+                        for (int j = 0; j < 8; ++j)
+                            if (col + j < K) dst[j] = (uint16_t)(ow[j >> 1] >> (16 * (j & 1)));
+                    }
+                    col0 += 256;
+                },
+                [&]() {});
         cur = mend;
     }
 }
@@ -929,18 +958,22 @@ int grid_for(const DeviceInfo& d, int64_t work_items, int ctas_per_sm) {
     return (int)std::max<int64_t>(1, std::min(full, need));
 }
 
-template <int B>
-int launch_huff_gemv_b(const HuffGemvArgs& a, size_t smem, int grid, int block, cudaStream_t s) {
-    if (set_smem(huff_gemv_kernel<B>, smem) != EC_OK) return EC_ERR_CUDA;
-    return launch_ex(huff_gemv_kernel<B>, grid, block, smem, s, a);
+/* kPart selects the allocation-free variant, lng the kernel that walks the
+ * hierarchical table for codewords longer than the pair-table window. */
+template <int B, bool kPart>
+int launch_huff_gemv_b(const HuffGemvArgs& a, bool lng, size_t smem, int grid, int block, cudaStream_t s) {
+    auto kern = lng ? huff_gemv_kernel<B, kPart, true> : huff_gemv_kernel<B, kPart, false>;
+    if (set_smem(kern, smem) != EC_OK) return EC_ERR_CUDA;
+    return launch_ex(kern, grid, block, smem, s, a);
 }
 
-int launch_huff_gemv(const HuffGemvArgs& a, size_t smem, int grid, int block, cudaStream_t s) {
-    if (a.batch <= 1) return launch_huff_gemv_b<1>(a, smem, grid, block, s);
-    if (a.batch <= 2) return launch_huff_gemv_b<2>(a, smem, grid, block, s);
-    if (a.batch <= 4) return launch_huff_gemv_b<4>(a, smem, grid, block, s);
-    if (a.batch <= 8) return launch_huff_gemv_b<8>(a, smem, grid, block, s);
-    return launch_huff_gemv_b<16>(a, smem, grid, block, s);
+template <bool kPart>
+int launch_huff_gemv(const HuffGemvArgs& a, bool lng, size_t smem, int grid, int block, cudaStream_t s) {
+    if (a.batch <= 1) return launch_huff_gemv_b<1, kPart>(a, lng, smem, grid, block, s);
+    if (a.batch <= 2) return launch_huff_gemv_b<2, kPart>(a, lng, smem, grid, block, s);
+    if (a.batch <= 4) return launch_huff_gemv_b<4, kPart>(a, lng, smem, grid, block, s);
+    if (a.batch <= 8) return launch_huff_gemv_b<8, kPart>(a, lng, smem, grid, block, s);
+    return launch_huff_gemv_b<16, kPart>(a, lng, smem, grid, block, s);
 }
 
 template <bool G, int B>
@@ -967,10 +1000,34 @@ int rows_per_pass(int64_t k_pad, int batch, size_t budget, int elem = 4) {
 }
 
 /* ----------------------------------------------------------- Huffman GEMV */
+/* Launch shape of a Huffman GEMV: warps per CTA (as many as fit next to the pair
+ * tables and one batch row of x, capped by the kernel's register budget for the
+ * batch width), batch rows per pass, one CTA per SM at most. */
+struct GemvPlan {
+    int warps, per_pass, grid;
+    size_t fixed, xrow;
+};
+
+int plan_huff_gemv(const DeviceInfo& d, int count, int code_bytes, int64_t kp, int batch, int64_t total_tiles,
+                   GemvPlan* pl) {
+    const size_t tables = (size_t)count * kPairTabBytes, per_warp = huff_warp_bytes(code_bytes);
+    pl->xrow = xs_row_bytes((uint32_t)kp);
+    if (tables + pl->xrow + 4 * per_warp > d.smem_optin) return EC_ERR_UNSUPPORTED;
+    const int cap = huff_max_warps(batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : batch <= 8 ? 8 : 16);
+    pl->warps = (int)std::min<size_t>(cap, (d.smem_optin - tables - pl->xrow) / per_warp);
+    pl->fixed = tables + (size_t)pl->warps * per_warp;
+    pl->per_pass = (int)std::min<size_t>(batch, (d.smem_optin - pl->fixed) / pl->xrow);
+    if (pl->per_pass < 1) return EC_ERR_UNSUPPORTED;
+    pl->grid = (int)std::max<int64_t>(1, std::min<int64_t>(d.sms, (total_tiles + pl->warps - 1) / pl->warps));
+    return EC_OK;
+}
+
+
 int huff_gemv(const ec_matrix* const* Ws, int count, const uint16_t* x, float* const* ys, int batch,
               cudaStream_t s, int dev, DeviceInfo* d) {
     int64_t total = 0;
     int code_bytes = 16;
+    bool lng = false;
     HuffGemvArgs a{};
     a.count = count;
     const int64_t K = Ws[0]->hdr.k_cols, kp = Ws[0]->hdr.k_pad;
@@ -980,6 +1037,7 @@ int huff_gemv(const ec_matrix* const* Ws, int count, const uint16_t* x, float* c
         a.m[k].tile_begin = total;
         total += W->hdr.n_tiles;
         code_bytes = std::max(code_bytes, (int)W->hdr.max_code_bytes);
+        lng = lng || W->hdr.max_len > EC_L1_BITS;
         if (a.m[k].atomic_y || W->hdr.n_tiles == 0) {
             if (cudaMemsetAsync(ys[k], 0, sizeof(float) * (size_t)batch * (size_t)W->hdr.n_rows, s) != cudaSuccess)
                 return EC_ERR_CUDA;
@@ -990,23 +1048,16 @@ int huff_gemv(const ec_matrix* const* Ws, int count, const uint16_t* x, float* c
     a.status = d->status;
     a.code_bytes = code_bytes;
     if (total == 0) return EC_OK;
-    /* warps per CTA: as many as fit next to the tables and one batch row of x (>= 4) */
-    const size_t tables = (size_t)count * kMultiBytes, per_warp = huff_warp_bytes(code_bytes);
-    const size_t xrow = xs_row_bytes((uint32_t)kp);
-    if (tables + xrow + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED;
-    const int warps = (int)std::min<size_t>(kHW, (d->smem_optin - tables - xrow) / per_warp);
-    const size_t fixed = tables + (size_t)warps * per_warp;
-    const int per_pass = (int)std::min<size_t>(batch, (d->smem_optin - fixed) / xrow);
-    if (per_pass < 1) return EC_ERR_UNSUPPORTED;
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(d->sms, (total + warps - 1) / warps));
-    for (int b0 = 0; b0 < batch; b0 += per_pass) {
-        const int nb = std::min(per_pass, batch - b0);
+    GemvPlan pl;
+    int rc = plan_huff_gemv(*d, count, code_bytes, kp, batch, total, &pl);
+    if (rc != EC_OK) return rc;
+    for (int b0 = 0; b0 < batch; b0 += pl.per_pass) {
+        const int nb = std::min(pl.per_pass, batch - b0);
         a.batch = nb;
         a.x = x + (int64_t)b0 * K;
         for (int k = 0; k < count; ++k) a.m[k].y = ys[k] + (int64_t)b0 * Ws[k]->hdr.n_rows;
-        const size_t smem = fixed + xrow * nb;
-        const int rc = launch_huff_gemv(a, smem, grid, warps * 32, s);
-        if (rc != EC_OK) return rc;
+        if ((rc = launch_huff_gemv<false>(a, lng, pl.fixed + pl.xrow * nb, pl.grid, pl.warps * 32, s)) != EC_OK)
+            return rc;
     }
     return EC_OK;
 }
@@ -1099,22 +1150,6 @@ int static_device(int dev, StaticDevice** out) {
     return EC_OK;
 }
 
-template <int B>
-int launch_huff_gemv_part_b(const HuffGemvArgs& a, size_t smem, int grid, int block, cudaStream_t s) {
-    if (cudaFuncSetAttribute(huff_gemv_kernel<B, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-        return EC_ERR_CUDA;
-    return launch_ex(huff_gemv_kernel<B, true>, grid, block, smem, s, a);
-}
-
-int launch_huff_gemv_part(const HuffGemvArgs& a, size_t smem, int grid, int block, cudaStream_t s) {
-    if (a.batch <= 1) return launch_huff_gemv_part_b<1>(a, smem, grid, block, s);
-    if (a.batch <= 2) return launch_huff_gemv_part_b<2>(a, smem, grid, block, s);
-    if (a.batch <= 4) return launch_huff_gemv_part_b<4>(a, smem, grid, block, s);
-    if (a.batch <= 8) return launch_huff_gemv_part_b<8>(a, smem, grid, block, s);
-    return launch_huff_gemv_part_b<16>(a, smem, grid, block, s);
-}
-
 }  // namespace
 
 /* ================================================================ C ABI */
@@ -1157,6 +1192,7 @@ extern "C" int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs
     HuffDecodeArgs a{};
     int64_t total = 0;
     int code_bytes = 16;
+    bool lng = false;
     for (int k = 0; k < count; ++k) {
         if ((rc = check_matrix(Ws[k], dev)) != EC_OK) return rc;
         const int64_t n = Ws[k]->hdr.n_rows * Ws[k]->hdr.k_cols;
@@ -1170,6 +1206,7 @@ extern "C" int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs
         m.tile_begin = total;
         total += Ws[k]->hdr.n_tiles;
         code_bytes = std::max(code_bytes, (int)Ws[k]->hdr.max_code_bytes);
+        lng = lng || Ws[k]->hdr.max_len > EC_L1_BITS;
         a.m[a.count++] = m;
     }
     if (a.count == 0 || total == 0) return EC_OK;
@@ -1178,12 +1215,13 @@ extern "C" int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs
     a.status = d->status;
     a.code_bytes = code_bytes;
     const size_t per_warp = decode_warp_bytes(code_bytes);
-    if (kMultiBytes + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED;
-    const int warps = (int)std::min<size_t>(kHW, (d->smem_optin - kMultiBytes) / per_warp);
-    const size_t smem = kMultiBytes + (size_t)warps * per_warp;
-    if (set_smem(huff_decode_kernel, smem) != EC_OK) return EC_ERR_CUDA;
+    if (kPairTabBytes + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED;
+    const int warps = (int)std::min<size_t>(kMaxHW, (d->smem_optin - kPairTabBytes) / per_warp);
+    const size_t smem = kPairTabBytes + (size_t)warps * per_warp;
+    auto kern = lng ? huff_decode_kernel<true> : huff_decode_kernel<false>;
+    if (set_smem(kern, smem) != EC_OK) return EC_ERR_CUDA;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(d->sms, (total + warps - 1) / warps));
-    return launch_ex(huff_decode_kernel, grid, warps * 32, smem, stream, a);
+    return launch_ex(kern, grid, warps * 32, smem, stream, a);
 }
 
 extern "C" int ec_decode(const ec_matrix* W, uint16_t* out, cudaStream_t stream) {
@@ -1273,18 +1311,18 @@ extern "C" int ec_gemv_static(const ec_matrix* W, const uint16_t* x, float* y, i
     a.part_slots = (int)slots;
     if (a.code_bytes < 16) a.code_bytes = 16;
     if (cudaMemsetAsync(d->scratch, 0, sizeof(int), stream) != cudaSuccess) return EC_ERR_CUDA;
-    const size_t tables = kMultiBytes, per_warp = huff_warp_bytes(a.code_bytes);
-    const size_t xrow = xs_row_bytes((uint32_t)h.k_pad);
-    if (tables + xrow + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED;
-    const int warps = (int)std::min<size_t>(kHW, (d->smem_optin - tables - xrow) / per_warp);
-    const size_t fixed = tables + (size_t)warps * per_warp;
-    const int per_pass = (int)std::min<size_t>(batch, (d->smem_optin - fixed) / xrow);
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(d->sms, (h.n_tiles + warps - 1) / warps));
-    for (int b0 = 0; b0 < batch; b0 += per_pass) {
-        const int nb = std::min(per_pass, batch - b0);
+    GemvPlan pl;
+    DeviceInfo di{};
+    di.sms = d->sms;
+    di.smem_optin = d->smem_optin;
+    if ((rc = plan_huff_gemv(di, 1, a.code_bytes, h.k_pad, batch, h.n_tiles, &pl)) != EC_OK) return rc;
+    for (int b0 = 0; b0 < batch; b0 += pl.per_pass) {
+        const int nb = std::min(pl.per_pass, batch - b0);
         a.batch = nb;
         a.x = x + (int64_t)b0 * h.k_cols;
-        if ((rc = launch_huff_gemv_part(a, fixed + xrow * nb, grid, warps * 32, stream)) != EC_OK) return rc;
+        if ((rc = launch_huff_gemv<true>(a, h.max_len > EC_L1_BITS, pl.fixed + pl.xrow * nb, pl.grid, pl.warps * 32,
+                                         stream)) != EC_OK)
+            return rc;
         const int64_t n = (int64_t)nb * h.n_rows;
         part_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(a.part, a.part_slots, h.n_rows, h.k_pad,
                                                                            T, nb, y + (int64_t)b0 * h.n_rows);

@@ -135,6 +135,92 @@ def read_huffman(blob: bytes, lengths: np.ndarray) -> np.ndarray:
     return flat.reshape(n, kp)[:, :k]
 
 
+def walk_pair_table(blob: bytes):
+    """Decode a Huffman blob the way a GPU lane does: two exponents per lookup of
+    the pair table, a second lookup when only the first codeword fits, and the
+    hierarchical table for codewords longer than the window.  Returns the
+    exponent of every padded position and whether every lane ended in the last
+    byte before the next lane's start."""
+    h, dev = parse(blob)
+    tab = np.frombuffer(dev, np.uint32, h["table_words"], h["table_off"])
+    pair, hier = tab[:4096], tab[4096:]
+    T = 32 * h["steps"]
+    n_pad = h["n_rows"] * h["k_pad"]
+    toff = np.frombuffer(dev, np.uint32, h["n_tiles"] + 1, h["tile_off_off"])
+    exps = np.zeros(n_pad, np.int64)
+    ends_ok = True
+
+    def one(bits, p):  # hierarchical walk for one codeword
+        win = int(bits[p:p + 32], 2)
+        ent = int(hier[win >> 20])
+        while ent & 0x80000000:
+            used = (ent >> 16) & 31
+            ent = int(hier[4096 + (ent & 0xFFFF) * 256 + (((win << used) & 0xFFFFFFFF) >> 24)])
+        assert not ent & 0x40000000
+        return (ent & 0xFFFF) >> 7, (ent >> 16) & 31
+
+    for t in range(h["n_tiles"]):
+        rec = h["records_off"] + int(toff[t]) * 16
+        S = min(T, n_pad - t * T) // 32
+        start = np.frombuffer(dev, np.uint16, 32, rec)
+        area_off = rec + 64 + 32 * ((S + 15) // 16 * 16)
+        area_end = h["records_off"] + int(toff[t + 1]) * 16
+        words = np.frombuffer(dev, np.uint32, (area_end - area_off) // 4, area_off)
+        bits = "".join(format(int(x), "032b") for x in words) + "0" * 64
+        for l in range(32):
+            p = 8 * int(start[l])
+            for s in range(S // 2):
+                e = int(pair[int(bits[p:p + 12], 2)])
+                if e & 15:
+                    x0, x1, adv = (e >> 7) & 255, (e >> 23) & 255, e & 15
+                else:
+                    l0 = (e >> 16) & 15
+                    x0, l0 = ((e >> 7) & 255, l0) if l0 else one(bits, p)
+                    f = int(pair[int(bits[p + l0:p + l0 + 12], 2)])
+                    l1 = (f >> 16) & 15
+                    x1, l1 = ((f >> 7) & 255, l1) if l1 else one(bits, p + l0)
+                    adv = l0 + l1
+                exps[t * T + 32 * (2 * s) + l] = x0
+                exps[t * T + 32 * (2 * s + 1) + l] = x1
+                p += adv
+            if l < 31:
+                ends_ok &= 8 * int(start[l + 1]) - 8 < p <= 8 * int(start[l + 1])
+            else:
+                ends_ok &= p + 64 <= 32 * len(words)
+    return exps, ends_ok
+
+
+@pytest.mark.parametrize("case", ["llama", "fib24", "fib12", "one_symbol", "all_patterns"])
+def test_pair_table_walk_decodes_exponents(ec, case):
+    if case == "llama":
+        w = synth.llama_bf16(2010, 24, 2048)
+        W = ec.encode_bf16(w, device=-1)
+    elif case.startswith("fib"):
+        fib = [1, 1]
+        while len(fib) < 30:
+            fib.append(fib[-1] + fib[-2])
+        e = np.concatenate([np.full(f, 100 + i) for i, f in enumerate(fib)])[: 64 * 4096]
+        rng = np.random.default_rng(1)
+        rng.shuffle(e)
+        w = ((e.astype(np.uint16) << 7) | (np.arange(e.size) % 128).astype(np.uint16)).reshape(-1, 4096)[:8]
+        W = ec.encode_bf16(w, max_code_len=int(case[3:]), device=-1)
+        # L=24: codewords longer than the window reach the hierarchical table;
+        # L=12: the longest codeword fills the window exactly
+        assert W.code_lengths().max() > 12 if case == "fib24" else W.code_lengths().max() == 12
+    elif case == "one_symbol":
+        w = np.full((3, 512), 0x3F80, np.uint16)
+        W = ec.encode_bf16(w, device=-1)
+    else:
+        w = np.arange(65536, dtype=np.uint16).reshape(256, 256)
+        W = ec.encode_bf16(w, device=-1)
+    exps, ends_ok = walk_pair_table(W.serialize())
+    kp = W.stats()["k_pad"]
+    want = np.zeros((w.shape[0], kp), np.int64)
+    want[:, : w.shape[1]] = (w >> 7) & 0xFF
+    assert np.array_equal(exps.reshape(w.shape[0], kp), want)
+    assert ends_ok
+
+
 @pytest.mark.parametrize("shape,steps", [((7, 13), 128), ((3, 300), 32), ((40, 1024), 64), ((2, 4097), 128)])
 def test_huffman_blob_reads_back(ec, shape, steps):
     w = synth.llama_bf16(2007, *shape)
@@ -144,7 +230,7 @@ def test_huffman_blob_reads_back(ec, shape, steps):
 
 
 def test_all_bf16_patterns_blob_reads_back(ec):
-    w = np.arange(65536, dtype=np.uint16).reshape(256, 256)
+    w = np.arange(65536, dtype=np.uint16).reshape(128, 512)  # k_pad = K: no padding, uniform histogram
     W = ec.encode_bf16(w, device=-1)
     assert (W.code_lengths() == 8).all()
     assert np.array_equal(read_huffman(W.serialize(), W.code_lengths()), w)
@@ -158,7 +244,7 @@ def test_code_lengths_match_oracle(ec, seed):
     counts = np.floor(2.0 ** rng.uniform(0, 15, n)).astype(np.int64) + 1  # skewed, deep trees
     e = np.repeat(exps, counts)
     w = (e.astype(np.uint16) << 7) | (np.arange(e.size) % 128).astype(np.uint16)
-    k = 256
+    k = 512  # a multiple of the row alignment: no padding columns
     rows = (w.size + k - 1) // k
     pad = rows * k - w.size
     # pad with an exponent already present so the histogram matches the oracle's
