@@ -234,17 +234,47 @@ __device__ __forceinline__ uint32_t window(uint32_t area, uint32_t p) {
     return __funnelshift_l(lds32(a + 4), lds32(a), p);
 }
 
+/* A lane's read position: bit p of the staged code area, and the area words
+ * k = p / 32 (lo) and k + 1 (hi) that hold the 32 bits starting at p. */
+struct LaneBits {
+    uint32_t p, k, lo, hi;
+};
+
+__device__ __forceinline__ void bits_seek(LaneBits& s, uint32_t area, uint32_t p) {
+    s.p = p;
+    s.k = p >> 5;
+    const uint32_t a = area + (s.k << 2);
+    s.lo = lds32(a);
+    s.hi = lds32(a + 4);
+}
+
+/* Advance by adv <= 32 bits: the word index moves by at most one, so lo takes
+ * the old hi and only hi is loaded, and only by lanes that crossed a word. */
+__device__ __forceinline__ void bits_step(LaneBits& s, uint32_t area, uint32_t adv) {
+    s.p += adv;
+    const uint32_t k2 = s.p >> 5;
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.u32 q, %2, %3;\n\t"
+        "@q mov.b32 %0, %1;\n\t"
+        "@q ld.shared.u32 %1, [%4];\n\t}"
+        : "+r"(s.lo), "+r"(s.hi)
+        : "r"(k2), "r"(s.k), "r"(area + (k2 << 2) + 4)
+        : "memory");
+    s.k = k2;
+}
+
 /* Decode the lane's next two symbols: returns their exponents in BF16 position
- * [e(i+1) << 23 | e(i) << 7] (other bits unspecified) and advances p.  A window
- * whose two codewords do not both fit takes a second lookup at the end of the
- * first; with kLong (a launch holding codewords longer than the window) a first
- * or second codeword the window cannot hold walks the hierarchical table.  A
- * window no codeword matches (corrupt data) advances one bit and marks `bad`. */
+ * [e(i+1) << 23 | e(i) << 7] (other bits unspecified) and advances the lane.  A
+ * window whose two codewords do not both fit takes a second lookup at the end of
+ * the first; with kLong (a launch holding codewords longer than the window) a
+ * first or second codeword the window cannot hold walks the hierarchical table.
+ * A window no codeword matches (corrupt data) advances one bit and marks `bad`. */
 template <bool kLong, class Args>
-__device__ __forceinline__ uint32_t pair_step(uint32_t& p, uint32_t& bad, const PairCtx& c, const Args& a) {
-    const uint32_t win = window(c.area, p);
+__device__ __forceinline__ uint32_t pair_step(LaneBits& s, uint32_t& bad, const PairCtx& c, const Args& a) {
+    const uint32_t win = __funnelshift_l(s.hi, s.lo, s.p);
     uint32_t e = lds32(c.tab + ((win >> (32 - EC_L1_BITS)) << 2));
-    uint32_t adv = e & EC_PAIR_LEN_MASK;
+    const uint32_t adv = e & EC_PAIR_LEN_MASK;
     if (__builtin_expect(adv == 0, 0)) {
         uint32_t l0 = (e >> EC_PAIR_FIRST_SHIFT) & 15u, x0 = (e >> 7) & 0xFFu;
         if (kLong && l0 == 0) {
@@ -255,7 +285,7 @@ __device__ __forceinline__ uint32_t pair_step(uint32_t& p, uint32_t& bad, const 
         }
         bad |= l0 == 0;
         l0 = max(l0, 1u);
-        const uint32_t w1 = window(c.area, p + l0);
+        const uint32_t w1 = window(c.area, s.p + l0);
         const uint32_t f = lds32(c.tab + ((w1 >> (32 - EC_L1_BITS)) << 2));
         uint32_t l1 = (f >> EC_PAIR_FIRST_SHIFT) & 15u, x1 = (f >> 7) & 0xFFu;
         if (kLong && l1 == 0) {
@@ -267,9 +297,10 @@ __device__ __forceinline__ uint32_t pair_step(uint32_t& p, uint32_t& bad, const 
         bad |= l1 == 0;
         l1 = max(l1, 1u);
         e = (x0 << 7) | (x1 << 23);
-        adv = l0 + l1;
+        bits_seek(s, c.area, s.p + l0 + l1);
+    } else {
+        bits_step(s, c.area, adv);
     }
-    p += adv;
     return e;
 }
 
@@ -282,12 +313,12 @@ __device__ __forceinline__ uint32_t merge2(uint32_t e, uint32_t r, uint32_t sel)
 
 /* Eight symbols of the lane (raw bytes r0 = symbols 0..3, r1 = 4..7). */
 template <bool kLong, class Args>
-__device__ __forceinline__ void decode8(uint32_t& p, uint32_t& bad, const PairCtx& c, const Args& a, uint32_t r0,
+__device__ __forceinline__ void decode8(LaneBits& s, uint32_t& bad, const PairCtx& c, const Args& a, uint32_t r0,
                                         uint32_t r1, uint32_t (&w)[4]) {
-    w[0] = merge2(pair_step<kLong>(p, bad, c, a), r0, 0x1100);
-    w[1] = merge2(pair_step<kLong>(p, bad, c, a), r0, 0x3322);
-    w[2] = merge2(pair_step<kLong>(p, bad, c, a), r1, 0x1100);
-    w[3] = merge2(pair_step<kLong>(p, bad, c, a), r1, 0x3322);
+    w[0] = merge2(pair_step<kLong>(s, bad, c, a), r0, 0x1100);
+    w[1] = merge2(pair_step<kLong>(s, bad, c, a), r0, 0x3322);
+    w[2] = merge2(pair_step<kLong>(s, bad, c, a), r1, 0x1100);
+    w[3] = merge2(pair_step<kLong>(s, bad, c, a), r1, 0x3322);
 }
 
 /* acc += w0 * x0 + w1 * x1 for BF16 pairs w = [w1|w0], x = [x1|x0]; the products are
@@ -403,7 +434,9 @@ __device__ __forceinline__ void huff_walk(const Args& a, int64_t g0, int64_t str
         const uint4* raw4 = (const uint4*)(cur.rec + 64) + lane;
         const int nb = cur.S / 16;
         const uint32_t pmax = 8u * (uint32_t)cur.area;
-        uint32_t p = 8u * min(s0, (uint32_t)cur.area), bad = 0;
+        uint32_t bad = 0;
+        LaneBits s;
+        bits_seek(s, c.area, 8u * min(s0, (uint32_t)cur.area));
         if (!raw_ready) {
             rr[0] = __ldg(raw4);
             if (nb > 1) rr[1] = __ldg(raw4 + 32);
@@ -420,11 +453,11 @@ __device__ __forceinline__ void huff_walk(const Args& a, int64_t g0, int64_t str
                 const int blk = b0 + u;
                 if (u == 0 || blk < nb) {
                     block();
-                    p = min(p, pmax);
+                    if (__builtin_expect(s.p > pmax, 0)) bits_seek(s, c.area, pmax); /* corrupt data only */
                     uint32_t w[4];
-                    decode8<kLong>(p, bad, c, a, rr[u].x, rr[u].y, w);
+                    decode8<kLong>(s, bad, c, a, rr[u].x, rr[u].y, w);
                     half(w);
-                    decode8<kLong>(p, bad, c, a, rr[u].z, rr[u].w, w);
+                    decode8<kLong>(s, bad, c, a, rr[u].z, rr[u].w, w);
                     half(w);
                     const int pf = blk + 2;
                     const uint4* src = pf < nb ? raw4 + 32 * pf : nraw4 + 32 * (pf - nb);
@@ -435,6 +468,7 @@ __device__ __forceinline__ void huff_walk(const Args& a, int64_t g0, int64_t str
         raw_ready = chain;
         /* every lane's codewords end in the last byte before the next lane's start
          * (the last lane: before the >= 8 zero bytes closing the area) */
+        const uint32_t p = s.p;
         bad |= lane < 31 ? (p > 8u * s1 || p + 8u <= 8u * s1) : (p + 64u > pmax);
         if (__any_sync(kFull, bad) && lane == 0) flag_corrupt(a.status);
         end();
@@ -484,9 +518,21 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
 
     const uint32_t jrow = kp / 32;
     float acc[B][2];
+    /* x of the current 8 symbols: loaded one half-block ahead for narrow batches,
+     * at use for wide ones (whose registers go to the accumulators) */
+    constexpr bool kAhead = B <= 4;
+    uint4 xv[kAhead ? B : 1];
     int64_t row = 0, t_cur = 0;
     uint32_t jc = 0; /* x column block of the current 8 symbols */
     const HuffMat* Mp = &a.m[0];
+    auto load_x = [&](uint32_t j) {
+        const uint32_t xa = xs_lane + 2 * j;
+#pragma unroll
+        for (int b = 0; b < (kAhead ? B : 0); ++b) {
+            if (B > 1 && b >= batch) break;
+            xv[b] = lds128(xa + (uint32_t)(b * xs_row_bytes(kp)));
+        }
+    };
     auto flush = [&](int64_t r) {
         const HuffMat& M = *Mp;
         int64_t slot = 0;
@@ -516,6 +562,7 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
             const int64_t T = 32 * (int64_t)Mp->steps;
             row = tile_row(r.t, T, kp, EC_HUFF_ROW_ALIGN);
             jc = (uint32_t)(r.t * T - row * (int64_t)kp) / 32;
+            if (kAhead) load_x(jc);
 #pragma unroll
             for (int b = 0; b < B; ++b) acc[b][0] = acc[b][1] = 0.f;
         },
@@ -527,17 +574,17 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
             }
         },
         [&](const uint32_t (&w)[4]) {
-            const uint32_t xa = xs_lane + 2 * jc;
 #pragma unroll
             for (int b = 0; b < B; ++b) {
                 if (B > 1 && b >= batch) break;
-                const uint4 xv = lds128(xa + (uint32_t)(b * xs_row_bytes(kp)));
-                acc[b][0] = fma2_bf16(w[0], xv.x, acc[b][0]);
-                acc[b][1] = fma2_bf16(w[1], xv.y, acc[b][1]);
-                acc[b][0] = fma2_bf16(w[2], xv.z, acc[b][0]);
-                acc[b][1] = fma2_bf16(w[3], xv.w, acc[b][1]);
+                const uint4 x4 = kAhead ? xv[b] : lds128(xs_lane + 2 * jc + (uint32_t)(b * xs_row_bytes(kp)));
+                acc[b][0] = fma2_bf16(w[0], x4.x, acc[b][0]);
+                acc[b][1] = fma2_bf16(w[1], x4.y, acc[b][1]);
+                acc[b][0] = fma2_bf16(w[2], x4.z, acc[b][0]);
+                acc[b][1] = fma2_bf16(w[3], x4.w, acc[b][1]);
             }
             jc += 8;
+            if (kAhead) load_x(jc >= jrow ? jc - jrow : jc); /* the next half starts a new row there */
         },
         [&]() { flush(row); });
 }
