@@ -249,7 +249,9 @@ __device__ __forceinline__ void bits_seek(LaneBits& s, uint32_t area, uint32_t p
 }
 
 /* Advance by adv <= 32 bits: the word index moves by at most one, so lo takes
- * the old hi and only hi is loaded, and only by lanes that crossed a word. */
+ * the old hi and only hi is loaded, and only by lanes that crossed a word.
+ * (The per-block clamp of p to the area only ever moves it back for corrupt
+ * data; the loads then stay inside the area and its slack.) */
 __device__ __forceinline__ void bits_step(LaneBits& s, uint32_t area, uint32_t adv) {
     s.p += adv;
     const uint32_t k2 = s.p >> 5;
@@ -267,14 +269,15 @@ __device__ __forceinline__ void bits_step(LaneBits& s, uint32_t area, uint32_t a
 /* Decode the lane's next two symbols: returns their exponents in BF16 position
  * [e(i+1) << 23 | e(i) << 7] (other bits unspecified) and advances the lane.  A
  * window whose two codewords do not both fit takes a second lookup at the end of
- * the first; with kLong (a launch holding codewords longer than the window) a
+ * the first; its 12 bits lie within the 64 the lane already holds (offset at most
+ * 31 + 12).  With kLong (a launch holding codewords longer than the window) a
  * first or second codeword the window cannot hold walks the hierarchical table.
  * A window no codeword matches (corrupt data) advances one bit and marks `bad`. */
 template <bool kLong, class Args>
 __device__ __forceinline__ uint32_t pair_step(LaneBits& s, uint32_t& bad, const PairCtx& c, const Args& a) {
     const uint32_t win = __funnelshift_l(s.hi, s.lo, s.p);
     uint32_t e = lds32(c.tab + ((win >> (32 - EC_L1_BITS)) << 2));
-    const uint32_t adv = e & EC_PAIR_LEN_MASK;
+    uint32_t adv = e & EC_PAIR_LEN_MASK;
     if (__builtin_expect(adv == 0, 0)) {
         uint32_t l0 = (e >> EC_PAIR_FIRST_SHIFT) & 15u, x0 = (e >> 7) & 0xFFu;
         if (kLong && l0 == 0) {
@@ -285,7 +288,8 @@ __device__ __forceinline__ uint32_t pair_step(LaneBits& s, uint32_t& bad, const 
         }
         bad |= l0 == 0;
         l0 = max(l0, 1u);
-        const uint32_t w1 = window(c.area, s.p + l0);
+        const uint32_t o = (s.p & 31u) + l0;
+        const uint32_t w1 = kLong ? window(c.area, s.p + l0) : o < 32 ? __funnelshift_l(s.hi, s.lo, o) : s.hi << (o & 31u);
         const uint32_t f = lds32(c.tab + ((w1 >> (32 - EC_L1_BITS)) << 2));
         uint32_t l1 = (f >> EC_PAIR_FIRST_SHIFT) & 15u, x1 = (f >> 7) & 0xFFu;
         if (kLong && l1 == 0) {
@@ -297,10 +301,13 @@ __device__ __forceinline__ uint32_t pair_step(LaneBits& s, uint32_t& bad, const 
         bad |= l1 == 0;
         l1 = max(l1, 1u);
         e = (x0 << 7) | (x1 << 23);
-        bits_seek(s, c.area, s.p + l0 + l1);
-    } else {
-        bits_step(s, c.area, adv);
+        adv = l0 + l1;
+        if (kLong) { /* up to 48 bits: reload both words */
+            bits_seek(s, c.area, s.p + adv);
+            return e;
+        }
     }
+    bits_step(s, c.area, adv); /* adv <= 24 */
     return e;
 }
 
