@@ -55,6 +55,8 @@ struct HuffMat {
     int64_t n_tiles, tile_begin;
     int64_t records_bytes;
     int32_t steps, atomic_y;
+    int32_t last_steps;         /* symbols per lane of the last tile */
+    uint32_t rec16;             /* records region size in 16-byte units */
 };
 
 struct HuffGemvArgs {
@@ -271,41 +273,46 @@ __device__ __forceinline__ void bits_step(LaneBits& s, uint32_t area, uint32_t a
  * window whose two codewords do not both fit takes a second lookup at the end of
  * the first; its 12 bits lie within the 64 the lane already holds (offset at most
  * 31 + 12).  With kLong (a launch holding codewords longer than the window) a
- * first or second codeword the window cannot hold walks the hierarchical table.
- * A window no codeword matches (corrupt data) advances one bit and marks `bad`. */
+ * first or second codeword the window cannot hold walks the hierarchical table
+ * (which reports a window no codeword matches through the status word). */
 template <bool kLong, class Args>
-__device__ __forceinline__ uint32_t pair_step(LaneBits& s, uint32_t& bad, const PairCtx& c, const Args& a) {
+__device__ __forceinline__ uint32_t pair_step(LaneBits& s, const PairCtx& c, const Args& a) {
     const uint32_t win = __funnelshift_l(s.hi, s.lo, s.p);
     uint32_t e = lds32(c.tab + ((win >> (32 - EC_L1_BITS)) << 2));
     uint32_t adv = e & EC_PAIR_LEN_MASK;
     if (__builtin_expect(adv == 0, 0)) {
-        uint32_t l0 = (e >> EC_PAIR_FIRST_SHIFT) & 15u, x0 = (e >> 7) & 0xFFu;
-        if (kLong && l0 == 0) {
-            const HuffMat& M = a.m[c.mi];
-            const uint2 lc = long_codeword(win, M.table + EC_PAIR_WORDS, M.table_words - EC_PAIR_WORDS, a.status);
-            x0 = lc.x;
-            l0 = lc.y;
-        }
-        bad |= l0 == 0;
-        l0 = max(l0, 1u);
-        const uint32_t o = (s.p & 31u) + l0;
-        const uint32_t w1 = kLong ? window(c.area, s.p + l0) : o < 32 ? __funnelshift_l(s.hi, s.lo, o) : s.hi << (o & 31u);
-        const uint32_t f = lds32(c.tab + ((w1 >> (32 - EC_L1_BITS)) << 2));
-        uint32_t l1 = (f >> EC_PAIR_FIRST_SHIFT) & 15u, x1 = (f >> 7) & 0xFFu;
-        if (kLong && l1 == 0) {
-            const HuffMat& M = a.m[c.mi];
-            const uint2 lc = long_codeword(w1, M.table + EC_PAIR_WORDS, M.table_words - EC_PAIR_WORDS, a.status);
-            x1 = lc.x;
-            l1 = lc.y;
-        }
-        bad |= l1 == 0;
-        l1 = max(l1, 1u);
-        e = (x0 << 7) | (x1 << 23);
-        adv = l0 + l1;
-        if (kLong) { /* up to 48 bits: reload both words */
-            bits_seek(s, c.area, s.p + adv);
+        if (kLong) {
+            uint32_t l0 = (e >> EC_PAIR_FIRST_SHIFT) & 15u, x0 = (e >> 7) & 0xFFu;
+            if (l0 == 0) {
+                const HuffMat& M = a.m[c.mi];
+                const uint2 lc = long_codeword(win, M.table + EC_PAIR_WORDS, M.table_words - EC_PAIR_WORDS, a.status);
+                x0 = lc.x;
+                l0 = lc.y;
+            }
+            const uint32_t w1 = window(c.area, s.p + l0);
+            const uint32_t f = lds32(c.tab + ((w1 >> (32 - EC_L1_BITS)) << 2));
+            uint32_t l1 = (f >> EC_PAIR_FIRST_SHIFT) & 15u, x1 = (f >> 7) & 0xFFu;
+            if (l1 == 0) {
+                const HuffMat& M = a.m[c.mi];
+                const uint2 lc = long_codeword(w1, M.table + EC_PAIR_WORDS, M.table_words - EC_PAIR_WORDS, a.status);
+                x1 = lc.x;
+                l1 = lc.y;
+            }
+            e = (x0 << 7) | (x1 << 23);
+            bits_seek(s, c.area, s.p + l0 + l1); /* up to 48 bits: reload both words */
             return e;
         }
+        /* Every codeword fits the window: the entry holds the first one (its
+         * exponent already in bits 7..14, its length in bits 16..19 with nothing
+         * above) and the second is looked up at its end, at most 31 + 12 bits
+         * into the 64 the lane holds.  A window no codeword matches (corrupt
+         * data) yields length 0; the end-of-tile offset check reports it. */
+        const uint32_t l0 = e >> EC_PAIR_FIRST_SHIFT;
+        const uint32_t o = (s.p & 31u) + l0;
+        const uint32_t w1 = o < 32 ? __funnelshift_l(s.hi, s.lo, o) : s.hi << (o & 31u);
+        const uint32_t f = lds32(c.tab + ((w1 >> (32 - EC_L1_BITS)) << 2));
+        adv = l0 + ((f >> EC_PAIR_FIRST_SHIFT) & 15u);
+        e = ((f << 16) & 0x7F800000u) | (e & 0x7F80u);
     }
     bits_step(s, c.area, adv); /* adv <= 24 */
     return e;
@@ -320,12 +327,12 @@ __device__ __forceinline__ uint32_t merge2(uint32_t e, uint32_t r, uint32_t sel)
 
 /* Eight symbols of the lane (raw bytes r0 = symbols 0..3, r1 = 4..7). */
 template <bool kLong, class Args>
-__device__ __forceinline__ void decode8(LaneBits& s, uint32_t& bad, const PairCtx& c, const Args& a, uint32_t r0,
-                                        uint32_t r1, uint32_t (&w)[4]) {
-    w[0] = merge2(pair_step<kLong>(s, bad, c, a), r0, 0x1100);
-    w[1] = merge2(pair_step<kLong>(s, bad, c, a), r0, 0x3322);
-    w[2] = merge2(pair_step<kLong>(s, bad, c, a), r1, 0x1100);
-    w[3] = merge2(pair_step<kLong>(s, bad, c, a), r1, 0x3322);
+__device__ __forceinline__ void decode8(LaneBits& s, const PairCtx& c, const Args& a, uint32_t r0, uint32_t r1,
+                                        uint32_t (&w)[4]) {
+    w[0] = merge2(pair_step<kLong>(s, c, a), r0, 0x1100);
+    w[1] = merge2(pair_step<kLong>(s, c, a), r0, 0x3322);
+    w[2] = merge2(pair_step<kLong>(s, c, a), r1, 0x1100);
+    w[3] = merge2(pair_step<kLong>(s, c, a), r1, 0x3322);
 }
 
 /* acc += w0 * x0 + w1 * x1 for BF16 pairs w = [w1|w0], x = [x1|x0]; the products are
@@ -381,13 +388,12 @@ __device__ __forceinline__ TileRef tile_ref(const Args& a, int64_t g, uint2 off)
     r.mi = owner(a, g);
     const HuffMat& M = a.m[r.mi];
     r.t = g - M.tile_begin;
-    const int64_t T = 32 * (int64_t)M.steps;
-    r.S = (int)(min(T, M.n_rows * M.k_pad - r.t * T) / 32);
-    const int64_t lo = (int64_t)off.x * 16, hi = (int64_t)off.y * 16;
-    const int64_t area = hi - lo - 64 - EC_RAW_BYTES(r.S);
-    const bool ok = lo <= hi && hi <= M.records_bytes && area >= 16 && area <= a.code_bytes;
-    r.rec = M.records + (ok ? lo : 0);
-    r.area = ok ? (int)area : 0;
+    r.S = r.t == M.n_tiles - 1 ? M.last_steps : M.steps;
+    /* offsets are 16-byte units; a record is far below 4 GB */
+    const int area = (int)((off.y - off.x) * 16u) - 64 - EC_RAW_BYTES(r.S);
+    const bool ok = off.x <= off.y && off.y <= M.rec16 && area >= 16 && area <= a.code_bytes;
+    r.rec = M.records + (size_t)(ok ? off.x : 0u) * 16;
+    r.area = ok ? area : 0;
     return r;
 }
 
@@ -441,7 +447,6 @@ __device__ __forceinline__ void huff_walk(const Args& a, int64_t g0, int64_t str
         const uint4* raw4 = (const uint4*)(cur.rec + 64) + lane;
         const int nb = cur.S / 16;
         const uint32_t pmax = 8u * (uint32_t)cur.area;
-        uint32_t bad = 0;
         LaneBits s;
         bits_seek(s, c.area, 8u * min(s0, (uint32_t)cur.area));
         if (!raw_ready) {
@@ -462,9 +467,9 @@ __device__ __forceinline__ void huff_walk(const Args& a, int64_t g0, int64_t str
                     block();
                     if (__builtin_expect(s.p > pmax, 0)) bits_seek(s, c.area, pmax); /* corrupt data only */
                     uint32_t w[4];
-                    decode8<kLong>(s, bad, c, a, rr[u].x, rr[u].y, w);
+                    decode8<kLong>(s, c, a, rr[u].x, rr[u].y, w);
                     half(w);
-                    decode8<kLong>(s, bad, c, a, rr[u].z, rr[u].w, w);
+                    decode8<kLong>(s, c, a, rr[u].z, rr[u].w, w);
                     half(w);
                     const int pf = blk + 2;
                     const uint4* src = pf < nb ? raw4 + 32 * pf : nraw4 + 32 * (pf - nb);
@@ -476,7 +481,7 @@ __device__ __forceinline__ void huff_walk(const Args& a, int64_t g0, int64_t str
         /* every lane's codewords end in the last byte before the next lane's start
          * (the last lane: before the >= 8 zero bytes closing the area) */
         const uint32_t p = s.p;
-        bad |= lane < 31 ? (p > 8u * s1 || p + 8u <= 8u * s1) : (p + 64u > pmax);
+        const bool bad = lane < 31 ? (p > 8u * s1 || p + 8u <= 8u * s1) : (p + 64u > pmax);
         if (__any_sync(kFull, bad) && lane == 0) flag_corrupt(a.status);
         end();
         cur = nxt;
@@ -976,6 +981,8 @@ HuffMat huff_desc(const ec_matrix* W) {
     m.steps = h.steps;
     const int64_t T = 32 * (int64_t)h.steps;
     m.atomic_y = (h.k_pad > 0 && T % h.k_pad == 0) ? 0 : 1;
+    m.last_steps = h.n_tiles > 0 ? (int32_t)((h.n_rows * h.k_pad - (h.n_tiles - 1) * T) / 32) : 0;
+    m.rec16 = (uint32_t)(m.records_bytes / 16);
     return m;
 }
 
