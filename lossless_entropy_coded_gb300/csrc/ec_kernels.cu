@@ -410,8 +410,8 @@ __device__ __forceinline__ void prefetch_code(uint32_t buf, const TileRef& r, in
 /* Walk combined tiles g0, g0 + stride, ... < g_end.  The first tile's copy must
  * already be in flight (prefetch_code).  For every tile with a sound record:
  * begin(tile) once; then, for each block of 16 symbols of the lane, block() and
- * two calls half(w) for its two 8-symbol halves in order (w = four words
- * [w(i+1) | w(i)]); then end().  Rows start on block boundaries (k_pad is a
+ * two calls half(w, h) for its two 8-symbol halves h = 0, 1 in order (w = four
+ * words [w(i+1) | w(i)]); then end().  Rows start on block boundaries (k_pad is a
  * multiple of 16 * 32 positions).  The raw bytes of block b + 2 are loaded right
  * after block b is decoded, into the ring slot it frees; blocks 0 and 1 of the
  * next tile are loaded the same way at the end of the current one. */
@@ -457,25 +457,29 @@ __device__ __forceinline__ void huff_walk(const Args& a, int64_t g0, int64_t str
          * tile's block count is even */
         const bool chain = has_next && nxt.area > 0 && (nb & 1) == 0;
         const uint4* nraw4 = (const uint4*)((chain ? nxt.rec : cur.rec) + 64) + lane;
-        const int lim = nb + (chain ? min(2, nxt.S / 16) : 0);
+        const int nnbc = chain ? min(2, nxt.S / 16) : 0; /* next-tile blocks to prefetch */
+        const uint4* rp = raw4 + 64;                    /* blocks b0 + 2, b0 + 3 */
         begin(cur);
         for (int b0 = 0; b0 < nb; b0 += 2) {
+            const bool last_pair = b0 + 2 >= nb;
+            const uint4* src = last_pair ? nraw4 : rp;
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int blk = b0 + u;
                 if (u == 0 || blk < nb) {
                     block();
-                    if (__builtin_expect(s.p > pmax, 0)) bits_seek(s, c.area, pmax); /* corrupt data only */
+                    /* a position past the area (corrupt data only) is pulled back; the
+                     * held words are then stale but every load stays in the area */
+                    s.p = min(s.p, pmax);
                     uint32_t w[4];
                     decode8<kLong>(s, c, a, rr[u].x, rr[u].y, w);
-                    half(w);
+                    half(w, 0);
                     decode8<kLong>(s, c, a, rr[u].z, rr[u].w, w);
-                    half(w);
-                    const int pf = blk + 2;
-                    const uint4* src = pf < nb ? raw4 + 32 * pf : nraw4 + 32 * (pf - nb);
-                    if (pf < lim) rr[u] = __ldg(src);
+                    half(w, 1);
+                    if (last_pair ? u < nnbc : blk + 2 < nb) rr[u] = __ldg(src + 32 * u);
                 }
             }
+            rp += 64;
         }
         raw_ready = chain;
         /* every lane's codewords end in the last byte before the next lane's start
@@ -585,7 +589,7 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
                 ++row;
             }
         },
-        [&](const uint32_t (&w)[4]) {
+        [&](const uint32_t (&w)[4], int h) {
 #pragma unroll
             for (int b = 0; b < B; ++b) {
                 if (B > 1 && b >= batch) break;
@@ -596,7 +600,9 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
                 acc[b][1] = fma2_bf16(w[3], x4.w, acc[b][1]);
             }
             jc += 8;
-            if (kAhead) load_x(jc >= jrow ? jc - jrow : jc); /* the next half starts a new row there */
+            /* rows start on block boundaries: only a second half can be followed by
+             * a new row */
+            if (kAhead) load_x(h == 1 && jc >= jrow ? jc - jrow : jc);
         },
         [&]() { flush(row); });
 }
@@ -651,7 +657,7 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_decode_kernel(const __gri
                         ++row;
                     }
                 },
-                [&](const uint32_t (&w)[4]) {
+                [&](const uint32_t (&w)[4], int) {
                     /* lane's 8 outputs are positions 32 i + lane, i = 8k'..8k'+7: transpose */
                     __syncwarp();
 #pragma unroll
