@@ -376,6 +376,58 @@ def extras(torch, ec, stream, device):
     return out
 
 
+def batch_sweep(torch, ec, stack, stream, device):
+    """Fused GEMV over the 8B layer set at batch 1, 2, 4, 8 and 16 (layers 0 and 1
+    of the stack alternately, 600 MB, so repeated replays do not run from L2), and
+    the same layer set coded with the 24-bit length limit at batch 1."""
+    import synth
+    dev = f"cuda:{device}"
+    n_l = min(2, stack.n_layers)
+    out = {}
+
+    def t_graph(fn, iters=20, warm=3):
+        g = capture(torch, fn, stream)
+        return time_graph(torch, g, stream, iters, warm)
+
+    sweep = {}
+    for b in (1, 2, 4, 8, 16):
+        bufs = []
+        for l in range(n_l):
+            for gname, names in Stack.GROUPS:
+                Ws = [stack.mats[l][n] for n in names]
+                k = stack.specs[l][names[0]].k_cols
+                x = torch.from_numpy(synth.make_x(stack.specs[l][names[0]].seed, b, k).view(np.int16)).to(dev)
+                ys = [torch.empty((b, stack.specs[l][n].n_rows), device=dev) for n in names]
+                bufs.append((Ws, x, ys))
+
+        def run(bufs=bufs, b=b):
+            for Ws, x, ys in bufs:
+                ec.gemv_group(Ws, x, ys, batch=b)
+        sweep[str(b)] = round(t_graph(run) / n_l, 1)
+    out["batch_sweep_us_per_layer_set"] = sweep
+    # the 24-bit limit (hierarchical-table kernel) on layer 0..n_l-1 at batch 1
+    mats24, bufs = [], []
+    for l in range(n_l):
+        specs = stack.specs[l]
+        m = {nm: ec.encode_bf16(synth.make_weights(s), max_code_len=24, device=device) for nm, s in specs.items()}
+        mats24.append(m)
+        for gname, names in Stack.GROUPS:
+            k = specs[names[0]].k_cols
+            x = torch.from_numpy(synth.make_x(specs[names[0]].seed, 1, k).view(np.int16)).to(dev)
+            ys = [torch.empty((1, specs[n].n_rows), device=dev) for n in names]
+            bufs.append(([m[n] for n in names], x, ys))
+
+    def run24():
+        for Ws, x, ys in bufs:
+            ec.gemv_group(Ws, x, ys, batch=1)
+    out["layer_set_us_maxlen24"] = round(t_graph(run24) / n_l, 1)
+    out["layer_set_bpw_maxlen24"] = round(8 * sum(W.stats()["device_bytes"] for m in mats24 for W in m.values())
+                                          / sum(s.n_rows * s.k_cols for l in range(n_l)
+                                                for s in stack.specs[l].values()), 4)
+    assert ec.status(stream) == 0
+    return out
+
+
 # ------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -438,6 +490,11 @@ def main():
                         post=lambda: stack.y_pinned.copy_(stack.y_dev_all, non_blocking=True))
     launches = per_launch_us(torch, stack, stream)
     assert ec.status(stream) == 0
+    groups = {}
+    for gi, (gname, names) in enumerate(Stack.GROUPS):
+        us_g = float(launches[gi::len(Stack.GROUPS)].mean())
+        nbytes = sum(stack.mats[0][n].stats()["device_bytes"] for n in names)
+        groups[gname] = {"us": round(us_g, 2), "compressed_gbs": round(nbytes / us_g / 1e3, 1)}
 
     t_max = torch.tensor([us_ec], device="cuda")
     if world > 1:
@@ -452,6 +509,7 @@ def main():
     ex = {}
     if rank == 0 and not args.no_extras:
         ex = extras(torch, ec, stream, local)
+        ex.update(batch_sweep(torch, ec, stack, stream, local))
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         sample = OracleSample()
@@ -488,6 +546,7 @@ def main():
                 "step_frac_of_8tbs": round(stack.compressed_bytes / us_step / 1e3 / 8000.0, 4),
                 "bits_per_weight": round(8 * stack.compressed_bytes / stack.weights, 3),
                 "effective_weights_per_s": float(f"{stack.weights / us_step * 1e6:.4g}"),
+                "launch_groups": groups,
                 "setup_s": round(setup_s, 1), "encode_s": round(stack.encode_s, 1),
                 **ex,
             },

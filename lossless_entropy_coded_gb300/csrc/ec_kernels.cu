@@ -172,7 +172,7 @@ constexpr int kSlackBytes = 64;                /* after a code area: reads run <
 constexpr uint32_t kPairTabBytes = 4u * EC_PAIR_WORDS;
 constexpr uint32_t kSignMant = 0x807F807Fu;    /* sign and mantissa bits of two BF16 */
 
-__host__ __device__ constexpr int huff_max_warps(int b) { return b <= 2 ? 32 : (b <= 4 ? 24 : 16); }
+__host__ __device__ constexpr int huff_max_warps(int b) { return b <= 1 ? 32 : (b <= 4 ? 24 : 16); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
@@ -364,6 +364,40 @@ static_assert(huff_warp_bytes(16) % 16 == 0 && huff_warp_bytes(4112) % 16 == 0, 
 __host__ __device__ constexpr uint32_t xs_lane_stride(uint32_t kp) { return kp / 32 + 8; }
 __host__ __device__ constexpr size_t xs_row_bytes(uint32_t kp) { return (size_t)2 * 32 * xs_lane_stride(kp); }
 
+/* Stage x [batch, K] (BF16) transposed into shared memory, xs_t[b][l][j] =
+ * x[b][32 j + l], zero past K: 16-byte loads, four in flight per thread, when
+ * rows are 16-byte aligned (K % 8 == 0; x itself is 16-byte aligned), else
+ * 2-byte loads. */
+__device__ __forceinline__ void stage_x(uint16_t* xs, const uint16_t* __restrict__ x, int batch, int64_t K,
+                                        uint32_t kp, uint32_t lx) {
+    if ((K & 7) == 0) {
+        const uint32_t per_row = kp / 8, n = (uint32_t)batch * per_row;
+        for (uint32_t i0 = threadIdx.x; i0 < n; i0 += 4 * blockDim.x) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t i = i0 + u * blockDim.x, b = i / per_row, c = (i - b * per_row) * 8;
+                v[u] = i < n && c < K ? __ldg((const uint4*)(x + (int64_t)b * K + c)) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t i = i0 + u * blockDim.x;
+                if (i < n) {
+                    const uint32_t b = i / per_row, c = (i - b * per_row) * 8;
+                    uint16_t* dst = xs + (size_t)b * 32 * lx + (c >> 5);
+                    const uint32_t vw[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) dst[((c + j) & 31) * lx] = (uint16_t)(vw[j >> 1] >> (16 * (j & 1)));
+                }
+            }
+        }
+    } else {
+        for (int b = 0; b < batch; ++b)
+            for (uint32_t c = threadIdx.x; c < kp; c += blockDim.x)
+                xs[(size_t)b * 32 * lx + (c & 31) * lx + (c >> 5)] = c < K ? x[(int64_t)b * K + c] : (uint16_t)0;
+    }
+}
+
 /* A resolved tile record (all lanes hold the same values). */
 struct TileRef {
     const uint8_t* rec; /* lane starts | raw | code area */
@@ -526,9 +560,7 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
     }
     grid_dep_launch();
     grid_dep_wait(); /* x and y belong to the preceding kernel in the stream from here on */
-    for (int b = 0; b < batch; ++b)
-        for (uint32_t c = threadIdx.x; c < kp; c += blockDim.x)
-            xs[(size_t)b * 32 * lx + (c & 31) * lx + (c >> 5)] = c < K ? a.x[(int64_t)b * K + c] : (uint16_t)0;
+    stage_x(xs, a.x, batch, K, kp, lx);
     __syncthreads();
     if (gw >= a.total_tiles) return;
 
