@@ -370,7 +370,7 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
     *out = nullptr;
     if (n_rows < 0 || k_cols < 0) return EC_ERR_SHAPE;
     const int max_len = params ? params->max_code_len : EC_DEFAULT_MAX_CODE_LEN;
-    const int steps = params ? params->tile_steps : 128;
+    const int steps = params ? params->tile_steps : EC_DEFAULT_TILE_STEPS;
     if (max_len < 1 || max_len > EC_MAX_CODE_LEN) return EC_ERR_INVALID_ARG;
     if (steps != 32 && steps != 64 && steps != 128) return EC_ERR_INVALID_ARG;
     int64_t nk = 0, k_pad = round_up(k_cols, EC_HUFF_ROW_ALIGN), n_pad = 0, tmp = 0;

@@ -309,9 +309,19 @@ def test_deserialize_rejects_structural_corruption(ec, kind):
         assert e.value.code == -5, name
 
 
+def test_tile_width_aux_bounds(ec):
+    w = synth.llama_bf16(2001, 1024, 4096)
+    for steps, lo, hi in ((128, 0.125, 0.25), (64, 0.25, 0.40)):
+        s = ec.encode_bf16(w, tile_steps=steps, device=-1).stats()
+        assert s["n_tiles"] == w.size // (32 * steps)
+        # per tile: 64 B of lane starts, each lane's last byte (about 4 bits x 32
+        # lanes) and the area's >= 8 zero bytes and 16-byte padding
+        assert lo < s["aux_bytes"] * 8 / w.size < hi, steps
+
+
 def test_stats_accounting(ec):
     w = synth.llama_bf16(2001, 1024, 4096)
-    W = ec.encode_bf16(w, device=-1)
+    W = ec.encode_bf16(w, tile_steps=128, device=-1)
     s = W.stats()
     n = w.size
     assert s["k_pad"] == 4096 and s["n_tiles"] == n // 4096

@@ -151,8 +151,9 @@ def test_payload_corruption_is_reported_not_faulted(ec):
     h, devb = parse(bytes(blob))
     meta = len(blob) - len(devb)
     rec = meta + h["records_off"]
-    # flip bits inside the first tile's code area (after 64 B of lane starts + 4096 raw bytes)
-    for off in (64 + 4096 + 3, 64 + 4096 + 200, 64 + 4096 + 900):
+    # flip bits inside the first tile's code area (after 64 B of lane starts and the raw bytes)
+    area = 64 + 32 * h["steps"]
+    for off in (area + 3, area + 200, area + 500):
         blob[rec + off] ^= 0x5A
     Wc = ec.deserialize(bytes(blob), device=0)
     out = torch.zeros((64, 4096), dtype=torch.int16, device="cuda")
