@@ -90,6 +90,8 @@ struct RansMat {
     int64_t n_tiles;
     int64_t records_bytes;
     int32_t steps, prob_bits, atomic_y, words_cap;
+    int32_t last_steps;         /* symbols per lane of the last tile */
+    uint32_t rec16;             /* records region size in 16-byte units */
 };
 
 struct RansArgs {
@@ -114,27 +116,6 @@ __device__ __forceinline__ int owner(const Args& a, int64_t g) {
     int k = 0;
     while (k + 1 < a.count && g >= a.m[k + 1].tile_begin) ++k;
     return k;
-}
-
-/* Start and length (bytes) of tile t's record; a range outside the records region
- * (only possible with a corrupted offset table) yields an empty record. */
-__device__ __forceinline__ int64_t record_span(const uint32_t* __restrict__ tile_off, int64_t t, int64_t records_bytes,
-                                               int64_t* bytes, int* status, int lane) {
-    const int64_t a = (int64_t)__ldg(tile_off + t) * 16, b = (int64_t)__ldg(tile_off + t + 1) * 16;
-    if (a > b || b > records_bytes) {
-        if (lane == 0) flag_corrupt(status);
-        *bytes = 0;
-        return 0;
-    }
-    *bytes = b - a;
-    return a;
-}
-
-/* Copy `bytes` (multiple of 16) from global to shared memory with the warp. */
-__device__ __forceinline__ void warp_copy16(void* dst, const void* src, int bytes, int lane) {
-    const uint4* s = (const uint4*)src;
-    uint4* d = (uint4*)dst;
-    for (int i = lane; i < bytes / 16; i += 32) d[i] = __ldg(s + i);
 }
 
 /* floor(t * T / kp) where `unit` divides both T and kp (32-bit division when it fits). */
@@ -714,121 +695,223 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_decode_kernel(const __gri
 }
 
 /* ============================================================ rANS kernels */
-/* Decode one tile; calls sink(step, code, lane position) for every symbol. */
+/*
+ * One warp per 4096-symbol tile (EntroPack, independent rANS tiles): lane l holds
+ * state x_l and decodes positions 32 j + l.  A step looks the slot x & (2^b - 1)
+ * up in the shared slot table (symbol, freq, slot - cum), sets
+ * x = freq * (x >> b) + slot - cum, and lanes whose state fell below 2^16 pull the
+ * next 16-bit word, in lane order (ballot + popc).  Words and the 32 initial
+ * states of the warp's next tile arrive by cp.async into the second of two
+ * shared buffers while the current tile is decoded.  Rows are multiples of 128
+ * columns, so the scale group (128 consecutive weights, FP16) of 4 steps is one
+ * value for the warp, and the scales of a tile's groups are contiguous: lane g
+ * loads group g's scale at the start of the previous tile.  GEMV: sum code * x
+ * over a group in FP32, then multiply by the group's scale (both exact up to the
+ * FP32 sums); decode: BF16 round-to-nearest-even of code * scale (exact in FP32).
+ */
+/* Stage x [batch, K] (BF16) into shared rows of k_pad entries, zero past K:
+ * 16-byte loads and stores, four in flight per thread, when K % 8 == 0. */
+__device__ __forceinline__ void stage_x_rows(uint16_t* xs, const uint16_t* __restrict__ x, int batch, int64_t K,
+                                             uint32_t kp) {
+    if ((K & 7) == 0) {
+        const uint32_t per_row = kp / 8, n = (uint32_t)batch * per_row;
+        for (uint32_t i0 = threadIdx.x; i0 < n; i0 += 4 * blockDim.x) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t i = i0 + u * blockDim.x, b = i / per_row, c = (i - b * per_row) * 8;
+                v[u] = i < n && c < K ? __ldg((const uint4*)(x + (int64_t)b * K + c)) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t i = i0 + u * blockDim.x;
+                if (i < n) *(uint4*)(xs + (size_t)i * 8) = v[u];
+            }
+        }
+    } else {
+        for (int b = 0; b < batch; ++b)
+            for (uint32_t c = threadIdx.x; c < kp; c += blockDim.x) xs[(size_t)b * kp + c] = c < K ? x[b * K + c] : 0;
+    }
+}
+
+__host__ __device__ constexpr int rans_max_warps(int b) { return b <= 1 ? 32 : (b <= 4 ? 24 : 16); }
+
+/* one tile buffer: 32 states, the words (capacity rounded to 16 bytes), slack */
+__host__ __device__ constexpr size_t rans_buf_bytes(int words_cap) {
+    return 128 + (((size_t)words_cap * 2 + 15) & ~(size_t)15) + 64;
+}
+
+struct RansTile {
+    const uint8_t* rec;
+    int64_t t;
+    int S;      /* symbols per lane */
+    int words;  /* payload words; -1 = corrupt record (skipped) */
+};
+
+__device__ __forceinline__ RansTile rans_tile(const RansMat& M, int64_t t, uint2 off) {
+    RansTile r;
+    r.t = t;
+    r.S = t == M.n_tiles - 1 ? M.last_steps : M.steps;
+    const int wb = (int)((off.y - off.x) * 16u) - 128;
+    const bool ok = off.x <= off.y && off.y <= M.rec16 && wb >= 0 && wb <= 2 * M.words_cap;
+    r.rec = M.records + (size_t)(ok ? off.x : 0u) * 16;
+    r.words = ok ? wb / 2 : -1;
+    return r;
+}
+
+__device__ __forceinline__ void rans_prefetch(uint32_t buf, const RansTile& r, int lane) {
+    if (r.words >= 0) {
+        if (lane < 8) cp_async16(buf + 16 * lane, r.rec + 16 * lane);
+        for (int i = lane; i < r.words / 8; i += 32) cp_async16(buf + 128 + 16 * i, r.rec + 128 + 16 * i);
+    }
+    cp_async_commit();
+}
+
+__device__ __forceinline__ uint32_t lds16_if(bool p, uint32_t a, uint32_t v) {
+    asm volatile("{\n\t.reg .pred q;\n\t.reg .b16 h;\n\t"
+                 "setp.ne.u32 q, %1, 0;\n\t"
+                 "@q ld.shared.u16 h, [%2];\n\t"
+                 "@q cvt.u32.u16 %0, h;\n\t}"
+                 : "+r"(v)
+                 : "r"((uint32_t)p), "r"(a)
+                 : "memory");
+    return v;
+}
+
 template <bool kGemv, int B>
-__global__ void __launch_bounds__(kWarps * 32) rans_kernel(const __grid_constant__ RansArgs a) {
+__global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) rans_kernel(const __grid_constant__ RansArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const RansMat& M = a.m;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t kp = M.k_pad, K = M.k_cols;
-    const uint32_t mask_b = (1u << M.prob_bits) - 1;
-    uint32_t* tab = (uint32_t*)smem;
-    float* xs = (float*)(smem + ((size_t)4 << M.prob_bits));
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+    const uint32_t kp = (uint32_t)M.k_pad;
+    const int64_t K = M.k_cols;
+    const int pb = M.prob_bits;
+    const uint32_t mask_b = (1u << pb) - 1;
     const int batch = kGemv ? a.batch : 0;
-    uint16_t* words = (uint16_t*)((uint8_t*)(xs + (size_t)batch * kp) + (size_t)warp * (2 * M.words_cap));
+    const uint32_t tab_s = smem_u32(smem);
+    uint16_t* xs = (uint16_t*)(smem + ((size_t)4 << pb));
+    const uint32_t xs_s = smem_u32(xs);
+    const uint32_t buf_bytes = (uint32_t)rans_buf_bytes(M.words_cap);
+    const uint32_t bufs = xs_s + (uint32_t)(2 * (size_t)batch * kp) + (uint32_t)warp * 2 * buf_bytes;
+    const uint32_t cap = (buf_bytes - 128) / 2 - 1; /* last word index inside the buffer */
+    const int64_t T = 32 * (int64_t)M.steps;
 
-    for (int i = threadIdx.x; i <= (int)mask_b; i += blockDim.x) tab[i] = __ldg(M.table + i);
-    if (kGemv)
-        for (int b = 0; b < batch; ++b)
-            for (int64_t c = threadIdx.x; c < kp; c += blockDim.x)
-                xs[(int64_t)b * kp + c] = c < K ? __uint_as_float((uint32_t)a.x[(int64_t)b * K + c] << 16) : 0.f;
+    const int64_t gw = (int64_t)blockIdx.x * nwarp + warp, nw = (int64_t)gridDim.x * nwarp;
+    RansTile cur{};
+    float sc = 0.f; /* lane g: scale of group g of the current tile */
+    if (gw < M.n_tiles) {
+        cur = rans_tile(M, gw, make_uint2(__ldg(M.tile_off + gw), __ldg(M.tile_off + gw + 1)));
+        rans_prefetch(bufs, cur, lane);
+        const int64_t g0 = gw * (T / 128) + lane;
+        if (lane < cur.S / 4) sc = __half2float(__ushort_as_half(__ldg(M.scales + g0)));
+    }
+    {
+        const uint4* src = (const uint4*)M.table;
+        uint4* dst = (uint4*)smem;
+        for (int i = threadIdx.x; i < (1 << pb) / 4; i += blockDim.x) dst[i] = __ldg(src + i);
+    }
+    grid_dep_launch();
+    grid_dep_wait(); /* x, y and out belong to the preceding kernel in the stream from here on */
+    if (kGemv) stage_x_rows(xs, a.x, batch, K, kp);
     __syncthreads();
+    if (gw >= M.n_tiles) return;
 
-    const int64_t groups = kp / 128;
-    const int64_t gw = (int64_t)blockIdx.x * kWarps + warp, nw = (int64_t)gridDim.x * kWarps;
+    uint2 off_next = gw + nw < M.n_tiles ? make_uint2(__ldg(M.tile_off + gw + nw), __ldg(M.tile_off + gw + nw + 1))
+                                         : make_uint2(0u, 0u);
+    const uint32_t lt = (1u << lane) - 1u;
+    uint32_t cb = bufs;
     for (int64_t t = gw; t < M.n_tiles; t += nw) {
-        const int64_t T = 32 * (int64_t)M.steps;
-        const int64_t base = t * T;
-        const int64_t n_t = min(T, M.n_rows * kp - base);
-        const int S = (int)(n_t / 32);
-        int64_t rec_bytes = 0;
-        const uint8_t* rec = M.records + record_span(M.tile_off, t, M.records_bytes, &rec_bytes, a.status, lane);
-        if (rec_bytes < 128) {
-            if (lane == 0) flag_corrupt(a.status);
-            continue;
-        }
-        int wbytes = (int)(rec_bytes - 128);
-        if (wbytes < 0 || wbytes > 2 * M.words_cap) {
-            if (lane == 0) flag_corrupt(a.status);
-            wbytes = max(0, min(wbytes, 2 * M.words_cap));
-        }
-        const int nwords = wbytes / 2;
-        uint32_t x = __ldg((const uint32_t*)rec + lane);
-        warp_copy16(words, rec + 128, wbytes, lane);
+        cp_async_wait_all();
         __syncwarp();
-        int wp = 0;
-        int64_t row = tile_row(t, T, kp, EC_RANS_ROW_ALIGN);
-        int64_t col0 = base - row * kp; /* column of lane 0 at the current step */
-        float acc[B], accg[B];
+        const uint32_t nb_buf = cb == bufs ? bufs + buf_bytes : bufs;
+        RansTile nxt{};
+        float sc_next = 0.f;
+        if (t + nw < M.n_tiles) {
+            nxt = rans_tile(M, t + nw, off_next);
+            rans_prefetch(nb_buf, nxt, lane);
+            if (lane < nxt.S / 4) sc_next = __half2float(__ushort_as_half(__ldg(M.scales + (t + nw) * (T / 128) + lane)));
+            if (t + 2 * nw < M.n_tiles)
+                off_next = make_uint2(__ldg(M.tile_off + t + 2 * nw), __ldg(M.tile_off + t + 2 * nw + 1));
+        }
+        if (cur.words < 0) {
+            if (lane == 0) flag_corrupt(a.status);
+        } else {
+            uint32_t x = lds32(cb + 4 * lane);
+            const uint32_t wbase = cb + 128;
+            uint32_t wp = 0;
+            int64_t row = tile_row(t, T, kp, EC_RANS_ROW_ALIGN);
+            uint32_t col = (uint32_t)(t * T - row * (int64_t)kp) + lane; /* this lane's column */
+            float acc[B], accg[B];
 #pragma unroll
-        for (int b = 0; b < B; ++b) acc[b] = accg[b] = 0.f;
-
-        for (int j = 0; j < S; ++j) {
-            const uint32_t e = tab[x & mask_b];
-            const int code = (int)(e & 15u) - 8;
-            x = (e >> 16) * (x >> M.prob_bits) + ((e >> 4) & 0xFFFu);
-            const bool need = x < 65536u;
-            const unsigned bal = __ballot_sync(kFull, need);
-            if (need) {
-                const int idx = wp + __popc(bal & ((1u << lane) - 1u));
-                uint32_t v = 0;
-                if (idx < nwords) v = words[idx];
-                else flag_corrupt(a.status);
-                x = (x << 16) | v;
-            }
-            wp += __popc(bal);
-            if (col0 >= kp) {
-                if (kGemv) {
-#pragma unroll
-                    for (int b = 0; b < B; ++b) {
-                        if (b >= batch) break;
-                        const float v = warp_sum(acc[b]);
-                        if (lane == 0) {
-                            float* dst = M.y + (int64_t)b * M.n_rows + row;
-                            if (M.atomic_y) atomicAdd(dst, v);
-                            else *dst = v;
-                        }
-                        acc[b] = 0.f;
-                    }
-                }
-                col0 -= kp;
-                ++row;
-            }
-            const int64_t col = col0 + lane;
-            const float scale = __half2float(__ushort_as_half(__ldg(M.scales + row * groups + col0 / 128)));
-            if (kGemv) {
-                const float cf = (float)code;
+            for (int b = 0; b < B; ++b) acc[b] = accg[b] = 0.f;
+            auto flush = [&]() {
 #pragma unroll
                 for (int b = 0; b < B; ++b) {
-                    if (b >= batch) break;
-                    accg[b] = fmaf(cf, xs[(int64_t)b * kp + col], accg[b]);
+                    if (B > 1 && b >= batch) break;
+                    const float v = warp_sum(acc[b]);
+                    if (lane == 0) {
+                        float* dst = M.y + (int64_t)b * M.n_rows + row;
+                        if (M.atomic_y) atomicAdd(dst, v);
+                        else *dst = v;
+                    }
+                    acc[b] = 0.f;
                 }
-                if ((j & 3) == 3) { /* 128 positions = one scale group of one row */
+            };
+            const int ng = cur.S / 4;
+            for (int gi = 0; gi < ng; ++gi) {
+                if (col >= kp) { /* rows start on group boundaries */
+                    if (kGemv) flush();
+                    col -= kp;
+                    ++row;
+                }
+                if ((gi & 31) == 0 && gi > 0) /* tiles of more than 32 groups */
+                    sc = lane < ng - gi ? __half2float(__ushort_as_half(__ldg(M.scales + t * (T / 128) + gi + lane)))
+                                        : 0.f;
+                const float scale = __shfl_sync(kFull, sc, gi & 31);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint32_t e = lds32(tab_s + ((x & mask_b) << 2));
+                    x = (e >> 16) * (x >> pb) + ((e >> 4) & 0xFFFu);
+                    const bool need = x < 65536u;
+                    const uint32_t bal = __ballot_sync(kFull, need);
+                    const uint32_t idx = min(wp + __popc(bal & lt), cap);
+                    const uint32_t v = lds16_if(need, wbase + 2 * idx, 0u);
+                    x = need ? (x << 16) | v : x;
+                    wp += __popc(bal);
+                    /* code + 8 in the low 4 bits: (float)code = (2^23 + code + 8) - (2^23 + 8) */
+                    const float cf = __int_as_float(0x4B000000 | (e & 15u)) - 8388616.0f;
+                    const uint32_t c = col + 32 * s;
+                    if (kGemv) {
+#pragma unroll
+                        for (int b = 0; b < B; ++b) {
+                            if (B > 1 && b >= batch) break;
+                            uint32_t xv;
+                            asm volatile("ld.shared.u16 %0, [%1];" : "=r"(xv) : "r"(xs_s + 2 * (b * kp + c)) : "memory");
+                            accg[b] = fmaf(cf, __uint_as_float(xv << 16), accg[b]);
+                        }
+                    } else if (c < K) {
+                        M.out[row * K + c] = __bfloat16_as_ushort(__float2bfloat16_rn(cf * scale));
+                    }
+                }
+                if (kGemv) {
 #pragma unroll
                     for (int b = 0; b < B; ++b) {
                         acc[b] = fmaf(accg[b], scale, acc[b]);
                         accg[b] = 0.f;
                     }
                 }
-            } else if (col < K) {
-                M.out[row * K + col] = __bfloat16_as_ushort(__float2bfloat16_rn((float)code * scale));
+                col += 128;
             }
-            col0 += 32;
-        }
-        if (x != 65536u) flag_corrupt(a.status); /* every lane must return to its initial state */
-        if (kGemv) {
-#pragma unroll
-            for (int b = 0; b < B; ++b) {
-                if (b >= batch) break;
-                const float v = warp_sum(acc[b]);
-                if (lane == 0) {
-                    float* dst = M.y + (int64_t)b * M.n_rows + row;
-                    if (M.atomic_y) atomicAdd(dst, v);
-                    else *dst = v;
-                }
+            /* every lane returns to its initial state 2^16 and the words are used up
+             * (the encoder pads the words to 16 bytes: up to 7 trailing zeros) */
+            if (__any_sync(kFull, x != 65536u) || wp > (uint32_t)cur.words || (uint32_t)cur.words - wp > 7) {
+                if (lane == 0) flag_corrupt(a.status);
             }
+            if (kGemv) flush();
         }
-        __syncwarp();
+        cur = nxt;
+        sc = sc_next;
+        cb = nb_buf;
     }
 }
 
@@ -1041,6 +1124,8 @@ RansMat rans_desc(const ec_matrix* W) {
     const int64_t T = 32 * (int64_t)h.steps;
     m.atomic_y = (h.k_pad > 0 && T % h.k_pad == 0) ? 0 : 1;
     m.words_cap = (h.max_words + 7) / 8 * 8;
+    m.last_steps = h.n_tiles > 0 ? (int32_t)((h.n_rows * h.k_pad - (h.n_tiles - 1) * T) / 32) : 0;
+    m.rec16 = (uint32_t)(m.records_bytes / 16);
     return m;
 }
 
@@ -1076,19 +1161,18 @@ int launch_huff_gemv(const HuffGemvArgs& a, bool lng, size_t smem, int grid, int
 }
 
 template <bool G, int B>
-int launch_rans_b(const RansArgs& a, size_t smem, int grid, cudaStream_t s) {
+int launch_rans_b(const RansArgs& a, size_t smem, int grid, int block, cudaStream_t s) {
     if (set_smem(rans_kernel<G, B>, smem) != EC_OK) return EC_ERR_CUDA;
-    rans_kernel<G, B><<<grid, kWarps * 32, smem, s>>>(a);
-    return launch_result();
+    return launch_ex(rans_kernel<G, B>, grid, block, smem, s, a);
 }
 
-int launch_rans(bool gemv, const RansArgs& a, size_t smem, int grid, cudaStream_t s) {
-    if (!gemv) return launch_rans_b<false, 1>(a, smem, grid, s);
-    if (a.batch <= 1) return launch_rans_b<true, 1>(a, smem, grid, s);
-    if (a.batch <= 2) return launch_rans_b<true, 2>(a, smem, grid, s);
-    if (a.batch <= 4) return launch_rans_b<true, 4>(a, smem, grid, s);
-    if (a.batch <= 8) return launch_rans_b<true, 8>(a, smem, grid, s);
-    return launch_rans_b<true, 16>(a, smem, grid, s);
+int launch_rans(bool gemv, const RansArgs& a, size_t smem, int grid, int block, cudaStream_t s) {
+    if (!gemv) return launch_rans_b<false, 1>(a, smem, grid, block, s);
+    if (a.batch <= 1) return launch_rans_b<true, 1>(a, smem, grid, block, s);
+    if (a.batch <= 2) return launch_rans_b<true, 2>(a, smem, grid, block, s);
+    if (a.batch <= 4) return launch_rans_b<true, 4>(a, smem, grid, block, s);
+    if (a.batch <= 8) return launch_rans_b<true, 8>(a, smem, grid, block, s);
+    return launch_rans_b<true, 16>(a, smem, grid, block, s);
 }
 
 /* Batch rows whose copy of x (elem bytes per value) fits in `budget` bytes of shared memory. */
@@ -1174,21 +1258,25 @@ int rans_run(const ec_matrix* W, const uint16_t* x, float* y, uint16_t* out, int
             return EC_ERR_CUDA;
     }
     if (W->hdr.n_tiles == 0) return EC_OK;
-    const size_t fixed = ((size_t)4 << a.m.prob_bits) + (size_t)kWarps * 2 * a.m.words_cap;
-    if (fixed > d->smem_optin) return EC_ERR_UNSUPPORTED;
+    /* one CTA per SM: slot table | x (BF16) [rows of this pass][k_pad] | two tile buffers per warp */
+    const size_t table = (size_t)4 << a.m.prob_bits, per_warp = 2 * rans_buf_bytes(a.m.words_cap);
     const int64_t kp = W->hdr.k_pad, K = W->hdr.k_cols;
-    const int per_pass = gemv ? rows_per_pass(kp, batch, d->smem_optin - fixed) : 1;
+    const size_t xrow = gemv ? (size_t)2 * kp : 0;
+    if (table + xrow + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED;
+    const int cap = gemv ? rans_max_warps(batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : batch <= 8 ? 8 : 16)
+                         : rans_max_warps(1);
+    const int warps = (int)std::min<size_t>(cap, (d->smem_optin - table - xrow) / per_warp);
+    const size_t fixed = table + (size_t)warps * per_warp;
+    const int per_pass = gemv ? (int)std::min<size_t>(batch, (d->smem_optin - fixed) / xrow) : 1;
     if (per_pass < 1) return EC_ERR_UNSUPPORTED;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(d->sms, (W->hdr.n_tiles + warps - 1) / warps));
     const int passes = gemv ? batch : 1;
     for (int b0 = 0; b0 < passes; b0 += per_pass) {
         const int nb = gemv ? std::min(per_pass, batch - b0) : 0;
         a.batch = nb;
         a.x = gemv ? x + (int64_t)b0 * K : nullptr;
         if (gemv) a.m.y = y + (int64_t)b0 * W->hdr.n_rows;
-        const size_t smem = fixed + (size_t)4 * nb * kp;
-        const int ctas = std::max(1, (int)(d->smem_optin / (smem + 1024)));
-        const int grid = grid_for(*d, W->hdr.n_tiles, std::min(ctas, 2));
-        const int rc = launch_rans(gemv, a, smem, grid, s);
+        const int rc = launch_rans(gemv, a, fixed + xrow * nb, grid, warps * 32, s);
         if (rc != EC_OK) return rc;
     }
     return EC_OK;
