@@ -1197,7 +1197,22 @@ int plan_huff_gemv(const DeviceInfo& d, int count, int code_bytes, int64_t kp, i
     pl->xrow = xs_row_bytes((uint32_t)kp);
     if (tables + pl->xrow + 4 * per_warp > d.smem_optin) return EC_ERR_UNSUPPORTED;
     const int cap = huff_max_warps(batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : batch <= 8 ? 8 : 16);
-    pl->warps = (int)std::min<size_t>(cap, (d.smem_optin - tables - pl->xrow) / per_warp);
+    const int wmax = (int)std::min<size_t>(cap, (d.smem_optin - tables - pl->xrow) / per_warp);
+    /* Each warp takes every (grid * warps)-th tile, so a launch lasts ceil(tiles /
+     * (sms * w)) rounds of one tile per warp, and a round takes time in proportion
+     * to the warps sharing an SM (the SM is issue-bound from about 16 warps on):
+     * pick the w in [min(16, wmax), wmax] with the fewest rounds * w, the larger
+     * on ties. */
+    int best = wmax;
+    int64_t best_cost = INT64_MAX;
+    for (int w = wmax; w >= std::min(16, wmax) && w >= 1; --w) {
+        const int64_t slots = (int64_t)d.sms * w, cost = (total_tiles + slots - 1) / slots * w;
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = w;
+        }
+    }
+    pl->warps = best;
     pl->fixed = tables + (size_t)pl->warps * per_warp;
     pl->per_pass = (int)std::min<size_t>(batch, (d.smem_optin - pl->fixed) / pl->xrow);
     if (pl->per_pass < 1) return EC_ERR_UNSUPPORTED;
