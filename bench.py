@@ -61,7 +61,7 @@ def profiled_traffic():
         return None
     txt = open(PROFILE).read()
     m = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
-    t = re.search(r"dram_bytes_per_token:\s*([0-9.eE+]+)", txt)
+    t = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
     if not m or not t or m.group(1) != kernel_hash():
         return None
     return float(t.group(1))
