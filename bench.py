@@ -428,6 +428,17 @@ def batch_sweep(torch, ec, stack, stream, device):
     return out
 
 
+def aggregate_ranks(torch, dist, us_local: float, world: int, device: str):
+    """Replicas: every rank decodes its own token per step.  The step time is the
+    slowest rank's (max over ranks); the whole job makes `world` tokens per step,
+    so microseconds per token = step time / world."""
+    t = torch.tensor([us_local], dtype=torch.float64, device=device)
+    if dist is not None and world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    us_step = float(t.item())
+    return us_step, us_step / world
+
+
 # ------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -496,11 +507,7 @@ def main():
         nbytes = sum(stack.mats[0][n].stats()["device_bytes"] for n in names)
         groups[gname] = {"us": round(us_g, 2), "compressed_gbs": round(nbytes / us_g / 1e3, 1)}
 
-    t_max = torch.tensor([us_ec], device="cuda")
-    if world > 1:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    us_step = float(t_max.item())
-    value = us_step / world  # replicas: `world` tokens per step
+    us_step, value = aggregate_ranks(torch, dist if world > 1 else None, us_ec, world, "cuda")
 
     peak, peak_kind = peaks()
     per_launch_bytes = stack.algo_bytes / len(stack.calls)
