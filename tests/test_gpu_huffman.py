@@ -174,3 +174,42 @@ def test_empty_and_zero_k(ec):
     W0 = ec.encode_bf16(np.zeros((0, 64), np.uint16))
     ec.decode(W0, torch.zeros(8, dtype=torch.int16, device="cuda"))
     assert ec.status() == 0
+
+
+def test_block_70b_decode_batch_is_bit_exact(ec):
+    """One 70B-shaped decoder block (q, o 8192^2; k, v 1024x8192; gate, up
+    28672x8192; down 8192x28672; 855.6 M weights) decoded to BF16 by a single
+    ec_decode_batch launch, as timed by the bench: every weight equals the input."""
+    Ws, outs, refs = [], [], []
+    for s in synth.block_70b():
+        w = synth.make_weights(s)
+        Ws.append(ec.encode_bf16(w))
+        refs.append(torch.from_numpy(w.view(np.int16)).cuda())
+        outs.append(torch.empty((s.n_rows, s.k_cols), dtype=torch.int16, device="cuda"))
+        del w
+    ec.decode_batch(Ws, outs)
+    assert ec.status() == 0
+    for s, o, r in zip(synth.block_70b(), outs, refs):
+        assert torch.equal(o, r), s.name
+
+
+def test_full_size_layer_grouped_batch16_sampled_rows(ec):
+    """The 8B layer set at batch 16 through the grouped launches the bench times
+    (q/k/v, o, gate/up, down); 96 sampled rows of every matrix against the oracle's
+    FP64 GEMV of those rows."""
+    specs = {s.name.split(".")[-1]: s for s in synth.layer_8b()}
+    groups = [["q", "k", "v"], ["o"], ["gate", "up"], ["down"]]
+    rng = np.random.default_rng(7)
+    for names in groups:
+        ws = [synth.make_weights(specs[n]) for n in names]
+        Ws = [ec.encode_bf16(w) for w in ws]
+        x = synth.make_x(specs[names[0]].seed, 16, specs[names[0]].k_cols)
+        ys = [torch.full((16, specs[n].n_rows), float("nan"), device="cuda") for n in names]
+        ec.gemv_group(Ws, dev(x.view(np.int16)), ys, batch=16)
+        assert ec.status() == 0
+        for n, w, y in zip(names, ws, ys):
+            rows = np.sort(rng.choice(w.shape[0], 96, replace=False))
+            y_ref, a_ref = O.gemv_bf16(np.ascontiguousarray(w[rows]), x)
+            check_gemv(y.cpu().numpy()[:, rows], y_ref, a_ref, f"{n} batch 16")
+        for W in Ws:
+            W.free()
