@@ -1199,14 +1199,16 @@ int plan_huff_gemv(const DeviceInfo& d, int count, int code_bytes, int64_t kp, i
     const int cap = huff_max_warps(batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : batch <= 8 ? 8 : 16);
     const int wmax = (int)std::min<size_t>(cap, (d.smem_optin - tables - pl->xrow) / per_warp);
     /* Each warp takes every (grid * warps)-th tile, so a launch lasts ceil(tiles /
-     * (sms * w)) rounds of one tile per warp, and a round takes time in proportion
-     * to the warps sharing an SM (the SM is issue-bound from about 16 warps on):
-     * pick the w in [min(16, wmax), wmax] with the fewest rounds * w, the larger
-     * on ties. */
+     * (sms * w)) rounds of one tile per warp.  Below about 24 warps an SM is
+     * latency-bound and a round takes the same time whatever w; above, it is
+     * issue-bound and a round takes time in proportion to w.  Pick the w with the
+     * fewest rounds * max(w, 24), the larger on ties. */
+    constexpr int kKnee = 24;
     int best = wmax;
     int64_t best_cost = INT64_MAX;
-    for (int w = wmax; w >= std::min(16, wmax) && w >= 1; --w) {
-        const int64_t slots = (int64_t)d.sms * w, cost = (total_tiles + slots - 1) / slots * w;
+    for (int w = wmax; w >= 1; --w) {
+        const int64_t slots = (int64_t)d.sms * w;
+        const int64_t cost = (total_tiles + slots - 1) / slots * std::max(w, kKnee);
         if (cost < best_cost) {
             best_cost = cost;
             best = w;
