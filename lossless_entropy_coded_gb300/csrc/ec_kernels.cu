@@ -1,29 +1,30 @@
 /*
  * ec_kernels.cu -- sm_103a kernels and the device-side entry points of the C ABI
- * (ec_decode, ec_decode_batch, ec_gemv, ec_gemv_group, ec_bf16_gemv, ec_status).
+ * (ec_decode, ec_decode_batch, ec_gemv, ec_gemv_group, ec_gemv_static,
+ * ec_bf16_gemv, ec_status).
  *
  * Huffman path (DFloat11, "70% Size, 100% Accuracy", Algorithm 1, re-cut for the
- * fused product of MINE section 4 "Fused mvm"):
- *   one warp owns one tile of 32 * steps weights.  Each lane decodes its own
- *   codeword sequence (positions l, l + 32, ...) from a byte offset stored in the
- *   tile record, with a 12-bit level-1 table in shared memory and 8-bit
- *   sub-tables behind pointer entries (the hierarchical LUTs of Fig. 4 / 14).
- *   Decoded exponent fields go to a per-warp shared-memory stage, 1024 weights at
- *   a time; the stage is then read back 8 consecutive weights per lane and merged
- *   with the raw sign/mantissa bytes:
- *       bf16 = (sign << 15) | (exponent << 7) | mantissa      (Algorithm 1 / Eq. (1))
- *   and either stored (decode) or multiplied with x in FP32 (GEMV).  Partial sums
- *   of a row are reduced across the warp with shuffles and written once, or added
- *   atomically when a row spans several tiles.
+ * fused product of MINE section 4 "Fused mvm"): one warp owns one tile of
+ * 32 * steps weights; lane l decodes its own codeword sequence (positions l,
+ * l + 32, ...) from a byte offset stored in the tile record.  Every lookup of a
+ * 12-bit pair table in shared memory yields two exponents already in BF16
+ * position; a window whose two codewords do not both fit takes a second lookup,
+ * and codewords longer than the window (only when the caller asks for a limit
+ * above 12 bits) walk the hierarchical table of DFloat11 Fig. 4 / 14 in global
+ * memory.  The decoded pair is merged with the raw sign/mantissa bytes
+ *     bf16 = (sign << 15) | (exponent << 7) | mantissa      (Algorithm 1 / Eq. (1))
+ * in registers and either stored (decode, through a small shared transpose) or
+ * multiplied with x in FP32 (GEMV).  Row sums are reduced across the warp with
+ * shuffles and written once, or added atomically when a row spans tiles.
  *
- * rANS path (EntroPack section 3.6, appendix C.3): one warp per tile, lane l
+ * rANS path (EntroPack, independent rANS tiles): one warp per tile, lane l
  * decodes positions 32 j + l; a lane whose state drops below 2^16 pulls the next
  * 16-bit word, the lanes of one step taking consecutive words in lane order
  * (ballot + popc).  w = code * scale (FP16 scale per 128 weights) is exact in FP32.
  *
  * Robustness: every loop has a fixed trip count; reads of code words, sub-tables
- * and payload words are clamped to the tile / table and an out-of-range index sets
- * the device status word (EC_ERR_CORRUPT) instead of faulting.
+ * and payload words are clamped to the tile / table and inconsistent records or
+ * streams set the device status word (EC_ERR_CORRUPT) instead of faulting.
  */
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -876,7 +877,7 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) rans_kernel(const _
                     const uint32_t bal = __ballot_sync(kFull, need);
                     const uint32_t idx = min(wp + __popc(bal & lt), cap);
                     const uint32_t v = lds16_if(need, wbase + 2 * idx, 0u);
-                    x = need ? (x << 16) | v : x;
+                    x = need ? x * 65536u + v : x; /* v < 2^16 and x < 2^16: the shift-or as one multiply-add */
                     wp += __popc(bal);
                     /* code + 8 in the low 4 bits: (float)code = (2^23 + code + 8) - (2^23 + 8) */
                     const float cf = __int_as_float(0x4B000000 | (e & 15u)) - 8388616.0f;
