@@ -58,7 +58,6 @@ enum {
 
 #define EC_MAX_BATCH 16
 #define EC_DEFAULT_MAX_CODE_LEN 12
-#define EC_DEFAULT_TILE_STEPS 128
 #define EC_MAX_GROUP 8
 #define EC_MAX_DECODE_BATCH 64
 
@@ -72,10 +71,11 @@ typedef struct ec_matrix ec_matrix; /* opaque: host descriptor + one device blob
  *                weights the limit costs about 0.004 bits per exponent over
  *                the unconstrained code.  Longer limits decode through a
  *                hierarchical table in global memory, more slowly.
- *  tile_steps    symbols per lane in one tile of 32 lanes; 32, 64 or 128 (default
- *                EC_DEFAULT_TILE_STEPS = 128, i.e. 4096-weight tiles: 0.125 bit
- *                per weight of lane offsets; 64 doubles that but needs half the
- *                per-warp shared memory). */
+ *  tile_steps    symbols per lane in one tile of 32 lanes: 32, 64 or 128, or 0
+ *                (the default) to choose by size: 128 (4096-weight tiles, 0.125
+ *                bit per weight of lane offsets) for matrices of at least 4 M
+ *                padded weights, 64 from 2 M, else 32, so that a matrix has about
+ *                1024 tiles or more to spread over the SMs. */
 typedef struct {
     int32_t max_code_len;
     int32_t tile_steps;

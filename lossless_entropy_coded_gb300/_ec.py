@@ -162,7 +162,7 @@ class Matrix:
             pass
 
 
-def encode_bf16(w, max_code_len: int = 12, tile_steps: int = 128, device: int = 0) -> Matrix:
+def encode_bf16(w, max_code_len: int = 12, tile_steps: int = 0, device: int = 0) -> Matrix:
     """Huffman-exponent encode a host BF16 matrix [N, K] (uint16 bit patterns)."""
     n, k = int(w.shape[0]), int(w.shape[1])
     p, keep = _host_ptr(w)

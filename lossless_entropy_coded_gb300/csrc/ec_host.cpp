@@ -370,13 +370,15 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
     *out = nullptr;
     if (n_rows < 0 || k_cols < 0) return EC_ERR_SHAPE;
     const int max_len = params ? params->max_code_len : EC_DEFAULT_MAX_CODE_LEN;
-    const int steps = params ? params->tile_steps : EC_DEFAULT_TILE_STEPS;
+    int steps = params ? params->tile_steps : 0;
     if (max_len < 1 || max_len > EC_MAX_CODE_LEN) return EC_ERR_INVALID_ARG;
-    if (steps != 32 && steps != 64 && steps != 128) return EC_ERR_INVALID_ARG;
+    if (steps != 0 && steps != 32 && steps != 64 && steps != 128) return EC_ERR_INVALID_ARG;
     int64_t nk = 0, k_pad = round_up(k_cols, EC_HUFF_ROW_ALIGN), n_pad = 0, tmp = 0;
     if (k_cols > INT64_MAX - EC_HUFF_ROW_ALIGN) return EC_ERR_OVERFLOW;
     if (!mul_ok(n_rows, k_cols, &nk) || !mul_ok(n_rows, k_pad, &n_pad) || !mul_ok(n_pad, 4, &tmp))
         return EC_ERR_OVERFLOW;
+    if (steps == 0) /* automatic: at least 1024 tiles where the matrix allows it */
+        steps = n_pad >= (int64_t)1024 * 32 * 128 ? 128 : n_pad >= (int64_t)1024 * 32 * 64 ? 64 : 32;
     if (nk > 0 && !w) return EC_ERR_INVALID_ARG;
 
     return guarded([&]() -> int {
