@@ -58,6 +58,8 @@ struct HuffMat {
     int32_t steps, atomic_y;
     int32_t last_steps;         /* symbols per lane of the last tile */
     uint32_t rec16;             /* records region size in 16-byte units */
+    int64_t d_row;              /* GEMV: rows and columns a warp's next tile lies past */
+    int64_t d_col;              /*   its current one (the launch's warps x tile width) */
 };
 
 struct HuffGemvArgs {
@@ -334,9 +336,10 @@ __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.w
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
 
 /* Per-warp shared memory: two tile buffers, each the 64 bytes of lane starts, the
- * code area and slack.  Multiples of 16 bytes when code_bytes is. */
+ * code area and slack, then the two buffers' mbarriers (8 bytes each).  Multiples
+ * of 16 bytes when code_bytes is. */
 __host__ __device__ constexpr size_t tile_buf_bytes(int code_bytes) { return 64 + (size_t)code_bytes + kSlackBytes; }
-__host__ __device__ constexpr size_t huff_warp_bytes(int code_bytes) { return 2 * tile_buf_bytes(code_bytes); }
+__host__ __device__ constexpr size_t huff_warp_bytes(int code_bytes) { return 2 * tile_buf_bytes(code_bytes) + 16; }
 static_assert(kSlackBytes % 16 == 0 && kSlackBytes >= 8 * 48 / 8 + 16 && kPairTabBytes % 16 == 0, "alignment");
 static_assert(huff_warp_bytes(16) % 16 == 0 && huff_warp_bytes(4112) % 16 == 0, "per-warp block alignment");
 
@@ -413,14 +416,55 @@ __device__ __forceinline__ TileRef tile_ref(const Args& a, int64_t g, uint2 off)
     return r;
 }
 
-/* Start the copy of a tile's lane starts and code area into a tile buffer. */
-__device__ __forceinline__ void prefetch_code(uint32_t buf, const TileRef& r, int lane) {
-    if (r.area > 0) {
-        const uint8_t* area = r.rec + 64 + EC_RAW_BYTES(r.S);
-        if (lane < 4) cp_async16(buf + 16 * lane, r.rec + 16 * lane);
-        for (int i = lane; i < r.area / 16; i += 32) cp_async16(buf + 64 + 16 * i, area + 16 * i);
+/* mbarrier and bulk-copy helpers (one arrival per phase: the issuing lane's). */
+__device__ __forceinline__ void mbar_init(uint32_t mbar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(mbar)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t mbar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+/* Wait for phase `parity` of mbar with a bound on the attempts (each of which may
+ * suspend the thread for a while); false when the bound ran out. */
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
+    for (int i = 0; i < (1 << 20); ++i)
+        if (mbar_try_wait(mbar, parity)) return true;
+    return false;
+}
+
+/* Start the copy of a tile's lane starts (64 bytes) and code area into a tile
+ * buffer: one lane arms the buffer's mbarrier with the byte count and issues two
+ * bulk copies (16-byte aligned, multiples of 16 bytes); a corrupt record only
+ * arrives, so the phase still completes. */
+__device__ __forceinline__ void prefetch_code(uint32_t buf, uint32_t mbar, const TileRef& r, int lane) {
+    if (lane == 0) {
+        if (r.area > 0) {
+            mbar_arrive_tx(mbar, 64u + (uint32_t)r.area);
+            bulk_g2s(buf, r.rec, 64u, mbar);
+            bulk_g2s(buf + 64, r.rec + 64 + EC_RAW_BYTES(r.S), (uint32_t)r.area, mbar);
+        } else {
+            mbar_arrive_tx(mbar, 0u);
+        }
     }
-    cp_async_commit();
 }
 
 /* Walk combined tiles g0, g0 + stride, ... < g_end.  The first tile's copy must
@@ -433,21 +477,25 @@ __device__ __forceinline__ void prefetch_code(uint32_t buf, const TileRef& r, in
  * next tile are loaded the same way at the end of the current one. */
 template <bool kLong, class Args, class TabOf, class Begin, class Block, class Half, class End>
 __device__ __forceinline__ void huff_walk(const Args& a, int64_t g0, int64_t stride, int64_t g_end, TileRef cur,
-                                          uint32_t bufs, uint32_t buf_bytes, int lane, TabOf&& tab_of,
-                                          Begin&& begin, Block&& block, Half&& half, End&& end) {
+                                          uint32_t bufs, uint32_t buf_bytes, uint32_t& ph, int lane,
+                                          TabOf&& tab_of, Begin&& begin, Block&& block, Half&& half, End&& end) {
+    const uint32_t mbars = bufs + 2 * buf_bytes;
     uint2 off_next = g0 + stride < g_end ? tile_offsets(a, g0 + stride) : make_uint2(0u, 0u);
     uint4 rr[2] = {};
     bool raw_ready = false;
     uint32_t cb = bufs; /* buffer of the current tile */
     for (int64_t g = g0; g < g_end; g += stride) {
-        cp_async_wait_all();
-        __syncwarp(); /* the current tile's copy is visible; every lane is done with the other buffer */
+        const uint32_t bi = cb == bufs ? 0u : 1u;
+        const bool arrived = mbar_wait(mbars + 8 * bi, (ph >> bi) & 1u); /* the current tile's copy */
+        ph ^= 1u << bi;
+        __syncwarp(); /* every lane is done with the other buffer */
+        if (!arrived) cur.area = 0; /* (never seen: the copy did not complete in time) */
         const uint32_t nb_buf = cb == bufs ? bufs + buf_bytes : bufs; /* the next tile's buffer */
         const bool has_next = g + stride < g_end;
         TileRef nxt{};
         if (has_next) {
             nxt = tile_ref(a, g + stride, off_next);
-            prefetch_code(nb_buf, nxt, lane);
+            prefetch_code(nb_buf, mbars + 8 * (bi ^ 1u), nxt, lane);
             if (g + 2 * stride < g_end) off_next = tile_offsets(a, g + 2 * stride);
         }
         if (cur.area == 0) {
@@ -531,10 +579,18 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
 
     const int nwarp = blockDim.x >> 5;
     const int64_t gw = (int64_t)blockIdx.x * nwarp + warp, nw = (int64_t)gridDim.x * nwarp;
+    const uint32_t mbars = bufs + 2 * buf_bytes;
+    if (lane == 0) {
+        mbar_init(mbars);
+        mbar_init(mbars + 8);
+        mbar_fence_init();
+    }
+    __syncwarp();
+    uint32_t ph = 0; /* parity of the next phase of each buffer's mbarrier */
     TileRef first{};
     if (gw < a.total_tiles) {
         first = tile_ref(a, gw, tile_offsets(a, gw));
-        prefetch_code(bufs, first, lane);
+        prefetch_code(bufs, mbars, first, lane);
     }
     for (int k = 0; k < a.count; ++k) {
         const uint4* src = (const uint4*)a.m[k].table;
@@ -547,6 +603,8 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
     if (gw >= a.total_tiles) return;
 
     const uint32_t jrow = kp / 32;
+    int prev_mi = -1;
+    int64_t prev_t = 0, row0 = 0, col0 = 0; /* where this warp's current tile starts */
     float acc[B][2];
     /* x of the current 8 symbols: loaded one half-block ahead for narrow batches,
      * at use for wide ones (whose registers go to the accumulators) */
@@ -585,13 +643,27 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
         }
     };
     huff_walk<kLong>(
-        a, gw, nw, a.total_tiles, first, bufs, buf_bytes, lane, [&](int mi) { return tabs_s + mi * kPairTabBytes; },
+        a, gw, nw, a.total_tiles, first, bufs, buf_bytes, ph, lane,
+        [&](int mi) { return tabs_s + mi * kPairTabBytes; },
         [&](const TileRef& r) {
             Mp = &a.m[r.mi];
             t_cur = r.t;
-            const int64_t T = 32 * (int64_t)Mp->steps;
-            row = tile_row(r.t, T, kp, EC_HUFF_ROW_ALIGN);
-            jc = (uint32_t)(r.t * T - row * (int64_t)kp) / 32;
+            if (r.mi == prev_mi && r.t == prev_t + nw) { /* the same matrix, the next tile of this warp */
+                row0 += Mp->d_row;
+                col0 += Mp->d_col;
+                if (col0 >= kp) {
+                    col0 -= kp;
+                    ++row0;
+                }
+            } else {
+                const int64_t T = 32 * (int64_t)Mp->steps;
+                row0 = tile_row(r.t, T, kp, EC_HUFF_ROW_ALIGN);
+                col0 = r.t * T - row0 * (int64_t)kp;
+            }
+            prev_mi = r.mi;
+            prev_t = r.t;
+            row = row0; /* advanced by the block hook as rows end inside the tile */
+            jc = (uint32_t)col0 / 32;
             if (kAhead) load_x(jc);
 #pragma unroll
             for (int b = 0; b < B; ++b) acc[b][0] = acc[b][1] = 0.f;
@@ -636,6 +708,14 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_decode_kernel(const __gri
     uint8_t* wbase = smem + kPairTabBytes + (size_t)warp * decode_warp_bytes(a.code_bytes);
     const uint32_t bufs = smem_u32(wbase), buf_bytes = (uint32_t)tile_buf_bytes(a.code_bytes);
     const uint32_t tbuf = bufs + (uint32_t)huff_warp_bytes(a.code_bytes), tab_s = smem_u32(tab);
+    const uint32_t mbars = bufs + 2 * buf_bytes;
+    if (lane == 0) {
+        mbar_init(mbars);
+        mbar_init(mbars + 8);
+        mbar_fence_init();
+    }
+    __syncwarp();
+    uint32_t ph = 0; /* parity of the next phase of each buffer's mbarrier */
     grid_dep_launch();
     grid_dep_wait();
 
@@ -648,7 +728,7 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_decode_kernel(const __gri
         TileRef first{};
         if (g0 < mend) {
             first = tile_ref(a, g0, tile_offsets(a, g0));
-            prefetch_code(bufs, first, lane);
+            prefetch_code(bufs, mbars, first, lane);
         }
         __syncthreads();
         const uint4* src = (const uint4*)M.table;
@@ -659,7 +739,7 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_decode_kernel(const __gri
         int64_t row = 0, col0 = 0;
         if (g0 < mend)
             huff_walk<kLong>(
-                a, g0, nwarp, mend, first, bufs, buf_bytes, lane, [&](int) { return tab_s; },
+                a, g0, nwarp, mend, first, bufs, buf_bytes, ph, lane, [&](int) { return tab_s; },
                 [&](const TileRef& r) {
                     const int64_t T = 32 * (int64_t)M.steps;
                     row = tile_row(r.t, T, kp, EC_HUFF_ROW_ALIGN);
@@ -1192,6 +1272,13 @@ struct GemvPlan {
     size_t fixed, xrow;
 };
 
+/* Rows and columns between a tile and the one `warps_total` tiles later. */
+void set_tile_stride(HuffMat& m, int64_t warps_total) {
+    const int64_t span = warps_total * 32 * (int64_t)m.steps;
+    m.d_row = m.k_pad > 0 ? span / m.k_pad : 0;
+    m.d_col = m.k_pad > 0 ? span % m.k_pad : 0;
+}
+
 int plan_huff_gemv(const DeviceInfo& d, int count, int code_bytes, int64_t kp, int batch, int64_t total_tiles,
                    GemvPlan* pl) {
     const size_t tables = (size_t)count * kPairTabBytes, per_warp = huff_warp_bytes(code_bytes);
@@ -1252,6 +1339,7 @@ int huff_gemv(const ec_matrix* const* Ws, int count, const uint16_t* x, float* c
     GemvPlan pl;
     int rc = plan_huff_gemv(*d, count, code_bytes, kp, batch, total, &pl);
     if (rc != EC_OK) return rc;
+    for (int k = 0; k < count; ++k) set_tile_stride(a.m[k], (int64_t)pl.grid * pl.warps);
     for (int b0 = 0; b0 < batch; b0 += pl.per_pass) {
         const int nb = std::min(pl.per_pass, batch - b0);
         a.batch = nb;
@@ -1521,6 +1609,7 @@ extern "C" int ec_gemv_static(const ec_matrix* W, const uint16_t* x, float* y, i
     di.sms = d->sms;
     di.smem_optin = d->smem_optin;
     if ((rc = plan_huff_gemv(di, 1, a.code_bytes, h.k_pad, batch, h.n_tiles, &pl)) != EC_OK) return rc;
+    set_tile_stride(a.m[0], (int64_t)pl.grid * pl.warps);
     for (int b0 = 0; b0 < batch; b0 += pl.per_pass) {
         const int nb = std::min(pl.per_pass, batch - b0);
         a.batch = nb;
