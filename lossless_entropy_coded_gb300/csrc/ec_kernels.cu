@@ -1286,26 +1286,30 @@ int plan_huff_gemv(const DeviceInfo& d, int count, int code_bytes, int64_t kp, i
     if (tables + pl->xrow + 4 * per_warp > d.smem_optin) return EC_ERR_UNSUPPORTED;
     const int cap = huff_max_warps(batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : batch <= 8 ? 8 : 16);
     const int wmax = (int)std::min<size_t>(cap, (d.smem_optin - tables - pl->xrow) / per_warp);
-    /* Each warp takes every (grid * warps)-th tile, so a launch lasts ceil(tiles /
+    /* Each warp takes every (grid * warps)-th tile, so a pass lasts ceil(tiles /
      * (sms * w)) rounds of one tile per warp.  Below about 24 warps an SM is
      * latency-bound and a round takes the same time whatever w; above, it is
-     * issue-bound and a round takes time in proportion to w.  Pick the w with the
-     * fewest rounds * max(w, 24), the larger on ties. */
+     * issue-bound and a round takes time in proportion to w.  Batch rows whose x
+     * does not fit next to the warps' buffers take further passes, each decoding
+     * the matrices again.  Pick the w with the fewest passes * rounds * max(w, 24),
+     * the larger on ties. */
     constexpr int kKnee = 24;
-    int best = wmax;
+    int best = wmax, best_rows = 1;
     int64_t best_cost = INT64_MAX;
     for (int w = wmax; w >= 1; --w) {
-        const int64_t slots = (int64_t)d.sms * w;
-        const int64_t cost = (total_tiles + slots - 1) / slots * std::max(w, kKnee);
+        const size_t fixed = tables + (size_t)w * per_warp;
+        const int rows = (int)std::min<size_t>(batch, (d.smem_optin - fixed) / pl->xrow);
+        const int64_t passes = (batch + rows - 1) / rows, slots = (int64_t)d.sms * w;
+        const int64_t cost = passes * ((total_tiles + slots - 1) / slots) * std::max(w, kKnee);
         if (cost < best_cost) {
             best_cost = cost;
             best = w;
+            best_rows = rows;
         }
     }
     pl->warps = best;
     pl->fixed = tables + (size_t)pl->warps * per_warp;
-    pl->per_pass = (int)std::min<size_t>(batch, (d.smem_optin - pl->fixed) / pl->xrow);
-    if (pl->per_pass < 1) return EC_ERR_UNSUPPORTED;
+    pl->per_pass = best_rows;
     pl->grid = (int)std::max<int64_t>(1, std::min<int64_t>(d.sms, (total_tiles + pl->warps - 1) / pl->warps));
     return EC_OK;
 }
