@@ -280,6 +280,57 @@ class OracleSample:
                 f"to the {self.token_weights} weights of one token")
 
 
+def oracle_timings():
+    """The oracle on configs 1, 2 and 4 (the 1024x1024 matrix, the 8B layer set, one
+    rANS shape): decode + FP64 GEMV, timed single-threaded and on all host cores.
+    The work is cut into independent row blocks of 1024 rows, each encoded on its
+    own outside the timed part; all cores run the blocks in a thread pool (the
+    oracle's C calls release the GIL), single-threaded runs them in order."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle as O
+    import synth
+    cores = os.cpu_count() or 1
+
+    def blocks_bf16(specs):
+        jobs = []
+        for s in specs:
+            w = synth.make_weights(s)
+            x = synth.make_x(s.seed, 1, s.k_cols)
+            for r0 in range(0, s.n_rows, 1024):
+                wb = np.ascontiguousarray(w[r0:r0 + 1024])
+                d = O.DF11(wb)
+                jobs.append(lambda d=d, shape=wb.shape, x=x: O.gemv_bf16(d.decode().reshape(shape), x))
+        return jobs
+
+    def blocks_rans(idx):
+        codes, scales = synth.make_rans_case(idx)
+        n, k = codes.shape
+        x = synth.make_x(4000 + idx, 1, k)
+        jobs = []
+        for r0 in range(0, n, 1024):
+            cb, sb = np.ascontiguousarray(codes[r0:r0 + 1024]), np.ascontiguousarray(scales[r0:r0 + 1024])
+            rc = O.Rans(cb)
+            jobs.append(lambda rc=rc, cb=cb, sb=sb, x=x: (rc.decode(), O.gemv_rans(cb, sb, x)))
+        return jobs
+
+    out = {"cores": cores, "unit": "s", "blocks": "1024 rows, encoded outside the timed part"}
+    for name, make in (("config1_1024x1024", lambda: blocks_bf16([synth.single_1024()])),
+                       ("config2_8b_layer_set", lambda: blocks_bf16(synth.layer_8b())),
+                       ("config4_rans_14336x4096", lambda: blocks_rans(0))):
+        jobs = make()
+        t0 = time.perf_counter()
+        for j in jobs:
+            j()
+        single = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        with ThreadPoolExecutor(cores) as ex:
+            list(ex.map(lambda j: j(), jobs))
+        allc = time.perf_counter() - t0
+        out[name] = {"single_thread_s": round(single, 3), "all_cores_s": round(allc, 3)}
+    return out
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -522,6 +573,7 @@ def main():
         sample = OracleSample()
         v, dt = sample.run()
         cpu = {"value": round(v, 1), "unit": "us/token", "cores": 1, "kind": "oracle", "sample": sample.describe(dt)}
+        ex["oracle_timings"] = oracle_timings()
 
     if rank == 0:
         line = {
