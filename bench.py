@@ -456,6 +456,38 @@ def batch_sweep(torch, ec, stack, stream, device):
                 ec.gemv_group(Ws, x, ys, batch=b)
         sweep[str(b)] = round(t_graph(run) / n_l, 1)
     out["batch_sweep_us_per_layer_set"] = sweep
+
+    # materialisation for larger batches: decode each layer's matrices to BF16
+    # (one ec_decode_batch launch per layer) and multiply with cuBLAS, against
+    # cuBLAS on the uncompressed BF16 weights; per layer set
+    F, bf = torch.nn.functional, torch.bfloat16
+    dec = [{n: torch.empty((s.n_rows, s.k_cols), dtype=torch.int16, device=dev) for n, s in stack.specs[l].items()}
+           for l in range(n_l)]
+    mat, ref = {}, {}
+    for b in (16, 64, 256):
+        xs = {}
+        for l in range(n_l):
+            for gname, names in Stack.GROUPS:
+                k = stack.specs[l][names[0]].k_cols
+                xs[(l, gname)] = torch.randn((b, k), device=dev).to(bf)
+
+        def run_mat(b=b, xs=xs):
+            for l in range(n_l):
+                names = list(stack.specs[l])
+                ec.decode_batch([stack.mats[l][n] for n in names], [dec[l][n] for n in names])
+                for gname, gn in Stack.GROUPS:
+                    for n in gn:
+                        F.linear(xs[(l, gname)], dec[l][n].view(bf))
+
+        def run_ref(b=b, xs=xs):
+            for l in range(n_l):
+                for gname, gn in Stack.GROUPS:
+                    for n in gn:
+                        F.linear(xs[(l, gname)], stack.bf16[l][n].view(bf))
+        mat[str(b)] = round(t_graph(run_mat) / n_l, 1)
+        ref[str(b)] = round(t_graph(run_ref) / n_l, 1)
+    out["materialize_gemm_us_per_layer_set"] = mat
+    out["bf16_cublas_gemm_us_per_layer_set"] = ref
     # the 24-bit limit (hierarchical-table kernel) on layer 0..n_l-1 at batch 1
     mats24, bufs = [], []
     for l in range(n_l):
