@@ -213,3 +213,46 @@ def test_full_size_layer_grouped_batch16_sampled_rows(ec):
             check_gemv(y.cpu().numpy()[:, rows], y_ref, a_ref, f"{n} batch 16")
         for W in Ws:
             W.free()
+
+
+def test_group_mixing_code_limits_uses_the_long_code_kernel(ec):
+    """A group whose matrices have different length limits (24 with codewords
+    longer than the pair window, and 12) runs as one launch of the kernel that
+    walks the hierarchical table, with every matrix's result exact."""
+    w_long = fib_weights()[:, :2048]
+    w_a = synth.llama_bf16(2600, w_long.shape[0], 2048)
+    Ws = [ec.encode_bf16(w_long, max_code_len=24), ec.encode_bf16(w_a)]
+    assert Ws[0].code_lengths().max() > 12 and Ws[1].code_lengths().max() <= 12
+    x = synth.make_x(2600, 3, 2048)
+    ys = [torch.full((3, w_long.shape[0]), float("nan"), device="cuda") for _ in Ws]
+    ec.gemv_group(Ws, dev(x.view(np.int16)), ys, batch=3)
+    assert ec.status() == 0
+    for w, y in zip((w_long, w_a), ys):
+        y_ref, a_ref = O.gemv_bf16(w, x)
+        check_gemv(y.cpu().numpy(), y_ref, a_ref, "mixed limits")
+
+
+def test_decode_batch_mixes_rans_and_huffman(ec):
+    w = synth.llama_bf16(2601, 96, 1536)
+    codes, scales = synth.make_rans_case(0, 40, 1024)
+    Ws = [ec.encode_bf16(w), ec.encode_rans(codes, scales)]
+    outs = [torch.zeros((96, 1536), dtype=torch.int16, device="cuda"),
+            torch.zeros((40, 1024), dtype=torch.int16, device="cuda")]
+    ec.decode_batch(Ws, outs)
+    assert ec.status() == 0
+    assert np.array_equal(outs[0].cpu().numpy().view(np.uint16), w)
+    assert np.array_equal(outs[1].cpu().numpy().view(np.uint16), O.rans_dequant_bf16(codes, scales))
+
+
+def test_misaligned_device_pointers_are_rejected(ec):
+    from lossless_entropy_coded_gb300 import _ec
+    w = synth.llama_bf16(2602, 32, 1024)
+    W = ec.encode_bf16(w)
+    x = torch.zeros(1024 + 8, dtype=torch.int16, device="cuda")
+    y = torch.zeros(32 + 4, dtype=torch.float32, device="cuda")
+    lib = ec.lib
+    assert lib.ec_gemv(W.handle, x.data_ptr() + 2, y.data_ptr(), 1, None) == _ec.EC_ERR_INVALID_ARG
+    assert lib.ec_gemv(W.handle, x.data_ptr(), y.data_ptr() + 4, 1, None) == _ec.EC_ERR_INVALID_ARG
+    out = torch.zeros(32 * 1024 + 8, dtype=torch.int16, device="cuda")
+    assert lib.ec_decode(W.handle, out.data_ptr() + 2, None) == _ec.EC_ERR_INVALID_ARG
+    assert ec.status() == 0
