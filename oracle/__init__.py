@@ -75,7 +75,9 @@ def _L():
         "orc_df11_sm_mut": ([vp], vp),
         "orc_df11_stream_mut": ([vp], vp),
         "orc_rans_freqs": ([vp, i32, vp], i32),
+        "orc_rans_freqs_n": ([vp, i32, i32, vp], i32),
         "orc_rans_encode": ([vp, i64, i32, i32], vp),
+        "orc_rans_encode_k": ([vp, i64, i32, i32, i32], vp),
         "orc_rans_decode": ([vp, vp, vp], i32),
         "orc_rans_free": ([vp], None),
         "orc_rans_info": ([vp, vp], i64),
@@ -260,10 +262,12 @@ class DF11:
 
 # --------------------------------------------------------------------------- rANS codec
 def rans_freqs(counts, prob_bits: int = 12) -> np.ndarray:
-    c = np.zeros(16, dtype=np.uint64)
+    """Normalised frequencies (sum 2^prob_bits) of a 16- or 256-symbol histogram."""
+    nsym = 16 if len(counts) <= 16 else 256
+    c = np.zeros(nsym, dtype=np.uint64)
     c[: len(counts)] = counts
-    out = np.zeros(16, dtype=np.uint32)
-    if _L().orc_rans_freqs(_p(c), prob_bits, _p(out)) < 0:
+    out = np.zeros(nsym, dtype=np.uint32)
+    if _L().orc_rans_freqs_n(_p(c), nsym, prob_bits, _p(out)) < 0:
         raise ValueError("cannot normalise")
     return out
 
@@ -271,10 +275,14 @@ def rans_freqs(counts, prob_bits: int = 12) -> np.ndarray:
 class Rans:
     """Independent-tile interleaved rANS encoding of 4-bit codes (-8..7)."""
 
-    def __init__(self, codes: np.ndarray, prob_bits: int = 12, tile: int = 4096):
+    def __init__(self, codes: np.ndarray, prob_bits: int = 12, tile: int = 4096, k: int = 1):
+        """k = codes per symbol: 1, or 2 for pair symbols (a lane's steps 2m, 2m+1;
+        the tile and the code count must then be multiples of 64)."""
         c = np.ascontiguousarray(codes, dtype=np.int8).ravel()
         self._c = c
-        h = _L().orc_rans_encode(_p(c) if c.size else 0, c.size, prob_bits, tile)
+        self.k = k
+        self.nsym = 16 if k == 1 else 256
+        h = _L().orc_rans_encode_k(_p(c) if c.size else 0, c.size, prob_bits, tile, k)
         if not h:
             raise ValueError("rANS encode failed")
         self._h = h
@@ -290,11 +298,11 @@ class Rans:
 
     @property
     def freqs(self):
-        return _view(_L().orc_rans_freqs_of(self._h), np.uint32, 16)
+        return _view(_L().orc_rans_freqs_of(self._h), np.uint32, self.nsym)
 
     @property
     def counts(self):
-        return _view(_L().orc_rans_counts_of(self._h), np.uint64, 16)
+        return _view(_L().orc_rans_counts_of(self._h), np.uint64, self.nsym)
 
     @property
     def states(self):

@@ -537,33 +537,36 @@ uint8_t* orc_df11_sm_mut(orc_df11* d) { return d->sm; }
 uint8_t* orc_df11_stream_mut(orc_df11* d) { return d->stream; }
 
 /* ===========================================================================
- * rANS tile codec (EntroPack section 3.6, appendix C.3; rANS after Duda 2013).
+ * rANS tile codec (EntroPack section 3.6, appendix C.3; rANS after Duda 2013),
+ * with MINE's k-tuple symbols (section 4, dtANS-LLM: "Pair" for k = 2).
  *
- * Alphabet: 4-bit codes -8..7 as symbols 0..15.  One frequency table per matrix
- * with sum 2^prob_bits.  The matrix is flattened row-major and cut into tiles of
- * `tile` symbols (the last may be short).  Inside a tile, position q = 32*j + l
- * belongs to lane l, step j.  State x lives in [2^16, 2^32); payload words are
- * 16 bits; the encoder starts every lane at x = 2^16.
+ * Alphabet: 4-bit codes -8..7 as values 0..15; a symbol is one code (k = 1) or the
+ * codes of a lane's steps 2m and 2m+1 (k = 2), symbol = 16 * (c0 + 8) + (c1 + 8).
+ * One frequency table per matrix with sum 2^prob_bits.  The matrix is flattened
+ * row-major and cut into tiles of `tile` codes (the last may be short).  Inside a
+ * tile, position q = 32*j + l belongs to lane l, step j.  State x lives in
+ * [2^16, 2^32); payload words are 16 bits; the encoder starts every lane at
+ * x = 2^16.
  * ========================================================================= */
 
 /* reading: f_s = max(1, floor(M*c_s/n)) for present s; while the sum is short,
  * add 1 to the present symbol with the largest remainder M*c_s - f_s*n (ties to
  * the lower symbol); while it is over, take 1 from the present symbol with f_s > 1
  * and the smallest remainder (ties to the lower symbol).  Absent symbols get 0. */
-int orc_rans_freqs(const uint64_t counts[16], int prob_bits, uint32_t freqs[16]) {
+int orc_rans_freqs_n(const uint64_t* counts, int nsym, int prob_bits, uint32_t* freqs) {
     const int64_t M = (int64_t)1 << prob_bits;
     uint64_t n = 0;
     int present = 0;
-    for (int s = 0; s < 16; ++s) {
+    for (int s = 0; s < nsym; ++s) {
         n += counts[s];
         present += counts[s] != 0;
     }
-    memset(freqs, 0, 16 * sizeof(uint32_t));
+    memset(freqs, 0, (size_t)nsym * sizeof(uint32_t));
     if (n == 0) return 0;
     if (present > M) return -1;
-    __int128 rem[16];
+    __int128* rem = (__int128*)calloc((size_t)nsym, sizeof(__int128));
     int64_t sum = 0;
-    for (int s = 0; s < 16; ++s) {
+    for (int s = 0; s < nsym; ++s) {
         if (!counts[s]) continue;
         int64_t f = (int64_t)(((unsigned __int128)M * counts[s]) / n);
         if (f < 1) f = 1;
@@ -573,7 +576,7 @@ int orc_rans_freqs(const uint64_t counts[16], int prob_bits, uint32_t freqs[16])
     }
     while (sum < M) {
         int best = -1;
-        for (int s = 0; s < 16; ++s)
+        for (int s = 0; s < nsym; ++s)
             if (counts[s] && (best < 0 || rem[s] > rem[best])) best = s;
         freqs[best]++;
         rem[best] -= (__int128)n;
@@ -581,22 +584,30 @@ int orc_rans_freqs(const uint64_t counts[16], int prob_bits, uint32_t freqs[16])
     }
     while (sum > M) {
         int best = -1;
-        for (int s = 0; s < 16; ++s)
+        for (int s = 0; s < nsym; ++s)
             if (counts[s] && freqs[s] > 1 && (best < 0 || rem[s] < rem[best])) best = s;
-        if (best < 0) return -1;
+        if (best < 0) {
+            free(rem);
+            return -1;
+        }
         freqs[best]--;
         rem[best] += (__int128)n;
         --sum;
     }
+    free(rem);
     return present;
 }
 
+int orc_rans_freqs(const uint64_t counts[16], int prob_bits, uint32_t freqs[16]) {
+    return orc_rans_freqs_n(counts, 16, prob_bits, freqs);
+}
+
 typedef struct {
-    int64_t n;            /* symbols */
-    int prob_bits, tile;
+    int64_t n;            /* codes */
+    int prob_bits, tile, k, nsym;
     int64_t n_tiles;
-    uint32_t freqs[16], cum[16];
-    uint64_t counts[16];
+    uint32_t freqs[256], cum[256];
+    uint64_t counts[256];
     uint32_t* states;     /* n_tiles * 32: the decoder's initial (encoder's final) states */
     uint32_t* offsets;    /* n_tiles + 1: start of each tile's payload, in 16-bit words */
     uint16_t* payload;
@@ -613,35 +624,51 @@ void orc_rans_free(orc_rans* r) {
 
 static int64_t lane_steps(int64_t n_t, int l) { return n_t > l ? (n_t - l + 31) / 32 : 0; }
 
-/* Encoder: each lane is encoded in reverse (last step first); within a step the
- * lanes go 31 -> 0.  Before encoding s into x: while x >= f_s * 2^(32-prob_bits),
+/* Symbol of lane l's symbol step m of a tile (codes at steps k*m .. k*m + k-1). */
+static int tuple_symbol(const int8_t* tile_codes, int k, int64_t m, int l) {
+    int s = 0;
+    for (int i = 0; i < k; ++i) s = 16 * s + (tile_codes[32 * (k * m + i) + l] + 8);
+    return s;
+}
+
+/* Encoder: each lane is encoded in reverse (last symbol step first); within a step
+ * the lanes go 31 -> 0.  Before encoding s into x: while x >= f_s * 2^(32-prob_bits),
  * emit the low 16 bits and shift x right by 16 (with 2^16 <= x < 2^32 this is the
  * renormalisation bound ((2^16 >> b) << 16) * f_s).  Then
  * x = floor(x / f_s) * 2^b + (x mod f_s) + c_s.  Emitted words go on a stack; the
  * tile's payload is the stack read from the top, which is the order in which the
- * decoder asks for them. */
-orc_rans* orc_rans_encode(const int8_t* codes, int64_t n, int prob_bits, int tile) {
+ * decoder asks for them.  With k = 2 every lane of every tile must hold an even
+ * number of codes: tile and n multiples of 64. */
+orc_rans* orc_rans_encode_k(const int8_t* codes, int64_t n, int prob_bits, int tile, int k) {
     if (n < 0 || prob_bits < 5 || prob_bits > 15 || tile < 32 || tile % 32) return NULL;
+    if (k != 1 && k != 2) return NULL;
+    if (k == 2 && (tile % 64 || n % 64)) return NULL;
     orc_rans* r = (orc_rans*)calloc(1, sizeof(orc_rans));
     r->n = n;
     r->prob_bits = prob_bits;
     r->tile = tile;
+    r->k = k;
+    r->nsym = k == 1 ? 16 : 256;
     for (int64_t i = 0; i < n; ++i) {
         if (codes[i] < -8 || codes[i] > 7) {
             orc_rans_free(r);
             return NULL;
         }
-        r->counts[codes[i] + 8]++;
     }
-    if (orc_rans_freqs(r->counts, prob_bits, r->freqs) < 0) {
+    r->n_tiles = (n + tile - 1) / tile;
+    for (int64_t t = 0; t < r->n_tiles; ++t) {
+        const int64_t base = t * tile, n_t = (n - base < tile) ? n - base : tile;
+        for (int l = 0; l < 32; ++l)
+            for (int64_t m = 0; m < lane_steps(n_t, l) / k; ++m) r->counts[tuple_symbol(codes + base, k, m, l)]++;
+    }
+    if (orc_rans_freqs_n(r->counts, r->nsym, prob_bits, r->freqs) < 0) {
         orc_rans_free(r);
         return NULL;
     }
-    for (int s = 0, c = 0; s < 16; ++s) {
+    for (int s = 0, c = 0; s < r->nsym; ++s) {
         r->cum[s] = (uint32_t)c;
         c += (int)r->freqs[s];
     }
-    r->n_tiles = (n + tile - 1) / tile;
     r->states = (uint32_t*)malloc(sizeof(uint32_t) * 32 * (size_t)(r->n_tiles > 0 ? r->n_tiles : 1));
     r->offsets = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)(r->n_tiles + 1));
     r->payload = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(n > 0 ? n : 1)); /* <= 1 word per symbol */
@@ -654,11 +681,11 @@ orc_rans* orc_rans_encode(const int8_t* codes, int64_t n, int prob_bits, int til
         uint64_t x[32];
         for (int l = 0; l < 32; ++l) x[l] = 1u << 16;
         int64_t sp = 0;
-        const int64_t steps = (n_t + 31) / 32;
-        for (int64_t j = steps - 1; j >= 0; --j) {
+        const int64_t steps = (n_t + 31) / 32 / k;
+        for (int64_t m = steps - 1; m >= 0; --m) {
             for (int l = 31; l >= 0; --l) {
-                if (j >= lane_steps(n_t, l)) continue;
-                const int s = codes[base + 32 * j + l] + 8;
+                if (m >= lane_steps(n_t, l) / k) continue;
+                const int s = tuple_symbol(codes + base, k, m, l);
                 const uint64_t f = r->freqs[s];
                 while (x[l] >= f * renorm_unit) {
                     stack[sp++] = (uint16_t)(x[l] & 0xFFFF);
@@ -677,13 +704,19 @@ orc_rans* orc_rans_encode(const int8_t* codes, int64_t n, int prob_bits, int til
     return r;
 }
 
-/* Decoder: for step j = 0.., lanes ascending: slot = x mod 2^b, s = the symbol with
- * c_s <= slot < c_s + f_s, x = f_s * (x >> b) + slot - c_s; if x < 2^16 then
- * x = (x << 16) | next payload word.  Writes codes; also reports the lanes' final
- * states (each must be 2^16) and the words consumed (must be the tile's count).
- * Returns 0, -1 on a corrupt stream, -2 if a final state or word count is off. */
+orc_rans* orc_rans_encode(const int8_t* codes, int64_t n, int prob_bits, int tile) {
+    return orc_rans_encode_k(codes, n, prob_bits, tile, 1);
+}
+
+/* Decoder: for symbol step m = 0.., lanes ascending: slot = x mod 2^b, s = the
+ * symbol with c_s <= slot < c_s + f_s, x = f_s * (x >> b) + slot - c_s; if x < 2^16
+ * then x = (x << 16) | next payload word; the symbol's codes go to the lane's
+ * steps k*m .. k*m + k-1.  Also reports the lanes' final states (each must be
+ * 2^16) and the words consumed (must be the tile's count).  Returns 0, -1 on a
+ * corrupt stream, -2 if a final state or word count is off. */
 int orc_rans_decode(const orc_rans* r, int8_t* out, uint32_t* final_states /* n_tiles*32 or NULL */) {
     const uint32_t M = 1u << r->prob_bits;
+    const int k = r->k;
     int rc = 0;
     for (int64_t t = 0; t < r->n_tiles; ++t) {
         const int64_t base = t * r->tile;
@@ -692,21 +725,21 @@ int orc_rans_decode(const orc_rans* r, int8_t* out, uint32_t* final_states /* n_
         for (int l = 0; l < 32; ++l) x[l] = r->states[t * 32 + l];
         int64_t wp = r->offsets[t];
         const int64_t wend = r->offsets[t + 1];
-        const int64_t steps = (n_t + 31) / 32;
-        for (int64_t j = 0; j < steps; ++j) {
+        const int64_t steps = (n_t + 31) / 32 / k;
+        for (int64_t m = 0; m < steps; ++m) {
             for (int l = 0; l < 32; ++l) {
-                if (j >= lane_steps(n_t, l)) continue;
+                if (m >= lane_steps(n_t, l) / k) continue;
                 const uint32_t slot = (uint32_t)(x[l] & (M - 1));
                 int s = -1;
-                for (int k = 0; k < 16; ++k)
-                    if (r->freqs[k] && slot >= r->cum[k] && slot < r->cum[k] + r->freqs[k]) s = k;
+                for (int q = 0; q < r->nsym; ++q)
+                    if (r->freqs[q] && slot >= r->cum[q] && slot < r->cum[q] + r->freqs[q]) s = q;
                 if (s < 0) return -1;
                 x[l] = (uint64_t)r->freqs[s] * (x[l] >> r->prob_bits) + slot - r->cum[s];
                 if (x[l] < (1u << 16)) {
                     if (wp >= wend) return -1;
                     x[l] = (x[l] << 16) | r->payload[wp++];
                 }
-                out[base + 32 * j + l] = (int8_t)(s - 8);
+                for (int i = k - 1, v = s; i >= 0; --i, v /= 16) out[base + 32 * (k * m + i) + l] = (int8_t)(v % 16 - 8);
             }
         }
         for (int l = 0; l < 32; ++l) {
