@@ -388,24 +388,26 @@ def extras(torch, ec, stream, device):
     out["w1024_decode_us"] = round(t_loop(g2.replay, 200), 2)
     out["w1024_bpw"] = round(W.stats()["bits_per_weight"], 3)
 
-    # rANS 4-bit tiles, both shapes (rotate 8 copies to stay out of L2)
+    # rANS 4-bit tiles, both shapes, one code per symbol and pair symbols (rotate 8
+    # copies to stay out of L2)
     for idx, (n, k) in enumerate(synth.RANS_SHAPES):
         codes, scales = synth.make_rans_case(idx)
-        blob = ec.encode_rans(codes, scales, device=-1).serialize()
-        Rs = [ec.deserialize(blob, device=device) for _ in range(8)]
         xr = torch.from_numpy(synth.make_x(4000 + idx, 1, k).view(np.int16)).to(dev)
         yr = torch.empty((1, n), device=dev)
-        st = Rs[0].stats()
+        for tup, tag in ((1, ""), (2, "_pair")):
+            blob = ec.encode_rans(codes, scales, device=-1, codes_per_symbol=tup).serialize()
+            Rs = [ec.deserialize(blob, device=device) for _ in range(8)]
+            st = Rs[0].stats()
 
-        def rg():
-            for R in Rs:
-                ec.gemv(R, xr, yr)
-        gr = capture(torch, rg, stream)
-        us = t_loop(gr.replay, 20) / len(Rs)
-        out[f"rans_{n}x{k}_gemv_us"] = round(us, 2)
-        out[f"rans_{n}x{k}_bpw"] = round(st["bits_per_weight"], 3)
-        out[f"rans_{n}x{k}_gbs"] = round(st["device_bytes"] / us / 1e3, 1)
-        del Rs
+            def rg():
+                for R in Rs:
+                    ec.gemv(R, xr, yr)
+            gr = capture(torch, rg, stream)
+            us = t_loop(gr.replay, 20) / len(Rs)
+            out[f"rans{tag}_{n}x{k}_gemv_us"] = round(us, 2)
+            out[f"rans{tag}_{n}x{k}_bpw"] = round(st["bits_per_weight"], 3)
+            out[f"rans{tag}_{n}x{k}_gbs"] = round(st["device_bytes"] / us / 1e3, 1)
+            del Rs, gr
 
     # 70B-shaped block: one batched decode of all seven matrices to BF16
     Ws, outs, comp, nw = [], [], 0, 0

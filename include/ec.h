@@ -83,14 +83,18 @@ typedef struct {
 } ec_huff_params;
 
 /* rANS codec parameters (NULL = defaults).
- *  prob_bits  frequency precision b, 9..15 (default 12)
- *  tile_syms  symbols per independent tile, a multiple of 32 (default 4096)
- *  group      weights per FP16 scale along a row (only 128 is supported) */
+ *  prob_bits         frequency precision b, 9..15 (default 12)
+ *  tile_syms         codes per independent tile, a multiple of 128 (default 4096)
+ *  group             weights per FP16 scale along a row (only 128 is supported)
+ *  codes_per_symbol  1 (default; 0 means 1): one 4-bit code per rANS symbol;
+ *                    2: a symbol is the pair of a lane's consecutive codes (MINE's
+ *                    k-tuple symbols), 256 symbols, half the decode steps, at
+ *                    about 0.01 bit per code over single codes with b = 12 */
 typedef struct {
     int32_t prob_bits;
     int32_t tile_syms;
     int32_t group;
-    int32_t reserved;
+    int32_t codes_per_symbol;
 } ec_rans_params;
 
 enum { EC_KIND_HUFFMAN_BF16 = 1, EC_KIND_RANS_INT4 = 2 };

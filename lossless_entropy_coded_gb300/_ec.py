@@ -45,7 +45,7 @@ class HuffParams(ctypes.Structure):
 
 class RansParams(ctypes.Structure):
     _fields_ = [("prob_bits", ctypes.c_int32), ("tile_syms", ctypes.c_int32), ("group", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("codes_per_symbol", ctypes.c_int32)]
 
 
 class Stats(ctypes.Structure):
@@ -174,12 +174,13 @@ def encode_bf16(w, max_code_len: int = 12, tile_steps: int = 0, device: int = 0)
 
 
 def encode_rans(codes, scales_f16, prob_bits: int = 12, tile_syms: int = 4096, group: int = 128,
-                device: int = 0) -> Matrix:
-    """rANS-encode host int8 codes [N, K] in [-8, 7] with FP16 scales [N, ceil(K/group)]."""
+                device: int = 0, codes_per_symbol: int = 1) -> Matrix:
+    """rANS-encode host int8 codes [N, K] in [-8, 7] with FP16 scales [N, ceil(K/group)]
+    (codes_per_symbol 2: one symbol per pair of a lane's consecutive codes)."""
     n, k = int(codes.shape[0]), int(codes.shape[1])
     pc, kc = _host_ptr(codes)
     ps, ks = _host_ptr(scales_f16)
-    prm = RansParams(prob_bits, tile_syms, group, 0)
+    prm = RansParams(prob_bits, tile_syms, group, codes_per_symbol)
     h = ctypes.c_void_p()
     _check(lib.ec_encode_rans(pc, ps, n, k, ctypes.byref(prm), device, ctypes.byref(h)), "ec_encode_rans")
     return Matrix(h.value, n, k, EC_KIND_RANS_INT4, device)

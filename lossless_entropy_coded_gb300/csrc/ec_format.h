@@ -42,7 +42,7 @@
 #include <stdint.h>
 
 #define EC_BLOB_MAGIC 0x31434345u /* "ECC1" */
-#define EC_BLOB_VERSION 3u
+#define EC_BLOB_VERSION 4u
 
 #define EC_L1_BITS 12            /* level-1 Huffman window */
 #define EC_SUB_BITS 8            /* bits per sub-table level */
@@ -84,8 +84,11 @@
 #define EC_ENT_PTR 0x80000000u
 #define EC_ENT_BAD 0x40000000u
 
-/* rANS slot entry (u32): bits 0..3 = symbol (code + 8), bits 4..15 = slot - cum[s],
- * bits 16..28 = freq[s]. */
+/* rANS slot entry (u32), one code per symbol: bits 0..3 = symbol (code + 8),
+ * bits 4..15 = slot - cum[s], bits 16..28 = freq[s].
+ * Two codes per symbol (symbol = 16 (c0 + 8) + (c1 + 8) for a lane's steps 2m and
+ * 2m + 1): bits 0..7 = symbol, bits 8..19 = slot - cum[s], bits 20..31 =
+ * freq[s] - 1. */
 
 typedef struct {
     uint32_t magic, version;
@@ -102,7 +105,8 @@ typedef struct {
     int32_t prob_bits;                /* rANS */
     int32_t max_words;                /* rANS: largest payload of any tile (u16 words) */
     int32_t max_len;                  /* Huffman: longest codeword in use */
-    uint8_t pad[256 - 4 * 4 - 8 * 10 - 4 * 4];
+    int32_t rans_tuple;               /* rANS: codes per symbol, 1 or 2 */
+    uint8_t pad[256 - 4 * 4 - 8 * 10 - 4 * 5];
 } ec_blob_header;
 
 #endif /* EC_FORMAT_H_ */

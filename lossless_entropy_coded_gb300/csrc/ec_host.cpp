@@ -269,15 +269,20 @@ std::vector<uint32_t> build_pair_table(const std::vector<uint32_t>& h) {
  * the present symbol with the largest remainder M c_s - f_s n, while it is over
  * take one from the present symbol with f_s > 1 and the smallest remainder (ties
  * to the lower symbol in both cases). */
-bool rans_normalise(const uint64_t counts[16], int prob_bits, uint32_t f[16]) {
+bool rans_normalise(const uint64_t* counts, int nsym, int prob_bits, uint32_t* f) {
     const int64_t M = int64_t(1) << prob_bits;
     unsigned __int128 n = 0;
-    for (int s = 0; s < 16; ++s) n += counts[s];
-    std::memset(f, 0, 16 * sizeof(uint32_t));
+    int present = 0;
+    for (int s = 0; s < nsym; ++s) {
+        n += counts[s];
+        present += counts[s] != 0;
+    }
+    std::memset(f, 0, (size_t)nsym * sizeof(uint32_t));
     if (n == 0) return true;
-    __int128 rem[16] = {};
+    if (present > M) return false;
+    std::vector<__int128> rem((size_t)nsym, 0);
     int64_t sum = 0;
-    for (int s = 0; s < 16; ++s) {
+    for (int s = 0; s < nsym; ++s) {
         if (!counts[s]) continue;
         int64_t v = (int64_t)((unsigned __int128)M * counts[s] / n);
         v = std::max<int64_t>(v, 1);
@@ -287,14 +292,14 @@ bool rans_normalise(const uint64_t counts[16], int prob_bits, uint32_t f[16]) {
     }
     for (; sum < M; ++sum) {
         int b = -1;
-        for (int s = 0; s < 16; ++s)
+        for (int s = 0; s < nsym; ++s)
             if (counts[s] && (b < 0 || rem[s] > rem[b])) b = s;
         f[b]++;
         rem[b] -= (__int128)n;
     }
     for (; sum > M; --sum) {
         int b = -1;
-        for (int s = 0; s < 16; ++s)
+        for (int s = 0; s < nsym; ++s)
             if (counts[s] && f[s] > 1 && (b < 0 || rem[s] < rem[b])) b = s;
         if (b < 0) return false;
         f[b]--;
@@ -539,7 +544,10 @@ extern "C" int ec_encode_rans(const int8_t* codes, const uint16_t* scales, int64
     const int b = params ? params->prob_bits : 12;
     const int T = params ? params->tile_syms : 4096;
     const int group = params ? params->group : 128;
+    const int k = params && params->codes_per_symbol ? params->codes_per_symbol : 1;
     if (b < 9 || b > 15 || T < 32 || T % EC_RANS_ROW_ALIGN || T > 65536) return EC_ERR_INVALID_ARG;
+    if (k != 1 && k != 2) return EC_ERR_INVALID_ARG;
+    if (k == 2 && b > 12) return EC_ERR_INVALID_ARG; /* pair entries hold freq - 1 and the slot bias in 12 bits */
     if (group != 128) return EC_ERR_UNSUPPORTED;
     if (k_cols > INT64_MAX - EC_RANS_ROW_ALIGN) return EC_ERR_OVERFLOW;
     const int64_t KP = round_up(k_cols, EC_RANS_ROW_ALIGN), G = KP / 128;
@@ -555,24 +563,50 @@ extern "C" int ec_encode_rans(const int8_t* codes, const uint16_t* scales, int64
             if (codes[i] < -8 || codes[i] > 7) return EC_ERR_INVALID_ARG;
         ec_matrix* m = new_matrix();
         if (!m) return EC_ERR_OOM;
-        for (int64_t i = 0; i < nk; ++i) m->counts[codes[i] + 8]++;
-        m->counts[8] += (uint64_t)(n_rows * (KP - K));
-        if (!rans_normalise(m->counts, b, m->freqs)) {
+        const int nsym = k == 1 ? 16 : 256;
+        const int64_t n_tiles = (n_pad + T - 1) / T;
+        /* symbol of lane l's symbol step j in a tile's padded codes v */
+        auto symbol = [k](const int8_t* v, int64_t j, int l) {
+            return k == 1 ? v[32 * j + l] + 8 : 16 * (v[64 * j + l] + 8) + (v[64 * j + 32 + l] + 8);
+        };
+        if (k == 1) {
+            for (int64_t i = 0; i < nk; ++i) m->counts[codes[i] + 8]++;
+            m->counts[8] += (uint64_t)(n_rows * (KP - K));
+        } else { /* histogram of the pair symbols over the padded tile layout */
+            std::vector<std::array<uint64_t, 256>> part(host_threads());
+            for (auto& a : part) a.fill(0);
+            std::atomic<int> slot{0};
+            parallel_for(
+                n_tiles,
+                [&](int64_t lo, int64_t hi) {
+                    auto& hcount = part[slot++ % part.size()];
+                    std::vector<int8_t> v(T);
+                    for (int64_t t = lo; t < hi; ++t) {
+                        const int64_t base = t * T, n_t = std::min<int64_t>(T, n_pad - base), S = n_t / 32;
+                        gather_padded(codes, K, KP, base, n_t, v.data());
+                        for (int64_t j = 0; j < S / 2; ++j)
+                            for (int l = 0; l < 32; ++l) hcount[symbol(v.data(), j, l)]++;
+                    }
+                }); /* at most one chunk per thread: one histogram each */
+            for (auto& a : part)
+                for (int s = 0; s < 256; ++s) m->counts[s] += a[s];
+        }
+        if (!rans_normalise(m->counts, nsym, b, m->freqs)) {
             delete m;
             return EC_ERR_INVALID_ARG;
         }
         const uint32_t M = 1u << b;
-        uint32_t cum[16];
-        for (int s = 0, c = 0; s < 16; ++s) {
+        std::vector<uint32_t> cum(nsym, 0);
+        for (int s = 0, c = 0; s < nsym; ++s) {
             cum[s] = (uint32_t)c;
             c += (int)m->freqs[s];
         }
         std::vector<uint32_t> table(M, 0);
-        for (int s = 0; s < 16; ++s)
-            for (uint32_t k = 0; k < m->freqs[s]; ++k)
-                table[cum[s] + k] = (uint32_t)s | (k << 4) | (m->freqs[s] << 16);
+        for (int s = 0; s < nsym; ++s)
+            for (uint32_t q = 0; q < m->freqs[s]; ++q)
+                table[cum[s] + q] = k == 1 ? (uint32_t)s | (q << 4) | (m->freqs[s] << 16)
+                                           : (uint32_t)s | (q << 8) | ((m->freqs[s] - 1) << 20);
 
-        const int64_t n_tiles = (n_pad + T - 1) / T;
         std::vector<std::vector<uint16_t>> words(n_tiles);
         std::vector<std::array<uint32_t, 32>> states(n_tiles);
         const uint64_t unit = uint64_t(1) << (32 - b);
@@ -585,9 +619,9 @@ extern "C" int ec_encode_rans(const int8_t* codes, const uint16_t* scales, int64
                 uint64_t x[32];
                 for (int l = 0; l < 32; ++l) x[l] = 1u << 16;
                 stack.clear();
-                for (int64_t j = S - 1; j >= 0; --j)
+                for (int64_t j = S / k - 1; j >= 0; --j)
                     for (int l = 31; l >= 0; --l) {
-                        const int s = v[32 * j + l] + 8;
+                        const int s = symbol(v.data(), j, l);
                         const uint64_t f = m->freqs[s];
                         if (x[l] >= f * unit) {
                             stack.push_back((uint16_t)x[l]);
@@ -630,6 +664,7 @@ extern "C" int ec_encode_rans(const int8_t* codes, const uint16_t* scales, int64
         h.blob_bytes = h.records_off + total;
         h.prob_bits = b;
         h.max_words = (int32_t)max_words;
+        h.rans_tuple = k;
 
         std::vector<uint8_t> blob((size_t)h.blob_bytes, 0);
         std::memcpy(blob.data(), &h, sizeof h);
@@ -650,7 +685,7 @@ extern "C" int ec_encode_rans(const int8_t* codes, const uint16_t* scales, int64
         m->raw_bytes = 0;
         m->table_bytes = 4 * (int64_t)M + 2 * ns;
         m->aux_bytes = h.blob_bytes - m->table_bytes - payload / 8;
-        m->entropy = entropy_bits(m->counts, 16);
+        m->entropy = entropy_bits(m->counts, nsym) / k; /* bits per code */
         int rc = upload(m, blob, device);
         if (rc != EC_OK) {
             delete m;
@@ -722,16 +757,16 @@ extern "C" const char* ec_strerror(int code) {
 namespace {
 
 struct SerialMeta {
-    char magic[8];          /* "ECSER001" */
+    char magic[8];          /* "ECSER002" */
     int32_t kind, reserved;
     int64_t blob_bytes;
     uint64_t counts[256];
     uint8_t lengths[256];
-    uint32_t freqs[16];
+    uint32_t freqs[256];
     int64_t payload_bits, raw_bytes, aux_bytes, table_bytes;
     double entropy;
 };
-const char kSerialMagic[8] = {'E', 'C', 'S', 'E', 'R', '0', '0', '1'};
+const char kSerialMagic[8] = {'E', 'C', 'S', 'E', 'R', '0', '0', '2'};
 
 /* Structural validation of a device blob held in host memory: every field and
  * offset is checked with overflow-safe arithmetic before anything trusts it
@@ -765,6 +800,8 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
     } else {
         if (h.prob_bits < 9 || h.prob_bits > 15 || h.table_words != (int64_t(1) << h.prob_bits) || h.max_words < 0)
             return EC_ERR_CORRUPT;
+        if (h.rans_tuple != 1 && h.rans_tuple != 2) return EC_ERR_CORRUPT;
+        if (h.rans_tuple == 2 && h.prob_bits > 12) return EC_ERR_CORRUPT;
     }
     if (!mul_ok(h.table_words, 4, &t4) || !add_ok(h.table_off, t4, &end)) return EC_ERR_CORRUPT;
     if (!huff) {
@@ -803,10 +840,15 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
         }
         for (int64_t i = EC_PAIR_WORDS; i < h.table_words; ++i)
             if ((tab[i] & EC_ENT_PTR) && (int64_t)(tab[i] & 0xFFFFu) >= n_sub) return EC_ERR_CORRUPT;
-    } else {
+    } else if (h.rans_tuple == 1) {
         for (int64_t i = 0; i < h.table_words; ++i) {
             const uint32_t f = tab[i] >> 16, k = (tab[i] >> 4) & 0xFFF;
             if (f == 0 || f > (1u << h.prob_bits) || k >= f) return EC_ERR_CORRUPT;
+        }
+    } else {
+        for (int64_t i = 0; i < h.table_words; ++i) {
+            const uint32_t f = (tab[i] >> 20) + 1, k = (tab[i] >> 8) & 0xFFF;
+            if (f > (1u << h.prob_bits) || k >= f) return EC_ERR_CORRUPT;
         }
     }
     return EC_OK;

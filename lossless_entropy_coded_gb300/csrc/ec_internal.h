@@ -18,8 +18,8 @@ struct ec_matrix {
     uint8_t* h_blob;           /* host copy, kept only when device < 0 */
     /* host-side statistics */
     uint8_t lengths[256];
-    uint64_t counts[256];      /* exponent (Huffman) or code + 8 (rANS) histogram, padding included */
-    uint32_t freqs[16];        /* rANS */
+    uint64_t counts[256];      /* exponent (Huffman) or rANS symbol histogram, padding included */
+    uint32_t freqs[256];       /* rANS */
     int64_t payload_bits, raw_bytes, aux_bytes, table_bytes;
     double entropy;
 };

@@ -95,6 +95,7 @@ struct RansMat {
     int32_t steps, prob_bits, atomic_y, words_cap;
     int32_t last_steps;         /* symbols per lane of the last tile */
     uint32_t rec16;             /* records region size in 16-byte units */
+    int32_t tuple;              /* codes per symbol: 1 or 2 */
 };
 
 struct RansArgs {
@@ -859,7 +860,7 @@ __device__ __forceinline__ uint32_t lds16_if(bool p, uint32_t a, uint32_t v) {
     return v;
 }
 
-template <bool kGemv, int B>
+template <bool kGemv, int B, bool kPair>
 __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) rans_kernel(const __grid_constant__ RansArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const RansMat& M = a.m;
@@ -950,28 +951,39 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) rans_kernel(const _
                                         : 0.f;
                 const float scale = __shfl_sync(kFull, sc, gi & 31);
 #pragma unroll
-                for (int s = 0; s < 4; ++s) {
+                for (int s = 0; s < (kPair ? 2 : 4); ++s) {
                     const uint32_t e = lds32(tab_s + ((x & mask_b) << 2));
-                    x = (e >> 16) * (x >> pb) + ((e >> 4) & 0xFFFu);
+                    if (kPair) { /* freq - 1 in bits 20..31: f X = (f - 1) X + X */
+                        const uint32_t X = x >> pb;
+                        x = (e >> 20) * X + X + ((e >> 8) & 0xFFFu);
+                    } else {
+                        x = (e >> 16) * (x >> pb) + ((e >> 4) & 0xFFFu);
+                    }
                     const bool need = x < 65536u;
                     const uint32_t bal = __ballot_sync(kFull, need);
                     const uint32_t idx = min(wp + __popc(bal & lt), cap);
                     const uint32_t v = lds16_if(need, wbase + 2 * idx, 0u);
                     x = need ? x * 65536u + v : x; /* v < 2^16 and x < 2^16: the shift-or as one multiply-add */
                     wp += __popc(bal);
-                    /* code + 8 in the low 4 bits: (float)code = (2^23 + code + 8) - (2^23 + 8) */
-                    const float cf = __int_as_float(0x4B000000 | (e & 15u)) - 8388616.0f;
-                    const uint32_t c = col + 32 * s;
-                    if (kGemv) {
+                    /* a code + 8 in the low 4 bits: (float)code = (2^23 + code + 8) - (2^23 + 8).  Pairs:
+                     * the lane's earlier step in bits 4..7, the later one in bits 0..3 */
+                    const int nc = kPair ? 2 : 1;
 #pragma unroll
-                        for (int b = 0; b < B; ++b) {
-                            if (B > 1 && b >= batch) break;
-                            uint32_t xv;
-                            asm volatile("ld.shared.u16 %0, [%1];" : "=r"(xv) : "r"(xs_s + 2 * (b * kp + c)) : "memory");
-                            accg[b] = fmaf(cf, __uint_as_float(xv << 16), accg[b]);
+                    for (int q = 0; q < nc; ++q) {
+                        const uint32_t nib = kPair ? (q == 0 ? (e >> 4) & 15u : e & 15u) : e & 15u;
+                        const float cf = __int_as_float(0x4B000000 | nib) - 8388616.0f;
+                        const uint32_t c = col + 32 * (nc * s + q);
+                        if (kGemv) {
+#pragma unroll
+                            for (int b = 0; b < B; ++b) {
+                                if (B > 1 && b >= batch) break;
+                                uint32_t xv;
+                                asm volatile("ld.shared.u16 %0, [%1];" : "=r"(xv) : "r"(xs_s + 2 * (b * kp + c)) : "memory");
+                                accg[b] = fmaf(cf, __uint_as_float(xv << 16), accg[b]);
+                            }
+                        } else if (c < K) {
+                            M.out[row * K + c] = __bfloat16_as_ushort(__float2bfloat16_rn(cf * scale));
                         }
-                    } else if (c < K) {
-                        M.out[row * K + c] = __bfloat16_as_ushort(__float2bfloat16_rn(cf * scale));
                     }
                 }
                 if (kGemv) {
@@ -1207,6 +1219,7 @@ RansMat rans_desc(const ec_matrix* W) {
     m.words_cap = (h.max_words + 7) / 8 * 8;
     m.last_steps = h.n_tiles > 0 ? (int32_t)((h.n_rows * h.k_pad - (h.n_tiles - 1) * T) / 32) : 0;
     m.rec16 = (uint32_t)(m.records_bytes / 16);
+    m.tuple = h.rans_tuple;
     return m;
 }
 
@@ -1243,8 +1256,9 @@ int launch_huff_gemv(const HuffGemvArgs& a, bool lng, size_t smem, int grid, int
 
 template <bool G, int B>
 int launch_rans_b(const RansArgs& a, size_t smem, int grid, int block, cudaStream_t s) {
-    if (set_smem(rans_kernel<G, B>, smem) != EC_OK) return EC_ERR_CUDA;
-    return launch_ex(rans_kernel<G, B>, grid, block, smem, s, a);
+    auto kern = a.m.tuple == 2 ? rans_kernel<G, B, true> : rans_kernel<G, B, false>;
+    if (set_smem(kern, smem) != EC_OK) return EC_ERR_CUDA;
+    return launch_ex(kern, grid, block, smem, s, a);
 }
 
 int launch_rans(bool gemv, const RansArgs& a, size_t smem, int grid, int block, cudaStream_t s) {

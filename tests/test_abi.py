@@ -83,16 +83,16 @@ def test_argument_validation(ec):
 
 
 # --------------------------------------------------------------- blob reader
-HDR = struct.Struct("<IIii" + "q" * 10 + "iiii")
+HDR = struct.Struct("<IIii" + "q" * 10 + "iiiii")
 
 
 def parse(blob: bytes):
-    meta_size = 8 + 8 + 8 + 256 * 8 + 256 + 16 * 4 + 4 * 8 + 8
+    meta_size = 8 + 8 + 8 + 256 * 8 + 256 + 256 * 4 + 4 * 8 + 8
     dev = blob[meta_size:]
     f = HDR.unpack_from(dev, 0)
     keys = ["magic", "version", "kind", "steps", "n_rows", "k_cols", "k_pad", "n_tiles", "table_off",
             "table_words", "scales_off", "tile_off_off", "records_off", "blob_bytes", "max_code_bytes",
-            "prob_bits", "max_words", "max_len"]
+            "prob_bits", "max_words", "max_len", "rans_tuple"]
     h = dict(zip(keys, f))
     return h, dev
 
@@ -271,6 +271,62 @@ def test_rans_frequencies_match_oracle(ec):
         assert ((tab >> 16) == want[sym]).all()
 
 
+def rans_padded(codes: np.ndarray, k_pad: int) -> np.ndarray:
+    """The codes laid out as the library encodes them: rows padded to k_pad with code 0."""
+    n, k = codes.shape
+    out = np.zeros((n, k_pad), dtype=np.int8)
+    out[:, :k] = codes
+    return out
+
+
+@pytest.mark.parametrize("tuple_", [1, 2])
+@pytest.mark.parametrize("shape,tile", [((64, 1000), 4096), ((7, 300), 128), ((3, 4096), 1024), ((1, 1), 4096)])
+def test_rans_blob_matches_oracle_stream(ec, tuple_, shape, tile):
+    """The library's table, tile states and payload words equal the oracle's own
+    encoding of the padded code layout, word for word (single and pair symbols)."""
+    codes, scales = synth.make_rans_case(3, *shape)
+    W = ec.encode_rans(codes, scales, tile_syms=tile, device=-1, codes_per_symbol=tuple_)
+    h, dev = parse(W.serialize())
+    assert h["rans_tuple"] == tuple_
+    r = O.Rans(rans_padded(codes, h["k_pad"]), 12, tile, k=tuple_)
+    tab = np.frombuffer(dev, np.uint32, h["table_words"], h["table_off"]).astype(np.int64)
+    freqs = r.freqs.astype(np.int64)
+    cum = np.concatenate([[0], np.cumsum(freqs)[:-1]])
+    if tuple_ == 1:
+        sym, bias, f = tab & 15, (tab >> 4) & 0xFFF, tab >> 16
+    else:
+        sym, bias, f = tab & 0xFF, (tab >> 8) & 0xFFF, (tab >> 20) + 1
+    assert np.array_equal(np.bincount(sym, minlength=r.nsym), freqs)
+    assert np.array_equal(f, freqs[sym])
+    assert np.array_equal(bias, np.arange(4096) - cum[sym])
+    assert h["n_tiles"] == r.n_tiles
+    toff = np.frombuffer(dev, np.uint32, h["n_tiles"] + 1, h["tile_off_off"]).astype(np.int64)
+    ooff = r.offsets.astype(np.int64)
+    for t in range(h["n_tiles"]):
+        base = h["records_off"] + 16 * toff[t]
+        st = np.frombuffer(dev, np.uint32, 32, base)
+        assert np.array_equal(st, r.states[t]), t
+        nw = int(ooff[t + 1] - ooff[t])
+        words = np.frombuffer(dev, np.uint16, 8 * (toff[t + 1] - toff[t]) - 64, base + 128)
+        ow = np.ctypeslib.as_array(
+            (ctypes.c_uint16 * max(1, int(ooff[-1]))).from_address(O._L().orc_rans_payload_mut(r._h)))
+        assert np.array_equal(words[:nw], ow[ooff[t]:ooff[t + 1]]), t
+        assert len(words) - nw < 8 and not words[nw:].any()
+
+
+def test_rans_pair_limits(ec):
+    from lossless_entropy_coded_gb300 import _ec
+    codes, sc = synth.make_rans_case(0, 4, 256)
+    h = ctypes.c_void_p()
+    for prm, want in [((13, 4096, 128, 2), _ec.EC_ERR_INVALID_ARG), ((12, 4096, 128, 3), _ec.EC_ERR_INVALID_ARG),
+                      ((12, 4096, 128, -1), _ec.EC_ERR_INVALID_ARG)]:
+        assert _ec.lib.ec_encode_rans(codes.ctypes.data, sc.ctypes.data, 4, 256, ctypes.byref(_ec.RansParams(*prm)),
+                                     -1, ctypes.byref(h)) == want, prm
+    for b in (9, 12):
+        W = ec.encode_rans(codes, sc, prob_bits=b, device=-1, codes_per_symbol=2)
+        assert W.stats()["max_code_len"] == b
+
+
 def corruptions(blob: bytes):
     h, dev = parse(blob)
     meta = len(blob) - len(dev)
@@ -290,16 +346,24 @@ def corruptions(blob: bytes):
         x = bytearray(b); struct.pack_into("<I", x, meta + h["table_off"], 0x80000000 | 0x7FFF)
         yield "table pointer", bytes(x)
     else:
-        x = bytearray(b); struct.pack_into("<I", x, meta + h["table_off"], 0)
+        x = bytearray(b); struct.pack_into("<I", x, meta + h["table_off"], 0 if h["rans_tuple"] == 1 else 0xFFF00)
         yield "slot entry", bytes(x)
+        tup = meta + HDR.size - 4
+        x = bytearray(b); struct.pack_into("<i", x, tup, 3)
+        yield "codes per symbol", bytes(x)
+        if h["rans_tuple"] == 2:
+            pb = meta + HDR.size - 4 * 4  # prob_bits, then max_words, max_len, rans_tuple
+            x = bytearray(b); struct.pack_into("<i", x, pb, 13)
+            yield "pair precision", bytes(x)
 
 
-@pytest.mark.parametrize("kind", ["huffman", "rans"])
+@pytest.mark.parametrize("kind", ["huffman", "rans", "rans_pair"])
 def test_deserialize_rejects_structural_corruption(ec, kind):
     if kind == "huffman":
         W = ec.encode_bf16(synth.llama_bf16(2008, 20, 1000), device=-1)
     else:
-        W = ec.encode_rans(*synth.make_rans_case(0, 20, 1000), device=-1)
+        W = ec.encode_rans(*synth.make_rans_case(0, 20, 1000), device=-1,
+                           codes_per_symbol=2 if kind == "rans_pair" else 1)
     blob = W.serialize()
     W2 = ec.deserialize(blob, device=-1)
     assert W2.stats() == W.stats()

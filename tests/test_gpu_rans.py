@@ -24,22 +24,24 @@ def dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
+@pytest.mark.parametrize("tuple_", [1, 2])
 @pytest.mark.parametrize("shape", [(1, 1), (7, 13), (3, 300), (64, 1000), (40, 4096), (17, 14336)])
-def test_decode_ragged(ec, shape):
+def test_decode_ragged(ec, shape, tuple_):
     codes, scales = synth.make_rans_case(0, *shape)
-    W = ec.encode_rans(codes, scales)
+    W = ec.encode_rans(codes, scales, codes_per_symbol=tuple_)
     out = torch.zeros(shape, dtype=torch.int16, device="cuda")
     ec.decode(W, out)
     assert ec.status() == 0
     assert np.array_equal(out.cpu().numpy().view(np.uint16), O.rans_dequant_bf16(codes, scales))
 
 
+@pytest.mark.parametrize("tuple_", [1, 2])
 @pytest.mark.parametrize("shape", [(7, 13), (64, 1000), (256, 4096), (64, 14336)])
 @pytest.mark.parametrize("batch", [1, 4, 16])
-def test_gemv_parity(ec, shape, batch):
+def test_gemv_parity(ec, shape, batch, tuple_):
     codes, scales = synth.make_rans_case(1, *shape)
     x = synth.make_x(4100, batch, shape[1])
-    W = ec.encode_rans(codes, scales)
+    W = ec.encode_rans(codes, scales, codes_per_symbol=tuple_)
     y = torch.full((batch, shape[0]), float("nan"), device="cuda")
     ec.gemv(W, dev(x.view(np.int16)), y, batch=batch)
     assert ec.status() == 0
@@ -47,16 +49,18 @@ def test_gemv_parity(ec, shape, batch):
     check_gemv(y.cpu().numpy(), y_ref, a_ref, f"{shape} b={batch}")
 
 
+@pytest.mark.parametrize("tuple_", [1, 2])
 @pytest.mark.parametrize("idx", [0, 1])
-def test_full_size_config(ec, idx):
-    """14336x4096 and 4096x14336 at full size: bit-exact dequantised decode against
-    the oracle and the oracle's own tile codec round trip; GEMV on all rows."""
+def test_full_size_config(ec, idx, tuple_):
+    """14336x4096 and 4096x14336 at full size, single and pair symbols: bit-exact
+    dequantised decode against the oracle and the oracle's own tile codec round
+    trip; GEMV on all rows."""
     codes, scales = synth.make_rans_case(idx)
     n, k = codes.shape
-    r = O.Rans(codes)
+    r = O.Rans(codes, k=tuple_)
     dec, fin, rc = r.decode()
     assert rc == 0 and np.array_equal(dec, codes.ravel())
-    W = ec.encode_rans(codes, scales)
+    W = ec.encode_rans(codes, scales, codes_per_symbol=tuple_)
     out = torch.zeros((n, k), dtype=torch.int16, device="cuda")
     ec.decode(W, out)
     assert ec.status() == 0
@@ -71,9 +75,27 @@ def test_full_size_config(ec, idx):
     assert s["bits_per_weight"] < 2.9
 
 
-def test_payload_corruption_is_reported(ec):
+def test_mixed_tuple_group(ec):
+    """One grouped launch over a single-symbol and a pair-symbol matrix of the same K."""
+    k = 4096
+    c0, s0 = synth.make_rans_case(5, 96, k)
+    c1, s1 = synth.make_rans_case(6, 160, k)
+    W0 = ec.encode_rans(c0, s0)
+    W1 = ec.encode_rans(c1, s1, codes_per_symbol=2)
+    x = synth.make_x(4200, 1, k)
+    y0 = torch.full((1, 96), float("nan"), device="cuda")
+    y1 = torch.full((1, 160), float("nan"), device="cuda")
+    ec.gemv_group([W0, W1], dev(x.view(np.int16)), [y0, y1], batch=1)
+    assert ec.status() == 0
+    for y, c, s in ((y0, c0, s0), (y1, c1, s1)):
+        y_ref, a_ref = O.gemv_rans(c, s, x)
+        check_gemv(y.cpu().numpy(), y_ref, a_ref, "mixed tuple group")
+
+
+@pytest.mark.parametrize("tuple_", [1, 2])
+def test_payload_corruption_is_reported(ec, tuple_):
     codes, scales = synth.make_rans_case(0, 32, 4096)
-    W = ec.encode_rans(codes, scales)
+    W = ec.encode_rans(codes, scales, codes_per_symbol=tuple_)
     blob = bytearray(W.serialize())
     from test_abi import parse
     h, devb = parse(bytes(blob))
