@@ -56,7 +56,7 @@ enum {
     EC_ERR_OOM = -7          /* host or device allocation failed */
 };
 
-#define EC_MAX_BATCH 16
+#define EC_MAX_BATCH 64
 #define EC_DEFAULT_MAX_CODE_LEN 12
 #define EC_MAX_GROUP 8
 #define EC_MAX_DECODE_BATCH 64
@@ -71,11 +71,14 @@ typedef struct ec_matrix ec_matrix; /* opaque: host descriptor + one device blob
  *                weights the limit costs about 0.004 bits per exponent over
  *                the unconstrained code.  Longer limits decode through a
  *                hierarchical table in global memory, more slowly.
- *  tile_steps    symbols per lane in one tile of 32 lanes: 32, 64 or 128, or 0
- *                (the default) to choose by size: 128 (4096-weight tiles, 0.125
- *                bit per weight of lane offsets) for matrices of at least 4 M
- *                padded weights, 64 from 2 M, else 32, so that a matrix has about
- *                1024 tiles or more to spread over the SMs. */
+ *  tile_steps    symbols per lane in one tile of 32 lanes: a multiple of 16 up
+ *                to 128, or 0 (the default) to choose by size: 128 (4096-weight
+ *                tiles, 0.125 bit per weight of lane offsets) for matrices of at
+ *                least 4 M padded weights, 64 from 2 M, else 32, so that a matrix
+ *                has about 1024 tiles or more to spread over the SMs, then lowered
+ *                in steps of 16 until 32 * tile_steps divides the padded row (for
+ *                K = 14336: 112), so that no tile crosses a row; only such
+ *                matrices take the tensor-core GEMV (ec_gemv). */
 typedef struct {
     int32_t max_code_len;
     int32_t tile_steps;

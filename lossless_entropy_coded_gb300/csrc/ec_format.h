@@ -15,9 +15,11 @@
  * Coded layout of the weights.  The matrix is padded at the end of every row to
  * k_pad columns (a multiple of EC_HUFF_ROW_ALIGN / EC_RANS_ROW_ALIGN) with zero
  * weights, flattened row-major, and cut into tiles of 32 * steps positions (the
- * last tile may be shorter, always a multiple of the row alignment).  Inside a
- * tile, position q = 32 * i + l is symbol i of lane l: lane l of the decoding warp
- * owns positions l, l + 32, l + 64, ...
+ * last tile may be shorter, always a multiple of the row alignment).
+ * Huffman tiles: position q = 256 * (i / 8) + 8 * l + i % 8 is symbol i of lane
+ * l, so lane l of the decoding warp owns 8 consecutive positions out of every
+ * 256 (8 l .. 8 l + 7, 256 + 8 l .. 256 + 8 l + 7, ...).  rANS tiles: position
+ * q = 32 * i + l is symbol i of lane l (positions l, l + 32, l + 64, ...).
  *
  * Huffman tile record (DFloat11's EncodedExponent / PackedSignMantissa /
  * per-thread start offsets, re-cut so every lane owns a fixed number of symbols):
@@ -42,7 +44,7 @@
 #include <stdint.h>
 
 #define EC_BLOB_MAGIC 0x31434345u /* "ECC1" */
-#define EC_BLOB_VERSION 4u
+#define EC_BLOB_VERSION 5u
 
 #define EC_L1_BITS 12            /* level-1 Huffman window */
 #define EC_SUB_BITS 8            /* bits per sub-table level */

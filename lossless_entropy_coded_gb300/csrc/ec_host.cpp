@@ -377,13 +377,15 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
     const int max_len = params ? params->max_code_len : EC_DEFAULT_MAX_CODE_LEN;
     int steps = params ? params->tile_steps : 0;
     if (max_len < 1 || max_len > EC_MAX_CODE_LEN) return EC_ERR_INVALID_ARG;
-    if (steps != 0 && steps != 32 && steps != 64 && steps != 128) return EC_ERR_INVALID_ARG;
+    if (steps < 0 || steps > 128 || steps % 16) return EC_ERR_INVALID_ARG;
     int64_t nk = 0, k_pad = round_up(k_cols, EC_HUFF_ROW_ALIGN), n_pad = 0, tmp = 0;
     if (k_cols > INT64_MAX - EC_HUFF_ROW_ALIGN) return EC_ERR_OVERFLOW;
     if (!mul_ok(n_rows, k_cols, &nk) || !mul_ok(n_rows, k_pad, &n_pad) || !mul_ok(n_pad, 4, &tmp))
         return EC_ERR_OVERFLOW;
-    if (steps == 0) /* automatic: at least 1024 tiles where the matrix allows it */
+    if (steps == 0) { /* automatic: at least 1024 tiles where the matrix allows it, inside rows */
         steps = n_pad >= (int64_t)1024 * 32 * 128 ? 128 : n_pad >= (int64_t)1024 * 32 * 64 ? 64 : 32;
+        while ((k_pad / 32) % steps) steps -= 16; /* k_pad / 32 is a multiple of 16 */
+    }
     if (nk > 0 && !w) return EC_ERR_INVALID_ARG;
 
     return guarded([&]() -> int {
@@ -434,7 +436,7 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
                 const int64_t base = t * T, n_t = std::min(T, n_pad - base);
                 gather_padded(w, K, KP, base, n_t, v.data());
                 int64_t bits[32] = {0};
-                for (int64_t q = 0; q < n_t; ++q) bits[q & 31] += m->lengths[(v[q] >> 7) & 0xFF];
+                for (int64_t q = 0; q < n_t; ++q) bits[(q >> 3) & 31] += m->lengths[(v[q] >> 7) & 0xFF];
                 int64_t bytes = 0;
                 for (int l = 0; l < 32; ++l) bytes += (bits[l] + 7) / 8;
                 code_bytes[t] = round_up(bytes + 8, 16);
@@ -491,7 +493,7 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
                 uint8_t* raw = rec + 64;
                 uint32_t* area = (uint32_t*)(rec + 64 + EC_RAW_BYTES(S));
                 for (int64_t q = 0; q < n_t; ++q) {
-                    const int64_t l = q & 31, i = q >> 5; /* lane l, symbol i */
+                    const int64_t l = (q >> 3) & 31, i = ((q >> 8) << 3) | (q & 7); /* lane l, symbol i */
                     raw[((i >> 4) * 32 + l) * 16 + (i & 15)] = (uint8_t)(((v[q] >> 8) & 0x80) | (v[q] & 0x7F));
                 }
                 int64_t bitpos = 0;
@@ -499,7 +501,7 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
                     bitpos = round_up(bitpos, 8);
                     start[l] = (uint16_t)(bitpos / 8);
                     for (int64_t i = 0; i < S; ++i) {
-                        const int e = (v[32 * i + l] >> 7) & 0xFF;
+                        const int e = (v[256 * (i >> 3) + 8 * l + (i & 7)] >> 7) & 0xFF;
                         const int L = m->lengths[e];
                         const uint32_t c = code[e];
                         const int64_t wi = bitpos >> 5;
@@ -784,7 +786,7 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
     const bool huff = h.kind == EC_KIND_HUFFMAN_BF16;
     const int64_t align = huff ? EC_HUFF_ROW_ALIGN : EC_RANS_ROW_ALIGN;
     if (h.k_pad != round_up(h.k_cols, align)) return EC_ERR_CORRUPT;
-    if (huff ? (h.steps != 32 && h.steps != 64 && h.steps != 128) : (h.steps < 1 || (32 * h.steps) % align))
+    if (huff ? (h.steps < 16 || h.steps > 128 || h.steps % 16) : (h.steps < 1 || (32 * h.steps) % align))
         return EC_ERR_CORRUPT;
     int64_t n_pad = 0;
     if (!mul_ok(h.n_rows, h.k_pad, &n_pad)) return EC_ERR_CORRUPT;

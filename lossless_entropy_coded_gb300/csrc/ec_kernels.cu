@@ -5,16 +5,17 @@
  *
  * Huffman path (DFloat11, "70% Size, 100% Accuracy", Algorithm 1, re-cut for the
  * fused product of MINE section 4 "Fused mvm"): one warp owns one tile of
- * 32 * steps weights; lane l decodes its own codeword sequence (positions l,
- * l + 32, ...) from a byte offset stored in the tile record.  Every lookup of a
+ * 32 * steps weights; lane l decodes its own codeword sequence (8 consecutive
+ * positions out of every 256: 8 l .. 8 l + 7, 256 + 8 l .. 256 + 8 l + 7, ...)
+ * from a byte offset stored in the tile record.  Every lookup of a
  * 12-bit pair table in shared memory yields two exponents already in BF16
  * position; a window whose two codewords do not both fit takes a second lookup,
  * and codewords longer than the window (only when the caller asks for a limit
  * above 12 bits) walk the hierarchical table of DFloat11 Fig. 4 / 14 in global
  * memory.  The decoded pair is merged with the raw sign/mantissa bytes
  *     bf16 = (sign << 15) | (exponent << 7) | mantissa      (Algorithm 1 / Eq. (1))
- * in registers and either stored (decode, through a small shared transpose) or
- * multiplied with x in FP32 (GEMV).  Row sums are reduced across the warp with
+ * in registers and either stored (decode: one 16-byte store per lane per 8
+ * symbols) or multiplied with x in FP32 (GEMV).  Row sums are reduced across the warp with
  * shuffles and written once, or added atomically when a row spans tiles.
  *
  * rANS path (EntroPack, independent rANS tiles): one warp per tile, lane l
@@ -26,6 +27,8 @@
  * and payload words are clamped to the tile / table and inconsistent records or
  * streams set the device status word (EC_ERR_CORRUPT) instead of faulting.
  */
+#include <cuda.h> /* CUtensorMap and its encoder's signature (reached through the runtime) */
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -43,6 +46,7 @@ namespace {
 constexpr int kWarps = 8;          /* warps per CTA (rANS and BF16 kernels) */
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kMaxDecodeBatch = EC_MAX_DECODE_BATCH;
+constexpr int kFmaMaxRows = 16;   /* batch rows per pass of the CUDA-core GEMV kernels */
 
 /* ------------------------------------------------------------ descriptors */
 struct HuffMat {
@@ -80,6 +84,23 @@ struct HuffDecodeArgs {
     int64_t total_tiles;
     int* status;
     int code_bytes;
+};
+
+/* Tensor-core GEMV launch (matrices whose tiles never cross a row).  A work item
+ * is `rows` consecutive rows (one per decoding warp) x one tile column of a
+ * matrix; items are numbered matrix by matrix, row block by row block, tile
+ * column fastest. */
+struct HuffMmaArgs {
+    CUtensorMap xmap;                   /* x [batch, k_cols] BF16: boxes of 32 rows x 64 columns, 128-byte swizzle */
+    HuffMat m[EC_MAX_GROUP];
+    int count;
+    int batch;                          /* rows of x in this pass, 1..kMmaMaxBatch */
+    int* status;
+    int code_bytes;                     /* per-warp code buffer */
+    int64_t total_tiles;
+    int64_t item_begin[EC_MAX_GROUP + 1];
+    int32_t row_tiles[EC_MAX_GROUP];    /* tiles per row */
+    uint32_t idesc;                     /* tcgen05 instruction descriptor (M = 64, N = warps) */
 };
 
 struct RansMat {
@@ -132,7 +153,8 @@ __device__ __forceinline__ int64_t tile_row(int64_t t, int64_t T, int64_t kp, in
 /* ============================================================ Huffman path */
 /*
  * Work layout.  One warp decodes one tile at a time; lane l owns the tile's
- * symbols i = 0 .. S-1 at positions 32 i + l.  Each lookup of the pair table
+ * symbols i = 0 .. S-1 at positions 256 (i / 8) + 8 l + (i % 8), so every 8
+ * symbols of a lane are 8 consecutive columns.  Each lookup of the pair table
  * (shared memory, indexed by the next EC_L1_BITS bits of the lane's stream)
  * yields exactly two exponents, already sitting in the BF16 exponent fields of a
  * 32-bit word [w(i+1) | w(i)].  With a fixed two symbols per lookup the decoded
@@ -149,8 +171,9 @@ __device__ __forceinline__ int64_t tile_row(int64_t t, int64_t T, int64_t kp, in
  * copied with cp.async into the second of two shared-memory buffers while the
  * current tile is decoded from the first; the raw bytes arrive with one
  * coalesced 16-byte load per lane per 16 symbols, two blocks ahead of use and
- * continuing into the next tile; x sits transposed in shared memory
- * (xs_t[l][j] = x[32 j + l]) so lane l finds x for its symbols contiguously.
+ * continuing into the next tile; x sits in shared memory as it is in memory
+ * (rows of k_pad columns), and lane l reads the x of its 8 columns as one
+ * 16-byte load (the 32 lanes read 512 contiguous bytes).
  */
 constexpr int kMaxHW = 32;                     /* max warps per CTA */
 constexpr int kSlackBytes = 64;                /* after a code area: reads run <= 8 steps x 48 bits + 8 bytes past it */
@@ -174,9 +197,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
     return v;
-}
-__device__ __forceinline__ void sts16(uint32_t a, uint32_t v) {
-    asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"((unsigned short)v) : "memory");
 }
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -344,18 +364,13 @@ __host__ __device__ constexpr size_t huff_warp_bytes(int code_bytes) { return 2 
 static_assert(kSlackBytes % 16 == 0 && kSlackBytes >= 8 * 48 / 8 + 16 && kPairTabBytes % 16 == 0, "alignment");
 static_assert(huff_warp_bytes(16) % 16 == 0 && huff_warp_bytes(4112) % 16 == 0, "per-warp block alignment");
 
-/* x for the GEMV, transposed per batch row: xs_t[b][l][j] = x[b][32 j + l], lane
- * stride kp / 32 + 8 entries (the +8 spreads the lanes of a quarter-warp over
- * distinct banks for 16-byte loads). */
-__host__ __device__ constexpr uint32_t xs_lane_stride(uint32_t kp) { return kp / 32 + 8; }
-__host__ __device__ constexpr size_t xs_row_bytes(uint32_t kp) { return (size_t)2 * 32 * xs_lane_stride(kp); }
+/* x for the GEMV: per batch row, k_pad BF16 values (zero past K). */
+__host__ __device__ constexpr size_t xs_row_bytes(uint32_t kp) { return (size_t)2 * kp; }
 
-/* Stage x [batch, K] (BF16) transposed into shared memory, xs_t[b][l][j] =
- * x[b][32 j + l], zero past K: 16-byte loads, four in flight per thread, when
- * rows are 16-byte aligned (K % 8 == 0; x itself is 16-byte aligned), else
- * 2-byte loads. */
-__device__ __forceinline__ void stage_x(uint16_t* xs, const uint16_t* __restrict__ x, int batch, int64_t K,
-                                        uint32_t kp, uint32_t lx) {
+/* Stage x [batch, K] (BF16) into shared rows of k_pad entries, zero past K:
+ * 16-byte loads and stores, four in flight per thread, when K % 8 == 0. */
+__device__ __forceinline__ void stage_x_rows(uint16_t* xs, const uint16_t* __restrict__ x, int batch, int64_t K,
+                                             uint32_t kp) {
     if ((K & 7) == 0) {
         const uint32_t per_row = kp / 8, n = (uint32_t)batch * per_row;
         for (uint32_t i0 = threadIdx.x; i0 < n; i0 += 4 * blockDim.x) {
@@ -368,26 +383,19 @@ __device__ __forceinline__ void stage_x(uint16_t* xs, const uint16_t* __restrict
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const uint32_t i = i0 + u * blockDim.x;
-                if (i < n) {
-                    const uint32_t b = i / per_row, c = (i - b * per_row) * 8;
-                    uint16_t* dst = xs + (size_t)b * 32 * lx + (c >> 5);
-                    const uint32_t vw[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) dst[((c + j) & 31) * lx] = (uint16_t)(vw[j >> 1] >> (16 * (j & 1)));
-                }
+                if (i < n) *(uint4*)(xs + (size_t)i * 8) = v[u];
             }
         }
     } else {
         for (int b = 0; b < batch; ++b)
-            for (uint32_t c = threadIdx.x; c < kp; c += blockDim.x)
-                xs[(size_t)b * 32 * lx + (c & 31) * lx + (c >> 5)] = c < K ? x[(int64_t)b * K + c] : (uint16_t)0;
+            for (uint32_t c = threadIdx.x; c < kp; c += blockDim.x) xs[(size_t)b * kp + c] = c < K ? x[b * K + c] : 0;
     }
 }
 
 /* A resolved tile record (all lanes hold the same values). */
 struct TileRef {
     const uint8_t* rec; /* lane starts | raw | code area */
-    int64_t t;          /* tile index within its matrix */
+    uint32_t t;         /* tile index within its matrix (a launch has < 2^31 tiles) */
     int mi;             /* matrix of the launch */
     int S;              /* symbols per lane */
     int area;           /* code area bytes; 0 = corrupt record (skipped) */
@@ -407,7 +415,7 @@ __device__ __forceinline__ TileRef tile_ref(const Args& a, int64_t g, uint2 off)
     TileRef r;
     r.mi = owner(a, g);
     const HuffMat& M = a.m[r.mi];
-    r.t = g - M.tile_begin;
+    r.t = (uint32_t)(g - M.tile_begin);
     r.S = r.t == M.n_tiles - 1 ? M.last_steps : M.steps;
     /* offsets are 16-byte units; a record is far below 4 GB */
     const int area = (int)((off.y - off.x) * 16u) - 64 - EC_RAW_BYTES(r.S);
@@ -477,15 +485,15 @@ __device__ __forceinline__ void prefetch_code(uint32_t buf, uint32_t mbar, const
  * after block b is decoded, into the ring slot it frees; blocks 0 and 1 of the
  * next tile are loaded the same way at the end of the current one. */
 template <bool kLong, class Args, class TabOf, class Begin, class Block, class Half, class End>
-__device__ __forceinline__ void huff_walk(const Args& a, int64_t g0, int64_t stride, int64_t g_end, TileRef cur,
+__device__ __forceinline__ void huff_walk(const Args& a, uint32_t g0, uint32_t stride, uint32_t g_end, TileRef cur,
                                           uint32_t bufs, uint32_t buf_bytes, uint32_t& ph, int lane,
                                           TabOf&& tab_of, Begin&& begin, Block&& block, Half&& half, End&& end) {
     const uint32_t mbars = bufs + 2 * buf_bytes;
     uint2 off_next = g0 + stride < g_end ? tile_offsets(a, g0 + stride) : make_uint2(0u, 0u);
     uint4 rr[2] = {};
-    bool raw_ready = false;
+    bool raw_ready = false, raw_swap = false;
     uint32_t cb = bufs; /* buffer of the current tile */
-    for (int64_t g = g0; g < g_end; g += stride) {
+    for (uint32_t g = g0; g < g_end; g += stride) {
         const uint32_t bi = cb == bufs ? 0u : 1u;
         const bool arrived = mbar_wait(mbars + 8 * bi, (ph >> bi) & 1u); /* the current tile's copy */
         ph ^= 1u << bi;
@@ -517,17 +525,19 @@ __device__ __forceinline__ void huff_walk(const Args& a, int64_t g0, int64_t str
         if (!raw_ready) {
             rr[0] = __ldg(raw4);
             if (nb > 1) rr[1] = __ldg(raw4 + 32);
+        } else if (raw_swap) { /* the previous tile's block count was odd */
+            const uint4 t = rr[0];
+            rr[0] = rr[1];
+            rr[1] = t;
         }
-        /* blocks 0 and 1 of the next tile land in ring slots 0 and 1 when this
-         * tile's block count is even */
-        const bool chain = has_next && nxt.area > 0 && (nb & 1) == 0;
+        /* each decoded block's slot takes the block two ahead, continuing into blocks
+         * 0 and 1 of the next tile; after an odd block count those land in slots 1
+         * and 0 and are swapped when the next tile starts */
+        const bool chain = has_next && nxt.area > 0 && nb >= 2;
         const uint4* nraw4 = (const uint4*)((chain ? nxt.rec : cur.rec) + 64) + lane;
         const int nnbc = chain ? min(2, nxt.S / 16) : 0; /* next-tile blocks to prefetch */
-        const uint4* rp = raw4 + 64;                    /* blocks b0 + 2, b0 + 3 */
         begin(cur);
         for (int b0 = 0; b0 < nb; b0 += 2) {
-            const bool last_pair = b0 + 2 >= nb;
-            const uint4* src = last_pair ? nraw4 : rp;
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int blk = b0 + u;
@@ -541,12 +551,14 @@ __device__ __forceinline__ void huff_walk(const Args& a, int64_t g0, int64_t str
                     half(w, 0);
                     decode8<kLong>(s, c, a, rr[u].z, rr[u].w, w);
                     half(w, 1);
-                    if (last_pair ? u < nnbc : blk + 2 < nb) rr[u] = __ldg(src + 32 * u);
+                    const int ahead = blk + 2;
+                    if (ahead < nb) rr[u] = __ldg(raw4 + 32 * ahead);
+                    else if (ahead - nb < nnbc) rr[u] = __ldg(nraw4 + 32 * (ahead - nb));
                 }
             }
-            rp += 64;
         }
         raw_ready = chain;
+        raw_swap = chain && (nb & 1);
         /* every lane's codewords end in the last byte before the next lane's start
          * (the last lane: before the >= 8 zero bytes closing the area) */
         const uint32_t p = s.p;
@@ -569,14 +581,13 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
     const uint32_t kp = (uint32_t)a.m[0].k_pad;
     const int64_t K = a.m[0].k_cols;
     const int batch = a.batch;
-    const uint32_t lx = xs_lane_stride(kp);
 
-    /* shared: pair tables | x transposed [batch][32][lx] | per warp: two tile buffers */
+    /* shared: pair tables | x [batch][k_pad] | per warp: two tile buffers */
     uint4* tabs = (uint4*)smem;
     uint16_t* xs = (uint16_t*)(smem + (size_t)a.count * kPairTabBytes);
     uint8_t* wbase = (uint8_t*)xs + (size_t)batch * xs_row_bytes(kp) + (size_t)warp * huff_warp_bytes(a.code_bytes);
     const uint32_t bufs = smem_u32(wbase), buf_bytes = (uint32_t)tile_buf_bytes(a.code_bytes);
-    const uint32_t xs_lane = smem_u32(xs) + lane * lx * 2, tabs_s = smem_u32(tabs);
+    const uint32_t xs_lane = smem_u32(xs) + 16u * lane, tabs_s = smem_u32(tabs); /* x of the lane's 8 columns */
 
     const int nwarp = blockDim.x >> 5;
     const int64_t gw = (int64_t)blockIdx.x * nwarp + warp, nw = (int64_t)gridDim.x * nwarp;
@@ -599,34 +610,34 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
     }
     grid_dep_launch();
     grid_dep_wait(); /* x and y belong to the preceding kernel in the stream from here on */
-    stage_x(xs, a.x, batch, K, kp, lx);
+    stage_x_rows(xs, a.x, batch, K, kp);
     __syncthreads();
     if (gw >= a.total_tiles) return;
 
     const uint32_t jrow = kp / 32;
     int prev_mi = -1;
-    int64_t prev_t = 0, row0 = 0, col0 = 0; /* where this warp's current tile starts */
+    uint32_t prev_t = 0, row0 = 0, col0 = 0; /* where this warp's current tile starts (rows, columns < 2^31) */
     float acc[B][2];
     /* x of the current 8 symbols: loaded one half-block ahead for narrow batches,
      * at use for wide ones (whose registers go to the accumulators) */
     constexpr bool kAhead = B <= 4;
     uint4 xv[kAhead ? B : 1];
-    int64_t row = 0, t_cur = 0;
-    uint32_t jc = 0; /* x column block of the current 8 symbols */
+    uint32_t row = 0, t_cur = 0;
+    uint32_t jc = 0; /* first column / 32 of the current 8 symbols' 256-column block */
     const HuffMat* Mp = &a.m[0];
     auto load_x = [&](uint32_t j) {
-        const uint32_t xa = xs_lane + 2 * j;
+        const uint32_t xa = xs_lane + 64 * j;
 #pragma unroll
         for (int b = 0; b < (kAhead ? B : 0); ++b) {
             if (B > 1 && b >= batch) break;
             xv[b] = lds128(xa + (uint32_t)(b * xs_row_bytes(kp)));
         }
     };
-    auto flush = [&](int64_t r) {
+    auto flush = [&](uint32_t r) {
         const HuffMat& M = *Mp;
         int64_t slot = 0;
         if (kPart) /* tiles before this one that also cover row r */
-            slot = t_cur - (r * M.k_pad) / (32 * (int64_t)M.steps);
+            slot = (int64_t)t_cur - ((int64_t)r * M.k_pad) / (32 * (int64_t)M.steps);
 #pragma unroll
         for (int b = 0; b < B; ++b) {
             if (B > 1 && b >= batch) break;
@@ -649,17 +660,17 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
         [&](const TileRef& r) {
             Mp = &a.m[r.mi];
             t_cur = r.t;
-            if (r.mi == prev_mi && r.t == prev_t + nw) { /* the same matrix, the next tile of this warp */
-                row0 += Mp->d_row;
-                col0 += Mp->d_col;
+            if (r.mi == prev_mi && r.t == prev_t + (uint32_t)nw) { /* the same matrix, the next tile of this warp */
+                row0 += (uint32_t)Mp->d_row;
+                col0 += (uint32_t)Mp->d_col;
                 if (col0 >= kp) {
                     col0 -= kp;
                     ++row0;
                 }
             } else {
                 const int64_t T = 32 * (int64_t)Mp->steps;
-                row0 = tile_row(r.t, T, kp, EC_HUFF_ROW_ALIGN);
-                col0 = r.t * T - row0 * (int64_t)kp;
+                row0 = (uint32_t)tile_row(r.t, T, kp, EC_HUFF_ROW_ALIGN);
+                col0 = (uint32_t)((int64_t)r.t * T - (int64_t)row0 * kp);
             }
             prev_mi = r.mi;
             prev_t = r.t;
@@ -680,7 +691,7 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
 #pragma unroll
             for (int b = 0; b < B; ++b) {
                 if (B > 1 && b >= batch) break;
-                const uint4 x4 = kAhead ? xv[b] : lds128(xs_lane + 2 * jc + (uint32_t)(b * xs_row_bytes(kp)));
+                const uint4 x4 = kAhead ? xv[b] : lds128(xs_lane + 64 * jc + (uint32_t)(b * xs_row_bytes(kp)));
                 acc[b][0] = fma2_bf16(w[0], x4.x, acc[b][0]);
                 acc[b][1] = fma2_bf16(w[1], x4.y, acc[b][1]);
                 acc[b][0] = fma2_bf16(w[2], x4.z, acc[b][0]);
@@ -694,12 +705,379 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
         [&]() { flush(row); });
 }
 
+/* ========================================= Huffman tensor-core GEMV (tcgen05) */
+/*
+ * Small batches (MINE section 5: fused kernels for batch > 1 as the next step)
+ * put the product on the 5th-generation tensor cores: y^T = X W^T with BF16
+ * operands in shared memory and FP32 accumulators in tensor memory.
+ *
+ * Work item: `rows` consecutive rows (one per warp, rows = the CTA's warps, a
+ * multiple of 8) x one tile column, for matrices whose tiles do not cross rows.
+ * The item runs in chunks of 256 columns, 8 symbols of every lane.  Lane l of
+ * warp w decodes its 8 symbols (columns 8 l .. 8 l + 7 of the chunk) and stores
+ * them as ONE 16-byte row segment of a 128-byte-swizzled K-major operand; warp
+ * b < batch copies the same 16 bytes of x row b.  Lane l's segment is chunk
+ * l % 8 of the 128-byte row in swizzle atom l / 8, so the 32 stores of a warp hit
+ * all banks (4 wavefronts).
+ *
+ * MMA: M = 64 rows of x (the batch; rows past it are never read back), N =
+ * `rows` weight rows, K = 16, kind::f16 with BF16 inputs; 16 per chunk, issued
+ * by one lane (the chunk's issuing warp rotates over the CTA) once every warp
+ * has stored the chunk (mbarrier `full`), and committed to the chunk buffer's
+ * mbarrier (`done`), which the decoders wait on before reusing the buffer two
+ * chunks later.  MMAs that accumulate into one TMEM tile run one after the
+ * other, so a chunk spreads its 16 over four tiles (k step mod 4) and
+ * consecutive chunks use different sets of four: eight 32-column tiles per item,
+ * each touched again only two chunks later, after the waits above.  The batch
+ * rows 32..63 of the A operand are the weight rows of the same swizzle atom
+ * (batch <= 32 per pass): their products land in accumulator rows that are
+ * never read, so both operands of a chunk fit in 32 KB.
+ *
+ * Accumulators: TMEM columns [256 (i mod 2), 256 (i mod 2) + 256) for the i-th
+ * item of the CTA.  After an item's last chunk warps 0..3 read their lane quarter
+ * of the eight tiles (tcgen05.ld 32x32b) and add them in a fixed order: with
+ * M = 64, accumulator row 16 q + i sits in TMEM lane 32 q + i.  Row
+ * r of the item goes to y[b][row0 + r]: stored, or added when a row spans tiles.
+ */
+constexpr int kMmaChunk = 256;                  /* columns per chunk */
+constexpr uint32_t kMmaBufBytes = 32768u;       /* one chunk: 4 swizzle atoms of 8 KB */
+constexpr uint32_t kMmaAtomBytes = 8192u;       /* 64 rows x 128 B: x rows 0..31, then weight rows 0..31 */
+constexpr int kMmaMaxBatch = 32;                /* x rows per pass */
+constexpr size_t kMmaFixedBytes = 1024 + 2 * (size_t)kMmaBufBytes + 64; /* alignment, buffers, barriers */
+
+__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+__device__ __forceinline__ void mbar_init_n(uint32_t mbar, uint32_t n) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
+}
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+/* Shared-memory matrix descriptor of a 128-byte-swizzled K-major operand whose
+ * 8-row groups are 1024 bytes apart: start address >> 4 (bits 0..13), leading
+ * offset 16 B (unused by swizzled K-major layouts), stride offset 1024 B >> 4
+ * (bits 32..45), the descriptor version 1 (bit 46) and swizzle mode 2 = 128 B
+ * (bits 61..63).  Stepping K by 16 inside a 64-column atom adds 32 bytes to the
+ * start; the swizzle is applied to the absolute address, so atoms are 1024-aligned. */
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1u << 16) | ((uint64_t)(1024u >> 4) << 32) |
+           ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
+}
+
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t mbar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar) : "memory");
+}
+
+/* 2D tiled TMA load of one box (columns x0.., rows y0..) into shared memory,
+ * completing on mbar (x0 is a multiple of 64 columns: 128-byte aligned). */
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x0, int32_t y0,
+                                            uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"((uint64_t)map), "r"(x0), "r"(y0), "r"(mbar)
+        : "memory");
+}
+
+/* 32 lanes x 4 columns of 32 bits from TMEM (the lane quarter of the calling warp). */
+__device__ __forceinline__ void tc_ld4(uint32_t taddr, uint32_t (&v)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                 : "r"(taddr)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+/* The item a warp works on: matrix, first row, tile column, and the combined
+ * index of the tile of the warp's row (have = the row exists). */
+struct MmaItem {
+    int mi;
+    int64_t row0, tc, g;
+    bool have;
+};
+
+__device__ __forceinline__ MmaItem mma_item(const HuffMmaArgs& a, int64_t it, int rows, int d) {
+    MmaItem r;
+    r.mi = 0;
+    while (r.mi + 1 < a.count && it >= a.item_begin[r.mi + 1]) ++r.mi;
+    const HuffMat& M = a.m[r.mi];
+    const int64_t R = a.row_tiles[r.mi], local = it - a.item_begin[r.mi];
+    const int64_t rb = local / R;
+    r.tc = local - rb * R;
+    r.row0 = rb * rows;
+    const int64_t row = r.row0 + d;
+    r.have = d >= 0 && d < rows && row < M.n_rows;
+    r.g = M.tile_begin + (r.have ? row * R + r.tc : 0);
+    return r;
+}
+
+__device__ __forceinline__ TileRef mma_tile(const HuffMmaArgs& a, const MmaItem& it) {
+    if (it.have) return tile_ref(a, it.g, tile_offsets(a, it.g));
+    TileRef r{};
+    r.mi = it.mi;
+    r.S = a.m[it.mi].steps;
+    return r; /* area 0: nothing to copy or decode */
+}
+
+/* What the readout of a finished item needs. */
+struct MmaDone {
+    int mi;
+    int64_t row0;
+    uint32_t dcol, last; /* its accumulator tiles, and its last chunk */
+};
+
+template <bool kLong>
+__global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_constant__ HuffMmaArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+    const int rows = nwarp - 1, d = warp - 1; /* warp 0 produces; warps 1.. decode rows 0.. of the item */
+    /* shared: [align to 1 KB] | 2 chunk buffers | pair tables | per decoding warp: two
+     * tile buffers and their mbarriers | full[2], done[2], xfull[2] | TMEM address */
+    const uint32_t ops = (smem_u32(smem) + 1023u) & ~1023u;
+    const uint32_t tabs_s = ops + 2 * kMmaBufBytes;
+    const uint32_t warp_area = tabs_s + (uint32_t)a.count * kPairTabBytes;
+    const uint32_t wb = (uint32_t)huff_warp_bytes(a.code_bytes);
+    const uint32_t bufs = warp_area + (uint32_t)(d < 0 ? 0 : d) * wb, buf_bytes = (uint32_t)tile_buf_bytes(a.code_bytes);
+    const uint32_t mbars = bufs + 2 * buf_bytes;
+    const uint32_t full = warp_area + (uint32_t)rows * wb, done = full + 16, xfull = full + 32, tslot = full + 48;
+    const int64_t n_items = a.item_begin[a.count];
+
+    if (lane == 0) {
+        if (d >= 0) {
+            mbar_init(mbars);
+            mbar_init(mbars + 8);
+        } else {
+            mbar_init_n(full, (uint32_t)rows);
+            mbar_init_n(full + 8, (uint32_t)rows);
+            mbar_init(done);
+            mbar_init(done + 8);
+            mbar_init(xfull);
+            mbar_init(xfull + 8);
+        }
+        mbar_fence_init();
+    }
+    __syncwarp();
+    int64_t it = blockIdx.x;
+    MmaItem ci = mma_item(a, it, rows, d);
+    TileRef cur = mma_tile(a, ci);
+    if (d >= 0) prefetch_code(bufs, mbars, cur, lane);
+    for (int k = 0; k < a.count; ++k) {
+        const uint4* src = (const uint4*)a.m[k].table;
+        uint4* dst = (uint4*)(smem + (tabs_s - smem_u32(smem)) + (size_t)k * kPairTabBytes);
+        for (int i = threadIdx.x; i < EC_PAIR_WORDS / 4; i += blockDim.x) dst[i] = __ldg(src + i);
+    }
+    if (warp == 0) { /* all 512 TMEM columns: 2 items x 8 accumulator tiles of 32 columns */
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(tslot) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    grid_dep_launch();
+    grid_dep_wait(); /* x and y belong to the preceding kernel in the stream from here on */
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = lds32(tslot);
+
+    /* bounded waits; after one runs out (never seen: it needs a lost arrival) the
+     * thread stops waiting, so a fault in the pipeline cannot hold the SM for long */
+    bool live = true;
+    auto wait = [&](uint32_t bar, uint32_t parity) {
+        if (live && !mbar_wait(bar, parity)) {
+            live = false;
+            flag_corrupt(a.status);
+        }
+        return live;
+    };
+    /* x of chunk g (its columns from col on) into its buffer: 4 boxes of 32 rows x 64 columns */
+    auto load_x = [&](uint32_t g, uint32_t col) {
+        const uint32_t b = ops + (g & 1u) * kMmaBufBytes, bar = xfull + 8 * (g & 1u);
+        mbar_arrive_tx(bar, 4u * 32u * 128u);
+#pragma unroll
+        for (int at = 0; at < 4; ++at) tma_load_2d(b + at * kMmaAtomBytes, &a.xmap, (int32_t)(col + 64 * at), 0, bar);
+    };
+    /* y of a finished item: the warps of lane quarter q < 2 (batch rows 16 q ..) take 4
+     * of its 32 columns each and add the 8 partial tiles in a fixed order */
+    auto readout = [&](const MmaDone& f) {
+        const int q = warp & 3, j = warp >> 2;
+        if (q >= 2 || 16 * q >= a.batch || 4 * j >= rows) return;
+        /* one lane issues every MMA and a commit covers all of that lane's earlier ones, so
+         * the last chunk's suffices; no later chunk on its barrier can have completed yet
+         * (the next one on it needs this warp's stores, or, for the producer, its issue) */
+        wait(done + 8 * (f.last & 1u), (f.last >> 1) & 1u);
+        tc_fence_after();
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t t0 = tmem + ((uint32_t)(32 * q) << 16) + f.dcol + 4u * j;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t v[4][4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) tc_ld4(t0 + 32u * (4 * h + t), v[t]);
+            tc_wait_ld();
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) s[c] += __uint_as_float(v[t][c]);
+        }
+        tc_fence_before();
+        const HuffMat& M = a.m[f.mi];
+        const int b = 16 * q + lane;
+        if (lane < 16 && b < a.batch) {
+            float* yb = M.y + (int64_t)b * M.n_rows + f.row0;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int r = 4 * j + c;
+                if (r < rows && f.row0 + r < M.n_rows) {
+                    if (M.atomic_y) atomicAdd(yb + r, s[c]);
+                    else yb[r] = s[c];
+                }
+            }
+        }
+    };
+
+    uint32_t ph = 0;  /* parity of the next phase of each tile buffer's mbarrier */
+    uint32_t gc = 0;  /* chunks of this CTA so far */
+    uint32_t cb = bufs;
+    MmaDone prev{};
+    bool have_prev = false;
+    if (d < 0 && lane == 0) load_x(0, (uint32_t)(ci.tc * 32 * a.m[ci.mi].steps));
+    for (uint32_t iter = 0; it < n_items; it += gridDim.x, ++iter) {
+        const HuffMat& M = a.m[ci.mi];
+        const int nch = M.steps / 8;
+        const uint32_t dcol = 256u * (iter & 1u); /* this item's 8 accumulator tiles */
+        const uint32_t col_t = (uint32_t)ci.tc * 32u * (uint32_t)M.steps;
+        const int64_t nit = it + gridDim.x;
+        if (d < 0) {
+            /* ---- producer: x one chunk ahead, then the chunk's 16 MMAs ---- */
+            for (int ch = 0; ch < nch; ++ch, ++gc) {
+                const uint32_t sel = gc & 1u, opb = ops + sel * kMmaBufBytes;
+                if (lane == 0) {
+                    /* x of the next chunk, once the MMAs of chunk gc - 1 (its buffer) are done */
+                    const bool more = ch + 1 < nch || nit < n_items;
+                    if (more) {
+                        if (gc >= 1) wait(done + 8 * (sel ^ 1u), ((gc - 1) >> 1) & 1u);
+                        uint32_t ncol = col_t + (uint32_t)(ch + 1) * kMmaChunk;
+                        if (ch + 1 == nch) {
+                            const MmaItem ni = mma_item(a, nit, rows, d);
+                            ncol = (uint32_t)ni.tc * 32u * (uint32_t)a.m[ni.mi].steps;
+                        }
+                        load_x(gc + 1, ncol);
+                    }
+                    wait(full + 8 * sel, (gc >> 1) & 1u);
+                    wait(xfull + 8 * sel, (gc >> 1) & 1u);
+                    tc_fence_after();
+                    /* accumulator tile 4 (chunk & 1) + (k step & 3): four independent chains per
+                     * chunk, consecutive chunks on different tiles */
+                    const uint32_t dt = tmem + dcol + 128u * (uint32_t)(ch & 1);
+                    const uint64_t ad = sw128_desc(opb), bd = sw128_desc(opb + 4096u);
+#pragma unroll
+                    for (int ks = 0; ks < kMmaChunk / 16; ++ks) {
+                        const uint64_t off = (uint64_t)(((ks >> 2) * kMmaAtomBytes + (ks & 3) * 32) >> 4);
+                        tc_mma_bf16(dt + 32u * (ks & 3), ad + off, bd + off, a.idesc, ch > 1 || ks > 3);
+                    }
+                    tc_commit(done + 8 * sel);
+                }
+                __syncwarp();
+                if (ch == 0 && have_prev) readout(prev); /* the previous item, one chunk late */
+            }
+        } else {
+            /* ---- decoders: 8 symbols of the warp's row per chunk ---- */
+            const uint32_t bi = cb == bufs ? 0u : 1u;
+            const bool arrived = wait(mbars + 8 * bi, (ph >> bi) & 1u); /* this item's tile */
+            ph ^= 1u << bi;
+            __syncwarp();
+            if (!arrived) cur.area = 0;
+            const uint32_t nb_buf = cb == bufs ? bufs + buf_bytes : bufs;
+            if (nit < n_items) /* (the next item's descriptors are resolved again at the end) */
+                prefetch_code(nb_buf, mbars + 8 * (bi ^ 1u), mma_tile(a, mma_item(a, nit, rows, d)), lane);
+            if (ci.have && cur.area == 0 && lane == 0) flag_corrupt(a.status);
+            const bool dec = ci.have && cur.area > 0;
+            const PairCtx c{tabs_s + (uint32_t)ci.mi * kPairTabBytes, cb + 64, ci.mi};
+            const uint32_t pmax = 8u * (uint32_t)cur.area;
+            LaneBits s{};
+            uint32_t s1 = 0;
+            uint4 rr[2] = {};
+            const uint4* raw4 = (const uint4*)(cur.rec + 64) + lane;
+            if (dec) {
+                const uint32_t s0 = lds16(cb + 2 * lane);
+                s1 = lane < 31 ? lds16(cb + 2 * lane + 2) : 0u;
+                bits_seek(s, c.area, 8u * min(s0, (uint32_t)cur.area));
+                rr[0] = __ldg(raw4);
+                if (nch > 2) rr[1] = __ldg(raw4 + 32);
+            }
+            const uint32_t seg = (uint32_t)(lane >> 3) * kMmaAtomBytes + ((uint32_t)((lane & 7) ^ (d & 7)) << 4) +
+                                 4096u + (uint32_t)d * 128u;
+            auto chunk = [&](int ch, uint32_t r0, uint32_t r1) {
+                const uint32_t sel = gc & 1u;
+                uint32_t w[4] = {0u, 0u, 0u, 0u};
+                if (dec) {
+                    s.p = min(s.p, pmax);
+                    decode8<kLong>(s, c, a, r0, r1, w);
+                }
+                /* the buffer is free once the MMAs of chunk gc - 2 are done */
+                if (gc >= 2) wait(done + 8 * sel, ((gc >> 1) + 1u) & 1u);
+                sts128(ops + sel * kMmaBufBytes + seg, w[0], w[1], w[2], w[3]);
+                fence_async_smem(); /* the tensor cores read what the generic stores wrote */
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full + 8 * sel);
+                ++gc;
+            };
+            const int nb = nch / 2; /* raw blocks of 16 symbols; block b + 2 is loaded once block b is decoded */
+            for (int b0 = 0; b0 < nb; b0 += 2) {
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int blk = b0 + u;
+                    if (u == 0 || blk < nb) {
+                        chunk(2 * blk, rr[u].x, rr[u].y);
+                        if (u == 0 && b0 == 0 && have_prev) readout(prev); /* the previous item, one chunk late */
+                        chunk(2 * blk + 1, rr[u].z, rr[u].w);
+                        if (dec && blk + 2 < nb) rr[u] = __ldg(raw4 + 32 * (blk + 2));
+                    }
+                }
+            }
+            /* every lane's codewords end in the last byte before the next lane's start */
+            const uint32_t p = s.p;
+            const bool bad = dec && (lane < 31 ? (p > 8u * s1 || p + 8u <= 8u * s1) : (p + 64u > pmax));
+            if (__any_sync(kFull, bad) && lane == 0) flag_corrupt(a.status);
+            cb = nb_buf;
+        }
+        prev.mi = ci.mi;
+        prev.row0 = ci.row0;
+        prev.dcol = dcol;
+        prev.last = gc - 1;
+        have_prev = true;
+        if (nit < n_items) {
+            ci = mma_item(a, nit, rows, d);
+            cur = mma_tile(a, ci);
+        }
+    }
+    if (have_prev) readout(prev);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+    }
+}
+
 /* ====================================================== Huffman decode kernel */
 /* Each CTA owns a contiguous range of the launch's tiles; it walks the range one
- * matrix segment at a time, with that matrix's pair table in shared memory.  The
- * warp transposes each 256 outputs (8 symbols of 32 lanes) through a small shared
- * buffer so the stores to out are coalesced 16-byte writes. */
-__host__ __device__ constexpr size_t decode_warp_bytes(int code_bytes) { return huff_warp_bytes(code_bytes) + 512; }
+ * matrix segment at a time, with that matrix's pair table in shared memory.
+ * Every 8 symbols of a lane are 8 consecutive columns, so each lane stores them
+ * with one 16-byte write and a warp writes 512 contiguous bytes. */
+__host__ __device__ constexpr size_t decode_warp_bytes(int code_bytes) { return huff_warp_bytes(code_bytes); }
 
 template <bool kLong>
 __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_decode_kernel(const __grid_constant__ HuffDecodeArgs a) {
@@ -708,7 +1086,7 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_decode_kernel(const __gri
     uint4* tab = (uint4*)smem;
     uint8_t* wbase = smem + kPairTabBytes + (size_t)warp * decode_warp_bytes(a.code_bytes);
     const uint32_t bufs = smem_u32(wbase), buf_bytes = (uint32_t)tile_buf_bytes(a.code_bytes);
-    const uint32_t tbuf = bufs + (uint32_t)huff_warp_bytes(a.code_bytes), tab_s = smem_u32(tab);
+    const uint32_t tab_s = smem_u32(tab);
     const uint32_t mbars = bufs + 2 * buf_bytes;
     if (lane == 0) {
         mbar_init(mbars);
@@ -753,12 +1131,8 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_decode_kernel(const __gri
                     }
                 },
                 [&](const uint32_t (&w)[4], int) {
-                    /* lane's 8 outputs are positions 32 i + lane, i = 8k'..8k'+7: transpose */
-                    __syncwarp();
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) sts16(tbuf + 64 * j + 2 * lane, w[j >> 1] >> (16 * (j & 1)));
-                    __syncwarp();
-                    const uint4 o = lds128(tbuf + 16 * lane);
+                    /* the lane's 8 outputs are columns col0 + 8 lane .. + 7: one 16-byte store */
+                    const uint4 o = make_uint4(w[0], w[1], w[2], w[3]);
                     const int64_t col = col0 + 8 * lane;
                     uint16_t* dst = M.out + row * K + col;
                     if (vec) {
@@ -791,31 +1165,6 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_decode_kernel(const __gri
  * over a group in FP32, then multiply by the group's scale (both exact up to the
  * FP32 sums); decode: BF16 round-to-nearest-even of code * scale (exact in FP32).
  */
-/* Stage x [batch, K] (BF16) into shared rows of k_pad entries, zero past K:
- * 16-byte loads and stores, four in flight per thread, when K % 8 == 0. */
-__device__ __forceinline__ void stage_x_rows(uint16_t* xs, const uint16_t* __restrict__ x, int batch, int64_t K,
-                                             uint32_t kp) {
-    if ((K & 7) == 0) {
-        const uint32_t per_row = kp / 8, n = (uint32_t)batch * per_row;
-        for (uint32_t i0 = threadIdx.x; i0 < n; i0 += 4 * blockDim.x) {
-            uint4 v[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t i = i0 + u * blockDim.x, b = i / per_row, c = (i - b * per_row) * 8;
-                v[u] = i < n && c < K ? __ldg((const uint4*)(x + (int64_t)b * K + c)) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t i = i0 + u * blockDim.x;
-                if (i < n) *(uint4*)(xs + (size_t)i * 8) = v[u];
-            }
-        }
-    } else {
-        for (int b = 0; b < batch; ++b)
-            for (uint32_t c = threadIdx.x; c < kp; c += blockDim.x) xs[(size_t)b * kp + c] = c < K ? x[b * K + c] : 0;
-    }
-}
-
 __host__ __device__ constexpr int rans_max_warps(int b) { return b <= 1 ? 32 : (b <= 4 ? 24 : 16); }
 
 /* one tile buffer: 32 states, the words (capacity rounded to 16 bytes), slack */
@@ -1165,6 +1514,17 @@ bool use_pdl() {
     return on;
 }
 
+/* Smallest batch that the Huffman GEMV runs on the tensor cores (when the
+ * matrices' tiles lie inside rows); EC_MMA_MIN_BATCH overrides it (a value above
+ * EC_MAX_BATCH keeps every batch on the CUDA cores). */
+int mma_min_batch() {
+    static const int v = [] {
+        const char* e = std::getenv("EC_MMA_MIN_BATCH");
+        return e && e[0] ? std::max(1, std::atoi(e)) : 4;
+    }();
+    return v;
+}
+
 template <class... KArgs, class... Args>
 int launch_ex(void (*kernel)(KArgs...), int grid, int block, size_t smem, cudaStream_t s, Args... args) {
     cudaLaunchConfig_t cfg = {};
@@ -1226,6 +1586,11 @@ RansMat rans_desc(const ec_matrix* W) {
 int check_matrix(const ec_matrix* W, int dev) {
     if (!W || !W->d_blob || W->hdr.magic != EC_BLOB_MAGIC || W->hdr.version != EC_BLOB_VERSION) return EC_ERR_INVALID_ARG;
     if (W->device != dev) return EC_ERR_INVALID_ARG;
+    /* the Huffman kernels keep tile, row and column indices in 32 bits: a launch of
+     * up to EC_MAX_GROUP (or EC_MAX_DECODE_BATCH) such matrices stays below 2^31 tiles */
+    if (W->kind == EC_KIND_HUFFMAN_BF16 &&
+        (W->hdr.n_tiles > (int64_t(1) << 24) || W->hdr.n_rows >= (int64_t(1) << 31) || W->hdr.k_pad >= (int64_t(1) << 31)))
+        return EC_ERR_UNSUPPORTED;
     return EC_OK;
 }
 
@@ -1312,7 +1677,7 @@ int plan_huff_gemv(const DeviceInfo& d, int count, int code_bytes, int64_t kp, i
     int64_t best_cost = INT64_MAX;
     for (int w = wmax; w >= 1; --w) {
         const size_t fixed = tables + (size_t)w * per_warp;
-        const int rows = (int)std::min<size_t>(batch, (d.smem_optin - fixed) / pl->xrow);
+        const int rows = (int)std::min<size_t>(std::min(batch, kFmaMaxRows), (d.smem_optin - fixed) / pl->xrow);
         const int64_t passes = (batch + rows - 1) / rows, slots = (int64_t)d.sms * w;
         const int64_t cost = passes * ((total_tiles + slots - 1) / slots) * std::max(w, kKnee);
         if (cost < best_cost) {
@@ -1329,8 +1694,97 @@ int plan_huff_gemv(const DeviceInfo& d, int count, int code_bytes, int64_t kp, i
 }
 
 
+/* Tensor-core path: every matrix's tiles must lie inside one row. */
+bool mma_layout(const ec_matrix* W) {
+    const ec_blob_header& h = W->hdr;
+    return h.n_tiles > 0 && h.steps % 16 == 0 && h.k_pad % (32 * (int64_t)h.steps) == 0 && h.k_pad < (int64_t(1) << 31);
+}
+
+/* cuTensorMapEncodeTiled, reached through the runtime (no link against the driver library). */
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return (PFN_cuTensorMapEncodeTiled_v12000)p;
+    }();
+    return fn;
+}
+
+/* x [rows, K] BF16 as TMA boxes of 32 rows x 64 columns (128 bytes) with the
+ * 128-byte swizzle of the MMA operand; rows past `rows` and columns past K read
+ * as zero.  Needs K % 8 == 0 (16-byte row stride) and a 16-byte aligned x. */
+int encode_x_map(CUtensorMap* map, const uint16_t* x, int64_t K, int rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return EC_ERR_CUDA;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {64, 32}, estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)x, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? EC_OK : EC_ERR_CUDA;
+}
+
+int huff_mma(const ec_matrix* const* Ws, int count, const uint16_t* x, float* const* ys, int batch, cudaStream_t s,
+             DeviceInfo* d) {
+    HuffMmaArgs a{};
+    a.count = count;
+    a.status = d->status;
+    int code_bytes = 16;
+    bool lng = false;
+    int64_t total = 0;
+    const int64_t K = Ws[0]->hdr.k_cols;
+    for (int k = 0; k < count; ++k) {
+        const ec_matrix* W = Ws[k];
+        a.m[k] = huff_desc(W);
+        a.m[k].tile_begin = total;
+        total += W->hdr.n_tiles;
+        a.row_tiles[k] = (int32_t)(W->hdr.k_pad / (32 * (int64_t)W->hdr.steps));
+        code_bytes = std::max(code_bytes, (int)W->hdr.max_code_bytes);
+        lng = lng || W->hdr.max_len > EC_L1_BITS;
+        if (a.m[k].atomic_y &&
+            cudaMemsetAsync(ys[k], 0, sizeof(float) * (size_t)batch * (size_t)W->hdr.n_rows, s) != cudaSuccess)
+            return EC_ERR_CUDA;
+    }
+    code_bytes = (code_bytes + 15) & ~15;
+    a.code_bytes = code_bytes;
+    a.total_tiles = total;
+    /* warps: a multiple of 8, at most 32, as many as fit; one produces, the others
+     * decode one row each (rows per item = warps - 1, N = warps) */
+    const size_t fixed = kMmaFixedBytes + (size_t)count * kPairTabBytes, per_warp = huff_warp_bytes(code_bytes);
+    int nw = 0;
+    for (int w = kMaxHW; w >= 8 && !nw; w -= 8)
+        if (fixed + (size_t)(w - 1) * per_warp <= d->smem_optin) nw = w;
+    if (!nw) return EC_ERR_UNSUPPORTED;
+    const int rows = nw - 1;
+    const size_t smem = fixed + (size_t)rows * per_warp;
+    a.item_begin[0] = 0;
+    for (int k = 0; k < count; ++k)
+        a.item_begin[k + 1] = a.item_begin[k] + (Ws[k]->hdr.n_rows + rows - 1) / rows * a.row_tiles[k];
+    /* kind::f16 instruction descriptor: FP32 accumulators (bits 4..5 = 1), BF16 A and B
+     * (bits 7..9, 10..12 = 1), both K-major, N >> 3 in bits 17..22, M >> 4 in bits 24..28 */
+    a.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(nw >> 3) << 17) | ((64u >> 4) << 24);
+    const int grid = (int)std::min<int64_t>(d->sms, a.item_begin[count]);
+    auto kern = lng ? huff_mma_kernel<true> : huff_mma_kernel<false>;
+    if (set_smem(kern, smem) != EC_OK) return EC_ERR_CUDA;
+    for (int b0 = 0; b0 < batch; b0 += kMmaMaxBatch) {
+        a.batch = std::min(kMmaMaxBatch, batch - b0);
+        int rc = encode_x_map(&a.xmap, x + (int64_t)b0 * K, K, a.batch);
+        if (rc != EC_OK) return rc;
+        for (int k = 0; k < count; ++k) a.m[k].y = ys[k] + (int64_t)b0 * Ws[k]->hdr.n_rows;
+        if ((rc = launch_ex(kern, grid, nw * 32, smem, s, a)) != EC_OK) return rc;
+    }
+    return EC_OK;
+}
+
 int huff_gemv(const ec_matrix* const* Ws, int count, const uint16_t* x, float* const* ys, int batch,
               cudaStream_t s, int dev, DeviceInfo* d) {
+    bool mma = batch >= mma_min_batch() && Ws[0]->hdr.k_cols % 8 == 0; /* (TMA rows of x: 16-byte stride) */
+    for (int k = 0; k < count && mma; ++k) mma = mma_layout(Ws[k]);
+    if (mma) return huff_mma(Ws, count, x, ys, batch, s, d);
     int64_t total = 0;
     int code_bytes = 16;
     bool lng = false;
@@ -1391,7 +1845,7 @@ int rans_run(const ec_matrix* W, const uint16_t* x, float* y, uint16_t* out, int
                          : rans_max_warps(1);
     const int warps = (int)std::min<size_t>(cap, (d->smem_optin - table - xrow) / per_warp);
     const size_t fixed = table + (size_t)warps * per_warp;
-    const int per_pass = gemv ? (int)std::min<size_t>(batch, (d->smem_optin - fixed) / xrow) : 1;
+    const int per_pass = gemv ? (int)std::min<size_t>(std::min(batch, kFmaMaxRows), (d->smem_optin - fixed) / xrow) : 1;
     if (per_pass < 1) return EC_ERR_UNSUPPORTED;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(d->sms, (W->hdr.n_tiles + warps - 1) / warps));
     const int passes = gemv ? batch : 1;

@@ -79,7 +79,7 @@ def test_argument_validation(ec):
     W = ec.encode_bf16(synth.gauss_bf16(1, (4, 8), 0.02), device=-1)
     assert lib.ec_gemv(W.handle, None, None, 1, None) == _ec.EC_ERR_INVALID_ARG
     assert lib.ec_gemv(W.handle, None, None, 0, None) == _ec.EC_ERR_INVALID_ARG
-    assert lib.ec_gemv(W.handle, None, None, 17, None) == _ec.EC_ERR_UNSUPPORTED
+    assert lib.ec_gemv(W.handle, None, None, 65, None) == _ec.EC_ERR_UNSUPPORTED
 
 
 # --------------------------------------------------------------- blob reader
@@ -95,6 +95,11 @@ def parse(blob: bytes):
             "prob_bits", "max_words", "max_len", "rans_tuple"]
     h = dict(zip(keys, f))
     return h, dev
+
+
+def huff_pos(i: int, l: int) -> int:
+    """Position in its tile of symbol i of lane l: 8 consecutive positions of every 256."""
+    return 256 * (i // 8) + 8 * l + i % 8
 
 
 def read_huffman(blob: bytes, lengths: np.ndarray) -> np.ndarray:
@@ -129,9 +134,8 @@ def read_huffman(blob: bytes, lengths: np.ndarray) -> np.ndarray:
                     pos += 1
                     assert L <= 24
                 e = table[(L, c)]
-                q = 32 * i + l
-                r = int(raw[q])
-                flat[t * T + q] = ((r & 0x80) << 8) | (e << 7) | (r & 0x7F)
+                r = int(raw[32 * i + l])  # raw is [symbol][lane]
+                flat[t * T + huff_pos(i, l)] = ((r & 0x80) << 8) | (e << 7) | (r & 0x7F)
     return flat.reshape(n, kp)[:, :k]
 
 
@@ -180,8 +184,8 @@ def walk_pair_table(blob: bytes):
                     l1 = (f >> 16) & 15
                     x1, l1 = ((f >> 7) & 255, l1) if l1 else one(bits, p + l0)
                     adv = l0 + l1
-                exps[t * T + 32 * (2 * s) + l] = x0
-                exps[t * T + 32 * (2 * s + 1) + l] = x1
+                exps[t * T + huff_pos(2 * s, l)] = x0
+                exps[t * T + huff_pos(2 * s + 1, l)] = x1
                 p += adv
             if l < 31:
                 ends_ok &= 8 * int(start[l + 1]) - 8 < p <= 8 * int(start[l + 1])
