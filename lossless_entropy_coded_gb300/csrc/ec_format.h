@@ -44,12 +44,13 @@
 #include <stdint.h>
 
 #define EC_BLOB_MAGIC 0x31434345u /* "ECC1" */
-#define EC_BLOB_VERSION 5u
+#define EC_BLOB_VERSION 6u
 
 #define EC_L1_BITS 12            /* level-1 Huffman window */
 #define EC_SUB_BITS 8            /* bits per sub-table level */
 #define EC_PAIR_WORDS (1 << EC_L1_BITS) /* u32 words of the pair table */
 #define EC_HUFF_ROW_ALIGN 512    /* k_pad multiple for the Huffman layout (16 symbols x 32 lanes) */
+#define EC_MMA_WINDOW_ROWS 31     /* rows whose tiles one tensor-core work item stages together */
 #define EC_RANS_ROW_ALIGN 128    /* k_pad multiple for the rANS layout (= scale group) */
 #define EC_MAX_CODE_LEN 24
 
@@ -108,7 +109,10 @@ typedef struct {
     int32_t max_words;                /* rANS: largest payload of any tile (u16 words) */
     int32_t max_len;                  /* Huffman: longest codeword in use */
     int32_t rans_tuple;               /* rANS: codes per symbol, 1 or 2 */
-    uint8_t pad[256 - 4 * 4 - 8 * 10 - 4 * 5];
+    int32_t window_code_bytes;        /* Huffman, tiles inside rows: the largest sum of (64 + code area)
+                                       * over EC_MMA_WINDOW_ROWS consecutive rows' tiles of one tile
+                                       * column; 0 when tiles cross rows */
+    uint8_t pad[256 - 4 * 4 - 8 * 10 - 4 * 6];
 } ec_blob_header;
 
 #endif /* EC_FORMAT_H_ */

@@ -476,6 +476,22 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
         h.blob_bytes = h.records_off + total;
         h.max_code_bytes = (int32_t)max_code;
         h.max_len = *std::max_element(m->lengths, m->lengths + 256);
+        {   /* staging size for the tensor-core kernel: a window of rows (tiles inside rows) */
+            h.window_code_bytes = 0;
+            if (KP % T == 0 && n_tiles > 0) {
+                const int64_t R = KP / T;
+                int64_t best = 0;
+                for (int64_t tc = 0; tc < R; ++tc) {
+                    int64_t sum = 0;
+                    for (int64_t r = 0; r < n_rows; ++r) {
+                        sum += 64 + code_bytes[r * R + tc];
+                        if (r >= EC_MMA_WINDOW_ROWS) sum -= 64 + code_bytes[(r - EC_MMA_WINDOW_ROWS) * R + tc];
+                        best = std::max(best, sum);
+                    }
+                }
+                h.window_code_bytes = (int32_t)std::min<int64_t>(best, INT32_MAX);
+            }
+        }
 
         std::vector<uint8_t> blob((size_t)h.blob_bytes, 0);
         std::memcpy(blob.data(), &h, sizeof h);
@@ -799,6 +815,7 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
             (h.table_words - EC_PAIR_WORDS - (1 << EC_L1_BITS)) % 256)
             return EC_ERR_CORRUPT;
         if (h.max_len < 0 || h.max_len > EC_MAX_CODE_LEN || h.max_code_bytes < 0) return EC_ERR_CORRUPT;
+        if (h.window_code_bytes < 0) return EC_ERR_CORRUPT;
     } else {
         if (h.prob_bits < 9 || h.prob_bits > 15 || h.table_words != (int64_t(1) << h.prob_bits) || h.max_words < 0)
             return EC_ERR_CORRUPT;

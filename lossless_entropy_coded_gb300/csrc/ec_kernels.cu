@@ -101,6 +101,7 @@ struct HuffMmaArgs {
     int64_t item_begin[EC_MAX_GROUP + 1];
     int32_t row_tiles[EC_MAX_GROUP];    /* tiles per row */
     uint32_t idesc;                     /* tcgen05 instruction descriptor (M = 64, N = warps) */
+    int nbuf;                           /* chunk buffers (2 or 3) */
 };
 
 struct RansMat {
@@ -711,39 +712,45 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
  * put the product on the 5th-generation tensor cores: y^T = X W^T with BF16
  * operands in shared memory and FP32 accumulators in tensor memory.
  *
- * Work item: `rows` consecutive rows (one per warp, rows = the CTA's warps, a
- * multiple of 8) x one tile column, for matrices whose tiles do not cross rows.
- * The item runs in chunks of 256 columns, 8 symbols of every lane.  Lane l of
- * warp w decodes its 8 symbols (columns 8 l .. 8 l + 7 of the chunk) and stores
- * them as ONE 16-byte row segment of a 128-byte-swizzled K-major operand; warp
- * b < batch copies the same 16 bytes of x row b.  Lane l's segment is chunk
- * l % 8 of the 128-byte row in swizzle atom l / 8, so the 32 stores of a warp hit
- * all banks (4 wavefronts).
+ * Roles: warp 0 produces (x by TMA, the MMAs, a quarter of the read-out); warps
+ * 1 .. rows decode, one weight row each (rows = warps - 1; N = warps, a multiple
+ * of 8, the operand's last row unused).
  *
- * MMA: M = 64 rows of x (the batch; rows past it are never read back), N =
- * `rows` weight rows, K = 16, kind::f16 with BF16 inputs; 16 per chunk, issued
- * by one lane (the chunk's issuing warp rotates over the CTA) once every warp
- * has stored the chunk (mbarrier `full`), and committed to the chunk buffer's
- * mbarrier (`done`), which the decoders wait on before reusing the buffer two
- * chunks later.  MMAs that accumulate into one TMEM tile run one after the
- * other, so a chunk spreads its 16 over four tiles (k step mod 4) and
- * consecutive chunks use different sets of four: eight 32-column tiles per item,
- * each touched again only two chunks later, after the waits above.  The batch
- * rows 32..63 of the A operand are the weight rows of the same swizzle atom
- * (batch <= 32 per pass): their products land in accumulator rows that are
- * never read, so both operands of a chunk fit in 32 KB.
+ * Work item: `rows` consecutive rows x one tile column, for matrices whose tiles
+ * do not cross rows.  The item runs in chunks of 256 columns, 8 symbols of every
+ * lane.  Lane l of a decoding warp decodes its 8 symbols (columns 8 l .. 8 l + 7
+ * of the chunk) and stores them as ONE 16-byte row segment of a
+ * 128-byte-swizzled K-major operand: chunk l % 8 of the 128-byte row in swizzle
+ * atom l / 8, so the 32 stores of a warp hit all banks (4 wavefronts).  x arrives
+ * by TMA in the same swizzled layout (boxes of 32 rows x 64 columns; rows past
+ * the batch and columns past K read as zero), issued one chunk ahead.
+ *
+ * MMA: M = 64 rows of x (the batch; rows past it are never read back), N = warps
+ * weight rows, K = 16, kind::f16 with BF16 inputs; 16 per chunk, issued by one
+ * elected lane of the converged producer warp once every decoding warp has
+ * stored the chunk (mbarrier `full`) and its x has landed (`xfull`), then
+ * committed to the chunk buffer's mbarrier (`done`), which the decoders and the
+ * next x copy wait on before reusing the buffer.  MMAs that accumulate into one
+ * TMEM tile run one after the other, so a chunk spreads its 16 over four tiles
+ * (k step mod 4) and consecutive chunks use different sets of four: eight
+ * 32-column tiles per item.  The batch rows 32..63 of the A operand are the
+ * weight rows of the same swizzle atom (batch <= 32 per pass): their products
+ * land in accumulator rows that are never read, so both operands of a chunk fit
+ * in 32 KB.
  *
  * Accumulators: TMEM columns [256 (i mod 2), 256 (i mod 2) + 256) for the i-th
- * item of the CTA.  After an item's last chunk warps 0..3 read their lane quarter
- * of the eight tiles (tcgen05.ld 32x32b) and add them in a fixed order: with
- * M = 64, accumulator row 16 q + i sits in TMEM lane 32 q + i.  Row
- * r of the item goes to y[b][row0 + r]: stored, or added when a row spans tiles.
+ * item of the CTA.  One chunk into the next item (or at the end), the 8 warps of
+ * each lane quarter that holds batch rows read 4 of the 32 columns each
+ * (tcgen05.ld 32x32b) and add the eight tiles in a fixed order: with M = 64,
+ * accumulator row 16 q + i sits in TMEM lane 32 q + i.  Row r of the item goes
+ * to y[b][row0 + r]: stored, or added when a row spans tiles.
  */
 constexpr int kMmaChunk = 256;                  /* columns per chunk */
 constexpr uint32_t kMmaBufBytes = 32768u;       /* one chunk: 4 swizzle atoms of 8 KB */
 constexpr uint32_t kMmaAtomBytes = 8192u;       /* 64 rows x 128 B: x rows 0..31, then weight rows 0..31 */
 constexpr int kMmaMaxBatch = 32;                /* x rows per pass */
-constexpr size_t kMmaFixedBytes = 1024 + 2 * (size_t)kMmaBufBytes + 64; /* alignment, buffers, barriers */
+constexpr int kMmaMaxBufs = 3;                 /* chunk buffers in flight: 3 where shared memory allows, else 2 */
+__host__ __device__ constexpr size_t mma_fixed_bytes(int nbuf) { return 1024 + (size_t)nbuf * kMmaBufBytes + 128; } /* alignment, buffers, barriers */
 
 __device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
@@ -769,17 +776,24 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
            ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
 }
 
+/* One MMA, issued by one elected lane of a converged warp (the operands are warp-uniform). */
 __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+/* The completion of the elected lane's earlier MMAs arrives on mbar (converged warp). */
 __device__ __forceinline__ void tc_commit(uint32_t mbar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar) : "memory");
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(mbar)
+        : "memory");
 }
 
 /* 2D tiled TMA load of one box (columns x0.., rows y0..) into shared memory,
@@ -836,7 +850,8 @@ __device__ __forceinline__ TileRef mma_tile(const HuffMmaArgs& a, const MmaItem&
 struct MmaDone {
     int mi;
     int64_t row0;
-    uint32_t dcol, last; /* its accumulator tiles, and its last chunk */
+    uint32_t dcol;  /* its accumulator tiles */
+    uint32_t s, ph; /* buffer and phase parity of its last chunk */
 };
 
 template <bool kLong>
@@ -847,12 +862,13 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
     /* shared: [align to 1 KB] | 2 chunk buffers | pair tables | per decoding warp: two
      * tile buffers and their mbarriers | full[2], done[2], xfull[2] | TMEM address */
     const uint32_t ops = (smem_u32(smem) + 1023u) & ~1023u;
-    const uint32_t tabs_s = ops + 2 * kMmaBufBytes;
+    const int nbuf = a.nbuf;
+    const uint32_t tabs_s = ops + (uint32_t)nbuf * kMmaBufBytes;
     const uint32_t warp_area = tabs_s + (uint32_t)a.count * kPairTabBytes;
     const uint32_t wb = (uint32_t)huff_warp_bytes(a.code_bytes);
     const uint32_t bufs = warp_area + (uint32_t)(d < 0 ? 0 : d) * wb, buf_bytes = (uint32_t)tile_buf_bytes(a.code_bytes);
     const uint32_t mbars = bufs + 2 * buf_bytes;
-    const uint32_t full = warp_area + (uint32_t)rows * wb, done = full + 16, xfull = full + 32, tslot = full + 48;
+    const uint32_t full = warp_area + (uint32_t)rows * wb, done = full + 24, xfull = full + 48, tslot = full + 72;
     const int64_t n_items = a.item_begin[a.count];
 
     if (lane == 0) {
@@ -860,12 +876,11 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
             mbar_init(mbars);
             mbar_init(mbars + 8);
         } else {
-            mbar_init_n(full, (uint32_t)rows);
-            mbar_init_n(full + 8, (uint32_t)rows);
-            mbar_init(done);
-            mbar_init(done + 8);
-            mbar_init(xfull);
-            mbar_init(xfull + 8);
+            for (int i = 0; i < nbuf; ++i) {
+                mbar_init_n(full + 8 * i, (uint32_t)rows);
+                mbar_init(done + 8 * i);
+                mbar_init(xfull + 8 * i);
+            }
         }
         mbar_fence_init();
     }
@@ -900,9 +915,9 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
         }
         return live;
     };
-    /* x of chunk g (its columns from col on) into its buffer: 4 boxes of 32 rows x 64 columns */
-    auto load_x = [&](uint32_t g, uint32_t col) {
-        const uint32_t b = ops + (g & 1u) * kMmaBufBytes, bar = xfull + 8 * (g & 1u);
+    /* x of a chunk (its columns from col on) into buffer s: 4 boxes of 32 rows x 64 columns */
+    auto load_x = [&](uint32_t s, uint32_t col) {
+        const uint32_t b = ops + s * kMmaBufBytes, bar = xfull + 8 * s;
         mbar_arrive_tx(bar, 4u * 32u * 128u);
 #pragma unroll
         for (int at = 0; at < 4; ++at) tma_load_2d(b + at * kMmaAtomBytes, &a.xmap, (int32_t)(col + 64 * at), 0, bar);
@@ -915,7 +930,7 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
         /* one lane issues every MMA and a commit covers all of that lane's earlier ones, so
          * the last chunk's suffices; no later chunk on its barrier can have completed yet
          * (the next one on it needs this warp's stores, or, for the producer, its issue) */
-        wait(done + 8 * (f.last & 1u), (f.last >> 1) & 1u);
+        wait(done + 8 * f.s, f.ph);
         tc_fence_after();
         float s[4] = {0.f, 0.f, 0.f, 0.f};
         const uint32_t t0 = tmem + ((uint32_t)(32 * q) << 16) + f.dcol + 4u * j;
@@ -951,6 +966,16 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
     uint32_t cb = bufs;
     MmaDone prev{};
     bool have_prev = false;
+    /* chunk gc sits in buffer bs = gc % nbuf; bp = (gc / nbuf) & 1 is the parity of that use
+     * of the buffer's mbarriers (the previous use of the buffer had bp ^ 1) */
+    uint32_t bs = 0, bp = 0;
+    auto advance = [&]() {
+        ++gc;
+        if (++bs == (uint32_t)nbuf) {
+            bs = 0;
+            bp ^= 1u;
+        }
+    };
     if (d < 0 && lane == 0) load_x(0, (uint32_t)(ci.tc * 32 * a.m[ci.mi].steps));
     for (uint32_t iter = 0; it < n_items; it += gridDim.x, ++iter) {
         const HuffMat& M = a.m[ci.mi];
@@ -960,34 +985,35 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
         const int64_t nit = it + gridDim.x;
         if (d < 0) {
             /* ---- producer: x one chunk ahead, then the chunk's 16 MMAs ---- */
-            for (int ch = 0; ch < nch; ++ch, ++gc) {
-                const uint32_t sel = gc & 1u, opb = ops + sel * kMmaBufBytes;
-                if (lane == 0) {
-                    /* x of the next chunk, once the MMAs of chunk gc - 1 (its buffer) are done */
-                    const bool more = ch + 1 < nch || nit < n_items;
-                    if (more) {
-                        if (gc >= 1) wait(done + 8 * (sel ^ 1u), ((gc - 1) >> 1) & 1u);
-                        uint32_t ncol = col_t + (uint32_t)(ch + 1) * kMmaChunk;
-                        if (ch + 1 == nch) {
-                            const MmaItem ni = mma_item(a, nit, rows, d);
-                            ncol = (uint32_t)ni.tc * 32u * (uint32_t)a.m[ni.mi].steps;
-                        }
-                        load_x(gc + 1, ncol);
+            for (int ch = 0; ch < nch; ++ch, advance()) {
+                const uint32_t opb = ops + bs * kMmaBufBytes;
+                /* the whole warp runs this loop (its values stay warp-uniform); one lane
+                 * starts the copies, one elected lane issues each MMA */
+                const bool more = ch + 1 < nch || nit < n_items;
+                if (more) { /* x of the next chunk, once the MMAs of the buffer's previous chunk are done */
+                    const uint32_t ns = bs + 1 == (uint32_t)nbuf ? 0u : bs + 1, np = bs + 1 == (uint32_t)nbuf ? bp ^ 1u : bp;
+                    if (gc + 1 >= (uint32_t)nbuf) wait(done + 8 * ns, np ^ 1u);
+                    uint32_t ncol = col_t + (uint32_t)(ch + 1) * kMmaChunk;
+                    if (ch + 1 == nch) {
+                        const MmaItem ni = mma_item(a, nit, rows, d);
+                        ncol = (uint32_t)ni.tc * 32u * (uint32_t)a.m[ni.mi].steps;
                     }
-                    wait(full + 8 * sel, (gc >> 1) & 1u);
-                    wait(xfull + 8 * sel, (gc >> 1) & 1u);
-                    tc_fence_after();
-                    /* accumulator tile 4 (chunk & 1) + (k step & 3): four independent chains per
-                     * chunk, consecutive chunks on different tiles */
-                    const uint32_t dt = tmem + dcol + 128u * (uint32_t)(ch & 1);
-                    const uint64_t ad = sw128_desc(opb), bd = sw128_desc(opb + 4096u);
-#pragma unroll
-                    for (int ks = 0; ks < kMmaChunk / 16; ++ks) {
-                        const uint64_t off = (uint64_t)(((ks >> 2) * kMmaAtomBytes + (ks & 3) * 32) >> 4);
-                        tc_mma_bf16(dt + 32u * (ks & 3), ad + off, bd + off, a.idesc, ch > 1 || ks > 3);
-                    }
-                    tc_commit(done + 8 * sel);
+                    if (lane == 0) load_x(ns, ncol);
+                    __syncwarp();
                 }
+                wait(full + 8 * bs, bp);
+                wait(xfull + 8 * bs, bp);
+                tc_fence_after();
+                /* accumulator tile 4 (chunk & 1) + (k step & 3): four independent chains per
+                 * chunk, consecutive chunks on different tiles */
+                const uint32_t dt = tmem + dcol + 128u * (uint32_t)(ch & 1);
+                const uint64_t ad = sw128_desc(opb), bd = sw128_desc(opb + 4096u);
+#pragma unroll
+                for (int ks = 0; ks < kMmaChunk / 16; ++ks) {
+                    const uint64_t off = (uint64_t)(((ks >> 2) * kMmaAtomBytes + (ks & 3) * 32) >> 4);
+                    tc_mma_bf16(dt + 32u * (ks & 3), ad + off, bd + off, a.idesc, ch > 1 || ks > 3);
+                }
+                tc_commit(done + 8 * bs);
                 __syncwarp();
                 if (ch == 0 && have_prev) readout(prev); /* the previous item, one chunk late */
             }
@@ -1019,20 +1045,19 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
             const uint32_t seg = (uint32_t)(lane >> 3) * kMmaAtomBytes + ((uint32_t)((lane & 7) ^ (d & 7)) << 4) +
                                  4096u + (uint32_t)d * 128u;
             auto chunk = [&](int ch, uint32_t r0, uint32_t r1) {
-                const uint32_t sel = gc & 1u;
                 uint32_t w[4] = {0u, 0u, 0u, 0u};
                 if (dec) {
                     s.p = min(s.p, pmax);
                     decode8<kLong>(s, c, a, r0, r1, w);
                 }
-                /* the buffer is free once the MMAs of chunk gc - 2 are done */
-                if (gc >= 2) wait(done + 8 * sel, ((gc >> 1) + 1u) & 1u);
-                sts128(ops + sel * kMmaBufBytes + seg, w[0], w[1], w[2], w[3]);
+                /* the buffer is free once the MMAs of its previous chunk (gc - nbuf) are done */
+                if (gc >= (uint32_t)nbuf) wait(done + 8 * bs, bp ^ 1u);
+                sts128(ops + bs * kMmaBufBytes + seg, w[0], w[1], w[2], w[3]);
                 fence_async_smem(); /* the tensor cores read what the generic stores wrote */
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(full + 8 * sel);
-                ++gc;
+                if (lane == 0) mbar_arrive(full + 8 * bs);
+                advance();
             };
             const int nb = nch / 2; /* raw blocks of 16 symbols; block b + 2 is loaded once block b is decoded */
             for (int b0 = 0; b0 < nb; b0 += 2) {
@@ -1056,7 +1081,8 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
         prev.mi = ci.mi;
         prev.row0 = ci.row0;
         prev.dcol = dcol;
-        prev.last = gc - 1;
+        prev.s = bs == 0 ? (uint32_t)nbuf - 1 : bs - 1; /* the item's last chunk, gc - 1 */
+        prev.ph = bs == 0 ? bp ^ 1u : bp;
         have_prev = true;
         if (nit < n_items) {
             ci = mma_item(a, nit, rows, d);
@@ -1077,14 +1103,14 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
  * matrix segment at a time, with that matrix's pair table in shared memory.
  * Every 8 symbols of a lane are 8 consecutive columns, so each lane stores them
  * with one 16-byte write and a warp writes 512 contiguous bytes. */
-__host__ __device__ constexpr size_t decode_warp_bytes(int code_bytes) { return huff_warp_bytes(code_bytes); }
+
 
 template <bool kLong>
 __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_decode_kernel(const __grid_constant__ HuffDecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
     uint4* tab = (uint4*)smem;
-    uint8_t* wbase = smem + kPairTabBytes + (size_t)warp * decode_warp_bytes(a.code_bytes);
+    uint8_t* wbase = smem + kPairTabBytes + (size_t)warp * huff_warp_bytes(a.code_bytes);
     const uint32_t bufs = smem_u32(wbase), buf_bytes = (uint32_t)tile_buf_bytes(a.code_bytes);
     const uint32_t tab_s = smem_u32(tab);
     const uint32_t mbars = bufs + 2 * buf_bytes;
@@ -1754,11 +1780,17 @@ int huff_mma(const ec_matrix* const* Ws, int count, const uint16_t* x, float* co
     a.total_tiles = total;
     /* warps: a multiple of 8, at most 32, as many as fit; one produces, the others
      * decode one row each (rows per item = warps - 1, N = warps) */
-    const size_t fixed = kMmaFixedBytes + (size_t)count * kPairTabBytes, per_warp = huff_warp_bytes(code_bytes);
-    int nw = 0;
-    for (int w = kMaxHW; w >= 8 && !nw; w -= 8)
-        if (fixed + (size_t)(w - 1) * per_warp <= d->smem_optin) nw = w;
+    const size_t per_warp = huff_warp_bytes(code_bytes);
+    int nw = 0, nbuf = 0;
+    for (int nb = kMmaMaxBufs; nb >= 2 && !nw; --nb) /* 32 warps first, then 3 chunk buffers */
+        for (int w = kMaxHW; w >= (nb == 2 ? 8 : kMaxHW) && !nw; w -= 8)
+            if (mma_fixed_bytes(nb) + (size_t)count * kPairTabBytes + (size_t)(w - 1) * per_warp <= d->smem_optin) {
+                nw = w;
+                nbuf = nb;
+            }
     if (!nw) return EC_ERR_UNSUPPORTED;
+    a.nbuf = nbuf;
+    const size_t fixed = mma_fixed_bytes(nbuf) + (size_t)count * kPairTabBytes;
     const int rows = nw - 1;
     const size_t smem = fixed + (size_t)rows * per_warp;
     a.item_begin[0] = 0;
@@ -1979,7 +2011,7 @@ extern "C" int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs
     a.total_tiles = total;
     a.status = d->status;
     a.code_bytes = code_bytes;
-    const size_t per_warp = decode_warp_bytes(code_bytes);
+    const size_t per_warp = huff_warp_bytes(code_bytes);
     if (kPairTabBytes + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED;
     const int warps = (int)std::min<size_t>(kMaxHW, (d->smem_optin - kPairTabBytes) / per_warp);
     const size_t smem = kPairTabBytes + (size_t)warps * per_warp;

@@ -83,16 +83,25 @@ def test_argument_validation(ec):
 
 
 # --------------------------------------------------------------- blob reader
-HDR = struct.Struct("<IIii" + "q" * 10 + "iiiii")
+HDR = struct.Struct("<IIii" + "q" * 10 + "i" * 6)
+
+
+HDR_KEYS = ["magic", "version", "kind", "steps", "n_rows", "k_cols", "k_pad", "n_tiles", "table_off",
+            "table_words", "scales_off", "tile_off_off", "records_off", "blob_bytes", "max_code_bytes",
+            "prob_bits", "max_words", "max_len", "rans_tuple", "window_code_bytes"]
+
+
+def hdr_offset(key: str) -> int:
+    """Byte offset of a header field."""
+    i = HDR_KEYS.index(key)
+    return 16 + 8 * 10 + 4 * (i - 14) if i >= 14 else (4 * i if i < 4 else 16 + 8 * (i - 4))
 
 
 def parse(blob: bytes):
     meta_size = 8 + 8 + 8 + 256 * 8 + 256 + 256 * 4 + 4 * 8 + 8
     dev = blob[meta_size:]
     f = HDR.unpack_from(dev, 0)
-    keys = ["magic", "version", "kind", "steps", "n_rows", "k_cols", "k_pad", "n_tiles", "table_off",
-            "table_words", "scales_off", "tile_off_off", "records_off", "blob_bytes", "max_code_bytes",
-            "prob_bits", "max_words", "max_len", "rans_tuple"]
+    keys = HDR_KEYS
     h = dict(zip(keys, f))
     return h, dev
 
@@ -349,14 +358,16 @@ def corruptions(blob: bytes):
         yield "lane start", bytes(x)
         x = bytearray(b); struct.pack_into("<I", x, meta + h["table_off"], 0x80000000 | 0x7FFF)
         yield "table pointer", bytes(x)
+        x = bytearray(b); struct.pack_into("<i", x, meta + hdr_offset("window_code_bytes"), -1)
+        yield "window size", bytes(x)
     else:
         x = bytearray(b); struct.pack_into("<I", x, meta + h["table_off"], 0 if h["rans_tuple"] == 1 else 0xFFF00)
         yield "slot entry", bytes(x)
-        tup = meta + HDR.size - 4
+        tup = meta + hdr_offset("rans_tuple")
         x = bytearray(b); struct.pack_into("<i", x, tup, 3)
         yield "codes per symbol", bytes(x)
         if h["rans_tuple"] == 2:
-            pb = meta + HDR.size - 4 * 4  # prob_bits, then max_words, max_len, rans_tuple
+            pb = meta + hdr_offset("prob_bits")
             x = bytearray(b); struct.pack_into("<i", x, pb, 13)
             yield "pair precision", bytes(x)
 
@@ -375,6 +386,26 @@ def test_deserialize_rejects_structural_corruption(ec, kind):
         with pytest.raises(ec.EcError) as e:
             ec.deserialize(bad, device=-1)
         assert e.value.code == -5, name
+
+
+@pytest.mark.parametrize("shape,steps", [((300, 4096), 128), ((70, 14336), 0), ((40, 1000), 64), ((5, 300), 16)])
+def test_huffman_window_size_matches_tiles(ec, shape, steps):
+    """The header's largest 31-row window of one tile column (64 bytes of lane
+    starts plus the code area per tile), recomputed from the tile offsets."""
+    W = ec.encode_bf16(synth.llama_bf16(3300 + shape[0], *shape), tile_steps=steps, device=-1)
+    h, dev = parse(W.serialize())
+    toff = np.frombuffer(dev, np.uint32, h["n_tiles"] + 1, h["tile_off_off"]).astype(np.int64) * 16
+    code = np.diff(toff) - 64 - 32 * ((h["steps"] + 15) // 16 * 16)
+    assert code.max() == h["max_code_bytes"]
+    T = 32 * h["steps"]
+    if h["k_pad"] % T:
+        assert h["window_code_bytes"] == 0
+    else:
+        R = h["k_pad"] // T
+        per = (64 + code).reshape(h["n_rows"], R)
+        c = np.vstack([np.zeros((1, R), np.int64), np.cumsum(per, axis=0)])
+        wmax = max(int((c[min(r + 31, h["n_rows"])] - c[r]).max()) for r in range(h["n_rows"]))
+        assert h["window_code_bytes"] == wmax
 
 
 def test_tile_width_aux_bounds(ec):
