@@ -102,6 +102,7 @@ struct HuffMmaArgs {
     int32_t row_tiles[EC_MAX_GROUP];    /* tiles per row */
     uint32_t idesc;                     /* tcgen05 instruction descriptor (M = 64, N = warps) */
     int nbuf;                           /* chunk buffers (2 or 3) */
+    int pool_bytes;                     /* one item's packed code areas, with slack */
 };
 
 struct RansMat {
@@ -750,7 +751,7 @@ constexpr uint32_t kMmaBufBytes = 32768u;       /* one chunk: 4 swizzle atoms of
 constexpr uint32_t kMmaAtomBytes = 8192u;       /* 64 rows x 128 B: x rows 0..31, then weight rows 0..31 */
 constexpr int kMmaMaxBatch = 32;                /* x rows per pass */
 constexpr int kMmaMaxBufs = 3;                 /* chunk buffers in flight: 3 where shared memory allows, else 2 */
-__host__ __device__ constexpr size_t mma_fixed_bytes(int nbuf) { return 1024 + (size_t)nbuf * kMmaBufBytes + 128; } /* alignment, buffers, barriers */
+__host__ __device__ constexpr size_t mma_fixed_bytes(int nbuf) { return (size_t)nbuf * kMmaBufBytes + 96; } /* buffers, barriers */
 
 __device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
@@ -856,26 +857,57 @@ struct MmaDone {
 
 template <bool kLong>
 __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_constant__ HuffMmaArgs a) {
-    extern __shared__ __align__(16) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t mma_smem[]; /* (the dynamic block, 1 KB aligned) */
+    uint8_t* const smem = mma_smem;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
     const int rows = nwarp - 1, d = warp - 1; /* warp 0 produces; warps 1.. decode rows 0.. of the item */
-    /* shared: [align to 1 KB] | 2 chunk buffers | pair tables | per decoding warp: two
-     * tile buffers and their mbarriers | full[2], done[2], xfull[2] | TMEM address */
-    const uint32_t ops = (smem_u32(smem) + 1023u) & ~1023u;
+    if (smem_u32(smem) & 1023u) { /* the swizzled operands need 1 KB alignment (never seen otherwise) */
+        if (threadIdx.x == 0) flag_corrupt(a.status);
+        return;
+    }
+    /* shared: nbuf chunk buffers | pair tables | two code pools (items alternate) | the
+     * pools' mbarriers | full, done, xfull [nbuf each] | TMEM address.  A lane's reads
+     * run up to kSlackBytes past its tile's code area: into the next tile, the other
+     * pool or the mbarriers, all inside the block. */
+    const uint32_t ops = smem_u32(smem);
     const int nbuf = a.nbuf;
     const uint32_t tabs_s = ops + (uint32_t)nbuf * kMmaBufBytes;
-    const uint32_t warp_area = tabs_s + (uint32_t)a.count * kPairTabBytes;
-    const uint32_t wb = (uint32_t)huff_warp_bytes(a.code_bytes);
-    const uint32_t bufs = warp_area + (uint32_t)(d < 0 ? 0 : d) * wb, buf_bytes = (uint32_t)tile_buf_bytes(a.code_bytes);
-    const uint32_t mbars = bufs + 2 * buf_bytes;
-    const uint32_t full = warp_area + (uint32_t)rows * wb, done = full + 24, xfull = full + 48, tslot = full + 72;
+    const uint32_t pools = tabs_s + (uint32_t)a.count * kPairTabBytes;
+    const uint32_t mbars = pools + 2u * (uint32_t)a.pool_bytes; /* pool p complete: all decoding warps' copies */
+    const uint32_t full = mbars + 16, done = full + 24, xfull = full + 48, tslot = full + 72;
     const int64_t n_items = a.item_begin[a.count];
 
+    /* A decoding warp's tile of an item goes into pool p, packed after the tiles of
+     * the item's earlier rows (64 bytes of lane starts + the code area each, sizes
+     * from the tile offsets, a prefix sum over the lanes); `region` receives its
+     * place.  A tile that does not fit (corrupt offsets only) comes back with area 0. */
+    auto stage = [&](const MmaItem& itm, uint32_t p, uint32_t& region) -> TileRef {
+        const HuffMat& M = a.m[itm.mi];
+        const int64_t row = itm.row0 + lane;
+        uint32_t sz = 0;
+        if (lane < rows && row < M.n_rows) {
+            const int64_t g = M.tile_begin + row * a.row_tiles[itm.mi] + itm.tc;
+            const TileRef r = tile_ref(a, g, tile_offsets(a, g));
+            sz = r.area > 0 ? 64u + (uint32_t)r.area : 0u;
+        }
+        uint32_t inc = sz;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(kFull, inc, o);
+            if (lane >= o) inc += v;
+        }
+        const uint32_t off = __shfl_sync(kFull, inc - sz, d);
+        TileRef r = mma_tile(a, itm);
+        if (r.area > 0 && off + 64u + (uint32_t)r.area > (uint32_t)a.pool_bytes) r.area = 0;
+        region = pools + p * (uint32_t)a.pool_bytes + off;
+        prefetch_code(region, mbars + 8 * p, r, lane);
+        return r;
+    };
+
     if (lane == 0) {
-        if (d >= 0) {
-            mbar_init(mbars);
-            mbar_init(mbars + 8);
-        } else {
+        if (d < 0) {
+            mbar_init_n(mbars, (uint32_t)rows);
+            mbar_init_n(mbars + 8, (uint32_t)rows);
             for (int i = 0; i < nbuf; ++i) {
                 mbar_init_n(full + 8 * i, (uint32_t)rows);
                 mbar_init(done + 8 * i);
@@ -884,11 +916,13 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
         }
         mbar_fence_init();
     }
-    __syncwarp();
+    __syncthreads(); /* the pools' mbarriers (set up by warp 0) before any copy arrives on them */
     int64_t it = blockIdx.x;
     MmaItem ci = mma_item(a, it, rows, d);
-    TileRef cur = mma_tile(a, ci);
-    if (d >= 0) prefetch_code(bufs, mbars, cur, lane);
+    TileRef cur{};
+    uint32_t region = 0; /* this warp's tile in the current pool */
+    bool fits = true;    /* the next item's tile found room */
+    if (d >= 0) cur = stage(ci, 0, region);
     for (int k = 0; k < a.count; ++k) {
         const uint4* src = (const uint4*)a.m[k].table;
         uint4* dst = (uint4*)(smem + (tabs_s - smem_u32(smem)) + (size_t)k * kPairTabBytes);
@@ -961,9 +995,7 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
         }
     };
 
-    uint32_t ph = 0;  /* parity of the next phase of each tile buffer's mbarrier */
     uint32_t gc = 0;  /* chunks of this CTA so far */
-    uint32_t cb = bufs;
     MmaDone prev{};
     bool have_prev = false;
     /* chunk gc sits in buffer bs = gc % nbuf; bp = (gc / nbuf) & 1 is the parity of that use
@@ -976,7 +1008,10 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
             bp ^= 1u;
         }
     };
-    if (d < 0 && lane == 0) load_x(0, (uint32_t)(ci.tc * 32 * a.m[ci.mi].steps));
+    if (d < 0 && lane == 0) { /* x of the first nbuf - 1 chunks (an item has at least 2) */
+        const uint32_t col0 = (uint32_t)(ci.tc * 32 * a.m[ci.mi].steps);
+        for (int j = 0; j + 1 < nbuf; ++j) load_x((uint32_t)j, col0 + (uint32_t)j * kMmaChunk);
+    }
     for (uint32_t iter = 0; it < n_items; it += gridDim.x, ++iter) {
         const HuffMat& M = a.m[ci.mi];
         const int nch = M.steps / 8;
@@ -989,18 +1024,6 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
                 const uint32_t opb = ops + bs * kMmaBufBytes;
                 /* the whole warp runs this loop (its values stay warp-uniform); one lane
                  * starts the copies, one elected lane issues each MMA */
-                const bool more = ch + 1 < nch || nit < n_items;
-                if (more) { /* x of the next chunk, once the MMAs of the buffer's previous chunk are done */
-                    const uint32_t ns = bs + 1 == (uint32_t)nbuf ? 0u : bs + 1, np = bs + 1 == (uint32_t)nbuf ? bp ^ 1u : bp;
-                    if (gc + 1 >= (uint32_t)nbuf) wait(done + 8 * ns, np ^ 1u);
-                    uint32_t ncol = col_t + (uint32_t)(ch + 1) * kMmaChunk;
-                    if (ch + 1 == nch) {
-                        const MmaItem ni = mma_item(a, nit, rows, d);
-                        ncol = (uint32_t)ni.tc * 32u * (uint32_t)a.m[ni.mi].steps;
-                    }
-                    if (lane == 0) load_x(ns, ncol);
-                    __syncwarp();
-                }
                 wait(full + 8 * bs, bp);
                 wait(xfull + 8 * bs, bp);
                 tc_fence_after();
@@ -1014,19 +1037,37 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
                     tc_mma_bf16(dt + 32u * (ks & 3), ad + off, bd + off, a.idesc, ch > 1 || ks > 3);
                 }
                 tc_commit(done + 8 * bs);
+                /* x of chunk gc + nbuf - 1, into the buffer of chunk gc - 1 once its MMAs are done */
+                const int ahead = ch + nbuf - 1; /* in this item's numbering; the next item follows */
+                if (ahead < nch || nit < n_items) {
+                    uint32_t xcol;
+                    if (ahead < nch) {
+                        xcol = col_t + (uint32_t)ahead * kMmaChunk;
+                    } else {
+                        const MmaItem ni = mma_item(a, nit, rows, d);
+                        xcol = (uint32_t)ni.tc * 32u * (uint32_t)a.m[ni.mi].steps + (uint32_t)(ahead - nch) * kMmaChunk;
+                    }
+                    const uint32_t ps = bs == 0 ? (uint32_t)nbuf - 1 : bs - 1, pp = bs == 0 ? bp ^ 1u : bp;
+                    if (gc >= 1) wait(done + 8 * ps, pp);
+                    if (lane == 0) load_x(ps, xcol);
+                }
                 __syncwarp();
                 if (ch == 0 && have_prev) readout(prev); /* the previous item, one chunk late */
             }
         } else {
             /* ---- decoders: 8 symbols of the warp's row per chunk ---- */
-            const uint32_t bi = cb == bufs ? 0u : 1u;
-            const bool arrived = wait(mbars + 8 * bi, (ph >> bi) & 1u); /* this item's tile */
-            ph ^= 1u << bi;
+            const uint32_t pi = iter & 1u;
+            const bool arrived = wait(mbars + 8 * pi, (iter >> 1) & 1u); /* this item's tile */
             __syncwarp();
             if (!arrived) cur.area = 0;
-            const uint32_t nb_buf = cb == bufs ? bufs + buf_bytes : bufs;
-            if (nit < n_items) /* (the next item's descriptors are resolved again at the end) */
-                prefetch_code(nb_buf, mbars + 8 * (bi ^ 1u), mma_tile(a, mma_item(a, nit, rows, d)), lane);
+            const uint32_t cb = region;
+            if (nit < n_items) {
+                /* the other pool held the previous item: every decoding warp is done with it
+                 * once all have stored that item's last chunk.  (The next item's tile is
+                 * resolved again at the end; only whether it fit is kept.) */
+                if (have_prev) wait(full + 8 * prev.s, prev.ph);
+                fits = stage(mma_item(a, nit, rows, d), pi ^ 1u, region).area > 0 || !mma_item(a, nit, rows, d).have;
+            }
             if (ci.have && cur.area == 0 && lane == 0) flag_corrupt(a.status);
             const bool dec = ci.have && cur.area > 0;
             const PairCtx c{tabs_s + (uint32_t)ci.mi * kPairTabBytes, cb + 64, ci.mi};
@@ -1076,7 +1117,6 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
             const uint32_t p = s.p;
             const bool bad = dec && (lane < 31 ? (p > 8u * s1 || p + 8u <= 8u * s1) : (p + 64u > pmax));
             if (__any_sync(kFull, bad) && lane == 0) flag_corrupt(a.status);
-            cb = nb_buf;
         }
         prev.mi = ci.mi;
         prev.row0 = ci.row0;
@@ -1087,6 +1127,7 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
         if (nit < n_items) {
             ci = mma_item(a, nit, rows, d);
             cur = mma_tile(a, ci);
+            if (!fits) cur.area = 0;
         }
     }
     if (have_prev) readout(prev);
@@ -1546,7 +1587,7 @@ bool use_pdl() {
 int mma_min_batch() {
     static const int v = [] {
         const char* e = std::getenv("EC_MMA_MIN_BATCH");
-        return e && e[0] ? std::max(1, std::atoi(e)) : 4;
+        return e && e[0] ? std::max(1, std::atoi(e)) : 6;
     }();
     return v;
 }
@@ -1723,7 +1764,8 @@ int plan_huff_gemv(const DeviceInfo& d, int count, int code_bytes, int64_t kp, i
 /* Tensor-core path: every matrix's tiles must lie inside one row. */
 bool mma_layout(const ec_matrix* W) {
     const ec_blob_header& h = W->hdr;
-    return h.n_tiles > 0 && h.steps % 16 == 0 && h.k_pad % (32 * (int64_t)h.steps) == 0 && h.k_pad < (int64_t(1) << 31);
+    return h.n_tiles > 0 && h.steps % 16 == 0 && h.k_pad % (32 * (int64_t)h.steps) == 0 && h.k_pad < (int64_t(1) << 31) &&
+           h.window_code_bytes > 0;
 }
 
 /* cuTensorMapEncodeTiled, reached through the runtime (no link against the driver library). */
@@ -1778,21 +1820,24 @@ int huff_mma(const ec_matrix* const* Ws, int count, const uint16_t* x, float* co
     code_bytes = (code_bytes + 15) & ~15;
     a.code_bytes = code_bytes;
     a.total_tiles = total;
-    /* warps: a multiple of 8, at most 32, as many as fit; one produces, the others
-     * decode one row each (rows per item = warps - 1, N = warps) */
-    const size_t per_warp = huff_warp_bytes(code_bytes);
+    /* one item's tiles, packed: the largest window of EC_MMA_WINDOW_ROWS rows, plus slack */
+    int64_t window = 0;
+    for (int k = 0; k < count; ++k) window = std::max<int64_t>(window, Ws[k]->hdr.window_code_bytes);
+    a.pool_bytes = (int)((window + 15) & ~int64_t(15));
+    /* warps: a multiple of 8, at most 32 (one produces, the others decode one row each:
+     * rows per item = warps - 1 <= EC_MMA_WINDOW_ROWS, N = warps); 3 chunk buffers where they fit */
+    const size_t fixed_rest = (size_t)count * kPairTabBytes + 2 * (size_t)a.pool_bytes;
     int nw = 0, nbuf = 0;
-    for (int nb = kMmaMaxBufs; nb >= 2 && !nw; --nb) /* 32 warps first, then 3 chunk buffers */
+    for (int nb = kMmaMaxBufs; nb >= 2 && !nw; --nb)
         for (int w = kMaxHW; w >= (nb == 2 ? 8 : kMaxHW) && !nw; w -= 8)
-            if (mma_fixed_bytes(nb) + (size_t)count * kPairTabBytes + (size_t)(w - 1) * per_warp <= d->smem_optin) {
+            if (mma_fixed_bytes(nb) + fixed_rest <= d->smem_optin) {
                 nw = w;
                 nbuf = nb;
             }
     if (!nw) return EC_ERR_UNSUPPORTED;
     a.nbuf = nbuf;
-    const size_t fixed = mma_fixed_bytes(nbuf) + (size_t)count * kPairTabBytes;
     const int rows = nw - 1;
-    const size_t smem = fixed + (size_t)rows * per_warp;
+    const size_t smem = mma_fixed_bytes(nbuf) + fixed_rest;
     a.item_begin[0] = 0;
     for (int k = 0; k < count; ++k)
         a.item_begin[k + 1] = a.item_begin[k] + (Ws[k]->hdr.n_rows + rows - 1) / rows * a.row_tiles[k];
