@@ -430,9 +430,10 @@ def extras(torch, ec, stream, device):
 
 
 def batch_sweep(torch, ec, stack, stream, device):
-    """Fused GEMV over the 8B layer set at batch 1, 2, 4, 8 and 16 (layers 0 and 1
-    of the stack alternately, 600 MB, so repeated replays do not run from L2), and
-    the same layer set coded with the 24-bit length limit at batch 1."""
+    """Fused GEMV over the 8B layer set at batch 1 .. 64 (layers 0 and 1 of the stack
+    alternately, 600 MB, so repeated replays do not run from L2), with the kernel
+    family the library picks at each batch (CUDA cores, or from batch 6 the tensor
+    cores), and the same layer set coded with the 24-bit length limit at batch 1."""
     import synth
     dev = f"cuda:{device}"
     n_l = min(2, stack.n_layers)
@@ -442,8 +443,9 @@ def batch_sweep(torch, ec, stack, stream, device):
         g = capture(torch, fn, stream)
         return time_graph(torch, g, stream, iters, warm)
 
-    sweep = {}
-    for b in (1, 2, 4, 8, 16):
+    sweep, paths = {}, {}
+    for b in (1, 2, 4, 8, 16, 32, 64):
+        paths[str(b)] = ec.gemv_path([stack.mats[0][n] for n in Stack.GROUPS[0][1]], b)
         bufs = []
         for l in range(n_l):
             for gname, names in Stack.GROUPS:
@@ -458,6 +460,7 @@ def batch_sweep(torch, ec, stack, stream, device):
                 ec.gemv_group(Ws, x, ys, batch=b)
         sweep[str(b)] = round(t_graph(run) / n_l, 1)
     out["batch_sweep_us_per_layer_set"] = sweep
+    out["batch_sweep_kernels"] = paths
 
     # materialisation for larger batches: decode each layer's matrices to BF16
     # (one ec_decode_batch launch per layer) and multiply with cuBLAS, against

@@ -145,8 +145,20 @@ int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs, int count
 
 /* y[b, i] = sum_j W[i, j] * x[b, j] for b < batch (1..EC_MAX_BATCH), with the weights
  * decoded in registers / shared memory and FP32 accumulation.  x: BF16 [batch,
- * k_cols] device; y: FP32 [batch, n_rows] device, overwritten. */
+ * k_cols] device; y: FP32 [batch, n_rows] device, overwritten.
+ * Huffman matrices run on the CUDA cores (one FMA per weight and batch row, in
+ * passes of up to 16 rows), or, from batch 6 (EC_MMA_MIN_BATCH overrides) when
+ * every tile lies inside a row (the automatic tile size ensures it) and k_cols % 8
+ * == 0, on the tensor cores (tcgen05, BF16 products, FP32 accumulators; passes of
+ * up to 32 rows).  ec_gemv_path tells which. */
 int ec_gemv(const ec_matrix* W, const uint16_t* x_bf16, float* y, int batch, cudaStream_t stream);
+
+enum { EC_PATH_CUDA_CORES = 1, EC_PATH_TENSOR_CORES = 2 };
+
+/* The kernel family ec_gemv_group(Ws, count, ..., batch, ...) would use (host only;
+ * no device access): EC_PATH_*, or a negative EC_ERR_* for arguments it rejects
+ * before launching (null or mixed matrices, batch out of range). */
+int ec_gemv_path(const ec_matrix* const* Ws, int count, int batch);
 
 /* Several GEMVs over the same input x in one launch (MINE section 4.2 "Launch":
  * q/k/v, gate/up).  All matrices must have the same kind and k_cols; count <=

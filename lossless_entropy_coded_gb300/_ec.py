@@ -36,7 +36,7 @@ EC_KIND_RANS_INT4 = 2
 
 EXPORTS = ["ec_encode_bf16", "ec_encode_rans", "ec_decode", "ec_decode_batch", "ec_gemv", "ec_gemv_group",
            "ec_bf16_gemv", "ec_stats", "ec_code_lengths", "ec_serialize", "ec_deserialize", "ec_status", "ec_free",
-           "ec_strerror", "ec_gemv_static"]
+           "ec_strerror", "ec_gemv_static", "ec_gemv_path"]
 
 
 class HuffParams(ctypes.Structure):
@@ -70,6 +70,7 @@ _sig = {
     "ec_gemv_group": ([_vp, _i32, _vp, _vp, _i32, _vp], _i32),
     "ec_bf16_gemv": ([_vp, _i64, _i64, _vp, _vp, _i32, _vp], _i32),
     "ec_gemv_static": ([_vp, _vp, _vp, _i32, _vp], _i32),
+    "ec_gemv_path": ([_vp, _i32, _i32], _i32),
     "ec_stats": ([_vp, ctypes.POINTER(Stats)], _i32),
     "ec_code_lengths": ([_vp, _vp], _i32),
     "ec_serialize": ([_vp, _vp, _i64, ctypes.POINTER(_i64)], _i32),
@@ -216,6 +217,19 @@ def gemv_static(W: Matrix, x, y, batch: int = 1, stream=None) -> None:
     """ec_gemv_static: the GEMV with no device or host allocation (fixed built-in
     scratch; serialise calls that could overlap on the GPU)."""
     _check(lib.ec_gemv_static(W.handle, _dev_ptr(x), _dev_ptr(y), batch, _stream_ptr(stream)), "ec_gemv_static")
+
+
+EC_PATH_CUDA_CORES, EC_PATH_TENSOR_CORES = 1, 2
+
+
+def gemv_path(Ws, batch: int = 1) -> str:
+    """Which kernels gemv_group(Ws, ..., batch) uses: "cuda_cores" or "tensor_cores"."""
+    if not isinstance(Ws, (list, tuple)):
+        Ws = [Ws]
+    hs = (ctypes.c_void_p * len(Ws))(*[W.handle.value for W in Ws])
+    rc = lib.ec_gemv_path(hs, len(Ws), batch)
+    _check(rc if rc < 0 else 0, "ec_gemv_path")
+    return "tensor_cores" if rc == EC_PATH_TENSOR_CORES else "cuda_cores"
 
 
 def gemv_group(Ws, x, ys, batch: int = 1, stream=None) -> None:

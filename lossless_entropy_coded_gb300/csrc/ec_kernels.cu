@@ -1,7 +1,7 @@
 /*
  * ec_kernels.cu -- sm_103a kernels and the device-side entry points of the C ABI
- * (ec_decode, ec_decode_batch, ec_gemv, ec_gemv_group, ec_gemv_static,
- * ec_bf16_gemv, ec_status).
+ * (ec_decode, ec_decode_batch, ec_gemv, ec_gemv_group, ec_gemv_path,
+ * ec_gemv_static, ec_bf16_gemv, ec_status).
  *
  * Huffman path (DFloat11, "70% Size, 100% Accuracy", Algorithm 1, re-cut for the
  * fused product of MINE section 4 "Fused mvm"): one warp owns one tile of
@@ -724,7 +724,9 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
  * 128-byte-swizzled K-major operand: chunk l % 8 of the 128-byte row in swizzle
  * atom l / 8, so the 32 stores of a warp hit all banks (4 wavefronts).  x arrives
  * by TMA in the same swizzled layout (boxes of 32 rows x 64 columns; rows past
- * the batch and columns past K read as zero), issued one chunk ahead.
+ * the batch and columns past K read as zero), nbuf - 1 chunks ahead.  An item's
+ * code areas (64 bytes of lane starts + the code area per row) are staged packed
+ * in one of two pools, the next item's while this one is decoded.
  *
  * MMA: M = 64 rows of x (the batch; rows past it are never read back), N = warps
  * weight rows, K = 16, kind::f16 with BF16 inputs; 16 per chunk, issued by one
@@ -1796,6 +1798,14 @@ int encode_x_map(CUtensorMap* map, const uint16_t* x, int64_t K, int rows) {
     return r == CUDA_SUCCESS ? EC_OK : EC_ERR_CUDA;
 }
 
+/* Huffman GEMVs from mma_min_batch() on, on matrices whose tiles lie inside rows and
+ * rows of x that TMA can address (16-byte stride), take the tensor-core kernel. */
+bool use_mma(const ec_matrix* const* Ws, int count, int batch) {
+    bool mma = batch >= mma_min_batch() && Ws[0]->hdr.k_cols % 8 == 0;
+    for (int k = 0; k < count && mma; ++k) mma = mma_layout(Ws[k]);
+    return mma;
+}
+
 int huff_mma(const ec_matrix* const* Ws, int count, const uint16_t* x, float* const* ys, int batch, cudaStream_t s,
              DeviceInfo* d) {
     HuffMmaArgs a{};
@@ -1859,9 +1869,7 @@ int huff_mma(const ec_matrix* const* Ws, int count, const uint16_t* x, float* co
 
 int huff_gemv(const ec_matrix* const* Ws, int count, const uint16_t* x, float* const* ys, int batch,
               cudaStream_t s, int dev, DeviceInfo* d) {
-    bool mma = batch >= mma_min_batch() && Ws[0]->hdr.k_cols % 8 == 0; /* (TMA rows of x: 16-byte stride) */
-    for (int k = 0; k < count && mma; ++k) mma = mma_layout(Ws[k]);
-    if (mma) return huff_mma(Ws, count, x, ys, batch, s, d);
+    if (use_mma(Ws, count, batch)) return huff_mma(Ws, count, x, ys, batch, s, d);
     int64_t total = 0;
     int code_bytes = 16;
     bool lng = false;
@@ -2016,6 +2024,16 @@ extern "C" int ec_gemv_group(const ec_matrix* const* Ws, int count, const uint16
     for (int k = 0; k < count; ++k)
         if ((rc = rans_run(Ws[k], x, ys[k], nullptr, batch, stream, d)) != EC_OK) return rc;
     return EC_OK;
+}
+
+extern "C" int ec_gemv_path(const ec_matrix* const* Ws, int count, int batch) {
+    if (!Ws || count < 1 || count > EC_MAX_GROUP) return EC_ERR_INVALID_ARG;
+    if (batch < 1 || batch > EC_MAX_BATCH) return batch < 1 ? EC_ERR_INVALID_ARG : EC_ERR_UNSUPPORTED;
+    for (int k = 0; k < count; ++k) {
+        if (!Ws[k]) return EC_ERR_INVALID_ARG;
+        if (Ws[k]->kind != Ws[0]->kind || Ws[k]->hdr.k_cols != Ws[0]->hdr.k_cols) return EC_ERR_SHAPE;
+    }
+    return Ws[0]->kind == EC_KIND_HUFFMAN_BF16 && use_mma(Ws, count, batch) ? EC_PATH_TENSOR_CORES : EC_PATH_CUDA_CORES;
 }
 
 extern "C" int ec_gemv(const ec_matrix* W, const uint16_t* x, float* y, int batch, cudaStream_t stream) {

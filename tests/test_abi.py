@@ -408,6 +408,29 @@ def test_huffman_window_size_matches_tiles(ec, shape, steps):
         assert h["window_code_bytes"] == wmax
 
 
+def test_gemv_path_dispatch(ec):
+    """Which kernels a GEMV takes, decided on the host: tensor cores from batch 6 when
+    every tile lies inside a row and k_cols % 8 == 0, else CUDA cores."""
+    from lossless_entropy_coded_gb300 import _ec
+    if os.environ.get("EC_MMA_MIN_BATCH"):
+        pytest.skip("threshold overridden")
+    W = ec.encode_bf16(synth.llama_bf16(3400, 64, 4096), device=-1)
+    assert [ec.gemv_path(W, b) for b in (1, 5, 6, 32, 64)] == ["cuda_cores"] * 2 + ["tensor_cores"] * 3
+    Wodd = ec.encode_bf16(synth.llama_bf16(3401, 8, 13), device=-1)  # rows of x not 16-byte aligned
+    assert ec.gemv_path(Wodd, 16) == "cuda_cores"
+    Wx = ec.encode_bf16(synth.llama_bf16(3402, 8, 14336), tile_steps=128, device=-1)  # tiles cross rows
+    assert ec.gemv_path(Wx, 16) == "cuda_cores"
+    Wy = ec.encode_bf16(synth.llama_bf16(3403, 8, 14336), device=-1)  # automatic tiles: 112 steps, inside rows
+    assert ec.gemv_path(Wy, 16) == "tensor_cores"
+    assert ec.gemv_path([Wy, Wx], 16) == "cuda_cores"  # one matrix without the layout: the whole group
+    R = ec.encode_rans(*synth.make_rans_case(0, 8, 4096), device=-1)
+    assert ec.gemv_path(R, 16) == "cuda_cores"
+    hs = (ctypes.c_void_p * 2)(W.handle.value, R.handle.value)
+    assert ec.lib.ec_gemv_path(hs, 2, 16) == _ec.EC_ERR_SHAPE
+    assert ec.lib.ec_gemv_path(hs, 1, 0) == _ec.EC_ERR_INVALID_ARG
+    assert ec.lib.ec_gemv_path(hs, 1, 65) == _ec.EC_ERR_UNSUPPORTED
+
+
 def test_tile_width_aux_bounds(ec):
     w = synth.llama_bf16(2001, 1024, 4096)
     for steps, lo, hi in ((128, 0.125, 0.25), (64, 0.25, 0.40)):

@@ -38,6 +38,7 @@ def test_mma_gemv_parity(ec, shape, batch):
     W = ec.encode_bf16(w)
     h, _ = parse(W.serialize())
     assert h["k_pad"] % (32 * h["steps"]) == 0  # tiles inside rows: the tensor-core layout
+    assert ec.gemv_path(W, batch) == ("tensor_cores" if shape[1] % 8 == 0 else "cuda_cores")
     x = synth.make_x(2400 + batch, batch, shape[1])
     (y,) = run(ec, [W], x, batch)
     y_ref, a_ref = O.gemv_bf16(w, x)
