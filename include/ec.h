@@ -86,7 +86,11 @@ typedef struct {
 } ec_huff_params;
 
 /* rANS codec parameters (NULL = defaults).
- *  prob_bits         frequency precision b, 9..15 (default 12)
+ *  prob_bits         frequency precision b, 9..15 (default 12), or 0 to choose it per
+ *                    matrix as MINE tunes its table size (section 4.2 "Launch"): b = 9..12
+ *                    in increasing order, scored by the cross-entropy bound of the
+ *                    stored size (payload n * H(P, Q_b) plus 2^b 4-byte table entries)
+ *                    until a score exceeds the best so far by more than 1%; the best wins
  *  tile_syms         codes per independent tile, a multiple of 128 (default 4096)
  *  group             weights per FP16 scale along a row (only 128 is supported)
  *  codes_per_symbol  1 (default; 0 means 1): one 4-bit code per rANS symbol;

@@ -308,6 +308,29 @@ bool rans_normalise(const uint64_t* counts, int nsym, int prob_bits, uint32_t* f
     return true;
 }
 
+/* Table size for prob_bits = 0, MINE section 4.2 ("Launch"): candidate sizes 2^b,
+ * b = 9..12, in increasing order, each scored by the cross-entropy lower bound of
+ * the stored size, n * H(P, Q_b) bits of payload plus the table's 2^b 32-bit
+ * entries; the scan stops once a score exceeds the best so far by more than 1%,
+ * and the best is taken.  Returns 0 when no candidate can hold the alphabet. */
+int rans_table_bits(const uint64_t* counts, int nsym) {
+    int best_b = 0;
+    double best = 0;
+    std::vector<uint32_t> f(nsym);
+    for (int b = 9; b <= 12; ++b) {
+        if (!rans_normalise(counts, nsym, b, f.data())) continue;
+        double bits = 32.0 * (double)(1u << b);
+        for (int s = 0; s < nsym; ++s)
+            if (counts[s]) bits -= (double)counts[s] * std::log2((double)f[s] / (double)(1u << b));
+        if (best_b && bits > 1.01 * best) break;
+        if (!best_b || bits < best) {
+            best = bits;
+            best_b = b;
+        }
+    }
+    return best_b;
+}
+
 double entropy_bits(const uint64_t* c, int n) {
     double tot = 0, h = 0;
     for (int i = 0; i < n; ++i) tot += (double)c[i];
@@ -559,13 +582,14 @@ extern "C" int ec_encode_rans(const int8_t* codes, const uint16_t* scales, int64
     if (!out) return EC_ERR_INVALID_ARG;
     *out = nullptr;
     if (n_rows < 0 || k_cols < 0) return EC_ERR_SHAPE;
-    const int b = params ? params->prob_bits : 12;
+    const int b_req = params ? params->prob_bits : 12; /* 0: chosen from the histogram */
     const int T = params ? params->tile_syms : 4096;
     const int group = params ? params->group : 128;
     const int k = params && params->codes_per_symbol ? params->codes_per_symbol : 1;
-    if (b < 9 || b > 15 || T < 32 || T % EC_RANS_ROW_ALIGN || T > 65536) return EC_ERR_INVALID_ARG;
+    if ((b_req != 0 && (b_req < 9 || b_req > 15)) || T < 32 || T % EC_RANS_ROW_ALIGN || T > 65536)
+        return EC_ERR_INVALID_ARG;
     if (k != 1 && k != 2) return EC_ERR_INVALID_ARG;
-    if (k == 2 && b > 12) return EC_ERR_INVALID_ARG; /* pair entries hold freq - 1 and the slot bias in 12 bits */
+    if (k == 2 && b_req > 12) return EC_ERR_INVALID_ARG; /* pair entries hold freq - 1 and the slot bias in 12 bits */
     if (group != 128) return EC_ERR_UNSUPPORTED;
     if (k_cols > INT64_MAX - EC_RANS_ROW_ALIGN) return EC_ERR_OVERFLOW;
     const int64_t KP = round_up(k_cols, EC_RANS_ROW_ALIGN), G = KP / 128;
@@ -609,7 +633,8 @@ extern "C" int ec_encode_rans(const int8_t* codes, const uint16_t* scales, int64
             for (auto& a : part)
                 for (int s = 0; s < 256; ++s) m->counts[s] += a[s];
         }
-        if (!rans_normalise(m->counts, nsym, b, m->freqs)) {
+        const int b = b_req ? b_req : rans_table_bits(m->counts, nsym);
+        if (!b || !rans_normalise(m->counts, nsym, b, m->freqs)) {
             delete m;
             return EC_ERR_INVALID_ARG;
         }

@@ -272,6 +272,28 @@ def rans_freqs(counts, prob_bits: int = 12) -> np.ndarray:
     return out
 
 
+def rans_table_bits(counts, candidates=(9, 10, 11, 12), table_entry_bits: int = 32) -> int:
+    """MINE section 4.2 ("Launch") table-size tuning: candidate sizes 2^b taken in
+    increasing order, each scored by the cross-entropy lower bound of the stored size
+    (n * H(P, Q_b) payload bits plus 2^b table entries); stop once a score exceeds
+    the best so far by more than 1%, and return the best b."""
+    best_b, best = None, None
+    for b in candidates:
+        try:
+            f = rans_freqs(counts, b)
+        except ValueError:
+            continue
+        n = float(np.sum(np.asarray(counts, dtype=np.float64)))
+        score = n * cross_entropy(counts, f, b) + table_entry_bits * (1 << b)
+        if best is not None and score > 1.01 * best:
+            break
+        if best is None or score < best:
+            best_b, best = b, score
+    if best_b is None:
+        raise ValueError("no table size holds the alphabet")
+    return best_b
+
+
 class Rans:
     """Independent-tile interleaved rANS encoding of 4-bit codes (-8..7)."""
 

@@ -327,6 +327,39 @@ def test_rans_blob_matches_oracle_stream(ec, tuple_, shape, tile):
         assert len(words) - nw < 8 and not words[nw:].any()
 
 
+@pytest.mark.parametrize("tuple_", [1, 2])
+@pytest.mark.parametrize("case", ["gauss", "gauss_1024", "uniform", "peaked", "rare"])
+def test_rans_automatic_table_size_matches_oracle(ec, tuple_, case):
+    """prob_bits = 0: the library picks the table size the oracle's MINE rule picks
+    from the histogram of the padded layout (single codes or pairs).  Small streams
+    take 2^9 (the table dominates); 1024 x 4096 Gaussian codes take 2^10 / 2^11."""
+    rng = np.random.default_rng(len(case) * 7 + tuple_)
+    shape = (48, 1024)
+    if case == "gauss_1024":
+        codes = np.clip(np.round(np.random.default_rng(1).normal(0, 1.1, size=(1024, 4096))), -8, 7).astype(np.int8)
+        scales = np.full((1024, 32), 0x2000, np.uint16)
+        expect = {1: 10, 2: 11}[tuple_]
+    elif case == "gauss":
+        codes, scales = synth.make_rans_case(0, *shape)
+    else:
+        if case == "uniform":
+            codes = rng.integers(-8, 8, size=shape)
+        elif case == "peaked":
+            codes = np.clip(np.round(rng.normal(0, 0.35, size=shape)), -8, 7)
+        else:
+            codes = np.zeros(shape)
+            codes.flat[rng.choice(codes.size, 6, replace=False)] = [-8, -5, 3, 5, 6, 7]
+        codes = codes.astype(np.int8)
+        scales = np.full((shape[0], shape[1] // 128), 0x2000, np.uint16)
+    W = ec.encode_rans(codes, scales, prob_bits=0, device=-1, codes_per_symbol=tuple_)
+    h, _ = parse(W.serialize())
+    padded = rans_padded(codes, h["k_pad"])
+    counts = O.Rans(padded, 12, 4096, k=tuple_).counts
+    assert h["prob_bits"] == O.rans_table_bits(counts)
+    if case == "gauss_1024":
+        assert h["prob_bits"] == expect
+
+
 def test_rans_pair_limits(ec):
     from lossless_entropy_coded_gb300 import _ec
     codes, sc = synth.make_rans_case(0, 4, 256)

@@ -107,3 +107,24 @@ def test_payload_corruption_is_reported(ec, tuple_):
     ec.decode(Wc, out)
     st = ec.status()
     assert st == -5 or not np.array_equal(out.cpu().numpy().view(np.uint16), O.rans_dequant_bf16(codes, scales))
+
+
+@pytest.mark.parametrize("tuple_", [1, 2])
+def test_automatic_table_size_decodes(ec, tuple_):
+    """A matrix whose automatic table is small (uniform codes: 2^9 slots) decodes
+    bit-exactly and multiplies within tolerance."""
+    rng = np.random.default_rng(9 + tuple_)
+    codes = rng.integers(-8, 8, size=(64, 4096)).astype(np.int8)
+    scales = synth.make_rans_case(0, 64, 4096)[1]
+    W = ec.encode_rans(codes, scales, prob_bits=0, codes_per_symbol=tuple_)
+    assert W.stats()["max_code_len"] == 9
+    out = torch.zeros((64, 4096), dtype=torch.int16, device="cuda")
+    ec.decode(W, out)
+    assert ec.status() == 0
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), O.rans_dequant_bf16(codes, scales))
+    x = synth.make_x(4300, 4, 4096)
+    y = torch.zeros((4, 64), device="cuda")
+    ec.gemv(W, dev(x.view(np.int16)), y, batch=4)
+    assert ec.status() == 0
+    y_ref, a_ref = O.gemv_rans(codes, scales, x)
+    check_gemv(y.cpu().numpy(), y_ref, a_ref, "automatic table")

@@ -167,3 +167,57 @@ def test_pair_size_against_cross_entropy():
     assert abs(h2 - h1) < 2e-3
     assert ce2 >= h2 and ce2 <= ce1 + 0.02
     assert 16 * r2.payload_words <= c.size * ce2 * 1.005 + 32 * 16 * r2.n_tiles
+
+
+def test_table_bits_uniform_alphabet_takes_the_smallest_table():
+    """Every table size represents a uniform 16-symbol distribution exactly (cross
+    entropy 4 bits at any b >= 4), so the table's own size decides: b = 9."""
+    counts = np.full(16, 1000, dtype=np.uint64)
+    assert O.rans_table_bits(counts) == 9
+    for b in (9, 10, 11, 12):
+        assert abs(O.cross_entropy(counts, O.rans_freqs(counts, b), b) - 4.0) < 1e-12
+
+
+def test_table_bits_rare_symbols_need_the_largest_table():
+    """One dominant symbol and 15 singletons: at 2^b slots the singletons take at
+    least 15 slots, so the dominant symbol costs about -log2(1 - 15/2^b) bits; over
+    10^8 symbols that gap dwarfs the table sizes and the largest table wins."""
+    counts = np.ones(16, dtype=np.uint64)
+    counts[8] = 10 ** 8
+    assert O.rans_table_bits(counts) == 12
+    # the scores follow the closed form closely enough to order the candidates
+    n = float(counts.sum())
+    for b in (9, 12):
+        ce = O.cross_entropy(counts, O.rans_freqs(counts, b), b)
+        f = O.rans_freqs(counts, b)
+        assert f[8] == (1 << b) - 15
+        assert abs(ce - (-(1e8 / n) * np.log2(f[8] / 2 ** b) + 15 / n * b)) < 1e-9
+
+
+def test_table_bits_stops_after_a_one_percent_rise():
+    """The scan stops at the first candidate scoring more than 1% above the best so
+    far.  One symbol of 10^6 and 15 singletons: 2^10 slots beat 2^9 (the singletons'
+    15 slots cost the big symbol half as much), 2^11 costs more than 1% over 2^10 in
+    table entries, so the scan stops there and never scores 2^12; put 2^12 right
+    after 2^9 and the scan stops before reaching 2^10."""
+    counts = np.ones(16, dtype=np.uint64)
+    counts[8] = 10 ** 6
+    n = float(counts.sum())
+    score = {b: n * O.cross_entropy(counts, O.rans_freqs(counts, b), b) + 32 * (1 << b) for b in (9, 10, 11, 12)}
+    assert score[10] < score[9] and score[11] > 1.01 * score[10] and score[12] > 1.01 * score[9]
+    assert O.rans_table_bits(counts) == 10
+    assert O.rans_table_bits(counts, candidates=(9, 12, 10)) == 9
+
+
+@pytest.mark.parametrize("sigma", [0.4, 1.1, 3.0])
+def test_table_bits_estimate_bounds_the_coded_size(sigma):
+    """The chosen table's score is a lower bound: the oracle's stored stream (16-bit
+    payload words and 32-bit final states) is at least n * H(P, Q_b) bits."""
+    rng = np.random.default_rng(int(sigma * 10))
+    c = np.clip(np.round(rng.normal(0, sigma, 64 * 4096)), -8, 7).astype(np.int8)
+    counts = np.bincount(c.astype(np.int64) + 8, minlength=16).astype(np.uint64)
+    b = O.rans_table_bits(counts)
+    r = O.Rans(c, prob_bits=b)
+    assert np.array_equal(r.freqs, O.rans_freqs(counts, b))
+    stored = 16 * r.payload_words + 32 * 32 * r.n_tiles  # payload words and the 32 final states per tile
+    assert stored >= c.size * O.cross_entropy(counts, r.freqs, b)
