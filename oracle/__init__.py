@@ -13,6 +13,9 @@ Functions and the passages they follow (page titles and sections):
   flat_lut / hier_luts          DFloat11 appendix, Fig. 13 and Fig. 14
   DF11 (encode/decode)          DFloat11 sec. "Dynamic-Length Float", "two-phase kernel", Algorithm 1
   Rans (encode/decode)          EntroPack sec. 3.6 and appendix C.3; Duda's rANS
+  rans_table_bits               MINE sec. 4.2 "Launch" (table size by the cross-entropy bound)
+  e8_fields / e8_point / E8     EntroPack sec. 3.2, 3.3, 3.6, 3.7, appendix A.3 (E8 fields, 17 tables)
+  e8_reconstruct_bf16           EntroPack sec. 3.7 (lattice point x shared scale x row scale)
   gemv_bf16 / gemv_rans         y = W x with FP64 accumulation
 
 Every function is pinned by tests in tests/test_oracle_*.py against the pages'
@@ -89,6 +92,18 @@ def _L():
         "orc_rans_dequant_bf16": ([vp, vp, i64, i64, i32, vp], None),
         "orc_gemv_bf16": ([vp, i64, i64, vp, i32, vp, i64, vp, vp], None),
         "orc_gemv_rans": ([vp, vp, i64, i64, i32, vp, i32, vp, i64, vp, vp], None),
+        "orc_e8_fields": ([vp, vp], i32),
+        "orc_e8_point": ([vp, vp], None),
+        "orc_e8_encode": ([vp, i64, i32, i32], vp),
+        "orc_e8_decode": ([vp, vp, vp], i32),
+        "orc_e8_free": ([vp], None),
+        "orc_e8_info": ([vp, vp], i64),
+        "orc_e8_freqs_of": ([vp], vp),
+        "orc_e8_counts_of": ([vp], vp),
+        "orc_e8_states": ([vp], vp),
+        "orc_e8_offsets": ([vp], vp),
+        "orc_e8_payload_mut": ([vp], vp),
+        "orc_e8_reconstruct_bf16": ([vp, i64, i64, ctypes.c_float, vp, vp], None),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -346,6 +361,87 @@ class Rans:
         if rc == -1 or (strict and rc != 0):
             raise ValueError(f"rANS decode failed ({rc})")
         return out, fin[: 32 * self.n_tiles].reshape(self.n_tiles, 32), rc
+
+
+# --------------------------------------------------------------------------- E8 lattice fields
+E8_TABLES, E8_ALPHA = 17, 32
+
+
+def e8_fields(q) -> np.ndarray | None:
+    """Fields (c, z_1+16, .., z_7+16, m+16) of a doubled point q[8]; None if q is not in 2 E8."""
+    qq = np.ascontiguousarray(q, dtype=np.int8)
+    f = np.zeros(9, dtype=np.int32)
+    return f if _L().orc_e8_fields(_p(qq), _p(f)) == 0 else None
+
+
+def e8_point(fields) -> np.ndarray:
+    f = np.ascontiguousarray(fields, dtype=np.int32)
+    q = np.zeros(8, dtype=np.int8)
+    _L().orc_e8_point(_p(f), _p(q))
+    return q
+
+
+class E8:
+    """17-table rANS tile coding of doubled E8 points q [n_vec, 8]."""
+
+    def __init__(self, q: np.ndarray, prob_bits: int = 11, tile: int = 512):
+        qq = np.ascontiguousarray(q, dtype=np.int8).reshape(-1, 8)
+        self.n_vec = qq.shape[0]
+        h = _L().orc_e8_encode(_p(qq) if qq.size else 0, self.n_vec, prob_bits, tile)
+        if not h:
+            raise ValueError("E8 encode failed")
+        self._h = h
+        self.prob_bits = prob_bits
+        info = np.zeros(4, dtype=np.int64)
+        _L().orc_e8_info(h, _p(info))
+        _, self.n_tiles, self.payload_words, self.tile = (int(v) for v in info)
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            _L().orc_e8_free(self._h)
+            self._h = None
+
+    @property
+    def freqs(self):
+        return _view(_L().orc_e8_freqs_of(self._h), np.uint32, E8_TABLES * E8_ALPHA).reshape(E8_TABLES, E8_ALPHA)
+
+    @property
+    def counts(self):
+        return _view(_L().orc_e8_counts_of(self._h), np.uint64, E8_TABLES * E8_ALPHA).reshape(E8_TABLES, E8_ALPHA)
+
+    @property
+    def states(self):
+        return _view(_L().orc_e8_states(self._h), np.uint32, 32 * self.n_tiles).reshape(self.n_tiles, 32)
+
+    @property
+    def offsets(self):
+        return _view(_L().orc_e8_offsets(self._h), np.uint32, self.n_tiles + 1)
+
+    def payload(self) -> np.ndarray:
+        return np.ctypeslib.as_array((ctypes.c_uint16 * max(1, self.payload_words)).from_address(
+            _L().orc_e8_payload_mut(self._h)))[: self.payload_words].copy()
+
+    def flip_payload_bit(self, word: int, bit: int) -> None:
+        w = ctypes.c_uint16.from_address(_L().orc_e8_payload_mut(self._h) + 2 * word)
+        w.value ^= 1 << bit
+
+    def decode(self, strict: bool = True):
+        out = np.zeros((self.n_vec, 8), dtype=np.int8)
+        fin = np.zeros(max(1, 32 * self.n_tiles), dtype=np.uint32)
+        rc = _L().orc_e8_decode(self._h, _p(out) if self.n_vec else 0, _p(fin))
+        if rc == -1 or (strict and rc != 0):
+            raise ValueError(f"E8 decode failed ({rc})")
+        return out, fin[: 32 * self.n_tiles].reshape(self.n_tiles, 32), rc
+
+
+def e8_reconstruct_bf16(q: np.ndarray, scale: float, row_scales: np.ndarray) -> np.ndarray:
+    """BF16 weights of doubled points q [N, K]: bf16(fp32(q * fp32(s * r_i)) * 0.5)."""
+    qq = np.ascontiguousarray(q, dtype=np.int8)
+    r = np.ascontiguousarray(row_scales, dtype=np.float32)
+    n, k = qq.shape
+    out = np.zeros((n, k), dtype=np.uint16)
+    _L().orc_e8_reconstruct_bf16(_p(qq), n, k, ctypes.c_float(scale), _p(r), _p(out))
+    return out
 
 
 def rans_dequant_bf16(codes: np.ndarray, scales: np.ndarray, group: int = 128) -> np.ndarray:

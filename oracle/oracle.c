@@ -820,3 +820,227 @@ void orc_gemv_rans(const int8_t* codes, const uint16_t* scales, int64_t n_rows, 
         }
     }
 }
+
+/* ===========================================================================
+ * E8 lattice fields, EntroPack sections 3.2 (row-normalised lattice
+ * representation), 3.3 (coset-conditioned model), 3.6 (tiles), 3.7 (GPU
+ * reconstruction) and appendix A.3 (parity reduction).
+ *
+ * Weights go in blocks of 8 along a row; block p of row i stands for
+ * w = s * r_i * p with p in E8 = D8 u (D8 + h), h = (1/2, ..., 1/2) and
+ * D8 = { z in Z^8 : z_1 + ... + z_8 even }.  A point is given doubled, q = 2p
+ * (integers, all eight with the same parity).
+ *
+ * Readings (the pages name the fields, not their formulas):
+ *  - coset c = q_1 mod 2 (0: D8, 1: D8 + h); coordinates z_j = (q_j - c) / 2;
+ *  - parity reduction: the eighth coordinate is coded as m with
+ *    z_8 = 2 m + ((z_1 + ... + z_7) mod 2), so every coded (c, z_1..z_7, m) is a
+ *    lattice point and every lattice point has exactly one code;
+ *  - 17 categorical tables: table 0 for c, table 1 + 8 c + f for field f of
+ *    (z_1, ..., z_7, m) under coset c; field values are offset by 16 (z_j in
+ *    -16..15, m in -8..7, alphabet 0..31);
+ *  - reconstruction in FP32: g_i = s * r_i, w = (q * g_i) * 0.5, then BF16 (RNE).
+ *
+ * rANS as in the tile codec above (states in [2^16, 2^32), 16-bit words, one
+ * table per field with sum 2^prob_bits): tiles of `tile` vectors, lane l owns the
+ * tile's vectors l, l + 32, ...; vector j of a lane is nine symbol steps
+ * 9 j .. 9 j + 8 (c first), and at each step the lanes take words in lane order.
+ * ========================================================================= */
+#define E8_FIELDS 9
+#define E8_TABLES 17
+#define E8_ALPHA 32
+
+/* Fields of a doubled point q[8] (c, z_1 + 16, ..., z_7 + 16, m + 16); -1 if q is
+ * not in 2 E8 or a field is out of range. */
+int orc_e8_fields(const int8_t* q, int* fields) {
+    const int c = q[0] & 1;
+    int z[8], sum7 = 0;
+    for (int j = 0; j < 8; ++j) {
+        if ((q[j] & 1) != c) return -1;
+        z[j] = (q[j] - c) / 2;
+    }
+    int total = 0;
+    for (int j = 0; j < 8; ++j) total += z[j];
+    if (total % 2) return -1; /* z must be in D8 */
+    for (int j = 0; j < 7; ++j) sum7 += z[j];
+    const int par = ((sum7 % 2) + 2) % 2;
+    const int m = (z[7] - par) / 2; /* exact: z_8 - par is even */
+    fields[0] = c;
+    for (int j = 0; j < 7; ++j) {
+        if (z[j] < -16 || z[j] > 15) return -1;
+        fields[1 + j] = z[j] + 16;
+    }
+    if (m < -8 || m > 7) return -1;
+    fields[8] = m + 16;
+    return 0;
+}
+
+/* The doubled point of a field vector (inverse of orc_e8_fields). */
+void orc_e8_point(const int* fields, int8_t* q) {
+    const int c = fields[0];
+    int z[8], sum7 = 0;
+    for (int j = 0; j < 7; ++j) {
+        z[j] = fields[1 + j] - 16;
+        sum7 += z[j];
+    }
+    const int par = ((sum7 % 2) + 2) % 2;
+    z[7] = 2 * (fields[8] - 16) + par;
+    for (int j = 0; j < 8; ++j) q[j] = (int8_t)(2 * z[j] + c);
+}
+
+static int e8_table(int f, int c) { return f == 0 ? 0 : 1 + 8 * c + (f - 1); }
+
+typedef struct {
+    int64_t n_vec;
+    int prob_bits, tile;
+    int64_t n_tiles;
+    uint64_t counts[E8_TABLES][E8_ALPHA];
+    uint32_t freqs[E8_TABLES][E8_ALPHA], cum[E8_TABLES][E8_ALPHA];
+    uint32_t* states;
+    uint32_t* offsets;
+    uint16_t* payload;
+    int64_t payload_words;
+} orc_e8;
+
+void orc_e8_free(orc_e8* e) {
+    if (!e) return;
+    free(e->states);
+    free(e->offsets);
+    free(e->payload);
+    free(e);
+}
+
+/* Encode n_vec doubled points q[n_vec][8]; NULL if a point is invalid. */
+orc_e8* orc_e8_encode(const int8_t* q, int64_t n_vec, int prob_bits, int tile) {
+    if (n_vec < 0 || prob_bits < 5 || prob_bits > 15 || tile < 32 || tile % 32) return NULL;
+    orc_e8* e = (orc_e8*)calloc(1, sizeof(orc_e8));
+    e->n_vec = n_vec;
+    e->prob_bits = prob_bits;
+    e->tile = tile;
+    int* fields = (int*)malloc(sizeof(int) * E8_FIELDS * (size_t)(n_vec > 0 ? n_vec : 1));
+    for (int64_t v = 0; v < n_vec; ++v) {
+        if (orc_e8_fields(q + 8 * v, fields + E8_FIELDS * v) < 0) {
+            free(fields);
+            orc_e8_free(e);
+            return NULL;
+        }
+        const int* fv = fields + E8_FIELDS * v;
+        for (int f = 0; f < E8_FIELDS; ++f) e->counts[e8_table(f, fv[0])][fv[f]]++;
+    }
+    for (int t = 0; t < E8_TABLES; ++t) {
+        if (orc_rans_freqs_n(e->counts[t], E8_ALPHA, prob_bits, e->freqs[t]) < 0) {
+            free(fields);
+            orc_e8_free(e);
+            return NULL;
+        }
+        for (int s = 0, c = 0; s < E8_ALPHA; ++s) {
+            e->cum[t][s] = (uint32_t)c;
+            c += (int)e->freqs[t][s];
+        }
+    }
+    e->n_tiles = (n_vec + tile - 1) / tile;
+    e->states = (uint32_t*)malloc(sizeof(uint32_t) * 32 * (size_t)(e->n_tiles > 0 ? e->n_tiles : 1));
+    e->offsets = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)(e->n_tiles + 1));
+    e->payload = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(E8_FIELDS * n_vec + 1));
+    uint16_t* stack = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(E8_FIELDS * tile));
+    const uint64_t renorm_unit = (uint64_t)1 << (32 - prob_bits);
+    int64_t words = 0;
+    for (int64_t t = 0; t < e->n_tiles; ++t) {
+        const int64_t base = t * tile, n_t = (n_vec - base < tile) ? n_vec - base : tile;
+        uint64_t x[32];
+        for (int l = 0; l < 32; ++l) x[l] = 1u << 16;
+        int64_t sp = 0;
+        for (int64_t j = (n_t + 31) / 32 - 1; j >= 0; --j) {
+            for (int f = E8_FIELDS - 1; f >= 0; --f) {
+                for (int l = 31; l >= 0; --l) {
+                    const int64_t v = base + 32 * j + l;
+                    if (32 * j + l >= n_t) continue;
+                    const int* fv = fields + E8_FIELDS * v;
+                    const int tb = e8_table(f, fv[0]), s = fv[f];
+                    const uint64_t fr = e->freqs[tb][s];
+                    while (x[l] >= fr * renorm_unit) {
+                        stack[sp++] = (uint16_t)(x[l] & 0xFFFF);
+                        x[l] >>= 16;
+                    }
+                    x[l] = (x[l] / fr << prob_bits) + (x[l] % fr) + e->cum[tb][s];
+                }
+            }
+        }
+        for (int l = 0; l < 32; ++l) e->states[t * 32 + l] = (uint32_t)x[l];
+        e->offsets[t] = (uint32_t)words;
+        while (sp > 0) e->payload[words++] = stack[--sp];
+    }
+    e->offsets[e->n_tiles] = (uint32_t)words;
+    e->payload_words = words;
+    free(stack);
+    free(fields);
+    return e;
+}
+
+/* Decode to doubled points q_out[n_vec][8].  Returns 0, -1 on a corrupt stream, -2
+ * if a final state is not 2^16 or a tile's words are not used up. */
+int orc_e8_decode(const orc_e8* e, int8_t* q_out, uint32_t* final_states) {
+    const uint32_t M = 1u << e->prob_bits;
+    int rc = 0;
+    for (int64_t t = 0; t < e->n_tiles; ++t) {
+        const int64_t base = t * e->tile, n_t = (e->n_vec - base < e->tile) ? e->n_vec - base : e->tile;
+        uint64_t x[32];
+        int fv[32][E8_FIELDS];
+        for (int l = 0; l < 32; ++l) x[l] = e->states[t * 32 + l];
+        int64_t wp = e->offsets[t];
+        const int64_t wend = e->offsets[t + 1];
+        for (int64_t j = 0; j < (n_t + 31) / 32; ++j) {
+            for (int f = 0; f < E8_FIELDS; ++f) {
+                for (int l = 0; l < 32; ++l) {
+                    if (32 * j + l >= n_t) continue;
+                    const int tb = e8_table(f, f == 0 ? 0 : fv[l][0]);
+                    const uint32_t slot = (uint32_t)(x[l] & (M - 1));
+                    int s = -1;
+                    for (int k = 0; k < E8_ALPHA; ++k)
+                        if (e->freqs[tb][k] && slot >= e->cum[tb][k] && slot < e->cum[tb][k] + e->freqs[tb][k]) s = k;
+                    if (s < 0) return -1;
+                    x[l] = (uint64_t)e->freqs[tb][s] * (x[l] >> e->prob_bits) + slot - e->cum[tb][s];
+                    if (x[l] < (1u << 16)) {
+                        if (wp >= wend) return -1;
+                        x[l] = (x[l] << 16) | e->payload[wp++];
+                    }
+                    fv[l][f] = s;
+                }
+            }
+            for (int l = 0; l < 32; ++l)
+                if (32 * j + l < n_t) orc_e8_point(fv[l], q_out + 8 * (base + 32 * j + l));
+        }
+        for (int l = 0; l < 32; ++l) {
+            if (final_states) final_states[t * 32 + l] = (uint32_t)x[l];
+            if (x[l] != (1u << 16)) rc = -2;
+        }
+        if (wp != wend) rc = -2;
+    }
+    return rc;
+}
+
+int64_t orc_e8_info(const orc_e8* e, int64_t* out /* 4 */) {
+    out[0] = e->n_vec;
+    out[1] = e->n_tiles;
+    out[2] = e->payload_words;
+    out[3] = e->tile;
+    return 0;
+}
+const uint32_t* orc_e8_freqs_of(const orc_e8* e) { return &e->freqs[0][0]; }
+const uint64_t* orc_e8_counts_of(const orc_e8* e) { return &e->counts[0][0]; }
+const uint32_t* orc_e8_states(const orc_e8* e) { return e->states; }
+const uint32_t* orc_e8_offsets(const orc_e8* e) { return e->offsets; }
+uint16_t* orc_e8_payload_mut(orc_e8* e) { return e->payload; }
+
+/* BF16 weights of doubled points q [n_rows, k_cols] (k_cols % 8 == 0): row i's
+ * factor g_i = fp32(s * r_i), w = bf16(fp32(fp32(q) * g_i) * 0.5). */
+void orc_e8_reconstruct_bf16(const int8_t* q, int64_t n_rows, int64_t k_cols, float s, const float* r,
+                             uint16_t* out) {
+    for (int64_t i = 0; i < n_rows; ++i) {
+        const float g = s * r[i];
+        for (int64_t j = 0; j < k_cols; ++j) {
+            const float v = (float)q[i * k_cols + j] * g;
+            out[i * k_cols + j] = orc_f32_to_bf16_rne(v * 0.5f);
+        }
+    }
+}
