@@ -357,7 +357,7 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ extras
 def extras(torch, ec, stream, device):
-    """Secondary measurements: config 1 latency, rANS shapes, 70B-block decode."""
+    """Secondary measurements: config 1 latency, rANS shapes, E8 decode, 70B-block decode."""
     import synth
     out = {}
     dev = f"cuda:{device}"
@@ -408,6 +408,27 @@ def extras(torch, ec, stream, device):
             out[f"rans{tag}_{n}x{k}_bpw"] = round(st["bits_per_weight"], 3)
             out[f"rans{tag}_{n}x{k}_gbs"] = round(st["device_bytes"] / us / 1e3, 1)
             del Rs, gr
+
+    # E8 lattice points at about 4 bits per weight, 14336 x 4096: decode (17-table
+    # rANS tiles + reconstruction) to BF16, four copies rotated to stay out of L2
+    n8, k8 = 14336, 4096
+    q2, r8, s8 = synth.make_e8_case(7500, n8, k8)
+    blob = ec.encode_e8(q2, r8, s8, device=-1).serialize()
+    Es = [ec.deserialize(blob, device=device) for _ in range(4)]
+    de = torch.empty((n8, k8), dtype=torch.int16, device=dev)
+
+    def e8d():
+        for E in Es:
+            ec.decode(E, de)
+    ge = capture(torch, e8d, stream)
+    us = t_loop(ge.replay, 20) / len(Es)
+    st = Es[0].stats()
+    out["e8_14336x4096_decode_us"] = round(us, 2)
+    out["e8_14336x4096_bpw"] = round(st["bits_per_weight"], 3)
+    out["e8_14336x4096_decode_in_gbs"] = round(st["device_bytes"] / us / 1e3, 1)
+    out["e8_14336x4096_decode_hbm_gbs"] = round((st["device_bytes"] + 2 * n8 * k8) / us / 1e3, 1)
+    out["e8_14336x4096_weights_per_s"] = float(f"{n8 * k8 / us * 1e6:.4g}")
+    del Es, ge, de, q2
 
     # 70B-shaped block: one batched decode of all seven matrices to BF16
     Ws, outs, comp, nw = [], [], 0, 0

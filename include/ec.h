@@ -104,7 +104,22 @@ typedef struct {
     int32_t codes_per_symbol;
 } ec_rans_params;
 
-enum { EC_KIND_HUFFMAN_BF16 = 1, EC_KIND_RANS_INT4 = 2 };
+/* E8 lattice codec parameters (NULL = defaults).
+ *  prob_bits         frequency precision b of the 17 tables, 9..12 (default 11,
+ *                    EntroPack's starting precision for rates up to 7 bits)
+ *  tile_vectors      8-weight vectors per independent rANS tile, a multiple of 32
+ *                    up to 1024 (default 1024: 8192 weights, so the 132 bytes of
+ *                    terminal states and offset per tile stay near 3 % of a 4-bit
+ *                    stream, within EntroPack's reported range); the bound keeps the
+ *                    longest possible tile (12 bits for each of its 9 symbols a
+ *                    vector) within the decoder's shared-memory buffers */
+typedef struct {
+    int32_t prob_bits;
+    int32_t tile_vectors;
+    int32_t reserved[2];
+} ec_e8_params;
+
+enum { EC_KIND_HUFFMAN_BF16 = 1, EC_KIND_RANS_INT4 = 2, EC_KIND_E8 = 3 };
 
 /* Sizes and rates of one encoded matrix (ec_stats). */
 typedef struct {
@@ -136,6 +151,20 @@ int ec_encode_bf16(const uint16_t* w_host, int64_t n_rows, int64_t k_cols, const
  * The represented weight is w = code * scale (exact in FP32). */
 int ec_encode_rans(const int8_t* codes_host, const uint16_t* scales_f16_host, int64_t n_rows, int64_t k_cols,
                    const ec_rans_params* params, int device, ec_matrix** out);
+
+/* Encode E8 lattice points (EntroPack sections 3.2-3.7): row i of the matrix is
+ * cut into blocks of 8 weights, each w = s * r_i * p with p in E8 = D8 u (D8 + 1/2)
+ * (D8: integer vectors with an even sum).  q2_host [n_rows, k_cols] (host, int8,
+ * k_cols % 8 == 0) holds q = 2 p; row_scales_host [n_rows] are the FP32 r_i and
+ * `scale` the shared s.  Each point is coded as its coset c, seven coordinates
+ * z_j = (q_j - c) / 2 in -16..15 and m = (z_8 - (z_1 + .. + z_7) mod 2) / 2 in -8..7,
+ * with 17 frequency tables (c; each field under each coset) over independent rANS
+ * tiles.  A decode (ec_decode / ec_decode_batch) writes bf16(fp32(q * fp32(s * r_i))
+ * * 0.5).  Points outside that range or not in E8: EC_ERR_INVALID_ARG.  ec_gemv and
+ * ec_gemv_group on these matrices return EC_ERR_UNSUPPORTED (EntroPack decodes to a
+ * dense matrix before its matrix products). */
+int ec_encode_e8(const int8_t* q2_host, const float* row_scales_host, float scale, int64_t n_rows, int64_t k_cols,
+                 const ec_e8_params* params, int device, ec_matrix** out);
 
 /* Decode W to dense row-major BF16 [n_rows, k_cols] in device memory out_bf16.
  * Huffman: the original bit patterns.  rANS: BF16 round-to-nearest-even of

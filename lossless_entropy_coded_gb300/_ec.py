@@ -29,14 +29,15 @@ EC_ERR_UNSUPPORTED = -4
 EC_ERR_CORRUPT = -5
 EC_ERR_CUDA = -6
 EC_ERR_OOM = -7
-EC_MAX_BATCH = 16
+EC_MAX_BATCH = 64
 EC_MAX_GROUP = 8
 EC_KIND_HUFFMAN_BF16 = 1
 EC_KIND_RANS_INT4 = 2
+EC_KIND_E8 = 3
 
 EXPORTS = ["ec_encode_bf16", "ec_encode_rans", "ec_decode", "ec_decode_batch", "ec_gemv", "ec_gemv_group",
            "ec_bf16_gemv", "ec_stats", "ec_code_lengths", "ec_serialize", "ec_deserialize", "ec_status", "ec_free",
-           "ec_strerror", "ec_gemv_static", "ec_gemv_path"]
+           "ec_strerror", "ec_gemv_static", "ec_gemv_path", "ec_encode_e8"]
 
 
 class HuffParams(ctypes.Structure):
@@ -46,6 +47,10 @@ class HuffParams(ctypes.Structure):
 class RansParams(ctypes.Structure):
     _fields_ = [("prob_bits", ctypes.c_int32), ("tile_syms", ctypes.c_int32), ("group", ctypes.c_int32),
                 ("codes_per_symbol", ctypes.c_int32)]
+
+
+class E8Params(ctypes.Structure):
+    _fields_ = [("prob_bits", ctypes.c_int32), ("tile_vectors", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2)]
 
 
 class Stats(ctypes.Structure):
@@ -64,6 +69,8 @@ _vp, _i64, _i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
 _sig = {
     "ec_encode_bf16": ([_vp, _i64, _i64, ctypes.POINTER(HuffParams), _i32, ctypes.POINTER(_vp)], _i32),
     "ec_encode_rans": ([_vp, _vp, _i64, _i64, ctypes.POINTER(RansParams), _i32, ctypes.POINTER(_vp)], _i32),
+    "ec_encode_e8": ([_vp, _vp, ctypes.c_float, _i64, _i64, ctypes.POINTER(E8Params), _i32, ctypes.POINTER(_vp)],
+                     _i32),
     "ec_decode": ([_vp, _vp, _vp], _i32),
     "ec_decode_batch": ([_vp, _vp, _i32, _vp], _i32),
     "ec_gemv": ([_vp, _vp, _vp, _i32, _vp], _i32),
@@ -185,6 +192,20 @@ def encode_rans(codes, scales_f16, prob_bits: int = 12, tile_syms: int = 4096, g
     h = ctypes.c_void_p()
     _check(lib.ec_encode_rans(pc, ps, n, k, ctypes.byref(prm), device, ctypes.byref(h)), "ec_encode_rans")
     return Matrix(h.value, n, k, EC_KIND_RANS_INT4, device)
+
+
+def encode_e8(q2, row_scales, scale: float, prob_bits: int = 0, tile_vectors: int = 0,
+              device: int = 0) -> Matrix:
+    """Encode host int8 doubled E8 points q2 [N, K] (each run of 8 columns is 2 p with
+    p in E8) with FP32 row scales [N] and the global scale s; decode gives
+    bf16(q2 / 2 * s * r_i).  0 selects the defaults (2^11 slots, 1024 vectors a tile)."""
+    n, k = int(q2.shape[0]), int(q2.shape[1])
+    pq, kq = _host_ptr(q2)
+    pr, kr = _host_ptr(row_scales)
+    prm = E8Params(prob_bits, tile_vectors)
+    h = ctypes.c_void_p()
+    _check(lib.ec_encode_e8(pq, pr, float(scale), n, k, ctypes.byref(prm), device, ctypes.byref(h)), "ec_encode_e8")
+    return Matrix(h.value, n, k, EC_KIND_E8, device)
 
 
 def deserialize(data: bytes, device: int = 0) -> Matrix:

@@ -34,6 +34,14 @@
  *                             area is bit 31 - (b % 32) of word b / 32 (MSB first);
  *                             followed by >= 8 zero bytes, padded to 16 bytes.
  *
+ * E8 matrices (kind 3): rows padded to k_pad (a multiple of EC_E8_ROW_ALIGN) with
+ * zero points, flattened row-major into 8-weight vectors and cut into tiles of
+ * 32 * steps vectors; lane l owns the tile's vectors l, l + 32, ...; a vector is
+ * nine symbols (coset, z_1..z_7, m).  Tables: 17 x 32 u32 (freq | cum << 16), table
+ * t = 0 for the coset and 1 + 8 c + f for field f under coset c, then 17 x 2^b u8
+ * slot -> symbol maps.  [group scales] holds the FP32 row scales [n_rows].  Tile
+ * records as rANS below.
+ *
  * rANS tile record (EntroPack appendix C.3):
  *   u32 state[32]             the decoder's initial states (the encoder's final ones)
  *   u16 word[]                16-bit payload words in decoder order, padded to 16 B.
@@ -44,7 +52,7 @@
 #include <stdint.h>
 
 #define EC_BLOB_MAGIC 0x31434345u /* "ECC1" */
-#define EC_BLOB_VERSION 6u
+#define EC_BLOB_VERSION 7u
 
 #define EC_L1_BITS 12            /* level-1 Huffman window */
 #define EC_SUB_BITS 8            /* bits per sub-table level */
@@ -52,6 +60,9 @@
 #define EC_HUFF_ROW_ALIGN 512    /* k_pad multiple for the Huffman layout (16 symbols x 32 lanes) */
 #define EC_MMA_WINDOW_ROWS 31     /* rows whose tiles one tensor-core work item stages together */
 #define EC_RANS_ROW_ALIGN 128    /* k_pad multiple for the rANS layout (= scale group) */
+#define EC_E8_ROW_ALIGN 256      /* k_pad multiple for the E8 layout (32 vectors of 8) */
+#define EC_E8_TABLES 17          /* the coset, and 8 fields under each of 2 cosets */
+#define EC_E8_ALPHA 32           /* symbols per field: z + 16 (z in -16..15), m + 16 (m in -8..7) */
 #define EC_MAX_CODE_LEN 24
 
 /* bytes of the raw sign/mantissa section of a tile with `steps` symbols per lane */
@@ -112,7 +123,8 @@ typedef struct {
     int32_t window_code_bytes;        /* Huffman, tiles inside rows: the largest sum of (64 + code area)
                                        * over EC_MMA_WINDOW_ROWS consecutive rows' tiles of one tile
                                        * column; 0 when tiles cross rows */
-    uint8_t pad[256 - 4 * 4 - 8 * 10 - 4 * 6];
+    uint32_t e8_scale_bits;           /* E8: the shared scale s (FP32 bit pattern) */
+    uint8_t pad[256 - 4 * 4 - 8 * 10 - 4 * 7];
 } ec_blob_header;
 
 #endif /* EC_FORMAT_H_ */

@@ -739,6 +739,199 @@ extern "C" int ec_encode_rans(const int8_t* codes, const uint16_t* scales, int64
     });
 }
 
+/* ============================================================ E8 lattice encoder */
+namespace {
+/* Fields of a doubled E8 point q[8] (EntroPack sections 3.2, 3.3; appendix A.3):
+ * the coset c = q_1 mod 2, z_j = (q_j - c) / 2 (j = 1..7) offset by 16, and the
+ * parity-reduced m = (z_8 - (z_1 + .. + z_7) mod 2) / 2 offset by 16.  False if q is
+ * not in 2 E8 or a field leaves its alphabet. */
+bool e8_point_fields(const int8_t* q, int* fld) {
+    const int c = q[0] & 1;
+    int z[8], sum = 0;
+    for (int j = 0; j < 8; ++j) {
+        if ((q[j] & 1) != c) return false;
+        z[j] = (q[j] - c) / 2;
+        sum += z[j];
+    }
+    if (sum & 1) return false; /* not in D8 */
+    const int par = (sum - z[7]) & 1;
+    const int m = (z[7] - par) / 2;
+    fld[0] = c;
+    for (int j = 0; j < 7; ++j) {
+        if (z[j] < -16 || z[j] > 15) return false;
+        fld[1 + j] = z[j] + 16;
+    }
+    if (m < -8 || m > 7) return false;
+    fld[8] = m + 16;
+    return true;
+}
+inline int e8_table_of(int f, int c) { return f == 0 ? 0 : 1 + 8 * c + (f - 1); }
+}  // namespace
+
+extern "C" int ec_encode_e8(const int8_t* q2, const float* row_scales, float scale, int64_t n_rows, int64_t k_cols,
+                            const ec_e8_params* params, int device, ec_matrix** out) {
+    if (!out) return EC_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (n_rows < 0 || k_cols < 0 || k_cols % 8) return EC_ERR_SHAPE;
+    const int b = params && params->prob_bits ? params->prob_bits : 11;
+    const int TV = params && params->tile_vectors ? params->tile_vectors : 1024;
+    if (b < 9 || b > 12 || TV < 32 || TV % 32 || TV > 1024) return EC_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return EC_ERR_INVALID_ARG;
+    if (k_cols > INT64_MAX - EC_E8_ROW_ALIGN) return EC_ERR_OVERFLOW;
+    const int64_t KP = round_up(k_cols, EC_E8_ROW_ALIGN), VPR = KP / 8;
+    int64_t nk = 0, n_vec = 0, tmp = 0;
+    if (!mul_ok(n_rows, k_cols, &nk) || !mul_ok(n_rows, VPR, &n_vec) || !mul_ok(n_vec, 9 * 2, &tmp))
+        return EC_ERR_OVERFLOW;
+    if (nk > 0 && (!q2 || !row_scales)) return EC_ERR_INVALID_ARG;
+
+    return guarded([&]() -> int {
+        const int64_t K = k_cols;
+        /* fields of every vector of the padded layout (padding: the zero point) */
+        std::vector<uint8_t> fields((size_t)n_vec * 9, 0);
+        std::atomic<bool> bad{false};
+        parallel_for(n_rows, [&](int64_t lo, int64_t hi) {
+            int f[9];
+            for (int64_t r = lo; r < hi && !bad; ++r)
+                for (int64_t v = 0; v < VPR; ++v) {
+                    uint8_t* dst = fields.data() + 9 * (r * VPR + v);
+                    if (8 * v < K) {
+                        if (!e8_point_fields(q2 + r * K + 8 * v, f)) {
+                            bad = true;
+                            break;
+                        }
+                        for (int i = 0; i < 9; ++i) dst[i] = (uint8_t)f[i];
+                    } else {
+                        dst[0] = 0;
+                        for (int i = 1; i < 9; ++i) dst[i] = 16;
+                    }
+                }
+        });
+        if (bad) return EC_ERR_INVALID_ARG;
+        for (int64_t r = 0; r < n_rows; ++r)
+            if (!std::isfinite(row_scales[r])) return EC_ERR_INVALID_ARG;
+        ec_matrix* m = new_matrix();
+        if (!m) return EC_ERR_OOM;
+        uint64_t counts[EC_E8_TABLES][EC_E8_ALPHA] = {};
+        for (int64_t v = 0; v < n_vec; ++v) {
+            const uint8_t* fv = fields.data() + 9 * v;
+            for (int f = 0; f < 9; ++f) counts[e8_table_of(f, fv[0])][fv[f]]++;
+        }
+        const uint32_t M = 1u << b;
+        uint32_t freq[EC_E8_TABLES][EC_E8_ALPHA] = {}, cum[EC_E8_TABLES][EC_E8_ALPHA] = {};
+        std::vector<uint8_t> slot_sym((size_t)EC_E8_TABLES * M, 0);
+        double ideal_bits = 0;
+        for (int t = 0; t < EC_E8_TABLES; ++t) {
+            uint64_t n_t = 0;
+            for (int s = 0; s < EC_E8_ALPHA; ++s) n_t += counts[t][s];
+            if (!n_t) continue; /* a table no symbol uses (a coset that never occurs) */
+            if (!rans_normalise(counts[t], EC_E8_ALPHA, b, freq[t])) {
+                delete m;
+                return EC_ERR_INVALID_ARG;
+            }
+            for (int s = 0, c = 0; s < EC_E8_ALPHA; ++s) {
+                cum[t][s] = (uint32_t)c;
+                for (uint32_t q = 0; q < freq[t][s]; ++q) slot_sym[(size_t)t * M + c + q] = (uint8_t)s;
+                c += (int)freq[t][s];
+                if (counts[t][s]) ideal_bits -= (double)counts[t][s] * std::log2((double)counts[t][s] / (double)n_t);
+            }
+        }
+        /* tiles: vector j of lane l is tile vector 32 j + l; encoded last vector first,
+         * fields 8 -> 0, lanes 31 -> 0, so the decoder reads in the opposite order */
+        const int64_t n_tiles = (n_vec + TV - 1) / TV;
+        std::vector<std::vector<uint16_t>> words(n_tiles);
+        std::vector<std::array<uint32_t, 32>> states(n_tiles);
+        const uint64_t unit = uint64_t(1) << (32 - b);
+        parallel_for(n_tiles, [&](int64_t lo, int64_t hi) {
+            std::vector<uint16_t> stack;
+            for (int64_t t = lo; t < hi; ++t) {
+                const int64_t base = t * TV, n_t = std::min<int64_t>(TV, n_vec - base);
+                uint64_t x[32];
+                for (int l = 0; l < 32; ++l) x[l] = 1u << 16;
+                stack.clear();
+                for (int64_t j = (n_t + 31) / 32 - 1; j >= 0; --j)
+                    for (int f = 8; f >= 0; --f)
+                        for (int l = 31; l >= 0; --l) {
+                            if (32 * j + l >= n_t) continue;
+                            const uint8_t* fv = fields.data() + 9 * (base + 32 * j + l);
+                            const int tb = e8_table_of(f, fv[0]), s = fv[f];
+                            const uint64_t fr = freq[tb][s];
+                            while (x[l] >= fr * unit) {
+                                stack.push_back((uint16_t)(x[l] & 0xFFFF));
+                                x[l] >>= 16;
+                            }
+                            x[l] = (x[l] / fr << b) + (x[l] % fr) + cum[tb][s];
+                        }
+                for (int l = 0; l < 32; ++l) states[t][l] = (uint32_t)x[l];
+                words[t].assign(stack.rbegin(), stack.rend());
+            }
+        });
+        std::vector<uint32_t> tile_off(n_tiles + 1, 0);
+        int64_t total = 0, max_words = 0, payload = 0;
+        for (int64_t t = 0; t < n_tiles; ++t) {
+            tile_off[t] = (uint32_t)(total / 16);
+            total += 128 + round_up(2 * (int64_t)words[t].size(), 16);
+            max_words = std::max<int64_t>(max_words, (int64_t)words[t].size());
+            payload += 16 * (int64_t)words[t].size();
+        }
+        if (total / 16 > (int64_t)UINT32_MAX) {
+            delete m;
+            return EC_ERR_OVERFLOW;
+        }
+        tile_off[n_tiles] = (uint32_t)(total / 16);
+
+        const int64_t fc_words = EC_E8_TABLES * EC_E8_ALPHA, table_bytes = 4 * fc_words + (int64_t)EC_E8_TABLES * M;
+        ec_blob_header h{};
+        h.magic = EC_BLOB_MAGIC;
+        h.version = EC_BLOB_VERSION;
+        h.kind = EC_KIND_E8;
+        h.steps = TV / 32;
+        h.n_rows = n_rows;
+        h.k_cols = k_cols;
+        h.k_pad = KP;
+        h.n_tiles = n_tiles;
+        h.table_off = sizeof(ec_blob_header);
+        h.table_words = table_bytes / 4;
+        h.scales_off = round_up(h.table_off + table_bytes, 16);
+        h.tile_off_off = round_up(h.scales_off + 4 * n_rows, 16);
+        h.records_off = round_up(h.tile_off_off + 4 * (n_tiles + 1), 16);
+        h.blob_bytes = h.records_off + total;
+        h.prob_bits = b;
+        h.max_words = (int32_t)max_words;
+        std::memcpy(&h.e8_scale_bits, &scale, 4);
+
+        std::vector<uint8_t> blob((size_t)h.blob_bytes, 0);
+        std::memcpy(blob.data(), &h, sizeof h);
+        uint32_t* fc = (uint32_t*)(blob.data() + h.table_off);
+        for (int t = 0; t < EC_E8_TABLES; ++t)
+            for (int s = 0; s < EC_E8_ALPHA; ++s) fc[t * EC_E8_ALPHA + s] = freq[t][s] | (cum[t][s] << 16);
+        std::memcpy(blob.data() + h.table_off + 4 * fc_words, slot_sym.data(), slot_sym.size());
+        if (n_rows) std::memcpy(blob.data() + h.scales_off, row_scales, 4 * (size_t)n_rows);
+        std::memcpy(blob.data() + h.tile_off_off, tile_off.data(), 4 * tile_off.size());
+        parallel_for(n_tiles, [&](int64_t lo, int64_t hi) {
+            for (int64_t t = lo; t < hi; ++t) {
+                uint8_t* rec = blob.data() + h.records_off + (int64_t)tile_off[t] * 16;
+                std::memcpy(rec, states[t].data(), 128);
+                if (!words[t].empty()) std::memcpy(rec + 128, words[t].data(), 2 * words[t].size());
+            }
+        });
+        m->kind = EC_KIND_E8;
+        m->device = device;
+        m->hdr = h;
+        m->payload_bits = payload;
+        m->raw_bytes = 0;
+        m->table_bytes = table_bytes + 4 * n_rows;
+        m->aux_bytes = h.blob_bytes - m->table_bytes - payload / 8;
+        m->entropy = n_vec ? ideal_bits / (8.0 * (double)n_vec) : 0.0; /* ideal bits per weight, conditioned tables */
+        int rc = upload(m, blob, device);
+        if (rc != EC_OK) {
+            delete m;
+            return rc;
+        }
+        *out = m;
+        return EC_OK;
+    });
+}
+
 /* ======================================================= bookkeeping entry points */
 extern "C" int ec_stats(const ec_matrix* m, ec_stats_t* s) {
     if (!m || !s) return EC_ERR_INVALID_ARG;
@@ -822,15 +1015,16 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
     std::memcpy(&h, b, sizeof h);
     if (h.magic != EC_BLOB_MAGIC || h.version != EC_BLOB_VERSION) return EC_ERR_CORRUPT;
     if (h.blob_bytes != bytes) return EC_ERR_CORRUPT;
-    if (h.kind != EC_KIND_HUFFMAN_BF16 && h.kind != EC_KIND_RANS_INT4) return EC_ERR_CORRUPT;
+    if (h.kind != EC_KIND_HUFFMAN_BF16 && h.kind != EC_KIND_RANS_INT4 && h.kind != EC_KIND_E8) return EC_ERR_CORRUPT;
     if (h.n_rows < 0 || h.k_cols < 0 || h.k_cols > INT64_MAX / 2) return EC_ERR_CORRUPT;
-    const bool huff = h.kind == EC_KIND_HUFFMAN_BF16;
-    const int64_t align = huff ? EC_HUFF_ROW_ALIGN : EC_RANS_ROW_ALIGN;
+    const bool huff = h.kind == EC_KIND_HUFFMAN_BF16, e8 = h.kind == EC_KIND_E8;
+    const int64_t align = huff ? EC_HUFF_ROW_ALIGN : e8 ? EC_E8_ROW_ALIGN : EC_RANS_ROW_ALIGN;
     if (h.k_pad != round_up(h.k_cols, align)) return EC_ERR_CORRUPT;
-    if (huff ? (h.steps < 16 || h.steps > 128 || h.steps % 16) : (h.steps < 1 || (32 * h.steps) % align))
+    if (e8 ? (h.k_cols % 8 || h.steps < 1 || h.steps > 32)
+           : huff ? (h.steps < 16 || h.steps > 128 || h.steps % 16) : (h.steps < 1 || (32 * h.steps) % align))
         return EC_ERR_CORRUPT;
-    int64_t n_pad = 0;
-    if (!mul_ok(h.n_rows, h.k_pad, &n_pad)) return EC_ERR_CORRUPT;
+    int64_t n_pad = 0; /* symbols, or for E8 vectors of 8 weights */
+    if (!mul_ok(h.n_rows, e8 ? h.k_pad / 8 : h.k_pad, &n_pad)) return EC_ERR_CORRUPT;
     const int64_t T = 32 * (int64_t)h.steps;
     if (h.n_tiles != (n_pad + T - 1) / T) return EC_ERR_CORRUPT;
     if (h.table_off != (int64_t)sizeof(ec_blob_header)) return EC_ERR_CORRUPT;
@@ -841,6 +1035,10 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
             return EC_ERR_CORRUPT;
         if (h.max_len < 0 || h.max_len > EC_MAX_CODE_LEN || h.max_code_bytes < 0) return EC_ERR_CORRUPT;
         if (h.window_code_bytes < 0) return EC_ERR_CORRUPT;
+    } else if (e8) {
+        if (h.prob_bits < 9 || h.prob_bits > 12 || h.max_words < 0 ||
+            h.table_words != (4 * EC_E8_TABLES * EC_E8_ALPHA + ((int64_t)EC_E8_TABLES << h.prob_bits)) / 4)
+            return EC_ERR_CORRUPT;
     } else {
         if (h.prob_bits < 9 || h.prob_bits > 15 || h.table_words != (int64_t(1) << h.prob_bits) || h.max_words < 0)
             return EC_ERR_CORRUPT;
@@ -848,9 +1046,10 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
         if (h.rans_tuple == 2 && h.prob_bits > 12) return EC_ERR_CORRUPT;
     }
     if (!mul_ok(h.table_words, 4, &t4) || !add_ok(h.table_off, t4, &end)) return EC_ERR_CORRUPT;
-    if (!huff) {
+    if (!huff) { /* rANS: FP16 group scales; E8: FP32 row scales */
         int64_t ns = 0, s2 = 0;
-        if (!mul_ok(h.n_rows, h.k_pad / 128, &ns) || !mul_ok(ns, 2, &s2)) return EC_ERR_CORRUPT;
+        if (e8 ? !mul_ok(h.n_rows, 4, &s2) : (!mul_ok(h.n_rows, h.k_pad / 128, &ns) || !mul_ok(ns, 2, &s2)))
+            return EC_ERR_CORRUPT;
         if (h.scales_off < end || h.scales_off % 16 || !add_ok(h.scales_off, s2, &end)) return EC_ERR_CORRUPT;
     }
     int64_t to4 = 0;
@@ -884,6 +1083,23 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
         }
         for (int64_t i = EC_PAIR_WORDS; i < h.table_words; ++i)
             if ((tab[i] & EC_ENT_PTR) && (int64_t)(tab[i] & 0xFFFFu) >= n_sub) return EC_ERR_CORRUPT;
+    } else if (e8) { /* per table: frequencies summing to 2^b (or an unused all-zero table), cumulative
+                      * starts, and every slot mapped to the symbol whose range holds it */
+        const uint32_t M = 1u << h.prob_bits;
+        const uint8_t* ss = b + h.table_off + 4 * EC_E8_TABLES * EC_E8_ALPHA;
+        for (int t = 0; t < EC_E8_TABLES; ++t) {
+            uint32_t c = 0;
+            for (int s = 0; s < EC_E8_ALPHA; ++s) {
+                const uint32_t e = tab[t * EC_E8_ALPHA + s], f = e & 0xFFFF, cm = e >> 16;
+                if (cm != c || f > M) return EC_ERR_CORRUPT;
+                for (uint32_t q = 0; q < f; ++q)
+                    if (c + q >= M || ss[(size_t)t * M + c + q] != s) return EC_ERR_CORRUPT;
+                c += f;
+            }
+            if (c != M && c != 0) return EC_ERR_CORRUPT;
+            for (uint32_t q = c; q < M; ++q) /* an unused table maps every slot to symbol 0 */
+                if (ss[(size_t)t * M + q] != 0) return EC_ERR_CORRUPT;
+        }
     } else if (h.rans_tuple == 1) {
         for (int64_t i = 0; i < h.table_words; ++i) {
             const uint32_t f = tab[i] >> 16, k = (tab[i] >> 4) & 0xFFF;

@@ -128,6 +128,28 @@ struct RansArgs {
     int* status;
 };
 
+/* E8 lattice matrix (decode only). */
+struct E8Mat {
+    const uint8_t* records;
+    const uint32_t* tile_off;
+    const uint32_t* fc;         /* 17 x 32: freq | cum << 16 */
+    const uint8_t* slot_sym;    /* 17 x 2^prob_bits: slot -> symbol */
+    const float* row_scales;    /* [n_rows] */
+    uint16_t* out;              /* [n_rows, k_cols] BF16 */
+    int64_t n_rows, k_cols, k_pad;
+    int64_t n_tiles;
+    int64_t records_bytes;
+    int32_t steps, prob_bits, words_cap;
+    int32_t last_steps;         /* vectors per lane of the last tile */
+    uint32_t rec16;
+    float scale;                /* the shared scale s */
+};
+
+struct E8Args {
+    E8Mat m;
+    int* status;
+};
+
 /* ------------------------------------------------------------ small helpers */
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -1248,7 +1270,8 @@ struct RansTile {
     int words;  /* payload words; -1 = corrupt record (skipped) */
 };
 
-__device__ __forceinline__ RansTile rans_tile(const RansMat& M, int64_t t, uint2 off) {
+template <class Mat>
+__device__ __forceinline__ RansTile rans_tile(const Mat& M, int64_t t, uint2 off) {
     RansTile r;
     r.t = t;
     r.S = t == M.n_tiles - 1 ? M.last_steps : M.steps;
@@ -1428,6 +1451,130 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) rans_kernel(const _
 
 /* ======================================================== BF16 GEMV comparator */
 constexpr int kRowsPerWarp = 4;
+
+/* ======================================================= E8 lattice decode kernel */
+/* EntroPack section 3.7: recover the coset and coordinate fields of every 8-weight
+ * vector from independent rANS tiles, apply the algebraic inverse (z_8 from m and
+ * the parity of z_1..z_7, q = 2 z + c), rescale by the shared and the row scale and
+ * write BF16, with no intermediate symbol tensor and no reconstruction codebook.
+ * One warp per tile; lane l owns the tile's vectors l, l + 32, ...: nine symbol
+ * steps per vector (the coset first, then its 8 fields from the coset's tables),
+ * each step a slot -> symbol lookup, the state update and a refill taken in lane
+ * order (ballot + popc), as in the 4-bit kernel; the 8 weights of a vector are one
+ * 16-byte store (a warp writes 512 contiguous bytes). */
+__device__ __forceinline__ uint32_t lds8(uint32_t a) {
+    unsigned short v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
+    return v;
+}
+
+__global__ void __launch_bounds__(kMaxHW * 32, 1) e8_kernel(const __grid_constant__ E8Args a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const E8Mat& M = a.m;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+    const int pb = M.prob_bits;
+    const uint32_t mask = (1u << pb) - 1;
+    constexpr uint32_t kFcBytes = 4u * EC_E8_TABLES * EC_E8_ALPHA;
+    const uint32_t fc_s = smem_u32(smem), ss_s = fc_s + kFcBytes;
+    const uint32_t buf_bytes = (uint32_t)rans_buf_bytes(M.words_cap);
+    const uint32_t bufs = ss_s + ((uint32_t)EC_E8_TABLES << pb) + (uint32_t)warp * 2 * buf_bytes;
+    const uint32_t cap = (buf_bytes - 128) / 2 - 1;
+    const int64_t T = 32 * (int64_t)M.steps; /* vectors per tile */
+    const int64_t vpr = M.k_pad / 8, K = M.k_cols;
+
+    const int64_t gw = (int64_t)blockIdx.x * nwarp + warp, nw = (int64_t)gridDim.x * nwarp;
+    RansTile cur{};
+    if (gw < M.n_tiles) {
+        cur = rans_tile(M, gw, make_uint2(__ldg(M.tile_off + gw), __ldg(M.tile_off + gw + 1)));
+        rans_prefetch(bufs, cur, lane);
+    }
+    {
+        const uint4* src = (const uint4*)M.fc;
+        uint4* dst = (uint4*)smem;
+        for (uint32_t i = threadIdx.x; i < kFcBytes / 16; i += blockDim.x) dst[i] = __ldg(src + i);
+        const uint4* s2 = (const uint4*)M.slot_sym;
+        uint4* d2 = (uint4*)(smem + kFcBytes);
+        for (uint32_t i = threadIdx.x; i < ((uint32_t)EC_E8_TABLES << pb) / 16; i += blockDim.x) d2[i] = __ldg(s2 + i);
+    }
+    grid_dep_launch();
+    grid_dep_wait(); /* out belongs to the preceding kernel in the stream from here on */
+    __syncthreads();
+    if (gw >= M.n_tiles) return;
+
+    uint2 off_next = gw + nw < M.n_tiles ? make_uint2(__ldg(M.tile_off + gw + nw), __ldg(M.tile_off + gw + nw + 1))
+                                         : make_uint2(0u, 0u);
+    const uint32_t lt = (1u << lane) - 1u;
+    uint32_t cb = bufs;
+    for (int64_t t = gw; t < M.n_tiles; t += nw) {
+        cp_async_wait_all();
+        __syncwarp();
+        const uint32_t nb_buf = cb == bufs ? bufs + buf_bytes : bufs;
+        RansTile nxt{};
+        if (t + nw < M.n_tiles) {
+            nxt = rans_tile(M, t + nw, off_next);
+            rans_prefetch(nb_buf, nxt, lane);
+            if (t + 2 * nw < M.n_tiles)
+                off_next = make_uint2(__ldg(M.tile_off + t + 2 * nw), __ldg(M.tile_off + t + 2 * nw + 1));
+        }
+        if (cur.words < 0) {
+            if (lane == 0) flag_corrupt(a.status);
+        } else {
+            uint32_t x = lds32(cb + 4 * lane);
+            const uint32_t wbase = cb + 128;
+            uint32_t wp = 0;
+            const int64_t v0 = t * T + lane;
+            int64_t row = v0 / vpr;
+            int64_t cv = v0 - row * vpr; /* this lane's vector column */
+            /* one symbol of table tb */
+            auto step = [&](uint32_t tb) {
+                const uint32_t slot = x & mask;
+                const uint32_t sym = lds8(ss_s + (tb << pb) + slot);
+                const uint32_t e = lds32(fc_s + 4 * (tb * EC_E8_ALPHA + sym));
+                x = (e & 0xFFFFu) * (x >> pb) + slot - (e >> 16);
+                const bool need = x < 65536u;
+                const uint32_t bal = __ballot_sync(kFull, need);
+                const uint32_t idx = min(wp + __popc(bal & lt), cap);
+                const uint32_t v = lds16_if(need, wbase + 2 * idx, 0u);
+                x = need ? x * 65536u + v : x;
+                wp += __popc(bal);
+                return sym;
+            };
+            for (int j = 0; j < cur.S; ++j) {
+                const uint32_t c = step(0) & 1u;
+                int z[8];
+                int sum7 = 0;
+#pragma unroll
+                for (int f = 0; f < 7; ++f) {
+                    z[f] = (int)step(1 + 8 * c + f) - 16;
+                    sum7 += z[f];
+                }
+                const int mm = (int)step(1 + 8 * c + 7) - 16;
+                z[7] = 2 * mm + (sum7 & 1); /* parity reduction inverted: z is in D8 */
+                const float g = __fmul_rn(M.scale, __ldg(M.row_scales + row));
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float lo = __fmul_rn(__fmul_rn((float)(2 * z[2 * i] + (int)c), g), 0.5f);
+                    const float hi = __fmul_rn(__fmul_rn((float)(2 * z[2 * i + 1] + (int)c), g), 0.5f);
+                    w[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+                           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+                }
+                if (8 * cv < K) *(uint4*)(M.out + row * K + 8 * cv) = make_uint4(w[0], w[1], w[2], w[3]);
+                cv += 32;
+                if (cv >= vpr) {
+                    cv -= vpr;
+                    ++row;
+                }
+            }
+            /* every lane returns to 2^16 and the words are used up (up to 7 padding words) */
+            if (__any_sync(kFull, x != 65536u) || wp > (uint32_t)cur.words || (uint32_t)cur.words - wp > 7) {
+                if (lane == 0) flag_corrupt(a.status);
+            }
+        }
+        cur = nxt;
+        cb = nb_buf;
+    }
+}
 
 template <int B>
 __global__ void __launch_bounds__(kWarps * 32) bf16_gemv_kernel(const uint16_t* __restrict__ w, int64_t n_rows,
@@ -1649,6 +1796,29 @@ RansMat rans_desc(const ec_matrix* W) {
     m.last_steps = h.n_tiles > 0 ? (int32_t)((h.n_rows * h.k_pad - (h.n_tiles - 1) * T) / 32) : 0;
     m.rec16 = (uint32_t)(m.records_bytes / 16);
     m.tuple = h.rans_tuple;
+    return m;
+}
+
+E8Mat e8_desc(const ec_matrix* W) {
+    E8Mat m{};
+    const ec_blob_header& h = W->hdr;
+    m.records = W->d_blob + h.records_off;
+    m.tile_off = (const uint32_t*)(W->d_blob + h.tile_off_off);
+    m.fc = (const uint32_t*)(W->d_blob + h.table_off);
+    m.slot_sym = W->d_blob + h.table_off + 4 * EC_E8_TABLES * EC_E8_ALPHA;
+    m.row_scales = (const float*)(W->d_blob + h.scales_off);
+    m.n_rows = h.n_rows;
+    m.k_cols = h.k_cols;
+    m.k_pad = h.k_pad;
+    m.n_tiles = h.n_tiles;
+    m.records_bytes = h.blob_bytes - h.records_off;
+    m.steps = h.steps;
+    m.prob_bits = h.prob_bits;
+    m.words_cap = (h.max_words + 7) / 8 * 8;
+    const int64_t T = 32 * (int64_t)h.steps, n_vec = h.n_rows * (h.k_pad / 8);
+    m.last_steps = h.n_tiles > 0 ? (int32_t)((n_vec - (h.n_tiles - 1) * T) / 32) : 0;
+    m.rec16 = (uint32_t)(m.records_bytes / 16);
+    std::memcpy(&m.scale, &h.e8_scale_bits, 4);
     return m;
 }
 
@@ -1945,6 +2115,23 @@ int rans_run(const ec_matrix* W, const uint16_t* x, float* y, uint16_t* out, int
     return EC_OK;
 }
 
+/* E8 decode: one CTA per SM, the 17 tables in shared memory, two tile buffers per warp. */
+int e8_run(const ec_matrix* W, uint16_t* out, cudaStream_t s, DeviceInfo* d) {
+    E8Args a{};
+    a.m = e8_desc(W);
+    a.m.out = out;
+    a.status = d->status;
+    if (W->hdr.n_tiles == 0) return EC_OK;
+    const size_t tables = 4 * EC_E8_TABLES * EC_E8_ALPHA + ((size_t)EC_E8_TABLES << a.m.prob_bits);
+    const size_t per_warp = 2 * rans_buf_bytes(a.m.words_cap);
+    if (tables + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED; /* not for tiles of <= 1024 vectors */
+    const int warps = (int)std::min<size_t>(kMaxHW, (d->smem_optin - tables) / per_warp);
+    const size_t smem = tables + (size_t)warps * per_warp;
+    if (set_smem(e8_kernel, smem) != EC_OK) return EC_ERR_CUDA;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(d->sms, (W->hdr.n_tiles + warps - 1) / warps));
+    return launch_ex(e8_kernel, grid, warps * 32, smem, s, a);
+}
+
 /* ====================================================== allocation-free GEMV */
 /* Scratch for ec_gemv_static: one file-scope device array that every GPU loading
  * this library holds until exit.  Word 0 is the status word of those calls; the
@@ -2020,6 +2207,7 @@ extern "C" int ec_gemv_group(const ec_matrix* const* Ws, int count, const uint16
         if (!ys[k] || !aligned16(ys[k])) return EC_ERR_INVALID_ARG;
     }
     if (Ws[0]->hdr.k_cols > 0 && (!x || !aligned16(x))) return EC_ERR_INVALID_ARG;
+    if (Ws[0]->kind == EC_KIND_E8) return EC_ERR_UNSUPPORTED; /* decoded to a dense matrix instead */
     if (Ws[0]->kind == EC_KIND_HUFFMAN_BF16) return huff_gemv(Ws, count, x, ys, batch, stream, dev, d);
     for (int k = 0; k < count; ++k)
         if ((rc = rans_run(Ws[k], x, ys[k], nullptr, batch, stream, d)) != EC_OK) return rc;
@@ -2033,6 +2221,7 @@ extern "C" int ec_gemv_path(const ec_matrix* const* Ws, int count, int batch) {
         if (!Ws[k]) return EC_ERR_INVALID_ARG;
         if (Ws[k]->kind != Ws[0]->kind || Ws[k]->hdr.k_cols != Ws[0]->hdr.k_cols) return EC_ERR_SHAPE;
     }
+    if (Ws[0]->kind == EC_KIND_E8) return EC_ERR_UNSUPPORTED;
     return Ws[0]->kind == EC_KIND_HUFFMAN_BF16 && use_mma(Ws, count, batch) ? EC_PATH_TENSOR_CORES : EC_PATH_CUDA_CORES;
 }
 
@@ -2059,6 +2248,10 @@ extern "C" int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs
         if (n > 0 && (!outs[k] || !aligned16(outs[k]))) return EC_ERR_INVALID_ARG;
         if (Ws[k]->kind == EC_KIND_RANS_INT4) {
             if ((rc = rans_run(Ws[k], nullptr, nullptr, outs[k], 1, stream, d)) != EC_OK) return rc;
+            continue;
+        }
+        if (Ws[k]->kind == EC_KIND_E8) {
+            if ((rc = e8_run(Ws[k], outs[k], stream, d)) != EC_OK) return rc;
             continue;
         }
         HuffMat m = huff_desc(Ws[k]);

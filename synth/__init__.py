@@ -181,3 +181,32 @@ def make_rans_case(shape_index: int, n_rows: int | None = None, k_cols: int | No
 
 def synth_subseed(seed: int, tag: int) -> int:
     return int(_L().synth_subseed(seed, tag))
+
+
+def e8_points(seed: int, n_rows: int, k_cols: int, std: float = 3.5) -> np.ndarray:
+    """Doubled E8 points q = 2 z + c, int8 [n_rows, k_cols] (k_cols % 8 == 0).
+
+    Per run of 8 columns: coset c ~ Bernoulli(1/2); z_j = clip(rne(std * g_j), -15, 14)
+    with g ~ N(0, 1); if z_1 + ... + z_8 is odd, coordinate u (uniform in 0..7) moves
+    by one toward zero (away from zero if it is 0), which puts z in D8.  std = 3.5 gives
+    about 4 bits of entropy per weight."""
+    assert k_cols % 8 == 0
+    nv = n_rows * (k_cols // 8)
+    z = np.clip(np.rint(std * normal_f64(seed, 8 * nv)), -15, 14).astype(np.int16).reshape(nv, 8)
+    u = uniform_f64(synth_subseed(seed, 1), 2 * nv).reshape(nv, 2)
+    c = (u[:, 0] < 0.5).astype(np.int16)
+    odd = np.nonzero(z.sum(axis=1) & 1)[0]
+    j = np.minimum((u[odd, 1] * 8).astype(np.int64), 7)
+    v = z[odd, j]
+    z[odd, j] = np.where(v > 0, v - 1, v + 1)
+    return (2 * z + c[:, None]).astype(np.int8).reshape(n_rows, k_cols)
+
+
+def e8_row_scales(seed: int, n_rows: int, base: float = 0.02, ln_sigma: float = 0.5) -> np.ndarray:
+    """FP32 row scales r_i = base * exp(ln_sigma * g_i), g ~ N(0, 1)."""
+    return (base * np.exp(ln_sigma * normal_f64(seed, n_rows))).astype(np.float32)
+
+
+def make_e8_case(seed: int, n_rows: int, k_cols: int, std: float = 3.5, scale: float = 0.125):
+    """(q2, row_scales, scale) of an E8 matrix: w = bf16(q2 / 2 * scale * r_i)."""
+    return e8_points(seed, n_rows, k_cols, std), e8_row_scales(synth_subseed(seed, 2), n_rows), scale

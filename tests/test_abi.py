@@ -83,12 +83,12 @@ def test_argument_validation(ec):
 
 
 # --------------------------------------------------------------- blob reader
-HDR = struct.Struct("<IIii" + "q" * 10 + "i" * 6)
+HDR = struct.Struct("<IIii" + "q" * 10 + "i" * 6 + "I")
 
 
 HDR_KEYS = ["magic", "version", "kind", "steps", "n_rows", "k_cols", "k_pad", "n_tiles", "table_off",
             "table_words", "scales_off", "tile_off_off", "records_off", "blob_bytes", "max_code_bytes",
-            "prob_bits", "max_words", "max_len", "rans_tuple", "window_code_bytes"]
+            "prob_bits", "max_words", "max_len", "rans_tuple", "window_code_bytes", "e8_scale_bits"]
 
 
 def hdr_offset(key: str) -> int:
@@ -488,3 +488,124 @@ def test_stats_accounting(ec):
     # aux (lane starts, byte alignment, 16-byte record padding, offsets) well under 0.25 bit per weight
     assert s["aux_bytes"] * 8 / n < 0.25
     assert 10.5 < s["bits_per_weight"] < 11.3
+
+
+# --------------------------------------------------------------- E8 lattice codec
+def e8_padded(q2: np.ndarray, k_pad: int) -> np.ndarray:
+    """The points laid out as the library encodes them: rows padded to k_pad with the zero point."""
+    n, k = q2.shape
+    out = np.zeros((n, k_pad), dtype=np.int8)
+    out[:, :k] = q2
+    return out
+
+
+@pytest.mark.parametrize("shape,tile,b", [((3, 256), 32, 11), ((7, 264), 64, 9), ((40, 1024), 512, 11),
+                                          ((1, 8), 32, 12), ((5, 4096), 1024, 10), ((33, 776), 96, 11)])
+def test_e8_blob_matches_oracle_stream(ec, shape, tile, b):
+    """The library's 17 tables, row scales, shared scale, tile states and payload
+    words equal the oracle's own encoding of the padded point layout, word for word."""
+    q2, r, s = synth.make_e8_case(6000 + shape[1], *shape)
+    W = ec.encode_e8(q2, r, s, prob_bits=b, tile_vectors=tile, device=-1)
+    h, dev = parse(W.serialize())
+    assert h["kind"] == ec.EC_KIND_E8 and h["k_pad"] == (shape[1] + 255) // 256 * 256
+    assert h["steps"] == tile // 32 and h["prob_bits"] == b
+    assert struct.unpack("<f", struct.pack("<I", h["e8_scale_bits"]))[0] == np.float32(s)
+    e = O.E8(e8_padded(q2, h["k_pad"]), prob_bits=b, tile=tile)
+    assert h["n_tiles"] == e.n_tiles
+    M = 1 << b
+    fc = np.frombuffer(dev, np.uint32, O.E8_TABLES * O.E8_ALPHA, h["table_off"]).reshape(O.E8_TABLES, O.E8_ALPHA)
+    assert np.array_equal(fc & 0xFFFF, e.freqs)
+    cum = np.concatenate([np.zeros((O.E8_TABLES, 1), np.int64), np.cumsum(e.freqs, axis=1)[:, :-1]], axis=1)
+    used = e.freqs.sum(axis=1) > 0
+    assert np.array_equal((fc >> 16)[used], cum[used])
+    ss = np.frombuffer(dev, np.uint8, O.E8_TABLES * M, h["table_off"] + 4 * fc.size).reshape(O.E8_TABLES, M)
+    for t in np.nonzero(used)[0]:
+        assert np.array_equal(ss[t], np.repeat(np.arange(O.E8_ALPHA), e.freqs[t])), t
+    assert np.array_equal(np.frombuffer(dev, np.float32, shape[0], h["scales_off"]), r)
+    toff = np.frombuffer(dev, np.uint32, h["n_tiles"] + 1, h["tile_off_off"]).astype(np.int64)
+    ooff = e.offsets.astype(np.int64)
+    pay = e.payload()
+    for t in range(h["n_tiles"]):
+        base = h["records_off"] + 16 * toff[t]
+        assert np.array_equal(np.frombuffer(dev, np.uint32, 32, base), e.states[t]), t
+        nw = int(ooff[t + 1] - ooff[t])
+        words = np.frombuffer(dev, np.uint16, 8 * (toff[t + 1] - toff[t]) - 64, base + 128)
+        assert np.array_equal(words[:nw], pay[ooff[t]:ooff[t + 1]]), t
+        assert len(words) - nw < 8 and not words[nw:].any()
+    st = W.stats()
+    assert st["kind"] == ec.EC_KIND_E8 and st["n_rows"] == shape[0] and st["k_cols"] == shape[1]
+
+
+def test_e8_argument_validation(ec):
+    from lossless_entropy_coded_gb300 import _ec
+    q2, r, s = synth.make_e8_case(17, 4, 256)
+    h = ctypes.c_void_p()
+
+    def enc(q, n, k, prm=None, scale=s, rs=r):
+        qq = np.ascontiguousarray(q, np.int8)
+        return _ec.lib.ec_encode_e8(qq.ctypes.data, rs.ctypes.data, scale, n, k,
+                                    ctypes.byref(prm) if prm else None, -1, ctypes.byref(h))
+
+    assert enc(q2, 4, 256) == 0
+    _ec.lib.ec_free(h)
+    assert enc(q2, 4, 252) == _ec.EC_ERR_SHAPE            # k_cols % 8
+    assert enc(q2, -1, 256) == _ec.EC_ERR_SHAPE
+    for prm in [(13, 512), (8, 512), (11, 48), (11, 2048), (11, -32)]:
+        assert enc(q2, 4, 256, _ec.E8Params(*prm)) == _ec.EC_ERR_INVALID_ARG, prm
+    assert enc(q2, 4, 256, scale=float("inf")) == _ec.EC_ERR_INVALID_ARG
+    bad_r = r.copy(); bad_r[2] = np.nan
+    assert enc(q2, 4, 256, rs=bad_r) == _ec.EC_ERR_INVALID_ARG
+    for v, why in [([1, 1, 1, 1, 1, 1, 1, -1], "odd number of -1 in the odd coset"),
+                   ([2, 0, 0, 0, 0, 0, 0, 0], "odd sum in D8"), ([1, 0, 0, 0, 0, 0, 0, 1], "mixed parity"),
+                   ([32, 0, 0, 0, 0, 0, 0, 0], "z_1 = 16 out of range"),
+                   ([0, 0, 0, 0, 0, 0, 0, -34], "z_8 = -17: m out of range")]:
+        qb = q2.copy()
+        qb[1, 8:16] = v
+        assert enc(qb, 4, 256) == _ec.EC_ERR_INVALID_ARG, why
+    # the extremes of every field are accepted: z_j in -16..15, m in -8..7
+    qe = np.zeros((4, 256), np.int8)
+    qe[0, :8] = [-32, 30, 0, 0, 0, 0, 0, 2]          # c 0, z (-16, 15, 0 x 5, 1): m = 0
+    qe[1, :8] = [31, 31, 31, 31, 31, 31, 31, -29]    # c 1, z (15 x 7, -15): odd sum7, m = -8
+    qe[2, :8] = [0, 0, 0, 0, 0, 0, 0, -32]           # c 0, z_8 = -16: even sum7, m = -8
+    qe[3, :8] = [2, 0, 0, 0, 0, 0, 0, 30]            # c 0, z_8 = 15: odd sum7, m = 7
+    assert enc(qe, 4, 256, rs=np.ones(4, np.float32)) == 0
+    _ec.lib.ec_free(h)
+
+
+def test_e8_rejects_structural_corruption(ec):
+    q2, r, s = synth.make_e8_case(23, 20, 1000)
+    W = ec.encode_e8(q2, r, s, device=-1)
+    blob = W.serialize()
+    W2 = ec.deserialize(blob, device=-1)
+    assert W2.stats() == W.stats() and W2.kind == ec.EC_KIND_E8
+    h, dev = parse(blob)
+    meta = len(blob) - len(dev)
+    M = 1 << h["prob_bits"]
+    fc = np.frombuffer(dev, np.uint32, 17 * 32, h["table_off"]).reshape(17, 32)
+    ss0 = meta + h["table_off"] + 4 * 17 * 32
+    unused = [t for t in range(17) if not (fc[t] & 0xFFFF).any()]
+    cases = []
+    for name, off, fmt, val in [("precision", meta + hdr_offset("prob_bits"), "<i", 13),
+                                ("steps", meta + hdr_offset("steps"), "<i", 33),
+                                ("frequency", meta + h["table_off"] + 4 * 40, "<I", int(fc[1, 8]) + 1),
+                                ("slot symbol", ss0 + M + 5, "<B", 31),
+                                ("tile offset", meta + h["tile_off_off"] + 4, "<I", 0xFFFFFF),
+                                ("max words", meta + hdr_offset("max_words"), "<i", 1)]:
+        x = bytearray(blob); struct.pack_into(fmt, x, off, val)
+        cases.append((name, bytes(x)))
+    if unused:
+        x = bytearray(blob); struct.pack_into("<B", x, ss0 + unused[0] * M + 3, 7)
+        cases.append(("unused table slot", bytes(x)))
+    for name, bad in cases:
+        with pytest.raises(ec.EcError) as e:
+            ec.deserialize(bad, device=-1)
+        assert e.value.code == -5, name
+
+
+def test_e8_matrices_have_no_gemv(ec):
+    """EntroPack decodes to a dense matrix: the GEMV query (and the GEMV) refuse E8 matrices."""
+    q2, r, s = synth.make_e8_case(29, 8, 256)
+    W = ec.encode_e8(q2, r, s, device=-1)
+    with pytest.raises(ec.EcError) as e:
+        ec.gemv_path([W], 1)
+    assert e.value.code == -4
