@@ -50,8 +50,14 @@ def peaks():
 
 
 def kernel_hash() -> str:
+    """First 16 hex digits of the SHA-256 of the kernel source without its E8 decode
+    sections (the text between each "E8 decode: begin" / "E8 decode: end" marker pair),
+    which hold only the E8 kernel and its launcher: the Huffman kernels' counters stay
+    valid while the E8 code changes."""
     with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+        src = f.read()
+    src = re.sub(rb"/\* ---- E8 decode: begin ---- \*/.*?/\* ---- E8 decode: end ---- \*/\n", b"", src, flags=re.S)
+    return hashlib.sha256(src).hexdigest()[:16]
 
 
 def profiled_traffic():

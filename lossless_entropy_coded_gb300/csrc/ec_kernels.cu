@@ -148,6 +148,7 @@ struct E8Mat {
 struct E8Args {
     E8Mat m;
     int* status;
+    int nbuf; /* tile buffers per warp: 2 (prefetch the next tile while decoding) or 1 */
 };
 
 /* ------------------------------------------------------------ small helpers */
@@ -1452,6 +1453,7 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) rans_kernel(const _
 /* ======================================================== BF16 GEMV comparator */
 constexpr int kRowsPerWarp = 4;
 
+/* ---- E8 decode: begin ---- */
 /* ======================================================= E8 lattice decode kernel */
 /* EntroPack section 3.7: recover the coset and coordinate fields of every 8-weight
  * vector from independent rANS tiles, apply the algebraic inverse (z_8 from m and
@@ -1461,23 +1463,41 @@ constexpr int kRowsPerWarp = 4;
  * steps per vector (the coset first, then its 8 fields from the coset's tables),
  * each step a slot -> symbol lookup, the state update and a refill taken in lane
  * order (ballot + popc), as in the 4-bit kernel; the 8 weights of a vector are one
- * 16-byte store (a warp writes 512 contiguous bytes). */
-__device__ __forceinline__ uint32_t lds8(uint32_t a) {
-    unsigned short v;
-    asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
+ * 16-byte store (a warp writes 512 contiguous bytes).
+ *
+ * Shared memory: the 17 slot -> symbol byte tables from a 2^PB-aligned address (so
+ * a slot's address is one bitwise or), the 17 x 32 frequencies and the 17 x 32
+ * starts as u16 arrays, then two tile buffers per warp. */
+constexpr uint32_t kE8FreqBytes = 2u * EC_E8_TABLES * EC_E8_ALPHA; /* one u16 array: 1088 B */
+
+__host__ __device__ constexpr size_t e8_table_bytes(int pb) {
+    return ((size_t)1 << pb) /* alignment slack */ + ((size_t)EC_E8_TABLES << pb) + 2 * kE8FreqBytes;
+}
+
+__device__ __forceinline__ uint32_t e8_ld_sym(uint32_t addr) {
+    uint32_t v;
+    asm("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint2 e8_ld_freq(uint32_t addr) {
+    uint2 v;
+    asm("ld.shared.u16 %0, [%2];\n\tld.shared.u16 %1, [%2+%3];" : "=r"(v.x), "=r"(v.y) : "r"(addr), "n"(kE8FreqBytes));
     return v;
 }
 
+template <int PB>
 __global__ void __launch_bounds__(kMaxHW * 32, 1) e8_kernel(const __grid_constant__ E8Args a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const E8Mat& M = a.m;
+    constexpr uint32_t kSlots = 1u << PB, kMask = kSlots - 1;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
-    const int pb = M.prob_bits;
-    const uint32_t mask = (1u << pb) - 1;
-    constexpr uint32_t kFcBytes = 4u * EC_E8_TABLES * EC_E8_ALPHA;
-    const uint32_t fc_s = smem_u32(smem), ss_s = fc_s + kFcBytes;
+    const uint32_t base = smem_u32(smem);
+    const uint32_t pad = (kSlots - (base & kMask)) & kMask; /* a multiple of 16 */
+    uint8_t* const ss = smem + pad;
+    const uint32_t ss_s = base + pad, fq_s = ss_s + EC_E8_TABLES * kSlots;
     const uint32_t buf_bytes = (uint32_t)rans_buf_bytes(M.words_cap);
-    const uint32_t bufs = ss_s + ((uint32_t)EC_E8_TABLES << pb) + (uint32_t)warp * 2 * buf_bytes;
+    const uint32_t bufs = base + (uint32_t)e8_table_bytes(PB) + (uint32_t)(warp * a.nbuf) * buf_bytes;
+    const bool dbl = a.nbuf == 2;
     const uint32_t cap = (buf_bytes - 128) / 2 - 1;
     const int64_t T = 32 * (int64_t)M.steps; /* vectors per tile */
     const int64_t vpr = M.k_pad / 8, K = M.k_cols;
@@ -1489,12 +1509,15 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) e8_kernel(const __grid_constan
         rans_prefetch(bufs, cur, lane);
     }
     {
-        const uint4* src = (const uint4*)M.fc;
-        uint4* dst = (uint4*)smem;
-        for (uint32_t i = threadIdx.x; i < kFcBytes / 16; i += blockDim.x) dst[i] = __ldg(src + i);
         const uint4* s2 = (const uint4*)M.slot_sym;
-        uint4* d2 = (uint4*)(smem + kFcBytes);
-        for (uint32_t i = threadIdx.x; i < ((uint32_t)EC_E8_TABLES << pb) / 16; i += blockDim.x) d2[i] = __ldg(s2 + i);
+        uint4* d2 = (uint4*)ss;
+        for (uint32_t i = threadIdx.x; i < EC_E8_TABLES * kSlots / 16; i += blockDim.x) d2[i] = __ldg(s2 + i);
+        uint16_t* fq = (uint16_t*)(ss + EC_E8_TABLES * kSlots);
+        for (uint32_t i = threadIdx.x; i < EC_E8_TABLES * EC_E8_ALPHA; i += blockDim.x) {
+            const uint32_t e = __ldg(M.fc + i);
+            fq[i] = (uint16_t)(e & 0xFFFFu);
+            fq[EC_E8_TABLES * EC_E8_ALPHA + i] = (uint16_t)(e >> 16);
+        }
     }
     grid_dep_launch();
     grid_dep_wait(); /* out belongs to the preceding kernel in the stream from here on */
@@ -1508,62 +1531,80 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) e8_kernel(const __grid_constan
     for (int64_t t = gw; t < M.n_tiles; t += nw) {
         cp_async_wait_all();
         __syncwarp();
-        const uint32_t nb_buf = cb == bufs ? bufs + buf_bytes : bufs;
+        /* two buffers: the next tile streams into the other one during this decode;
+         * one buffer: it is loaded after this decode (other warps hide the wait) */
+        const uint32_t nb_buf = dbl ? (cb == bufs ? bufs + buf_bytes : bufs) : bufs;
         RansTile nxt{};
         if (t + nw < M.n_tiles) {
             nxt = rans_tile(M, t + nw, off_next);
-            rans_prefetch(nb_buf, nxt, lane);
+            if (dbl) rans_prefetch(nb_buf, nxt, lane);
             if (t + 2 * nw < M.n_tiles)
                 off_next = make_uint2(__ldg(M.tile_off + t + 2 * nw), __ldg(M.tile_off + t + 2 * nw + 1));
         }
         if (cur.words < 0) {
             if (lane == 0) flag_corrupt(a.status);
         } else {
-            uint32_t x = lds32(cb + 4 * lane);
-            const uint32_t wbase = cb + 128;
+            const uint8_t* bp = smem + (cb - base);
+            uint32_t x = ((const uint32_t*)bp)[lane];
+            const uint16_t* words = (const uint16_t*)(bp + 128);
             uint32_t wp = 0;
             const int64_t v0 = t * T + lane;
             int64_t row = v0 / vpr;
             int64_t cv = v0 - row * vpr; /* this lane's vector column */
-            /* one symbol of table tb */
-            auto step = [&](uint32_t tb) {
-                const uint32_t slot = x & mask;
-                const uint32_t sym = lds8(ss_s + (tb << pb) + slot);
-                const uint32_t e = lds32(fc_s + 4 * (tb * EC_E8_ALPHA + sym));
-                x = (e & 0xFFFFu) * (x >> pb) + slot - (e >> 16);
+            float g = __fmul_rn(M.scale, __ldg(M.row_scales + row));
+            /* one symbol: tab = the table's 2^PB-aligned slot base, fq = its frequency row */
+            auto step = [&](uint32_t tab, uint32_t fq) {
+                const uint32_t slot = x & kMask;
+                const uint32_t sym = e8_ld_sym(tab | slot);
+                const uint2 fc = e8_ld_freq(fq + 2 * sym);
+                x = fc.x * (x >> PB) + slot - fc.y;
                 const bool need = x < 65536u;
                 const uint32_t bal = __ballot_sync(kFull, need);
                 const uint32_t idx = min(wp + __popc(bal & lt), cap);
-                const uint32_t v = lds16_if(need, wbase + 2 * idx, 0u);
-                x = need ? x * 65536u + v : x;
+                const uint32_t v = words[idx];
+                x = need ? (x << 16) | v : x;
                 wp += __popc(bal);
                 return sym;
             };
             for (int j = 0; j < cur.S; ++j) {
-                const uint32_t c = step(0) & 1u;
-                int z[8];
-                int sum7 = 0;
+                const uint32_t c = step(ss_s, fq_s) & 1u;
+                const uint32_t tab = ss_s + ((1u + 8u * c) << PB), fq = fq_s + (1u + 8u * c) * 2u * EC_E8_ALPHA;
+                uint32_t s[8];
 #pragma unroll
-                for (int f = 0; f < 7; ++f) {
-                    z[f] = (int)step(1 + 8 * c + f) - 16;
-                    sum7 += z[f];
-                }
-                const int mm = (int)step(1 + 8 * c + 7) - 16;
-                z[7] = 2 * mm + (sum7 & 1); /* parity reduction inverted: z is in D8 */
-                const float g = __fmul_rn(M.scale, __ldg(M.row_scales + row));
+                for (int f = 0; f < 8; ++f) s[f] = step(tab + ((uint32_t)f << PB), fq + 2u * EC_E8_ALPHA * f);
+                /* z_j = s_j - 16; z_8 = 2 m + parity(z_1..z_7) with m = s_8 - 16; q = 2 z + c */
+                const uint32_t par = (s[0] ^ s[1] ^ s[2] ^ s[3] ^ s[4] ^ s[5] ^ s[6]) & 1u;
+                int q[8];
+#pragma unroll
+                for (int f = 0; f < 7; ++f) q[f] = 2 * (int)s[f] - 32 + (int)c;
+                q[7] = 4 * (int)s[7] - 64 + 2 * (int)par + (int)c;
                 uint32_t w[4];
+                /* fl(fl(q g) / 2) == fl(q (g / 2)) while g / 2 is normal and q g finite
+                 * (|q| <= 32): one rounding either way; otherwise both multiplies */
+                const float ag = fabsf(g);
+                if (ag >= 0x1p-125f && ag <= 0x1p120f) {
+                    const float gh = g * 0.5f;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float lo = __fmul_rn(__fmul_rn((float)(2 * z[2 * i] + (int)c), g), 0.5f);
-                    const float hi = __fmul_rn(__fmul_rn((float)(2 * z[2 * i + 1] + (int)c), g), 0.5f);
-                    w[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
-                           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+                    for (int i = 0; i < 4; ++i) {
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__int2float_rn(q[2 * i]), gh),
+                                                                       __fmul_rn(__int2float_rn(q[2 * i + 1]), gh));
+                        w[i] = *(const uint32_t*)&h;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(
+                            __fmul_rn(__fmul_rn(__int2float_rn(q[2 * i]), g), 0.5f),
+                            __fmul_rn(__fmul_rn(__int2float_rn(q[2 * i + 1]), g), 0.5f));
+                        w[i] = *(const uint32_t*)&h;
+                    }
                 }
                 if (8 * cv < K) *(uint4*)(M.out + row * K + 8 * cv) = make_uint4(w[0], w[1], w[2], w[3]);
                 cv += 32;
                 if (cv >= vpr) {
                     cv -= vpr;
                     ++row;
+                    if (j + 1 < cur.S) g = __fmul_rn(M.scale, __ldg(M.row_scales + row));
                 }
             }
             /* every lane returns to 2^16 and the words are used up (up to 7 padding words) */
@@ -1571,10 +1612,16 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) e8_kernel(const __grid_constan
                 if (lane == 0) flag_corrupt(a.status);
             }
         }
+        if (!dbl && t + nw < M.n_tiles) {
+            __syncwarp(); /* every lane has read the buffer before it is overwritten */
+            rans_prefetch(bufs, nxt, lane);
+        }
         cur = nxt;
         cb = nb_buf;
     }
 }
+
+/* ---- E8 decode: end ---- */
 
 template <int B>
 __global__ void __launch_bounds__(kWarps * 32) bf16_gemv_kernel(const uint16_t* __restrict__ w, int64_t n_rows,
@@ -1799,6 +1846,7 @@ RansMat rans_desc(const ec_matrix* W) {
     return m;
 }
 
+/* ---- E8 decode: begin ---- */
 E8Mat e8_desc(const ec_matrix* W) {
     E8Mat m{};
     const ec_blob_header& h = W->hdr;
@@ -1821,6 +1869,7 @@ E8Mat e8_desc(const ec_matrix* W) {
     std::memcpy(&m.scale, &h.e8_scale_bits, 4);
     return m;
 }
+/* ---- E8 decode: end ---- */
 
 int check_matrix(const ec_matrix* W, int dev) {
     if (!W || !W->d_blob || W->hdr.magic != EC_BLOB_MAGIC || W->hdr.version != EC_BLOB_VERSION) return EC_ERR_INVALID_ARG;
@@ -2115,22 +2164,65 @@ int rans_run(const ec_matrix* W, const uint16_t* x, float* y, uint16_t* out, int
     return EC_OK;
 }
 
+/* ---- E8 decode: begin ---- */
 /* E8 decode: one CTA per SM, the 17 tables in shared memory, two tile buffers per warp. */
+/* Warps per CTA and tile buffers per warp.  Two buffers when 32 warps fit with
+ * them, else one buffer and as many warps as fit (an issue-bound decode keeps the SM
+ * busy with the other warps while one waits for its next tile).  The warp count is
+ * then lowered to the fewest that keep the same number of tile rounds, so that the
+ * last round is full.  EC_E8_WARPS / EC_E8_BUFFERS override both. */
+struct E8Plan {
+    int warps, nbuf;
+};
+E8Plan e8_plan(size_t tables, size_t buf, int64_t n_tiles, const DeviceInfo* d) {
+    static const int env_w = [] { const char* e = std::getenv("EC_E8_WARPS"); return e && e[0] ? std::atoi(e) : 0; }();
+    static const int env_b = [] { const char* e = std::getenv("EC_E8_BUFFERS"); return e && e[0] ? std::atoi(e) : 0; }();
+    const size_t room = d->smem_optin - tables;
+    int nbuf = env_b == 1 || env_b == 2 ? env_b : (room / (2 * buf) >= (size_t)kMaxHW ? 2 : 1);
+    int wmax = (int)std::min<size_t>(kMaxHW, room / (nbuf * buf));
+    if (wmax < 1) {
+        nbuf = 1;
+        wmax = (int)std::min<size_t>(kMaxHW, room / buf);
+    }
+    int warps = wmax;
+    if (env_w > 0) {
+        warps = std::min(env_w, wmax);
+    } else {
+        const int64_t per_sm = (n_tiles + d->sms - 1) / d->sms;
+        const int64_t rounds = std::max<int64_t>(1, (per_sm + wmax - 1) / wmax);
+        warps = (int)std::max<int64_t>(1, std::min<int64_t>(wmax, (per_sm + rounds - 1) / rounds));
+    }
+    return {warps, nbuf};
+}
+
+template <int PB>
+int e8_launch(E8Args a, int64_t n_tiles, cudaStream_t s, DeviceInfo* d) {
+    const size_t tables = e8_table_bytes(PB), buf = rans_buf_bytes(a.m.words_cap);
+    if (tables + buf > d->smem_optin) return EC_ERR_UNSUPPORTED; /* not for tiles of <= 1024 vectors */
+    const E8Plan p = e8_plan(tables, buf, n_tiles, d);
+    a.nbuf = p.nbuf;
+    const size_t smem = tables + (size_t)(p.warps * p.nbuf) * buf;
+    if (set_smem(e8_kernel<PB>, smem) != EC_OK) return EC_ERR_CUDA;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(d->sms, (n_tiles + p.warps - 1) / p.warps));
+    return launch_ex(e8_kernel<PB>, grid, p.warps * 32, smem, s, a);
+}
+
 int e8_run(const ec_matrix* W, uint16_t* out, cudaStream_t s, DeviceInfo* d) {
     E8Args a{};
     a.m = e8_desc(W);
     a.m.out = out;
     a.status = d->status;
-    if (W->hdr.n_tiles == 0) return EC_OK;
-    const size_t tables = 4 * EC_E8_TABLES * EC_E8_ALPHA + ((size_t)EC_E8_TABLES << a.m.prob_bits);
-    const size_t per_warp = 2 * rans_buf_bytes(a.m.words_cap);
-    if (tables + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED; /* not for tiles of <= 1024 vectors */
-    const int warps = (int)std::min<size_t>(kMaxHW, (d->smem_optin - tables) / per_warp);
-    const size_t smem = tables + (size_t)warps * per_warp;
-    if (set_smem(e8_kernel, smem) != EC_OK) return EC_ERR_CUDA;
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(d->sms, (W->hdr.n_tiles + warps - 1) / warps));
-    return launch_ex(e8_kernel, grid, warps * 32, smem, s, a);
+    const int64_t nt = W->hdr.n_tiles;
+    if (nt == 0) return EC_OK;
+    switch (a.m.prob_bits) {
+        case 9: return e8_launch<9>(a, nt, s, d);
+        case 10: return e8_launch<10>(a, nt, s, d);
+        case 11: return e8_launch<11>(a, nt, s, d);
+        case 12: return e8_launch<12>(a, nt, s, d);
+        default: return EC_ERR_CORRUPT;
+    }
 }
+/* ---- E8 decode: end ---- */
 
 /* ====================================================== allocation-free GEMV */
 /* Scratch for ec_gemv_static: one file-scope device array that every GPU loading

@@ -61,6 +61,20 @@ def test_power_of_two_scales_are_exact(ec):
     assert np.array_equal(synth.bf16_to_f32(got).astype(np.float64), want)
 
 
+def test_extreme_row_scales(ec):
+    """Rows whose factor g_i = s r_i is subnormal, tiny, huge (q g overflows to
+    infinity) or zero take the two-multiply reconstruction; the others the single
+    multiply by g_i / 2.  Both agree with the oracle bit for bit."""
+    q2, r, s = synth.make_e8_case(47, 12, 512)
+    r = r.copy()
+    r[0], r[1], r[2], r[3] = 1e-38, 3e-37, 3e38, 0.0
+    r[4], r[5] = 2.0 ** -125, 2.0 ** 120  # g on both edges of the single-multiply range
+    r[6], r[7] = -0.03, -1e-39
+    W = ec.encode_e8(q2, r, 1.0)
+    got = decode(ec, W, q2.shape)
+    assert np.array_equal(got, O.e8_reconstruct_bf16(q2, 1.0, r))
+
+
 @pytest.mark.parametrize("shape", [(14336, 4096), (4096, 14336)])
 def test_full_size_config(ec, shape):
     """Llama-3.1-8B gate/up and down shapes at about 4 bits per weight: the whole
