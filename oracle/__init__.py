@@ -16,6 +16,9 @@ Functions and the passages they follow (page titles and sections):
   rans_table_bits               MINE sec. 4.2 "Launch" (table size by the cross-entropy bound)
   e8_fields / e8_point / E8     EntroPack sec. 3.2, 3.3, 3.6, 3.7, appendix A.3 (E8 fields, 17 tables)
   e8_reconstruct_bf16           EntroPack sec. 3.7 (lattice point x shared scale x row scale)
+  e8_reconstruct / f32_to_e4m3 / f32_to_s8
+                                EntroPack sec. 3.7 and appendix B.1 (FP8 / INT8 output); the OCP
+                                FP8 E4M3 format
   gemv_bf16 / gemv_rans         y = W x with FP64 accumulation
 
 Every function is pinned by tests in tests/test_oracle_*.py against the pages'
@@ -104,6 +107,9 @@ def _L():
         "orc_e8_offsets": ([vp], vp),
         "orc_e8_payload_mut": ([vp], vp),
         "orc_e8_reconstruct_bf16": ([vp, i64, i64, ctypes.c_float, vp, vp], None),
+        "orc_e8_reconstruct_as": ([vp, i64, i64, ctypes.c_float, vp, i32, vp], None),
+        "orc_f32_to_e4m3_satfinite": ([ctypes.c_float], ctypes.c_uint8),
+        "orc_f32_to_s8_rne_sat": ([ctypes.c_float], ctypes.c_int8),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -442,6 +448,33 @@ def e8_reconstruct_bf16(q: np.ndarray, scale: float, row_scales: np.ndarray) -> 
     out = np.zeros((n, k), dtype=np.uint16)
     _L().orc_e8_reconstruct_bf16(_p(qq), n, k, ctypes.c_float(scale), _p(r), _p(out))
     return out
+
+
+E8_DTYPES = {"bf16": (0, np.uint16), "e4m3": (1, np.uint8), "int8": (2, np.int8)}
+
+
+def e8_reconstruct(q: np.ndarray, scale: float, row_scales: np.ndarray, dtype: str = "bf16") -> np.ndarray:
+    """Weights of doubled points q [N, K] in `dtype` ("bf16" bit patterns as uint16,
+    "e4m3" codes as uint8, "int8"): dtype(fp32(fp32(q) * fp32(s * r_i)) * 0.5)."""
+    code, nptype = E8_DTYPES[dtype]
+    qq = np.ascontiguousarray(q, dtype=np.int8)
+    r = np.ascontiguousarray(row_scales, dtype=np.float32)
+    n, k = qq.shape
+    out = np.zeros((n, k), dtype=nptype)
+    _L().orc_e8_reconstruct_as(_p(qq), n, k, ctypes.c_float(scale), _p(r), code, _p(out))
+    return out
+
+
+def f32_to_e4m3(values) -> np.ndarray:
+    """FP8 E4M3 codes (uint8) of FP32 values: nearest, ties to even, saturating at 448."""
+    v = np.asarray(values, dtype=np.float32).ravel()
+    return np.array([_L().orc_f32_to_e4m3_satfinite(float(a)) for a in v], dtype=np.uint8)
+
+
+def f32_to_s8(values) -> np.ndarray:
+    """INT8 of FP32 values: nearest integer, ties to even, saturated to [-128, 127]."""
+    v = np.asarray(values, dtype=np.float32).ravel()
+    return np.array([_L().orc_f32_to_s8_rne_sat(float(a)) for a in v], dtype=np.int8)
 
 
 def rans_dequant_bf16(codes: np.ndarray, scales: np.ndarray, group: int = 128) -> np.ndarray:

@@ -64,6 +64,45 @@ uint16_t orc_f32_to_bf16_rne(float f) {
     return (uint16_t)upper;
 }
 
+/* FP32 -> FP8 E4M3 of the OCP 8-bit floating-point format: 1 sign bit, 4 exponent
+ * bits with bias 7, 3 mantissa bits; exponent field 0 holds the subnormals m/8 * 2^-6;
+ * S.1111.111 is NaN, so the largest finite magnitude is 1.75 * 2^8 = 448, and there are
+ * no infinities.  Rounding: the nearest finite code, ties to the even code ("satfinite":
+ * magnitudes beyond 448, infinities included, give 448).  The sign bit is the input's
+ * (so -0 and negative values rounding to zero give 0x80); NaN gives 0x7F | sign. */
+static double e4m3_value(int code) { /* magnitude of code 0..126 */
+    const int e = code >> 3, m = code & 7;
+    return e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+}
+
+uint8_t orc_f32_to_e4m3_satfinite(float f) {
+    const uint8_t sign = signbit(f) ? 0x80u : 0u;
+    if (isnan(f)) return (uint8_t)(sign | 0x7Fu);
+    const double a = fabs((double)f);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7Eu); /* the largest finite value is the nearest */
+    int best = 0;
+    double best_d = a;
+    for (int c = 1; c <= 126; ++c) {
+        const double d = fabs(e4m3_value(c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(sign | (uint8_t)best);
+}
+
+/* FP32 -> INT8: the nearest integer, ties to even, saturated to [-128, 127] (NaN: 0). */
+int8_t orc_f32_to_s8_rne_sat(float f) {
+    if (isnan(f)) return 0;
+    if (f >= 127.0f) return 127;
+    if (f <= -128.0f) return -128;
+    const double a = (double)f, r = floor(a), d = a - r;
+    double n = r;
+    if (d > 0.5 || (d == 0.5 && fmod(r, 2.0) != 0.0)) n = r + 1.0;
+    return (int8_t)n;
+}
+
 /* ===========================================================================
  * Entropy (DFloat11 Eq. (2); MINE section 3: H(P) lower-bounds the size).
  * ========================================================================= */
@@ -1031,6 +1070,24 @@ const uint64_t* orc_e8_counts_of(const orc_e8* e) { return &e->counts[0][0]; }
 const uint32_t* orc_e8_states(const orc_e8* e) { return e->states; }
 const uint32_t* orc_e8_offsets(const orc_e8* e) { return e->offsets; }
 uint16_t* orc_e8_payload_mut(orc_e8* e) { return e->payload; }
+
+/* The E8 reconstruction v = fp32(fp32(q) * g_i) * 0.5 with g_i = fp32(s * r_i), written
+ * in the requested dtype (EntroPack section 3.7: floating-point or integer output,
+ * FP8 and INT8 included): 0 = BF16 (u16 out, RNE), 1 = FP8 E4M3 (u8 out, RNE,
+ * saturating), 2 = INT8 (RNE, saturating). */
+void orc_e8_reconstruct_as(const int8_t* q, int64_t n_rows, int64_t k_cols, float s, const float* r, int dtype,
+                           void* out) {
+    for (int64_t i = 0; i < n_rows; ++i) {
+        const float g = s * r[i];
+        for (int64_t j = 0; j < k_cols; ++j) {
+            const float v = ((float)q[i * k_cols + j] * g) * 0.5f;
+            const int64_t at = i * k_cols + j;
+            if (dtype == 0) ((uint16_t*)out)[at] = orc_f32_to_bf16_rne(v);
+            else if (dtype == 1) ((uint8_t*)out)[at] = orc_f32_to_e4m3_satfinite(v);
+            else ((int8_t*)out)[at] = orc_f32_to_s8_rne_sat(v);
+        }
+    }
+}
 
 /* BF16 weights of doubled points q [n_rows, k_cols] (k_cols % 8 == 0): row i's
  * factor g_i = fp32(s * r_i), w = bf16(fp32(fp32(q) * g_i) * 0.5). */
