@@ -434,7 +434,14 @@ def extras(torch, ec, stream, device):
     out["e8_14336x4096_decode_in_gbs"] = round(st["device_bytes"] / us / 1e3, 1)
     out["e8_14336x4096_decode_hbm_gbs"] = round((st["device_bytes"] + 2 * n8 * k8) / us / 1e3, 1)
     out["e8_14336x4096_weights_per_s"] = float(f"{n8 * k8 / us * 1e6:.4g}")
-    del Es, ge, de, q2
+    d8 = torch.empty((n8, k8), dtype=torch.uint8, device=dev)
+
+    def e8f():
+        for E in Es:
+            ec.decode_as(E, d8, "e4m3")
+    gf = capture(torch, e8f, stream)
+    out["e8_14336x4096_decode_e4m3_us"] = round(t_loop(gf.replay, 20) / len(Es), 2)
+    del Es, ge, gf, de, d8, q2
 
     # 70B-shaped block: one batched decode of all seven matrices to BF16
     Ws, outs, comp, nw = [], [], 0, 0

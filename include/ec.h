@@ -121,6 +121,9 @@ typedef struct {
 
 enum { EC_KIND_HUFFMAN_BF16 = 1, EC_KIND_RANS_INT4 = 2, EC_KIND_E8 = 3 };
 
+/* Output dtypes of ec_decode_as. */
+enum { EC_DTYPE_BF16 = 0, EC_DTYPE_FP8_E4M3 = 1, EC_DTYPE_INT8 = 2 };
+
 /* Sizes and rates of one encoded matrix (ec_stats). */
 typedef struct {
     int32_t kind;
@@ -160,7 +163,8 @@ int ec_encode_rans(const int8_t* codes_host, const uint16_t* scales_f16_host, in
  * z_j = (q_j - c) / 2 in -16..15 and m = (z_8 - (z_1 + .. + z_7) mod 2) / 2 in -8..7,
  * with 17 frequency tables (c; each field under each coset) over independent rANS
  * tiles.  A decode (ec_decode / ec_decode_batch) writes bf16(fp32(q * fp32(s * r_i))
- * * 0.5).  Points outside that range or not in E8: EC_ERR_INVALID_ARG.  ec_gemv and
+ * * 0.5).  Points outside that range or not in E8, a non-finite scale, or a row whose
+ * fp32(s * r_i) is not finite: EC_ERR_INVALID_ARG.  ec_gemv and
  * ec_gemv_group on these matrices return EC_ERR_UNSUPPORTED (EntroPack decodes to a
  * dense matrix before its matrix products). */
 int ec_encode_e8(const int8_t* q2_host, const float* row_scales_host, float scale, int64_t n_rows, int64_t k_cols,
@@ -175,6 +179,17 @@ int ec_decode(const ec_matrix* W, uint16_t* out_bf16, cudaStream_t stream);
  * DFloat11 decompresses a whole transformer block at once (section
  * "Transformer-block-level decompression").  outs[m] is [n_rows(m), k_cols(m)]. */
 int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs, int count, cudaStream_t stream);
+
+/* Decode W into device memory `out` [n_rows, k_cols] in `dtype` (EntroPack section
+ * 3.7 and appendix B.1: the decoder writes floating-point or integer weights):
+ *  EC_DTYPE_BF16      uint16 BF16 bit patterns, as ec_decode;
+ *  EC_DTYPE_FP8_E4M3  uint8 OCP FP8 E4M3 codes of v = fp32(fp32(q) * fp32(s * r_i)) * 0.5,
+ *                     nearest with ties to even, magnitudes beyond 448 saturating to 448;
+ *  EC_DTYPE_INT8      int8 round-half-even of v, saturated to [-128, 127].
+ * FP8 and INT8 are for E8 matrices (EC_ERR_UNSUPPORTED for the other kinds).  out must
+ * be 16-byte aligned (EC_ERR_INVALID_ARG otherwise, or for an unknown dtype).  Async on
+ * `stream`; corruption found on the device is reported by ec_status. */
+int ec_decode_as(const ec_matrix* W, void* out, int dtype, cudaStream_t stream);
 
 /* y[b, i] = sum_j W[i, j] * x[b, j] for b < batch (1..EC_MAX_BATCH), with the weights
  * decoded in registers / shared memory and FP32 accumulation.  x: BF16 [batch,

@@ -37,7 +37,7 @@ EC_KIND_E8 = 3
 
 EXPORTS = ["ec_encode_bf16", "ec_encode_rans", "ec_decode", "ec_decode_batch", "ec_gemv", "ec_gemv_group",
            "ec_bf16_gemv", "ec_stats", "ec_code_lengths", "ec_serialize", "ec_deserialize", "ec_status", "ec_free",
-           "ec_strerror", "ec_gemv_static", "ec_gemv_path", "ec_encode_e8"]
+           "ec_strerror", "ec_gemv_static", "ec_gemv_path", "ec_encode_e8", "ec_decode_as"]
 
 
 class HuffParams(ctypes.Structure):
@@ -73,6 +73,7 @@ _sig = {
                      _i32),
     "ec_decode": ([_vp, _vp, _vp], _i32),
     "ec_decode_batch": ([_vp, _vp, _i32, _vp], _i32),
+    "ec_decode_as": ([_vp, _vp, _i32, _vp], _i32),
     "ec_gemv": ([_vp, _vp, _vp, _i32, _vp], _i32),
     "ec_gemv_group": ([_vp, _i32, _vp, _vp, _i32, _vp], _i32),
     "ec_bf16_gemv": ([_vp, _i64, _i64, _vp, _vp, _i32, _vp], _i32),
@@ -221,6 +222,15 @@ def deserialize(data: bytes, device: int = 0) -> Matrix:
 
 def decode(W: Matrix, out, stream=None) -> None:
     _check(lib.ec_decode(W.handle, _dev_ptr(out), _stream_ptr(stream)), "ec_decode")
+
+
+EC_DTYPE_BF16, EC_DTYPE_FP8_E4M3, EC_DTYPE_INT8 = 0, 1, 2
+_DTYPES = {"bf16": EC_DTYPE_BF16, "e4m3": EC_DTYPE_FP8_E4M3, "int8": EC_DTYPE_INT8}
+
+
+def decode_as(W: Matrix, out, dtype: str = "bf16", stream=None) -> None:
+    """ec_decode_as: decode into `out` as "bf16" (2 bytes), "e4m3" or "int8" (1 byte)."""
+    _check(lib.ec_decode_as(W.handle, _dev_ptr(out), _DTYPES[dtype], _stream_ptr(stream)), "ec_decode_as")
 
 
 def decode_batch(Ws, outs, stream=None) -> None:

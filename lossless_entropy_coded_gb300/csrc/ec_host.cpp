@@ -807,8 +807,8 @@ extern "C" int ec_encode_e8(const int8_t* q2, const float* row_scales, float sca
                 }
         });
         if (bad) return EC_ERR_INVALID_ARG;
-        for (int64_t r = 0; r < n_rows; ++r)
-            if (!std::isfinite(row_scales[r])) return EC_ERR_INVALID_ARG;
+        for (int64_t r = 0; r < n_rows; ++r) /* the decoder's row factor fp32(s * r_i) must be finite */
+            if (!std::isfinite(row_scales[r]) || !std::isfinite(scale * row_scales[r])) return EC_ERR_INVALID_ARG;
         ec_matrix* m = new_matrix();
         if (!m) return EC_ERR_OOM;
         uint64_t counts[EC_E8_TABLES][EC_E8_ALPHA] = {};

@@ -30,6 +30,7 @@
 #include <cuda.h> /* CUtensorMap and its encoder's signature (reached through the runtime) */
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -135,7 +136,7 @@ struct E8Mat {
     const uint32_t* fc;         /* 17 x 32: freq | cum << 16 */
     const uint8_t* slot_sym;    /* 17 x 2^prob_bits: slot -> symbol */
     const float* row_scales;    /* [n_rows] */
-    uint16_t* out;              /* [n_rows, k_cols] BF16 */
+    void* out;                  /* [n_rows, k_cols] BF16, FP8 E4M3 or INT8 */
     int64_t n_rows, k_cols, k_pad;
     int64_t n_tiles;
     int64_t records_bytes;
@@ -1481,11 +1482,42 @@ __device__ __forceinline__ uint32_t e8_ld_sym(uint32_t addr) {
 }
 __device__ __forceinline__ uint2 e8_ld_freq(uint32_t addr) {
     uint2 v;
-    asm("ld.shared.u16 %0, [%2];\n\tld.shared.u16 %1, [%2+%3];" : "=r"(v.x), "=r"(v.y) : "r"(addr), "n"(kE8FreqBytes));
+    asm("ld.shared.s16 %0, [%2];\n\tld.shared.u16 %1, [%2+%3];" : "=r"(v.x), "=r"(v.y) : "r"(addr), "n"(kE8FreqBytes));
     return v;
 }
 
-template <int PB>
+/* Bytes after the last tile buffer that a corrupt tile's refill reads may reach:
+ * the read position is checked once per vector (9 steps of at most 32 words). */
+constexpr uint32_t kE8Guard = 9 * 64;
+
+/* Eight reconstructed values v_i = fp32(q_i g) / 2 in the output dtype: 0 = BF16,
+ * 1 = FP8 E4M3 (nearest, ties to even, saturating), 2 = INT8 (same rounding). */
+template <int OUT>
+__device__ __forceinline__ void e8_store(void* out, int64_t at, const float (&v)[8]) {
+    if constexpr (OUT == 0) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+            w[i] = *(const uint32_t*)&h;
+        }
+        *(uint4*)((uint16_t*)out + at) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else if constexpr (OUT == 1) {
+        uint32_t h[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            h[i] = __nv_cvt_float2_to_fp8x2(make_float2(v[2 * i], v[2 * i + 1]), __NV_SATFINITE, __NV_E4M3);
+        *(uint2*)((uint8_t*)out + at) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+    } else {
+        uint32_t b[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) b[i] = (uint32_t)min(127, max(-128, __float2int_rn(v[i]))) & 0xFFu;
+        *(uint2*)((uint8_t*)out + at) =
+            make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+    }
+}
+
+template <int PB, int OUT>
 __global__ void __launch_bounds__(kMaxHW * 32, 1) e8_kernel(const __grid_constant__ E8Args a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const E8Mat& M = a.m;
@@ -1498,7 +1530,6 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) e8_kernel(const __grid_constan
     const uint32_t buf_bytes = (uint32_t)rans_buf_bytes(M.words_cap);
     const uint32_t bufs = base + (uint32_t)e8_table_bytes(PB) + (uint32_t)(warp * a.nbuf) * buf_bytes;
     const bool dbl = a.nbuf == 2;
-    const uint32_t cap = (buf_bytes - 128) / 2 - 1;
     const int64_t T = 32 * (int64_t)M.steps; /* vectors per tile */
     const int64_t vpr = M.k_pad / 8, K = M.k_cols;
 
@@ -1512,11 +1543,12 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) e8_kernel(const __grid_constan
         const uint4* s2 = (const uint4*)M.slot_sym;
         uint4* d2 = (uint4*)ss;
         for (uint32_t i = threadIdx.x; i < EC_E8_TABLES * kSlots / 16; i += blockDim.x) d2[i] = __ldg(s2 + i);
-        uint16_t* fq = (uint16_t*)(ss + EC_E8_TABLES * kSlots);
+        /* per table and symbol: f - 2^PB (so that x' = x + (x >> PB)(f - 2^PB) - start) and the start */
+        int16_t* fq = (int16_t*)(ss + EC_E8_TABLES * kSlots);
         for (uint32_t i = threadIdx.x; i < EC_E8_TABLES * EC_E8_ALPHA; i += blockDim.x) {
             const uint32_t e = __ldg(M.fc + i);
-            fq[i] = (uint16_t)(e & 0xFFFFu);
-            fq[EC_E8_TABLES * EC_E8_ALPHA + i] = (uint16_t)(e >> 16);
+            fq[i] = (int16_t)((int32_t)(e & 0xFFFFu) - (int32_t)kSlots);
+            fq[EC_E8_TABLES * EC_E8_ALPHA + i] = (int16_t)(e >> 16);
         }
     }
     grid_dep_launch();
@@ -1544,29 +1576,31 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) e8_kernel(const __grid_constan
         if (cur.words < 0) {
             if (lane == 0) flag_corrupt(a.status);
         } else {
-            const uint8_t* bp = smem + (cb - base);
-            uint32_t x = ((const uint32_t*)bp)[lane];
-            const uint16_t* words = (const uint16_t*)(bp + 128);
-            uint32_t wp = 0;
+            uint32_t x = ((const uint32_t*)(smem + (cb - base)))[lane];
+            const uint32_t w0 = cb + 128, wlim = w0 + 2 * (uint32_t)M.words_cap;
+            uint32_t wa = w0; /* shared address of the next unread payload word */
             const int64_t v0 = t * T + lane;
             int64_t row = v0 / vpr;
             int64_t cv = v0 - row * vpr; /* this lane's vector column */
             float g = __fmul_rn(M.scale, __ldg(M.row_scales + row));
+            bool bad = false;
             /* one symbol: tab = the table's 2^PB-aligned slot base, fq = its frequency row */
             auto step = [&](uint32_t tab, uint32_t fq) {
-                const uint32_t slot = x & kMask;
-                const uint32_t sym = e8_ld_sym(tab | slot);
-                const uint2 fc = e8_ld_freq(fq + 2 * sym);
-                x = fc.x * (x >> PB) + slot - fc.y;
+                const uint32_t sym = e8_ld_sym(tab | (x & kMask));
+                const uint2 fc = e8_ld_freq(fq + 2 * sym); /* (f - 2^PB) sign-extended, start */
+                x = (x >> PB) * fc.x + (x - fc.y);
                 const bool need = x < 65536u;
                 const uint32_t bal = __ballot_sync(kFull, need);
-                const uint32_t idx = min(wp + __popc(bal & lt), cap);
-                const uint32_t v = words[idx];
+                const uint32_t v = lds16(wa + 2 * __popc(bal & lt));
                 x = need ? (x << 16) | v : x;
-                wp += __popc(bal);
+                wa += 2 * __popc(bal);
                 return sym;
             };
             for (int j = 0; j < cur.S; ++j) {
+                if (wa > wlim) { /* warp-uniform: only a corrupt tile reads past its words */
+                    bad = true;
+                    break;
+                }
                 const uint32_t c = step(ss_s, fq_s) & 1u;
                 const uint32_t tab = ss_s + ((1u + 8u * c) << PB), fq = fq_s + (1u + 8u * c) * 2u * EC_E8_ALPHA;
                 uint32_t s[8];
@@ -1578,28 +1612,19 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) e8_kernel(const __grid_constan
 #pragma unroll
                 for (int f = 0; f < 7; ++f) q[f] = 2 * (int)s[f] - 32 + (int)c;
                 q[7] = 4 * (int)s[7] - 64 + 2 * (int)par + (int)c;
-                uint32_t w[4];
+                float v[8];
                 /* fl(fl(q g) / 2) == fl(q (g / 2)) while g / 2 is normal and q g finite
                  * (|q| <= 32): one rounding either way; otherwise both multiplies */
                 const float ag = fabsf(g);
                 if (ag >= 0x1p-125f && ag <= 0x1p120f) {
                     const float gh = g * 0.5f;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__int2float_rn(q[2 * i]), gh),
-                                                                       __fmul_rn(__int2float_rn(q[2 * i + 1]), gh));
-                        w[i] = *(const uint32_t*)&h;
-                    }
+                    for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(__int2float_rn(q[i]), gh);
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const __nv_bfloat162 h = __floats2bfloat162_rn(
-                            __fmul_rn(__fmul_rn(__int2float_rn(q[2 * i]), g), 0.5f),
-                            __fmul_rn(__fmul_rn(__int2float_rn(q[2 * i + 1]), g), 0.5f));
-                        w[i] = *(const uint32_t*)&h;
-                    }
+                    for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(__fmul_rn(__int2float_rn(q[i]), g), 0.5f);
                 }
-                if (8 * cv < K) *(uint4*)(M.out + row * K + 8 * cv) = make_uint4(w[0], w[1], w[2], w[3]);
+                if (8 * cv < K) e8_store<OUT>(M.out, row * K + 8 * cv, v);
                 cv += 32;
                 if (cv >= vpr) {
                     cv -= vpr;
@@ -1608,7 +1633,8 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) e8_kernel(const __grid_constan
                 }
             }
             /* every lane returns to 2^16 and the words are used up (up to 7 padding words) */
-            if (__any_sync(kFull, x != 65536u) || wp > (uint32_t)cur.words || (uint32_t)cur.words - wp > 7) {
+            const uint32_t used = (wa - w0) / 2;
+            if (bad || __any_sync(kFull, x != 65536u) || used > (uint32_t)cur.words || (uint32_t)cur.words - used > 7) {
                 if (lane == 0) flag_corrupt(a.status);
             }
         }
@@ -2195,31 +2221,41 @@ E8Plan e8_plan(size_t tables, size_t buf, int64_t n_tiles, const DeviceInfo* d) 
     return {warps, nbuf};
 }
 
-template <int PB>
+template <int PB, int OUT>
 int e8_launch(E8Args a, int64_t n_tiles, cudaStream_t s, DeviceInfo* d) {
     const size_t tables = e8_table_bytes(PB), buf = rans_buf_bytes(a.m.words_cap);
-    if (tables + buf > d->smem_optin) return EC_ERR_UNSUPPORTED; /* not for tiles of <= 1024 vectors */
-    const E8Plan p = e8_plan(tables, buf, n_tiles, d);
+    if (tables + buf + kE8Guard > d->smem_optin) return EC_ERR_UNSUPPORTED; /* not for tiles of <= 1024 vectors */
+    const E8Plan p = e8_plan(tables + kE8Guard, buf, n_tiles, d);
     a.nbuf = p.nbuf;
-    const size_t smem = tables + (size_t)(p.warps * p.nbuf) * buf;
-    if (set_smem(e8_kernel<PB>, smem) != EC_OK) return EC_ERR_CUDA;
+    const size_t smem = tables + (size_t)(p.warps * p.nbuf) * buf + kE8Guard;
+    if (set_smem(e8_kernel<PB, OUT>, smem) != EC_OK) return EC_ERR_CUDA;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(d->sms, (n_tiles + p.warps - 1) / p.warps));
-    return launch_ex(e8_kernel<PB>, grid, p.warps * 32, smem, s, a);
+    return launch_ex(e8_kernel<PB, OUT>, grid, p.warps * 32, smem, s, a);
 }
 
-int e8_run(const ec_matrix* W, uint16_t* out, cudaStream_t s, DeviceInfo* d) {
+template <int OUT>
+int e8_launch_pb(const E8Args& a, int64_t nt, cudaStream_t s, DeviceInfo* d) {
+    switch (a.m.prob_bits) {
+        case 9: return e8_launch<9, OUT>(a, nt, s, d);
+        case 10: return e8_launch<10, OUT>(a, nt, s, d);
+        case 11: return e8_launch<11, OUT>(a, nt, s, d);
+        case 12: return e8_launch<12, OUT>(a, nt, s, d);
+        default: return EC_ERR_CORRUPT;
+    }
+}
+
+int e8_run(const ec_matrix* W, void* out, int dtype, cudaStream_t s, DeviceInfo* d) {
     E8Args a{};
     a.m = e8_desc(W);
     a.m.out = out;
     a.status = d->status;
     const int64_t nt = W->hdr.n_tiles;
     if (nt == 0) return EC_OK;
-    switch (a.m.prob_bits) {
-        case 9: return e8_launch<9>(a, nt, s, d);
-        case 10: return e8_launch<10>(a, nt, s, d);
-        case 11: return e8_launch<11>(a, nt, s, d);
-        case 12: return e8_launch<12>(a, nt, s, d);
-        default: return EC_ERR_CORRUPT;
+    switch (dtype) {
+        case EC_DTYPE_BF16: return e8_launch_pb<0>(a, nt, s, d);
+        case EC_DTYPE_FP8_E4M3: return e8_launch_pb<1>(a, nt, s, d);
+        case EC_DTYPE_INT8: return e8_launch_pb<2>(a, nt, s, d);
+        default: return EC_ERR_INVALID_ARG;
     }
 }
 /* ---- E8 decode: end ---- */
@@ -2343,7 +2379,7 @@ extern "C" int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs
             continue;
         }
         if (Ws[k]->kind == EC_KIND_E8) {
-            if ((rc = e8_run(Ws[k], outs[k], stream, d)) != EC_OK) return rc;
+            if ((rc = e8_run(Ws[k], outs[k], EC_DTYPE_BF16, stream, d)) != EC_OK) return rc;
             continue;
         }
         HuffMat m = huff_desc(Ws[k]);
@@ -2371,6 +2407,24 @@ extern "C" int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs
 
 extern "C" int ec_decode(const ec_matrix* W, uint16_t* out, cudaStream_t stream) {
     return ec_decode_batch(&W, &out, 1, stream);
+}
+
+extern "C" int ec_decode_as(const ec_matrix* W, void* out, int dtype, cudaStream_t stream) {
+    if (!W || !W->d_blob) return EC_ERR_INVALID_ARG;
+    if (dtype != EC_DTYPE_BF16 && dtype != EC_DTYPE_FP8_E4M3 && dtype != EC_DTYPE_INT8) return EC_ERR_INVALID_ARG;
+    if (W->kind != EC_KIND_E8) {
+        if (dtype != EC_DTYPE_BF16) return EC_ERR_UNSUPPORTED;
+        uint16_t* o = (uint16_t*)out;
+        return ec_decode_batch(&W, &o, 1, stream);
+    }
+    int dev = 0;
+    if (current_device(&dev) != EC_OK) return EC_ERR_CUDA;
+    DeviceInfo* d = nullptr;
+    int rc = device_info(dev, &d);
+    if (rc != EC_OK) return rc;
+    if ((rc = check_matrix(W, dev)) != EC_OK) return rc;
+    if (W->hdr.n_rows * W->hdr.k_cols > 0 && (!out || !aligned16(out))) return EC_ERR_INVALID_ARG;
+    return e8_run(W, out, dtype, stream, d);
 }
 
 extern "C" int ec_bf16_gemv(const uint16_t* w, int64_t n_rows, int64_t k_cols, const uint16_t* x, float* y, int batch,

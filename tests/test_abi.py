@@ -555,6 +555,8 @@ def test_e8_argument_validation(ec):
     assert enc(q2, 4, 256, scale=float("inf")) == _ec.EC_ERR_INVALID_ARG
     bad_r = r.copy(); bad_r[2] = np.nan
     assert enc(q2, 4, 256, rs=bad_r) == _ec.EC_ERR_INVALID_ARG
+    big_r = r.copy(); big_r[1] = 3e38  # finite, but s * r_1 overflows FP32
+    assert enc(q2, 4, 256, scale=4.0, rs=big_r) == _ec.EC_ERR_INVALID_ARG
     for v, why in [([1, 1, 1, 1, 1, 1, 1, -1], "odd number of -1 in the odd coset"),
                    ([2, 0, 0, 0, 0, 0, 0, 0], "odd sum in D8"), ([1, 0, 0, 0, 0, 0, 0, 1], "mixed parity"),
                    ([32, 0, 0, 0, 0, 0, 0, 0], "z_1 = 16 out of range"),
@@ -600,6 +602,14 @@ def test_e8_rejects_structural_corruption(ec):
         with pytest.raises(ec.EcError) as e:
             ec.deserialize(bad, device=-1)
         assert e.value.code == -5, name
+
+
+def test_decode_as_argument_checks(ec):
+    from lossless_entropy_coded_gb300 import _ec
+    assert _ec.lib.ec_decode_as(None, None, 0, None) == _ec.EC_ERR_INVALID_ARG
+    q2, r, s = synth.make_e8_case(31, 8, 256)
+    W = ec.encode_e8(q2, r, s, device=-1)  # host-only: no device blob
+    assert _ec.lib.ec_decode_as(W.handle, None, 1, None) == _ec.EC_ERR_INVALID_ARG
 
 
 def test_e8_matrices_have_no_gemv(ec):

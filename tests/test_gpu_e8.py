@@ -75,6 +75,42 @@ def test_extreme_row_scales(ec):
     assert np.array_equal(got, O.e8_reconstruct_bf16(q2, 1.0, r))
 
 
+@pytest.mark.parametrize("dtype", ["e4m3", "int8", "bf16"])
+@pytest.mark.parametrize("shape,tile,scale", [((7, 264), 64, 0.125), ((40, 1024), 512, 64.0), ((33, 776), 96, 2000.0),
+                                              ((300, 4096), 1024, 400.0)])
+def test_decode_as_dtype(ec, dtype, shape, tile, scale):
+    """FP8 E4M3 and INT8 output (and BF16 through the same entry point), bit-exact
+    with the oracle: scales from E4M3 subnormals up to saturation, INT8 up to its
+    clamp."""
+    q2, r, _ = synth.make_e8_case(7300 + shape[0], *shape)
+    W = ec.encode_e8(q2, r, scale, tile_vectors=tile)
+    tdt = torch.int16 if dtype == "bf16" else torch.uint8 if dtype == "e4m3" else torch.int8
+    out = torch.full(shape, 0x55, dtype=tdt, device="cuda")
+    ec.decode_as(W, out, dtype)
+    assert ec.status() == 0
+    got = out.cpu().numpy()
+    want = O.e8_reconstruct(q2, scale, r, dtype)
+    assert np.array_equal(got.view(want.dtype), want)
+
+
+def test_decode_as_refusals(ec):
+    w = synth.llama_bf16(7400, 16, 512)
+    H = ec.encode_bf16(w)
+    out8 = torch.zeros((16, 512), dtype=torch.uint8, device="cuda")
+    with pytest.raises(ec.EcError) as e:
+        ec.decode_as(H, out8, "e4m3")
+    assert e.value.code == -4
+    out16 = torch.zeros((16, 512), dtype=torch.int16, device="cuda")
+    ec.decode_as(H, out16, "bf16")
+    assert ec.status() == 0 and np.array_equal(out16.cpu().numpy().view(np.uint16), w)
+    q2, r, s = synth.make_e8_case(7401, 16, 512)
+    E = ec.encode_e8(q2, r, s)
+    big = torch.zeros(16 * 512 + 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ec.EcError) as e:
+        ec.decode_as(E, big[1:], "int8")  # not 16-byte aligned
+    assert e.value.code == -1
+
+
 @pytest.mark.parametrize("shape", [(14336, 4096), (4096, 14336)])
 def test_full_size_config(ec, shape):
     """Llama-3.1-8B gate/up and down shapes at about 4 bits per weight: the whole
