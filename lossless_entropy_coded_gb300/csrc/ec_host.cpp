@@ -1097,6 +1097,9 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
                 c += f;
             }
             if (c != M && c != 0) return EC_ERR_CORRUPT;
+            if (t == 0 && c != M && n_pad > 0) return EC_ERR_CORRUPT; /* every point has a coset */
+            for (int s = 2; t == 0 && s < EC_E8_ALPHA; ++s) /* the coset is 0 or 1 */
+                if (tab[s] & 0xFFFFu) return EC_ERR_CORRUPT;
             for (uint32_t q = c; q < M; ++q) /* an unused table maps every slot to symbol 0 */
                 if (ss[(size_t)t * M + q] != 0) return EC_ERR_CORRUPT;
         }

@@ -1559,6 +1559,7 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) e8_kernel(const __grid_constan
     uint2 off_next = gw + nw < M.n_tiles ? make_uint2(__ldg(M.tile_off + gw + nw), __ldg(M.tile_off + gw + nw + 1))
                                          : make_uint2(0u, 0u);
     const uint32_t lt = (1u << lane) - 1u;
+    const uint32_t f0 = __ldg(M.fc) & 0xFFFFu, nf0 = f0 - kSlots, nf1 = (__ldg(M.fc + 1) & 0xFFFFu) - kSlots;
     uint32_t cb = bufs;
     for (int64_t t = gw; t < M.n_tiles; t += nw) {
         cp_async_wait_all();
@@ -1584,16 +1585,21 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) e8_kernel(const __grid_constan
             int64_t cv = v0 - row * vpr; /* this lane's vector column */
             float g = __fmul_rn(M.scale, __ldg(M.row_scales + row));
             bool bad = false;
-            /* one symbol: tab = the table's 2^PB-aligned slot base, fq = its frequency row */
-            auto step = [&](uint32_t tab, uint32_t fq) {
-                const uint32_t sym = e8_ld_sym(tab | (x & kMask));
-                const uint2 fc = e8_ld_freq(fq + 2 * sym); /* (f - 2^PB) sign-extended, start */
-                x = (x >> PB) * fc.x + (x - fc.y);
+            /* the refill after a symbol: lanes whose state fell below 2^16 take the next
+             * words in lane order */
+            auto refill = [&]() {
                 const bool need = x < 65536u;
                 const uint32_t bal = __ballot_sync(kFull, need);
                 const uint32_t v = lds16(wa + 2 * __popc(bal & lt));
                 x = need ? (x << 16) | v : x;
                 wa += 2 * __popc(bal);
+            };
+            /* one symbol: tab = the table's 2^PB-aligned slot base, fq = its frequency row */
+            auto step = [&](uint32_t tab, uint32_t fq) {
+                const uint32_t sym = e8_ld_sym(tab | (x & kMask));
+                const uint2 fc = e8_ld_freq(fq + 2 * sym); /* (f - 2^PB) sign-extended, start */
+                x = (x >> PB) * fc.x + (x - fc.y);
+                refill();
                 return sym;
             };
             for (int j = 0; j < cur.S; ++j) {
@@ -1601,7 +1607,11 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) e8_kernel(const __grid_constan
                     bad = true;
                     break;
                 }
-                const uint32_t c = step(ss_s, fq_s) & 1u;
+                /* the coset: table 0 holds symbols 0 and 1 only, so the slot's side of
+                 * start(1) = f(0) decides it, with no table lookup */
+                const uint32_t c = (x & kMask) >= f0 ? 1u : 0u;
+                x = (x >> PB) * (c ? nf1 : nf0) + (x - (c ? f0 : 0u));
+                refill();
                 const uint32_t tab = ss_s + ((1u + 8u * c) << PB), fq = fq_s + (1u + 8u * c) * 2u * EC_E8_ALPHA;
                 uint32_t s[8];
 #pragma unroll

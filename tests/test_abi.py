@@ -598,6 +598,15 @@ def test_e8_rejects_structural_corruption(ec):
     if unused:
         x = bytearray(blob); struct.pack_into("<B", x, ss0 + unused[0] * M + 3, 7)
         cases.append(("unused table slot", bytes(x)))
+    # a consistent coset table with a third symbol: one slot moved from symbol 1 to 2
+    f0, f1 = int(fc[0, 0] & 0xFFFF), int(fc[0, 1] & 0xFFFF)
+    x = bytearray(blob)
+    struct.pack_into("<I", x, meta + h["table_off"] + 4, (f1 - 1) | (f0 << 16))
+    struct.pack_into("<I", x, meta + h["table_off"] + 8, 1 | ((M - 1) << 16))
+    for s in range(3, 32):
+        struct.pack_into("<I", x, meta + h["table_off"] + 4 * s, M << 16)
+    struct.pack_into("<B", x, ss0 + M - 1, 2)
+    cases.append(("third coset", bytes(x)))
     for name, bad in cases:
         with pytest.raises(ec.EcError) as e:
             ec.deserialize(bad, device=-1)
