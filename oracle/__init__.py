@@ -16,6 +16,8 @@ Functions and the passages they follow (page titles and sections):
   rans_table_bits               MINE sec. 4.2 "Launch" (table size by the cross-entropy bound)
   e8_fields / e8_point / E8     EntroPack sec. 3.2, 3.3, 3.6, 3.7, appendix A.3 (E8 fields, 17 tables)
   e8_reconstruct_bf16           EntroPack sec. 3.7 (lattice point x shared scale x row scale)
+  Fp8 / fp8_table / e4m3_to_f32 MINE sec. 4 "Escapes" (top-t table, sparse correction records)
+  fp8_dequant_bf16 / gemv_fp8   FP8 E4M3 weights with FP32 row scales
   e8_reconstruct / f32_to_e4m3 / f32_to_s8
                                 EntroPack sec. 3.7 and appendix B.1 (FP8 / INT8 output); the OCP
                                 FP8 E4M3 format
@@ -110,6 +112,22 @@ def _L():
         "orc_e8_reconstruct_as": ([vp, i64, i64, ctypes.c_float, vp, i32, vp], None),
         "orc_f32_to_e4m3_satfinite": ([ctypes.c_float], ctypes.c_uint8),
         "orc_f32_to_s8_rne_sat": ([ctypes.c_float], ctypes.c_int8),
+        "orc_e4m3_to_f32": ([ctypes.c_uint8], ctypes.c_float),
+        "orc_fp8_table": ([vp, i32, vp], i32),
+        "orc_fp8_encode": ([vp, i64, i32, i32, i32], vp),
+        "orc_fp8_decode": ([vp, vp], i32),
+        "orc_fp8_free": ([vp], None),
+        "orc_fp8_info": ([vp, vp], i64),
+        "orc_fp8_table_of": ([vp], vp),
+        "orc_fp8_freqs_of": ([vp], vp),
+        "orc_fp8_counts_of": ([vp], vp),
+        "orc_fp8_states": ([vp], vp),
+        "orc_fp8_offsets": ([vp], vp),
+        "orc_fp8_payload_mut": ([vp], vp),
+        "orc_fp8_rec_off": ([vp], vp),
+        "orc_fp8_records": ([vp], vp),
+        "orc_fp8_dequant_bf16": ([vp, vp, i64, i64, vp], None),
+        "orc_gemv_fp8": ([vp, vp, i64, i64, vp, i32, vp, i64, vp, vp], None),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -475,6 +493,106 @@ def f32_to_s8(values) -> np.ndarray:
     """INT8 of FP32 values: nearest integer, ties to even, saturated to [-128, 127]."""
     v = np.asarray(values, dtype=np.float32).ravel()
     return np.array([_L().orc_f32_to_s8_rne_sat(float(a)) for a in v], dtype=np.int8)
+
+
+def e4m3_to_f32(codes) -> np.ndarray:
+    """FP32 values of FP8 E4M3 codes (NaN for S.1111.111)."""
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([_L().orc_e4m3_to_f32(int(v)) for v in c], dtype=np.float32)
+
+
+def fp8_table(counts, t: int) -> np.ndarray:
+    """The top-t table of a 256-bin code histogram: code 0 and the t - 1 most
+    frequent other present codes (ties to the lower code), ascending."""
+    cnt = np.ascontiguousarray(counts, dtype=np.uint64)
+    out = np.zeros(256, dtype=np.uint8)
+    n = _L().orc_fp8_table(_p(cnt), t, _p(out))
+    return out[:n].copy()
+
+
+class Fp8:
+    """FP8 codes of the padded layout (flattened) under a top-t table: the symbol
+    stream through the tile codec plus per-tile correction records."""
+
+    def __init__(self, codes: np.ndarray, t: int = 256, prob_bits: int = 12, tile: int = 4096):
+        c = np.ascontiguousarray(codes, dtype=np.uint8).ravel()
+        h = _L().orc_fp8_encode(_p(c) if c.size else 0, c.size, t, prob_bits, tile)
+        if not h:
+            raise ValueError("FP8 encode failed")
+        self._h = h
+        self.prob_bits = prob_bits
+        info = np.zeros(6, dtype=np.int64)
+        _L().orc_fp8_info(h, _p(info))
+        self.n, self.n_tiles, self.payload_words, self.tile, self.tsize, self.n_records = (int(v) for v in info)
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            _L().orc_fp8_free(self._h)
+            self._h = None
+
+    @property
+    def table(self):
+        return _view(_L().orc_fp8_table_of(self._h), np.uint8, self.tsize)
+
+    @property
+    def freqs(self):
+        return _view(_L().orc_fp8_freqs_of(self._h), np.uint32, self.tsize)
+
+    @property
+    def counts(self):
+        return _view(_L().orc_fp8_counts_of(self._h), np.uint64, self.tsize)
+
+    @property
+    def states(self):
+        return _view(_L().orc_fp8_states(self._h), np.uint32, 32 * self.n_tiles).reshape(self.n_tiles, 32)
+
+    @property
+    def offsets(self):
+        return _view(_L().orc_fp8_offsets(self._h), np.uint32, self.n_tiles + 1)
+
+    @property
+    def rec_off(self):
+        return _view(_L().orc_fp8_rec_off(self._h), np.uint32, self.n_tiles + 1)
+
+    @property
+    def records(self):
+        return _view(_L().orc_fp8_records(self._h), np.uint32, max(1, self.n_records))[: self.n_records]
+
+    def payload(self) -> np.ndarray:
+        return np.ctypeslib.as_array((ctypes.c_uint16 * max(1, self.payload_words)).from_address(
+            _L().orc_fp8_payload_mut(self._h)))[: self.payload_words].copy()
+
+    def flip_payload_bit(self, word: int, bit: int) -> None:
+        w = ctypes.c_uint16.from_address(_L().orc_fp8_payload_mut(self._h) + 2 * word)
+        w.value ^= 1 << bit
+
+    def decode(self):
+        out = np.zeros(max(1, self.n), dtype=np.uint8)
+        rc = _L().orc_fp8_decode(self._h, _p(out))
+        return out[: self.n], rc
+
+
+def fp8_dequant_bf16(codes: np.ndarray, row_scales: np.ndarray) -> np.ndarray:
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    r = np.ascontiguousarray(row_scales, dtype=np.float32)
+    n, k = c.shape
+    out = np.zeros((n, k), dtype=np.uint16)
+    _L().orc_fp8_dequant_bf16(_p(c), _p(r), n, k, _p(out))
+    return out
+
+
+def gemv_fp8(codes: np.ndarray, row_scales: np.ndarray, x: np.ndarray, rows=None):
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    s = np.ascontiguousarray(row_scales, dtype=np.float32)
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.uint16)
+    n, k = c.shape
+    batch = x.shape[0]
+    r, nsel = _rows_arg(rows)
+    nr = nsel if r is not None else n
+    y = np.zeros((batch, nr), dtype=np.float64)
+    a = np.zeros((batch, nr), dtype=np.float64)
+    _L().orc_gemv_fp8(_p(c), _p(s), n, k, _p(x), batch, _p(r) if r is not None else None, nsel, _p(y), _p(a))
+    return y, a
 
 
 def rans_dequant_bf16(codes: np.ndarray, scales: np.ndarray, group: int = 128) -> np.ndarray:

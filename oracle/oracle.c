@@ -861,6 +861,244 @@ void orc_gemv_rans(const int8_t* codes, const uint16_t* scales, int64_t n_rows, 
 }
 
 /* ===========================================================================
+ * FP8 weights with a top-t decoding table and a sparse correction stream (MINE
+ * section 4, "Escapes": the table keeps the t most frequent codes, always with
+ * 0; any other value is coded as 0 and its true value goes to a correction
+ * stream of one 32-bit record per escape).
+ *
+ * Readings (the pages fix the idea, not the record layout for this tile format):
+ *  - codes are OCP FP8 E4M3 bytes; weight = fp32(value(code)) * r_i with an FP32
+ *    scale per row; rows are padded to a multiple of 128 columns with code 0;
+ *  - the table is code 0x00 and the t - 1 most frequent other codes present in
+ *    the padded matrix (ties to the lower code), sorted by code; a symbol is a
+ *    code's rank in it; a code outside the table is coded as symbol 0 (code 0x00);
+ *  - symbols go through the tile codec above (one symbol per position, tiles of
+ *    `tile` positions, position 32 j + l of a tile is lane l's step j);
+ *  - tile t's records list its escapes by ascending position p: record =
+ *    p | code << 16; rec_off[t] .. rec_off[t + 1] index them.
+ * ========================================================================= */
+
+/* Value of an E4M3 code: sign, 4 exponent bits (bias 7), 3 mantissa bits;
+ * exponent field 0 holds the subnormals m/8 * 2^-6; S.1111.111 is NaN. */
+float orc_e4m3_to_f32(uint8_t code) {
+    const int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return (float)(s ? -v : v);
+}
+
+/* The top-t table of a code histogram: fills table[] (ascending codes) and
+ * returns its size (<= t; t >= 1). */
+int orc_fp8_table(const uint64_t counts[256], int t, uint8_t* table) {
+    int chosen[256] = {0};
+    chosen[0] = 1;
+    int size = 1;
+    while (size < t) {
+        int best = -1;
+        for (int c = 1; c < 256; ++c)
+            if (!chosen[c] && counts[c] && (best < 0 || counts[c] > counts[best])) best = c;
+        if (best < 0) break;
+        chosen[best] = 1;
+        ++size;
+    }
+    int n = 0;
+    for (int c = 0; c < 256; ++c)
+        if (chosen[c]) table[n++] = (uint8_t)c;
+    return n;
+}
+
+typedef struct {
+    int64_t n;                 /* positions (the padded layout, flattened) */
+    int tsize;
+    uint8_t table[256];
+    int16_t rank[256];         /* code -> symbol, -1 outside the table */
+    orc_rans* rans;            /* the symbol stream */
+    uint32_t* rec_off;         /* n_tiles + 1 */
+    uint32_t* records;
+    int64_t n_records;
+} orc_fp8;
+
+void orc_fp8_free(orc_fp8* f) {
+    if (!f) return;
+    orc_rans_free(f->rans);
+    free(f->rec_off);
+    free(f->records);
+    free(f);
+}
+
+/* Tile codec over a symbol array: as orc_rans_encode_k with k = 1, but the
+ * symbols 0..nsym-1 are given (nsym <= 256). */
+static orc_rans* rans_encode_symbols(const uint8_t* sym, int64_t n, int nsym, int prob_bits, int tile) {
+    if (n < 0 || prob_bits < 5 || prob_bits > 15 || tile < 32 || tile % 32 || nsym < 1 || nsym > 256) return NULL;
+    orc_rans* r = (orc_rans*)calloc(1, sizeof(orc_rans));
+    r->n = n;
+    r->prob_bits = prob_bits;
+    r->tile = tile;
+    r->k = 1;
+    r->nsym = nsym;
+    for (int64_t i = 0; i < n; ++i) r->counts[sym[i]]++;
+    if (orc_rans_freqs_n(r->counts, nsym, prob_bits, r->freqs) < 0) {
+        orc_rans_free(r);
+        return NULL;
+    }
+    for (int s = 0, c = 0; s < nsym; ++s) {
+        r->cum[s] = (uint32_t)c;
+        c += (int)r->freqs[s];
+    }
+    r->n_tiles = (n + tile - 1) / tile;
+    r->states = (uint32_t*)malloc(sizeof(uint32_t) * 32 * (size_t)(r->n_tiles > 0 ? r->n_tiles : 1));
+    r->offsets = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)(r->n_tiles + 1));
+    r->payload = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(n > 0 ? n : 1));
+    uint16_t* stack = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)tile);
+    const uint64_t unit = (uint64_t)1 << (32 - prob_bits);
+    int64_t words = 0;
+    for (int64_t t = 0; t < r->n_tiles; ++t) {
+        const int64_t base = t * tile, n_t = (n - base < tile) ? n - base : tile;
+        uint64_t x[32];
+        for (int l = 0; l < 32; ++l) x[l] = 1u << 16;
+        int64_t sp = 0;
+        for (int64_t m = (n_t + 31) / 32 - 1; m >= 0; --m)
+            for (int l = 31; l >= 0; --l) {
+                if (32 * m + l >= n_t) continue;
+                const int s = sym[base + 32 * m + l];
+                const uint64_t f = r->freqs[s];
+                while (x[l] >= f * unit) {
+                    stack[sp++] = (uint16_t)(x[l] & 0xFFFF);
+                    x[l] >>= 16;
+                }
+                x[l] = (x[l] / f << prob_bits) + (x[l] % f) + r->cum[s];
+            }
+        for (int l = 0; l < 32; ++l) r->states[t * 32 + l] = (uint32_t)x[l];
+        r->offsets[t] = (uint32_t)words;
+        while (sp > 0) r->payload[words++] = stack[--sp];
+    }
+    r->offsets[r->n_tiles] = (uint32_t)words;
+    r->payload_words = words;
+    free(stack);
+    return r;
+}
+
+/* Encode the padded FP8 layout codes[n] with a table of at most t codes. */
+orc_fp8* orc_fp8_encode(const uint8_t* codes, int64_t n, int t, int prob_bits, int tile) {
+    if (n < 0 || t < 1 || t > 256) return NULL;
+    for (int64_t i = 0; i < n; ++i)
+        if ((codes[i] & 0x7F) == 0x7F) return NULL; /* NaN */
+    orc_fp8* f = (orc_fp8*)calloc(1, sizeof(orc_fp8));
+    f->n = n;
+    uint64_t counts[256] = {0};
+    for (int64_t i = 0; i < n; ++i) counts[codes[i]]++;
+    f->tsize = orc_fp8_table(counts, t, f->table);
+    for (int c = 0; c < 256; ++c) f->rank[c] = -1;
+    for (int s = 0; s < f->tsize; ++s) f->rank[f->table[s]] = (int16_t)s;
+    uint8_t* sym = (uint8_t*)malloc((size_t)(n > 0 ? n : 1));
+    for (int64_t i = 0; i < n; ++i) sym[i] = f->rank[codes[i]] >= 0 ? (uint8_t)f->rank[codes[i]] : 0;
+    f->rans = rans_encode_symbols(sym, n, f->tsize, prob_bits, tile);
+    free(sym);
+    if (!f->rans) {
+        orc_fp8_free(f);
+        return NULL;
+    }
+    const int64_t nt = f->rans->n_tiles;
+    f->rec_off = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)(nt + 1));
+    int64_t ne = 0;
+    for (int64_t i = 0; i < n; ++i) ne += f->rank[codes[i]] < 0;
+    f->records = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)(ne > 0 ? ne : 1));
+    f->n_records = 0;
+    for (int64_t tt = 0; tt < nt; ++tt) {
+        f->rec_off[tt] = (uint32_t)f->n_records;
+        const int64_t base = tt * tile, n_t = (n - base < tile) ? n - base : tile;
+        for (int64_t p = 0; p < n_t; ++p)
+            if (f->rank[codes[base + p]] < 0) f->records[f->n_records++] = (uint32_t)p | ((uint32_t)codes[base + p] << 16);
+    }
+    f->rec_off[nt] = (uint32_t)f->n_records;
+    return f;
+}
+
+/* Decode back to codes: the tile codec's symbols through the table, then each
+ * record's code at its position.  Returns the tile codec's status (0 ok). */
+int orc_fp8_decode(const orc_fp8* f, uint8_t* codes) {
+    const orc_rans* r = f->rans;
+    const uint32_t M = 1u << r->prob_bits;
+    int rc = 0;
+    for (int64_t t = 0; t < r->n_tiles; ++t) {
+        const int64_t base = t * r->tile, n_t = (r->n - base < r->tile) ? r->n - base : r->tile;
+        uint64_t x[32];
+        for (int l = 0; l < 32; ++l) x[l] = r->states[t * 32 + l];
+        int64_t wp = r->offsets[t];
+        const int64_t wend = r->offsets[t + 1];
+        for (int64_t m = 0; m < (n_t + 31) / 32; ++m)
+            for (int l = 0; l < 32; ++l) {
+                if (32 * m + l >= n_t) continue;
+                const uint32_t slot = (uint32_t)(x[l] & (M - 1));
+                int s = -1;
+                for (int q = 0; q < r->nsym; ++q)
+                    if (r->freqs[q] && slot >= r->cum[q] && slot < r->cum[q] + r->freqs[q]) s = q;
+                if (s < 0) return -1;
+                x[l] = (uint64_t)r->freqs[s] * (x[l] >> r->prob_bits) + slot - r->cum[s];
+                if (x[l] < (1u << 16)) {
+                    if (wp >= wend) return -1;
+                    x[l] = (x[l] << 16) | r->payload[wp++];
+                }
+                codes[base + 32 * m + l] = f->table[s];
+            }
+        for (int l = 0; l < 32; ++l)
+            if (x[l] != (1u << 16)) rc = -2;
+        if (wp != wend) rc = -2;
+        for (uint32_t e = f->rec_off[t]; e < f->rec_off[t + 1]; ++e) {
+            const uint32_t p = f->records[e] & 0xFFFFu;
+            if ((int64_t)p >= n_t) return -1;
+            codes[base + p] = (uint8_t)(f->records[e] >> 16);
+        }
+    }
+    return rc;
+}
+
+int64_t orc_fp8_info(const orc_fp8* f, int64_t* out /* 6 */) {
+    out[0] = f->n;
+    out[1] = f->rans->n_tiles;
+    out[2] = f->rans->payload_words;
+    out[3] = f->rans->tile;
+    out[4] = f->tsize;
+    out[5] = f->n_records;
+    return 0;
+}
+const uint8_t* orc_fp8_table_of(const orc_fp8* f) { return f->table; }
+const uint32_t* orc_fp8_freqs_of(const orc_fp8* f) { return f->rans->freqs; }
+const uint64_t* orc_fp8_counts_of(const orc_fp8* f) { return f->rans->counts; }
+const uint32_t* orc_fp8_states(const orc_fp8* f) { return f->rans->states; }
+const uint32_t* orc_fp8_offsets(const orc_fp8* f) { return f->rans->offsets; }
+uint16_t* orc_fp8_payload_mut(orc_fp8* f) { return f->rans->payload; }
+const uint32_t* orc_fp8_rec_off(const orc_fp8* f) { return f->rec_off; }
+const uint32_t* orc_fp8_records(const orc_fp8* f) { return f->records; }
+
+/* Dense BF16 of FP8 codes [n_rows, k_cols] with FP32 row scales:
+ * bf16(fp32(value(code) * r_i)). */
+void orc_fp8_dequant_bf16(const uint8_t* codes, const float* r, int64_t n_rows, int64_t k_cols, uint16_t* out) {
+    for (int64_t i = 0; i < n_rows; ++i)
+        for (int64_t j = 0; j < k_cols; ++j)
+            out[i * k_cols + j] = orc_f32_to_bf16_rne(orc_e4m3_to_f32(codes[i * k_cols + j]) * r[i]);
+}
+
+/* FP64 y[b, i] = sum_j value(code_ij) r_i x_bj and a = sum |...|, in index order. */
+void orc_gemv_fp8(const uint8_t* codes, const float* r, int64_t n_rows, int64_t k_cols, const uint16_t* x,
+                  int batch, const int64_t* rows, int64_t n_sel, double* y, double* a) {
+    const int64_t nr = rows ? n_sel : n_rows;
+    for (int b = 0; b < batch; ++b)
+        for (int64_t q = 0; q < nr; ++q) {
+            const int64_t i = rows ? rows[q] : q;
+            double acc = 0.0, mag = 0.0;
+            for (int64_t j = 0; j < k_cols; ++j) {
+                const double p = (double)orc_e4m3_to_f32(codes[i * k_cols + j]) * (double)r[i] *
+                                 orc_bf16_to_f64(x[(int64_t)b * k_cols + j]);
+                acc += p;
+                mag += fabs(p);
+            }
+            y[(int64_t)b * nr + q] = acc;
+            a[(int64_t)b * nr + q] = mag;
+        }
+}
+
+/* ===========================================================================
  * E8 lattice fields, EntroPack sections 3.2 (row-normalised lattice
  * representation), 3.3 (coset-conditioned model), 3.6 (tiles), 3.7 (GPU
  * reconstruction) and appendix A.3 (parity reduction).

@@ -210,3 +210,29 @@ def e8_row_scales(seed: int, n_rows: int, base: float = 0.02, ln_sigma: float = 
 def make_e8_case(seed: int, n_rows: int, k_cols: int, std: float = 3.5, scale: float = 0.125):
     """(q2, row_scales, scale) of an E8 matrix: w = bf16(q2 / 2 * scale * r_i)."""
     return e8_points(seed, n_rows, k_cols, std), e8_row_scales(synth_subseed(seed, 2), n_rows), scale
+
+
+def fp8_codes(seed: int, n_rows: int, k_cols: int, spread: float = 100.0) -> np.ndarray:
+    """FP8 E4M3 bytes [n_rows, k_cols] with the skewed histogram of Gaussian weights
+    scaled to the format's range: m = spread * |g|, sign ~ Bernoulli(1/2); the
+    exponent field is floor(log2 m) + 7 clipped to 1..15 (field 0 and mantissa
+    floor(m / 2^-9) below 2^-6), the mantissa floor(8 (m / 2^e - 1)), and the NaN
+    pattern S.1111.111 is avoided (mantissa 6 there)."""
+    n = n_rows * k_cols
+    m = spread * np.abs(normal_f64(seed, n))
+    sign = (uniform_f64(synth_subseed(seed, 3), n) < 0.5).astype(np.uint8)
+    with np.errstate(divide="ignore"):
+        e = np.clip(np.floor(np.log2(np.maximum(m, 1e-300))), -6, 8)
+    mant = np.clip(np.floor(8 * (m / 2.0 ** e - 1)), 0, 7)
+    field = (e + 7).astype(np.int64)
+    sub = m < 2.0 ** -6
+    field[sub] = 0
+    mant[sub] = np.clip(np.floor(m[sub] / 2.0 ** -9), 0, 7)
+    mant = mant.astype(np.int64)
+    mant[(field == 15) & (mant == 7)] = 6
+    return ((sign.astype(np.int64) << 7) | (field << 3) | mant).astype(np.uint8).reshape(n_rows, k_cols)
+
+
+def make_fp8_case(seed: int, n_rows: int, k_cols: int):
+    """(codes, row_scales) of an FP8 matrix: weight = value(code) * r_i, r_i ~ 0.02 LogNormal(0, 0.5) / 448."""
+    return fp8_codes(seed, n_rows, k_cols), e8_row_scales(synth_subseed(seed, 4), n_rows, base=0.02 / 448)
