@@ -443,6 +443,27 @@ def extras(torch, ec, stream, device):
     out["e8_14336x4096_decode_e4m3_us"] = round(t_loop(gf.replay, 20) / len(Es), 2)
     del Es, ge, gf, de, d8, q2
 
+    # FP8 E4M3 weights, 14336 x 4096, batch-1 GEMV with every code in the table and
+    # with a 32-code table plus correction records (8 copies rotated)
+    cf, rf = synth.make_fp8_case(7600, 14336, 4096)
+    xf = torch.from_numpy(synth.make_x(7601, 1, 4096).view(np.int16)).to(dev)
+    yf = torch.empty((1, 14336), device=dev)
+    for t, tag in ((0, "all"), (32, "t32")):
+        blob = ec.encode_fp8(cf, rf, top_t=t, device=-1).serialize()
+        Fs = [ec.deserialize(blob, device=device) for _ in range(8)]
+        st = Fs[0].stats()
+
+        def fg():
+            for F in Fs:
+                ec.gemv(F, xf, yf)
+        gg = capture(torch, fg, stream)
+        us = t_loop(gg.replay, 20) / len(Fs)
+        out[f"fp8_{tag}_14336x4096_gemv_us"] = round(us, 2)
+        out[f"fp8_{tag}_14336x4096_bpw"] = round(st["bits_per_weight"], 3)
+        out[f"fp8_{tag}_14336x4096_gbs"] = round(st["device_bytes"] / us / 1e3, 1)
+        del Fs, gg
+    del cf
+
     # 70B-shaped block: one batched decode of all seven matrices to BF16
     Ws, outs, comp, nw = [], [], 0, 0
     for s in synth.block_70b():

@@ -119,7 +119,21 @@ typedef struct {
     int32_t reserved[2];
 } ec_e8_params;
 
-enum { EC_KIND_HUFFMAN_BF16 = 1, EC_KIND_RANS_INT4 = 2, EC_KIND_E8 = 3 };
+enum { EC_KIND_HUFFMAN_BF16 = 1, EC_KIND_RANS_INT4 = 2, EC_KIND_E8 = 3, EC_KIND_RANS_FP8 = 4 };
+
+/* FP8 codec parameters (NULL = defaults).
+ *  prob_bits         frequency precision b, 9..12 (default 12)
+ *  tile_syms         weights per rANS tile, a multiple of 128 up to 4096 (default 4096)
+ *  top_t             codes kept in the decoding table, 1..256, code 0 always among
+ *                    them (MINE section 4, "Escapes"); 0 (default) keeps every code
+ *                    present.  A weight whose code is not kept is coded as 0 and
+ *                    restored from a 32-bit correction record. */
+typedef struct {
+    int32_t prob_bits;
+    int32_t tile_syms;
+    int32_t top_t;
+    int32_t reserved;
+} ec_fp8_params;
 
 /* Output dtypes of ec_decode_as. */
 enum { EC_DTYPE_BF16 = 0, EC_DTYPE_FP8_E4M3 = 1, EC_DTYPE_INT8 = 2 };
@@ -169,6 +183,17 @@ int ec_encode_rans(const int8_t* codes_host, const uint16_t* scales_f16_host, in
  * dense matrix before its matrix products). */
 int ec_encode_e8(const int8_t* q2_host, const float* row_scales_host, float scale, int64_t n_rows, int64_t k_cols,
                  const ec_e8_params* params, int device, ec_matrix** out);
+
+/* Encode FP8 E4M3 weights: codes_host [n_rows, k_cols] (host, OCP E4M3 bytes; the NaN
+ * pattern S.1111.111 is refused with EC_ERR_INVALID_ARG) with FP32 row scales
+ * row_scales_host [n_rows] (finite), weight = fp32(value(code)) * r_i.  The codes kept
+ * by the top-t table (params->top_t) go through interleaved rANS tiles (32 lanes,
+ * 16-bit renormalisation, as ec_encode_rans); the others are coded as code 0 and
+ * listed per tile as records (position in the tile | code << 16).  ec_gemv applies the
+ * records inside the same kernel (batch 1..EC_MAX_BATCH, FP32 accumulation, y = r_i *
+ * sum_j value * x); ec_decode writes bf16(fp32(value * r_i)).  Errors as ec_encode_rans. */
+int ec_encode_fp8(const uint8_t* codes_host, const float* row_scales_host, int64_t n_rows, int64_t k_cols,
+                  const ec_fp8_params* params, int device, ec_matrix** out);
 
 /* Decode W to dense row-major BF16 [n_rows, k_cols] in device memory out_bf16.
  * Huffman: the original bit patterns.  rANS: BF16 round-to-nearest-even of

@@ -34,10 +34,11 @@ EC_MAX_GROUP = 8
 EC_KIND_HUFFMAN_BF16 = 1
 EC_KIND_RANS_INT4 = 2
 EC_KIND_E8 = 3
+EC_KIND_RANS_FP8 = 4
 
 EXPORTS = ["ec_encode_bf16", "ec_encode_rans", "ec_decode", "ec_decode_batch", "ec_gemv", "ec_gemv_group",
            "ec_bf16_gemv", "ec_stats", "ec_code_lengths", "ec_serialize", "ec_deserialize", "ec_status", "ec_free",
-           "ec_strerror", "ec_gemv_static", "ec_gemv_path", "ec_encode_e8", "ec_decode_as"]
+           "ec_strerror", "ec_gemv_static", "ec_gemv_path", "ec_encode_e8", "ec_decode_as", "ec_encode_fp8"]
 
 
 class HuffParams(ctypes.Structure):
@@ -51,6 +52,11 @@ class RansParams(ctypes.Structure):
 
 class E8Params(ctypes.Structure):
     _fields_ = [("prob_bits", ctypes.c_int32), ("tile_vectors", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2)]
+
+
+class Fp8Params(ctypes.Structure):
+    _fields_ = [("prob_bits", ctypes.c_int32), ("tile_syms", ctypes.c_int32), ("top_t", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class Stats(ctypes.Structure):
@@ -71,6 +77,7 @@ _sig = {
     "ec_encode_rans": ([_vp, _vp, _i64, _i64, ctypes.POINTER(RansParams), _i32, ctypes.POINTER(_vp)], _i32),
     "ec_encode_e8": ([_vp, _vp, ctypes.c_float, _i64, _i64, ctypes.POINTER(E8Params), _i32, ctypes.POINTER(_vp)],
                      _i32),
+    "ec_encode_fp8": ([_vp, _vp, _i64, _i64, ctypes.POINTER(Fp8Params), _i32, ctypes.POINTER(_vp)], _i32),
     "ec_decode": ([_vp, _vp, _vp], _i32),
     "ec_decode_batch": ([_vp, _vp, _i32, _vp], _i32),
     "ec_decode_as": ([_vp, _vp, _i32, _vp], _i32),
@@ -207,6 +214,19 @@ def encode_e8(q2, row_scales, scale: float, prob_bits: int = 0, tile_vectors: in
     h = ctypes.c_void_p()
     _check(lib.ec_encode_e8(pq, pr, float(scale), n, k, ctypes.byref(prm), device, ctypes.byref(h)), "ec_encode_e8")
     return Matrix(h.value, n, k, EC_KIND_E8, device)
+
+
+def encode_fp8(codes, row_scales, top_t: int = 0, prob_bits: int = 0, tile_syms: int = 0,
+               device: int = 0) -> Matrix:
+    """Encode host FP8 E4M3 bytes [N, K] with FP32 row scales [N] under a top-t table
+    (top_t 0: every code present; 0 for prob_bits / tile_syms: 12 and 4096)."""
+    n, k = int(codes.shape[0]), int(codes.shape[1])
+    pc, kc = _host_ptr(codes)
+    pr, kr = _host_ptr(row_scales)
+    prm = Fp8Params(prob_bits, tile_syms, top_t)
+    h = ctypes.c_void_p()
+    _check(lib.ec_encode_fp8(pc, pr, n, k, ctypes.byref(prm), device, ctypes.byref(h)), "ec_encode_fp8")
+    return Matrix(h.value, n, k, EC_KIND_RANS_FP8, device)
 
 
 def deserialize(data: bytes, device: int = 0) -> Matrix:

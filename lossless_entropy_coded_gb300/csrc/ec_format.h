@@ -52,7 +52,7 @@
 #include <stdint.h>
 
 #define EC_BLOB_MAGIC 0x31434345u /* "ECC1" */
-#define EC_BLOB_VERSION 7u
+#define EC_BLOB_VERSION 8u
 
 #define EC_L1_BITS 12            /* level-1 Huffman window */
 #define EC_SUB_BITS 8            /* bits per sub-table level */
@@ -104,6 +104,16 @@
  * 2m + 1): bits 0..7 = symbol, bits 8..19 = slot - cum[s], bits 20..31 =
  * freq[s] - 1. */
 
+/* FP8 blob (kind 4): the table section is 2^prob_bits slot entries in the pair
+ * layout above (bits 0..7 = symbol = rank of the code in the top-t table, bits
+ * 8..19 = slot - cum[s], bits 20..31 = freq[s] - 1), then 256 FP32 values of the
+ * symbols (unused ones 0), then 256 FP32 values of all E4M3 codes (the escapes'
+ * values); FP32 row scales at scales_off; u32 record offsets per tile at
+ * esc_off_off (record index, n_tiles + 1 entries) and the records at
+ * esc_records_off (position in the tile | code << 16, ascending positions within a
+ * tile); rANS tile records (32 states, u16 words) as for kind 2, last. */
+#define EC_FP8_VALUE_WORDS 512
+
 typedef struct {
     uint32_t magic, version;
     int32_t kind;             /* EC_KIND_* */
@@ -124,7 +134,11 @@ typedef struct {
                                        * over EC_MMA_WINDOW_ROWS consecutive rows' tiles of one tile
                                        * column; 0 when tiles cross rows */
     uint32_t e8_scale_bits;           /* E8: the shared scale s (FP32 bit pattern) */
-    uint8_t pad[256 - 4 * 4 - 8 * 10 - 4 * 7];
+    int32_t fp8_table_size;           /* FP8: codes in the decoding table (1..256) */
+    int64_t esc_off_off;              /* FP8: byte offset of u32 record offsets [n_tiles + 1] */
+    int64_t esc_records_off;          /* FP8: byte offset of the u32 correction records */
+    int64_t n_escapes;                /* FP8: correction records */
+    uint8_t pad[256 - 4 * 4 - 8 * 10 - 4 * 8 - 8 * 3];
 } ec_blob_header;
 
 #endif /* EC_FORMAT_H_ */

@@ -932,6 +932,194 @@ extern "C" int ec_encode_e8(const int8_t* q2, const float* row_scales, float sca
     });
 }
 
+/* ============================================================ FP8 top-t encoder */
+/* MINE section 4, "Escapes": the decoding table keeps the t most frequent codes, 0
+ * always among them; any other weight is coded as 0 and its code goes to a sparse
+ * correction stream of 32-bit records. */
+namespace {
+/* Value of an OCP FP8 E4M3 code: sign, exponent field e (bias 7), mantissa m; e = 0
+ * holds the subnormals m/8 * 2^-6; S.1111.111 is NaN. */
+float e4m3_value(int code) {
+    const int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return std::nanf("");
+    const float v = e == 0 ? std::ldexp((float)m / 8.0f, -6) : std::ldexp(1.0f + (float)m / 8.0f, e - 7);
+    return s ? -v : v;
+}
+}  // namespace
+
+extern "C" int ec_encode_fp8(const uint8_t* codes, const float* row_scales, int64_t n_rows, int64_t k_cols,
+                             const ec_fp8_params* params, int device, ec_matrix** out) {
+    if (!out) return EC_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (n_rows < 0 || k_cols < 0) return EC_ERR_SHAPE;
+    const int b = params && params->prob_bits ? params->prob_bits : 12;
+    const int T = params && params->tile_syms ? params->tile_syms : 4096;
+    const int t_req = params ? params->top_t : 0;
+    if (b < 9 || b > 12 || T < EC_RANS_ROW_ALIGN || T % EC_RANS_ROW_ALIGN || T > 4096 || t_req < 0 || t_req > 256)
+        return EC_ERR_INVALID_ARG;
+    if (k_cols > INT64_MAX - EC_RANS_ROW_ALIGN) return EC_ERR_OVERFLOW;
+    const int64_t KP = round_up(k_cols, EC_RANS_ROW_ALIGN);
+    int64_t nk = 0, n_pad = 0, tmp = 0;
+    if (!mul_ok(n_rows, k_cols, &nk) || !mul_ok(n_rows, KP, &n_pad) || !mul_ok(n_pad, 4, &tmp)) return EC_ERR_OVERFLOW;
+    if (nk > 0 && (!codes || !row_scales)) return EC_ERR_INVALID_ARG;
+
+    return guarded([&]() -> int {
+        const int64_t K = k_cols;
+        for (int64_t i = 0; i < nk; ++i)
+            if ((codes[i] & 0x7F) == 0x7F) return EC_ERR_INVALID_ARG; /* NaN */
+        for (int64_t r = 0; r < n_rows; ++r)
+            if (!std::isfinite(row_scales[r])) return EC_ERR_INVALID_ARG;
+        uint64_t hist[256] = {};
+        for (int64_t i = 0; i < nk; ++i) hist[codes[i]]++;
+        hist[0] += (uint64_t)(n_pad - nk); /* padding */
+        /* the table: code 0, then the most frequent other present codes (ties to the
+         * lower code) up to t, sorted by code; rank = symbol */
+        const int t = t_req ? t_req : 256;
+        bool kept[256] = {};
+        kept[0] = true;
+        for (int size = 1; size < t; ++size) {
+            int best = -1;
+            for (int c = 1; c < 256; ++c)
+                if (!kept[c] && hist[c] && (best < 0 || hist[c] > hist[best])) best = c;
+            if (best < 0) break;
+            kept[best] = true;
+        }
+        int rank[256], tsize = 0;
+        uint8_t table_codes[256] = {};
+        for (int c = 0; c < 256; ++c) {
+            rank[c] = kept[c] ? tsize : -1;
+            if (kept[c]) table_codes[tsize++] = (uint8_t)c;
+        }
+        ec_matrix* m = new_matrix();
+        if (!m) return EC_ERR_OOM;
+        for (int c = 0; c < 256; ++c) m->counts[rank[c] >= 0 ? rank[c] : 0] += hist[c];
+        if (!rans_normalise(m->counts, tsize, b, m->freqs)) {
+            delete m;
+            return EC_ERR_INVALID_ARG;
+        }
+        const uint32_t M = 1u << b;
+        std::vector<uint32_t> cum(tsize, 0);
+        for (int s = 0, c = 0; s < tsize; ++s) {
+            cum[s] = (uint32_t)c;
+            c += (int)m->freqs[s];
+        }
+        std::vector<uint32_t> table(M + EC_FP8_VALUE_WORDS, 0);
+        for (int s = 0; s < tsize; ++s)
+            for (uint32_t q = 0; q < m->freqs[s]; ++q)
+                table[cum[s] + q] = (uint32_t)s | (q << 8) | ((m->freqs[s] - 1) << 20);
+        for (int s = 0; s < tsize; ++s) {
+            const float v = e4m3_value(table_codes[s]);
+            std::memcpy(&table[M + s], &v, 4);
+        }
+        for (int c = 0; c < 256; ++c) {
+            const float v = e4m3_value(c);
+            std::memcpy(&table[M + 256 + c], &v, 4);
+        }
+
+        const int64_t n_tiles = (n_pad + T - 1) / T;
+        std::vector<std::vector<uint16_t>> words(n_tiles);
+        std::vector<std::vector<uint32_t>> recs(n_tiles);
+        std::vector<std::array<uint32_t, 32>> states(n_tiles);
+        const uint64_t unit = uint64_t(1) << (32 - b);
+        parallel_for(n_tiles, [&](int64_t lo, int64_t hi) {
+            std::vector<uint16_t> stack;
+            std::vector<uint8_t> v(T);
+            for (int64_t tt = lo; tt < hi; ++tt) {
+                const int64_t base = tt * T, n_t = std::min<int64_t>(T, n_pad - base), S = n_t / 32;
+                gather_padded(codes, K, KP, base, n_t, v.data());
+                for (int64_t p = 0; p < n_t; ++p)
+                    if (rank[v[p]] < 0) recs[tt].push_back((uint32_t)p | ((uint32_t)v[p] << 16));
+                uint64_t x[32];
+                for (int l = 0; l < 32; ++l) x[l] = 1u << 16;
+                stack.clear();
+                for (int64_t j = S - 1; j >= 0; --j)
+                    for (int l = 31; l >= 0; --l) {
+                        const int r = rank[v[32 * j + l]], s = r >= 0 ? r : 0;
+                        const uint64_t f = m->freqs[s];
+                        if (x[l] >= f * unit) {
+                            stack.push_back((uint16_t)x[l]);
+                            x[l] >>= 16;
+                        }
+                        x[l] = ((x[l] / f) << b) + x[l] % f + cum[s];
+                    }
+                for (int l = 0; l < 32; ++l) states[tt][l] = (uint32_t)x[l];
+                words[tt].assign(stack.rbegin(), stack.rend());
+            }
+        });
+        std::vector<uint32_t> tile_off(n_tiles + 1, 0), esc_off(n_tiles + 1, 0);
+        int64_t total = 0, max_words = 0, payload = 0, n_esc = 0;
+        for (int64_t tt = 0; tt < n_tiles; ++tt) {
+            tile_off[tt] = (uint32_t)(total / 16);
+            total += 128 + round_up(2 * (int64_t)words[tt].size(), 16);
+            max_words = std::max<int64_t>(max_words, (int64_t)words[tt].size());
+            payload += 16 * (int64_t)words[tt].size();
+            esc_off[tt] = (uint32_t)n_esc;
+            n_esc += (int64_t)recs[tt].size();
+        }
+        if (total / 16 > (int64_t)UINT32_MAX || n_esc > (int64_t)UINT32_MAX) {
+            delete m;
+            return EC_ERR_OVERFLOW;
+        }
+        tile_off[n_tiles] = (uint32_t)(total / 16);
+        esc_off[n_tiles] = (uint32_t)n_esc;
+
+        ec_blob_header h{};
+        h.magic = EC_BLOB_MAGIC;
+        h.version = EC_BLOB_VERSION;
+        h.kind = EC_KIND_RANS_FP8;
+        h.steps = T / 32;
+        h.n_rows = n_rows;
+        h.k_cols = k_cols;
+        h.k_pad = KP;
+        h.n_tiles = n_tiles;
+        h.table_off = sizeof(ec_blob_header);
+        h.table_words = (int64_t)M + EC_FP8_VALUE_WORDS;
+        h.scales_off = round_up(h.table_off + 4 * h.table_words, 16);
+        h.tile_off_off = round_up(h.scales_off + 4 * n_rows, 16);
+        h.esc_off_off = round_up(h.tile_off_off + 4 * (n_tiles + 1), 16);
+        h.esc_records_off = round_up(h.esc_off_off + 4 * (n_tiles + 1), 16);
+        h.records_off = round_up(h.esc_records_off + 4 * n_esc, 16);
+        h.blob_bytes = h.records_off + total;
+        h.prob_bits = b;
+        h.max_words = (int32_t)max_words;
+        h.rans_tuple = 1;
+        h.fp8_table_size = tsize;
+        h.n_escapes = n_esc;
+
+        std::vector<uint8_t> blob((size_t)h.blob_bytes, 0);
+        std::memcpy(blob.data(), &h, sizeof h);
+        std::memcpy(blob.data() + h.table_off, table.data(), 4 * table.size());
+        if (n_rows) std::memcpy(blob.data() + h.scales_off, row_scales, 4 * (size_t)n_rows);
+        std::memcpy(blob.data() + h.tile_off_off, tile_off.data(), 4 * tile_off.size());
+        std::memcpy(blob.data() + h.esc_off_off, esc_off.data(), 4 * esc_off.size());
+        parallel_for(n_tiles, [&](int64_t lo, int64_t hi) {
+            for (int64_t tt = lo; tt < hi; ++tt) {
+                uint8_t* rec = blob.data() + h.records_off + (int64_t)tile_off[tt] * 16;
+                std::memcpy(rec, states[tt].data(), 128);
+                if (!words[tt].empty()) std::memcpy(rec + 128, words[tt].data(), 2 * words[tt].size());
+                if (!recs[tt].empty())
+                    std::memcpy(blob.data() + h.esc_records_off + 4 * (int64_t)esc_off[tt], recs[tt].data(),
+                                4 * recs[tt].size());
+            }
+        });
+        m->kind = EC_KIND_RANS_FP8;
+        m->device = device;
+        m->hdr = h;
+        m->payload_bits = payload + 32 * n_esc;
+        m->raw_bytes = 0;
+        m->table_bytes = 4 * h.table_words + 4 * n_rows;
+        m->aux_bytes = h.blob_bytes - m->table_bytes - m->payload_bits / 8;
+        m->entropy = entropy_bits(hist, 256); /* bits per code */
+        int rc = upload(m, blob, device);
+        if (rc != EC_OK) {
+            delete m;
+            return rc;
+        }
+        *out = m;
+        return EC_OK;
+    });
+}
+
 /* ======================================================= bookkeeping entry points */
 extern "C" int ec_stats(const ec_matrix* m, ec_stats_t* s) {
     if (!m || !s) return EC_ERR_INVALID_ARG;
@@ -1015,9 +1203,11 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
     std::memcpy(&h, b, sizeof h);
     if (h.magic != EC_BLOB_MAGIC || h.version != EC_BLOB_VERSION) return EC_ERR_CORRUPT;
     if (h.blob_bytes != bytes) return EC_ERR_CORRUPT;
-    if (h.kind != EC_KIND_HUFFMAN_BF16 && h.kind != EC_KIND_RANS_INT4 && h.kind != EC_KIND_E8) return EC_ERR_CORRUPT;
+    if (h.kind != EC_KIND_HUFFMAN_BF16 && h.kind != EC_KIND_RANS_INT4 && h.kind != EC_KIND_E8 &&
+        h.kind != EC_KIND_RANS_FP8)
+        return EC_ERR_CORRUPT;
     if (h.n_rows < 0 || h.k_cols < 0 || h.k_cols > INT64_MAX / 2) return EC_ERR_CORRUPT;
-    const bool huff = h.kind == EC_KIND_HUFFMAN_BF16, e8 = h.kind == EC_KIND_E8;
+    const bool huff = h.kind == EC_KIND_HUFFMAN_BF16, e8 = h.kind == EC_KIND_E8, fp8 = h.kind == EC_KIND_RANS_FP8;
     const int64_t align = huff ? EC_HUFF_ROW_ALIGN : e8 ? EC_E8_ROW_ALIGN : EC_RANS_ROW_ALIGN;
     if (h.k_pad != round_up(h.k_cols, align)) return EC_ERR_CORRUPT;
     if (e8 ? (h.k_cols % 8 || h.steps < 1 || h.steps > 32)
@@ -1039,6 +1229,11 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
         if (h.prob_bits < 9 || h.prob_bits > 12 || h.max_words < 0 ||
             h.table_words != (4 * EC_E8_TABLES * EC_E8_ALPHA + ((int64_t)EC_E8_TABLES << h.prob_bits)) / 4)
             return EC_ERR_CORRUPT;
+    } else if (fp8) {
+        if (h.prob_bits < 9 || h.prob_bits > 12 || h.max_words < 0 || h.rans_tuple != 1 ||
+            h.table_words != (int64_t(1) << h.prob_bits) + EC_FP8_VALUE_WORDS || h.fp8_table_size < 1 ||
+            h.fp8_table_size > 256 || (32 * (int64_t)h.steps) > 4096 || h.n_escapes < 0)
+            return EC_ERR_CORRUPT;
     } else {
         if (h.prob_bits < 9 || h.prob_bits > 15 || h.table_words != (int64_t(1) << h.prob_bits) || h.max_words < 0)
             return EC_ERR_CORRUPT;
@@ -1046,9 +1241,9 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
         if (h.rans_tuple == 2 && h.prob_bits > 12) return EC_ERR_CORRUPT;
     }
     if (!mul_ok(h.table_words, 4, &t4) || !add_ok(h.table_off, t4, &end)) return EC_ERR_CORRUPT;
-    if (!huff) { /* rANS: FP16 group scales; E8: FP32 row scales */
+    if (!huff) { /* rANS: FP16 group scales; E8 and FP8: FP32 row scales */
         int64_t ns = 0, s2 = 0;
-        if (e8 ? !mul_ok(h.n_rows, 4, &s2) : (!mul_ok(h.n_rows, h.k_pad / 128, &ns) || !mul_ok(ns, 2, &s2)))
+        if (e8 || fp8 ? !mul_ok(h.n_rows, 4, &s2) : (!mul_ok(h.n_rows, h.k_pad / 128, &ns) || !mul_ok(ns, 2, &s2)))
             return EC_ERR_CORRUPT;
         if (h.scales_off < end || h.scales_off % 16 || !add_ok(h.scales_off, s2, &end)) return EC_ERR_CORRUPT;
     }
@@ -1056,6 +1251,13 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
     if (h.tile_off_off < end || h.tile_off_off % 16 || !mul_ok(h.n_tiles + 1, 4, &to4) ||
         !add_ok(h.tile_off_off, to4, &end))
         return EC_ERR_CORRUPT;
+    if (fp8) { /* record offsets, then the records */
+        int64_t e4 = 0;
+        if (h.esc_off_off < end || h.esc_off_off % 16 || !add_ok(h.esc_off_off, to4, &end)) return EC_ERR_CORRUPT;
+        if (h.esc_records_off < end || h.esc_records_off % 16 || !mul_ok(h.n_escapes, 4, &e4) ||
+            !add_ok(h.esc_records_off, e4, &end))
+            return EC_ERR_CORRUPT;
+    }
     if (h.records_off < end || h.records_off % 16 || h.records_off > bytes) return EC_ERR_CORRUPT;
     const uint32_t* off = (const uint32_t*)(b + h.tile_off_off);
     if (off[0] != 0 || (int64_t)off[h.n_tiles] * 16 != bytes - h.records_off) return EC_ERR_CORRUPT;
@@ -1071,6 +1273,20 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
                 if (start[l] > area || (l && start[l] < start[l - 1])) return EC_ERR_CORRUPT;
         } else {
             if (rb < 128 || (rb - 128) / 2 > round_up(h.max_words, 8)) return EC_ERR_CORRUPT;
+        }
+    }
+    if (fp8) { /* per tile: ascending record offsets, records at ascending positions inside the tile */
+        const uint32_t* eo = (const uint32_t*)(b + h.esc_off_off);
+        const uint32_t* er = (const uint32_t*)(b + h.esc_records_off);
+        if (eo[0] != 0 || (int64_t)eo[h.n_tiles] != h.n_escapes) return EC_ERR_CORRUPT;
+        for (int64_t t = 0; t < h.n_tiles; ++t) {
+            if (eo[t + 1] < eo[t]) return EC_ERR_CORRUPT;
+            const int64_t n_t = std::min(T, n_pad - t * T);
+            for (uint32_t e = eo[t]; e < eo[t + 1]; ++e) {
+                const uint32_t p = er[e] & 0xFFFFu;
+                if ((int64_t)p >= n_t || (er[e] >> 24) || (e > eo[t] && p <= (er[e - 1] & 0xFFFFu)))
+                    return EC_ERR_CORRUPT;
+            }
         }
     }
     const uint32_t* tab = (const uint32_t*)(b + h.table_off);
@@ -1102,6 +1318,11 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
                 if (tab[s] & 0xFFFFu) return EC_ERR_CORRUPT;
             for (uint32_t q = c; q < M; ++q) /* an unused table maps every slot to symbol 0 */
                 if (ss[(size_t)t * M + q] != 0) return EC_ERR_CORRUPT;
+        }
+    } else if (fp8) { /* pair-layout entries: symbol inside the table, bias below the frequency */
+        for (int64_t i = 0; i < (int64_t(1) << h.prob_bits); ++i) {
+            const uint32_t f = (tab[i] >> 20) + 1, k = (tab[i] >> 8) & 0xFFF;
+            if ((int32_t)(tab[i] & 0xFF) >= h.fp8_table_size || f > (1u << h.prob_bits) || k >= f) return EC_ERR_CORRUPT;
         }
     } else if (h.rans_tuple == 1) {
         for (int64_t i = 0; i < h.table_words; ++i) {

@@ -129,6 +129,31 @@ struct RansArgs {
     int* status;
 };
 
+/* An FP8 matrix: rANS tiles of top-t table symbols plus per-tile correction records. */
+struct Fp8Mat {
+    const uint8_t* records;
+    const uint32_t* tile_off;
+    const uint32_t* table;      /* 2^prob_bits slot entries, 256 symbol values, 256 code values (FP32) */
+    const float* row_scales;    /* [n_rows] */
+    const uint32_t* esc_off;    /* [n_tiles + 1] record index */
+    const uint32_t* esc;        /* position in the tile | code << 16 */
+    float* y;
+    uint16_t* out;
+    int64_t n_rows, k_cols, k_pad;
+    int64_t n_tiles;
+    int64_t records_bytes;
+    int32_t steps, prob_bits, atomic_y, words_cap;
+    int32_t last_steps;
+    uint32_t rec16;
+};
+
+struct Fp8Args {
+    Fp8Mat m;
+    int batch;
+    const uint16_t* x;
+    int* status;
+};
+
 /* E8 lattice matrix (decode only). */
 struct E8Mat {
     const uint8_t* records;
@@ -1451,6 +1476,154 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) rans_kernel(const _
     }
 }
 
+/* ============================================================== FP8 kernel */
+/* FP8 weights under a top-t table (MINE section 4, "Escapes"): the rANS tiles
+ * decode one table symbol per position (pair-layout slot entries: symbol, slot
+ * bias, frequency - 1), the symbol's FP32 value feeds the FMA (GEMV) or is scaled
+ * by the row scale and stored (decode); a weight outside the table was coded as
+ * code 0, and after its tile the warp applies the tile's correction records: each
+ * lane takes records in turn and adds r_i * value * x (GEMV, atomically) or writes
+ * bf16(value * r_i) over the 0 (decode). */
+template <bool kGemv, int B>
+__global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) fp8_kernel(const __grid_constant__ Fp8Args a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const Fp8Mat& M = a.m;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+    const uint32_t kp = (uint32_t)M.k_pad;
+    const int64_t K = M.k_cols;
+    const int pb = M.prob_bits;
+    const uint32_t mask_b = (1u << pb) - 1;
+    const int batch = kGemv ? a.batch : 0;
+    const uint32_t tab_s = smem_u32(smem);
+    const size_t tab_bytes = ((size_t)4 << pb) + 4 * EC_FP8_VALUE_WORDS;
+    const float* vals = (const float*)(smem + ((size_t)4 << pb)); /* [0, 256): symbols, [256, 512): codes */
+    uint16_t* xs = (uint16_t*)(smem + tab_bytes);
+    const uint32_t buf_bytes = (uint32_t)rans_buf_bytes(M.words_cap);
+    const uint32_t bufs = smem_u32(xs) + (uint32_t)(2 * (size_t)batch * kp) + (uint32_t)warp * 2 * buf_bytes;
+    const uint32_t cap = (buf_bytes - 128) / 2 - 1;
+    const int64_t T = 32 * (int64_t)M.steps;
+
+    const int64_t gw = (int64_t)blockIdx.x * nwarp + warp, nw = (int64_t)gridDim.x * nwarp;
+    RansTile cur{};
+    if (gw < M.n_tiles) {
+        cur = rans_tile(M, gw, make_uint2(__ldg(M.tile_off + gw), __ldg(M.tile_off + gw + 1)));
+        rans_prefetch(bufs, cur, lane);
+    }
+    {
+        const uint4* src = (const uint4*)M.table;
+        uint4* dst = (uint4*)smem;
+        for (int i = threadIdx.x; i < (int)(tab_bytes / 16); i += blockDim.x) dst[i] = __ldg(src + i);
+    }
+    grid_dep_launch();
+    grid_dep_wait(); /* x, y and out belong to the preceding kernel in the stream from here on */
+    if (kGemv) stage_x_rows(xs, a.x, batch, K, kp);
+    __syncthreads();
+    if (gw >= M.n_tiles) return;
+
+    uint2 off_next = gw + nw < M.n_tiles ? make_uint2(__ldg(M.tile_off + gw + nw), __ldg(M.tile_off + gw + nw + 1))
+                                         : make_uint2(0u, 0u);
+    const uint32_t lt = (1u << lane) - 1u;
+    uint32_t cb = bufs;
+    for (int64_t t = gw; t < M.n_tiles; t += nw) {
+        cp_async_wait_all();
+        __syncwarp();
+        const uint32_t nb_buf = cb == bufs ? bufs + buf_bytes : bufs;
+        RansTile nxt{};
+        if (t + nw < M.n_tiles) {
+            nxt = rans_tile(M, t + nw, off_next);
+            rans_prefetch(nb_buf, nxt, lane);
+            if (t + 2 * nw < M.n_tiles)
+                off_next = make_uint2(__ldg(M.tile_off + t + 2 * nw), __ldg(M.tile_off + t + 2 * nw + 1));
+        }
+        if (cur.words < 0) {
+            if (lane == 0) flag_corrupt(a.status);
+        } else {
+            uint32_t x = lds32(cb + 4 * lane);
+            const uint32_t wbase = cb + 128;
+            uint32_t wp = 0;
+            int64_t row = tile_row(t, T, kp, EC_RANS_ROW_ALIGN);
+            uint32_t col = (uint32_t)(t * T - row * (int64_t)kp) + lane; /* this lane's column */
+            float scale = __ldg(M.row_scales + row);
+            float acc[B];
+#pragma unroll
+            for (int b = 0; b < B; ++b) acc[b] = 0.f;
+            auto flush = [&]() {
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                    if (B > 1 && b >= batch) break;
+                    const float v = warp_sum(acc[b]) * scale;
+                    if (lane == 0) {
+                        float* dst = M.y + (int64_t)b * M.n_rows + row;
+                        if (M.atomic_y) atomicAdd(dst, v);
+                        else *dst = v;
+                    }
+                    acc[b] = 0.f;
+                }
+            };
+            const int ng = cur.S / 4;
+            for (int gi = 0; gi < ng; ++gi) {
+                if (col >= kp) { /* rows start on 128-column boundaries */
+                    if (kGemv) flush();
+                    col -= kp;
+                    ++row;
+                    scale = __ldg(M.row_scales + row);
+                }
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint32_t e = lds32(tab_s + ((x & mask_b) << 2));
+                    const uint32_t X = x >> pb;
+                    x = (e >> 20) * X + X + ((e >> 8) & 0xFFFu); /* f X + bias with f - 1 in bits 20..31 */
+                    const bool need = x < 65536u;
+                    const uint32_t bal = __ballot_sync(kFull, need);
+                    const uint32_t idx = min(wp + __popc(bal & lt), cap);
+                    const uint32_t v = lds16_if(need, wbase + 2 * idx, 0u);
+                    x = need ? x * 65536u + v : x;
+                    wp += __popc(bal);
+                    const float w = vals[e & 0xFFu];
+                    const uint32_t c = col + 32 * s;
+                    if (kGemv) {
+#pragma unroll
+                        for (int b = 0; b < B; ++b) {
+                            if (B > 1 && b >= batch) break;
+                            acc[b] = fmaf(w, __uint_as_float((uint32_t)xs[(size_t)b * kp + c] << 16), acc[b]);
+                        }
+                    } else if (c < K) {
+                        M.out[row * K + c] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(w, scale)));
+                    }
+                }
+                col += 128;
+            }
+            if (__any_sync(kFull, x != 65536u) || wp > (uint32_t)cur.words || (uint32_t)cur.words - wp > 7) {
+                if (lane == 0) flag_corrupt(a.status);
+            }
+            if (kGemv) flush();
+            /* the tile's corrections, after its own stores and sums */
+            __syncwarp();
+            const uint32_t e0 = __ldg(M.esc_off + t), e1 = __ldg(M.esc_off + t + 1);
+            const uint32_t n_t = 32u * (uint32_t)cur.S;
+            for (uint32_t e = e0 + lane; e < e1; e += 32) {
+                const uint32_t rec = __ldg(M.esc + e), p = rec & 0xFFFFu;
+                if (p >= n_t) {
+                    flag_corrupt(a.status);
+                    continue;
+                }
+                const int64_t q = t * T + p, r = q / (int64_t)kp, cc = q - r * (int64_t)kp;
+                if (cc >= K) continue;
+                const float w = vals[256 + ((rec >> 16) & 0xFFu)], sr = __ldg(M.row_scales + r);
+                if (kGemv) {
+                    for (int b = 0; b < batch; ++b)
+                        atomicAdd(M.y + (int64_t)b * M.n_rows + r,
+                                  sr * (w * __uint_as_float((uint32_t)xs[(size_t)b * kp + cc] << 16)));
+                } else {
+                    M.out[r * K + cc] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(w, sr)));
+                }
+            }
+        }
+        cur = nxt;
+        cb = nb_buf;
+    }
+}
+
 /* ======================================================== BF16 GEMV comparator */
 constexpr int kRowsPerWarp = 4;
 
@@ -1882,6 +2055,30 @@ RansMat rans_desc(const ec_matrix* W) {
     return m;
 }
 
+Fp8Mat fp8_desc(const ec_matrix* W) {
+    Fp8Mat m{};
+    const ec_blob_header& h = W->hdr;
+    m.records = W->d_blob + h.records_off;
+    m.tile_off = (const uint32_t*)(W->d_blob + h.tile_off_off);
+    m.table = (const uint32_t*)(W->d_blob + h.table_off);
+    m.row_scales = (const float*)(W->d_blob + h.scales_off);
+    m.esc_off = (const uint32_t*)(W->d_blob + h.esc_off_off);
+    m.esc = (const uint32_t*)(W->d_blob + h.esc_records_off);
+    m.n_rows = h.n_rows;
+    m.k_cols = h.k_cols;
+    m.k_pad = h.k_pad;
+    m.n_tiles = h.n_tiles;
+    m.records_bytes = h.blob_bytes - h.records_off;
+    m.steps = h.steps;
+    m.prob_bits = h.prob_bits;
+    const int64_t T = 32 * (int64_t)h.steps;
+    m.atomic_y = (h.k_pad > 0 && T % h.k_pad == 0) ? 0 : 1;
+    m.words_cap = (h.max_words + 7) / 8 * 8;
+    m.last_steps = h.n_tiles > 0 ? (int32_t)((h.n_rows * h.k_pad - (h.n_tiles - 1) * T) / 32) : 0;
+    m.rec16 = (uint32_t)(m.records_bytes / 16);
+    return m;
+}
+
 /* ---- E8 decode: begin ---- */
 E8Mat e8_desc(const ec_matrix* W) {
     E8Mat m{};
@@ -2200,6 +2397,60 @@ int rans_run(const ec_matrix* W, const uint16_t* x, float* y, uint16_t* out, int
     return EC_OK;
 }
 
+template <bool G, int B>
+int launch_fp8_b(const Fp8Args& a, size_t smem, int grid, int block, cudaStream_t s) {
+    if (set_smem(fp8_kernel<G, B>, smem) != EC_OK) return EC_ERR_CUDA;
+    return launch_ex(fp8_kernel<G, B>, grid, block, smem, s, a);
+}
+
+int launch_fp8(bool gemv, const Fp8Args& a, size_t smem, int grid, int block, cudaStream_t s) {
+    if (!gemv) return launch_fp8_b<false, 1>(a, smem, grid, block, s);
+    if (a.batch <= 1) return launch_fp8_b<true, 1>(a, smem, grid, block, s);
+    if (a.batch <= 2) return launch_fp8_b<true, 2>(a, smem, grid, block, s);
+    if (a.batch <= 4) return launch_fp8_b<true, 4>(a, smem, grid, block, s);
+    if (a.batch <= 8) return launch_fp8_b<true, 8>(a, smem, grid, block, s);
+    return launch_fp8_b<true, 16>(a, smem, grid, block, s);
+}
+
+/* FP8 GEMV (y != nullptr) or decode: one CTA per SM with the slot table, the value
+ * tables and x in shared memory, two tile buffers per warp; batch rows in passes. */
+int fp8_run(const ec_matrix* W, const uint16_t* x, float* y, uint16_t* out, int batch, cudaStream_t s,
+            DeviceInfo* d) {
+    Fp8Args a{};
+    a.m = fp8_desc(W);
+    a.m.y = y;
+    a.m.out = out;
+    a.status = d->status;
+    const bool gemv = y != nullptr;
+    if (gemv && (a.m.atomic_y || W->hdr.n_tiles == 0)) {
+        if (cudaMemsetAsync(y, 0, sizeof(float) * (size_t)batch * (size_t)W->hdr.n_rows, s) != cudaSuccess)
+            return EC_ERR_CUDA;
+    }
+    if (W->hdr.n_tiles == 0) return EC_OK;
+    const size_t table = ((size_t)4 << a.m.prob_bits) + 4 * EC_FP8_VALUE_WORDS;
+    const size_t per_warp = 2 * rans_buf_bytes(a.m.words_cap);
+    const int64_t kp = W->hdr.k_pad, K = W->hdr.k_cols;
+    const size_t xrow = gemv ? (size_t)2 * kp : 0;
+    if (table + xrow + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED;
+    const int cap = gemv ? rans_max_warps(batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : batch <= 8 ? 8 : 16)
+                         : rans_max_warps(1);
+    const int warps = (int)std::min<size_t>(cap, (d->smem_optin - table - xrow) / per_warp);
+    const size_t fixed = table + (size_t)warps * per_warp;
+    const int per_pass = gemv ? (int)std::min<size_t>(std::min(batch, kFmaMaxRows), (d->smem_optin - fixed) / xrow) : 1;
+    if (per_pass < 1) return EC_ERR_UNSUPPORTED;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(d->sms, (W->hdr.n_tiles + warps - 1) / warps));
+    const int passes = gemv ? batch : 1;
+    for (int b0 = 0; b0 < passes; b0 += per_pass) {
+        const int nb = gemv ? std::min(per_pass, batch - b0) : 0;
+        a.batch = nb;
+        a.x = gemv ? x + (int64_t)b0 * K : nullptr;
+        if (gemv) a.m.y = y + (int64_t)b0 * W->hdr.n_rows;
+        const int rc = launch_fp8(gemv, a, fixed + xrow * nb, grid, warps * 32, s);
+        if (rc != EC_OK) return rc;
+    }
+    return EC_OK;
+}
+
 /* ---- E8 decode: begin ---- */
 /* E8 decode: one CTA per SM, the 17 tables in shared memory, two tile buffers per warp. */
 /* Warps per CTA and tile buffers per warp.  Two buffers when 32 warps fit with
@@ -2347,8 +2598,11 @@ extern "C" int ec_gemv_group(const ec_matrix* const* Ws, int count, const uint16
     if (Ws[0]->hdr.k_cols > 0 && (!x || !aligned16(x))) return EC_ERR_INVALID_ARG;
     if (Ws[0]->kind == EC_KIND_E8) return EC_ERR_UNSUPPORTED; /* decoded to a dense matrix instead */
     if (Ws[0]->kind == EC_KIND_HUFFMAN_BF16) return huff_gemv(Ws, count, x, ys, batch, stream, dev, d);
-    for (int k = 0; k < count; ++k)
-        if ((rc = rans_run(Ws[k], x, ys[k], nullptr, batch, stream, d)) != EC_OK) return rc;
+    for (int k = 0; k < count; ++k) {
+        rc = Ws[0]->kind == EC_KIND_RANS_FP8 ? fp8_run(Ws[k], x, ys[k], nullptr, batch, stream, d)
+                                              : rans_run(Ws[k], x, ys[k], nullptr, batch, stream, d);
+        if (rc != EC_OK) return rc;
+    }
     return EC_OK;
 }
 
@@ -2386,6 +2640,10 @@ extern "C" int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs
         if (n > 0 && (!outs[k] || !aligned16(outs[k]))) return EC_ERR_INVALID_ARG;
         if (Ws[k]->kind == EC_KIND_RANS_INT4) {
             if ((rc = rans_run(Ws[k], nullptr, nullptr, outs[k], 1, stream, d)) != EC_OK) return rc;
+            continue;
+        }
+        if (Ws[k]->kind == EC_KIND_RANS_FP8) {
+            if ((rc = fp8_run(Ws[k], nullptr, nullptr, outs[k], 1, stream, d)) != EC_OK) return rc;
             continue;
         }
         if (Ws[k]->kind == EC_KIND_E8) {

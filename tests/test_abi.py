@@ -83,18 +83,18 @@ def test_argument_validation(ec):
 
 
 # --------------------------------------------------------------- blob reader
-HDR = struct.Struct("<IIii" + "q" * 10 + "i" * 6 + "I")
+HDR = struct.Struct("<IIii" + "q" * 10 + "i" * 6 + "Ii" + "qqq")
 
 
 HDR_KEYS = ["magic", "version", "kind", "steps", "n_rows", "k_cols", "k_pad", "n_tiles", "table_off",
             "table_words", "scales_off", "tile_off_off", "records_off", "blob_bytes", "max_code_bytes",
-            "prob_bits", "max_words", "max_len", "rans_tuple", "window_code_bytes", "e8_scale_bits"]
+            "prob_bits", "max_words", "max_len", "rans_tuple", "window_code_bytes", "e8_scale_bits",
+            "fp8_table_size", "esc_off_off", "esc_records_off", "n_escapes"]
 
 
 def hdr_offset(key: str) -> int:
-    """Byte offset of a header field."""
-    i = HDR_KEYS.index(key)
-    return 16 + 8 * 10 + 4 * (i - 14) if i >= 14 else (4 * i if i < 4 else 16 + 8 * (i - 4))
+    """Byte offset of a header field (the fields are naturally aligned: no padding)."""
+    return struct.calcsize("<" + HDR.format[1:][: HDR_KEYS.index(key)])
 
 
 def parse(blob: bytes):
@@ -628,3 +628,100 @@ def test_e8_matrices_have_no_gemv(ec):
     with pytest.raises(ec.EcError) as e:
         ec.gemv_path([W], 1)
     assert e.value.code == -4
+
+
+# --------------------------------------------------------------- FP8 top-t tables with escapes
+def fp8_padded(codes: np.ndarray, k_pad: int) -> np.ndarray:
+    n, k = codes.shape
+    out = np.zeros((n, k_pad), dtype=np.uint8)
+    out[:, :k] = codes
+    return out
+
+
+@pytest.mark.parametrize("shape,tile,t,b", [((7, 300), 128, 16, 12), ((64, 1000), 4096, 0, 12),
+                                            ((3, 4096), 1024, 2, 9), ((1, 1), 4096, 1, 10),
+                                            ((40, 4096), 4096, 64, 11)])
+def test_fp8_blob_matches_oracle_stream(ec, shape, tile, t, b):
+    """The library's slot table, symbol values, states, payload words and correction
+    records equal the oracle's encoding of the padded layout, word for word."""
+    codes, r = synth.make_fp8_case(8000 + shape[1], *shape)
+    W = ec.encode_fp8(codes, r, top_t=t, prob_bits=b, tile_syms=tile, device=-1)
+    h, dev = parse(W.serialize())
+    assert h["kind"] == ec.EC_KIND_RANS_FP8 and h["k_pad"] == (shape[1] + 127) // 128 * 128
+    o = O.Fp8(fp8_padded(codes, h["k_pad"]), t=t or 256, prob_bits=b, tile=tile)
+    assert h["fp8_table_size"] == o.tsize and h["n_tiles"] == o.n_tiles and h["n_escapes"] == o.n_records
+    M = 1 << b
+    tab = np.frombuffer(dev, np.uint32, M, h["table_off"]).astype(np.int64)
+    freqs = o.freqs.astype(np.int64)
+    cum = np.concatenate([[0], np.cumsum(freqs)[:-1]])
+    sym, bias, f = tab & 0xFF, (tab >> 8) & 0xFFF, (tab >> 20) + 1
+    assert np.array_equal(np.bincount(sym, minlength=o.tsize), freqs)
+    assert np.array_equal(f, freqs[sym]) and np.array_equal(bias, np.arange(M) - cum[sym])
+    vals = np.frombuffer(dev, np.float32, 512, h["table_off"] + 4 * M)
+    assert np.array_equal(vals[: o.tsize], O.e4m3_to_f32(o.table)) and not vals[o.tsize:256].any()
+    allv = O.e4m3_to_f32(np.arange(256))
+    assert np.array_equal(vals[256:], allv, equal_nan=True)
+    assert np.array_equal(np.frombuffer(dev, np.float32, shape[0], h["scales_off"]), r)
+    toff = np.frombuffer(dev, np.uint32, h["n_tiles"] + 1, h["tile_off_off"]).astype(np.int64)
+    ooff, pay = o.offsets.astype(np.int64), o.payload()
+    for tt in range(h["n_tiles"]):
+        base = h["records_off"] + 16 * toff[tt]
+        assert np.array_equal(np.frombuffer(dev, np.uint32, 32, base), o.states[tt]), tt
+        nw = int(ooff[tt + 1] - ooff[tt])
+        words = np.frombuffer(dev, np.uint16, 8 * (toff[tt + 1] - toff[tt]) - 64, base + 128)
+        assert np.array_equal(words[:nw], pay[ooff[tt]:ooff[tt + 1]]), tt
+    eoff = np.frombuffer(dev, np.uint32, h["n_tiles"] + 1, h["esc_off_off"])
+    assert np.array_equal(eoff, o.rec_off)
+    recs = np.frombuffer(dev, np.uint32, h["n_escapes"], h["esc_records_off"])
+    assert np.array_equal(recs, o.records)
+    if t == 0:
+        assert h["n_escapes"] == 0
+
+
+def test_fp8_argument_validation(ec):
+    from lossless_entropy_coded_gb300 import _ec
+    codes, r = synth.make_fp8_case(5, 4, 256)
+    h = ctypes.c_void_p()
+
+    def enc(c, n, k, prm=None, rs=r):
+        cc = np.ascontiguousarray(c, np.uint8)
+        return _ec.lib.ec_encode_fp8(cc.ctypes.data, rs.ctypes.data, n, k, ctypes.byref(prm) if prm else None, -1,
+                                     ctypes.byref(h))
+
+    assert enc(codes, 4, 256) == 0
+    _ec.lib.ec_free(h)
+    assert enc(codes, -1, 256) == _ec.EC_ERR_SHAPE
+    for prm in [(13, 4096, 0), (8, 4096, 0), (12, 64, 0), (12, 8192, 0), (12, 4096, 257), (12, 4096, -1)]:
+        assert enc(codes, 4, 256, _ec.Fp8Params(*prm)) == _ec.EC_ERR_INVALID_ARG, prm
+    for nan in (0x7F, 0xFF):
+        bad = codes.copy(); bad[2, 9] = nan
+        assert enc(bad, 4, 256) == _ec.EC_ERR_INVALID_ARG
+    bad_r = r.copy(); bad_r[0] = np.inf
+    assert enc(codes, 4, 256, rs=bad_r) == _ec.EC_ERR_INVALID_ARG
+
+
+def test_fp8_rejects_structural_corruption(ec):
+    codes, r = synth.make_fp8_case(6, 20, 1000)
+    W = ec.encode_fp8(codes, r, top_t=24, device=-1)
+    blob = W.serialize()
+    W2 = ec.deserialize(blob, device=-1)
+    assert W2.stats() == W.stats() and W2.kind == ec.EC_KIND_RANS_FP8
+    h, dev = parse(blob)
+    assert h["n_escapes"] > 2
+    meta = len(blob) - len(dev)
+    er = meta + h["esc_records_off"]
+    rec0 = struct.unpack_from("<I", blob, er)[0]
+    cases = []
+    for name, off, fmt, val in [("table size", meta + hdr_offset("fp8_table_size"), "<i", 0),
+                                ("symbol outside the table", meta + h["table_off"], "<I", 200 | (1 << 20)),
+                                ("record position", er, "<I", 0xFFFF | (rec0 & 0xFF0000)),
+                                ("record high bits", er, "<I", rec0 | 0x01000000),
+                                ("record order", er + 4, "<I", rec0),
+                                ("record count", meta + hdr_offset("n_escapes"), "<q", h["n_escapes"] - 1),
+                                ("record offsets", meta + h["esc_off_off"] + 4, "<I", 0xFFFFFF)]:
+        x = bytearray(blob); struct.pack_into(fmt, x, off, val)
+        cases.append((name, bytes(x)))
+    for name, bad in cases:
+        with pytest.raises(ec.EcError) as e:
+            ec.deserialize(bad, device=-1)
+        assert e.value.code == -5, name
