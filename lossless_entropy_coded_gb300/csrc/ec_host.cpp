@@ -1325,7 +1325,7 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
             if ((int32_t)(tab[i] & 0xFF) >= h.fp8_table_size || f > (1u << h.prob_bits) || k >= f) return EC_ERR_CORRUPT;
         }
     } else if (h.rans_tuple == 1) {
-        for (int64_t i = 0; i < h.table_words; ++i) {
+        for (int64_t i = 0; i < h.table_words && n_pad > 0; ++i) { /* an empty matrix has an empty table */
             const uint32_t f = tab[i] >> 16, k = (tab[i] >> 4) & 0xFFF;
             if (f == 0 || f > (1u << h.prob_bits) || k >= f) return EC_ERR_CORRUPT;
         }
