@@ -742,3 +742,32 @@ def test_empty_matrices_round_trip(ec, kind):
     assert h["n_tiles"] == 0 and h["n_rows"] == 0
     W2 = ec.deserialize(W.serialize(), device=-1)
     assert W2.stats() == W.stats()
+
+
+@pytest.mark.parametrize("kind", ["huffman", "rans", "rans_pair", "e8", "fp8"])
+def test_validator_survives_random_corruption(ec, kind):
+    """Random byte changes anywhere in the metadata part of a blob (header, tables,
+    offsets, records): deserialisation accepts or reports EC_ERR_CORRUPT, never
+    anything else (and never crashes)."""
+    rng = np.random.default_rng(len(kind))
+    if kind == "huffman":
+        W = ec.encode_bf16(synth.llama_bf16(9001, 24, 1000), device=-1)
+    elif kind.startswith("rans"):
+        W = ec.encode_rans(*synth.make_rans_case(0, 24, 1000), device=-1, codes_per_symbol=2 if kind == "rans_pair" else 1)
+    elif kind == "e8":
+        q2, r, s = synth.make_e8_case(9002, 24, 1000)
+        W = ec.encode_e8(q2, r, s, tile_vectors=96, device=-1)
+    else:
+        W = ec.encode_fp8(*synth.make_fp8_case(9003, 24, 1000), top_t=20, device=-1)
+    blob = W.serialize()
+    h, dev = parse(blob)
+    meta = len(blob) - len(dev)
+    hot = meta + h["records_off"] + 256  # header, tables, scales, offsets and the first records
+    for _ in range(300):
+        x = bytearray(blob)
+        for _ in range(int(rng.integers(1, 4))):
+            x[int(rng.integers(meta, min(hot, len(x))))] = int(rng.integers(0, 256))
+        try:
+            ec.deserialize(bytes(x), device=-1)
+        except ec.EcError as e:
+            assert e.code == -5
