@@ -197,7 +197,8 @@ int ec_encode_fp8(const uint8_t* codes_host, const float* row_scales_host, int64
 
 /* Decode W to dense row-major BF16 [n_rows, k_cols] in device memory out_bf16.
  * Huffman: the original bit patterns.  rANS: BF16 round-to-nearest-even of
- * code * scale. */
+ * code * scale.  FP8: of fp32(value * r_i), correction records applied.  E8: as
+ * ec_decode_as with EC_DTYPE_BF16. */
 int ec_decode(const ec_matrix* W, uint16_t* out_bf16, cudaStream_t stream);
 
 /* Decode `count` matrices (1..EC_MAX_DECODE_BATCH) in one launch, the way
@@ -223,7 +224,8 @@ int ec_decode_as(const ec_matrix* W, void* out, int dtype, cudaStream_t stream);
  * passes of up to 16 rows), or, from batch 6 (EC_MMA_MIN_BATCH overrides) when
  * every tile lies inside a row (the automatic tile size ensures it) and k_cols % 8
  * == 0, on the tensor cores (tcgen05, BF16 products, FP32 accumulators; passes of
- * up to 32 rows).  ec_gemv_path tells which. */
+ * up to 32 rows).  ec_gemv_path tells which.  rANS and FP8 matrices run on the CUDA
+ * cores; E8 matrices return EC_ERR_UNSUPPORTED (decode them instead). */
 int ec_gemv(const ec_matrix* W, const uint16_t* x_bf16, float* y, int batch, cudaStream_t stream);
 
 enum { EC_PATH_CUDA_CORES = 1, EC_PATH_TENSOR_CORES = 2 };
@@ -250,8 +252,8 @@ int ec_gemv_group(const ec_matrix* const* Ws, int count, const uint16_t* x_bf16,
  * output row, tile covering that row); the tiles' partial sums are added in tile
  * order by a second small kernel, so repeated calls give identical y.
  * Limits: batch * n_rows * (ceil(k_pad / tile) + 1) partial sums must fit in that
- * array (about 1M floats), otherwise EC_ERR_UNSUPPORTED; rANS matrices also return
- * EC_ERR_UNSUPPORTED.  The first call on a device looks up the array's device
+ * array (about 1M floats), otherwise EC_ERR_UNSUPPORTED; rANS, FP8 and E8 matrices
+ * also return EC_ERR_UNSUPPORTED.  The first call on a device looks up the array's device
  * address (cudaGetSymbolAddress) and the device's limits once; make that first call
  * before any stream capture.  All calls share the one array: calls whose work
  * overlaps on the GPU (other streams, other threads) race and corrupt each other's
