@@ -66,11 +66,7 @@ typedef struct ec_matrix ec_matrix; /* opaque: host descriptor + one device blob
 /* Huffman-exponent codec parameters (NULL = defaults).
  *  max_code_len  longest codeword, 1..24 (default EC_DEFAULT_MAX_CODE_LEN = 12);
  *                the code is textbook Huffman when it fits, otherwise the
- *                optimal length-limited code (package-merge).  At 12 every
- *                codeword fits the decoder's first table lookup; on LLM
- *                weights the limit costs about 0.004 bits per exponent over
- *                the unconstrained code.  Longer limits decode through a
- *                hierarchical table in global memory, more slowly.
+ *                optimal length-limited code (package-merge).
  *  tile_steps    symbols per lane in one tile of 32 lanes: a multiple of 16 up
  *                to 128, or 0 (the default) to choose by size: 128 (4096-weight
  *                tiles, 0.125 bit per weight of lane offsets) for matrices of at
@@ -78,11 +74,25 @@ typedef struct ec_matrix ec_matrix; /* opaque: host descriptor + one device blob
  *                has about 1024 tiles or more to spread over the SMs, then lowered
  *                in steps of 16 until 32 * tile_steps divides the padded row (for
  *                K = 14336: 112), so that no tile crosses a row; only such
- *                matrices take the tensor-core GEMV (ec_gemv). */
+ *                matrices take the tensor-core GEMV (ec_gemv).
+ *  hierarchical  0 (default): the decoder reads two codewords per lookup of a
+ *                12-bit window and never branches on the data.  Where a lane's two
+ *                consecutive codewords overflow the window (about 0.6 % of pairs
+ *                on LLM weights; also every codeword longer than 12 bits), the
+ *                encoder codes the shortest-coded exponent instead and keeps the
+ *                true one in a 32-bit correction record of the tile (MINE section
+ *                4, "Escapes"), about 0.08 bit per weight.  When two of the
+ *                shortest codewords exceed 12 bits (exponents nearly uniform) the
+ *                encoder takes the hierarchical mode instead.
+ *                1: no records; pairs that overflow the window and longer
+ *                codewords are decoded through DFloat11's hierarchical tables
+ *                (appendix, Fig. 14: 8-bit sub-tables behind the 12-bit first
+ *                level), one data-dependent branch per pair. */
 typedef struct {
     int32_t max_code_len;
     int32_t tile_steps;
-    int32_t reserved[2];
+    int32_t hierarchical;
+    int32_t reserved;
 } ec_huff_params;
 
 /* rANS codec parameters (NULL = defaults).
@@ -153,6 +163,8 @@ typedef struct {
     double bits_per_weight;    /* device_bytes * 8 / (n_rows * k_cols) */
     double entropy_bits;       /* H of the coded symbol (exponent byte or 4-bit code), Eq.(2) */
     double coded_bits_per_symbol; /* payload_bits / coded symbols */
+    int64_t n_records;         /* 32-bit correction records (FP8 escapes, Huffman window records),
+                                * counted in aux_bytes */
 } ec_stats_t;
 
 /* Encode a row-major BF16 matrix [n_rows, k_cols] (host memory, bit patterns) with

@@ -42,7 +42,8 @@ EXPORTS = ["ec_encode_bf16", "ec_encode_rans", "ec_decode", "ec_decode_batch", "
 
 
 class HuffParams(ctypes.Structure):
-    _fields_ = [("max_code_len", ctypes.c_int32), ("tile_steps", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2)]
+    _fields_ = [("max_code_len", ctypes.c_int32), ("tile_steps", ctypes.c_int32), ("hierarchical", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class RansParams(ctypes.Structure):
@@ -65,7 +66,7 @@ class Stats(ctypes.Structure):
                 ("payload_bits", ctypes.c_int64), ("raw_bytes", ctypes.c_int64), ("aux_bytes", ctypes.c_int64),
                 ("table_bytes", ctypes.c_int64), ("device_bytes", ctypes.c_int64),
                 ("bits_per_weight", ctypes.c_double), ("entropy_bits", ctypes.c_double),
-                ("coded_bits_per_symbol", ctypes.c_double)]
+                ("coded_bits_per_symbol", ctypes.c_double), ("n_records", ctypes.c_int64)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -178,11 +179,13 @@ class Matrix:
             pass
 
 
-def encode_bf16(w, max_code_len: int = 12, tile_steps: int = 0, device: int = 0) -> Matrix:
-    """Huffman-exponent encode a host BF16 matrix [N, K] (uint16 bit patterns)."""
+def encode_bf16(w, max_code_len: int = 12, tile_steps: int = 0, device: int = 0, hierarchical: bool = False) -> Matrix:
+    """Huffman-exponent encode a host BF16 matrix [N, K] (uint16 bit patterns);
+    hierarchical=True decodes overflowing pairs through DFloat11's hierarchical tables
+    instead of window records."""
     n, k = int(w.shape[0]), int(w.shape[1])
     p, keep = _host_ptr(w)
-    prm = HuffParams(max_code_len, tile_steps)
+    prm = HuffParams(max_code_len, tile_steps, 1 if hierarchical else 0)
     h = ctypes.c_void_p()
     _check(lib.ec_encode_bf16(p, n, k, ctypes.byref(prm), device, ctypes.byref(h)), "ec_encode_bf16")
     del keep

@@ -5,11 +5,13 @@
  * One contiguous device blob per matrix:
  *
  *   [ec_blob_header, 256 B]
- *   [decode table]            Huffman: pair table, then the hierarchical table
- *                             (level 1 + 256-entry sub-tables).
+ *   [decode table]            Huffman: pair table, then (without window records)
+ *                             the hierarchical sub-tables (256 entries each).
  *                             rANS:    2^prob_bits u32 slot entries.
  *   [group scales]            rANS only: FP16 [n_rows, k_pad / 128].
  *   [tile offsets]            u32 [n_tiles + 1], record start in 16-byte units.
+ *   [correction records]      FP8: u32 record offsets [n_tiles + 1], then the u32
+ *                             records.
  *   [tile records]            16-byte aligned, variable length.
  *
  * Coded layout of the weights.  The matrix is padded at the end of every row to
@@ -23,16 +25,42 @@
  *
  * Huffman tile record (DFloat11's EncodedExponent / PackedSignMantissa /
  * per-thread start offsets, re-cut so every lane owns a fixed number of symbols):
- *   u16 lane_start[32]        byte offset of lane l's codewords in the code area
- *   u8  raw[32 * S16]         (sign << 7) | mantissa, lane-transposed in 16-byte
+ *   u16 lane_start[32]        byte offset of lane l's codewords in the code area;
+ *                             lane 0 starts at 0, and its slot holds the number of
+ *                             window records of the tile instead
+ *   u8  raw[32 * S16]         sign and mantissa bits, lane-transposed in 16-byte
  *                             chunks: chunk j of lane l (bytes (32 j + l) * 16 ..
  *                             + 15) holds lane l's symbols 16 j .. 16 j + 15, so a
  *                             warp reading chunk j reads 512 contiguous bytes;
- *                             S16 = steps rounded up to 16, the tail zero
+ *                             S16 = steps rounded up to 16, the tail zero.  Each
+ *                             little-endian u32 r of a chunk holds symbols i .. i + 3
+ *                             (i % 4 == 0) with their sign / mantissa bits where a
+ *                             BF16 pair keeps them: the bits 0x807F807F of r are
+ *                             [w(i+1) | w(i)], those of r rotated right by 8 are
+ *                             [w(i+3) | w(i+2)].  Byte by byte:
+ *                               byte 0 = sign(i+3) << 7 | mant(i)
+ *                               byte 1 = sign(i)   << 7 | mant(i+2)
+ *                               byte 2 = sign(i+2) << 7 | mant(i+1)
+ *                               byte 3 = sign(i+1) << 7 | mant(i+3)
  *   u32 code[]                the code area: lane 0's codewords, then lane 1's, ...
- *                             each lane starting on a byte boundary; bit b of the
- *                             area is bit 31 - (b % 32) of word b / 32 (MSB first);
- *                             followed by >= 8 zero bytes, padded to 16 bytes.
+ *                             each lane starting on a byte boundary, LSB first: bit
+ *                             b of the area is bit b % 32 of word b / 32 (bit b % 8
+ *                             of byte b / 8), and a codeword's first bit (its most
+ *                             significant in the canonical code) comes first;
+ *                             followed by >= 8 zero bytes, padded to 16 bytes
+ *   u32 rec[n]                the tile's window records (n = lane_start[0]), zero-
+ *                             padded to 16 bytes
+ * Window records (window_records = 1): the decoder reads two codewords per lookup
+ * of a 12-bit window.  Wherever the two codewords of a lane's pair (symbols 2m,
+ * 2m + 1) would not both fit in 12 bits, the encoder writes the codeword of the
+ * shortest-coded exponent (header field huff_fill) in place of one (or both) and
+ * lists the weight in a record of the tile: u32 position in the tile (12 bits) |
+ * (sign << 7 | mantissa) << 12 | true exponent << 20, ascending positions, so a
+ * record alone gives both the true and the coded weight (MINE section 4,
+ * "Escapes", applied to exponent pairs).  The records follow the code area in the
+ * tile record, so the copy that stages the code area brings them along (up to the
+ * decoder's staging room).  Huffman tiles hold at most 4096 positions.  Without window records every pair that overflows the window, and
+ * every codeword longer than 12 bits, is decoded through the hierarchical tables.
  *
  * E8 matrices (kind 3): rows padded to k_pad (a multiple of EC_E8_ROW_ALIGN) with
  * zero points, flattened row-major into 8-weight vectors and cut into tiles of
@@ -52,7 +80,7 @@
 #include <stdint.h>
 
 #define EC_BLOB_MAGIC 0x31434345u /* "ECC1" */
-#define EC_BLOB_VERSION 8u
+#define EC_BLOB_VERSION 10u
 
 #define EC_L1_BITS 12            /* level-1 Huffman window */
 #define EC_SUB_BITS 8            /* bits per sub-table level */
@@ -71,30 +99,38 @@
 /* Huffman decode tables, in this order inside the table section:
  *
  * 1. pair table, 2^EC_L1_BITS u32 entries indexed by the next EC_L1_BITS bits of
- *    a lane's stream.  Entry layout (fields chosen so that the entry is already
- *    the exponent half of two BF16 weights [w(i+1) | w(i)]):
- *      bits  7..14  exponent of the first codeword in the window
- *      bits 23..30  exponent of the second codeword (pairs only)
- *      bits  0..3   total length of the two codewords when both end inside the
- *                   window, else 0
+ *    a lane's stream (the first stream bit is bit 0 of the index).  Fields sit
+ *    where they cost the decoder nothing: the two exponents already in the BF16
+ *    exponent fields of [w(i+1) | w(i)], everything else under the sign and
+ *    mantissa bits that the merge with the raw bytes overwrites:
+ *      bits  0..3   advance: the total length of the two codewords when both end
+ *                   inside the window; else the first codeword's length when it
+ *                   ends inside it; else 0
+ *      bits  4..6   0 (the decoder adds whole entries to its bit position, whose
+ *                   bit 5 then flips exactly when the position crosses a word)
+ *      bits  7..14  exponent of the first codeword; for a first codeword longer
+ *                   than the window, bits 7..15 are the index of its level-2
+ *                   sub-table instead
  *      bits 16..19  length of the first codeword when it ends inside the window,
- *                   else 0 (longer than the window, or no codeword matches)
- *      all other bits 0.
- *    The decoder reads bits 0..3 to advance; 0 sends it to a second lookup for
- *    the second codeword and, when bits 16..19 are 0 too, to table 2.
- * 2. hierarchical table (u32 entries, below): a 2^EC_L1_BITS level-1 table then
- *    256-entry sub-tables (DFloat11 appendix, Fig. 4 / Fig. 14). */
+ *                   else 0
+ *      bits 23..30  exponent of the second codeword (complete pairs only)
+ *      bit  31      1 when the pair is not complete (second codeword outside the
+ *                   window, first codeword longer than it, or no codeword matches)
+ * 2. hierarchical sub-tables (only without window records): 256 u32 entries each,
+ *    indexed by the next 8 stream bits after the bits already consumed (DFloat11
+ *    appendix, Fig. 4 / Fig. 14, behind a 12-bit first level that is the pair
+ *    table):
+ *      symbol:  bits 0..15 = exponent << 7, bits 16..20 = total code length
+ *      pointer: bit 31 = 1, bits 0..15 = sub-table index, bits 16..20 = stream bits
+ *               consumed before that sub-table (20)
+ *      invalid: bit 30 = 1 (a window no codeword matches). */
 #define EC_PAIR_LEN_MASK 0x0000000Fu
 #define EC_PAIR_FIRST_SHIFT 16
-#define EC_PAIR_FIELDS 0x7F8F7F8Fu /* every bit a valid entry may set */
+#define EC_PAIR_OPEN 0x80000000u   /* pair not complete */
+#define EC_PAIR_FIELDS 0xFF8FFF8Fu /* every bit a valid entry may set */
+#define EC_HUFF_WINDOW_REC 1       /* ec_blob_header.huff_flags: window records in use */
 
-/* Huffman table entry (u32):
- *   symbol:  bits 0..15 = exponent << 7 (the BF16 exponent field), bits 16..20 =
- *            total code length, bits 21..31 = 0
- *   pointer: bit 31 = 1, bits 0..15 = sub-table index, bits 16..20 = bits already
- *            consumed before the sub-table
- *   invalid: bit 30 = 1 (a window no codeword matches; only reachable from corrupt
- *            data or the padding of a one-symbol code). */
+/* Huffman sub-table entry (u32), see above. */
 #define EC_ENT_PTR 0x80000000u
 #define EC_ENT_BAD 0x40000000u
 
@@ -125,7 +161,7 @@ typedef struct {
     int64_t tile_off_off;             /* byte offset of u32 tile offsets */
     int64_t records_off;              /* byte offset of the first record */
     int64_t blob_bytes;
-    int32_t max_code_bytes;           /* Huffman: largest code area of any tile (bytes) */
+    int32_t max_code_bytes;           /* Huffman: largest records + code area of any tile (bytes) */
     int32_t prob_bits;                /* rANS */
     int32_t max_words;                /* rANS: largest payload of any tile (u16 words) */
     int32_t max_len;                  /* Huffman: longest codeword in use */
@@ -137,8 +173,12 @@ typedef struct {
     int32_t fp8_table_size;           /* FP8: codes in the decoding table (1..256) */
     int64_t esc_off_off;              /* FP8: byte offset of u32 record offsets [n_tiles + 1] */
     int64_t esc_records_off;          /* FP8: byte offset of the u32 correction records */
-    int64_t n_escapes;                /* FP8: correction records */
-    uint8_t pad[256 - 4 * 4 - 8 * 10 - 4 * 8 - 8 * 3];
+    int64_t n_escapes;                /* FP8 and Huffman: correction records */
+    int32_t huff_flags;               /* Huffman: EC_HUFF_WINDOW_REC */
+    int32_t huff_sub_tables;          /* Huffman: hierarchical sub-tables after the pair table */
+    int32_t huff_fill;                /* Huffman with window records: the exponent coded in place of a recorded one */
+    int32_t max_code_area;            /* Huffman: largest code area of any tile (records excluded) */
+    uint8_t pad[256 - 4 * 4 - 8 * 10 - 4 * 8 - 8 * 3 - 4 * 4];
 } ec_blob_header;
 
 #endif /* EC_FORMAT_H_ */

@@ -200,67 +200,117 @@ void canonical(const uint8_t len[256], uint32_t code[256]) {
     }
 }
 
-/* Hierarchical decode table: a 2^EC_L1_BITS level-1 table, then 256-entry tables
- * for every prefix that leads to longer codewords (the decomposition of
- * DFloat11's appendix, Fig. 4 / Fig. 14, with a wider first level). */
-std::vector<uint32_t> build_huff_table(const uint8_t len[256], const uint32_t code[256]) {
-    struct Tab {
-        uint32_t prefix;
-        int depth, width;
-        size_t base;
+/* The codeword of length l with canonical value c, in stream order: its first
+ * (most significant) bit becomes bit 0. */
+uint32_t stream_bits(uint32_t c, int l) {
+    uint32_t r = 0;
+    for (int i = 0; i < l; ++i) r |= ((c >> (l - 1 - i)) & 1u) << i;
+    return r;
+}
+
+/* Decode tables of the LSB-first stream (layout in ec_format.h).  one[w] names the
+ * codeword that a 12-bit window w starts with: exponent << 7 | length << 16 for a
+ * codeword that ends inside the window, EC_ENT_PTR for the 12-bit prefix of a
+ * longer one, EC_ENT_BAD where nothing matches (corrupt data, or the unused half of
+ * a one-symbol code's space). */
+struct HuffTables {
+    std::vector<uint32_t> pair; /* 2^EC_L1_BITS entries */
+    std::vector<uint32_t> sub;  /* hierarchical sub-tables, 256 entries each */
+};
+
+HuffTables build_huff_tables(const uint8_t len[256], const uint32_t code[256], bool hierarchical) {
+    const uint32_t W = EC_L1_BITS, mask = (1u << W) - 1;
+    std::vector<uint32_t> one(1u << W, EC_ENT_BAD);
+    HuffTables t;
+    /* level-2 sub-table of each 12-bit prefix of a longer codeword, level-3 of each
+     * 20-bit prefix of a codeword longer than 20 bits (codewords are at most 24) */
+    std::vector<int> l2(1u << W, -1);
+    std::vector<std::pair<uint32_t, int>> l3; /* (20-bit prefix, sub-table) */
+    auto new_sub = [&]() {
+        t.sub.resize(t.sub.size() + 256, EC_ENT_BAD);
+        return (int)(t.sub.size() / 256 - 1);
     };
-    std::vector<uint32_t> t(1u << EC_L1_BITS, EC_ENT_BAD);
-    std::vector<Tab> tabs{{0, 0, EC_L1_BITS, 0}};
-    for (size_t k = 0; k < tabs.size(); ++k) {
-        const Tab tb = tabs[k];
-        for (int s = 0; s < 256; ++s) {
-            const int l = len[s];
-            if (l <= tb.depth) continue;
-            if (tb.depth && (code[s] >> (l - tb.depth)) != tb.prefix) continue;
-            const int rem = l - tb.depth;
-            const uint32_t tail = code[s] & ((1u << rem) - 1);
-            if (rem <= tb.width) {
-                const uint32_t lo = tail << (tb.width - rem), hi = (tail + 1) << (tb.width - rem);
-                for (uint32_t i = lo; i < hi; ++i) t[tb.base + i] = ((uint32_t)s << 7) | ((uint32_t)l << 16);
-            } else {
-                const uint32_t idx = tail >> (rem - tb.width);
-                uint32_t& e = t[tb.base + idx];
-                if (!(e & EC_ENT_PTR)) {
-                    const size_t sub = tabs.size();
-                    tabs.push_back({(tb.prefix << tb.width) | idx, tb.depth + tb.width, EC_SUB_BITS,
-                                    t.size()});
-                    t.resize(t.size() + (1u << EC_SUB_BITS), EC_ENT_BAD);
-                    t[tb.base + idx] = EC_ENT_PTR | (uint32_t)(sub - 1) | ((uint32_t)(tb.depth + tb.width) << 16);
-                }
-            }
+    for (int s = 0; s < 256; ++s) {
+        const int l = len[s];
+        if (!l) continue;
+        const uint32_t bits = stream_bits(code[s], l), sym = ((uint32_t)s << 7) | ((uint32_t)l << 16);
+        if (l <= (int)W) {
+            for (uint32_t hi = 0; hi < (1u << (W - l)); ++hi) one[bits | (hi << l)] = sym;
+            continue;
         }
+        const uint32_t p12 = bits & mask;
+        one[p12] = EC_ENT_PTR;
+        if (!hierarchical) continue;
+        if (l2[p12] < 0) l2[p12] = new_sub();
+        const int t2 = l2[p12];
+        const int rem = l - (int)W;
+        if (rem <= 8) {
+            for (uint32_t hi = 0; hi < (1u << (8 - rem)); ++hi) t.sub[256 * t2 + ((bits >> W) | (hi << rem))] = sym;
+            continue;
+        }
+        const uint32_t p20 = bits & 0xFFFFFu, i2 = (bits >> W) & 0xFFu;
+        int t3 = -1;
+        for (auto& q : l3)
+            if (q.first == p20) t3 = q.second;
+        if (t3 < 0) {
+            t3 = new_sub();
+            l3.push_back({p20, t3});
+            t.sub[256 * t2 + i2] = EC_ENT_PTR | (uint32_t)t3 | (20u << 16);
+        }
+        const int rem3 = l - 20;
+        for (uint32_t hi = 0; hi < (1u << (8 - rem3)); ++hi) t.sub[256 * t3 + ((bits >> 20) | (hi << rem3))] = sym;
+    }
+    /* pair entries: the first codeword, and the second when it ends inside the window
+     * too (the window shifted right by the first length names it; it counts only if
+     * its length fits the bits that remain) */
+    t.pair.assign(EC_PAIR_WORDS, 0);
+    for (uint32_t w = 0; w <= mask; ++w) {
+        const uint32_t a = one[w];
+        if (a & EC_ENT_BAD) {
+            t.pair[w] = EC_PAIR_OPEN;
+            continue;
+        }
+        if (a & EC_ENT_PTR) { /* first codeword longer than the window: its sub-table */
+            t.pair[w] = EC_PAIR_OPEN | (hierarchical ? ((uint32_t)l2[w] << 7) : 0u);
+            continue;
+        }
+        const uint32_t l0 = (a >> 16) & 31, e0 = (a & 0xFFFFu) >> 7;
+        uint32_t ent = (e0 << 7) | (l0 << EC_PAIR_FIRST_SHIFT);
+        const uint32_t b = one[w >> l0];
+        const uint32_t l1 = (b >> 16) & 31;
+        if (!(b & (EC_ENT_PTR | EC_ENT_BAD)) && l0 + l1 <= W)
+            ent |= (((b & 0xFFFFu) >> 7) << 23) | (l0 + l1);
+        else
+            ent |= EC_PAIR_OPEN | l0;
+        t.pair[w] = ent;
     }
     return t;
 }
 
-/* Pair table: for every EC_L1_BITS-bit window, the first codeword (when it ends
- * inside the window) and the second one (when it ends inside it too), with their
- * exponents placed in the BF16 exponent fields of two weights.  Built from the
- * hierarchical level-1 table: the window shifted left by the first codeword's
- * length, zero-filled, names the second codeword, which counts only if it ends
- * inside the window. */
-std::vector<uint32_t> build_pair_table(const std::vector<uint32_t>& h) {
-    const uint32_t W = EC_L1_BITS, mask = (1u << W) - 1;
-    std::vector<uint32_t> t(EC_PAIR_WORDS, 0);
-    for (uint32_t v = 0; v <= mask; ++v) {
-        const uint32_t a = h[v];
-        if (a & (EC_ENT_PTR | EC_ENT_BAD)) continue; /* 0: long codeword or no match */
-        const uint32_t l0 = (a >> 16) & 31, e0 = (a & 0xFFFFu) >> 7;
-        uint32_t ent = (e0 << 7) | (l0 << EC_PAIR_FIRST_SHIFT);
-        if (l0 < W) {
-            const uint32_t b = h[(v << l0) & mask];
-            const uint32_t l1 = (b >> 16) & 31;
-            if (!(b & (EC_ENT_PTR | EC_ENT_BAD)) && l0 + l1 <= W)
-                ent |= (((b & 0xFFFFu) >> 7) << 23) | (l0 + l1);
+/* Window records: the pairs (2m, 2m + 1) of one lane whose codewords do not both fit
+ * the decoder's window get the shortest-coded exponent `fill` in place of one
+ * exponent (the second when the first leaves room for fill's codeword, else the
+ * first, and then the second too if it still does not fit).  e[] holds the lane's
+ * exponents in symbol order and is rewritten; each substitution is reported with
+ * rec(symbol index, true exponent).  Needs 2 len[fill] <= 12. */
+template <class Rec>
+void fit_pairs(uint8_t* e, int64_t S, const uint8_t len[256], int fill, Rec&& rec) {
+    const int W = EC_L1_BITS, lf = len[fill];
+    for (int64_t i = 0; i + 1 < S; i += 2) {
+        const int la = len[e[i]], lb = len[e[i + 1]];
+        if (la + lb <= W) continue;
+        if (la + lf <= W) {
+            rec(i + 1, e[i + 1]);
+            e[i + 1] = (uint8_t)fill;
+            continue;
         }
-        t[v] = ent;
+        rec(i, e[i]);
+        e[i] = (uint8_t)fill;
+        if (lf + lb > W) {
+            rec(i + 1, e[i + 1]);
+            e[i + 1] = (uint8_t)fill;
+        }
     }
-    return t;
 }
 
 /* ------------------------------------------------------------ rANS frequencies */
@@ -399,8 +449,10 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
     if (n_rows < 0 || k_cols < 0) return EC_ERR_SHAPE;
     const int max_len = params ? params->max_code_len : EC_DEFAULT_MAX_CODE_LEN;
     int steps = params ? params->tile_steps : 0;
+    const int hier_req = params ? params->hierarchical : 0;
     if (max_len < 1 || max_len > EC_MAX_CODE_LEN) return EC_ERR_INVALID_ARG;
     if (steps < 0 || steps > 128 || steps % 16) return EC_ERR_INVALID_ARG;
+    if (hier_req != 0 && hier_req != 1) return EC_ERR_INVALID_ARG;
     int64_t nk = 0, k_pad = round_up(k_cols, EC_HUFF_ROW_ALIGN), n_pad = 0, tmp = 0;
     if (k_cols > INT64_MAX - EC_HUFF_ROW_ALIGN) return EC_ERR_OVERFLOW;
     if (!mul_ok(n_rows, k_cols, &nk) || !mul_ok(n_rows, k_pad, &n_pad) || !mul_ok(n_pad, 4, &tmp))
@@ -445,29 +497,72 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
         }
         uint32_t code[256];
         canonical(m->lengths, code);
-        std::vector<uint32_t> table = build_pair_table(build_huff_table(m->lengths, code));
-        {
-            const std::vector<uint32_t> hier = build_huff_table(m->lengths, code);
-            table.insert(table.end(), hier.begin(), hier.end());
+        /* the exponent with the shortest codeword fills pairs that overflow the window;
+         * window records need two of its codewords to fit the window */
+        int fill = -1;
+        for (int s = 0; s < 256; ++s)
+            if (m->lengths[s] && (fill < 0 || m->lengths[s] < m->lengths[fill])) fill = s;
+        /* records pay when pairs rarely overflow: under independent exponents the share
+         * of pairs with l(a) + l(b) > 12 must stay within 2 % (LLM weights: about 0.6 %) */
+        double over = 0.0, tot = 0.0;
+        for (int s = 0; s < 256; ++s) tot += (double)m->counts[s];
+        for (int a = 0; a < 256 && tot > 0; ++a)
+            for (int b = 0; b < 256; ++b)
+                if (m->counts[a] && m->counts[b] && m->lengths[a] + m->lengths[b] > EC_L1_BITS)
+                    over += (double)m->counts[a] / tot * ((double)m->counts[b] / tot);
+        const bool records = !hier_req && (fill < 0 || (2 * m->lengths[fill] <= EC_L1_BITS && over <= 0.02));
+        const HuffTables tabs = build_huff_tables(m->lengths, code, !records);
+        if (tabs.sub.size() / 256 > 512) { /* sub-table indices have 9 bits */
+            delete m;
+            return EC_ERR_UNSUPPORTED;
         }
+        std::vector<uint32_t> table = tabs.pair;
+        table.insert(table.end(), tabs.sub.begin(), tabs.sub.end());
 
-        /* pass 1: per-tile record sizes */
-        std::vector<int64_t> rec_bytes(n_tiles + 1, 0), code_bytes(n_tiles, 0);
+        /* A lane's exponents in symbol order (lane l owns tile positions 256 (i / 8) +
+         * 8 l + i % 8), after window-record substitution; recs gets the records
+         * (position in the tile | sign and mantissa << 12 | true exponent << 20). */
+        auto lane_exponents = [&](const uint16_t* v, int64_t S, int l, uint8_t* e, std::vector<uint32_t>* recs) {
+            for (int64_t i = 0; i < S; ++i) e[i] = (uint8_t)((v[256 * (i >> 3) + 8 * l + (i & 7)] >> 7) & 0xFF);
+            if (records)
+                fit_pairs(e, S, m->lengths, fill, [&](int64_t i, int true_e) {
+                    if (recs) {
+                        const uint32_t q = (uint32_t)(256 * (i >> 3) + 8 * l + (i & 7)), wq = v[q];
+                        const uint32_t sm = ((wq >> 8) & 0x80u) | (wq & 0x7Fu);
+                        recs->push_back(q | (sm << 12) | ((uint32_t)true_e << 20));
+                    }
+                });
+        };
+
+        /* pass 1: per-tile record sizes and window records */
+        std::vector<int64_t> rec_bytes(n_tiles + 1, 0), code_bytes(n_tiles, 0), n_rec(n_tiles, 0), bits_t(n_tiles, 0),
+            area_bytes(n_tiles, 0);
         parallel_for(n_tiles, [&](int64_t lo, int64_t hi) {
             std::vector<uint16_t> v(T);
+            std::vector<uint8_t> e(T / 32);
+            std::vector<uint32_t> recs;
             for (int64_t t = lo; t < hi; ++t) {
-                const int64_t base = t * T, n_t = std::min(T, n_pad - base);
+                const int64_t base = t * T, n_t = std::min(T, n_pad - base), S = n_t / 32;
                 gather_padded(w, K, KP, base, n_t, v.data());
-                int64_t bits[32] = {0};
-                for (int64_t q = 0; q < n_t; ++q) bits[(q >> 3) & 31] += m->lengths[(v[q] >> 7) & 0xFF];
-                int64_t bytes = 0;
-                for (int l = 0; l < 32; ++l) bytes += (bits[l] + 7) / 8;
-                code_bytes[t] = round_up(bytes + 8, 16);
+                recs.clear();
+                int64_t bytes = 0, bits_all = 0;
+                for (int l = 0; l < 32; ++l) {
+                    lane_exponents(v.data(), S, l, e.data(), &recs);
+                    int64_t bits = 0;
+                    for (int64_t i = 0; i < S; ++i) bits += m->lengths[e[i]];
+                    bytes += (bits + 7) / 8;
+                    bits_all += bits;
+                }
+                /* the tile's window records follow its code area */
+                n_rec[t] = (int64_t)recs.size();
+                area_bytes[t] = round_up(bytes + 8, 16);
+                code_bytes[t] = area_bytes[t] + round_up(4 * n_rec[t], 16);
                 rec_bytes[t] = 64 + EC_RAW_BYTES(n_t / 32) + code_bytes[t];
+                bits_t[t] = bits_all;
             }
         });
         std::vector<uint32_t> tile_off(n_tiles + 1, 0);
-        int64_t total = 0, max_code = 0, payload = 0;
+        int64_t total = 0, max_code = 0, max_area = 0, payload = 0, n_records = 0;
         for (int64_t t = 0; t < n_tiles; ++t) {
             tile_off[t] = (uint32_t)(total / 16);
             if (!add_ok(total, rec_bytes[t], &total)) {
@@ -475,6 +570,9 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
                 return EC_ERR_OVERFLOW;
             }
             max_code = std::max(max_code, code_bytes[t]);
+            max_area = std::max(max_area, area_bytes[t]);
+            payload += bits_t[t];
+            n_records += n_rec[t];
         }
         if (total / 16 > (int64_t)UINT32_MAX) {
             delete m;
@@ -494,10 +592,15 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
         h.table_off = sizeof(ec_blob_header);
         h.table_words = (int64_t)table.size();
         h.scales_off = 0;
+        h.huff_flags = records ? EC_HUFF_WINDOW_REC : 0;
+        h.huff_fill = records && fill >= 0 ? fill : 0;
+        h.huff_sub_tables = (int32_t)(tabs.sub.size() / 256);
         h.tile_off_off = round_up(h.table_off + 4 * h.table_words, 16);
+        h.n_escapes = n_records;
         h.records_off = round_up(h.tile_off_off + 4 * (n_tiles + 1), 16);
         h.blob_bytes = h.records_off + total;
         h.max_code_bytes = (int32_t)max_code;
+        h.max_code_area = (int32_t)max_area;
         h.max_len = *std::max_element(m->lengths, m->lengths + 256);
         {   /* staging size for the tensor-core kernel: a window of rows (tiles inside rows) */
             h.window_code_bytes = 0;
@@ -524,6 +627,8 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
         /* pass 2: records */
         parallel_for(n_tiles, [&](int64_t lo, int64_t hi) {
             std::vector<uint16_t> v(T);
+            std::vector<uint8_t> e(T / 32);
+            std::vector<uint32_t> recs;
             for (int64_t t = lo; t < hi; ++t) {
                 uint8_t* rec = blob.data() + h.records_off + (int64_t)tile_off[t] * 16;
                 const int64_t base = t * T, n_t = std::min(T, n_pad - base), S = n_t / 32;
@@ -531,32 +636,43 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
                 uint16_t* start = (uint16_t*)rec;
                 uint8_t* raw = rec + 64;
                 uint32_t* area = (uint32_t*)(rec + 64 + EC_RAW_BYTES(S));
+                uint32_t* recs_at = area + area_bytes[t] / 4; /* the records follow the code area */
+                /* sign / mantissa bytes: lane l, symbol i; in each group of four symbols
+                 * the sign and mantissa bits of a pair sit where a BF16 pair keeps them,
+                 * the second pair's rotated by 8 bits (ec_format.h) */
                 for (int64_t q = 0; q < n_t; ++q) {
-                    const int64_t l = (q >> 3) & 31, i = ((q >> 8) << 3) | (q & 7); /* lane l, symbol i */
-                    raw[((i >> 4) * 32 + l) * 16 + (i & 15)] = (uint8_t)(((v[q] >> 8) & 0x80) | (v[q] & 0x7F));
+                    const int64_t l = (q >> 3) & 31, i = ((q >> 8) << 3) | (q & 7);
+                    const uint8_t sg = (uint8_t)((v[q] >> 8) & 0x80), mt = (uint8_t)(v[q] & 0x7F);
+                    uint8_t* g = raw + ((i >> 4) * 32 + l) * 16 + (i & 12); /* the group's four bytes */
+                    switch (i & 3) {
+                        case 0: g[0] |= mt; g[1] |= sg; break;
+                        case 1: g[2] |= mt; g[3] |= sg; break;
+                        case 2: g[1] |= mt; g[2] |= sg; break;
+                        default: g[3] |= mt; g[0] |= sg; break;
+                    }
                 }
+                recs.clear();
                 int64_t bitpos = 0;
                 for (int l = 0; l < 32; ++l) {
                     bitpos = round_up(bitpos, 8);
-                    start[l] = (uint16_t)(bitpos / 8);
+                    if (l) start[l] = (uint16_t)(bitpos / 8);
+                    lane_exponents(v.data(), S, l, e.data(), &recs);
                     for (int64_t i = 0; i < S; ++i) {
-                        const int e = (v[256 * (i >> 3) + 8 * l + (i & 7)] >> 7) & 0xFF;
-                        const int L = m->lengths[e];
-                        const uint32_t c = code[e];
+                        const int L = m->lengths[e[i]];
+                        const uint32_t c = stream_bits(code[e[i]], L);
                         const int64_t wi = bitpos >> 5;
                         const int o = (int)(bitpos & 31);
-                        if (o + L <= 32) {
-                            area[wi] |= c << (32 - o - L);
-                        } else {
-                            area[wi] |= c >> (o + L - 32);
-                            area[wi + 1] |= c << (64 - o - L);
-                        }
+                        area[wi] |= c << o;
+                        if (o + L > 32) area[wi + 1] |= c >> (32 - o);
                         bitpos += L;
                     }
                 }
+                /* lane 0 always starts at byte 0: its slot holds the record count */
+                start[0] = (uint16_t)recs.size();
+                std::sort(recs.begin(), recs.end(), [](uint32_t x, uint32_t y) { return (x & 0xFFF) < (y & 0xFFF); });
+                std::memcpy(recs_at, recs.data(), 4 * recs.size());
             }
         });
-        for (int s = 0; s < 256; ++s) payload += (int64_t)m->counts[s] * m->lengths[s];
 
         m->kind = EC_KIND_HUFFMAN_BF16;
         m->device = device;
@@ -1140,6 +1256,7 @@ extern "C" int ec_stats(const ec_matrix* m, ec_stats_t* s) {
     s->entropy_bits = m->entropy;
     const double coded = (double)m->hdr.n_rows * (double)m->hdr.k_pad;
     s->coded_bits_per_symbol = coded > 0 ? (double)m->payload_bits / coded : 0.0;
+    s->n_records = m->hdr.n_escapes;
     return EC_OK;
 }
 
@@ -1219,12 +1336,17 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
     if (h.n_tiles != (n_pad + T - 1) / T) return EC_ERR_CORRUPT;
     if (h.table_off != (int64_t)sizeof(ec_blob_header)) return EC_ERR_CORRUPT;
     int64_t end = 0, t4 = 0;
+    const bool hrec = huff && h.huff_flags == EC_HUFF_WINDOW_REC, recs = fp8;
     if (huff) {
-        if (h.table_words < EC_PAIR_WORDS + (1 << EC_L1_BITS) ||
-            (h.table_words - EC_PAIR_WORDS - (1 << EC_L1_BITS)) % 256)
+        if (h.huff_flags != 0 && h.huff_flags != EC_HUFF_WINDOW_REC) return EC_ERR_CORRUPT;
+        if (h.huff_sub_tables < 0 || h.huff_sub_tables > 512 || (hrec && h.huff_sub_tables != 0) ||
+            h.table_words != EC_PAIR_WORDS + 256 * (int64_t)h.huff_sub_tables)
             return EC_ERR_CORRUPT;
-        if (h.max_len < 0 || h.max_len > EC_MAX_CODE_LEN || h.max_code_bytes < 0) return EC_ERR_CORRUPT;
-        if (h.window_code_bytes < 0) return EC_ERR_CORRUPT;
+        if (h.max_len < 0 || h.max_len > EC_MAX_CODE_LEN || h.max_code_bytes < 0 || h.max_code_area < 0 ||
+            h.max_code_area > h.max_code_bytes)
+            return EC_ERR_CORRUPT;
+        if (h.window_code_bytes < 0 || h.n_escapes < 0 || (!hrec && h.n_escapes != 0)) return EC_ERR_CORRUPT;
+        if (hrec && (32 * (int64_t)h.steps > 4096 || h.huff_fill < 0 || h.huff_fill > 255)) return EC_ERR_CORRUPT;
     } else if (e8) {
         if (h.prob_bits < 9 || h.prob_bits > 12 || h.max_words < 0 ||
             h.table_words != (4 * EC_E8_TABLES * EC_E8_ALPHA + ((int64_t)EC_E8_TABLES << h.prob_bits)) / 4)
@@ -1251,7 +1373,7 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
     if (h.tile_off_off < end || h.tile_off_off % 16 || !mul_ok(h.n_tiles + 1, 4, &to4) ||
         !add_ok(h.tile_off_off, to4, &end))
         return EC_ERR_CORRUPT;
-    if (fp8) { /* record offsets, then the records */
+    if (recs) { /* record offsets, then the records */
         int64_t e4 = 0;
         if (h.esc_off_off < end || h.esc_off_off % 16 || !add_ok(h.esc_off_off, to4, &end)) return EC_ERR_CORRUPT;
         if (h.esc_records_off < end || h.esc_records_off % 16 || !mul_ok(h.n_escapes, 4, &e4) ||
@@ -1261,21 +1383,33 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
     if (h.records_off < end || h.records_off % 16 || h.records_off > bytes) return EC_ERR_CORRUPT;
     const uint32_t* off = (const uint32_t*)(b + h.tile_off_off);
     if (off[0] != 0 || (int64_t)off[h.n_tiles] * 16 != bytes - h.records_off) return EC_ERR_CORRUPT;
+    int64_t n_hrec = 0; /* Huffman window records seen in the tiles */
     for (int64_t t = 0; t < h.n_tiles; ++t) {
         if (off[t + 1] < off[t]) return EC_ERR_CORRUPT;
         const int64_t rb = ((int64_t)off[t + 1] - off[t]) * 16;
         const int64_t n_t = std::min(T, n_pad - t * T);
         if (huff) {
+            /* lane starts (lane 0's slot: the window record count), the code area, the records */
             const int64_t area = rb - 64 - EC_RAW_BYTES(n_t / 32);
             if (area < 16 || area > h.max_code_bytes) return EC_ERR_CORRUPT;
-            const uint16_t* start = (const uint16_t*)(b + h.records_off + (int64_t)off[t] * 16);
-            for (int l = 0; l < 32; ++l)
-                if (start[l] > area || (l && start[l] < start[l - 1])) return EC_ERR_CORRUPT;
+            const uint8_t* tr = b + h.records_off + (int64_t)off[t] * 16;
+            const uint16_t* start = (const uint16_t*)tr;
+            const int64_t nrec = start[0], code = area - round_up(4 * nrec, 16);
+            if ((!hrec && nrec) || code < 16 || code > h.max_code_area) return EC_ERR_CORRUPT;
+            for (int l = 1; l < 32; ++l)
+                if (start[l] > code || (l > 1 && start[l] < start[l - 1])) return EC_ERR_CORRUPT;
+            const uint32_t* rr = (const uint32_t*)(tr + 64 + EC_RAW_BYTES(n_t / 32) + code);
+            for (int64_t i = 0; i < nrec; ++i) /* 12-bit positions inside the tile, ascending */
+                if ((rr[i] >> 28) || (int64_t)(rr[i] & 0xFFFu) >= n_t || (i && (rr[i] & 0xFFFu) <= (rr[i - 1] & 0xFFFu)))
+                    return EC_ERR_CORRUPT;
+            n_hrec += nrec;
         } else {
             if (rb < 128 || (rb - 128) / 2 > round_up(h.max_words, 8)) return EC_ERR_CORRUPT;
         }
     }
-    if (fp8) { /* per tile: ascending record offsets, records at ascending positions inside the tile */
+    if (huff && n_hrec != h.n_escapes) return EC_ERR_CORRUPT;
+    if (recs) { /* per tile: ascending record offsets, records (position | code << 16) at ascending
+                 * positions inside the tile */
         const uint32_t* eo = (const uint32_t*)(b + h.esc_off_off);
         const uint32_t* er = (const uint32_t*)(b + h.esc_records_off);
         if (eo[0] != 0 || (int64_t)eo[h.n_tiles] != h.n_escapes) return EC_ERR_CORRUPT;
@@ -1291,11 +1425,18 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
     }
     const uint32_t* tab = (const uint32_t*)(b + h.table_off);
     if (huff) {
-        const int64_t n_sub = (h.table_words - EC_PAIR_WORDS - (1 << EC_L1_BITS)) / 256;
+        const int64_t n_sub = h.huff_sub_tables;
         for (int64_t i = 0; i < EC_PAIR_WORDS; ++i) { /* pair entries */
             const uint32_t e = tab[i], n = e & EC_PAIR_LEN_MASK, l0 = (e >> EC_PAIR_FIRST_SHIFT) & 15u;
             if ((e & ~EC_PAIR_FIELDS) || l0 > EC_L1_BITS || n > EC_L1_BITS) return EC_ERR_CORRUPT;
-            if (n ? (l0 == 0 || n <= l0) : (e >> 23) != 0) return EC_ERR_CORRUPT;
+            if (!(e & EC_PAIR_OPEN)) { /* complete: two codewords of length >= 1 */
+                if (l0 == 0 || n <= l0) return EC_ERR_CORRUPT;
+            } else if (l0 > 0) { /* the first codeword only */
+                if (n != l0 || ((e >> 23) & 0xFFu) != 0 || (e & 0x8000u)) return EC_ERR_CORRUPT;
+            } else { /* a longer first codeword (its sub-table), or no codeword */
+                if (n != 0 || ((e >> 23) & 0xFFu) != 0 || (int64_t)((e >> 7) & 0x1FFu) >= std::max<int64_t>(n_sub, 1))
+                    return EC_ERR_CORRUPT;
+            }
         }
         for (int64_t i = EC_PAIR_WORDS; i < h.table_words; ++i)
             if ((tab[i] & EC_ENT_PTR) && (int64_t)(tab[i] & 0xFFFFu) >= n_sub) return EC_ERR_CORRUPT;

@@ -53,8 +53,11 @@ constexpr int kFmaMaxRows = 16;   /* batch rows per pass of the CUDA-core GEMV k
 struct HuffMat {
     const uint8_t* records;
     const uint32_t* tile_off;   /* 16-byte units */
-    const uint32_t* table;      /* level 1 + sub-tables */
+    const uint32_t* table;      /* pair table, then the hierarchical sub-tables */
     int64_t table_words;
+    int32_t n_sub;              /* hierarchical sub-tables (256 entries each) */
+    int32_t fill;               /* the exponent coded in place of a recorded one */
+    int32_t sub_smem;           /* their first word in the launch's staged sub-tables, or -1 (global) */
     float* y;                   /* GEMV output [batch, n_rows] */
     uint16_t* out;              /* decode output [n_rows, k_cols] */
     int64_t n_rows, k_cols, k_pad;
@@ -77,6 +80,15 @@ struct HuffGemvArgs {
     int code_bytes;             /* per-warp code buffer */
     float* part;                /* allocation-free variant: per (row, tile) partial sums */
     int part_slots;             /* partial-sum slots per row */
+    int sub_words;              /* hierarchical sub-table words staged in shared memory */
+    /* x in tensor memory (batch 1, tiles inside rows, one tile width): TMEM lane l of
+     * every warp's lane quarter holds, for each tile column c of a row, the x of the
+     * columns lane l decodes in such a tile, 4 words per 8 symbols.  tx_cols = 0: x
+     * is read from shared memory. */
+    int tx_cols;                /* TMEM columns allocated (a power of 2 >= 32) */
+    int tx_layout_cols;         /* columns per tile column: steps / 2 */
+    int tx_used;                /* columns written: tile columns x tx_layout_cols */
+    uint32_t tx_T;              /* tile width, 32 * steps */
 };
 
 struct HuffDecodeArgs {
@@ -85,6 +97,7 @@ struct HuffDecodeArgs {
     int64_t total_tiles;
     int* status;
     int code_bytes;
+    int sub_words;              /* staged sub-table words (the largest single matrix's) */
 };
 
 /* Tensor-core GEMV launch (matrices whose tiles never cross a row).  A work item
@@ -104,6 +117,7 @@ struct HuffMmaArgs {
     uint32_t idesc;                     /* tcgen05 instruction descriptor (M = 64, N = warps) */
     int nbuf;                           /* chunk buffers (2 or 3) */
     int pool_bytes;                     /* one item's packed code areas, with slack */
+    int sub_words;                      /* hierarchical sub-table words staged in shared memory */
 };
 
 struct RansMat {
@@ -186,6 +200,15 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 __device__ __forceinline__ void flag_corrupt(int* status) { atomicOr(status, 1); }
 
+/* A read-only global load issued where it stands: loads that run a tile ahead of
+ * their use must not be moved next to the use by the compiler, or their latency
+ * comes back. */
+__device__ __forceinline__ uint32_t ldg_early(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
 /* Which matrix of a launch owns combined tile index g (count is small). */
 template <class Args>
 __device__ __forceinline__ int owner(const Args& a, int64_t g) {
@@ -227,9 +250,12 @@ __device__ __forceinline__ int64_t tile_row(int64_t t, int64_t T, int64_t kp, in
  * 16-byte load (the 32 lanes read 512 contiguous bytes).
  */
 constexpr int kMaxHW = 32;                     /* max warps per CTA */
-constexpr int kSlackBytes = 64;                /* after a code area: reads run <= 8 steps x 48 bits + 8 bytes past it */
+/* After a code area: a lane whose data is corrupt may read up to 24 words past the
+ * clamp point of its block (8 pairs, at most three word crossings each) */
+constexpr int kSlackBytes = 128;
 constexpr uint32_t kPairTabBytes = 4u * EC_PAIR_WORDS;
 constexpr uint32_t kSignMant = 0x807F807Fu;    /* sign and mantissa bits of two BF16 */
+constexpr int kSubSmemTables = 8;             /* hierarchical sub-tables staged in shared memory per launch */
 
 __host__ __device__ constexpr int huff_max_warps(int b) { return b <= 1 ? 32 : (b <= 4 ? 24 : 16); }
 
@@ -255,140 +281,174 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-/* Codeword longer than the pair-table window (rare): walk the hierarchical table
- * in global memory from its level-1 entry for this window.  Returns the exponent
- * (.x) and the codeword length (.y, up to 24 bits).  Corrupt data (no codeword
- * matches) yields exponent 0 of length 1 and sets the status. */
-__device__ __noinline__ uint2 long_codeword(uint32_t win, const uint32_t* __restrict__ hier, int64_t hier_words,
-                                            int* status) {
-    uint32_t ent = __ldg(hier + (win >> (32 - EC_L1_BITS)));
-#pragma unroll 1
-    for (int lvl = 0; lvl < 3 && (ent & EC_ENT_PTR) && !(ent & EC_ENT_BAD); ++lvl) {
-        const int used = (int)((ent >> 16) & 31);
-        const int64_t at = (int64_t(1) << EC_L1_BITS) + (int64_t)(ent & 0xFFFFu) * 256 + ((win << used) >> 24);
-        if (used > 24 || at >= hier_words) {
-            ent = EC_ENT_BAD;
-            break;
-        }
-        ent = __ldg(hier + at);
-    }
-    if (ent & (EC_ENT_PTR | EC_ENT_BAD)) {
-        flag_corrupt(status);
-        ent = 1u << 16;
-    }
-    return make_uint2((ent & 0xFFFFu) >> 7, min((ent >> 16) & 31, (uint32_t)EC_MAX_CODE_LEN));
+/* Tensor memory (TMEM) access of a warp: its 32 lanes are TMEM lanes 32 (warp % 4)
+ * .. + 31 of the address's lane field; x4 = four consecutive 32-bit columns. */
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_ld4(uint32_t taddr, uint32_t (&v)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                 : "r"(taddr)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_st4(uint32_t taddr, const uint4& v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+/* Wait for this thread's TMEM loads; v (a load's destination) is tied to the wait
+ * so that no use of it can be scheduled before the data is there. */
+__device__ __forceinline__ void tc_wait_ld_into(uint32_t (&v)[4]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3])::"memory");
 }
 
-/* Per-warp decoding context: shared addresses of the pair table and the staged
- * code area, and the launch matrix whose hierarchical table backs them up. */
-struct PairCtx {
-    uint32_t tab, area;
-    int mi;
+/*
+ * A lane's bit reader.  The lane's codewords sit LSB first in the staged code
+ * area; A is the area bit where its next codeword starts.  The lane holds the two
+ * area words lo, hi that cover bits S = A - 2 .. S + 63 (word index floor(S / 32)
+ * and the next), so that
+ *     v = funnel-shift-right(lo, hi, S mod 32)
+ * has the stream's next 12 bits at bits 2..13 and v & 0x3FFC is already the byte
+ * offset of their pair-table entry: one shift and one mask per lookup.
+ * P accumulates whole table entries: only its low 5 bits (S mod 32, all the funnel
+ * shift reads) and bit 5 matter.  An entry's bits 0..3 hold its advance and bits
+ * 4..6 are 0, so bit 5 of P flips exactly when S crosses into the next word; then
+ * lo takes hi, hi takes nx (the word after hi, loaded one crossing ahead so that
+ * the next lookup never waits for a load) and nx the word at wa.
+ */
+struct Lane {
+    uint32_t P, lo, hi, nx, wa;
 };
 
-/* The 32 stream bits starting at bit p of the staged code area (MSB first). */
-__device__ __forceinline__ uint32_t window(uint32_t area, uint32_t p) {
-    const uint32_t a = area + ((p >> 5) << 2);
-    return __funnelshift_l(lds32(a + 4), lds32(a), p);
-}
-
-/* A lane's read position: bit p of the staged code area, and the area words
- * k = p / 32 (lo) and k + 1 (hi) that hold the 32 bits starting at p. */
-struct LaneBits {
-    uint32_t p, k, lo, hi;
-};
-
-__device__ __forceinline__ void bits_seek(LaneBits& s, uint32_t area, uint32_t p) {
-    s.p = p;
-    s.k = p >> 5;
-    const uint32_t a = area + (s.k << 2);
+/* Position the lane at area bit A (a byte boundary); the two words before the area
+ * (its lane starts) are readable, so A = 0 is fine. */
+__device__ __forceinline__ void lane_seek(Lane& s, uint32_t area, uint32_t A) {
+    const int32_t S = (int32_t)A - 2;
+    const uint32_t a = area + (uint32_t)((S >> 5) * 4);
     s.lo = lds32(a);
     s.hi = lds32(a + 4);
+    s.nx = lds32(a + 8);
+    s.wa = a + 12;
+    s.P = (uint32_t)S;
 }
 
-/* Advance by adv <= 32 bits: the word index moves by at most one, so lo takes
- * the old hi and only hi is loaded, and only by lanes that crossed a word.
- * (The per-block clamp of p to the area only ever moves it back for corrupt
- * data; the loads then stay inside the area and its slack.) */
-__device__ __forceinline__ void bits_step(LaneBits& s, uint32_t area, uint32_t adv) {
-    s.p += adv;
-    const uint32_t k2 = s.p >> 5;
+/* Advance by the low bits of `e` (an entry, or a length below 32). */
+__device__ __forceinline__ void lane_adv(Lane& s, uint32_t e) {
+    const uint32_t pn = s.P + e;
     asm volatile(
-        "{\n\t.reg .pred q;\n\t"
-        "setp.ne.u32 q, %2, %3;\n\t"
+        "{\n\t.reg .pred q;\n\t.reg .b32 t;\n\t"
+        "lop3.b32 t, %4, %5, 32, 0x28;\n\t" /* (pn ^ P) & 32 */
+        "setp.ne.u32 q, t, 0;\n\t"
         "@q mov.b32 %0, %1;\n\t"
-        "@q ld.shared.u32 %1, [%4];\n\t}"
-        : "+r"(s.lo), "+r"(s.hi)
-        : "r"(k2), "r"(s.k), "r"(area + (k2 << 2) + 4)
+        "@q mov.b32 %1, %2;\n\t"
+        "@q ld.shared.u32 %2, [%3];\n\t"
+        "@q add.u32 %3, %3, 4;\n\t}"
+        : "+r"(s.lo), "+r"(s.hi), "+r"(s.nx), "+r"(s.wa)
+        : "r"(pn), "r"(s.P)
         : "memory");
-    s.k = k2;
+    s.P = pn;
 }
 
-/* Decode the lane's next two symbols: returns their exponents in BF16 position
- * [e(i+1) << 23 | e(i) << 7] (other bits unspecified) and advances the lane.  A
- * window whose two codewords do not both fit takes a second lookup at the end of
- * the first; its 12 bits lie within the 64 the lane already holds (offset at most
- * 31 + 12).  With kLong (a launch holding codewords longer than the window) a
- * first or second codeword the window cannot hold walks the hierarchical table
- * (which reports a window no codeword matches through the status word). */
-template <bool kLong, class Args>
-__device__ __forceinline__ uint32_t pair_step(LaneBits& s, const PairCtx& c, const Args& a) {
-    const uint32_t win = __funnelshift_l(s.hi, s.lo, s.p);
-    uint32_t e = lds32(c.tab + ((win >> (32 - EC_L1_BITS)) << 2));
-    uint32_t adv = e & EC_PAIR_LEN_MASK;
-    if (__builtin_expect(adv == 0, 0)) {
-        if (kLong) {
-            uint32_t l0 = (e >> EC_PAIR_FIRST_SHIFT) & 15u, x0 = (e >> 7) & 0xFFu;
-            if (l0 == 0) {
-                const HuffMat& M = a.m[c.mi];
-                const uint2 lc = long_codeword(win, M.table + EC_PAIR_WORDS, M.table_words - EC_PAIR_WORDS, a.status);
-                x0 = lc.x;
-                l0 = lc.y;
-            }
-            const uint32_t w1 = window(c.area, s.p + l0);
-            const uint32_t f = lds32(c.tab + ((w1 >> (32 - EC_L1_BITS)) << 2));
-            uint32_t l1 = (f >> EC_PAIR_FIRST_SHIFT) & 15u, x1 = (f >> 7) & 0xFFu;
-            if (l1 == 0) {
-                const HuffMat& M = a.m[c.mi];
-                const uint2 lc = long_codeword(w1, M.table + EC_PAIR_WORDS, M.table_words - EC_PAIR_WORDS, a.status);
-                x1 = lc.x;
-                l1 = lc.y;
-            }
-            e = (x0 << 7) | (x1 << 23);
-            bits_seek(s, c.area, s.p + l0 + l1); /* up to 48 bits: reload both words */
-            return e;
+/* Area bit of the lane's next codeword. */
+__device__ __forceinline__ uint32_t lane_pos(const Lane& s, uint32_t area) { return 8u * (s.wa - area) - 94u + (s.P & 31u); }
+
+/* Keep the lane's loads inside the area and its slack (corrupt data only ever
+ * moves wa past `limit`; the lane then decodes garbage, which the end-of-tile
+ * check reports). */
+__device__ __forceinline__ void lane_clamp(Lane& s, uint32_t limit) { s.wa = min(s.wa, limit); }
+
+/* Hierarchical decoding context of the warp's current matrix (kHier launches). */
+struct HierCtx {
+    const uint32_t* sub; /* sub-tables (shared or global memory), 256 entries each */
+    int n_sub;
+    int* status;
+};
+
+/* A codeword longer than the window (or none, for corrupt data): walk the
+ * sub-tables from the pair entry's sub-table index with the 30 stream bits w (the
+ * codeword's first bit at bit 0).  Returns (exponent, length); corrupt data gives
+ * exponent 0 of length 1 and sets the status. */
+__device__ __forceinline__ uint2 long_codeword(uint32_t w, uint32_t ent, const HierCtx& h) {
+    uint32_t t = (ent >> 7) & 0x1FFu, used = EC_L1_BITS, e = EC_ENT_BAD;
+#pragma unroll 1
+    for (int lvl = 0; lvl < 2; ++lvl) {
+        if ((int)t >= h.n_sub || used > 22) {
+            e = EC_ENT_BAD;
+            break;
         }
-        /* Every codeword fits the window: the entry holds the first one (its
-         * exponent already in bits 7..14, its length in bits 16..19 with nothing
-         * above) and the second is looked up at its end, at most 31 + 12 bits
-         * into the 64 the lane holds.  A window no codeword matches (corrupt
-         * data) yields length 0; the end-of-tile offset check reports it. */
-        const uint32_t l0 = e >> EC_PAIR_FIRST_SHIFT;
-        const uint32_t o = (s.p & 31u) + l0;
-        const uint32_t w1 = o < 32 ? __funnelshift_l(s.hi, s.lo, o) : s.hi << (o & 31u);
-        const uint32_t f = lds32(c.tab + ((w1 >> (32 - EC_L1_BITS)) << 2));
-        adv = l0 + ((f >> EC_PAIR_FIRST_SHIFT) & 15u);
-        e = ((f << 16) & 0x7F800000u) | (e & 0x7F80u);
+        e = h.sub[256 * t + ((w >> used) & 0xFFu)];
+        if (!(e & EC_ENT_PTR) || (e & EC_ENT_BAD)) break;
+        t = e & 0xFFFFu;
+        used = (e >> 16) & 31u;
     }
-    bits_step(s, c.area, adv); /* adv <= 24 */
+    if (e & (EC_ENT_PTR | EC_ENT_BAD) || ((e >> 16) & 31u) > 30u || ((e >> 16) & 31u) == 0u) {
+        flag_corrupt(h.status);
+        return make_uint2(0u, 1u);
+    }
+    return make_uint2((e & 0xFFFFu) >> 7, (e >> 16) & 31u);
+}
+
+/* An open pair entry e (hierarchical launches): the lane has already advanced by
+ * the first codeword when it fits the window; decode what is missing and return
+ * the pair's exponents in BF16 position [e1 << 23 | e0 << 7]. */
+__device__ __forceinline__ uint32_t pair_open(Lane& s, uint32_t e, uint32_t tab, const HierCtx& h) {
+    uint32_t e0 = (e >> 7) & 0xFFu;
+    if (((e >> EC_PAIR_FIRST_SHIFT) & 15u) == 0) {
+        const uint2 r = long_codeword(__funnelshift_r(s.lo, s.hi, s.P) >> 2, e, h);
+        e0 = r.x;
+        lane_adv(s, r.y);
+    }
+    const uint32_t f = lds32(tab + (__funnelshift_r(s.lo, s.hi, s.P) & 0x3FFCu));
+    uint32_t e1 = (f >> 7) & 0xFFu, l1 = (f >> EC_PAIR_FIRST_SHIFT) & 15u;
+    if (l1 == 0) {
+        const uint2 r = long_codeword(__funnelshift_r(s.lo, s.hi, s.P) >> 2, f, h);
+        e1 = r.x;
+        l1 = r.y;
+    }
+    lane_adv(s, l1);
+    return (e0 << 7) | (e1 << 23);
+}
+
+/* The lane's next two symbols: their exponents in BF16 position [e(i+1) << 23 |
+ * e(i) << 7] (other bits unspecified).  Without kHier the encoder guarantees every
+ * pair fits the window (window records), so a step is one shift, one mask, one
+ * table load and the advance, with no branch on the data. */
+template <bool kHier>
+__device__ __forceinline__ uint32_t pair_step(Lane& s, uint32_t tab, const HierCtx& h) {
+    const uint32_t e = lds32(tab + (__funnelshift_r(s.lo, s.hi, s.P) & 0x3FFCu));
+    lane_adv(s, e);
+    if (kHier && __builtin_expect((int32_t)e < 0, 0)) return pair_open(s, e, tab, h);
     return e;
 }
 
-/* Two BF16 weights [w(i+1) | w(i)]: exponents from a pair entry, sign and
- * mantissa from raw bytes a and a + 1 of r (duplicated into both bytes of each
- * half by sel). */
-__device__ __forceinline__ uint32_t merge2(uint32_t e, uint32_t r, uint32_t sel) {
-    return (__byte_perm(r, 0, sel) & kSignMant) | (e & ~kSignMant);
+/* (r & 0x807F807F) | (e & ~0x807F807F) in one instruction. */
+__device__ __forceinline__ uint32_t merge_sm(uint32_t r, uint32_t e) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xE4;" : "=r"(d) : "r"(r), "r"(e), "n"(kSignMant));
+    return d;
 }
 
-/* Eight symbols of the lane (raw bytes r0 = symbols 0..3, r1 = 4..7). */
-template <bool kLong, class Args>
-__device__ __forceinline__ void decode8(LaneBits& s, const PairCtx& c, const Args& a, uint32_t r0, uint32_t r1,
+/* Eight symbols of the lane (raw words r0 = symbols 0..3, r1 = 4..7) as four
+ * words [w(i+1) | w(i)]. */
+template <bool kHier>
+__device__ __forceinline__ void decode8(Lane& s, uint32_t tab, const HierCtx& h, uint32_t r0, uint32_t r1,
                                         uint32_t (&w)[4]) {
-    w[0] = merge2(pair_step<kLong>(s, c, a), r0, 0x1100);
-    w[1] = merge2(pair_step<kLong>(s, c, a), r0, 0x3322);
-    w[2] = merge2(pair_step<kLong>(s, c, a), r1, 0x1100);
-    w[3] = merge2(pair_step<kLong>(s, c, a), r1, 0x3322);
+    const uint32_t e0 = pair_step<kHier>(s, tab, h);
+    const uint32_t e1 = pair_step<kHier>(s, tab, h);
+    w[0] = merge_sm(r0, e0);
+    w[1] = merge_sm(__funnelshift_r(r0, r0, 8), e1);
+    const uint32_t e2 = pair_step<kHier>(s, tab, h);
+    const uint32_t e3 = pair_step<kHier>(s, tab, h);
+    w[2] = merge_sm(r1, e2);
+    w[3] = merge_sm(__funnelshift_r(r1, r1, 8), e3);
+}
+
+/* A window record (12-bit tile position | sign and mantissa << 12 | exponent << 20):
+ * the BF16 weight with exponent `expo` (the record's own, or the coded one). */
+__device__ __forceinline__ uint32_t rec_weight(uint32_t r, uint32_t expo) {
+    return ((r >> 4) & 0x8000u) | (expo << 7) | ((r >> 12) & 0x7Fu);
 }
 
 /* acc += w0 * x0 + w1 * x1 for BF16 pairs w = [w1|w0], x = [x1|x0]; the products are
@@ -399,6 +459,26 @@ __device__ __forceinline__ float fma2_bf16(uint32_t w, uint32_t x, float acc) {
         "mov.b32 {xl, xh}, %2;\n\t"
         "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
         "fma.rn.f32.bf16 %0, wh, xh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w), "r"(x));
+    return acc;
+}
+/* acc0 += w0 * x0, acc1 += w1 * x1 (two chains). */
+__device__ __forceinline__ void fma2x_bf16(uint32_t w, uint32_t x, float& acc0, float& acc1) {
+    asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+        "mov.b32 {wl, wh}, %2;\n\t"
+        "mov.b32 {xl, xh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
+        "fma.rn.f32.bf16 %1, wh, xh, %1;\n\t}"
+        : "+f"(acc0), "+f"(acc1)
+        : "r"(w), "r"(x));
+}
+/* acc += w * x for one BF16 weight and one BF16 activation (low halves). */
+__device__ __forceinline__ float fma1_bf16(uint32_t w, uint32_t x, float acc) {
+    asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+        "mov.b32 {wl, wh}, %1;\n\t"
+        "mov.b32 {xl, xh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t}"
         : "+f"(acc)
         : "r"(w), "r"(x));
     return acc;
@@ -449,14 +529,14 @@ struct TileRef {
     uint32_t t;         /* tile index within its matrix (a launch has < 2^31 tiles) */
     int mi;             /* matrix of the launch */
     int S;              /* symbols per lane */
-    int area;           /* code area bytes; 0 = corrupt record (skipped) */
+    int area;           /* bytes of window records + code area; 0 = corrupt record (skipped) */
 };
 
 template <class Args>
 __device__ __forceinline__ uint2 tile_offsets(const Args& a, int64_t g) {
     const HuffMat& M = a.m[owner(a, g)];
     const int64_t t = g - M.tile_begin;
-    return make_uint2(__ldg(M.tile_off + t), __ldg(M.tile_off + t + 1));
+    return make_uint2(ldg_early(M.tile_off + t), ldg_early(M.tile_off + t + 1));
 }
 
 /* Resolve combined tile g from its record offsets (16-byte units); a record whose
@@ -470,7 +550,7 @@ __device__ __forceinline__ TileRef tile_ref(const Args& a, int64_t g, uint2 off)
     r.S = r.t == M.n_tiles - 1 ? M.last_steps : M.steps;
     /* offsets are 16-byte units; a record is far below 4 GB */
     const int area = (int)((off.y - off.x) * 16u) - 64 - EC_RAW_BYTES(r.S);
-    const bool ok = off.x <= off.y && off.y <= M.rec16 && area >= 16 && area <= a.code_bytes;
+    const bool ok = off.x <= off.y && off.y <= M.rec16 && area >= 16;
     r.rec = M.records + (size_t)(ok ? off.x : 0u) * 16;
     r.area = ok ? area : 0;
     return r;
@@ -515,30 +595,87 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
  * buffer: one lane arms the buffer's mbarrier with the byte count and issues two
  * bulk copies (16-byte aligned, multiples of 16 bytes); a corrupt record only
  * arrives, so the phase still completes. */
-__device__ __forceinline__ void prefetch_code(uint32_t buf, uint32_t mbar, const TileRef& r, int lane) {
+__device__ __forceinline__ void prefetch_code(uint32_t buf, uint32_t mbar, const TileRef& r, int lane, int cap) {
     if (lane == 0) {
         if (r.area > 0) {
-            mbar_arrive_tx(mbar, 64u + (uint32_t)r.area);
+            const uint32_t n = (uint32_t)min(r.area, cap); /* the code area, then as many records as fit */
+            mbar_arrive_tx(mbar, 64u + n);
             bulk_g2s(buf, r.rec, 64u, mbar);
-            bulk_g2s(buf + 64, r.rec + 64 + EC_RAW_BYTES(r.S), (uint32_t)r.area, mbar);
+            bulk_g2s(buf + 64, r.rec + 64 + EC_RAW_BYTES(r.S), n, mbar);
         } else {
             mbar_arrive_tx(mbar, 0u);
         }
     }
 }
 
+/* Decoding context of one matrix of a launch: its pair table in shared memory and,
+ * for hierarchical launches, its sub-tables. */
+struct WalkCtx {
+    uint32_t tab;
+    HierCtx h;
+};
+
+/* Sub-tables of matrix M: staged in shared memory (`staged`, the launch's block of
+ * them) when the launch staged them, else read from the blob. */
+__device__ __forceinline__ HierCtx hier_ctx(const HuffMat& M, const uint32_t* staged, int* status) {
+    HierCtx h;
+    h.sub = M.sub_smem >= 0 ? staged + M.sub_smem : M.table + EC_PAIR_WORDS;
+    h.n_sub = M.n_sub;
+    h.status = status;
+    return h;
+}
+
+/* Stage the launch's sub-tables that fit (kSubSmemTables in all) into shared memory. */
+template <class Args>
+__device__ __forceinline__ void stage_sub_tables(const Args& a, uint32_t* dst) {
+    for (int k = 0; k < a.count; ++k) {
+        const HuffMat& M = a.m[k];
+        if (M.sub_smem < 0) continue;
+        const uint4* src = (const uint4*)(M.table + EC_PAIR_WORDS);
+        uint4* d = (uint4*)(dst + M.sub_smem);
+        for (int i = threadIdx.x; i < 64 * M.n_sub; i += blockDim.x) d[i] = __ldg(src + i);
+    }
+}
+
+/* Layout of a staged tile: its buffer holds the 64 bytes of lane starts (lane 0's
+ * slot: the window record count n), the code area, and the records as far as the
+ * buffer's room `cap` allows; the rest stay in the tile record in global memory. */
+struct TileRecs {
+    int n;          /* window records; -1: inconsistent counts (corrupt data) */
+    uint32_t code;  /* code area bytes */
+    uint32_t staged; /* records in the buffer, after the code area */
+};
+__device__ __forceinline__ TileRecs tile_recs(uint32_t buf, int area, int cap) {
+    TileRecs t;
+    t.n = (int)lds16(buf);
+    const int code = area - 16 * ((4 * t.n + 15) / 16);
+    if (area <= 0 || code < 16 || code > cap) {
+        t.n = -1;
+        t.code = t.staged = 0;
+        return t;
+    }
+    t.code = (uint32_t)code;
+    t.staged = (uint32_t)min(t.n, (min(area, cap) - code) / 4);
+    return t;
+}
+/* Where the tile's records beyond the staged ones sit in global memory. */
+__device__ __forceinline__ const uint32_t* far_records(const TileRef& r, uint32_t code) {
+    return (const uint32_t*)(r.rec + 64 + EC_RAW_BYTES(r.S) + code);
+}
+
 /* Walk combined tiles g0, g0 + stride, ... < g_end.  The first tile's copy must
  * already be in flight (prefetch_code).  For every tile with a sound record:
- * begin(tile) once; then, for each block of 16 symbols of the lane, block() and
- * two calls half(w, h) for its two 8-symbol halves h = 0, 1 in order (w = four
- * words [w(i+1) | w(i)]); then end().  Rows start on block boundaries (k_pad is a
- * multiple of 16 * 32 positions).  The raw bytes of block b + 2 are loaded right
+ * begin(tile) once; then, for each block of 16 symbols of the lane, block(buf,
+ * tile) and two calls half(w, h) for its two 8-symbol halves h = 0, 1 in order (w =
+ * four words [w(i+1) | w(i)]); then end(tile, buf).  buf is the tile's shared
+ * buffer: lane starts, the code area, then its window records (tile_recs).  Rows start on block boundaries (k_pad is
+ * a multiple of 16 * 32 positions).  The raw bytes of block b + 2 are loaded right
  * after block b is decoded, into the ring slot it frees; blocks 0 and 1 of the
  * next tile are loaded the same way at the end of the current one. */
-template <bool kLong, class Args, class TabOf, class Begin, class Block, class Half, class End>
+template <bool kHier, class Args, class CtxOf, class Begin, class Block, class Half, class End>
 __device__ __forceinline__ void huff_walk(const Args& a, uint32_t g0, uint32_t stride, uint32_t g_end, TileRef cur,
                                           uint32_t bufs, uint32_t buf_bytes, uint32_t& ph, int lane,
-                                          TabOf&& tab_of, Begin&& begin, Block&& block, Half&& half, End&& end) {
+                                          CtxOf&& ctx_of, Begin&& begin, Block&& block, Half&& half, End&& end) {
     const uint32_t mbars = bufs + 2 * buf_bytes;
     uint2 off_next = g0 + stride < g_end ? tile_offsets(a, g0 + stride) : make_uint2(0u, 0u);
     uint4 rr[2] = {};
@@ -555,24 +692,27 @@ __device__ __forceinline__ void huff_walk(const Args& a, uint32_t g0, uint32_t s
         TileRef nxt{};
         if (has_next) {
             nxt = tile_ref(a, g + stride, off_next);
-            prefetch_code(nb_buf, mbars + 8 * (bi ^ 1u), nxt, lane);
+            prefetch_code(nb_buf, mbars + 8 * (bi ^ 1u), nxt, lane, a.code_bytes);
             if (g + 2 * stride < g_end) off_next = tile_offsets(a, g + 2 * stride);
         }
-        if (cur.area == 0) {
+        const TileRecs tr = tile_recs(cb, cur.area, a.code_bytes);
+        if (tr.n < 0) {
             if (lane == 0) flag_corrupt(a.status);
             raw_ready = false;
             cur = nxt;
             cb = nb_buf;
             continue;
         }
-        const uint32_t s0 = lds16(cb + 2 * lane);
+        const uint32_t cbytes = tr.code;
+        const uint32_t s0 = lane ? lds16(cb + 2 * lane) : 0u;
         const uint32_t s1 = lane < 31 ? lds16(cb + 2 * lane + 2) : 0u;
-        const PairCtx c{tab_of(cur.mi), cb + 64, cur.mi};
+        const WalkCtx c = ctx_of(cur.mi);
+        const uint32_t area = cb + 64;
         const uint4* raw4 = (const uint4*)(cur.rec + 64) + lane;
         const int nb = cur.S / 16;
-        const uint32_t pmax = 8u * (uint32_t)cur.area;
-        LaneBits s;
-        bits_seek(s, c.area, 8u * min(s0, (uint32_t)cur.area));
+        const uint32_t limit = area + cbytes;
+        Lane s;
+        lane_seek(s, area, 8u * min(s0, cbytes));
         if (!raw_ready) {
             rr[0] = __ldg(raw4);
             if (nb > 1) rr[1] = __ldg(raw4 + 32);
@@ -593,14 +733,12 @@ __device__ __forceinline__ void huff_walk(const Args& a, uint32_t g0, uint32_t s
             for (int u = 0; u < 2; ++u) {
                 const int blk = b0 + u;
                 if (u == 0 || blk < nb) {
-                    block();
-                    /* a position past the area (corrupt data only) is pulled back; the
-                     * held words are then stale but every load stays in the area */
-                    s.p = min(s.p, pmax);
+                    block(cb, cur);
+                    lane_clamp(s, limit);
                     uint32_t w[4];
-                    decode8<kLong>(s, c, a, rr[u].x, rr[u].y, w);
+                    decode8<kHier>(s, c.tab, c.h, rr[u].x, rr[u].y, w);
                     half(w, 0);
-                    decode8<kLong>(s, c, a, rr[u].z, rr[u].w, w);
+                    decode8<kHier>(s, c.tab, c.h, rr[u].z, rr[u].w, w);
                     half(w, 1);
                     const int ahead = blk + 2;
                     if (ahead < nb) rr[u] = __ldg(raw4 + 32 * ahead);
@@ -612,33 +750,56 @@ __device__ __forceinline__ void huff_walk(const Args& a, uint32_t g0, uint32_t s
         raw_swap = chain && (nb & 1);
         /* every lane's codewords end in the last byte before the next lane's start
          * (the last lane: before the >= 8 zero bytes closing the area) */
-        const uint32_t p = s.p;
+        const uint32_t p = lane_pos(s, area), pmax = 8u * cbytes;
         const bool bad = lane < 31 ? (p > 8u * s1 || p + 8u <= 8u * s1) : (p + 64u > pmax);
         if (__any_sync(kFull, bad) && lane == 0) flag_corrupt(a.status);
-        end();
+        end(cur, cb);
         cur = nxt;
         cb = nb_buf;
     }
 }
 
+/* Records j in [from, n) of a tile, read from global memory (those the tile buffer
+ * had no room for): the lane's share of sum (w - w_coded) * x over the records at
+ * tile positions [lo, hi), x[column] at xrow + 2 (col_base + position).  Rare; its
+ * loads are volatile so that they stay inside the branch that needs them. */
+__device__ __forceinline__ float far_records_dot(const uint32_t* far, uint32_t from, uint32_t n, uint32_t lo, uint32_t hi,
+                                              uint32_t col_base, uint32_t xrow, uint32_t fill, int lane) {
+    float d = 0.f;
+    for (uint32_t j = from + (uint32_t)lane; j < n; j += 32) {
+        const uint32_t e = ldg_early(far + j), q = e & 0xFFFu;
+        if (q >= lo && q < hi) {
+            const uint32_t xv1 = lds16(xrow + 2u * (col_base + q));
+            d = fma1_bf16(rec_weight(e, e >> 20), xv1, d);
+            d = fma1_bf16(rec_weight(e, fill) ^ 0x8000u, xv1, d);
+        }
+    }
+    return d;
+}
+
 /* ======================================================== Huffman GEMV kernel */
 /* kPart = false: row sums go to y (stored, or added atomically when a row spans
  * tiles).  kPart = true (allocation-free entry point): every row segment a tile
- * produces goes to its own slot of a.part, summed into y by part_reduce_kernel. */
-template <int B, bool kPart, bool kLong>
+ * produces goes to its own slot of a.part, summed into y by part_reduce_kernel.
+ * kHier: some matrix of the launch decodes through the hierarchical tables. */
+template <int B, bool kPart, bool kHier, bool kTx>
 __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(const __grid_constant__ HuffGemvArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t kp = (uint32_t)a.m[0].k_pad;
     const int64_t K = a.m[0].k_cols;
     const int batch = a.batch;
+    static_assert(!kTx || B == 1, "x in tensor memory: batch 1 only");
 
-    /* shared: pair tables | x [batch][k_pad] | per warp: two tile buffers */
-    uint4* tabs = (uint4*)smem;
-    uint16_t* xs = (uint16_t*)(smem + (size_t)a.count * kPairTabBytes);
+    /* shared: TMEM address (16 B) | pair tables | staged sub-tables | x [batch][k_pad] |
+     * per warp: two tile buffers */
+    const uint32_t tslot = smem_u32(smem);
+    uint4* tabs = (uint4*)(smem + 16);
+    uint32_t* subs = (uint32_t*)(smem + 16 + (size_t)a.count * kPairTabBytes);
+    uint16_t* xs = (uint16_t*)(subs + a.sub_words);
     uint8_t* wbase = (uint8_t*)xs + (size_t)batch * xs_row_bytes(kp) + (size_t)warp * huff_warp_bytes(a.code_bytes);
     const uint32_t bufs = smem_u32(wbase), buf_bytes = (uint32_t)tile_buf_bytes(a.code_bytes);
-    const uint32_t xs_lane = smem_u32(xs) + 16u * lane, tabs_s = smem_u32(tabs); /* x of the lane's 8 columns */
+    const uint32_t xs_s = smem_u32(xs), xs_lane = xs_s + 16u * lane, tabs_s = smem_u32(tabs); /* x of the lane's 8 columns */
 
     const int nwarp = blockDim.x >> 5;
     const int64_t gw = (int64_t)blockIdx.x * nwarp + warp, nw = (int64_t)gridDim.x * nwarp;
@@ -653,26 +814,53 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
     TileRef first{};
     if (gw < a.total_tiles) {
         first = tile_ref(a, gw, tile_offsets(a, gw));
-        prefetch_code(bufs, mbars, first, lane);
+        prefetch_code(bufs, mbars, first, lane, a.code_bytes);
     }
     for (int k = 0; k < a.count; ++k) {
         const uint4* src = (const uint4*)a.m[k].table;
         for (int i = threadIdx.x; i < EC_PAIR_WORDS / 4; i += blockDim.x) tabs[k * (EC_PAIR_WORDS / 4) + i] = __ldg(src + i);
     }
+    if (kHier) stage_sub_tables(a, subs);
+    if (kTx && warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tslot), "r"(a.tx_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
     grid_dep_launch();
     grid_dep_wait(); /* x and y belong to the preceding kernel in the stream from here on */
     stage_x_rows(xs, a.x, batch, K, kp);
+    uint32_t tx = 0; /* TMEM address of the warp's lane quarter, column 0 */
+    if (kTx) {
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        tx = lds32(tslot) + ((uint32_t)(32 * (warp & 3)) << 16);
+        if (warp < 4) { /* one warp per lane quarter writes the x layouts */
+            for (uint32_t c = 0; c < (uint32_t)a.tx_used; c += 4) {
+                const uint32_t L = c / (uint32_t)a.tx_layout_cols, m = (c - L * (uint32_t)a.tx_layout_cols) / 4;
+                tc_st4(tx + c, lds128(xs_s + 2u * (L * a.tx_T + 256u * m + 8u * lane)));
+            }
+            tc_wait_st();
+        }
+        tc_fence_before();
+    }
     __syncthreads();
-    if (gw >= a.total_tiles) return;
+    if (kTx) tc_fence_after();
 
+    if (gw < a.total_tiles) {
     const uint32_t jrow = kp / 32;
     int prev_mi = -1;
     uint32_t prev_t = 0, row0 = 0, col0 = 0; /* where this warp's current tile starts (rows, columns < 2^31) */
-    float acc[B][2];
+    /* batch 1: four independent sums (two FMAs each per 8 symbols: products of the high
+     * BF16 halves have the longer latency); wider batches two per row */
+    constexpr int kAcc = B == 1 ? 4 : 2;
+    float acc[B][kAcc];
     /* x of the current 8 symbols: loaded one half-block ahead for narrow batches,
      * at use for wide ones (whose registers go to the accumulators) */
     constexpr bool kAhead = B <= 4;
     uint4 xv[kAhead ? B : 1];
+    uint32_t xt[4] = {0u, 0u, 0u, 0u}; /* kTx: x of the next 8 symbols, loading from TMEM */
+    uint32_t xcol = 0, xend = 0;       /* kTx: its TMEM address; the end of the tile's layout */
     uint32_t row = 0, t_cur = 0;
     uint32_t jc = 0; /* first column / 32 of the current 8 symbols' 256-column block */
     const HuffMat* Mp = &a.m[0];
@@ -684,30 +872,70 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
             xv[b] = lds128(xa + (uint32_t)(b * xs_row_bytes(kp)));
         }
     };
-    auto flush = [&](uint32_t r) {
+    /* Row r of the current tile (buffer cb) is complete: fold in its window records
+     * (each adds (w - w_coded) * x, both products exact; they came with the tile's
+     * code area, all but those beyond the buffer's room), then reduce across the warp. */
+    auto flush = [&](uint32_t r, uint32_t cb, const TileRef& tile) {
         const HuffMat& M = *Mp;
+        const uint32_t seg_end = (r - row0 + 1) * kp - col0;    /* tile positions of rows <= r */
+        const uint32_t seg_begin = r == row0 ? 0u : seg_end - kp; /* ... of rows < r */
+        const uint32_t col_base = col0 - (r - row0) * kp;         /* column = col_base + position */
+        const TileRecs tr = tile_recs(cb, tile.area, a.code_bytes);
+        for (uint32_t j = (uint32_t)lane; j < tr.staged; j += 32) {
+            const uint32_t e = lds32(cb + 64 + tr.code + 4 * j), q = e & 0xFFFu;
+            if (q >= seg_begin && q < seg_end) {
+                const uint32_t col = col_base + q;
+                const uint32_t wt = rec_weight(e, e >> 20);
+                const uint32_t wf = rec_weight(e, (uint32_t)M.fill) ^ 0x8000u; /* minus the coded weight */
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                    if (B > 1 && b >= batch) break;
+                    const uint32_t xv1 = lds16(xs_s + 2u * ((uint32_t)b * kp + col));
+                    acc[b][0] = fma1_bf16(wt, xv1, acc[b][0]);
+                    acc[b][0] = fma1_bf16(wf, xv1, acc[b][0]);
+                }
+            }
+        }
+        if (tr.n > (int)tr.staged) { /* (rare) records beyond the buffer's room */
+            const uint32_t* far = far_records(tile, tr.code);
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                if (B > 1 && b >= batch) break;
+                acc[b][0] += far_records_dot(far, tr.staged, (uint32_t)tr.n, seg_begin, seg_end, col_base,
+                                             xs_s + 2u * (uint32_t)b * kp, (uint32_t)M.fill, lane);
+            }
+        }
         int64_t slot = 0;
         if (kPart) /* tiles before this one that also cover row r */
             slot = (int64_t)t_cur - ((int64_t)r * M.k_pad) / (32 * (int64_t)M.steps);
 #pragma unroll
         for (int b = 0; b < B; ++b) {
             if (B > 1 && b >= batch) break;
-            const float s = warp_sum(acc[b][0] + acc[b][1]);
+            float t = acc[b][0];
+#pragma unroll
+            for (int j = 1; j < kAcc; ++j) t += acc[b][j];
+            const float sum = warp_sum(t);
             if (lane == 0) {
                 if (kPart) {
-                    a.part[((int64_t)b * M.n_rows + r) * a.part_slots + slot] = s;
+                    a.part[((int64_t)b * M.n_rows + r) * a.part_slots + slot] = sum;
                 } else {
                     float* dst = M.y + (int64_t)b * M.n_rows + r;
-                    if (M.atomic_y) atomicAdd(dst, s);
-                    else *dst = s;
+                    if (M.atomic_y) atomicAdd(dst, sum);
+                    else *dst = sum;
                 }
             }
-            acc[b][0] = acc[b][1] = 0.f;
+#pragma unroll
+            for (int j = 0; j < kAcc; ++j) acc[b][j] = 0.f;
         }
     };
-    huff_walk<kLong>(
+    huff_walk<kHier>(
         a, gw, nw, a.total_tiles, first, bufs, buf_bytes, ph, lane,
-        [&](int mi) { return tabs_s + mi * kPairTabBytes; },
+        [&](int mi) {
+            WalkCtx c;
+            c.tab = tabs_s + mi * kPairTabBytes;
+            c.h = hier_ctx(a.m[mi], subs, a.status);
+            return c;
+        },
         [&](const TileRef& r) {
             Mp = &a.m[r.mi];
             t_cur = r.t;
@@ -726,34 +954,66 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
             prev_mi = r.mi;
             prev_t = r.t;
             row = row0; /* advanced by the block hook as rows end inside the tile */
-            jc = (uint32_t)col0 / 32;
-            if (kAhead) load_x(jc);
+            if (!kTx) jc = (uint32_t)col0 / 32;
+            if (kTx) {
+                xcol = tx + (col0 / a.tx_T) * (uint32_t)a.tx_layout_cols;
+                xend = xcol + (uint32_t)a.tx_layout_cols;
+                tc_ld4(xcol, xt);
+            } else if (kAhead) {
+                load_x(jc);
+            }
 #pragma unroll
-            for (int b = 0; b < B; ++b) acc[b][0] = acc[b][1] = 0.f;
+            for (int b = 0; b < B; ++b)
+#pragma unroll
+                for (int j = 0; j < kAcc; ++j) acc[b][j] = 0.f;
         },
-        [&]() {
-            if (jc >= jrow) {
-                flush(row);
+        [&](uint32_t cb, const TileRef& tile) {
+            if (!kTx && jc >= jrow) { /* (with x in TMEM tiles lie inside rows) */
+                flush(row, cb, tile);
                 jc -= jrow;
                 ++row;
             }
         },
         [&](const uint32_t (&w)[4], int h) {
+            if (kTx) tc_wait_ld_into(xt);
 #pragma unroll
             for (int b = 0; b < B; ++b) {
                 if (B > 1 && b >= batch) break;
-                const uint4 x4 = kAhead ? xv[b] : lds128(xs_lane + 64 * jc + (uint32_t)(b * xs_row_bytes(kp)));
-                acc[b][0] = fma2_bf16(w[0], x4.x, acc[b][0]);
-                acc[b][1] = fma2_bf16(w[1], x4.y, acc[b][1]);
-                acc[b][0] = fma2_bf16(w[2], x4.z, acc[b][0]);
-                acc[b][1] = fma2_bf16(w[3], x4.w, acc[b][1]);
+                const uint4 x4 = kTx ? make_uint4(xt[0], xt[1], xt[2], xt[3])
+                                     : kAhead ? xv[b] : lds128(xs_lane + 64 * jc + (uint32_t)(b * xs_row_bytes(kp)));
+                if (B == 1) {
+                    fma2x_bf16(w[0], x4.x, acc[b][0], acc[b][1 % kAcc]);
+                    fma2x_bf16(w[1], x4.y, acc[b][2 % kAcc], acc[b][3 % kAcc]);
+                    fma2x_bf16(w[2], x4.z, acc[b][0], acc[b][1 % kAcc]);
+                    fma2x_bf16(w[3], x4.w, acc[b][2 % kAcc], acc[b][3 % kAcc]);
+                } else {
+                    fma2x_bf16(w[0], x4.x, acc[b][0], acc[b][1]);
+                    fma2x_bf16(w[1], x4.y, acc[b][0], acc[b][1]);
+                    fma2x_bf16(w[2], x4.z, acc[b][0], acc[b][1]);
+                    fma2x_bf16(w[3], x4.w, acc[b][0], acc[b][1]);
+                }
             }
-            jc += 8;
-            /* rows start on block boundaries: only a second half can be followed by
-             * a new row */
-            if (kAhead) load_x(h == 1 && jc >= jrow ? jc - jrow : jc);
+            if (!kTx) jc += 8;
+            if (kTx) { /* the next 8 symbols' x, if the tile has them (one load in flight at a time) */
+                xcol += 4;
+                if (xcol < xend) tc_ld4(xcol, xt);
+            } else if (kAhead) {
+                /* rows start on block boundaries: only a second half can be followed by
+                 * a new row */
+                load_x(h == 1 && jc >= jrow ? jc - jrow : jc);
+            }
         },
-        [&]() { flush(row); });
+        [&](const TileRef& tile, uint32_t cb) { flush(row, cb, tile); });
+    }
+    if (kTx) { /* every warp is done with tensor memory */
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) {
+            tc_fence_after();
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(lds32(tslot)), "r"(a.tx_cols)
+                         : "memory");
+        }
+    }
 }
 
 /* ========================================= Huffman tensor-core GEMV (tcgen05) */
@@ -802,7 +1062,8 @@ constexpr uint32_t kMmaBufBytes = 32768u;       /* one chunk: 4 swizzle atoms of
 constexpr uint32_t kMmaAtomBytes = 8192u;       /* 64 rows x 128 B: x rows 0..31, then weight rows 0..31 */
 constexpr int kMmaMaxBatch = 32;                /* x rows per pass */
 constexpr int kMmaMaxBufs = 3;                 /* chunk buffers in flight: 3 where shared memory allows, else 2 */
-__host__ __device__ constexpr size_t mma_fixed_bytes(int nbuf) { return (size_t)nbuf * kMmaBufBytes + 96; } /* buffers, barriers */
+/* chunk buffers, barriers and the read slack after the last code pool */
+__host__ __device__ constexpr size_t mma_fixed_bytes(int nbuf) { return (size_t)nbuf * kMmaBufBytes + 96 + kSlackBytes; }
 
 __device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
@@ -814,8 +1075,6 @@ __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
 }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 /* Shared-memory matrix descriptor of a 128-byte-swizzled K-major operand whose
  * 8-row groups are 1024 bytes apart: start address >> 4 (bits 0..13), leading
@@ -859,13 +1118,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 }
 
 /* 32 lanes x 4 columns of 32 bits from TMEM (the lane quarter of the calling warp). */
-__device__ __forceinline__ void tc_ld4(uint32_t taddr, uint32_t (&v)[4]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
-                 : "r"(taddr)
-                 : "memory");
-}
-__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 /* The item a warp works on: matrix, first row, tile column, and the combined
  * index of the tile of the warp's row (have = the row exists). */
@@ -906,7 +1158,7 @@ struct MmaDone {
     uint32_t s, ph; /* buffer and phase parity of its last chunk */
 };
 
-template <bool kLong>
+template <bool kHier>
 __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_constant__ HuffMmaArgs a) {
     extern __shared__ __align__(1024) uint8_t mma_smem[]; /* (the dynamic block, 1 KB aligned) */
     uint8_t* const smem = mma_smem;
@@ -916,14 +1168,16 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
         if (threadIdx.x == 0) flag_corrupt(a.status);
         return;
     }
-    /* shared: nbuf chunk buffers | pair tables | two code pools (items alternate) | the
-     * pools' mbarriers | full, done, xfull [nbuf each] | TMEM address.  A lane's reads
-     * run up to kSlackBytes past its tile's code area: into the next tile, the other
-     * pool or the mbarriers, all inside the block. */
+    /* shared: nbuf chunk buffers | pair tables | staged sub-tables | two code pools
+     * (items alternate) | the pools' mbarriers | full, done, xfull [nbuf each] | TMEM
+     * address | slack.  A lane's reads run up to kSlackBytes past its tile's code area:
+     * into the next tile, the other pool, the mbarriers or the slack, all inside the
+     * block. */
     const uint32_t ops = smem_u32(smem);
     const int nbuf = a.nbuf;
     const uint32_t tabs_s = ops + (uint32_t)nbuf * kMmaBufBytes;
-    const uint32_t pools = tabs_s + (uint32_t)a.count * kPairTabBytes;
+    uint32_t* const subs = (uint32_t*)(smem + (size_t)nbuf * kMmaBufBytes + (size_t)a.count * kPairTabBytes);
+    const uint32_t pools = tabs_s + (uint32_t)a.count * kPairTabBytes + 4u * (uint32_t)a.sub_words;
     const uint32_t mbars = pools + 2u * (uint32_t)a.pool_bytes; /* pool p complete: all decoding warps' copies */
     const uint32_t full = mbars + 16, done = full + 24, xfull = full + 48, tslot = full + 72;
     const int64_t n_items = a.item_begin[a.count];
@@ -951,7 +1205,7 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
         TileRef r = mma_tile(a, itm);
         if (r.area > 0 && off + 64u + (uint32_t)r.area > (uint32_t)a.pool_bytes) r.area = 0;
         region = pools + p * (uint32_t)a.pool_bytes + off;
-        prefetch_code(region, mbars + 8 * p, r, lane);
+        prefetch_code(region, mbars + 8 * p, r, lane, r.area);
         return r;
     };
 
@@ -979,6 +1233,7 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
         uint4* dst = (uint4*)(smem + (tabs_s - smem_u32(smem)) + (size_t)k * kPairTabBytes);
         for (int i = threadIdx.x; i < EC_PAIR_WORDS / 4; i += blockDim.x) dst[i] = __ldg(src + i);
     }
+    if (kHier) stage_sub_tables(a, subs);
     if (warp == 0) { /* all 512 TMEM columns: 2 items x 8 accumulator tiles of 32 columns */
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(tslot) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -1119,32 +1374,61 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
                 if (have_prev) wait(full + 8 * prev.s, prev.ph);
                 fits = stage(mma_item(a, nit, rows, d), pi ^ 1u, region).area > 0 || !mma_item(a, nit, rows, d).have;
             }
-            if (ci.have && cur.area == 0 && lane == 0) flag_corrupt(a.status);
-            const bool dec = ci.have && cur.area > 0;
-            const PairCtx c{tabs_s + (uint32_t)ci.mi * kPairTabBytes, cb + 64, ci.mi};
-            const uint32_t pmax = 8u * (uint32_t)cur.area;
-            LaneBits s{};
+            /* the staged tile: lane starts, code area, window records (all of them: the pools
+             * are sized for whole tiles) */
+            const TileRecs tr = ci.have ? tile_recs(cb, cur.area, cur.area) : TileRecs{-1, 0u, 0u};
+            if (ci.have && tr.n < 0 && lane == 0) flag_corrupt(a.status);
+            const bool dec = tr.n >= 0;
+            const uint32_t cbytes = tr.code;
+            const uint32_t tab = tabs_s + (uint32_t)ci.mi * kPairTabBytes, area = cb + 64;
+            const HierCtx hc = hier_ctx(a.m[ci.mi], subs, a.status);
+            const uint32_t limit = area + cbytes;
+            Lane s{};
             uint32_t s1 = 0;
             uint4 rr[2] = {};
             const uint4* raw4 = (const uint4*)(cur.rec + 64) + lane;
+            uint2 rc = make_uint2(0u, 0u); /* the tile's window records: (applied, count) */
             if (dec) {
-                const uint32_t s0 = lds16(cb + 2 * lane);
+                const uint32_t s0 = lane ? lds16(cb + 2 * lane) : 0u;
                 s1 = lane < 31 ? lds16(cb + 2 * lane + 2) : 0u;
-                bits_seek(s, c.area, 8u * min(s0, (uint32_t)cur.area));
+                lane_seek(s, area, 8u * min(s0, cbytes));
                 rr[0] = __ldg(raw4);
                 if (nch > 2) rr[1] = __ldg(raw4 + 32);
+                rc = make_uint2(0u, (uint32_t)tr.n);
             }
             const uint32_t seg = (uint32_t)(lane >> 3) * kMmaAtomBytes + ((uint32_t)((lane & 7) ^ (d & 7)) << 4) +
                                  4096u + (uint32_t)d * 128u;
             auto chunk = [&](int ch, uint32_t r0, uint32_t r1) {
                 uint32_t w[4] = {0u, 0u, 0u, 0u};
                 if (dec) {
-                    s.p = min(s.p, pmax);
-                    decode8<kLong>(s, c, a, r0, r1, w);
+                    lane_clamp(s, limit);
+                    decode8<kHier>(s, tab, hc, r0, r1, w);
                 }
                 /* the buffer is free once the MMAs of its previous chunk (gc - nbuf) are done */
                 if (gc >= (uint32_t)nbuf) wait(done + 8 * bs, bp ^ 1u);
-                sts128(ops + bs * kMmaBufBytes + seg, w[0], w[1], w[2], w[3]);
+                const uint32_t opb = ops + bs * kMmaBufBytes;
+                sts128(opb + seg, w[0], w[1], w[2], w[3]);
+                /* window records of this chunk (tile positions below 256 (ch + 1)): the
+                 * true weight over the coded one, at its lane's row segment */
+                if (rc.x < rc.y) {
+                    __syncwarp();
+                    while (rc.x < rc.y) {
+                        const uint32_t idx = rc.x + (uint32_t)lane;
+                        const uint32_t e = idx < rc.y ? lds32(cb + 64 + cbytes + 4 * idx) : 0xFFFFFFFFu;
+                        const uint32_t q = e & 0xFFFu;
+                        const bool in = idx < rc.y && q < 256u * (uint32_t)(ch + 1);
+                        if (in) {
+                            const uint32_t lr = (q >> 3) & 31u;
+                            const uint32_t at = opb + (lr >> 3) * kMmaAtomBytes + (((lr & 7u) ^ (uint32_t)(d & 7)) << 4) +
+                                                4096u + (uint32_t)d * 128u + 2u * (q & 7u);
+                            const uint32_t wt = rec_weight(e, e >> 20);
+                            asm volatile("st.shared.u16 [%0], %1;" ::"r"(at), "h"((unsigned short)wt) : "memory");
+                        }
+                        const uint32_t n = (uint32_t)__popc(__ballot_sync(kFull, in));
+                        rc.x += n;
+                        if (n < 32) break;
+                    }
+                }
                 fence_async_smem(); /* the tensor cores read what the generic stores wrote */
                 tc_fence_before();
                 __syncwarp();
@@ -1165,7 +1449,7 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
                 }
             }
             /* every lane's codewords end in the last byte before the next lane's start */
-            const uint32_t p = s.p;
+            const uint32_t p = lane_pos(s, area), pmax = 8u * cbytes;
             const bool bad = dec && (lane < 31 ? (p > 8u * s1 || p + 8u <= 8u * s1) : (p + 64u > pmax));
             if (__any_sync(kFull, bad) && lane == 0) flag_corrupt(a.status);
         }
@@ -1197,12 +1481,26 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
  * with one 16-byte write and a warp writes 512 contiguous bytes. */
 
 
-template <bool kLong>
+/* Window records of a decoded tile that starts at flattened position `start` of
+ * its matrix: the true weight over the coded one (kept out of line: rare, and the
+ * decode loop needs every register). */
+__device__ __noinline__ void decode_records(uint32_t recs, uint32_t staged, const uint32_t* far, uint32_t nrec,
+                                            uint16_t* out, int64_t K, int64_t kp, int64_t start, int lane) {
+    for (uint32_t j = (uint32_t)lane; j < nrec; j += 32) {
+        const uint32_t e = j < staged ? lds32(recs + 4 * j) : __ldg(far + j), q = e & 0xFFFu;
+        const int64_t f = start + q, rr = f / kp, cc = f - rr * kp;
+        if (cc < K) out[rr * K + cc] = (uint16_t)rec_weight(e, e >> 20);
+    }
+}
+
+template <bool kHier>
 __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_decode_kernel(const __grid_constant__ HuffDecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+    /* shared: the current matrix's pair table | its staged sub-tables | per warp: two tile buffers */
     uint4* tab = (uint4*)smem;
-    uint8_t* wbase = smem + kPairTabBytes + (size_t)warp * huff_warp_bytes(a.code_bytes);
+    uint32_t* subs = (uint32_t*)(smem + kPairTabBytes);
+    uint8_t* wbase = smem + kPairTabBytes + 4 * (size_t)a.sub_words + (size_t)warp * huff_warp_bytes(a.code_bytes);
     const uint32_t bufs = smem_u32(wbase), buf_bytes = (uint32_t)tile_buf_bytes(a.code_bytes);
     const uint32_t tab_s = smem_u32(tab);
     const uint32_t mbars = bufs + 2 * buf_bytes;
@@ -1225,24 +1523,39 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_decode_kernel(const __gri
         TileRef first{};
         if (g0 < mend) {
             first = tile_ref(a, g0, tile_offsets(a, g0));
-            prefetch_code(bufs, mbars, first, lane);
+            prefetch_code(bufs, mbars, first, lane, a.code_bytes);
         }
         __syncthreads();
         const uint4* src = (const uint4*)M.table;
         for (int i = threadIdx.x; i < EC_PAIR_WORDS / 4; i += blockDim.x) tab[i] = __ldg(src + i);
+        /* this matrix's sub-tables, when they were sized to fit (sub_smem == 0) */
+        HuffMat Ms = M;
+        if (kHier && M.sub_smem >= 0 && 256 * M.n_sub <= a.sub_words) {
+            Ms.sub_smem = 0;
+            const uint4* ss = (const uint4*)(M.table + EC_PAIR_WORDS);
+            for (int i = threadIdx.x; i < 64 * M.n_sub; i += blockDim.x) ((uint4*)subs)[i] = __ldg(ss + i);
+        } else {
+            Ms.sub_smem = -1;
+        }
         __syncthreads();
         const int64_t kp = M.k_pad, K = M.k_cols;
         const bool vec = (K % 8) == 0;
         int64_t row = 0, col0 = 0;
         if (g0 < mend)
-            huff_walk<kLong>(
-                a, g0, nwarp, mend, first, bufs, buf_bytes, ph, lane, [&](int) { return tab_s; },
+            huff_walk<kHier>(
+                a, g0, nwarp, mend, first, bufs, buf_bytes, ph, lane,
+                [&](int) {
+                    WalkCtx c;
+                    c.tab = tab_s;
+                    c.h = hier_ctx(Ms, subs, a.status);
+                    return c;
+                },
                 [&](const TileRef& r) {
                     const int64_t T = 32 * (int64_t)M.steps;
                     row = tile_row(r.t, T, kp, EC_HUFF_ROW_ALIGN);
                     col0 = r.t * T - row * kp;
                 },
-                [&]() {
+                [&](uint32_t, const TileRef&) {
                     if (col0 >= kp) {
                         col0 -= kp;
                         ++row;
@@ -1263,7 +1576,16 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_decode_kernel(const __gri
                     }
                     col0 += 256;
                 },
-                [&]() {});
+                [&](const TileRef& r, uint32_t cb) {
+                    /* window records: the true weight over the coded one (stored above by
+                     * some lane of this warp) */
+                    const TileRecs tr = tile_recs(cb, r.area, a.code_bytes);
+                    if (tr.n > 0) {
+                        __syncwarp();
+                        decode_records(cb + 64 + tr.code, tr.staged, far_records(r, tr.code), (uint32_t)tr.n, M.out, K,
+                                       kp, 32 * (int64_t)M.steps * r.t, lane);
+                    }
+                });
         cur = mend;
     }
 }
@@ -2019,6 +2341,9 @@ HuffMat huff_desc(const ec_matrix* W) {
     m.tile_off = (const uint32_t*)(W->d_blob + h.tile_off_off);
     m.table = (const uint32_t*)(W->d_blob + h.table_off);
     m.table_words = h.table_words;
+    m.n_sub = h.huff_sub_tables;
+    m.sub_smem = -1;
+    m.fill = h.huff_fill;
     m.n_rows = h.n_rows;
     m.k_cols = h.k_cols;
     m.k_pad = h.k_pad;
@@ -2122,11 +2447,41 @@ int grid_for(const DeviceInfo& d, int64_t work_items, int ctas_per_sm) {
     return (int)std::max<int64_t>(1, std::min(full, need));
 }
 
-/* kPart selects the allocation-free variant, lng the kernel that walks the
- * hierarchical table for codewords longer than the pair-table window. */
+/* Room of a per-warp tile buffer for matrix W (after the 64 bytes of lane starts):
+ * its largest code area and kStagedRecs window records; a tile's further records
+ * are read from global memory. */
+constexpr int kStagedRecs = 64;
+int staged_code_bytes(const ec_matrix* W) {
+    const int area = (W->hdr.max_code_area + 15) & ~15;
+    return std::min(area + 4 * kStagedRecs, std::max(area, (W->hdr.max_code_bytes + 15) & ~15));
+}
+
+/* A matrix decoded through the hierarchical tables (no window records). */
+bool huff_hier(const ec_matrix* W) { return !(W->hdr.huff_flags & EC_HUFF_WINDOW_REC); }
+
+/* Stage the sub-tables of a launch's hierarchical matrices in shared memory, in
+ * order, while kSubSmemTables hold them; returns the staged words. */
+template <int N>
+int plan_sub_tables(HuffMat (&m)[N], int count) {
+    int used = 0;
+    for (int k = 0; k < count; ++k) {
+        m[k].sub_smem = -1;
+        if (m[k].n_sub == 0) continue;
+        if (used + m[k].n_sub <= kSubSmemTables) {
+            m[k].sub_smem = 256 * used;
+            used += m[k].n_sub;
+        }
+    }
+    return 256 * used;
+}
+
+/* kPart selects the allocation-free variant, lng (hierarchical) the kernel that
+ * checks every pair and walks the sub-tables for what the window cannot hold. */
 template <int B, bool kPart>
 int launch_huff_gemv_b(const HuffGemvArgs& a, bool lng, size_t smem, int grid, int block, cudaStream_t s) {
-    auto kern = lng ? huff_gemv_kernel<B, kPart, true> : huff_gemv_kernel<B, kPart, false>;
+    auto kern = lng ? huff_gemv_kernel<B, kPart, true, false> : huff_gemv_kernel<B, kPart, false, false>;
+    if (B == 1 && !kPart && a.tx_cols > 0)
+        kern = lng ? huff_gemv_kernel<1, false, true, true> : huff_gemv_kernel<1, false, false, true>;
     if (set_smem(kern, smem) != EC_OK) return EC_ERR_CUDA;
     return launch_ex(kern, grid, block, smem, s, a);
 }
@@ -2180,8 +2535,9 @@ void set_tile_stride(HuffMat& m, int64_t warps_total) {
 }
 
 int plan_huff_gemv(const DeviceInfo& d, int count, int code_bytes, int64_t kp, int batch, int64_t total_tiles,
-                   GemvPlan* pl) {
-    const size_t tables = (size_t)count * kPairTabBytes, per_warp = huff_warp_bytes(code_bytes);
+                   int sub_words, GemvPlan* pl) {
+    /* the TMEM address slot (16 B), the pair tables and the staged sub-tables */
+    const size_t tables = 16 + (size_t)count * kPairTabBytes + 4 * (size_t)sub_words, per_warp = huff_warp_bytes(code_bytes);
     pl->xrow = xs_row_bytes((uint32_t)kp);
     if (tables + pl->xrow + 4 * per_warp > d.smem_optin) return EC_ERR_UNSUPPORTED;
     const int cap = huff_max_warps(batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : batch <= 8 ? 8 : 16);
@@ -2274,11 +2630,12 @@ int huff_mma(const ec_matrix* const* Ws, int count, const uint16_t* x, float* co
         total += W->hdr.n_tiles;
         a.row_tiles[k] = (int32_t)(W->hdr.k_pad / (32 * (int64_t)W->hdr.steps));
         code_bytes = std::max(code_bytes, (int)W->hdr.max_code_bytes);
-        lng = lng || W->hdr.max_len > EC_L1_BITS;
+        lng = lng || huff_hier(W);
         if (a.m[k].atomic_y &&
             cudaMemsetAsync(ys[k], 0, sizeof(float) * (size_t)batch * (size_t)W->hdr.n_rows, s) != cudaSuccess)
             return EC_ERR_CUDA;
     }
+    a.sub_words = plan_sub_tables(a.m, count);
     code_bytes = (code_bytes + 15) & ~15;
     a.code_bytes = code_bytes;
     a.total_tiles = total;
@@ -2288,7 +2645,7 @@ int huff_mma(const ec_matrix* const* Ws, int count, const uint16_t* x, float* co
     a.pool_bytes = (int)((window + 15) & ~int64_t(15));
     /* warps: a multiple of 8, at most 32 (one produces, the others decode one row each:
      * rows per item = warps - 1 <= EC_MMA_WINDOW_ROWS, N = warps); 3 chunk buffers where they fit */
-    const size_t fixed_rest = (size_t)count * kPairTabBytes + 2 * (size_t)a.pool_bytes;
+    const size_t fixed_rest = (size_t)count * kPairTabBytes + 4 * (size_t)a.sub_words + 2 * (size_t)a.pool_bytes;
     int nw = 0, nbuf = 0;
     for (int nb = kMmaMaxBufs; nb >= 2 && !nw; --nb)
         for (int w = kMaxHW; w >= (nb == 2 ? 8 : kMaxHW) && !nw; w -= 8)
@@ -2333,8 +2690,8 @@ int huff_gemv(const ec_matrix* const* Ws, int count, const uint16_t* x, float* c
         a.m[k] = huff_desc(W);
         a.m[k].tile_begin = total;
         total += W->hdr.n_tiles;
-        code_bytes = std::max(code_bytes, (int)W->hdr.max_code_bytes);
-        lng = lng || W->hdr.max_len > EC_L1_BITS;
+        code_bytes = std::max(code_bytes, staged_code_bytes(W));
+        lng = lng || huff_hier(W);
         if (a.m[k].atomic_y || W->hdr.n_tiles == 0) {
             if (cudaMemsetAsync(ys[k], 0, sizeof(float) * (size_t)batch * (size_t)W->hdr.n_rows, s) != cudaSuccess)
                 return EC_ERR_CUDA;
@@ -2344,11 +2701,27 @@ int huff_gemv(const ec_matrix* const* Ws, int count, const uint16_t* x, float* c
     a.total_tiles = total;
     a.status = d->status;
     a.code_bytes = code_bytes;
+    a.sub_words = plan_sub_tables(a.m, count);
     if (total == 0) return EC_OK;
     GemvPlan pl;
-    int rc = plan_huff_gemv(*d, count, code_bytes, kp, batch, total, &pl);
+    int rc = plan_huff_gemv(*d, count, code_bytes, kp, batch, total, a.sub_words, &pl);
     if (rc != EC_OK) return rc;
     for (int k = 0; k < count; ++k) set_tile_stride(a.m[k], (int64_t)pl.grid * pl.warps);
+    /* batch 1 over tiles that lie inside rows, all of one width: x from tensor memory */
+    if (batch == 1) {
+        const int64_t T = 32 * (int64_t)Ws[0]->hdr.steps;
+        bool ok = T > 0 && kp % T == 0;
+        for (int k = 0; k < count && ok; ++k) ok = Ws[k]->hdr.steps == Ws[0]->hdr.steps;
+        const int64_t used = ok ? (kp / T) * (T / 64) : 0;
+        int cols = 32;
+        while (cols < used) cols *= 2;
+        if (ok && used > 0 && cols <= 512) {
+            a.tx_cols = cols;
+            a.tx_layout_cols = (int)(T / 64);
+            a.tx_used = (int)used;
+            a.tx_T = (uint32_t)T;
+        }
+    }
     for (int b0 = 0; b0 < batch; b0 += pl.per_pass) {
         const int nb = std::min(pl.per_pass, batch - b0);
         a.batch = nb;
@@ -2654,8 +3027,13 @@ extern "C" int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs
         m.out = outs[k];
         m.tile_begin = total;
         total += Ws[k]->hdr.n_tiles;
-        code_bytes = std::max(code_bytes, (int)Ws[k]->hdr.max_code_bytes);
-        lng = lng || Ws[k]->hdr.max_len > EC_L1_BITS;
+        code_bytes = std::max(code_bytes, staged_code_bytes(Ws[k]));
+        lng = lng || huff_hier(Ws[k]);
+        /* one matrix at a time is resident: its sub-tables are staged when they fit */
+        if (huff_hier(Ws[k]) && m.n_sub > 0 && m.n_sub <= kSubSmemTables) {
+            m.sub_smem = 0;
+            a.sub_words = std::max(a.sub_words, 256 * m.n_sub);
+        }
         a.m[a.count++] = m;
     }
     if (a.count == 0 || total == 0) return EC_OK;
@@ -2663,10 +3041,10 @@ extern "C" int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs
     a.total_tiles = total;
     a.status = d->status;
     a.code_bytes = code_bytes;
-    const size_t per_warp = huff_warp_bytes(code_bytes);
-    if (kPairTabBytes + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED;
-    const int warps = (int)std::min<size_t>(kMaxHW, (d->smem_optin - kPairTabBytes) / per_warp);
-    const size_t smem = kPairTabBytes + (size_t)warps * per_warp;
+    const size_t per_warp = huff_warp_bytes(code_bytes), fixed = kPairTabBytes + 4 * (size_t)a.sub_words;
+    if (fixed + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED;
+    const int warps = (int)std::min<size_t>(kMaxHW, (d->smem_optin - fixed) / per_warp);
+    const size_t smem = fixed + (size_t)warps * per_warp;
     auto kern = lng ? huff_decode_kernel<true> : huff_decode_kernel<false>;
     if (set_smem(kern, smem) != EC_OK) return EC_ERR_CUDA;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(d->sms, (total + warps - 1) / warps));
@@ -2773,22 +3151,23 @@ extern "C" int ec_gemv_static(const ec_matrix* W, const uint16_t* x, float* y, i
     a.count = 1;
     a.total_tiles = h.n_tiles;
     a.status = (int*)d->scratch;
-    a.code_bytes = ((int)h.max_code_bytes + 15) & ~15;
+    a.code_bytes = staged_code_bytes(W);
     a.part = d->scratch + kStaticHeaderFloats;
     a.part_slots = (int)slots;
+    a.sub_words = plan_sub_tables(a.m, 1);
     if (a.code_bytes < 16) a.code_bytes = 16;
     if (cudaMemsetAsync(d->scratch, 0, sizeof(int), stream) != cudaSuccess) return EC_ERR_CUDA;
     GemvPlan pl;
     DeviceInfo di{};
     di.sms = d->sms;
     di.smem_optin = d->smem_optin;
-    if ((rc = plan_huff_gemv(di, 1, a.code_bytes, h.k_pad, batch, h.n_tiles, &pl)) != EC_OK) return rc;
+    if ((rc = plan_huff_gemv(di, 1, a.code_bytes, h.k_pad, batch, h.n_tiles, a.sub_words, &pl)) != EC_OK) return rc;
     set_tile_stride(a.m[0], (int64_t)pl.grid * pl.warps);
     for (int b0 = 0; b0 < batch; b0 += pl.per_pass) {
         const int nb = std::min(pl.per_pass, batch - b0);
         a.batch = nb;
         a.x = x + (int64_t)b0 * h.k_cols;
-        if ((rc = launch_huff_gemv<true>(a, h.max_len > EC_L1_BITS, pl.fixed + pl.xrow * nb, pl.grid, pl.warps * 32,
+        if ((rc = launch_huff_gemv<true>(a, huff_hier(W), pl.fixed + pl.xrow * nb, pl.grid, pl.warps * 32,
                                          stream)) != EC_OK)
             return rc;
         const int64_t n = (int64_t)nb * h.n_rows;

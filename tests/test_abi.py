@@ -83,13 +83,14 @@ def test_argument_validation(ec):
 
 
 # --------------------------------------------------------------- blob reader
-HDR = struct.Struct("<IIii" + "q" * 10 + "i" * 6 + "Ii" + "qqq")
+HDR = struct.Struct("<IIii" + "q" * 10 + "i" * 6 + "Ii" + "qqq" + "iiii")
 
 
 HDR_KEYS = ["magic", "version", "kind", "steps", "n_rows", "k_cols", "k_pad", "n_tiles", "table_off",
             "table_words", "scales_off", "tile_off_off", "records_off", "blob_bytes", "max_code_bytes",
             "prob_bits", "max_words", "max_len", "rans_tuple", "window_code_bytes", "e8_scale_bits",
-            "fp8_table_size", "esc_off_off", "esc_records_off", "n_escapes"]
+            "fp8_table_size", "esc_off_off", "esc_records_off", "n_escapes", "huff_flags", "huff_sub_tables",
+            "huff_fill", "max_code_area"]
 
 
 def hdr_offset(key: str) -> int:
@@ -111,8 +112,66 @@ def huff_pos(i: int, l: int) -> int:
     return 256 * (i // 8) + 8 * l + i % 8
 
 
+def raw_sign_mantissa(raw_t: np.ndarray, S: int) -> np.ndarray:
+    """Sign/mantissa bytes [symbol][lane] of a tile's raw section: lane-transposed
+    16-byte chunks, and inside each group of four symbols i..i+3 the bits laid out so
+    that a little-endian word r holds [w(i+1)|w(i)] under 0x807F807F and [w(i+3)|w(i+2)]
+    under the same mask after rotating right by 8."""
+    S16 = (S + 15) // 16 * 16
+    g = raw_t.reshape(S16 // 16, 32, 4, 4)  # [chunk][lane][group][byte]
+    b0, b1, b2, b3 = (g[..., j].astype(np.int64) for j in range(4))
+    sm = np.stack([(b1 & 0x80) | (b0 & 0x7F),   # symbol i:   sign in byte 1, mantissa in byte 0
+                   (b3 & 0x80) | (b2 & 0x7F),   # symbol i+1: sign in byte 3, mantissa in byte 2
+                   (b2 & 0x80) | (b1 & 0x7F),   # symbol i+2: sign in byte 2, mantissa in byte 1
+                   (b0 & 0x80) | (b3 & 0x7F)],  # symbol i+3: sign in byte 0, mantissa in byte 3
+                  axis=-1)  # [chunk][lane][group][symbol in group]
+    return sm.transpose(0, 2, 3, 1).reshape(S16, 32)[:S]
+
+
+def area_bits(words: np.ndarray) -> str:
+    """The code area as a string of bits in stream order (LSB first within each word)."""
+    return "".join(format(int(x), "032b")[::-1] for x in words)
+
+
+def tile_layout(h, dev, t):
+    """(record offset, symbols per lane, sign/mantissa bytes, record count, code area offset,
+    code area end) of tile t: lane starts (lane 0's slot holds the window record count),
+    raw bytes, the code area, then the records (padded to 16 bytes)."""
+    T = 32 * h["steps"]
+    toff = np.frombuffer(dev, np.uint32, h["n_tiles"] + 1, h["tile_off_off"])
+    rec = h["records_off"] + int(toff[t]) * 16
+    S = min(T, h["n_rows"] * h["k_pad"] - t * T) // 32
+    raw_bytes = 32 * ((S + 15) // 16 * 16)
+    nrec = int(np.frombuffer(dev, np.uint16, 1, rec)[0])
+    area_off = rec + 64 + raw_bytes
+    area_end = h["records_off"] + int(toff[t + 1]) * 16 - 16 * ((4 * nrec + 15) // 16)
+    return rec, S, raw_bytes, nrec, area_off, area_end
+
+
+def lane_starts(dev, rec):
+    st = np.frombuffer(dev, np.uint16, 32, rec).astype(np.int64).copy()
+    st[0] = 0  # lane 0 starts at the area's first byte
+    return st
+
+
+def tile_records(h, dev, t, with_sm=False):
+    """Window records of tile t: (position, true exponent, coded exponent[, sign/mantissa byte])
+    from 12-bit position | sign and mantissa << 12 | exponent << 20."""
+    rec, S, raw_bytes, nrec, _, area_end = tile_layout(h, dev, t)
+    assert nrec == 0 or h["huff_flags"] & 1
+    er = np.frombuffer(dev, np.uint32, nrec, area_end)
+    out = []
+    for i in range(nrec):
+        r = int(er[i])
+        assert r >> 28 == 0
+        rec = (r & 0xFFF, (r >> 20) & 0xFF, h["huff_fill"])
+        out.append(rec + ((r >> 12) & 0xFF,) if with_sm else rec)
+    return out
+
+
 def read_huffman(blob: bytes, lengths: np.ndarray) -> np.ndarray:
-    """Reconstruct the BF16 matrix from a Huffman blob with a bit-by-bit reader."""
+    """Reconstruct the BF16 matrix from a Huffman blob with a bit-by-bit reader
+    (canonical codewords, first bit first), then apply the window records."""
     h, dev = parse(blob)
     codes = O.canonical_codes(lengths)
     table = {(int(lengths[s]), int(codes[s])): s for s in range(256) if lengths[s]}
@@ -121,77 +180,83 @@ def read_huffman(blob: bytes, lengths: np.ndarray) -> np.ndarray:
     toff = np.frombuffer(dev, np.uint32, h["n_tiles"] + 1, h["tile_off_off"])
     flat = np.zeros(n * kp, np.uint16)
     for t in range(h["n_tiles"]):
-        rec = h["records_off"] + int(toff[t]) * 16
-        n_t = min(T, n * kp - t * T)
-        start = np.frombuffer(dev, np.uint16, 32, rec)
-        S = n_t // 32
-        S16 = (S + 15) // 16 * 16
-        raw_t = np.frombuffer(dev, np.uint8, 32 * S16, rec + 64)
-        # lane-transposed 16-byte chunks: chunk j of lane l holds symbols 16j..16j+15
-        raw = raw_t.reshape(S16 // 16, 32, 16).transpose(0, 2, 1).reshape(S16, 32)[:S].ravel()
-        area_off = rec + 64 + 32 * S16
-        area_end = h["records_off"] + int(toff[t + 1]) * 16
-        words = np.frombuffer(dev, np.uint32, (area_end - area_off) // 4, area_off)
-        bits = "".join(format(int(x), "032b") for x in words)
+        rec, S, raw_bytes, _, area_off, area_end = tile_layout(h, dev, t)
+        start = lane_starts(dev, rec)
+        raw = raw_sign_mantissa(np.frombuffer(dev, np.uint8, raw_bytes, rec + 64), S)
+        bits = area_bits(np.frombuffer(dev, np.uint32, (area_end - area_off) // 4, area_off))
+        expo = {}
         for l in range(32):
             pos = 8 * int(start[l])
-            for i in range(n_t // 32):
+            for i in range(S):
                 L, c = 0, 0
                 while (L, c) not in table:
                     c = (c << 1) | (bits[pos] == "1")
                     L += 1
                     pos += 1
                     assert L <= 24
-                e = table[(L, c)]
-                r = int(raw[32 * i + l])  # raw is [symbol][lane]
-                flat[t * T + huff_pos(i, l)] = ((r & 0x80) << 8) | (e << 7) | (r & 0x7F)
+                expo[huff_pos(i, l)] = table[(L, c)]
+        sm_of = {}
+        for q, e_true, e_coded, sm in tile_records(h, dev, t, with_sm=True):
+            assert expo[q] == e_coded
+            expo[q] = e_true
+            sm_of[q] = sm
+        for l in range(32):
+            for i in range(S):
+                q = huff_pos(i, l)
+                r = int(raw[i, l])
+                assert sm_of.get(q, r) == r  # a record carries the weight's own sign and mantissa
+                flat[t * T + q] = ((r & 0x80) << 8) | (expo[q] << 7) | (r & 0x7F)
     return flat.reshape(n, kp)[:, :k]
 
 
 def walk_pair_table(blob: bytes):
     """Decode a Huffman blob the way a GPU lane does: two exponents per lookup of
-    the pair table, a second lookup when only the first codeword fits, and the
-    hierarchical table for codewords longer than the window.  Returns the
-    exponent of every padded position and whether every lane ended in the last
-    byte before the next lane's start."""
+    the pair table (indexed by the next 12 stream bits, the first at bit 0); an open
+    entry (only without window records) takes a second lookup, and codewords longer
+    than the window walk the sub-tables.  Window records then replace the coded
+    exponents.  Returns the exponent of every padded position and whether every
+    lane ended in the last byte before the next lane's start."""
     h, dev = parse(blob)
     tab = np.frombuffer(dev, np.uint32, h["table_words"], h["table_off"])
-    pair, hier = tab[:4096], tab[4096:]
+    pair, sub = tab[:4096], tab[4096:]
     T = 32 * h["steps"]
     n_pad = h["n_rows"] * h["k_pad"]
     toff = np.frombuffer(dev, np.uint32, h["n_tiles"] + 1, h["tile_off_off"])
     exps = np.zeros(n_pad, np.int64)
     ends_ok = True
+    records = bool(h["huff_flags"] & 1)
 
-    def one(bits, p):  # hierarchical walk for one codeword
-        win = int(bits[p:p + 32], 2)
-        ent = int(hier[win >> 20])
-        while ent & 0x80000000:
-            used = (ent >> 16) & 31
-            ent = int(hier[4096 + (ent & 0xFFFF) * 256 + (((win << used) & 0xFFFFFFFF) >> 24)])
-        assert not ent & 0x40000000
-        return (ent & 0xFFFF) >> 7, (ent >> 16) & 31
+    def win(bits, p, n):  # the next n stream bits, the first at bit 0
+        return sum(1 << j for j in range(n) if bits[p + j] == "1")
+
+    def long_cw(bits, p, ent):  # sub-table walk for a codeword longer than the window
+        t, used = (ent >> 7) & 0x1FF, 12
+        while True:
+            e = int(sub[256 * t + win(bits, p + used, 8)])
+            if not e & 0x80000000:
+                break
+            t, used = e & 0xFFFF, (e >> 16) & 31
+        assert not e & 0x40000000
+        return (e & 0xFFFF) >> 7, (e >> 16) & 31
 
     for t in range(h["n_tiles"]):
-        rec = h["records_off"] + int(toff[t]) * 16
-        S = min(T, n_pad - t * T) // 32
-        start = np.frombuffer(dev, np.uint16, 32, rec)
-        area_off = rec + 64 + 32 * ((S + 15) // 16 * 16)
-        area_end = h["records_off"] + int(toff[t + 1]) * 16
+        rec, S, _, _, area_off, area_end = tile_layout(h, dev, t)
+        start = lane_starts(dev, rec)
         words = np.frombuffer(dev, np.uint32, (area_end - area_off) // 4, area_off)
-        bits = "".join(format(int(x), "032b") for x in words) + "0" * 64
+        bits = area_bits(words) + "0" * 64
         for l in range(32):
             p = 8 * int(start[l])
             for s in range(S // 2):
-                e = int(pair[int(bits[p:p + 12], 2)])
-                if e & 15:
+                e = int(pair[win(bits, p, 12)])
+                if not e & 0x80000000:
                     x0, x1, adv = (e >> 7) & 255, (e >> 23) & 255, e & 15
                 else:
+                    assert not records, "an open pair entry in a stream with window records"
                     l0 = (e >> 16) & 15
-                    x0, l0 = ((e >> 7) & 255, l0) if l0 else one(bits, p)
-                    f = int(pair[int(bits[p + l0:p + l0 + 12], 2)])
+                    x0, l0 = ((e >> 7) & 255, l0) if l0 else long_cw(bits, p, e)
+                    f = int(pair[win(bits, p + l0, 12)])
                     l1 = (f >> 16) & 15
-                    x1, l1 = ((f >> 7) & 255, l1) if l1 else one(bits, p + l0)
+                    x1, l1 = ((f >> 7) & 255, l1) if l1 else long_cw(bits, p + l0, f)
                     adv = l0 + l1
                 exps[t * T + huff_pos(2 * s, l)] = x0
                 exps[t * T + huff_pos(2 * s + 1, l)] = x1
@@ -200,14 +265,18 @@ def walk_pair_table(blob: bytes):
                 ends_ok &= 8 * int(start[l + 1]) - 8 < p <= 8 * int(start[l + 1])
             else:
                 ends_ok &= p + 64 <= 32 * len(words)
+        for q, e_true, e_coded in tile_records(h, dev, t):
+            assert exps[t * T + q] == e_coded
+            exps[t * T + q] = e_true
     return exps, ends_ok
 
 
+@pytest.mark.parametrize("hier", [False, True])
 @pytest.mark.parametrize("case", ["llama", "fib24", "fib12", "one_symbol", "all_patterns"])
-def test_pair_table_walk_decodes_exponents(ec, case):
+def test_pair_table_walk_decodes_exponents(ec, case, hier):
     if case == "llama":
         w = synth.llama_bf16(2010, 24, 2048)
-        W = ec.encode_bf16(w, device=-1)
+        W = ec.encode_bf16(w, device=-1, hierarchical=hier)
     elif case.startswith("fib"):
         fib = [1, 1]
         while len(fib) < 30:
@@ -216,22 +285,63 @@ def test_pair_table_walk_decodes_exponents(ec, case):
         rng = np.random.default_rng(1)
         rng.shuffle(e)
         w = ((e.astype(np.uint16) << 7) | (np.arange(e.size) % 128).astype(np.uint16)).reshape(-1, 4096)[:8]
-        W = ec.encode_bf16(w, max_code_len=int(case[3:]), device=-1)
-        # L=24: codewords longer than the window reach the hierarchical table;
+        W = ec.encode_bf16(w, max_code_len=int(case[3:]), device=-1, hierarchical=hier)
+        # L=24: codewords longer than the window reach the sub-tables (or, with window
+        # records, are coded as the shortest codeword and recorded);
         # L=12: the longest codeword fills the window exactly
         assert W.code_lengths().max() > 12 if case == "fib24" else W.code_lengths().max() == 12
     elif case == "one_symbol":
         w = np.full((3, 512), 0x3F80, np.uint16)
-        W = ec.encode_bf16(w, device=-1)
+        W = ec.encode_bf16(w, device=-1, hierarchical=hier)
     else:
         w = np.arange(65536, dtype=np.uint16).reshape(256, 256)
-        W = ec.encode_bf16(w, device=-1)
-    exps, ends_ok = walk_pair_table(W.serialize())
+        W = ec.encode_bf16(w, device=-1, hierarchical=hier)
+    blob = W.serialize()
+    h, _ = parse(blob)
+    # window records unless asked otherwise, or unless two shortest codewords overflow
+    # the window (the uniform histogram of all patterns: every codeword is 8 bits)
+    assert h["huff_flags"] == (0 if hier or case == "all_patterns" else 1)
+    if h["huff_flags"]:
+        assert h["huff_sub_tables"] == 0
+        if case in ("llama", "fib24"):
+            assert h["n_escapes"] > 0
+    elif case == "fib24":
+        assert h["huff_sub_tables"] > 0
+    exps, ends_ok = walk_pair_table(blob)
     kp = W.stats()["k_pad"]
     want = np.zeros((w.shape[0], kp), np.int64)
     want[:, : w.shape[1]] = (w >> 7) & 0xFF
     assert np.array_equal(exps.reshape(w.shape[0], kp), want)
     assert ends_ok
+
+
+@pytest.mark.parametrize("hier", [False, True])
+def test_window_records_bound(ec, hier):
+    """Window records replace exactly the symbols of pairs whose codewords overflow the
+    12-bit window: the record count equals what the code lengths imply (one record when
+    the shortest codeword fits beside the first, else one or two)."""
+    w = synth.llama_bf16(2011, 64, 4096)
+    W = ec.encode_bf16(w, device=-1, hierarchical=hier)
+    h, dev = parse(W.serialize())
+    lens = W.code_lengths().astype(np.int64)
+    if hier:
+        assert h["huff_flags"] == 0 and h["n_escapes"] == 0
+        return
+    fill = int(np.argmin(np.where(lens > 0, lens, 99)))
+    lf = lens[fill]
+    e = ((w >> 7) & 0xFF).astype(np.int64)  # 4096 columns: one tile per row, no padding
+    n_rec = 0
+    for row in e:
+        lanes = row.reshape(16, 32, 8).transpose(1, 0, 2).reshape(32, -1)  # [lane][symbol]
+        for seq in lanes:
+            a, b = lens[seq[0::2]], lens[seq[1::2]]
+            over = a + b > 12
+            first_fits = a + lf <= 12
+            n_rec += int((over & first_fits).sum()) + int((over & ~first_fits).sum()) + int(
+                (over & ~first_fits & (lf + b > 12)).sum())
+    assert h["n_escapes"] == n_rec
+    st = W.stats()
+    assert 8 * 4 * h["n_escapes"] / w.size < 0.2  # records cost well under 0.2 bit per weight
 
 
 @pytest.mark.parametrize("shape,steps", [((7, 13), 128), ((3, 300), 32), ((40, 1024), 64), ((2, 4097), 128)])
@@ -467,11 +577,16 @@ def test_gemv_path_dispatch(ec):
 def test_tile_width_aux_bounds(ec):
     w = synth.llama_bf16(2001, 1024, 4096)
     for steps, lo, hi in ((128, 0.125, 0.25), (64, 0.25, 0.40)):
-        s = ec.encode_bf16(w, tile_steps=steps, device=-1).stats()
+        W = ec.encode_bf16(w, tile_steps=steps, device=-1)
+        s = W.stats()
+        h, _ = parse(W.serialize())
         assert s["n_tiles"] == w.size // (32 * steps)
         # per tile: 64 B of lane starts, each lane's last byte (about 4 bits x 32
-        # lanes) and the area's >= 8 zero bytes and 16-byte padding
-        assert lo < s["aux_bytes"] * 8 / w.size < hi, steps
+        # lanes) and the area's >= 8 zero bytes and 16-byte padding; besides these, the
+        # window records (4 bytes each, padded to 16 per tile)
+        rec_bytes = 4 * h["n_escapes"] + 12 * h["n_tiles"]
+        assert h["huff_flags"] == 1 and 0 < rec_bytes * 8 / w.size < 0.2
+        assert lo < (s["aux_bytes"] - rec_bytes) * 8 / w.size < hi, steps
 
 
 def test_stats_accounting(ec):
@@ -481,13 +596,24 @@ def test_stats_accounting(ec):
     n = w.size
     assert s["k_pad"] == 4096 and s["n_tiles"] == n // 4096
     cnt = np.bincount(((w >> 7) & 0xFF).ravel(), minlength=256)
+    lens = W.code_lengths().astype(np.int64)
     assert s["entropy_bits"] == pytest.approx(O.entropy(cnt), rel=1e-12)
-    assert s["payload_bits"] == int((cnt * W.code_lengths()).sum())
+    # the stream holds every exponent's codeword except where a window record put the
+    # shortest one in its place
+    h, dev = parse(W.serialize())
+    recs = [r for t in range(h["n_tiles"]) for r in tile_records(h, dev, t)]
+    assert len(recs) == h["n_escapes"] > 0
+    saved = sum(int(lens[e_true] - lens[e_coded]) for _, e_true, e_coded in recs)
+    assert s["payload_bits"] == int((cnt * lens).sum()) - saved
     assert s["raw_bytes"] == n
     assert s["device_bytes"] * 8 / n == pytest.approx(s["bits_per_weight"])
-    # aux (lane starts, byte alignment, 16-byte record padding, offsets) well under 0.25 bit per weight
-    assert s["aux_bytes"] * 8 / n < 0.25
+    # aux (lane starts, byte alignment, 16-byte record padding, offsets) well under 0.25 bit per
+    # weight, plus the window records
+    assert (s["aux_bytes"] - 4 * len(recs)) * 8 / n < 0.25
     assert 10.5 < s["bits_per_weight"] < 11.3
+    Wh = ec.encode_bf16(w, tile_steps=128, device=-1, hierarchical=True)
+    sh = Wh.stats()
+    assert sh["payload_bits"] == int((cnt * lens).sum()) and sh["aux_bytes"] * 8 / n < 0.25
 
 
 # --------------------------------------------------------------- E8 lattice codec

@@ -139,28 +139,38 @@ def test_full_size_8b_layer(ec):
         y_ref, a_ref = O.gemv_bf16(w, x)
         check_gemv(gemv_gpu(ec, W, x, spec.n_rows), y_ref, a_ref, spec.name)
         s = W.stats()
-        assert s["aux_bytes"] * 8 / w.size < 0.25
+        # lane starts, alignment and offsets; window records (4 bytes each) besides
+        assert (s["aux_bytes"] - 4 * s["n_records"]) * 8 / w.size < 0.25
+        assert 4 * s["n_records"] * 8 / w.size < 0.2
         W.free()
 
 
-def test_payload_corruption_is_reported_not_faulted(ec):
+@pytest.mark.parametrize("hier", [False, True])
+def test_payload_corruption_is_reported_not_faulted(ec, hier):
+    """Lane 3's codewords of tile 0 overwritten with ones: every lookup then decodes
+    the all-ones codeword (the longest, 12 bits; the code is complete), so the lane
+    runs far past the next lane's start and the walker must report EC_ERR_CORRUPT,
+    for the decode and for the GEMV, without a fault."""
     w = synth.llama_bf16(2500, 64, 4096)
-    W = ec.encode_bf16(w)
+    W = ec.encode_bf16(w, hierarchical=hier)
+    assert W.code_lengths().max() == 12
     blob = bytearray(W.serialize())
-    from test_abi import parse
+    from test_abi import parse, tile_layout, lane_starts
     h, devb = parse(bytes(blob))
     meta = len(blob) - len(devb)
-    rec = meta + h["records_off"]
-    # flip bits inside the first tile's code area (after 64 B of lane starts and the raw bytes)
-    area = 64 + 32 * h["steps"]
-    for off in (area + 3, area + 200, area + 500):
-        blob[rec + off] ^= 0x5A
+    rec, S, _, _, area_off, _ = tile_layout(h, devb, 0)
+    st = lane_starts(devb, rec)
+    assert 8 * (st[4] - st[3]) < 12 * S  # the lane's true code is shorter than S ones-codewords
+    for b in range(area_off + st[3], area_off + st[4]):
+        blob[meta + b] = 0xFF
     Wc = ec.deserialize(bytes(blob), device=0)
     out = torch.zeros((64, 4096), dtype=torch.int16, device="cuda")
     ec.decode(Wc, out)
-    st = ec.status()
-    got = out.cpu().numpy().view(np.uint16)
-    assert st == -5 or not np.array_equal(got, w)
+    assert ec.status() == -5
+    x = synth.make_x(2500, 1, 4096)
+    y = torch.zeros((1, 64), dtype=torch.float32, device="cuda")
+    ec.gemv(Wc, dev(x.view(np.int16)), y, batch=1)
+    assert ec.status() == -5
     # the context is still healthy and the clean matrix still decodes exactly
     assert np.array_equal(decode_gpu(ec, W, 64, 4096), w)
 
