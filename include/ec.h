@@ -270,8 +270,9 @@ int ec_gemv_group(const ec_matrix* const* Ws, int count, const uint16_t* x_bf16,
  * before any stream capture.  All calls share the one array: calls whose work
  * overlaps on the GPU (other streams, other threads) race and corrupt each other's
  * partial sums, so serialise them.  Corruption found in the payload is recorded in
- * the array's status word, not in the word ec_status() reads.  The pages have no
- * counterpart to this entry point. */
+ * the array's status word, which stays set until ec_status() reads and clears it
+ * (together with the regular one).  The pages have no counterpart to this entry
+ * point. */
 int ec_gemv_static(const ec_matrix* W, const uint16_t* x_bf16, float* y, int batch, cudaStream_t stream);
 
 /* Uncompressed comparator: y = W x for a dense BF16 W [n_rows, k_cols] in device

@@ -1493,8 +1493,11 @@ __device__ __noinline__ void decode_records(uint32_t recs, uint32_t staged, cons
     }
 }
 
+/* warps per CTA of the decode kernel: 24, so that each thread may hold 85 registers */
+constexpr int kDecodeWarps = 24;
+
 template <bool kHier>
-__global__ void __launch_bounds__(kMaxHW * 32, 1) huff_decode_kernel(const __grid_constant__ HuffDecodeArgs a) {
+__global__ void __launch_bounds__(kDecodeWarps * 32, 1) huff_decode_kernel(const __grid_constant__ HuffDecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
     /* shared: the current matrix's pair table | its staged sub-tables | per warp: two tile buffers */
@@ -3043,7 +3046,7 @@ extern "C" int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs
     a.code_bytes = code_bytes;
     const size_t per_warp = huff_warp_bytes(code_bytes), fixed = kPairTabBytes + 4 * (size_t)a.sub_words;
     if (fixed + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED;
-    const int warps = (int)std::min<size_t>(kMaxHW, (d->smem_optin - fixed) / per_warp);
+    const int warps = (int)std::min<size_t>(kDecodeWarps, (d->smem_optin - fixed) / per_warp);
     const size_t smem = fixed + (size_t)warps * per_warp;
     auto kern = lng ? huff_decode_kernel<true> : huff_decode_kernel<false>;
     if (set_smem(kern, smem) != EC_OK) return EC_ERR_CUDA;
@@ -3123,7 +3126,15 @@ extern "C" int ec_status(cudaStream_t stream) {
     int v = 0;
     if (cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return EC_ERR_CUDA;
     if (v && cudaMemset(d->status, 0, sizeof(int)) != cudaSuccess) return EC_ERR_CUDA;
-    return v ? EC_ERR_CORRUPT : EC_OK;
+    /* and the status word of the allocation-free GEMV (word 0 of its scratch array;
+     * symbol copies allocate nothing) */
+    int w = 0;
+    if (cudaMemcpyFromSymbol(&w, g_ec_static_scratch, sizeof(int)) != cudaSuccess) return EC_ERR_CUDA;
+    if (w) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_ec_static_scratch, &zero, sizeof(int)) != cudaSuccess) return EC_ERR_CUDA;
+    }
+    return v || w ? EC_ERR_CORRUPT : EC_OK;
 }
 
 /* Allocation-free GEMV (declared in ec.h, where its contract is described). */
@@ -3134,10 +3145,10 @@ extern "C" int ec_gemv_static(const ec_matrix* W, const uint16_t* x, float* y, i
     if (!y || !aligned16(y) || (W->hdr.k_cols > 0 && (!x || !aligned16(x)))) return EC_ERR_INVALID_ARG;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return EC_ERR_CUDA;
-    if (check_matrix(W, dev) != EC_OK) return EC_ERR_INVALID_ARG;
-    StaticDevice* d = nullptr;
-    int rc = static_device(dev, &d);
+    int rc = check_matrix(W, dev);
     if (rc != EC_OK) return rc;
+    StaticDevice* d = nullptr;
+    if ((rc = static_device(dev, &d)) != EC_OK) return rc;
     const ec_blob_header& h = W->hdr;
     const int64_t T = 32 * (int64_t)h.steps;
     const int64_t slots = (h.k_pad + T - 1) / T + 1;
@@ -3156,7 +3167,7 @@ extern "C" int ec_gemv_static(const ec_matrix* W, const uint16_t* x, float* y, i
     a.part_slots = (int)slots;
     a.sub_words = plan_sub_tables(a.m, 1);
     if (a.code_bytes < 16) a.code_bytes = 16;
-    if (cudaMemsetAsync(d->scratch, 0, sizeof(int), stream) != cudaSuccess) return EC_ERR_CUDA;
+    /* (the status word is not cleared here: a report stays until ec_status reads it) */
     GemvPlan pl;
     DeviceInfo di{};
     di.sms = d->sms;

@@ -164,5 +164,5 @@ def test_payload_corruption_is_reported(ec, word):
     Wc = ec.deserialize(bytes(blob), device=0)
     out = torch.zeros(q2.shape, dtype=torch.int16, device="cuda")
     ec.decode(Wc, out)
-    st = ec.status()
-    assert st == -5 or not np.array_equal(out.cpu().numpy().view(np.uint16), O.e8_reconstruct_bf16(q2, s, r))
+    # the rANS tile's final states no longer return to 2^16: reported
+    assert ec.status() == -5

@@ -107,5 +107,5 @@ def test_payload_corruption_is_reported(ec):
     Wc = ec.deserialize(bytes(blob), device=0)
     out = torch.zeros((32, 4096), dtype=torch.int16, device="cuda")
     ec.decode(Wc, out)
-    st = ec.status()
-    assert st == -5 or not np.array_equal(out.cpu().numpy().view(np.uint16), O.fp8_dequant_bf16(codes, r))
+    # the rANS tile's final states no longer return to 2^16: reported
+    assert ec.status() == -5

@@ -110,22 +110,25 @@ def test_mma_repeated_calls_identical(ec):
 
 
 def test_mma_payload_corruption_is_reported_not_faulted(ec):
+    """Lane 3 of tile 0 overwritten with ones (every lookup then decodes the 12-bit
+    all-ones codeword): the tensor-core kernel's end-of-tile check must report it."""
+    from test_abi import tile_layout, lane_starts
     w = synth.llama_bf16(2900, 64, 4096)
     W = ec.encode_bf16(w)
     blob = bytearray(W.serialize())
     h, devb = parse(bytes(blob))
     meta = len(blob) - len(devb)
-    rec = meta + h["records_off"]
-    area = 64 + 32 * h["steps"]  # tile 0's code area: after the lane starts and the raw bytes
-    for off in (area + 3, area + 200, area + 500):
-        blob[rec + off] ^= 0x5A
+    rec, S, _, _, area_off, _ = tile_layout(h, devb, 0)
+    st = lane_starts(devb, rec)
+    for b in range(area_off + st[3], area_off + st[4]):
+        blob[meta + b] = 0xFF
     Wc = ec.deserialize(bytes(blob), device=0)
     x = synth.make_x(2910, 16, 4096)
     y = torch.zeros((16, 64), device="cuda")
+    assert ec.gemv_path([Wc], 16) == "tensor_cores"
     ec.gemv(Wc, dev(x.view(np.int16)), y, batch=16)
-    st = ec.status()
-    y_ref, a_ref = O.gemv_bf16(w, x)
-    assert st == -5 or not np.array_equal(y.cpu().numpy(), y_ref)
+    assert ec.status() == -5
     # the context is still healthy: the clean matrix gives the right product
+    y_ref, a_ref = O.gemv_bf16(w, x)
     (y2,) = run(ec, [W], x, 16)
     check_gemv(y2, y_ref, a_ref, "clean after corrupt")

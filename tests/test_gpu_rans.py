@@ -105,8 +105,9 @@ def test_payload_corruption_is_reported(ec, tuple_):
     Wc = ec.deserialize(bytes(blob), device=0)
     out = torch.zeros((32, 4096), dtype=torch.int16, device="cuda")
     ec.decode(Wc, out)
-    st = ec.status()
-    assert st == -5 or not np.array_equal(out.cpu().numpy().view(np.uint16), O.rans_dequant_bf16(codes, scales))
+    # the flipped word changes every later state of its lane: the final states (2^16 each)
+    # and the count of words used no longer match, which the decoder reports
+    assert ec.status() == -5
 
 
 @pytest.mark.parametrize("tuple_", [1, 2])
