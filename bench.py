@@ -527,7 +527,7 @@ def batch_sweep(torch, ec, stack, stream, device):
     F, bf = torch.nn.functional, torch.bfloat16
     dec = [{n: torch.empty((s.n_rows, s.k_cols), dtype=torch.int16, device=dev) for n, s in stack.specs[l].items()}
            for l in range(n_l)]
-    mat, ref = {}, {}
+    mat, ref, gem, own = {}, {}, {}, {}
     for b in (16, 64, 256):
         xs = {}
         for l in range(n_l):
@@ -548,10 +548,32 @@ def batch_sweep(torch, ec, stack, stream, device):
                 for gname, gn in Stack.GROUPS:
                     for n in gn:
                         F.linear(xs[(l, gname)], stack.bf16[l][n].view(bf))
+        # the library's prefill route (ec_gemm: decode into the work buffer, then the
+        # tcgen05 GEMM) and that GEMM alone on the uncompressed weights
+        ys = {(l, n): torch.empty((b, s.n_rows), device=dev) for l in range(n_l) for n, s in stack.specs[l].items()}
+        wb = max(ec.gemm_work_bytes(stack.mats[l][n], b) for l in range(n_l) for n in stack.specs[l])
+        work = torch.empty(wb, dtype=torch.uint8, device=dev)
+
+        def run_gemm(b=b, xs=xs, ys=ys, work=work):
+            for l in range(n_l):
+                for gname, gn in Stack.GROUPS:
+                    for n in gn:
+                        ec.gemm(stack.mats[l][n], xs[(l, gname)].view(torch.int16), ys[(l, n)], b, work=work)
+
+        def run_own(b=b, xs=xs, ys=ys, work=work):
+            for l in range(n_l):
+                for gname, gn in Stack.GROUPS:
+                    for n in gn:
+                        ec.bf16_gemm(stack.bf16[l][n], xs[(l, gname)].view(torch.int16), ys[(l, n)], b, work=work)
         mat[str(b)] = round(t_graph(run_mat) / n_l, 1)
         ref[str(b)] = round(t_graph(run_ref) / n_l, 1)
+        gem[str(b)] = round(t_graph(run_gemm) / n_l, 1)
+        own[str(b)] = round(t_graph(run_own) / n_l, 1)
+        del work
     out["materialize_gemm_us_per_layer_set"] = mat
     out["bf16_cublas_gemm_us_per_layer_set"] = ref
+    out["ec_gemm_us_per_layer_set"] = gem
+    out["own_tcgen05_bf16_gemm_us_per_layer_set"] = own
     # the 24-bit limit (hierarchical-table kernel) on layer 0..n_l-1 at batch 1
     mats24, bufs = [], []
     for l in range(n_l):

@@ -31,10 +31,18 @@
  *  - Corruption that only the GPU can see (payload bits) never faults or hangs
  *    a kernel: loops are bounded, reads are clamped to the matrix's buffer, and
  *    a device status word records EC_ERR_CORRUPT; ec_status() returns it.
+ *
+ * Environment (read once per process; both leave results unchanged):
+ *  - EC_NO_PDL=1 launches every kernel without programmatic dependent launch
+ *    (by default a kernel's prologue overlaps the end of the previous kernel in
+ *    the stream, and it waits for that kernel before touching x, y or outputs).
+ *  - EC_MMA_MIN_BATCH=n moves the batch from which the Huffman GEMV takes the
+ *    tensor cores (default 6; above EC_MAX_BATCH: never).
  */
 #ifndef EC_H_
 #define EC_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -168,8 +176,12 @@ typedef struct {
 } ec_stats_t;
 
 /* Encode a row-major BF16 matrix [n_rows, k_cols] (host memory, bit patterns) with
- * the Huffman-exponent codec and upload it to `device`.  Every one of the 65536
- * BF16 patterns round-trips exactly.  On success *out owns a device blob; free it
+ * the Huffman-exponent codec and upload it to `device` (DFloat11, "Dynamic-Length
+ * Float", Fig. 3: Huffman codes for the exponent byte, sign and mantissa stored as
+ * they are; Eq. 2 bounds the size; length-limited codes as in its appendix).  The
+ * stream is cut into tiles of 32 lanes with stored start offsets (the "stored by the
+ * encoder" form of the per-thread positions of Algorithm 1's first phase).  Every one
+ * of the 65536 BF16 patterns round-trips exactly.  On success *out owns a device blob; free it
  * with ec_free.  device < 0 keeps the blob in host memory (no CUDA call is made;
  * such a matrix can be serialised and inspected but not decoded on a GPU). */
 int ec_encode_bf16(const uint16_t* w_host, int64_t n_rows, int64_t k_cols, const ec_huff_params* params,
@@ -207,7 +219,10 @@ int ec_encode_e8(const int8_t* q2_host, const float* row_scales_host, float scal
 int ec_encode_fp8(const uint8_t* codes_host, const float* row_scales_host, int64_t n_rows, int64_t k_cols,
                   const ec_fp8_params* params, int device, ec_matrix** out);
 
-/* Decode W to dense row-major BF16 [n_rows, k_cols] in device memory out_bf16.
+/* Decode W to dense row-major BF16 [n_rows, k_cols] in device memory out_bf16
+ * (DFloat11 Algorithm 1, second phase: table lookups, then sign | exponent |
+ * mantissa reassembled and written at each symbol's output position; EntroPack
+ * section 3.6 for the rANS tiles).
  * Huffman: the original bit patterns.  rANS: BF16 round-to-nearest-even of
  * code * scale.  FP8: of fp32(value * r_i), correction records applied.  E8: as
  * ec_decode_as with EC_DTYPE_BF16. */
@@ -230,7 +245,10 @@ int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs, int count
 int ec_decode_as(const ec_matrix* W, void* out, int dtype, cudaStream_t stream);
 
 /* y[b, i] = sum_j W[i, j] * x[b, j] for b < batch (1..EC_MAX_BATCH), with the weights
- * decoded in registers / shared memory and FP32 accumulation.  x: BF16 [batch,
+ * decoded in registers / shared memory and FP32 accumulation (MINE section 4, "Fused
+ * mvm": the decoded weight goes straight into the multiply-accumulate and never to
+ * global memory).  Deviation from the proposed boundary: batches above 16 are
+ * accepted, up to EC_MAX_BATCH.  x: BF16 [batch,
  * k_cols] device; y: FP32 [batch, n_rows] device, overwritten.
  * Huffman matrices run on the CUDA cores (one FMA per weight and batch row, in
  * passes of up to 16 rows), or, from batch 6 (EC_MMA_MIN_BATCH overrides) when
@@ -280,14 +298,50 @@ int ec_gemv_static(const ec_matrix* W, const uint16_t* x_bf16, float* y, int bat
 int ec_bf16_gemv(const uint16_t* w_bf16, int64_t n_rows, int64_t k_cols, const uint16_t* x_bf16, float* y,
                  int batch, cudaStream_t stream);
 
-/* Sizes and rates (host only). */
+/* Prefill / batched products: y[b, i] = sum_j W[i, j] * x[b, j] for any batch >= 1
+ * (MINE section 4: at batch > 1 the layer is materialised, then multiplied by a
+ * GEMM; DFloat11 "Transformer-block-level decompression").  Huffman matrices are
+ * decoded in chunks of rows (about 48 MB of BF16, so a chunk stays in the 129 MB
+ * L2 between its decode and its use) into `work`, and each chunk is multiplied on
+ * the tensor cores (tcgen05, BF16 products, FP32 accumulators in tensor memory)
+ * before the next chunk is decoded; rANS, FP8 and E8 matrices are decoded whole
+ * (k_cols % 8 == 0, else EC_ERR_UNSUPPORTED).  When K is split across CTAs the
+ * partial sums go to `work` and are added in a fixed order, so repeated calls
+ * give identical y.  x: BF16 [batch, k_cols], y: FP32 [batch, n_rows] (device,
+ * 16-byte aligned, y overwritten).  work: device memory owned by the caller,
+ * 16-byte aligned, work_bytes at least ec_gemm_work_bytes() for the full chunk
+ * size; a smaller buffer makes the chunks smaller (EC_ERR_INVALID_ARG when not even
+ * one chunk of the minimum height fits).  Asynchronous on `stream`; allocates
+ * nothing; corruption is reported by ec_status. */
+int ec_gemm(const ec_matrix* W, const uint16_t* x_bf16, float* y, int batch, void* work, size_t work_bytes,
+            cudaStream_t stream);
+
+/* Work bytes ec_gemm(W, ..., batch, ...) uses with full-size chunks on the current
+ * device (host only). */
+int ec_gemm_work_bytes(const ec_matrix* W, int batch, size_t* bytes);
+
+/* Uncompressed comparator for ec_gemm: y = W x for a dense BF16 W [n_rows, k_cols]
+ * (k_cols % 8 == 0, else EC_ERR_UNSUPPORTED) through the same tensor-core GEMM.
+ * work (may be NULL) holds partial sums when K is split: with less than
+ * splits * batch * n_rows floats the split is reduced. */
+int ec_bf16_gemm(const uint16_t* w_bf16, int64_t n_rows, int64_t k_cols, const uint16_t* x_bf16, float* y,
+                 int batch, void* work, size_t work_bytes, cudaStream_t stream);
+
+/* Sizes and rates (host only): the stored bytes by section, bits per weight, and
+ * the exponent entropy H of DFloat11 Eq. 2 (or of the 4-bit code for rANS), so
+ * that the coded rate can be checked against the entropy bound. */
 int ec_stats(const ec_matrix* W, ec_stats_t* out);
 
 /* Code length of each exponent value (Huffman matrices; 0 = absent). */
 int ec_code_lengths(const ec_matrix* W, uint8_t lengths[256]);
 
-/* Synchronise `stream`, then return and clear the device status word of the
- * current device: EC_OK, or EC_ERR_CORRUPT if a kernel met inconsistent data. */
+/* Synchronise `stream`, then return and clear the device status words of the
+ * current device (the regular one and that of ec_gemv_static): EC_OK, or
+ * EC_ERR_CORRUPT if a kernel met inconsistent data (a lane whose codewords do not
+ * end at the next lane's stored start, a tile record out of range, an rANS tile
+ * whose final states differ from the initial value: the consistency checks that the
+ * per-tile offsets of DFloat11 Algorithm 1 and the terminal states of EntroPack
+ * section 3.6 make possible). */
 int ec_status(cudaStream_t stream);
 
 /* Serialise W into host memory: a fixed metadata block followed by the device blob

@@ -38,7 +38,8 @@ EC_KIND_RANS_FP8 = 4
 
 EXPORTS = ["ec_encode_bf16", "ec_encode_rans", "ec_decode", "ec_decode_batch", "ec_gemv", "ec_gemv_group",
            "ec_bf16_gemv", "ec_stats", "ec_code_lengths", "ec_serialize", "ec_deserialize", "ec_status", "ec_free",
-           "ec_strerror", "ec_gemv_static", "ec_gemv_path", "ec_encode_e8", "ec_decode_as", "ec_encode_fp8"]
+           "ec_strerror", "ec_gemv_static", "ec_gemv_path", "ec_encode_e8", "ec_decode_as", "ec_encode_fp8",
+           "ec_gemm", "ec_gemm_work_bytes", "ec_bf16_gemm"]
 
 
 class HuffParams(ctypes.Structure):
@@ -85,6 +86,9 @@ _sig = {
     "ec_gemv": ([_vp, _vp, _vp, _i32, _vp], _i32),
     "ec_gemv_group": ([_vp, _i32, _vp, _vp, _i32, _vp], _i32),
     "ec_bf16_gemv": ([_vp, _i64, _i64, _vp, _vp, _i32, _vp], _i32),
+    "ec_gemm": ([_vp, _vp, _vp, _i32, _vp, ctypes.c_size_t, _vp], _i32),
+    "ec_gemm_work_bytes": ([_vp, _i32, ctypes.POINTER(ctypes.c_size_t)], _i32),
+    "ec_bf16_gemm": ([_vp, _i64, _i64, _vp, _vp, _i32, _vp, ctypes.c_size_t, _vp], _i32),
     "ec_gemv_static": ([_vp, _vp, _vp, _i32, _vp], _i32),
     "ec_gemv_path": ([_vp, _i32, _i32], _i32),
     "ec_stats": ([_vp, ctypes.POINTER(Stats)], _i32),
@@ -297,6 +301,32 @@ def bf16_gemv(w, x, y, batch: int = 1, stream=None) -> None:
     n, k = int(w.shape[0]), int(w.shape[1])
     _check(lib.ec_bf16_gemv(_dev_ptr(w), n, k, _dev_ptr(x), _dev_ptr(y), batch, _stream_ptr(stream)),
            "ec_bf16_gemv")
+
+
+def gemm_work_bytes(W: Matrix, batch: int) -> int:
+    """ec_gemm_work_bytes: the work buffer ec_gemm uses with full-size chunks."""
+    n = ctypes.c_size_t(0)
+    _check(lib.ec_gemm_work_bytes(W.handle, batch, ctypes.byref(n)), "ec_gemm_work_bytes")
+    return int(n.value)
+
+
+def gemm(W: Matrix, x, y, batch: int, work=None, stream=None) -> None:
+    """ec_gemm: y = x W^T for any batch (chunked decode + tensor-core GEMM).  work: a
+    device tensor (its bytes are the buffer); None allocates one of gemm_work_bytes."""
+    if work is None:
+        import torch
+        work = torch.empty(gemm_work_bytes(W, batch), dtype=torch.uint8, device=x.device)
+    nbytes = work.numel() * work.element_size()
+    _check(lib.ec_gemm(W.handle, _dev_ptr(x), _dev_ptr(y), batch, _dev_ptr(work), nbytes, _stream_ptr(stream)),
+           "ec_gemm")
+
+
+def bf16_gemm(w, x, y, batch: int, work=None, stream=None) -> None:
+    """ec_bf16_gemm: the same tensor-core GEMM on a dense BF16 matrix (work: partial sums, optional)."""
+    n, k = int(w.shape[0]), int(w.shape[1])
+    nbytes = 0 if work is None else work.numel() * work.element_size()
+    _check(lib.ec_bf16_gemm(_dev_ptr(w), n, k, _dev_ptr(x), _dev_ptr(y), batch, _dev_ptr(work), nbytes,
+                            _stream_ptr(stream)), "ec_bf16_gemm")
 
 
 def status(stream=None) -> int:

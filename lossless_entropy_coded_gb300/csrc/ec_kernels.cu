@@ -35,9 +35,11 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdint>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <numeric>
 #include <vector>
 
 #include "ec_internal.h"
@@ -59,7 +61,8 @@ struct HuffMat {
     int32_t fill;               /* the exponent coded in place of a recorded one */
     int32_t sub_smem;           /* their first word in the launch's staged sub-tables, or -1 (global) */
     float* y;                   /* GEMV output [batch, n_rows] */
-    uint16_t* out;              /* decode output [n_rows, k_cols] */
+    uint16_t* out;              /* decode output: row r at out + (r - out_row0) * out_ld */
+    int64_t out_ld, out_row0;   /*   (k_cols and 0, except for the chunks of the prefill GEMM) */
     int64_t n_rows, k_cols, k_pad;
     int64_t n_tiles, tile_begin;
     int64_t records_bytes;
@@ -1474,6 +1477,221 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
     }
 }
 
+/* ============================================== tensor-core GEMM (prefill) */
+/*
+ * Batch > 1 materialises the layer and runs a GEMM (MINE, "Prefill"; DFloat11,
+ * "Transformer-block-level decompression"): here the decoded rows arrive in an
+ * L2-sized chunk of BF16 [rows, ld] and this kernel forms y[b][row] = sum_k
+ * W[row][k] x[b][k] over it.
+ *
+ * Tile: 128 weight rows (MMA M, the TMEM lanes) x bn batch rows (MMA N, TMEM
+ * columns, a multiple of 16 up to 256), K in blocks of 64 columns (one 128-byte
+ * swizzle atom).  Per block a stage of shared memory holds the A box (128 rows x
+ * 128 B) and the B box (bn rows x 128 B), both 128-byte swizzled by TMA; four
+ * kind::f16 MMAs of K = 16 consume it.  Warp roles: warp 0 issues the TMA copies
+ * (one lane), warp 1 the MMAs (one elected lane), warps 2..5 read the finished
+ * accumulators back (tcgen05.ld 32x32b, lane quarter = warp % 4) and store them:
+ * for a batch row b the 32 lanes of a warp hold 32 consecutive weight rows, so
+ * each store is 128 contiguous bytes.  Two accumulators (2 bn TMEM columns)
+ * alternate between work items so that the read-back of one overlaps the MMAs of
+ * the next.  A work item is (row tile, batch tile, K split); with more than one K
+ * split each writes its own partial sums, which gemm_reduce_kernel adds in split
+ * order, so results do not depend on timing.
+ *
+ * Barriers: full[s] (TMA bytes landed), empty[s] (the MMAs that read stage s are
+ * done: tcgen05.commit), accf[a] (accumulator a complete), acce[a] (its read-back
+ * done: one arrival per epilogue warp).  Every wait is bounded; a wait that runs
+ * out flags the status word and the thread stops waiting.
+ */
+constexpr int kGemmBM = 128;
+constexpr int kGemmBK = 64;
+constexpr int kGemmEpiWarps = 4;
+constexpr int kGemmThreads = 32 * (2 + kGemmEpiWarps);
+constexpr uint32_t kGemmABytes = (uint32_t)kGemmBM * 128u; /* 16 KB */
+
+struct GemmArgs {
+    CUtensorMap amap; /* W rows [rows, K] BF16, boxes of 64 columns x 128 rows, 128-byte swizzle */
+    CUtensorMap bmap; /* x [batch, K] BF16, boxes of 64 columns x bn rows, 128-byte swizzle */
+    float* y;         /* ksplit == 1: y[b * ldy + row_off + row] */
+    float* part;      /* ksplit > 1: part[(split * batch + b) * rows + row] */
+    int64_t ldy, row_off;
+    int rows, batch, kblocks, bn;
+    int m_tiles, n_tiles, ksplit, kb_per_split;
+    int stages;
+    uint32_t idesc;   /* kind::f16, M = 128, N = bn */
+    uint32_t tmem_cols;
+    int* status;
+};
+
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld16(uint32_t (&v)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                   "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                   "+r"(v[15])::"memory");
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_kernel(const __grid_constant__ GemmArgs a) {
+    extern __shared__ __align__(1024) uint8_t gemm_smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t base = smem_u32(gemm_smem);
+    if (base & 1023u) { /* the swizzled operands need 1 KB alignment (never seen otherwise) */
+        if (threadIdx.x == 0) flag_corrupt(a.status);
+        return;
+    }
+    const uint32_t stage_bytes = kGemmABytes + (uint32_t)a.bn * 128u;
+    const uint32_t bars = base + (uint32_t)a.stages * stage_bytes;
+    const uint32_t full = bars, empty = bars + 8u * (uint32_t)a.stages, accf = empty + 8u * (uint32_t)a.stages,
+                   acce = accf + 16u, tslot = acce + 16u;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(full + 8 * s);
+            mbar_init(empty + 8 * s);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(accf + 8 * i);
+            mbar_init_n(acce + 8 * i, kGemmEpiWarps);
+        }
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tslot),
+                     "r"(a.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = lds32(tslot);
+    grid_dep_launch();
+    grid_dep_wait(); /* the weight rows and x come from the preceding kernels in the stream */
+
+    bool live = true;
+    auto wait = [&](uint32_t bar, uint32_t parity) {
+        if (live && !mbar_wait(bar, parity)) {
+            live = false;
+            flag_corrupt(a.status);
+        }
+        return live;
+    };
+    const int items = a.m_tiles * a.n_tiles * a.ksplit;
+    auto item_of = [&](int it, int& mt, int& nt, int& kb0, int& kb1) {
+        const int ks = it % a.ksplit, mn = it / a.ksplit;
+        nt = mn % a.n_tiles;
+        mt = mn / a.n_tiles;
+        kb0 = ks * a.kb_per_split;
+        kb1 = min(a.kblocks, kb0 + a.kb_per_split);
+    };
+
+    if (warp == 0) {
+        /* ---- TMA producer ---- */
+        if (lane == 0) {
+            uint32_t s = 0, ph = 0;
+            for (int it = blockIdx.x; it < items; it += gridDim.x) {
+                int mt, nt, kb0, kb1;
+                item_of(it, mt, nt, kb0, kb1);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    wait(empty + 8 * s, ph ^ 1u);
+                    const uint32_t st = base + s * stage_bytes;
+                    mbar_arrive_tx(full + 8 * s, stage_bytes);
+                    tma_load_2d(st, &a.amap, kb * kGemmBK, mt * kGemmBM, full + 8 * s);
+                    tma_load_2d(st + kGemmABytes, &a.bmap, kb * kGemmBK, nt * a.bn, full + 8 * s);
+                    if (++s == (uint32_t)a.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        /* ---- MMA issuer (the whole warp walks the loop; one elected lane issues) ---- */
+        uint32_t s = 0, ph = 0, n = 0;
+        for (int it = blockIdx.x; it < items; it += gridDim.x, ++n) {
+            int mt, nt, kb0, kb1;
+            item_of(it, mt, nt, kb0, kb1);
+            const uint32_t ab = n & 1u, aph = (n >> 1) & 1u;
+            wait(acce + 8 * ab, aph ^ 1u); /* the read-back of this accumulator's previous item is done */
+            tc_fence_after();
+            const uint32_t d = tmem + ab * (uint32_t)a.bn;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                wait(full + 8 * s, ph);
+                tc_fence_after();
+                const uint32_t st = base + s * stage_bytes;
+                const uint64_t ad = sw128_desc(st), bd = sw128_desc(st + kGemmABytes);
+#pragma unroll
+                for (int k = 0; k < kGemmBK / 16; ++k)
+                    tc_mma_bf16(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), a.idesc, kb > kb0 || k > 0);
+                tc_commit(empty + 8 * s);
+                if (++s == (uint32_t)a.stages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            tc_commit(accf + 8 * ab);
+            __syncwarp();
+        }
+    } else {
+        /* ---- epilogue: TMEM lanes 32 q .. 32 q + 31 = weight rows of the tile ---- */
+        const int q = warp & 3;
+        uint32_t n = 0;
+        for (int it = blockIdx.x; it < items; it += gridDim.x, ++n) {
+            int mt, nt, kb0, kb1;
+            item_of(it, mt, nt, kb0, kb1);
+            const uint32_t ab = n & 1u, aph = (n >> 1) & 1u;
+            wait(accf + 8 * ab, aph);
+            tc_fence_after();
+            const int row = mt * kGemmBM + 32 * q + lane;
+            const int ks = it % a.ksplit;
+            const bool row_ok = row < a.rows;
+            for (int c0 = 0; c0 < a.bn; c0 += 16) {
+                uint32_t v[16];
+                tc_ld16(tmem + ((uint32_t)(32 * q) << 16) + ab * (uint32_t)a.bn + (uint32_t)c0, v);
+                tc_wait_ld16(v);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int b = nt * a.bn + c0 + j;
+                    if (row_ok && b < a.batch) {
+                        if (a.ksplit == 1) a.y[(int64_t)b * a.ldy + a.row_off + row] = __uint_as_float(v[j]);
+                        else a.part[((int64_t)ks * a.batch + b) * a.rows + row] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce + 8 * ab);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
+    }
+}
+
+/* y[b * ldy + row_off + r] = sum over splits s (in order) of part[(s * batch + b) * rows + r]. */
+__global__ void gemm_reduce_kernel(const float* __restrict__ part, int ksplit, int batch, int rows, float* y,
+                                   int64_t ldy, int64_t row_off) {
+    grid_dep_launch();
+    grid_dep_wait();
+    const int64_t n = (int64_t)batch * rows;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = i / rows, r = i - b * rows;
+        float s = 0.f;
+        for (int k = 0; k < ksplit; ++k) s += part[((int64_t)k * batch + b) * rows + r];
+        y[b * ldy + row_off + r] = s;
+    }
+}
+
 /* ====================================================== Huffman decode kernel */
 /* Each CTA owns a contiguous range of the launch's tiles; it walks the range one
  * matrix segment at a time, with that matrix's pair table in shared memory.
@@ -1482,19 +1700,19 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
 
 
 /* Window records of a decoded tile that starts at flattened position `start` of
- * its matrix: the true weight over the coded one (kept out of line: rare, and the
- * decode loop needs every register). */
-__device__ __noinline__ void decode_records(uint32_t recs, uint32_t staged, const uint32_t* far, uint32_t nrec,
-                                            uint16_t* out, int64_t K, int64_t kp, int64_t start, int lane) {
+ * its matrix: the true weight over the coded one (inline: most tiles have a few,
+ * and a call would spill the walker's registers around it). */
+__device__ __forceinline__ void decode_records(uint32_t recs, uint32_t staged, const uint32_t* far, uint32_t nrec,
+                                            const HuffMat& M, int64_t start, int lane) {
     for (uint32_t j = (uint32_t)lane; j < nrec; j += 32) {
         const uint32_t e = j < staged ? lds32(recs + 4 * j) : __ldg(far + j), q = e & 0xFFFu;
-        const int64_t f = start + q, rr = f / kp, cc = f - rr * kp;
-        if (cc < K) out[rr * K + cc] = (uint16_t)rec_weight(e, e >> 20);
+        const int64_t f = start + q, rr = f / M.k_pad, cc = f - rr * M.k_pad;
+        if (cc < M.k_cols) M.out[(rr - M.out_row0) * M.out_ld + cc] = (uint16_t)rec_weight(e, e >> 20);
     }
 }
 
-/* warps per CTA of the decode kernel: 24, so that each thread may hold 85 registers */
-constexpr int kDecodeWarps = 24;
+/* warps per CTA of the decode kernel (64 registers a thread) */
+constexpr int kDecodeWarps = 32;
 
 template <bool kHier>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 1) huff_decode_kernel(const __grid_constant__ HuffDecodeArgs a) {
@@ -1541,9 +1759,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) huff_decode_kernel(const
             Ms.sub_smem = -1;
         }
         __syncthreads();
-        const int64_t kp = M.k_pad, K = M.k_cols;
-        const bool vec = (K % 8) == 0;
-        int64_t row = 0, col0 = 0;
+        const int64_t kp = M.k_pad, K = M.k_cols, ld = M.out_ld;
+        /* 16-byte stores when rows are 16-byte aligned (a store past column K stays
+         * inside the row: ld >= K rounded up to 8) */
+        const bool vec = (ld % 8) == 0;
+        /* the current row's output (lane-private: this lane's first column of the row's
+         * segment) and the segment's first column; rows and columns stay below 2^31 */
+        uint16_t* dst = nullptr;
+        uint32_t col0 = 0;
+        const uint32_t kp32 = (uint32_t)kp, K32 = (uint32_t)K;
         if (g0 < mend)
             huff_walk<kHier>(
                 a, g0, nwarp, mend, first, bufs, buf_bytes, ph, lane,
@@ -1555,27 +1779,25 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) huff_decode_kernel(const
                 },
                 [&](const TileRef& r) {
                     const int64_t T = 32 * (int64_t)M.steps;
-                    row = tile_row(r.t, T, kp, EC_HUFF_ROW_ALIGN);
-                    col0 = r.t * T - row * kp;
+                    const int64_t row = tile_row(r.t, T, kp, EC_HUFF_ROW_ALIGN);
+                    col0 = (uint32_t)(r.t * T - row * kp);
+                    dst = M.out + (row - M.out_row0) * ld + 8 * lane;
                 },
                 [&](uint32_t, const TileRef&) {
-                    if (col0 >= kp) {
-                        col0 -= kp;
-                        ++row;
+                    if (col0 >= kp32) {
+                        col0 -= kp32;
+                        dst += ld;
                     }
                 },
                 [&](const uint32_t (&w)[4], int) {
                     /* the lane's 8 outputs are columns col0 + 8 lane .. + 7: one 16-byte store */
-                    const uint4 o = make_uint4(w[0], w[1], w[2], w[3]);
-                    const int64_t col = col0 + 8 * lane;
-                    uint16_t* dst = M.out + row * K + col;
+                    const uint32_t col = col0 + 8u * (uint32_t)lane;
                     if (vec) {
-                        if (col < K) *(uint4*)dst = o;
+                        if (col < K32) *(uint4*)(dst + col0) = make_uint4(w[0], w[1], w[2], w[3]);
                     } else {
-                        const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            if (col + j < K) dst[j] = (uint16_t)(ow[j >> 1] >> (16 * (j & 1)));
+                            if (col + j < K32) dst[col0 + j] = (uint16_t)(w[j >> 1] >> (16 * (j & 1)));
                     }
                     col0 += 256;
                 },
@@ -1585,8 +1807,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) huff_decode_kernel(const
                     const TileRecs tr = tile_recs(cb, r.area, a.code_bytes);
                     if (tr.n > 0) {
                         __syncwarp();
-                        decode_records(cb + 64 + tr.code, tr.staged, far_records(r, tr.code), (uint32_t)tr.n, M.out, K,
-                                       kp, 32 * (int64_t)M.steps * r.t, lane);
+                        decode_records(cb + 64 + tr.code, tr.staged, far_records(r, tr.code), (uint32_t)tr.n, M,
+                                       32 * (int64_t)M.steps * r.t, lane);
                     }
                 });
         cur = mend;
@@ -2350,6 +2572,7 @@ HuffMat huff_desc(const ec_matrix* W) {
     m.n_rows = h.n_rows;
     m.k_cols = h.k_cols;
     m.k_pad = h.k_pad;
+    m.out_ld = h.k_cols;
     m.n_tiles = h.n_tiles;
     m.records_bytes = h.blob_bytes - h.records_off;
     m.steps = h.steps;
@@ -2833,28 +3056,21 @@ int fp8_run(const ec_matrix* W, const uint16_t* x, float* y, uint16_t* out, int 
  * them, else one buffer and as many warps as fit (an issue-bound decode keeps the SM
  * busy with the other warps while one waits for its next tile).  The warp count is
  * then lowered to the fewest that keep the same number of tile rounds, so that the
- * last round is full.  EC_E8_WARPS / EC_E8_BUFFERS override both. */
+ * last round is full. */
 struct E8Plan {
     int warps, nbuf;
 };
 E8Plan e8_plan(size_t tables, size_t buf, int64_t n_tiles, const DeviceInfo* d) {
-    static const int env_w = [] { const char* e = std::getenv("EC_E8_WARPS"); return e && e[0] ? std::atoi(e) : 0; }();
-    static const int env_b = [] { const char* e = std::getenv("EC_E8_BUFFERS"); return e && e[0] ? std::atoi(e) : 0; }();
     const size_t room = d->smem_optin - tables;
-    int nbuf = env_b == 1 || env_b == 2 ? env_b : (room / (2 * buf) >= (size_t)kMaxHW ? 2 : 1);
+    int nbuf = room / (2 * buf) >= (size_t)kMaxHW ? 2 : 1;
     int wmax = (int)std::min<size_t>(kMaxHW, room / (nbuf * buf));
     if (wmax < 1) {
         nbuf = 1;
         wmax = (int)std::min<size_t>(kMaxHW, room / buf);
     }
-    int warps = wmax;
-    if (env_w > 0) {
-        warps = std::min(env_w, wmax);
-    } else {
-        const int64_t per_sm = (n_tiles + d->sms - 1) / d->sms;
-        const int64_t rounds = std::max<int64_t>(1, (per_sm + wmax - 1) / wmax);
-        warps = (int)std::max<int64_t>(1, std::min<int64_t>(wmax, (per_sm + rounds - 1) / rounds));
-    }
+    const int64_t per_sm = (n_tiles + d->sms - 1) / d->sms;
+    const int64_t rounds = std::max<int64_t>(1, (per_sm + wmax - 1) / wmax);
+    const int warps = (int)std::max<int64_t>(1, std::min<int64_t>(wmax, (per_sm + rounds - 1) / rounds));
     return {warps, nbuf};
 }
 
@@ -2952,6 +3168,183 @@ int static_device(int dev, StaticDevice** out) {
     return EC_OK;
 }
 
+
+/* ------------------------------------------------------------ prefill GEMM */
+/* The Huffman decode kernel over a.total_tiles tiles (a.m, a.count, a.sub_words set). */
+int launch_huff_decode(HuffDecodeArgs& a, int code_bytes, bool lng, cudaStream_t stream, DeviceInfo* d) {
+    code_bytes = (code_bytes + 15) & ~15;
+    a.status = d->status;
+    a.code_bytes = code_bytes;
+    const size_t per_warp = huff_warp_bytes(code_bytes), fixed = kPairTabBytes + 4 * (size_t)a.sub_words;
+    if (fixed + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED;
+    const int warps = (int)std::min<size_t>(kDecodeWarps, (d->smem_optin - fixed) / per_warp);
+    const size_t smem = fixed + (size_t)warps * per_warp;
+    auto kern = lng ? huff_decode_kernel<true> : huff_decode_kernel<false>;
+    if (set_smem(kern, smem) != EC_OK) return EC_ERR_CUDA;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(d->sms, (a.total_tiles + warps - 1) / warps));
+    return launch_ex(kern, grid, warps * 32, smem, stream, a);
+}
+
+/* Rows [rows, cols] BF16 with row stride ld elements as TMA boxes of 64 columns x
+ * box_rows rows with the 128-byte swizzle of the MMA operands; columns past `cols`
+ * and rows past `rows` read as zero.  ld % 8 == 0 and p 16-byte aligned. */
+int encode_rows_map(CUtensorMap* map, const uint16_t* p, int64_t cols, int64_t rows, int64_t ld, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return EC_ERR_CUDA;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows}, estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)p, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? EC_OK : EC_ERR_CUDA;
+}
+
+struct GemmPlan {
+    int bn, n_tiles, m_tiles, kblocks, ksplit, kbps, stages, grid;
+    uint32_t tmem_cols;
+    size_t smem, part_bytes;
+};
+
+/* Tiles of 128 rows x bn batch rows (batch split evenly into tiles of at most 256);
+ * K split so that about one work item per SM exists (at least 4 blocks of 64
+ * columns per split), within part_cap bytes of partial sums. */
+GemmPlan plan_gemm(int64_t rows, int64_t K, int batch, int sms, size_t smem_optin, size_t part_cap) {
+    GemmPlan p{};
+    p.n_tiles = (batch + 255) / 256;
+    const int per = (batch + p.n_tiles - 1) / p.n_tiles;
+    p.bn = (per + 15) & ~15;
+    p.m_tiles = (int)((rows + kGemmBM - 1) / kGemmBM);
+    p.kblocks = (int)std::max<int64_t>(1, (K + kGemmBK - 1) / kGemmBK);
+    const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
+    int ks = (int)std::max<int64_t>(1, std::min<int64_t>(sms / std::max<int64_t>(1, tiles), p.kblocks / 4));
+    for (; ks > 1; --ks) {
+        const int kbps = (p.kblocks + ks - 1) / ks, n = (p.kblocks + kbps - 1) / kbps;
+        if ((size_t)n * (size_t)batch * (size_t)rows * 4 <= part_cap) break;
+    }
+    p.kbps = (p.kblocks + ks - 1) / ks;
+    p.ksplit = (p.kblocks + p.kbps - 1) / p.kbps;
+    p.part_bytes = p.ksplit > 1 ? (size_t)p.ksplit * (size_t)batch * (size_t)rows * 4 : 0;
+    const size_t stage = kGemmABytes + (size_t)p.bn * 128, extra = 64;
+    p.stages = (int)std::min<size_t>(8, (smem_optin - extra) / (stage + 16));
+    p.smem = (size_t)p.stages * (stage + 16) + extra;
+    p.tmem_cols = 32;
+    while (p.tmem_cols < 2u * (uint32_t)p.bn) p.tmem_cols <<= 1;
+    p.grid = (int)std::min<int64_t>(sms, tiles * p.ksplit);
+    return p;
+}
+
+/* y[b * ldy + row_off + r] = sum_k A[r][k] x[b][k] for the rows r < rows of A (ld
+ * elements apart) and batch rows b of x (xld apart): the tensor-core kernel, then
+ * the split reduction when K is split (partial sums in part, part_cap bytes). */
+int gemm_run(const uint16_t* A, int64_t rows, int64_t K, int64_t lda, const uint16_t* x, int64_t xld, int batch,
+             float* y, int64_t ldy, int64_t row_off, float* part, size_t part_cap, cudaStream_t s, DeviceInfo* d) {
+    if (rows == 0 || batch == 0) return EC_OK;
+    const GemmPlan p = plan_gemm(rows, K, batch, d->sms, d->smem_optin, part ? part_cap : 0);
+    if (p.stages < 2) return EC_ERR_UNSUPPORTED;
+    if (rows > INT32_MAX || (int64_t)p.m_tiles * p.n_tiles * p.ksplit > INT32_MAX) return EC_ERR_UNSUPPORTED;
+    GemmArgs a{};
+    int rc = encode_rows_map(&a.amap, A, K, rows, lda, kGemmBM);
+    if (rc == EC_OK) rc = encode_rows_map(&a.bmap, x, K, batch, xld, p.bn);
+    if (rc != EC_OK) return rc;
+    a.y = y;
+    a.part = part;
+    a.ldy = ldy;
+    a.row_off = row_off;
+    a.rows = (int)rows;
+    a.batch = batch;
+    a.kblocks = p.kblocks;
+    a.bn = p.bn;
+    a.m_tiles = p.m_tiles;
+    a.n_tiles = p.n_tiles;
+    a.ksplit = p.ksplit;
+    a.kb_per_split = p.kbps;
+    a.stages = p.stages;
+    /* kind::f16: FP32 accumulators, BF16 A and B, both K-major, N >> 3, M >> 4 */
+    a.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(p.bn >> 3) << 17) | ((uint32_t)(kGemmBM >> 4) << 24);
+    a.tmem_cols = p.tmem_cols;
+    a.status = d->status;
+    if (set_smem(gemm_bf16_kernel, p.smem) != EC_OK) return EC_ERR_CUDA;
+    if ((rc = launch_ex(gemm_bf16_kernel, p.grid, kGemmThreads, p.smem, s, a)) != EC_OK) return rc;
+    if (p.ksplit > 1) {
+        const int64_t n = (int64_t)batch * rows;
+        const int grid = (int)std::min<int64_t>((n + 255) / 256, 8 * (int64_t)d->sms);
+        rc = launch_ex(gemm_reduce_kernel, grid, 256, 0, s, (const float*)part, p.ksplit, batch, (int)rows, y, ldy,
+                       row_off);
+    }
+    return rc;
+}
+
+/* How the prefill GEMM of W at `batch` rows uses its work buffer: chunks of
+ * chunk_rows decoded rows (row stride ld) at offset 0, x with row stride ld at
+ * x_off when K % 8 != 0 (TMA rows must be 16-byte aligned), partial sums at
+ * part_off (part_cap bytes). */
+struct PrefillPlan {
+    int64_t ld, chunk_rows;
+    size_t x_off, part_off, part_cap, need;
+};
+
+constexpr size_t kPrefillChunkBytes = size_t(128) << 20; /* decoded rows per chunk (about the L2 size) */
+
+size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
+
+/* Work bytes for chunks of cr rows (0: the partial sums alone would not fit). */
+size_t prefill_need(const ec_matrix* W, int batch, int64_t cr, int64_t ld, const DeviceInfo& d, size_t* x_off,
+                    size_t* part_off, size_t* part_cap) {
+    const ec_blob_header& h = W->hdr;
+    const size_t chunk = round256((size_t)cr * (size_t)ld * 2);
+    const size_t xb = h.k_cols % 8 ? round256((size_t)batch * (size_t)ld * 2) : 0;
+    /* the partial sums of the largest plan among the full and the last chunk */
+    const int64_t last = h.n_rows % cr ? h.n_rows % cr : cr;
+    size_t part = 0;
+    for (int64_t r : {cr, last}) part = std::max(part, plan_gemm(r, h.k_cols, batch, d.sms, d.smem_optin, SIZE_MAX).part_bytes);
+    *x_off = chunk;
+    *part_off = chunk + xb;
+    *part_cap = part;
+    return chunk + xb + part;
+}
+
+/* Warps per CTA that the Huffman decode kernel launches with for W. */
+int huff_decode_warps(const ec_matrix* W, const DeviceInfo& d) {
+    const int code_bytes = (std::max(16, staged_code_bytes(W)) + 15) & ~15;
+    const bool sub = huff_hier(W) && W->hdr.huff_sub_tables > 0 && W->hdr.huff_sub_tables <= kSubSmemTables;
+    const size_t per_warp = huff_warp_bytes(code_bytes), fixed = kPairTabBytes + (sub ? 1024 * (size_t)W->hdr.huff_sub_tables : 0);
+    if (fixed + per_warp > d.smem_optin) return 1;
+    return (int)std::max<size_t>(1, std::min<size_t>(kDecodeWarps, (d.smem_optin - fixed) / per_warp));
+}
+
+/* Rows per chunk: a multiple of `step` (chunk starts fall on tile starts), the
+ * most that fit in work_bytes (0: the default chunk size).  By default a chunk holds the tiles of whole rounds of the decode
+ * launch (one tile per warp of every CTA), as many rounds as fit in about
+ * kPrefillChunkBytes (at least one): a chunk of 1.3 rounds would take as long to
+ * decode as one of 2. */
+int plan_prefill(const ec_matrix* W, int batch, size_t work_bytes, const DeviceInfo& d, PrefillPlan* pp) {
+    const ec_blob_header& h = W->hdr;
+    pp->ld = (h.k_cols + 7) & ~int64_t(7);
+    int64_t step = h.n_rows, cr = h.n_rows;
+    if (W->kind == EC_KIND_HUFFMAN_BF16 && h.k_pad > 0) {
+        const int64_t T = 32 * (int64_t)h.steps;
+        step = T / std::gcd(T, h.k_pad);
+        const int64_t slots = (int64_t)d.sms * huff_decode_warps(W, d);
+        const int64_t round_bytes = slots * T * 2;
+        const int64_t rounds = std::max<int64_t>(1, (int64_t)kPrefillChunkBytes / std::max<int64_t>(1, round_bytes));
+        cr = rounds * slots * T / h.k_pad;
+    }
+    step = std::max<int64_t>(1, std::min(step, h.n_rows));
+    cr = std::max(step, cr / step * step);
+    cr = std::min(cr, h.n_rows);
+    for (;;) {
+        const size_t need = prefill_need(W, batch, cr, pp->ld, d, &pp->x_off, &pp->part_off, &pp->part_cap);
+        if (work_bytes == 0 || need <= work_bytes) {
+            pp->chunk_rows = cr;
+            pp->need = need;
+            return EC_OK;
+        }
+        if (cr <= step) return EC_ERR_INVALID_ARG; /* the work buffer is too small */
+        cr = std::max(step, (cr - 1) / step * step);
+    }
+}
+
 }  // namespace
 
 /* ================================================================ C ABI */
@@ -3040,18 +3433,112 @@ extern "C" int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs
         a.m[a.count++] = m;
     }
     if (a.count == 0 || total == 0) return EC_OK;
-    code_bytes = (code_bytes + 15) & ~15;
     a.total_tiles = total;
-    a.status = d->status;
-    a.code_bytes = code_bytes;
-    const size_t per_warp = huff_warp_bytes(code_bytes), fixed = kPairTabBytes + 4 * (size_t)a.sub_words;
-    if (fixed + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED;
-    const int warps = (int)std::min<size_t>(kDecodeWarps, (d->smem_optin - fixed) / per_warp);
-    const size_t smem = fixed + (size_t)warps * per_warp;
-    auto kern = lng ? huff_decode_kernel<true> : huff_decode_kernel<false>;
-    if (set_smem(kern, smem) != EC_OK) return EC_ERR_CUDA;
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(d->sms, (total + warps - 1) / warps));
-    return launch_ex(kern, grid, warps * 32, smem, stream, a);
+    return launch_huff_decode(a, code_bytes, lng, stream, d);
+}
+
+extern "C" int ec_gemm_work_bytes(const ec_matrix* W, int batch, size_t* bytes) {
+    if (!W || !bytes || batch < 1) return EC_ERR_INVALID_ARG;
+    int dev = 0;
+    if (current_device(&dev) != EC_OK) return EC_ERR_CUDA;
+    DeviceInfo* d = nullptr;
+    int rc = device_info(dev, &d);
+    if (rc != EC_OK) return rc;
+    PrefillPlan pp;
+    if ((rc = plan_prefill(W, batch, 0, *d, &pp)) != EC_OK) return rc;
+    *bytes = pp.need;
+    return EC_OK;
+}
+
+extern "C" int ec_gemm(const ec_matrix* W, const uint16_t* x, float* y, int batch, void* work, size_t work_bytes,
+                       cudaStream_t stream) {
+    if (!W || !W->d_blob || batch < 1) return EC_ERR_INVALID_ARG;
+    int dev = 0;
+    if (current_device(&dev) != EC_OK) return EC_ERR_CUDA;
+    DeviceInfo* d = nullptr;
+    int rc = device_info(dev, &d);
+    if (rc != EC_OK) return rc;
+    if ((rc = check_matrix(W, dev)) != EC_OK) return rc;
+    const ec_blob_header& h = W->hdr;
+    const int64_t K = h.k_cols;
+    if (!y || !aligned16(y) || (K > 0 && (!x || !aligned16(x)))) return EC_ERR_INVALID_ARG;
+    if (h.n_rows == 0) return EC_OK;
+    if (K == 0)
+        return cudaMemsetAsync(y, 0, sizeof(float) * (size_t)batch * (size_t)h.n_rows, stream) == cudaSuccess
+                   ? EC_OK
+                   : EC_ERR_CUDA;
+    const bool huff = W->kind == EC_KIND_HUFFMAN_BF16;
+    if (!huff && K % 8) return EC_ERR_UNSUPPORTED; /* decoded whole, rows K apart: TMA needs 16-byte rows */
+    PrefillPlan pp;
+    if ((rc = plan_prefill(W, batch, work_bytes, *d, &pp)) != EC_OK) return rc;
+    if (!work || !aligned16(work) || work_bytes < pp.need) return EC_ERR_INVALID_ARG;
+    uint8_t* wb = (uint8_t*)work;
+    uint16_t* chunk = (uint16_t*)wb;
+    float* part = pp.part_cap ? (float*)(wb + pp.part_off) : nullptr;
+    const uint16_t* xs = x;
+    int64_t xld = K;
+    if (K % 8) { /* x rows re-strided to ld for TMA (the columns past K are never read) */
+        uint16_t* xp = (uint16_t*)(wb + pp.x_off);
+        if (cudaMemcpy2DAsync(xp, (size_t)pp.ld * 2, x, (size_t)K * 2, (size_t)K * 2, (size_t)batch,
+                              cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+            return EC_ERR_CUDA;
+        xs = xp;
+        xld = pp.ld;
+    }
+    if (!huff) { /* one chunk: the whole matrix through its own decoder */
+        rc = W->kind == EC_KIND_RANS_INT4  ? rans_run(W, nullptr, nullptr, chunk, 1, stream, d)
+             : W->kind == EC_KIND_RANS_FP8 ? fp8_run(W, nullptr, nullptr, chunk, 1, stream, d)
+                                           : e8_run(W, chunk, EC_DTYPE_BF16, stream, d);
+        if (rc != EC_OK) return rc;
+        return gemm_run(chunk, h.n_rows, K, K, xs, xld, batch, y, h.n_rows, 0, part, pp.part_cap, stream, d);
+    }
+    HuffDecodeArgs a{};
+    a.count = 1;
+    HuffMat m = huff_desc(W);
+    m.out = chunk;
+    m.out_ld = pp.ld;
+    const bool lng = huff_hier(W);
+    if (lng && m.n_sub > 0 && m.n_sub <= kSubSmemTables) {
+        m.sub_smem = 0;
+        a.sub_words = 256 * m.n_sub;
+    }
+    const int code_bytes = std::max(16, staged_code_bytes(W));
+    const int64_t T = 32 * (int64_t)h.steps;
+    for (int64_t r0 = 0; r0 < h.n_rows; r0 += pp.chunk_rows) {
+        const int64_t r1 = std::min(h.n_rows, r0 + pp.chunk_rows);
+        /* chunk starts are tile starts: the chunk's tiles cover exactly its rows */
+        const int64_t t0 = r0 * h.k_pad / T, t1 = r1 == h.n_rows ? h.n_tiles : r1 * h.k_pad / T;
+        a.m[0] = m;
+        a.m[0].out_row0 = r0;
+        a.m[0].tile_begin = -t0;
+        a.total_tiles = t1 - t0;
+        if ((rc = launch_huff_decode(a, code_bytes, lng, stream, d)) != EC_OK) return rc;
+        if ((rc = gemm_run(chunk, r1 - r0, K, pp.ld, xs, xld, batch, y, h.n_rows, r0, part, pp.part_cap, stream, d)) !=
+            EC_OK)
+            return rc;
+    }
+    return EC_OK;
+}
+
+extern "C" int ec_bf16_gemm(const uint16_t* w, int64_t n_rows, int64_t k_cols, const uint16_t* x, float* y, int batch,
+                            void* work, size_t work_bytes, cudaStream_t stream) {
+    if (n_rows < 0 || k_cols < 0 || batch < 1) return EC_ERR_INVALID_ARG;
+    if (n_rows == 0) return EC_OK;
+    if (!y || !aligned16(y)) return EC_ERR_INVALID_ARG;
+    if (k_cols == 0)
+        return cudaMemsetAsync(y, 0, sizeof(float) * (size_t)batch * (size_t)n_rows, stream) == cudaSuccess
+                   ? EC_OK
+                   : EC_ERR_CUDA;
+    if (!w || !x || !aligned16(w) || !aligned16(x)) return EC_ERR_INVALID_ARG;
+    if (k_cols % 8) return EC_ERR_UNSUPPORTED;
+    if (work && !aligned16(work)) return EC_ERR_INVALID_ARG;
+    int dev = 0;
+    if (current_device(&dev) != EC_OK) return EC_ERR_CUDA;
+    DeviceInfo* d = nullptr;
+    int rc = device_info(dev, &d);
+    if (rc != EC_OK) return rc;
+    return gemm_run(w, n_rows, k_cols, k_cols, x, k_cols, batch, y, n_rows, 0, (float*)work, work ? work_bytes : 0,
+                    stream, d);
 }
 
 extern "C" int ec_decode(const ec_matrix* W, uint16_t* out, cudaStream_t stream) {
