@@ -17,6 +17,9 @@ Functions and the passages they follow (page titles and sections):
   e8_fields / e8_point / E8     EntroPack sec. 3.2, 3.3, 3.6, 3.7, appendix A.3 (E8 fields, 17 tables)
   e8_reconstruct_bf16           EntroPack sec. 3.7 (lattice point x shared scale x row scale)
   Fp8 / fp8_table / e4m3_to_f32 MINE sec. 4 "Escapes" (top-t table, sparse correction records)
+  Expx / expx_bound / expx_choose_t / pad_rows
+                                MINE sec. 4: BF16 exponents through rANS tiles with a top-t
+                                table, escapes and "Pair" symbols; sec. 4.2 "Tuning t"
   fp8_dequant_bf16 / gemv_fp8   FP8 E4M3 weights with FP32 row scales
   e8_reconstruct / f32_to_e4m3 / f32_to_s8
                                 EntroPack sec. 3.7 and appendix B.1 (FP8 / INT8 output); the OCP
@@ -126,6 +129,21 @@ def _L():
         "orc_fp8_payload_mut": ([vp], vp),
         "orc_fp8_rec_off": ([vp], vp),
         "orc_fp8_records": ([vp], vp),
+        "orc_expx_bound": ([vp, i64, i32, i32, i32, i32], f64),
+        "orc_expx_choose_t": ([vp, i64, i32, i32, i32, i32], i32),
+        "orc_expx_encode": ([vp, i64, i32, i32, i32, i32], vp),
+        "orc_expx_decode": ([vp, vp], i32),
+        "orc_expx_free": ([vp], None),
+        "orc_expx_info": ([vp, vp], i64),
+        "orc_expx_table_of": ([vp], vp),
+        "orc_expx_freqs_of": ([vp], vp),
+        "orc_expx_counts_of": ([vp], vp),
+        "orc_expx_states": ([vp], vp),
+        "orc_expx_offsets": ([vp], vp),
+        "orc_expx_payload_mut": ([vp], vp),
+        "orc_expx_rec_off": ([vp], vp),
+        "orc_expx_records": ([vp], vp),
+        "orc_expx_sm": ([vp], vp),
         "orc_fp8_dequant_bf16": ([vp, vp, i64, i64, vp], None),
         "orc_gemv_fp8": ([vp, vp, i64, i64, vp, i32, vp, i64, vp, vp], None),
     }
@@ -569,6 +587,97 @@ class Fp8:
     def decode(self):
         out = np.zeros(max(1, self.n), dtype=np.uint8)
         rc = _L().orc_fp8_decode(self._h, _p(out))
+        return out[: self.n], rc
+
+
+def pad_rows(w: np.ndarray, align: int = 128) -> np.ndarray:
+    """BF16 patterns [n_rows, k_cols] with each row padded by zero weights to a
+    multiple of `align` columns (the padded layout of the rANS codecs)."""
+    n, k = w.shape
+    kp = -(-k // align) * align if k else 0
+    out = np.zeros((n, kp), dtype=np.uint16)
+    out[:, :k] = w
+    return out
+
+
+def expx_bound(w: np.ndarray, k: int, t: int, prob_bits: int = 12, tile: int = 4096) -> float:
+    """Size bound in bits of the exponent codec with table size t (-1: the table cannot hold the symbols)."""
+    f = np.ascontiguousarray(w, dtype=np.uint16).ravel()
+    return float(_L().orc_expx_bound(_p(f) if f.size else None, f.size, k, t, prob_bits, tile))
+
+
+def expx_choose_t(w: np.ndarray, k: int, t_max: int, prob_bits: int = 12, tile: int = 4096) -> int:
+    """The smallest t in 1..t_max whose size bound is least (MINE sec. 4.2 "Tuning t")."""
+    f = np.ascontiguousarray(w, dtype=np.uint16).ravel()
+    return int(_L().orc_expx_choose_t(_p(f) if f.size else None, f.size, k, t_max, prob_bits, tile))
+
+
+class Expx:
+    """BF16 patterns of the padded layout (flattened): exponents through rANS tiles
+    under a top-t table (single values, k = 1, or pairs of a lane's consecutive
+    steps, k = 2), escaped exponents as per-tile records, sign and mantissa as one
+    plain byte per weight (MINE sec. 4, BF16 handling, "Escapes", "Pair")."""
+
+    def __init__(self, w: np.ndarray, t: int = 256, prob_bits: int = 12, tile: int = 4096, k: int = 1):
+        f = np.ascontiguousarray(w, dtype=np.uint16).ravel()
+        h = _L().orc_expx_encode(_p(f) if f.size else None, f.size, t, prob_bits, tile, k)
+        if not h:
+            raise ValueError("exponent codec: encode failed")
+        self._h = h
+        self.prob_bits = prob_bits
+        info = np.zeros(8, dtype=np.int64)
+        _L().orc_expx_info(h, _p(info))
+        (self.n, self.n_tiles, self.payload_words, self.tile, self.tsize, self.n_records, self.nsym,
+         self.k) = (int(v) for v in info)
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            _L().orc_expx_free(self._h)
+            self._h = None
+
+    @property
+    def table(self):
+        return _view(_L().orc_expx_table_of(self._h), np.uint8, self.tsize)
+
+    @property
+    def freqs(self):
+        return _view(_L().orc_expx_freqs_of(self._h), np.uint32, self.nsym)
+
+    @property
+    def counts(self):
+        return _view(_L().orc_expx_counts_of(self._h), np.uint64, self.nsym)
+
+    @property
+    def states(self):
+        return _view(_L().orc_expx_states(self._h), np.uint32, 32 * self.n_tiles).reshape(self.n_tiles, 32)
+
+    @property
+    def offsets(self):
+        return _view(_L().orc_expx_offsets(self._h), np.uint32, self.n_tiles + 1)
+
+    @property
+    def rec_off(self):
+        return _view(_L().orc_expx_rec_off(self._h), np.uint32, self.n_tiles + 1)
+
+    @property
+    def records(self):
+        return _view(_L().orc_expx_records(self._h), np.uint32, max(1, self.n_records))[: self.n_records]
+
+    @property
+    def sm(self):
+        return _view(_L().orc_expx_sm(self._h), np.uint8, max(1, self.n))[: self.n]
+
+    def payload(self) -> np.ndarray:
+        return np.ctypeslib.as_array((ctypes.c_uint16 * max(1, self.payload_words)).from_address(
+            _L().orc_expx_payload_mut(self._h)))[: self.payload_words].copy()
+
+    def flip_payload_bit(self, word: int, bit: int) -> None:
+        w = ctypes.c_uint16.from_address(_L().orc_expx_payload_mut(self._h) + 2 * word)
+        w.value ^= 1 << bit
+
+    def decode(self):
+        out = np.zeros(max(1, self.n), dtype=np.uint16)
+        rc = _L().orc_expx_decode(self._h, _p(out))
         return out[: self.n], rc
 
 

@@ -1339,3 +1339,304 @@ void orc_e8_reconstruct_bf16(const int8_t* q, int64_t n_rows, int64_t k_cols, fl
         }
     }
 }
+
+/* ===========================================================================
+ * BF16 exponents through rANS tiles with a top-t table and escape records
+ * (MINE section 4: dtANS-LLM's BF16 handling -- the exponent is entropy-coded,
+ * sign and mantissa are kept as one plain byte; "Escapes": the table holds the t
+ * most frequent values and always 0, a value outside it is coded as 0 and listed
+ * in a sparse correction stream; "Pair" symbols of two values when t^2 <= M;
+ * "Tuning t": the t with the smallest size bound, cross-entropy of the stream plus
+ * a 4-byte record per escape).
+ *
+ * Readings:
+ *  - the coded value is the exponent field e = bits 7..14 of the BF16 pattern;
+ *    the plain byte is sign << 7 | mantissa (bits 15 and 0..6);
+ *  - the table is exponent 0 and the t - 1 most frequent other exponents present
+ *    (ties to the lower exponent), sorted ascending (the rule of orc_fp8_table);
+ *    an exponent's symbol value is its rank there, and an escaped exponent is
+ *    coded as rank 0 (exponent 0);
+ *  - positions are those of the padded layout (rows of k_pad columns, zero
+ *    weights in the padding), flattened, in tiles of `tile` positions; position
+ *    32 j + l of a tile is lane l's step j (as the tile codec above);
+ *  - k = 1: one symbol per lane step; k = 2: the symbol of lane steps 2 m and
+ *    2 m + 1 is rank(e_2m) * tsize + rank(e_2m+1) (tile and n multiples of 64);
+ *  - one frequency table over the tsize^k symbol values (orc_rans_freqs_n),
+ *    states and payload words as the tile codec above;
+ *  - tile t's records list its escapes by ascending position p: p | e << 16;
+ *  - size bound of a table size t: sum over the stream's symbols of
+ *    log2(2^prob_bits / f_s) bits plus 32 bits per escape; the automatic t is the
+ *    smallest t in 1..t_max with the least bound.
+ * ========================================================================= */
+typedef struct {
+    int64_t n;                 /* positions */
+    int k, tsize, prob_bits, tile, nsym;
+    uint8_t table[256];
+    int16_t rank[256];
+    uint32_t* freqs;           /* nsym */
+    uint32_t* cum;
+    uint64_t* counts;
+    int64_t n_tiles;
+    uint32_t* states;          /* n_tiles * 32 */
+    uint32_t* offsets;         /* n_tiles + 1 */
+    uint16_t* payload;
+    int64_t payload_words;
+    uint32_t* rec_off;         /* n_tiles + 1 */
+    uint32_t* records;
+    int64_t n_records;
+    uint8_t* sm;               /* n plain bytes: sign << 7 | mantissa */
+} orc_expx;
+
+void orc_expx_free(orc_expx* f) {
+    if (!f) return;
+    free(f->freqs);
+    free(f->cum);
+    free(f->counts);
+    free(f->states);
+    free(f->offsets);
+    free(f->payload);
+    free(f->rec_off);
+    free(f->records);
+    free(f->sm);
+    free(f);
+}
+
+static int expx_field(uint16_t w) { return (w >> 7) & 0xFF; }
+
+/* The symbol of lane l's symbol step m in the tile starting at `base` (n_t
+ * positions), given the rank of every position's exponent (escapes already 0). */
+static int expx_symbol(const uint8_t* rk, int64_t base, int k, int tsize, int64_t m, int l) {
+    int s = 0;
+    for (int i = 0; i < k; ++i) s = s * tsize + rk[base + 32 * (k * m + i) + l];
+    return s;
+}
+
+/* Ranks of every position under the table of size t built from `counts`; the
+ * number of escapes goes to *n_esc.  Returns the table size. */
+static int expx_ranks(const uint16_t* w, int64_t n, const uint64_t counts[256], int t, uint8_t* table, int16_t* rank,
+                      uint8_t* rk, int64_t* n_esc) {
+    const int tsize = orc_fp8_table(counts, t, table);
+    for (int e = 0; e < 256; ++e) rank[e] = -1;
+    for (int s = 0; s < tsize; ++s) rank[table[s]] = (int16_t)s;
+    int64_t ne = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        const int r = rank[expx_field(w[i])];
+        rk[i] = (uint8_t)(r < 0 ? 0 : r);
+        ne += r < 0;
+    }
+    *n_esc = ne;
+    return tsize;
+}
+
+/* Histogram of the symbol stream (nsym values). */
+static void expx_histogram(const uint8_t* rk, int64_t n, int k, int tsize, int tile, uint64_t* counts, int nsym) {
+    memset(counts, 0, sizeof(uint64_t) * (size_t)nsym);
+    for (int64_t base = 0; base < n; base += tile) {
+        const int64_t n_t = (n - base < tile) ? n - base : tile;
+        for (int l = 0; l < 32; ++l)
+            for (int64_t m = 0; m < lane_steps(n_t, l) / k; ++m) counts[expx_symbol(rk, base, k, tsize, m, l)]++;
+    }
+}
+
+/* Size bound in bits of table size t (k, prob_bits fixed); -1 when the table
+ * cannot hold the symbol values (tsize^k > 2^prob_bits). */
+double orc_expx_bound(const uint16_t* w, int64_t n, int k, int t, int prob_bits, int tile) {
+    uint64_t cnt[256] = {0};
+    for (int64_t i = 0; i < n; ++i) cnt[expx_field(w[i])]++;
+    uint8_t table[256];
+    int16_t rank[256];
+    uint8_t* rk = (uint8_t*)malloc((size_t)(n > 0 ? n : 1));
+    int64_t ne = 0;
+    const int tsize = expx_ranks(w, n, cnt, t, table, rank, rk, &ne);
+    const int nsym = k == 1 ? tsize : tsize * tsize;
+    if (nsym > (1 << prob_bits)) {
+        free(rk);
+        return -1.0;
+    }
+    uint64_t* counts = (uint64_t*)calloc((size_t)nsym, sizeof(uint64_t));
+    uint32_t* freqs = (uint32_t*)calloc((size_t)nsym, sizeof(uint32_t));
+    expx_histogram(rk, n, k, tsize, tile, counts, nsym);
+    double bits = 0.0;
+    if (orc_rans_freqs_n(counts, nsym, prob_bits, freqs) >= 0)
+        for (int s = 0; s < nsym; ++s)
+            if (counts[s]) bits += (double)counts[s] * ((double)prob_bits - log2((double)freqs[s]));
+    free(counts);
+    free(freqs);
+    free(rk);
+    return bits + 32.0 * (double)ne;
+}
+
+/* The smallest t in 1..t_max with the least bound (t_max capped where tsize^k
+ * would exceed the table). */
+int orc_expx_choose_t(const uint16_t* w, int64_t n, int k, int t_max, int prob_bits, int tile) {
+    int best = 1;
+    double best_bits = -1.0;
+    for (int t = 1; t <= t_max && t <= 256; ++t) {
+        const double b = orc_expx_bound(w, n, k, t, prob_bits, tile);
+        if (b < 0) break;
+        if (best_bits < 0 || b < best_bits) {
+            best_bits = b;
+            best = t;
+        }
+    }
+    return best;
+}
+
+/* Encode BF16 patterns w[n] (the padded layout, flattened). */
+orc_expx* orc_expx_encode(const uint16_t* w, int64_t n, int t, int prob_bits, int tile, int k) {
+    if (n < 0 || t < 1 || t > 256 || prob_bits < 5 || prob_bits > 15 || tile < 32 || tile % 32) return NULL;
+    if (k != 1 && k != 2) return NULL;
+    if (k == 2 && (tile % 64 || n % 64)) return NULL;
+    orc_expx* f = (orc_expx*)calloc(1, sizeof(orc_expx));
+    f->n = n;
+    f->k = k;
+    f->prob_bits = prob_bits;
+    f->tile = tile;
+    uint64_t cnt[256] = {0};
+    for (int64_t i = 0; i < n; ++i) cnt[expx_field(w[i])]++;
+    uint8_t* rk = (uint8_t*)malloc((size_t)(n > 0 ? n : 1));
+    int64_t ne = 0;
+    f->tsize = expx_ranks(w, n, cnt, t, f->table, f->rank, rk, &ne);
+    f->nsym = k == 1 ? f->tsize : f->tsize * f->tsize;
+    if (f->nsym > (1 << prob_bits)) {
+        free(rk);
+        orc_expx_free(f);
+        return NULL;
+    }
+    f->counts = (uint64_t*)calloc((size_t)f->nsym, sizeof(uint64_t));
+    f->freqs = (uint32_t*)calloc((size_t)f->nsym, sizeof(uint32_t));
+    f->cum = (uint32_t*)calloc((size_t)f->nsym, sizeof(uint32_t));
+    expx_histogram(rk, n, k, f->tsize, tile, f->counts, f->nsym);
+    if (orc_rans_freqs_n(f->counts, f->nsym, prob_bits, f->freqs) < 0) {
+        free(rk);
+        orc_expx_free(f);
+        return NULL;
+    }
+    for (int s = 0, c = 0; s < f->nsym; ++s) {
+        f->cum[s] = (uint32_t)c;
+        c += (int)f->freqs[s];
+    }
+    /* the symbol stream: each lane in reverse, lanes 31 -> 0 within a step (as
+     * orc_rans_encode_k) */
+    f->n_tiles = (n + tile - 1) / tile;
+    f->states = (uint32_t*)malloc(sizeof(uint32_t) * 32 * (size_t)(f->n_tiles > 0 ? f->n_tiles : 1));
+    f->offsets = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)(f->n_tiles + 1));
+    f->payload = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(n > 0 ? n : 1));
+    uint16_t* stack = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)tile);
+    const uint64_t unit = (uint64_t)1 << (32 - prob_bits);
+    int64_t words = 0;
+    for (int64_t tt = 0; tt < f->n_tiles; ++tt) {
+        const int64_t base = tt * tile, n_t = (n - base < tile) ? n - base : tile;
+        uint64_t x[32];
+        for (int l = 0; l < 32; ++l) x[l] = 1u << 16;
+        int64_t sp = 0;
+        for (int64_t m = (n_t + 31) / 32 / k - 1; m >= 0; --m)
+            for (int l = 31; l >= 0; --l) {
+                if (m >= lane_steps(n_t, l) / k) continue;
+                const int s = expx_symbol(rk, base, k, f->tsize, m, l);
+                const uint64_t fs = f->freqs[s];
+                while (x[l] >= fs * unit) {
+                    stack[sp++] = (uint16_t)(x[l] & 0xFFFF);
+                    x[l] >>= 16;
+                }
+                x[l] = (x[l] / fs << prob_bits) + (x[l] % fs) + f->cum[s];
+            }
+        for (int l = 0; l < 32; ++l) f->states[tt * 32 + l] = (uint32_t)x[l];
+        f->offsets[tt] = (uint32_t)words;
+        while (sp > 0) f->payload[words++] = stack[--sp];
+    }
+    f->offsets[f->n_tiles] = (uint32_t)words;
+    f->payload_words = words;
+    free(stack);
+    free(rk);
+    /* escapes and plain bytes */
+    f->rec_off = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)(f->n_tiles + 1));
+    f->records = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)(ne > 0 ? ne : 1));
+    f->sm = (uint8_t*)malloc((size_t)(n > 0 ? n : 1));
+    for (int64_t tt = 0; tt < f->n_tiles; ++tt) {
+        f->rec_off[tt] = (uint32_t)f->n_records;
+        const int64_t base = tt * tile, n_t = (n - base < tile) ? n - base : tile;
+        for (int64_t p = 0; p < n_t; ++p) {
+            const int e = expx_field(w[base + p]);
+            if (f->rank[e] < 0) f->records[f->n_records++] = (uint32_t)p | ((uint32_t)e << 16);
+        }
+    }
+    f->rec_off[f->n_tiles] = (uint32_t)f->n_records;
+    for (int64_t i = 0; i < n; ++i) f->sm[i] = (uint8_t)(((w[i] >> 8) & 0x80) | (w[i] & 0x7F));
+    return f;
+}
+
+/* Decode back to BF16 patterns: symbols through the table (ranks to exponents),
+ * each record's exponent at its position, then sign | exponent | mantissa.
+ * Returns 0, -1 on a corrupt stream, -2 if a final state or word count is off. */
+int orc_expx_decode(const orc_expx* f, uint16_t* out) {
+    const uint32_t M = 1u << f->prob_bits;
+    const int k = f->k;
+    int rc = 0;
+    uint8_t* ex = (uint8_t*)malloc((size_t)(f->n > 0 ? f->n : 1));
+    for (int64_t t = 0; t < f->n_tiles; ++t) {
+        const int64_t base = t * f->tile, n_t = (f->n - base < f->tile) ? f->n - base : f->tile;
+        uint64_t x[32];
+        for (int l = 0; l < 32; ++l) x[l] = f->states[t * 32 + l];
+        int64_t wp = f->offsets[t];
+        const int64_t wend = f->offsets[t + 1];
+        for (int64_t m = 0; m < (n_t + 31) / 32 / k; ++m)
+            for (int l = 0; l < 32; ++l) {
+                if (m >= lane_steps(n_t, l) / k) continue;
+                const uint32_t slot = (uint32_t)(x[l] & (M - 1));
+                int s = -1;
+                for (int q = 0; q < f->nsym; ++q)
+                    if (f->freqs[q] && slot >= f->cum[q] && slot < f->cum[q] + f->freqs[q]) s = q;
+                if (s < 0) {
+                    free(ex);
+                    return -1;
+                }
+                x[l] = (uint64_t)f->freqs[s] * (x[l] >> f->prob_bits) + slot - f->cum[s];
+                if (x[l] < (1u << 16)) {
+                    if (wp >= wend) {
+                        free(ex);
+                        return -1;
+                    }
+                    x[l] = (x[l] << 16) | f->payload[wp++];
+                }
+                for (int i = k - 1, v = s; i >= 0; --i, v /= f->tsize)
+                    ex[base + 32 * (k * m + i) + l] = f->table[v % f->tsize];
+            }
+        for (int l = 0; l < 32; ++l)
+            if (x[l] != (1u << 16)) rc = -2;
+        if (wp != wend) rc = -2;
+        for (uint32_t e = f->rec_off[t]; e < f->rec_off[t + 1]; ++e) {
+            const uint32_t p = f->records[e] & 0xFFFFu;
+            if ((int64_t)p >= n_t) {
+                free(ex);
+                return -1;
+            }
+            ex[base + p] = (uint8_t)(f->records[e] >> 16);
+        }
+    }
+    for (int64_t i = 0; i < f->n; ++i)
+        out[i] = (uint16_t)(((uint16_t)(f->sm[i] & 0x80) << 8) | ((uint16_t)ex[i] << 7) | (f->sm[i] & 0x7F));
+    free(ex);
+    return rc;
+}
+
+int64_t orc_expx_info(const orc_expx* f, int64_t* out /* 8 */) {
+    out[0] = f->n;
+    out[1] = f->n_tiles;
+    out[2] = f->payload_words;
+    out[3] = f->tile;
+    out[4] = f->tsize;
+    out[5] = f->n_records;
+    out[6] = f->nsym;
+    out[7] = f->k;
+    return 0;
+}
+const uint8_t* orc_expx_table_of(const orc_expx* f) { return f->table; }
+const uint32_t* orc_expx_freqs_of(const orc_expx* f) { return f->freqs; }
+const uint64_t* orc_expx_counts_of(const orc_expx* f) { return f->counts; }
+const uint32_t* orc_expx_states(const orc_expx* f) { return f->states; }
+const uint32_t* orc_expx_offsets(const orc_expx* f) { return f->offsets; }
+uint16_t* orc_expx_payload_mut(orc_expx* f) { return f->payload; }
+const uint32_t* orc_expx_rec_off(const orc_expx* f) { return f->rec_off; }
+const uint32_t* orc_expx_records(const orc_expx* f) { return f->records; }
+const uint8_t* orc_expx_sm(const orc_expx* f) { return f->sm; }
