@@ -137,7 +137,26 @@ typedef struct {
     int32_t reserved[2];
 } ec_e8_params;
 
-enum { EC_KIND_HUFFMAN_BF16 = 1, EC_KIND_RANS_INT4 = 2, EC_KIND_E8 = 3, EC_KIND_RANS_FP8 = 4 };
+enum { EC_KIND_HUFFMAN_BF16 = 1, EC_KIND_RANS_INT4 = 2, EC_KIND_E8 = 3, EC_KIND_RANS_FP8 = 4, EC_KIND_RANS_EXP = 5 };
+
+/* Parameters of the rANS codec for BF16 exponents (NULL = defaults).
+ *  prob_bits   frequency precision b, 9..12 (default 12)
+ *  tile_syms   weights per rANS tile, a multiple of 128 up to 4096 (default 4096)
+ *  top_t       exponents kept in the decoding table, exponent 0 always among them:
+ *              1..256 with single symbols, 1..16 with pairs; 0 (default) takes the
+ *              smallest t with the least bound of the coded size, the cross-entropy
+ *              of the symbol stream under the normalised table plus 32 bits per
+ *              escape (MINE section 4.2, "Tuning t")
+ *  single      0 (default): a symbol is the pair of exponents of a lane's two
+ *              consecutive weights (MINE's "Pair" symbols; t^2 <= 2^prob_bits, and
+ *              this format's 8-bit symbol field limits t to 16); 1: one exponent per
+ *              symbol */
+typedef struct {
+    int32_t prob_bits;
+    int32_t tile_syms;
+    int32_t top_t;
+    int32_t single;
+} ec_exp_params;
 
 /* FP8 codec parameters (NULL = defaults).
  *  prob_bits         frequency precision b, 9..12 (default 12)
@@ -218,6 +237,18 @@ int ec_encode_e8(const int8_t* q2_host, const float* row_scales_host, float scal
  * sum_j value * x); ec_decode writes bf16(fp32(value * r_i)).  Errors as ec_encode_rans. */
 int ec_encode_fp8(const uint8_t* codes_host, const float* row_scales_host, int64_t n_rows, int64_t k_cols,
                   const ec_fp8_params* params, int device, ec_matrix** out);
+
+/* Encode a row-major BF16 matrix [n_rows, k_cols] (host, bit patterns) with the
+ * exponent going through rANS tiles under a top-t table and sign and mantissa kept
+ * as one plain byte (MINE section 4: dtANS-LLM's BF16 handling; "Escapes": an
+ * exponent outside the table is coded as exponent 0 and its weight listed in a
+ * per-tile 32-bit record, position | BF16 pattern << 16; "Pair" symbols).  The
+ * coding is lossless: every BF16 pattern round-trips.  ec_gemv / ec_gemv_group
+ * (CUDA cores, batch 1..EC_MAX_BATCH, the records folded into each row's sum),
+ * ec_decode, ec_decode_batch and ec_gemm accept the result.  Errors as
+ * ec_encode_bf16; parameters out of range give EC_ERR_INVALID_ARG. */
+int ec_encode_bf16_exp(const uint16_t* w_host, int64_t n_rows, int64_t k_cols, const ec_exp_params* params,
+                       int device, ec_matrix** out);
 
 /* Decode W to dense row-major BF16 [n_rows, k_cols] in device memory out_bf16
  * (DFloat11 Algorithm 1, second phase: table lookups, then sign | exponent |

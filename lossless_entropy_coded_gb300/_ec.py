@@ -35,11 +35,12 @@ EC_KIND_HUFFMAN_BF16 = 1
 EC_KIND_RANS_INT4 = 2
 EC_KIND_E8 = 3
 EC_KIND_RANS_FP8 = 4
+EC_KIND_RANS_EXP = 5
 
 EXPORTS = ["ec_encode_bf16", "ec_encode_rans", "ec_decode", "ec_decode_batch", "ec_gemv", "ec_gemv_group",
            "ec_bf16_gemv", "ec_stats", "ec_code_lengths", "ec_serialize", "ec_deserialize", "ec_status", "ec_free",
            "ec_strerror", "ec_gemv_static", "ec_gemv_path", "ec_encode_e8", "ec_decode_as", "ec_encode_fp8",
-           "ec_gemm", "ec_gemm_work_bytes", "ec_bf16_gemm"]
+           "ec_gemm", "ec_gemm_work_bytes", "ec_bf16_gemm", "ec_encode_bf16_exp"]
 
 
 class HuffParams(ctypes.Structure):
@@ -61,6 +62,11 @@ class Fp8Params(ctypes.Structure):
                 ("reserved", ctypes.c_int32)]
 
 
+class ExpParams(ctypes.Structure):
+    _fields_ = [("prob_bits", ctypes.c_int32), ("tile_syms", ctypes.c_int32), ("top_t", ctypes.c_int32),
+                ("single", ctypes.c_int32)]
+
+
 class Stats(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("max_code_len", ctypes.c_int32), ("n_rows", ctypes.c_int64),
                 ("k_cols", ctypes.c_int64), ("k_pad", ctypes.c_int64), ("n_tiles", ctypes.c_int64),
@@ -80,6 +86,7 @@ _sig = {
     "ec_encode_e8": ([_vp, _vp, ctypes.c_float, _i64, _i64, ctypes.POINTER(E8Params), _i32, ctypes.POINTER(_vp)],
                      _i32),
     "ec_encode_fp8": ([_vp, _vp, _i64, _i64, ctypes.POINTER(Fp8Params), _i32, ctypes.POINTER(_vp)], _i32),
+    "ec_encode_bf16_exp": ([_vp, _i64, _i64, ctypes.POINTER(ExpParams), _i32, ctypes.POINTER(_vp)], _i32),
     "ec_decode": ([_vp, _vp, _vp], _i32),
     "ec_decode_batch": ([_vp, _vp, _i32, _vp], _i32),
     "ec_decode_as": ([_vp, _vp, _i32, _vp], _i32),
@@ -234,6 +241,21 @@ def encode_fp8(codes, row_scales, top_t: int = 0, prob_bits: int = 0, tile_syms:
     h = ctypes.c_void_p()
     _check(lib.ec_encode_fp8(pc, pr, n, k, ctypes.byref(prm), device, ctypes.byref(h)), "ec_encode_fp8")
     return Matrix(h.value, n, k, EC_KIND_RANS_FP8, device)
+
+
+def encode_bf16_exp(w, prob_bits: int = 0, tile_syms: int = 0, top_t: int = 0, single: bool = False,
+                    device: int = 0) -> Matrix:
+    """Encode a host BF16 matrix [N, K] (uint16 bit patterns) with its exponents as rANS
+    symbols under a top-t table (pairs of a lane's consecutive exponents unless single),
+    escaped exponents as records, sign and mantissa as plain bytes.  0 selects the
+    defaults (2^12 slots, 4096-weight tiles, t chosen by the size bound)."""
+    n, k = int(w.shape[0]), int(w.shape[1])
+    p, keep = _host_ptr(w)
+    prm = ExpParams(prob_bits, tile_syms, top_t, 1 if single else 0)
+    h = ctypes.c_void_p()
+    _check(lib.ec_encode_bf16_exp(p, n, k, ctypes.byref(prm), device, ctypes.byref(h)), "ec_encode_bf16_exp")
+    del keep
+    return Matrix(h.value, n, k, EC_KIND_RANS_EXP, device)
 
 
 def deserialize(data: bytes, device: int = 0) -> Matrix:

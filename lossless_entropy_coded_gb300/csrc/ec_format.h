@@ -150,6 +150,22 @@
  * tile); rANS tile records (32 states, u16 words) as for kind 2, last. */
 #define EC_FP8_VALUE_WORDS 512
 
+/* Exponent blob (kind 5): BF16 weights whose exponent goes through rANS tiles under
+ * a top-t table.  Rows padded to k_pad (a multiple of EC_RANS_ROW_ALIGN) with zero
+ * weights; rANS positions as above (position 32 i + l of a tile is lane l's step i).
+ * Table section: 2^prob_bits slot entries (bits 0..7 = the exponent itself for single
+ * symbols, or the pair symbol 16 r0 + r1 of the exponents' ranks r0 (step 2m), r1
+ * (step 2m + 1) in the ascending top-t table; bits 8..19 = slot - cum[s]; bits
+ * 20..31 = freq[s] - 1), then 256 u32 holding, for pair symbol s, the two exponents
+ * where a BF16 pair [w(2m+1) | w(2m)] keeps them (e0 << 7 | e1 << 23).  The section at
+ * scales_off holds the sign / mantissa bytes: per tile EC_RAW_BYTES(steps) bytes in
+ * the lane-transposed, pair-shuffled layout of the Huffman tiles (lane l's symbol i
+ * at position 32 i + l).  Records as FP8 (u32 offsets per tile at esc_off_off, u32
+ * records at esc_records_off), each = position in the tile | BF16 pattern << 16 of a
+ * weight whose exponent is outside the table (coded as exponent 0, the table's first
+ * entry).  fp8_table_size = the table size t, rans_tuple = 1 or 2; rANS tile records
+ * (32 states, u16 words) last. */
+
 typedef struct {
     uint32_t magic, version;
     int32_t kind;             /* EC_KIND_* */

@@ -24,6 +24,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <queue>
 #include <thread>
@@ -1236,6 +1237,275 @@ extern "C" int ec_encode_fp8(const uint8_t* codes, const float* row_scales, int6
     });
 }
 
+/* ============================================== BF16 exponents, rANS top-t codec */
+namespace {
+/* The exponent table of size up to t from an exponent histogram: exponent 0, then
+ * the most frequent other present exponents (ties to the lower one), ascending.
+ * rank[e] = index in it, -1 outside. */
+int exp_table(const uint64_t hist[256], int t, uint8_t* table, int* rank) {
+    bool kept[256] = {};
+    kept[0] = true;
+    for (int size = 1; size < t; ++size) {
+        int best = -1;
+        for (int e = 1; e < 256; ++e)
+            if (!kept[e] && hist[e] && (best < 0 || hist[e] > hist[best])) best = e;
+        if (best < 0) break;
+        kept[best] = true;
+    }
+    int n = 0;
+    for (int e = 0; e < 256; ++e) {
+        rank[e] = kept[e] ? n : -1;
+        if (kept[e]) table[n++] = (uint8_t)e;
+    }
+    return n;
+}
+
+/* Symbol histogram of table size t (symbol = rank, or 16 r0 + r1 for pairs, escapes
+ * coded as rank 0) from the exponent histogram (single) or the histogram of the
+ * exponent pairs of consecutive lane steps (pairs, 65536 entries); the escape count
+ * goes to *esc.  Returns the table size. */
+int exp_symbol_hist(bool pair, const uint64_t* hist, const uint64_t* pair_hist, int t, uint8_t* table, int* rank,
+                    uint64_t counts[256], uint64_t* esc) {
+    const int ts = exp_table(hist, t, table, rank);
+    std::fill(counts, counts + 256, uint64_t(0));
+    *esc = 0;
+    for (int e = 0; e < 256; ++e)
+        if (rank[e] < 0) *esc += hist[e];
+    if (!pair) {
+        for (int e = 0; e < 256; ++e) counts[rank[e] < 0 ? 0 : rank[e]] += hist[e];
+    } else {
+        for (int e0 = 0; e0 < 256; ++e0)
+            for (int e1 = 0; e1 < 256; ++e1) {
+                const uint64_t c = pair_hist[e0 * 256 + e1];
+                if (c) counts[16 * (rank[e0] < 0 ? 0 : rank[e0]) + (rank[e1] < 0 ? 0 : rank[e1])] += c;
+            }
+    }
+    return ts;
+}
+}  // namespace
+
+extern "C" int ec_encode_bf16_exp(const uint16_t* w, int64_t n_rows, int64_t k_cols, const ec_exp_params* params,
+                                  int device, ec_matrix** out) {
+    if (!out) return EC_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (n_rows < 0 || k_cols < 0) return EC_ERR_SHAPE;
+    const int b = params && params->prob_bits ? params->prob_bits : 12;
+    const int T = params && params->tile_syms ? params->tile_syms : 4096;
+    const bool pair = !params || params->single == 0;
+    const int t_req = params ? params->top_t : 0;
+    const int t_cap = pair ? 16 : 256;
+    if (b < 9 || b > 12 || T < EC_RANS_ROW_ALIGN || T % EC_RANS_ROW_ALIGN || T > 4096 || t_req < 0 || t_req > t_cap ||
+        (params && (params->single < 0 || params->single > 1)))
+        return EC_ERR_INVALID_ARG;
+    if (k_cols > INT64_MAX - EC_RANS_ROW_ALIGN) return EC_ERR_OVERFLOW;
+    const int64_t KP = round_up(k_cols, EC_RANS_ROW_ALIGN);
+    int64_t nk = 0, n_pad = 0, tmp = 0;
+    if (!mul_ok(n_rows, k_cols, &nk) || !mul_ok(n_rows, KP, &n_pad) || !mul_ok(n_pad, 4, &tmp)) return EC_ERR_OVERFLOW;
+    if (nk > 0 && !w) return EC_ERR_INVALID_ARG;
+
+    return guarded([&]() -> int {
+        const int64_t K = k_cols;
+        const int64_t n_tiles = (n_pad + T - 1) / T;
+        /* histograms over the padded layout: exponents, and for pairs the exponents of
+         * each lane's steps 2m, 2m + 1 (positions 64 m + l and 64 m + 32 + l of a tile) */
+        uint64_t hist[256] = {};
+        std::vector<uint64_t> pair_hist(pair ? 65536 : 0, 0);
+        {
+            std::mutex mu;
+            parallel_for(n_tiles, [&](int64_t lo, int64_t hi) {
+                uint64_t h[256] = {};
+                std::vector<uint64_t> ph(pair ? 65536 : 0, 0);
+                std::vector<uint16_t> v(T);
+                for (int64_t tt = lo; tt < hi; ++tt) {
+                    const int64_t base = tt * T, n_t = std::min<int64_t>(T, n_pad - base);
+                    gather_padded(w, K, KP, base, n_t, v.data());
+                    for (int64_t q = 0; q < n_t; ++q) h[(v[q] >> 7) & 0xFF]++;
+                    if (pair)
+                        for (int64_t q = 0; q < n_t; q += 64)
+                            for (int l = 0; l < 32; ++l) ph[((v[q + l] >> 7) & 0xFF) * 256 + ((v[q + 32 + l] >> 7) & 0xFF)]++;
+                }
+                std::lock_guard<std::mutex> lk(mu);
+                for (int e = 0; e < 256; ++e) hist[e] += h[e];
+                for (size_t i = 0; i < ph.size(); ++i) pair_hist[i] += ph[i];
+            });
+        }
+        /* table size: the requested one, or the smallest with the least bound of the
+         * coded size (cross-entropy of the stream under the normalised table plus 32
+         * bits per escape; MINE section 4.2, "Tuning t") */
+        uint8_t table_e[256] = {};
+        int rank[256];
+        uint64_t counts[256], esc = 0;
+        uint32_t freqs[256];
+        int t = t_req;
+        if (!t) {
+            double best = -1.0;
+            for (int c = 1; c <= t_cap; ++c) {
+                exp_symbol_hist(pair, hist, pair_hist.data(), c, table_e, rank, counts, &esc);
+                if (!rans_normalise(counts, 256, b, freqs)) continue;
+                double bits = 32.0 * (double)esc;
+                for (int s = 0; s < 256; ++s)
+                    if (counts[s]) bits += (double)counts[s] * ((double)b - std::log2((double)freqs[s]));
+                if (best < 0 || bits < best) {
+                    best = bits;
+                    t = c;
+                }
+            }
+            if (best < 0) return EC_ERR_INVALID_ARG;
+        }
+        const int tsize = exp_symbol_hist(pair, hist, pair_hist.data(), t, table_e, rank, counts, &esc);
+        ec_matrix* m = new_matrix();
+        if (!m) return EC_ERR_OOM;
+        std::copy(counts, counts + 256, m->counts);
+        if (!rans_normalise(counts, 256, b, m->freqs)) {
+            delete m;
+            return EC_ERR_INVALID_ARG;
+        }
+        const uint32_t M = 1u << b;
+        uint32_t cum[256];
+        for (int s = 0, c = 0; s < 256; ++s) {
+            cum[s] = (uint32_t)c;
+            c += (int)m->freqs[s];
+        }
+        /* slot entries: payload (single: the exponent; pair: the symbol) | slot - cum
+         * << 8 | freq - 1 << 20; then per pair symbol its two exponent fields */
+        std::vector<uint32_t> table(M + 256, 0);
+        for (int s = 0; s < 256; ++s)
+            for (uint32_t q = 0; q < m->freqs[s]; ++q)
+                table[cum[s] + q] = (uint32_t)(pair ? s : table_e[s]) | (q << 8) | ((m->freqs[s] - 1) << 20);
+        if (pair)
+            for (int r0 = 0; r0 < tsize; ++r0)
+                for (int r1 = 0; r1 < tsize; ++r1)
+                    table[M + 16 * r0 + r1] = ((uint32_t)table_e[r0] << 7) | ((uint32_t)table_e[r1] << 23);
+
+        const int64_t S_full = T / 32, raw_tile = EC_RAW_BYTES(S_full);
+        std::vector<std::vector<uint16_t>> words(n_tiles);
+        std::vector<std::vector<uint32_t>> recs(n_tiles);
+        std::vector<std::array<uint32_t, 32>> states(n_tiles);
+        int64_t raw_total = 0;
+        if (!mul_ok(n_tiles, raw_tile, &raw_total)) {
+            delete m;
+            return EC_ERR_OVERFLOW;
+        }
+        std::vector<uint8_t> raw((size_t)raw_total, 0);
+        const uint64_t unit = uint64_t(1) << (32 - b);
+        const int k = pair ? 2 : 1;
+        parallel_for(n_tiles, [&](int64_t lo, int64_t hi) {
+            std::vector<uint16_t> stack;
+            std::vector<uint16_t> v(T);
+            for (int64_t tt = lo; tt < hi; ++tt) {
+                const int64_t base = tt * T, n_t = std::min<int64_t>(T, n_pad - base), S = n_t / 32;
+                gather_padded(w, K, KP, base, n_t, v.data());
+                auto rk = [&](int64_t q) {
+                    const int r = rank[(v[q] >> 7) & 0xFF];
+                    return r < 0 ? 0 : r;
+                };
+                for (int64_t q = 0; q < n_t; ++q)
+                    if (rank[(v[q] >> 7) & 0xFF] < 0) recs[tt].push_back((uint32_t)q | ((uint32_t)v[q] << 16));
+                /* sign / mantissa bytes of lane l's symbol i (position 32 i + l) in the
+                 * lane-transposed, pair-shuffled layout of the Huffman tiles */
+                uint8_t* rt = raw.data() + tt * raw_tile;
+                for (int64_t q = 0; q < n_t; ++q) {
+                    const int64_t l = q & 31, i = q >> 5;
+                    const uint8_t sg = (uint8_t)((v[q] >> 8) & 0x80), mt = (uint8_t)(v[q] & 0x7F);
+                    uint8_t* g = rt + ((i >> 4) * 32 + l) * 16 + (i & 12);
+                    switch (i & 3) {
+                        case 0: g[0] |= mt; g[1] |= sg; break;
+                        case 1: g[2] |= mt; g[3] |= sg; break;
+                        case 2: g[1] |= mt; g[2] |= sg; break;
+                        default: g[3] |= mt; g[0] |= sg; break;
+                    }
+                }
+                uint64_t x[32];
+                for (int l = 0; l < 32; ++l) x[l] = 1u << 16;
+                stack.clear();
+                for (int64_t j = S / k - 1; j >= 0; --j)
+                    for (int l = 31; l >= 0; --l) {
+                        const int s = pair ? 16 * rk(64 * j + l) + rk(64 * j + 32 + l) : rk(32 * j + l);
+                        const uint64_t f = m->freqs[s];
+                        if (x[l] >= f * unit) {
+                            stack.push_back((uint16_t)x[l]);
+                            x[l] >>= 16;
+                        }
+                        x[l] = ((x[l] / f) << b) + x[l] % f + cum[s];
+                    }
+                for (int l = 0; l < 32; ++l) states[tt][l] = (uint32_t)x[l];
+                words[tt].assign(stack.rbegin(), stack.rend());
+            }
+        });
+        std::vector<uint32_t> tile_off(n_tiles + 1, 0), esc_off(n_tiles + 1, 0);
+        int64_t total = 0, max_words = 0, payload = 0, n_esc = 0;
+        for (int64_t tt = 0; tt < n_tiles; ++tt) {
+            tile_off[tt] = (uint32_t)(total / 16);
+            total += 128 + round_up(2 * (int64_t)words[tt].size(), 16);
+            max_words = std::max<int64_t>(max_words, (int64_t)words[tt].size());
+            payload += 16 * (int64_t)words[tt].size();
+            esc_off[tt] = (uint32_t)n_esc;
+            n_esc += (int64_t)recs[tt].size();
+        }
+        if (total / 16 > (int64_t)UINT32_MAX || n_esc > (int64_t)UINT32_MAX) {
+            delete m;
+            return EC_ERR_OVERFLOW;
+        }
+        tile_off[n_tiles] = (uint32_t)(total / 16);
+        esc_off[n_tiles] = (uint32_t)n_esc;
+
+        ec_blob_header h{};
+        h.magic = EC_BLOB_MAGIC;
+        h.version = EC_BLOB_VERSION;
+        h.kind = EC_KIND_RANS_EXP;
+        h.steps = T / 32;
+        h.n_rows = n_rows;
+        h.k_cols = k_cols;
+        h.k_pad = KP;
+        h.n_tiles = n_tiles;
+        h.table_off = sizeof(ec_blob_header);
+        h.table_words = (int64_t)M + 256;
+        h.scales_off = round_up(h.table_off + 4 * h.table_words, 16); /* the sign / mantissa section */
+        h.tile_off_off = round_up(h.scales_off + raw_total, 16);
+        h.esc_off_off = round_up(h.tile_off_off + 4 * (n_tiles + 1), 16);
+        h.esc_records_off = round_up(h.esc_off_off + 4 * (n_tiles + 1), 16);
+        h.records_off = round_up(h.esc_records_off + 4 * n_esc, 16);
+        h.blob_bytes = h.records_off + total;
+        h.prob_bits = b;
+        h.max_words = (int32_t)max_words;
+        h.rans_tuple = k;
+        h.fp8_table_size = tsize;
+        h.n_escapes = n_esc;
+
+        std::vector<uint8_t> blob((size_t)h.blob_bytes, 0);
+        std::memcpy(blob.data(), &h, sizeof h);
+        std::memcpy(blob.data() + h.table_off, table.data(), 4 * table.size());
+        if (raw_total) std::memcpy(blob.data() + h.scales_off, raw.data(), (size_t)raw_total);
+        std::memcpy(blob.data() + h.tile_off_off, tile_off.data(), 4 * tile_off.size());
+        std::memcpy(blob.data() + h.esc_off_off, esc_off.data(), 4 * esc_off.size());
+        parallel_for(n_tiles, [&](int64_t lo, int64_t hi) {
+            for (int64_t tt = lo; tt < hi; ++tt) {
+                uint8_t* rec = blob.data() + h.records_off + (int64_t)tile_off[tt] * 16;
+                std::memcpy(rec, states[tt].data(), 128);
+                if (!words[tt].empty()) std::memcpy(rec + 128, words[tt].data(), 2 * words[tt].size());
+                if (!recs[tt].empty())
+                    std::memcpy(blob.data() + h.esc_records_off + 4 * (int64_t)esc_off[tt], recs[tt].data(),
+                                4 * recs[tt].size());
+            }
+        });
+        m->kind = EC_KIND_RANS_EXP;
+        m->device = device;
+        m->hdr = h;
+        m->payload_bits = payload + 32 * n_esc;
+        m->raw_bytes = n_pad;
+        m->table_bytes = 4 * h.table_words;
+        m->aux_bytes = h.blob_bytes - m->table_bytes - payload / 8 - n_pad;
+        m->entropy = entropy_bits(hist, 256); /* bits per exponent */
+        int rc = upload(m, blob, device);
+        if (rc != EC_OK) {
+            delete m;
+            return rc;
+        }
+        *out = m;
+        return EC_OK;
+    });
+}
+
 /* ======================================================= bookkeeping entry points */
 extern "C" int ec_stats(const ec_matrix* m, ec_stats_t* s) {
     if (!m || !s) return EC_ERR_INVALID_ARG;
@@ -1321,10 +1591,11 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
     if (h.magic != EC_BLOB_MAGIC || h.version != EC_BLOB_VERSION) return EC_ERR_CORRUPT;
     if (h.blob_bytes != bytes) return EC_ERR_CORRUPT;
     if (h.kind != EC_KIND_HUFFMAN_BF16 && h.kind != EC_KIND_RANS_INT4 && h.kind != EC_KIND_E8 &&
-        h.kind != EC_KIND_RANS_FP8)
+        h.kind != EC_KIND_RANS_FP8 && h.kind != EC_KIND_RANS_EXP)
         return EC_ERR_CORRUPT;
     if (h.n_rows < 0 || h.k_cols < 0 || h.k_cols > INT64_MAX / 2) return EC_ERR_CORRUPT;
-    const bool huff = h.kind == EC_KIND_HUFFMAN_BF16, e8 = h.kind == EC_KIND_E8, fp8 = h.kind == EC_KIND_RANS_FP8;
+    const bool huff = h.kind == EC_KIND_HUFFMAN_BF16, e8 = h.kind == EC_KIND_E8, fp8 = h.kind == EC_KIND_RANS_FP8,
+               ex = h.kind == EC_KIND_RANS_EXP;
     const int64_t align = huff ? EC_HUFF_ROW_ALIGN : e8 ? EC_E8_ROW_ALIGN : EC_RANS_ROW_ALIGN;
     if (h.k_pad != round_up(h.k_cols, align)) return EC_ERR_CORRUPT;
     if (e8 ? (h.k_cols % 8 || h.steps < 1 || h.steps > 32)
@@ -1336,7 +1607,7 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
     if (h.n_tiles != (n_pad + T - 1) / T) return EC_ERR_CORRUPT;
     if (h.table_off != (int64_t)sizeof(ec_blob_header)) return EC_ERR_CORRUPT;
     int64_t end = 0, t4 = 0;
-    const bool hrec = huff && h.huff_flags == EC_HUFF_WINDOW_REC, recs = fp8;
+    const bool hrec = huff && h.huff_flags == EC_HUFF_WINDOW_REC, recs = fp8 || ex;
     if (huff) {
         if (h.huff_flags != 0 && h.huff_flags != EC_HUFF_WINDOW_REC) return EC_ERR_CORRUPT;
         if (h.huff_sub_tables < 0 || h.huff_sub_tables > 512 || (hrec && h.huff_sub_tables != 0) ||
@@ -1356,6 +1627,11 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
             h.table_words != (int64_t(1) << h.prob_bits) + EC_FP8_VALUE_WORDS || h.fp8_table_size < 1 ||
             h.fp8_table_size > 256 || (32 * (int64_t)h.steps) > 4096 || h.n_escapes < 0)
             return EC_ERR_CORRUPT;
+    } else if (ex) {
+        if (h.prob_bits < 9 || h.prob_bits > 12 || h.max_words < 0 || (h.rans_tuple != 1 && h.rans_tuple != 2) ||
+            h.table_words != (int64_t(1) << h.prob_bits) + 256 || h.fp8_table_size < 1 ||
+            h.fp8_table_size > (h.rans_tuple == 2 ? 16 : 256) || (32 * (int64_t)h.steps) > 4096 || h.n_escapes < 0)
+            return EC_ERR_CORRUPT;
     } else {
         if (h.prob_bits < 9 || h.prob_bits > 15 || h.table_words != (int64_t(1) << h.prob_bits) || h.max_words < 0)
             return EC_ERR_CORRUPT;
@@ -1363,9 +1639,10 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
         if (h.rans_tuple == 2 && h.prob_bits > 12) return EC_ERR_CORRUPT;
     }
     if (!mul_ok(h.table_words, 4, &t4) || !add_ok(h.table_off, t4, &end)) return EC_ERR_CORRUPT;
-    if (!huff) { /* rANS: FP16 group scales; E8 and FP8: FP32 row scales */
+    if (!huff) { /* rANS: FP16 group scales; E8 and FP8: FP32 row scales; exponents: sign / mantissa bytes */
         int64_t ns = 0, s2 = 0;
-        if (e8 || fp8 ? !mul_ok(h.n_rows, 4, &s2) : (!mul_ok(h.n_rows, h.k_pad / 128, &ns) || !mul_ok(ns, 2, &s2)))
+        if (ex ? !mul_ok(h.n_tiles, EC_RAW_BYTES(h.steps), &s2)
+               : e8 || fp8 ? !mul_ok(h.n_rows, 4, &s2) : (!mul_ok(h.n_rows, h.k_pad / 128, &ns) || !mul_ok(ns, 2, &s2)))
             return EC_ERR_CORRUPT;
         if (h.scales_off < end || h.scales_off % 16 || !add_ok(h.scales_off, s2, &end)) return EC_ERR_CORRUPT;
     }
@@ -1418,7 +1695,7 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
             const int64_t n_t = std::min(T, n_pad - t * T);
             for (uint32_t e = eo[t]; e < eo[t + 1]; ++e) {
                 const uint32_t p = er[e] & 0xFFFFu;
-                if ((int64_t)p >= n_t || (er[e] >> 24) || (e > eo[t] && p <= (er[e - 1] & 0xFFFFu)))
+                if ((int64_t)p >= n_t || (fp8 && (er[e] >> 24)) || (e > eo[t] && p <= (er[e - 1] & 0xFFFFu)))
                     return EC_ERR_CORRUPT;
             }
         }
@@ -1465,6 +1742,15 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
             const uint32_t f = (tab[i] >> 20) + 1, k = (tab[i] >> 8) & 0xFFF;
             if ((int32_t)(tab[i] & 0xFF) >= h.fp8_table_size || f > (1u << h.prob_bits) || k >= f) return EC_ERR_CORRUPT;
         }
+    } else if (ex) { /* pair-layout entries (pair symbols inside the t x t square); the pairs'
+                      * exponent fields hold nothing else */
+        const uint32_t M = 1u << h.prob_bits, ts = (uint32_t)h.fp8_table_size;
+        for (uint32_t i = 0; i < M; ++i) {
+            const uint32_t f = (tab[i] >> 20) + 1, k = (tab[i] >> 8) & 0xFFF, s = tab[i] & 0xFF;
+            if (f > M || k >= f || (h.rans_tuple == 2 && ((s >> 4) >= ts || (s & 15) >= ts))) return EC_ERR_CORRUPT;
+        }
+        for (uint32_t i = 0; i < 256; ++i)
+            if (tab[M + i] & ~0x7F807F80u) return EC_ERR_CORRUPT;
     } else if (h.rans_tuple == 1) {
         for (int64_t i = 0; i < h.table_words && n_pad > 0; ++i) { /* an empty matrix has an empty table */
             const uint32_t f = tab[i] >> 16, k = (tab[i] >> 4) & 0xFFF;

@@ -171,6 +171,33 @@ struct Fp8Args {
     int* status;
 };
 
+/* A BF16 matrix whose exponents are rANS symbols under a top-t table (kind 5). */
+struct ExpMat {
+    const uint8_t* records;
+    const uint32_t* tile_off;
+    const uint32_t* table;      /* 2^prob_bits slot entries, then 256 exponent pairs */
+    const uint8_t* raw;         /* sign / mantissa bytes, raw_tile bytes per tile */
+    const uint32_t* esc_off;    /* [n_tiles + 1] record index */
+    const uint32_t* esc;        /* position in the tile | BF16 pattern << 16 */
+    float* y;
+    uint16_t* out;
+    int64_t n_rows, k_cols, k_pad;
+    int64_t n_tiles;
+    int64_t records_bytes;
+    int32_t steps, prob_bits, atomic_y, words_cap;
+    int32_t last_steps;
+    uint32_t rec16;
+    int32_t raw_tile;
+    int32_t tuple;              /* exponents per symbol: 1 or 2 */
+};
+
+struct ExpArgs {
+    ExpMat m;
+    int batch;
+    const uint16_t* x;
+    int* status;
+};
+
 /* E8 lattice matrix (decode only). */
 struct E8Mat {
     const uint8_t* records;
@@ -2171,6 +2198,225 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) fp8_kernel(const __
     }
 }
 
+/* ================================================== BF16 exponents through rANS */
+/*
+ * Kind 5 (MINE section 4, BF16 handling): the exponents of a tile's 32 lanes are
+ * rANS symbols under a top-t table -- one exponent per symbol, or the exponents of
+ * a lane's steps 2m and 2m + 1 ("Pair") -- and sign and mantissa are a plain byte
+ * per weight, lane-transposed and pair-shuffled as in the Huffman tiles, so that
+ * for every group of four lane steps one 32-bit word r holds [w(i+1) | w(i)] under
+ * the mask 0x807F807F and [w(i+3) | w(i+2)] under the same mask after rotating by 8
+ * bits.  A step: slot entry e = table[x mod 2^b], state update x = f (x >> b) +
+ * (slot - cum), ballot + popc refill from the staged words (as the other rANS
+ * kernels).  Single symbols carry the exponent in e's low byte; pair symbols index
+ * a 256-entry table of exponent pairs already in BF16 position.
+ *
+ * GEMV: x sits in shared memory permuted per 128-column block, x'[128 k + 4 l + s] =
+ * x[128 k + 32 s + l], so that lane l reads the x of its four steps in a block as
+ * one 8-byte load; two FMA chains per batch row take the weight pairs.  A weight
+ * whose exponent is outside the table was decoded with exponent 0; its record
+ * (position | true BF16 << 16) adds (w - w_coded) x to the lane's sums before the
+ * row's warp reduction, so no record needs an atomic of its own.
+ */
+/* x [batch, K] into shared rows of k_pad entries in the per-128-column permuted
+ * order above (zero past K). */
+__device__ __forceinline__ void stage_x_perm(uint16_t* xs, const uint16_t* __restrict__ x, int batch, int64_t K,
+                                             uint32_t kp) {
+    const uint32_t n = (uint32_t)batch * kp;
+    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
+        const uint32_t b = i / kp, q = i - b * kp, blk = q & ~127u, r = q & 127u;
+        const uint32_t c = blk + 32u * (r & 3u) + (r >> 2);
+        xs[i] = c < (uint32_t)K ? __ldg(x + (int64_t)b * K + c) : (uint16_t)0;
+    }
+}
+
+/* x'-index of column c (the permutation above). */
+__device__ __forceinline__ uint32_t x_perm_index(uint32_t c) { return (c & ~127u) + 4u * (c & 31u) + ((c >> 5) & 3u); }
+
+template <bool kGemv, int B, bool kPair>
+__global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) exp_kernel(const __grid_constant__ ExpArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const ExpMat& M = a.m;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+    const uint32_t kp = (uint32_t)M.k_pad;
+    const int64_t K = M.k_cols;
+    const int pb = M.prob_bits;
+    const uint32_t mask_b = (1u << pb) - 1;
+    const int batch = kGemv ? a.batch : 0;
+    const uint32_t tab_s = smem_u32(smem), vals_s = tab_s + (4u << pb);
+    const size_t tab_bytes = ((size_t)4 << pb) + 1024;
+    uint16_t* xs = (uint16_t*)(smem + tab_bytes);
+    const uint32_t xs_s = smem_u32(xs);
+    const uint32_t buf_bytes = (uint32_t)rans_buf_bytes(M.words_cap);
+    const uint32_t bufs = xs_s + (uint32_t)(2 * (size_t)batch * kp) + (uint32_t)warp * 2 * buf_bytes;
+    const uint32_t cap = (buf_bytes - 128) / 2 - 1;
+    const int64_t T = 32 * (int64_t)M.steps;
+
+    const int64_t gw = (int64_t)blockIdx.x * nwarp + warp, nw = (int64_t)gridDim.x * nwarp;
+    RansTile cur{};
+    if (gw < M.n_tiles) {
+        cur = rans_tile(M, gw, make_uint2(__ldg(M.tile_off + gw), __ldg(M.tile_off + gw + 1)));
+        rans_prefetch(bufs, cur, lane);
+    }
+    {
+        const uint4* src = (const uint4*)M.table;
+        uint4* dst = (uint4*)smem;
+        for (int i = threadIdx.x; i < (int)(tab_bytes / 16); i += blockDim.x) dst[i] = __ldg(src + i);
+    }
+    grid_dep_launch();
+    grid_dep_wait(); /* x, y and out belong to the preceding kernel in the stream from here on */
+    if (kGemv) stage_x_perm(xs, a.x, batch, K, kp);
+    __syncthreads();
+    if (gw >= M.n_tiles) return;
+
+    uint2 off_next = gw + nw < M.n_tiles ? make_uint2(__ldg(M.tile_off + gw + nw), __ldg(M.tile_off + gw + nw + 1))
+                                         : make_uint2(0u, 0u);
+    const uint32_t lt = (1u << lane) - 1u;
+    uint32_t cb = bufs;
+    for (int64_t t = gw; t < M.n_tiles; t += nw) {
+        cp_async_wait_all();
+        __syncwarp();
+        const uint32_t nb_buf = cb == bufs ? bufs + buf_bytes : bufs;
+        RansTile nxt{};
+        if (t + nw < M.n_tiles) {
+            nxt = rans_tile(M, t + nw, off_next);
+            rans_prefetch(nb_buf, nxt, lane);
+            if (t + 2 * nw < M.n_tiles)
+                off_next = make_uint2(__ldg(M.tile_off + t + 2 * nw), __ldg(M.tile_off + t + 2 * nw + 1));
+        }
+        if (cur.words < 0) {
+            if (lane == 0) flag_corrupt(a.status);
+        } else {
+            uint32_t x = lds32(cb + 4 * lane);
+            const uint32_t wbase = cb + 128;
+            uint32_t wp = 0;
+            int64_t row = tile_row(t, T, kp, EC_RANS_ROW_ALIGN);
+            uint32_t col0 = (uint32_t)(t * T - row * (int64_t)kp); /* first column of the current 128-block */
+            const uint32_t n_t = 32u * (uint32_t)cur.S;
+            const uint32_t e_begin = __ldg(M.esc_off + t), e_end = __ldg(M.esc_off + t + 1);
+            uint32_t er = e_begin; /* the tile's next record not yet folded in */
+            float acc[B][2];
+#pragma unroll
+            for (int b = 0; b < B; ++b) acc[b][0] = acc[b][1] = 0.f;
+            /* the records of positions below p_end (the current row's end in the tile),
+             * then the warp's sums of the row */
+            auto flush = [&](uint32_t p_end) {
+                const int64_t q0 = t * T - row * (int64_t)kp; /* column of tile position 0 in this row */
+                while (er < e_end) {
+                    const uint32_t j = er + (uint32_t)lane;
+                    const uint32_t rec = j < e_end ? __ldg(M.esc + j) : 0xFFFFFFFFu, p = rec & 0xFFFFu;
+                    const bool in = j < e_end && p < p_end;
+                    if (in) {
+                        if (p >= n_t) {
+                            flag_corrupt(a.status);
+                        } else {
+                            const uint32_t c = (uint32_t)(q0 + p), wt = rec >> 16, wd = wt & 0x807Fu;
+#pragma unroll
+                            for (int b = 0; b < B; ++b) {
+                                if (B > 1 && b >= batch) break;
+                                const uint32_t xv = xs[(size_t)b * kp + x_perm_index(c)];
+                                acc[b][0] = fma1_bf16(wt, xv, acc[b][0]);
+                                acc[b][1] = fma1_bf16(wd ^ 0x8000u, xv, acc[b][1]); /* - w_coded x */
+                            }
+                        }
+                    }
+                    const uint32_t nin = (uint32_t)__popc(__ballot_sync(kFull, in));
+                    er += nin;
+                    if (nin < 32) break;
+                }
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                    if (B > 1 && b >= batch) break;
+                    const float v = warp_sum(acc[b][0] + acc[b][1]);
+                    if (lane == 0) {
+                        float* dst = M.y + (int64_t)b * M.n_rows + row;
+                        if (M.atomic_y) atomicAdd(dst, v);
+                        else *dst = v;
+                    }
+                    acc[b][0] = acc[b][1] = 0.f;
+                }
+            };
+            /* one rANS step: the slot entry of the decoded symbol */
+            auto step = [&]() {
+                const uint32_t e = lds32(tab_s + ((x & mask_b) << 2));
+                const uint32_t X = x >> pb;
+                x = (e >> 20) * X + X + ((e >> 8) & 0xFFFu);
+                const bool need = x < 65536u;
+                const uint32_t bal = __ballot_sync(kFull, need);
+                const uint32_t idx = min(wp + __popc(bal & lt), cap);
+                const uint32_t v = lds16_if(need, wbase + 2 * idx, 0u);
+                x = need ? x * 65536u + v : x;
+                wp += __popc(bal);
+                return e;
+            };
+            const uint4* rawp = (const uint4*)(M.raw + t * (int64_t)M.raw_tile) + lane;
+            const int ng = cur.S / 4; /* groups of four lane steps: 128 columns each */
+            uint4 rq = __ldg(rawp), rn = ng > 4 ? __ldg(rawp + 32) : make_uint4(0u, 0u, 0u, 0u);
+            for (int gi = 0; gi < ng; ++gi) {
+                if (col0 >= kp) { /* rows start on 128-column boundaries */
+                    if (kGemv) flush(128u * (uint32_t)gi);
+                    col0 -= kp;
+                    ++row;
+                }
+                const uint32_t r = (gi & 3) == 0 ? rq.x : (gi & 3) == 1 ? rq.y : (gi & 3) == 2 ? rq.z : rq.w;
+                if ((gi & 3) == 3) {
+                    rq = rn;
+                    if (gi + 5 < ng) rn = __ldg(rawp + 32 * ((gi + 5) >> 2));
+                }
+                uint32_t E01, E23;
+                if (kPair) {
+                    E01 = lds32(vals_s + ((step() & 0xFFu) << 2));
+                    E23 = lds32(vals_s + ((step() & 0xFFu) << 2));
+                } else {
+                    const uint32_t e0 = step() & 0xFFu, e1 = step() & 0xFFu, e2 = step() & 0xFFu, e3 = step() & 0xFFu;
+                    E01 = (e0 << 7) | (e1 << 23);
+                    E23 = (e2 << 7) | (e3 << 23);
+                }
+                const uint32_t W01 = (r & kSignMant) | E01, W23 = (__funnelshift_r(r, r, 8) & kSignMant) | E23;
+                if (kGemv) {
+#pragma unroll
+                    for (int b = 0; b < B; ++b) {
+                        if (B > 1 && b >= batch) break;
+                        uint2 xv;
+                        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                                     : "=r"(xv.x), "=r"(xv.y)
+                                     : "r"(xs_s + 2u * ((uint32_t)b * kp + col0 + 4u * (uint32_t)lane)));
+                        fma2x_bf16(W01, xv.x, acc[b][0], acc[b][1]);
+                        fma2x_bf16(W23, xv.y, acc[b][0], acc[b][1]);
+                    }
+                } else {
+                    const uint32_t c = col0 + (uint32_t)lane;
+                    uint16_t* o = M.out + row * K;
+                    if (c < K) o[c] = (uint16_t)W01;
+                    if (c + 32 < K) o[c + 32] = (uint16_t)(W01 >> 16);
+                    if (c + 64 < K) o[c + 64] = (uint16_t)W23;
+                    if (c + 96 < K) o[c + 96] = (uint16_t)(W23 >> 16);
+                }
+                col0 += 128;
+            }
+            if (__any_sync(kFull, x != 65536u) || wp > (uint32_t)cur.words || (uint32_t)cur.words - wp > 7) {
+                if (lane == 0) flag_corrupt(a.status);
+            }
+            if (kGemv) {
+                flush(n_t);
+            } else { /* the tile's records, after its own stores */
+                __syncwarp();
+                for (uint32_t e = e_begin + lane; e < e_end; e += 32) {
+                    const uint32_t rec = __ldg(M.esc + e), p = rec & 0xFFFFu;
+                    if (p >= n_t) {
+                        flag_corrupt(a.status);
+                        continue;
+                    }
+                    const int64_t q = t * T + p, rr = q / (int64_t)kp, cc = q - rr * (int64_t)kp;
+                    if (cc < K) M.out[rr * K + cc] = (uint16_t)(rec >> 16);
+                }
+            }
+        }
+        cur = nxt;
+        cb = nb_buf;
+    }
+}
+
 /* ======================================================== BF16 GEMV comparator */
 constexpr int kRowsPerWarp = 4;
 
@@ -2630,6 +2876,32 @@ Fp8Mat fp8_desc(const ec_matrix* W) {
     return m;
 }
 
+ExpMat exp_desc(const ec_matrix* W) {
+    ExpMat m{};
+    const ec_blob_header& h = W->hdr;
+    m.records = W->d_blob + h.records_off;
+    m.tile_off = (const uint32_t*)(W->d_blob + h.tile_off_off);
+    m.table = (const uint32_t*)(W->d_blob + h.table_off);
+    m.raw = W->d_blob + h.scales_off;
+    m.esc_off = (const uint32_t*)(W->d_blob + h.esc_off_off);
+    m.esc = (const uint32_t*)(W->d_blob + h.esc_records_off);
+    m.n_rows = h.n_rows;
+    m.k_cols = h.k_cols;
+    m.k_pad = h.k_pad;
+    m.n_tiles = h.n_tiles;
+    m.records_bytes = h.blob_bytes - h.records_off;
+    m.steps = h.steps;
+    m.prob_bits = h.prob_bits;
+    const int64_t T = 32 * (int64_t)h.steps;
+    m.atomic_y = (h.k_pad > 0 && T % h.k_pad == 0) ? 0 : 1;
+    m.words_cap = (h.max_words + 7) / 8 * 8;
+    m.last_steps = h.n_tiles > 0 ? (int32_t)((h.n_rows * h.k_pad - (h.n_tiles - 1) * T) / 32) : 0;
+    m.rec16 = (uint32_t)(m.records_bytes / 16);
+    m.raw_tile = EC_RAW_BYTES(h.steps);
+    m.tuple = h.rans_tuple;
+    return m;
+}
+
 /* ---- E8 decode: begin ---- */
 E8Mat e8_desc(const ec_matrix* W) {
     E8Mat m{};
@@ -3050,6 +3322,64 @@ int fp8_run(const ec_matrix* W, const uint16_t* x, float* y, uint16_t* out, int 
     return EC_OK;
 }
 
+template <bool G, int B, bool P>
+int launch_exp_b(const ExpArgs& a, size_t smem, int grid, int block, cudaStream_t s) {
+    if (set_smem(exp_kernel<G, B, P>, smem) != EC_OK) return EC_ERR_CUDA;
+    return launch_ex(exp_kernel<G, B, P>, grid, block, smem, s, a);
+}
+
+template <bool P>
+int launch_exp_p(bool gemv, const ExpArgs& a, size_t smem, int grid, int block, cudaStream_t s) {
+    if (!gemv) return launch_exp_b<false, 1, P>(a, smem, grid, block, s);
+    if (a.batch <= 1) return launch_exp_b<true, 1, P>(a, smem, grid, block, s);
+    if (a.batch <= 2) return launch_exp_b<true, 2, P>(a, smem, grid, block, s);
+    if (a.batch <= 4) return launch_exp_b<true, 4, P>(a, smem, grid, block, s);
+    if (a.batch <= 8) return launch_exp_b<true, 8, P>(a, smem, grid, block, s);
+    return launch_exp_b<true, 16, P>(a, smem, grid, block, s);
+}
+
+/* Exponent-coded GEMV (y != nullptr) or decode: one CTA per SM with the slot table,
+ * the exponent pairs and x in shared memory, two tile buffers per warp; batch rows in
+ * passes. */
+int exp_run(const ec_matrix* W, const uint16_t* x, float* y, uint16_t* out, int batch, cudaStream_t s,
+            DeviceInfo* d) {
+    ExpArgs a{};
+    a.m = exp_desc(W);
+    a.m.y = y;
+    a.m.out = out;
+    a.status = d->status;
+    const bool gemv = y != nullptr;
+    if (gemv && (a.m.atomic_y || W->hdr.n_tiles == 0)) {
+        if (cudaMemsetAsync(y, 0, sizeof(float) * (size_t)batch * (size_t)W->hdr.n_rows, s) != cudaSuccess)
+            return EC_ERR_CUDA;
+    }
+    if (W->hdr.n_tiles == 0) return EC_OK;
+    const size_t table = ((size_t)4 << a.m.prob_bits) + 1024;
+    const size_t per_warp = 2 * rans_buf_bytes(a.m.words_cap);
+    const int64_t kp = W->hdr.k_pad, K = W->hdr.k_cols;
+    const size_t xrow = gemv ? (size_t)2 * kp : 0;
+    if (table + xrow + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED;
+    const int cap = gemv ? rans_max_warps(batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : batch <= 8 ? 8 : 16)
+                         : rans_max_warps(1);
+    const int warps = (int)std::min<size_t>(cap, (d->smem_optin - table - xrow) / per_warp);
+    const size_t fixed = table + (size_t)warps * per_warp;
+    const int per_pass = gemv ? (int)std::min<size_t>(std::min(batch, kFmaMaxRows), (d->smem_optin - fixed) / xrow) : 1;
+    if (per_pass < 1) return EC_ERR_UNSUPPORTED;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(d->sms, (W->hdr.n_tiles + warps - 1) / warps));
+    const int passes = gemv ? batch : 1;
+    for (int b0 = 0; b0 < passes; b0 += per_pass) {
+        const int nb = gemv ? std::min(per_pass, batch - b0) : 0;
+        a.batch = nb;
+        a.x = gemv ? x + (int64_t)b0 * K : nullptr;
+        if (gemv) a.m.y = y + (int64_t)b0 * W->hdr.n_rows;
+        const size_t sm = fixed + xrow * nb;
+        const int rc = a.m.tuple == 2 ? launch_exp_p<true>(gemv, a, sm, grid, warps * 32, s)
+                                      : launch_exp_p<false>(gemv, a, sm, grid, warps * 32, s);
+        if (rc != EC_OK) return rc;
+    }
+    return EC_OK;
+}
+
 /* ---- E8 decode: begin ---- */
 /* E8 decode: one CTA per SM, the 17 tables in shared memory, two tile buffers per warp. */
 /* Warps per CTA and tile buffers per warp.  Two buffers when 32 warps fit with
@@ -3368,7 +3698,8 @@ extern "C" int ec_gemv_group(const ec_matrix* const* Ws, int count, const uint16
     if (Ws[0]->kind == EC_KIND_E8) return EC_ERR_UNSUPPORTED; /* decoded to a dense matrix instead */
     if (Ws[0]->kind == EC_KIND_HUFFMAN_BF16) return huff_gemv(Ws, count, x, ys, batch, stream, dev, d);
     for (int k = 0; k < count; ++k) {
-        rc = Ws[0]->kind == EC_KIND_RANS_FP8 ? fp8_run(Ws[k], x, ys[k], nullptr, batch, stream, d)
+        rc = Ws[0]->kind == EC_KIND_RANS_FP8   ? fp8_run(Ws[k], x, ys[k], nullptr, batch, stream, d)
+             : Ws[0]->kind == EC_KIND_RANS_EXP ? exp_run(Ws[k], x, ys[k], nullptr, batch, stream, d)
                                               : rans_run(Ws[k], x, ys[k], nullptr, batch, stream, d);
         if (rc != EC_OK) return rc;
     }
@@ -3409,6 +3740,10 @@ extern "C" int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs
         if (n > 0 && (!outs[k] || !aligned16(outs[k]))) return EC_ERR_INVALID_ARG;
         if (Ws[k]->kind == EC_KIND_RANS_INT4) {
             if ((rc = rans_run(Ws[k], nullptr, nullptr, outs[k], 1, stream, d)) != EC_OK) return rc;
+            continue;
+        }
+        if (Ws[k]->kind == EC_KIND_RANS_EXP) {
+            if ((rc = exp_run(Ws[k], nullptr, nullptr, outs[k], 1, stream, d)) != EC_OK) return rc;
             continue;
         }
         if (Ws[k]->kind == EC_KIND_RANS_FP8) {
@@ -3488,6 +3823,7 @@ extern "C" int ec_gemm(const ec_matrix* W, const uint16_t* x, float* y, int batc
     if (!huff) { /* one chunk: the whole matrix through its own decoder */
         rc = W->kind == EC_KIND_RANS_INT4  ? rans_run(W, nullptr, nullptr, chunk, 1, stream, d)
              : W->kind == EC_KIND_RANS_FP8 ? fp8_run(W, nullptr, nullptr, chunk, 1, stream, d)
+             : W->kind == EC_KIND_RANS_EXP ? exp_run(W, nullptr, nullptr, chunk, 1, stream, d)
                                            : e8_run(W, chunk, EC_DTYPE_BF16, stream, d);
         if (rc != EC_OK) return rc;
         return gemm_run(chunk, h.n_rows, K, K, xs, xld, batch, y, h.n_rows, 0, part, pp.part_cap, stream, d);
