@@ -492,7 +492,8 @@ def batch_sweep(torch, ec, stack, stream, device):
     """Fused GEMV over the 8B layer set at batch 1 .. 64 (layers 0 and 1 of the stack
     alternately, 600 MB, so repeated replays do not run from L2), with the kernel
     family the library picks at each batch (CUDA cores, or from batch 6 the tensor
-    cores), and the same layer set coded with the 24-bit length limit at batch 1."""
+    cores), the same layer set coded with the 24-bit length limit at batch 1, and
+    the same layer set through the rANS exponent codec at batch 1."""
     import synth
     dev = f"cuda:{device}"
     n_l = min(2, stack.n_layers)
@@ -548,17 +549,19 @@ def batch_sweep(torch, ec, stack, stream, device):
                 for gname, gn in Stack.GROUPS:
                     for n in gn:
                         F.linear(xs[(l, gname)], stack.bf16[l][n].view(bf))
-        # the library's prefill route (ec_gemm: decode into the work buffer, then the
-        # tcgen05 GEMM) and that GEMM alone on the uncompressed weights
+        # the library's prefill route (ec_gemm_group per layer: the layer decoded into
+        # the work buffer in one launch, then the tcgen05 GEMMs) and that GEMM alone on
+        # the uncompressed weights
         ys = {(l, n): torch.empty((b, s.n_rows), device=dev) for l in range(n_l) for n, s in stack.specs[l].items()}
-        wb = max(ec.gemm_work_bytes(stack.mats[l][n], b) for l in range(n_l) for n in stack.specs[l])
+        order = [(gname, n) for gname, gn in Stack.GROUPS for n in gn]
+        wb = max(ec.gemm_group_work_bytes([stack.mats[l][n] for _, n in order], b) for l in range(n_l))
         work = torch.empty(wb, dtype=torch.uint8, device=dev)
 
-        def run_gemm(b=b, xs=xs, ys=ys, work=work):
-            for l in range(n_l):
-                for gname, gn in Stack.GROUPS:
-                    for n in gn:
-                        ec.gemm(stack.mats[l][n], xs[(l, gname)].view(torch.int16), ys[(l, n)], b, work=work)
+        def run_gemm(b=b, xs=xs, ys=ys, work=work, order=order):
+            for l in range(n_l):  # one ec_gemm_group per layer: the block decoded in one launch
+                ec.gemm_group([stack.mats[l][n] for _, n in order],
+                              [xs[(l, g)].view(torch.int16) for g, _ in order], [ys[(l, n)] for _, n in order], b,
+                              work=work)
 
         def run_own(b=b, xs=xs, ys=ys, work=work):
             for l in range(n_l):
@@ -593,6 +596,26 @@ def batch_sweep(torch, ec, stack, stream, device):
     out["layer_set_bpw_maxlen24"] = round(8 * sum(W.stats()["device_bytes"] for m in mats24 for W in m.values())
                                           / sum(s.n_rows * s.k_cols for l in range(n_l)
                                                 for s in stack.specs[l].values()), 4)
+    # the same layer set through the rANS exponent codec (pair symbols, table size by
+    # the size bound) at batch 1, beside the Huffman walker
+    mats_x, bufs = [], []
+    for l in range(n_l):
+        specs = stack.specs[l]
+        m = {nm: ec.encode_bf16_exp(synth.make_weights(s), device=device) for nm, s in specs.items()}
+        mats_x.append(m)
+        for gname, names in Stack.GROUPS:
+            k = specs[names[0]].k_cols
+            x = torch.from_numpy(synth.make_x(specs[names[0]].seed, 1, k).view(np.int16)).to(dev)
+            ys = [torch.empty((1, specs[n].n_rows), device=dev) for n in names]
+            bufs.append(([m[n] for n in names], x, ys))
+
+    def run_exp():
+        for Ws, x, ys in bufs:
+            ec.gemv_group(Ws, x, ys, batch=1)
+    out["layer_set_us_rans_exponents"] = round(t_graph(run_exp) / n_l, 1)
+    out["layer_set_bpw_rans_exponents"] = round(8 * sum(W.stats()["device_bytes"] for m in mats_x for W in m.values())
+                                                / sum(s.n_rows * s.k_cols for l in range(n_l)
+                                                      for s in stack.specs[l].values()), 4)
     assert ec.status(stream) == 0
     return out
 

@@ -351,6 +351,19 @@ int ec_gemm(const ec_matrix* W, const uint16_t* x_bf16, float* y, int batch, voi
  * device (host only). */
 int ec_gemm_work_bytes(const ec_matrix* W, int batch, size_t* bytes);
 
+/* ec_gemm over `count` matrices (1..EC_MAX_DECODE_BATCH), ys[m] = xs[m] W_m^T at the
+ * same batch (x and y per matrix: a transformer block's matrices take different
+ * inputs).  Huffman matrices with k_cols % 8 == 0 whose decoded rows fit in `work`
+ * together (beside the partial sums) are decoded in one launch, as ec_decode_batch
+ * decodes a block (DFloat11, "Transformer-block-level decompression"), then
+ * multiplied one after the other; any other matrix goes through ec_gemm on its own,
+ * in row chunks.  ec_gemm_group_work_bytes gives the size that decodes every
+ * packable matrix in one launch; less work memory makes more launches.  Results as
+ * ec_gemm. */
+int ec_gemm_group(const ec_matrix* const* Ws, int count, const uint16_t* const* xs_bf16, float* const* ys,
+                  int batch, void* work, size_t work_bytes, cudaStream_t stream);
+int ec_gemm_group_work_bytes(const ec_matrix* const* Ws, int count, int batch, size_t* bytes);
+
 /* Uncompressed comparator for ec_gemm: y = W x for a dense BF16 W [n_rows, k_cols]
  * (k_cols % 8 == 0, else EC_ERR_UNSUPPORTED) through the same tensor-core GEMM.
  * work (may be NULL) holds partial sums when K is split: with less than

@@ -40,7 +40,8 @@ EC_KIND_RANS_EXP = 5
 EXPORTS = ["ec_encode_bf16", "ec_encode_rans", "ec_decode", "ec_decode_batch", "ec_gemv", "ec_gemv_group",
            "ec_bf16_gemv", "ec_stats", "ec_code_lengths", "ec_serialize", "ec_deserialize", "ec_status", "ec_free",
            "ec_strerror", "ec_gemv_static", "ec_gemv_path", "ec_encode_e8", "ec_decode_as", "ec_encode_fp8",
-           "ec_gemm", "ec_gemm_work_bytes", "ec_bf16_gemm", "ec_encode_bf16_exp"]
+           "ec_gemm", "ec_gemm_work_bytes", "ec_bf16_gemm", "ec_encode_bf16_exp", "ec_gemm_group",
+           "ec_gemm_group_work_bytes"]
 
 
 class HuffParams(ctypes.Structure):
@@ -95,6 +96,8 @@ _sig = {
     "ec_bf16_gemv": ([_vp, _i64, _i64, _vp, _vp, _i32, _vp], _i32),
     "ec_gemm": ([_vp, _vp, _vp, _i32, _vp, ctypes.c_size_t, _vp], _i32),
     "ec_gemm_work_bytes": ([_vp, _i32, ctypes.POINTER(ctypes.c_size_t)], _i32),
+    "ec_gemm_group": ([_vp, _i32, _vp, _vp, _i32, _vp, ctypes.c_size_t, _vp], _i32),
+    "ec_gemm_group_work_bytes": ([_vp, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)], _i32),
     "ec_bf16_gemm": ([_vp, _i64, _i64, _vp, _vp, _i32, _vp, ctypes.c_size_t, _vp], _i32),
     "ec_gemv_static": ([_vp, _vp, _vp, _i32, _vp], _i32),
     "ec_gemv_path": ([_vp, _i32, _i32], _i32),
@@ -341,6 +344,28 @@ def gemm(W: Matrix, x, y, batch: int, work=None, stream=None) -> None:
     nbytes = work.numel() * work.element_size()
     _check(lib.ec_gemm(W.handle, _dev_ptr(x), _dev_ptr(y), batch, _dev_ptr(work), nbytes, _stream_ptr(stream)),
            "ec_gemm")
+
+
+def gemm_group_work_bytes(Ws, batch: int) -> int:
+    """ec_gemm_group_work_bytes: the work buffer that decodes every packable matrix in one launch."""
+    hs = (ctypes.c_void_p * len(Ws))(*[W.handle.value for W in Ws])
+    n = ctypes.c_size_t(0)
+    _check(lib.ec_gemm_group_work_bytes(hs, len(Ws), batch, ctypes.byref(n)), "ec_gemm_group_work_bytes")
+    return int(n.value)
+
+
+def gemm_group(Ws, xs, ys, batch: int, work=None, stream=None) -> None:
+    """ec_gemm_group: ys[m] = xs[m] W_m^T for several matrices, decoded together where
+    the work buffer allows (None allocates gemm_group_work_bytes)."""
+    n = len(Ws)
+    if work is None:
+        import torch
+        work = torch.empty(gemm_group_work_bytes(Ws, batch), dtype=torch.uint8, device=ys[0].device)
+    hs = (ctypes.c_void_p * n)(*[W.handle.value for W in Ws])
+    xp = (ctypes.c_void_p * n)(*[_dev_ptr(x) for x in xs])
+    yp = (ctypes.c_void_p * n)(*[_dev_ptr(y) for y in ys])
+    nbytes = work.numel() * work.element_size()
+    _check(lib.ec_gemm_group(hs, n, xp, yp, batch, _dev_ptr(work), nbytes, _stream_ptr(stream)), "ec_gemm_group")
 
 
 def bf16_gemm(w, x, y, batch: int, work=None, stream=None) -> None:

@@ -2055,9 +2055,10 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) rans_kernel(const _
  * decode one table symbol per position (pair-layout slot entries: symbol, slot
  * bias, frequency - 1), the symbol's FP32 value feeds the FMA (GEMV) or is scaled
  * by the row scale and stored (decode); a weight outside the table was coded as
- * code 0, and after its tile the warp applies the tile's correction records: each
- * lane takes records in turn and adds r_i * value * x (GEMV, atomically) or writes
- * bf16(value * r_i) over the 0 (decode). */
+ * code 0 (value 0).  GEMV: before each row's warp reduction the lanes take that
+ * row's correction records in turn and add value * x to their own sums (the row
+ * scale then multiplies the whole sum), so no record needs an atomic of its own;
+ * decode: after its tile the warp writes bf16(value * r_i) over the 0. */
 template <bool kGemv, int B>
 __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) fp8_kernel(const __grid_constant__ Fp8Args a) {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -2121,7 +2122,35 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) fp8_kernel(const __
             float acc[B];
 #pragma unroll
             for (int b = 0; b < B; ++b) acc[b] = 0.f;
-            auto flush = [&]() {
+            const uint32_t n_t = 32u * (uint32_t)cur.S;
+            const uint32_t e_begin = __ldg(M.esc_off + t), e_end = __ldg(M.esc_off + t + 1);
+            uint32_t er = e_begin; /* the tile's next record not yet folded in */
+            /* the records of positions below p_end (the current row's end in the tile:
+             * their weights were decoded as code 0, value 0, so each adds value * x),
+             * then the warp's sums of the row, scaled by the row's r_i */
+            auto flush = [&](uint32_t p_end) {
+                const int64_t q0 = t * T - row * (int64_t)kp; /* column of tile position 0 in this row */
+                while (er < e_end) {
+                    const uint32_t j = er + (uint32_t)lane;
+                    const uint32_t rec = j < e_end ? __ldg(M.esc + j) : 0xFFFFFFFFu, p = rec & 0xFFFFu;
+                    const bool in = j < e_end && p < p_end;
+                    if (in) {
+                        if (p >= n_t) {
+                            flag_corrupt(a.status);
+                        } else {
+                            const uint32_t c = (uint32_t)(q0 + p);
+                            const float w = vals[256 + ((rec >> 16) & 0xFFu)];
+#pragma unroll
+                            for (int b = 0; b < B; ++b) {
+                                if (B > 1 && b >= batch) break;
+                                acc[b] = fmaf(w, __uint_as_float((uint32_t)xs[(size_t)b * kp + c] << 16), acc[b]);
+                            }
+                        }
+                    }
+                    const uint32_t nin = (uint32_t)__popc(__ballot_sync(kFull, in));
+                    er += nin;
+                    if (nin < 32) break;
+                }
 #pragma unroll
                 for (int b = 0; b < B; ++b) {
                     if (B > 1 && b >= batch) break;
@@ -2137,7 +2166,7 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) fp8_kernel(const __
             const int ng = cur.S / 4;
             for (int gi = 0; gi < ng; ++gi) {
                 if (col >= kp) { /* rows start on 128-column boundaries */
-                    if (kGemv) flush();
+                    if (kGemv) flush(128u * (uint32_t)gi);
                     col -= kp;
                     ++row;
                     scale = __ldg(M.row_scales + row);
@@ -2170,25 +2199,19 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) fp8_kernel(const __
             if (__any_sync(kFull, x != 65536u) || wp > (uint32_t)cur.words || (uint32_t)cur.words - wp > 7) {
                 if (lane == 0) flag_corrupt(a.status);
             }
-            if (kGemv) flush();
-            /* the tile's corrections, after its own stores and sums */
-            __syncwarp();
-            const uint32_t e0 = __ldg(M.esc_off + t), e1 = __ldg(M.esc_off + t + 1);
-            const uint32_t n_t = 32u * (uint32_t)cur.S;
-            for (uint32_t e = e0 + lane; e < e1; e += 32) {
-                const uint32_t rec = __ldg(M.esc + e), p = rec & 0xFFFFu;
-                if (p >= n_t) {
-                    flag_corrupt(a.status);
-                    continue;
-                }
-                const int64_t q = t * T + p, r = q / (int64_t)kp, cc = q - r * (int64_t)kp;
-                if (cc >= K) continue;
-                const float w = vals[256 + ((rec >> 16) & 0xFFu)], sr = __ldg(M.row_scales + r);
-                if (kGemv) {
-                    for (int b = 0; b < batch; ++b)
-                        atomicAdd(M.y + (int64_t)b * M.n_rows + r,
-                                  sr * (w * __uint_as_float((uint32_t)xs[(size_t)b * kp + cc] << 16)));
-                } else {
+            if (kGemv) {
+                flush(n_t);
+            } else { /* the tile's corrections, after its own stores */
+                __syncwarp();
+                for (uint32_t e = e_begin + lane; e < e_end; e += 32) {
+                    const uint32_t rec = __ldg(M.esc + e), p = rec & 0xFFFFu;
+                    if (p >= n_t) {
+                        flag_corrupt(a.status);
+                        continue;
+                    }
+                    const int64_t q = t * T + p, r = q / (int64_t)kp, cc = q - r * (int64_t)kp;
+                    if (cc >= K) continue;
+                    const float w = vals[256 + ((rec >> 16) & 0xFFu)], sr = __ldg(M.row_scales + r);
                     M.out[r * K + cc] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(w, sr)));
                 }
             }
@@ -3854,6 +3877,125 @@ extern "C" int ec_gemm(const ec_matrix* W, const uint16_t* x, float* y, int batc
             return rc;
     }
     return EC_OK;
+}
+
+namespace {
+/* Whether ec_gemm_group packs W with others into one decode launch. */
+bool gemm_packable(const ec_matrix* W) { return W->kind == EC_KIND_HUFFMAN_BF16 && W->hdr.k_cols % 8 == 0; }
+
+/* Partial-sum bytes the GEMM of a whole packable matrix needs at `batch`. */
+size_t gemm_part_bytes(const ec_matrix* W, int batch, const DeviceInfo& d) {
+    return plan_gemm(W->hdr.n_rows, W->hdr.k_cols, batch, d.sms, d.smem_optin, SIZE_MAX).part_bytes;
+}
+}  // namespace
+
+extern "C" int ec_gemm_group_work_bytes(const ec_matrix* const* Ws, int count, int batch, size_t* bytes) {
+    if (!Ws || !bytes || count < 1 || count > kMaxDecodeBatch || batch < 1) return EC_ERR_INVALID_ARG;
+    int dev = 0;
+    if (current_device(&dev) != EC_OK) return EC_ERR_CUDA;
+    DeviceInfo* d = nullptr;
+    int rc = device_info(dev, &d);
+    if (rc != EC_OK) return rc;
+    size_t packed = 0, part = 0, alone = 0;
+    for (int k = 0; k < count; ++k) {
+        if (!Ws[k]) return EC_ERR_INVALID_ARG;
+        if (gemm_packable(Ws[k])) {
+            packed += round256((size_t)Ws[k]->hdr.n_rows * (size_t)Ws[k]->hdr.k_cols * 2);
+            part = std::max(part, round256(gemm_part_bytes(Ws[k], batch, *d)));
+        } else {
+            PrefillPlan pp;
+            if ((rc = plan_prefill(Ws[k], batch, 0, *d, &pp)) != EC_OK) return rc;
+            alone = std::max(alone, pp.need);
+        }
+    }
+    *bytes = std::max(packed + part, alone);
+    return EC_OK;
+}
+
+extern "C" int ec_gemm_group(const ec_matrix* const* Ws, int count, const uint16_t* const* xs, float* const* ys,
+                             int batch, void* work, size_t work_bytes, cudaStream_t stream) {
+    if (!Ws || !xs || !ys || count < 1 || count > kMaxDecodeBatch || batch < 1) return EC_ERR_INVALID_ARG;
+    if (!work || !aligned16(work)) return EC_ERR_INVALID_ARG;
+    int dev = 0;
+    if (current_device(&dev) != EC_OK) return EC_ERR_CUDA;
+    DeviceInfo* d = nullptr;
+    int rc = device_info(dev, &d);
+    if (rc != EC_OK) return rc;
+    size_t part = 0;
+    for (int k = 0; k < count; ++k) {
+        if (!Ws[k] || !Ws[k]->d_blob) return EC_ERR_INVALID_ARG;
+        if ((rc = check_matrix(Ws[k], dev)) != EC_OK) return rc;
+        if (!ys[k] || !aligned16(ys[k]) || (Ws[k]->hdr.k_cols > 0 && (!xs[k] || !aligned16(xs[k]))))
+            return EC_ERR_INVALID_ARG;
+        if (gemm_packable(Ws[k])) part = std::max(part, round256(gemm_part_bytes(Ws[k], batch, *d)));
+    }
+    /* [decoded matrices of one pack | partial sums] */
+    const size_t area = work_bytes > part ? work_bytes - part : 0;
+    float* part_p = part ? (float*)((uint8_t*)work + area) : nullptr;
+    std::vector<int> pack;
+    size_t used = 0;
+    auto flush = [&]() -> int {
+        if (pack.empty()) return EC_OK;
+        HuffDecodeArgs a{};
+        int64_t total = 0;
+        int code_bytes = 16;
+        bool lng = false;
+        size_t off = 0;
+        std::vector<size_t> at;
+        for (int k : pack) {
+            const ec_matrix* W = Ws[k];
+            HuffMat m = huff_desc(W);
+            m.out = (uint16_t*)((uint8_t*)work + off);
+            m.tile_begin = total;
+            at.push_back(off);
+            off += round256((size_t)W->hdr.n_rows * (size_t)W->hdr.k_cols * 2);
+            total += W->hdr.n_tiles;
+            code_bytes = std::max(code_bytes, staged_code_bytes(W));
+            lng = lng || huff_hier(W);
+            if (huff_hier(W) && m.n_sub > 0 && m.n_sub <= kSubSmemTables) { /* one matrix at a time is resident */
+                m.sub_smem = 0;
+                a.sub_words = std::max(a.sub_words, 256 * m.n_sub);
+            }
+            a.m[a.count++] = m;
+        }
+        int r = EC_OK;
+        if (total > 0) {
+            a.total_tiles = total;
+            if ((r = launch_huff_decode(a, code_bytes, lng, stream, d)) != EC_OK) return r;
+        }
+        for (size_t i = 0; i < pack.size(); ++i) {
+            const ec_matrix* W = Ws[pack[i]];
+            const ec_blob_header& h = W->hdr;
+            if (h.n_rows == 0) continue;
+            if (h.k_cols == 0) {
+                if (cudaMemsetAsync(ys[pack[i]], 0, sizeof(float) * (size_t)batch * (size_t)h.n_rows, stream) !=
+                    cudaSuccess)
+                    return EC_ERR_CUDA;
+                continue;
+            }
+            const uint16_t* rows = (const uint16_t*)((uint8_t*)work + at[i]);
+            if ((r = gemm_run(rows, h.n_rows, h.k_cols, h.k_cols, xs[pack[i]], h.k_cols, batch, ys[pack[i]], h.n_rows,
+                              0, part_p, part, stream, d)) != EC_OK)
+                return r;
+        }
+        pack.clear();
+        used = 0;
+        return EC_OK;
+    };
+    for (int k = 0; k < count; ++k) {
+        const ec_matrix* W = Ws[k];
+        const size_t sz = gemm_packable(W) ? round256((size_t)W->hdr.n_rows * (size_t)W->hdr.k_cols * 2) : SIZE_MAX;
+        if (sz <= area) {
+            if (used + sz > area && (rc = flush()) != EC_OK) return rc;
+            pack.push_back(k);
+            used += sz;
+            continue;
+        }
+        /* alone, in row chunks of its own */
+        if ((rc = flush()) != EC_OK) return rc;
+        if ((rc = ec_gemm(W, xs[k], ys[k], batch, work, work_bytes, stream)) != EC_OK) return rc;
+    }
+    return flush();
 }
 
 extern "C" int ec_bf16_gemm(const uint16_t* w, int64_t n_rows, int64_t k_cols, const uint16_t* x, float* y, int batch,

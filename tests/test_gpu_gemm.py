@@ -162,3 +162,26 @@ def test_gemm_reports_corruption(ec):
     assert ec.status() == 0
     ec.gemm(Wc, x, y, 64)
     assert ec.status() == -5
+
+
+def test_gemm_group_matches_oracle(ec):
+    """ec_gemm_group over matrices with their own x: Huffman matrices decoded together,
+    one with K % 8 != 0 and an exponent-codec matrix taken alone; with the full work
+    buffer (one decode launch for the packable ones), then with 1.5 MB, where the pack
+    splits over several decode launches and the largest matrix, bigger than the area
+    left beside the partial sums, goes alone in row chunks."""
+    batch = 48
+    specs = [(256, 1024), (96, 1024), (300, 1000), (128, 13), (1100, 1024), (200, 1024)]
+    ws = [synth.llama_bf16(3900 + i, n, k) for i, (n, k) in enumerate(specs)]
+    Ws = [ec.encode_bf16(w) for w in ws[:5]] + [ec.encode_bf16_exp(ws[5])]
+    xs = [synth.make_x(3950 + i, batch, k) for i, (_, k) in enumerate(specs)]
+    xd = [torch.from_numpy(x.view(np.int16)).cuda() for x in xs]
+    refs = [oracle_gemm(w, x) for w, x in zip(ws, xs)]
+    full = ec.gemm_group_work_bytes(Ws, batch)
+    for work_bytes in (full, 1536 * 1024):
+        work = torch.empty(work_bytes, dtype=torch.uint8, device="cuda")
+        ys = [torch.full((batch, n), float("nan"), device="cuda") for n, _ in specs]
+        ec.gemm_group(Ws, xd, ys, batch, work=work)
+        assert ec.status() == 0
+        for i, (y, (y_ref, a_ref)) in enumerate(zip(ys, refs)):
+            check_gemv(y.cpu().numpy().astype(np.float64), y_ref, a_ref, f"group {i} work={work_bytes}")
