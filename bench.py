@@ -632,6 +632,61 @@ def aggregate_ranks(torch, dist, us_local: float, world: int, device: str):
 
 
 # ------------------------------------------------------------------ main
+PROFILE_CASES = ("gemm", "bf16_gemm", "exp", "rans_pair", "decode", "fp8_t32")
+
+
+def profile_case(name: str, batch: int) -> None:
+    """One library call on a named workload, three times, untimed: the command that
+    the ncu summaries in profiles/ capture.  gemm: ec_gemm_group over layer 0 of the
+    8B stack at `batch`; bf16_gemm: the tcgen05 GEMM on layer 0's gate matrix
+    uncompressed; exp: the rANS exponent codec's GEMV on layer 0's gate matrix; rans_pair:
+    the 4-bit pair-symbol GEMV on 14336 x 4096; decode: ec_decode_batch of layer 0;
+    fp8_t32: the FP8 GEMV with a 32-code table on 14336 x 4096."""
+    import torch
+    import lossless_entropy_coded_gb300 as ec
+    import synth
+    dev = "cuda:0"
+    specs = synth.layer_8b(0)
+    gate = [s for s in specs if s.name.endswith("gate")][0]
+
+    def xs_of(k, b=batch):
+        return torch.from_numpy(synth.make_x(k, b, k).view(np.int16)).to(dev)
+    if name == "gemm":
+        Ws = [ec.encode_bf16(synth.make_weights(s), device=0) for s in specs]
+        xs = [xs_of(s.k_cols) for s in specs]
+        ys = [torch.empty((batch, s.n_rows), device=dev) for s in specs]
+        work = torch.empty(ec.gemm_group_work_bytes(Ws, batch), dtype=torch.uint8, device=dev)
+        run = lambda: ec.gemm_group(Ws, xs, ys, batch, work=work)
+    elif name == "bf16_gemm":
+        w = torch.from_numpy(synth.make_weights(gate).view(np.int16)).to(dev)
+        x, y = xs_of(gate.k_cols), torch.empty((batch, gate.n_rows), device=dev)
+        work = torch.empty(64 << 20, dtype=torch.uint8, device=dev)
+        run = lambda: ec.bf16_gemm(w, x, y, batch, work=work)
+    elif name == "exp":
+        W = ec.encode_bf16_exp(synth.make_weights(gate), device=0)
+        x, y = xs_of(gate.k_cols, 1), torch.empty((1, gate.n_rows), device=dev)
+        run = lambda: ec.gemv(W, x, y)
+    elif name == "rans_pair":
+        codes, scales = synth.make_rans_case(0)
+        W = ec.encode_rans(codes, scales, codes_per_symbol=2, device=0)
+        x, y = xs_of(codes.shape[1], 1), torch.empty((1, codes.shape[0]), device=dev)
+        run = lambda: ec.gemv(W, x, y)
+    elif name == "decode":
+        Ws = [ec.encode_bf16(synth.make_weights(s), device=0) for s in specs]
+        outs = [torch.empty((s.n_rows, s.k_cols), dtype=torch.int16, device=dev) for s in specs]
+        run = lambda: ec.decode_batch(Ws, outs)
+    else:
+        codes, r = synth.make_fp8_case(8000, 14336, 4096)
+        W = ec.encode_fp8(codes, r, top_t=32, device=0)
+        x, y = xs_of(4096, 1), torch.empty((1, 14336), device=dev)
+        run = lambda: ec.gemv(W, x, y)
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    assert ec.status() == 0
+    print(json.dumps({"case": name, "batch": batch, "status": "ok"}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -641,7 +696,11 @@ def main():
     ap.add_argument("--layers", type=int, default=32)
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=PROFILE_CASES, help="run one named workload untimed (for ncu) and exit")
+    ap.add_argument("--batch", type=int, default=256, help="batch rows of --case gemm / bf16_gemm")
     args = ap.parse_args()
+    if args.case:
+        return profile_case(args.case, args.batch)
     args.warmup = max(3, args.warmup)
     args.warmup_ref = 0
     if args.impl == "reference":
