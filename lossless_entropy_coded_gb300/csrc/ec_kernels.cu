@@ -1842,6 +1842,21 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) huff_decode_kernel(const
     }
 }
 
+/* x [batch, K] into shared rows of k_pad entries in the per-128-column permuted
+ * order above (zero past K). */
+__device__ __forceinline__ void stage_x_perm(uint16_t* xs, const uint16_t* __restrict__ x, int batch, int64_t K,
+                                             uint32_t kp) {
+    const uint32_t n = (uint32_t)batch * kp;
+    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
+        const uint32_t b = i / kp, q = i - b * kp, blk = q & ~127u, r = q & 127u;
+        const uint32_t c = blk + 32u * (r & 3u) + (r >> 2);
+        xs[i] = c < (uint32_t)K ? __ldg(x + (int64_t)b * K + c) : (uint16_t)0;
+    }
+}
+
+/* x'-index of column c (the permutation above). */
+__device__ __forceinline__ uint32_t x_perm_index(uint32_t c) { return (c & ~127u) + 4u * (c & 31u) + ((c >> 5) & 3u); }
+
 /* ============================================================ rANS kernels */
 /*
  * One warp per 4096-symbol tile (EntroPack, independent rANS tiles): lane l holds
@@ -1912,8 +1927,10 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) rans_kernel(const _
     const int pb = M.prob_bits;
     const uint32_t mask_b = (1u << pb) - 1;
     const int batch = kGemv ? a.batch : 0;
-    const uint32_t tab_s = smem_u32(smem);
-    uint16_t* xs = (uint16_t*)(smem + ((size_t)4 << pb));
+    /* shared: slot table | (GEMV) 256 code pairs as packed BF16 | (GEMV) x, permuted per
+     * 128 columns | two tile buffers per warp */
+    const uint32_t tab_s = smem_u32(smem), lut_s = tab_s + (4u << pb);
+    uint16_t* xs = (uint16_t*)(smem + ((size_t)4 << pb) + (kGemv ? 1024 : 0));
     const uint32_t xs_s = smem_u32(xs);
     const uint32_t buf_bytes = (uint32_t)rans_buf_bytes(M.words_cap);
     const uint32_t bufs = xs_s + (uint32_t)(2 * (size_t)batch * kp) + (uint32_t)warp * 2 * buf_bytes;
@@ -1923,6 +1940,12 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) rans_kernel(const _
     const int64_t gw = (int64_t)blockIdx.x * nwarp + warp, nw = (int64_t)gridDim.x * nwarp;
     RansTile cur{};
     float sc = 0.f; /* lane g: scale of group g of the current tile */
+    if (kGemv) /* entry i: [bf16(c1) | bf16(c0)], c0 = (i >> 4) - 8 (the earlier step), c1 = (i & 15) - 8 */
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+            const uint32_t c0 = __bfloat16_as_ushort(__int2bfloat16_rn((i >> 4) - 8));
+            const uint32_t c1 = __bfloat16_as_ushort(__int2bfloat16_rn((i & 15) - 8));
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(lut_s + 4u * (uint32_t)i), "r"(c0 | (c1 << 16)) : "memory");
+        }
     if (gw < M.n_tiles) {
         cur = rans_tile(M, gw, make_uint2(__ldg(M.tile_off + gw), __ldg(M.tile_off + gw + 1)));
         rans_prefetch(bufs, cur, lane);
@@ -1936,7 +1959,7 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) rans_kernel(const _
     }
     grid_dep_launch();
     grid_dep_wait(); /* x, y and out belong to the preceding kernel in the stream from here on */
-    if (kGemv) stage_x_rows(xs, a.x, batch, K, kp);
+    if (kGemv) stage_x_perm(xs, a.x, batch, K, kp);
     __syncthreads();
     if (gw >= M.n_tiles) return;
 
@@ -1965,9 +1988,9 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) rans_kernel(const _
             uint32_t wp = 0;
             int64_t row = tile_row(t, T, kp, EC_RANS_ROW_ALIGN);
             uint32_t col = (uint32_t)(t * T - row * (int64_t)kp) + lane; /* this lane's column */
-            float acc[B], accg[B];
+            float acc[B];
 #pragma unroll
-            for (int b = 0; b < B; ++b) acc[b] = accg[b] = 0.f;
+            for (int b = 0; b < B; ++b) acc[b] = 0.f;
             auto flush = [&]() {
 #pragma unroll
                 for (int b = 0; b < B; ++b) {
@@ -1992,6 +2015,52 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) rans_kernel(const _
                     sc = lane < ng - gi ? __half2float(__ushort_as_half(__ldg(M.scales + t * (T / 128) + gi + lane)))
                                         : 0.f;
                 const float scale = __shfl_sync(kFull, sc, gi & 31);
+                if (kGemv) {
+                    /* one rANS step: the slot entry of the decoded symbol */
+                    auto step = [&]() {
+                        const uint32_t e = lds32(tab_s + ((x & mask_b) << 2));
+                        if (kPair) { /* freq - 1 in bits 20..31: f X = (f - 1) X + X */
+                            const uint32_t X = x >> pb;
+                            x = (e >> 20) * X + X + ((e >> 8) & 0xFFFu);
+                        } else {
+                            x = (e >> 16) * (x >> pb) + ((e >> 4) & 0xFFFu);
+                        }
+                        const bool need = x < 65536u;
+                        const uint32_t bal = __ballot_sync(kFull, need);
+                        const uint32_t idx = min(wp + __popc(bal & lt), cap);
+                        const uint32_t v = lds16_if(need, wbase + 2 * idx, 0u);
+                        x = need ? x * 65536u + v : x;
+                        wp += __popc(bal);
+                        return e;
+                    };
+                    /* the group's four codes (lane steps 4 gi .. 4 gi + 3, columns col + 32 k) as
+                     * two packed BF16 pairs from the code-pair table: a pair symbol's earlier
+                     * code sits in bits 4..7, a single code in bits 0..3 */
+                    uint32_t w01, w23;
+                    if (kPair) {
+                        w01 = lds32(lut_s + ((step() & 0xFFu) << 2));
+                        w23 = lds32(lut_s + ((step() & 0xFFu) << 2));
+                    } else {
+                        const uint32_t e0 = step() & 15u, e1 = step() & 15u, e2 = step() & 15u, e3 = step() & 15u;
+                        w01 = lds32(lut_s + (((e0 << 4) | e1) << 2));
+                        w23 = lds32(lut_s + (((e2 << 4) | e3) << 2));
+                    }
+                    /* x of the four columns, one 8-byte load per batch row (permuted layout);
+                     * the exact products are summed in FP32, then scaled by the group's scale */
+                    const uint32_t xa = xs_s + 2u * ((col - (uint32_t)lane) + 4u * (uint32_t)lane);
+#pragma unroll
+                    for (int b = 0; b < B; ++b) {
+                        if (B > 1 && b >= batch) break;
+                        uint2 xq;
+                        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(xq.x), "=r"(xq.y) : "r"(xa + 2u * (uint32_t)b * kp));
+                        float g0 = 0.f, g1 = 0.f;
+                        fma2x_bf16(w01, xq.x, g0, g1);
+                        fma2x_bf16(w23, xq.y, g0, g1);
+                        acc[b] = fmaf(g0 + g1, scale, acc[b]);
+                    }
+                    col += 128;
+                    continue;
+                }
 #pragma unroll
                 for (int s = 0; s < (kPair ? 2 : 4); ++s) {
                     const uint32_t e = lds32(tab_s + ((x & mask_b) << 2));
@@ -2015,24 +2084,7 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) rans_kernel(const _
                         const uint32_t nib = kPair ? (q == 0 ? (e >> 4) & 15u : e & 15u) : e & 15u;
                         const float cf = __int_as_float(0x4B000000 | nib) - 8388616.0f;
                         const uint32_t c = col + 32 * (nc * s + q);
-                        if (kGemv) {
-#pragma unroll
-                            for (int b = 0; b < B; ++b) {
-                                if (B > 1 && b >= batch) break;
-                                uint32_t xv;
-                                asm volatile("ld.shared.u16 %0, [%1];" : "=r"(xv) : "r"(xs_s + 2 * (b * kp + c)) : "memory");
-                                accg[b] = fmaf(cf, __uint_as_float(xv << 16), accg[b]);
-                            }
-                        } else if (c < K) {
-                            M.out[row * K + c] = __bfloat16_as_ushort(__float2bfloat16_rn(cf * scale));
-                        }
-                    }
-                }
-                if (kGemv) {
-#pragma unroll
-                    for (int b = 0; b < B; ++b) {
-                        acc[b] = fmaf(accg[b], scale, acc[b]);
-                        accg[b] = 0.f;
+                        if (c < K) M.out[row * K + c] = __bfloat16_as_ushort(__float2bfloat16_rn(cf * scale));
                     }
                 }
                 col += 128;
@@ -2241,21 +2293,6 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) fp8_kernel(const __
  * (position | true BF16 << 16) adds (w - w_coded) x to the lane's sums before the
  * row's warp reduction, so no record needs an atomic of its own.
  */
-/* x [batch, K] into shared rows of k_pad entries in the per-128-column permuted
- * order above (zero past K). */
-__device__ __forceinline__ void stage_x_perm(uint16_t* xs, const uint16_t* __restrict__ x, int batch, int64_t K,
-                                             uint32_t kp) {
-    const uint32_t n = (uint32_t)batch * kp;
-    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
-        const uint32_t b = i / kp, q = i - b * kp, blk = q & ~127u, r = q & 127u;
-        const uint32_t c = blk + 32u * (r & 3u) + (r >> 2);
-        xs[i] = c < (uint32_t)K ? __ldg(x + (int64_t)b * K + c) : (uint16_t)0;
-    }
-}
-
-/* x'-index of column c (the permutation above). */
-__device__ __forceinline__ uint32_t x_perm_index(uint32_t c) { return (c & ~127u) + 4u * (c & 31u) + ((c >> 5) & 3u); }
-
 template <bool kGemv, int B, bool kPair>
 __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) exp_kernel(const __grid_constant__ ExpArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -3267,8 +3304,9 @@ int rans_run(const ec_matrix* W, const uint16_t* x, float* y, uint16_t* out, int
             return EC_ERR_CUDA;
     }
     if (W->hdr.n_tiles == 0) return EC_OK;
-    /* one CTA per SM: slot table | x (BF16) [rows of this pass][k_pad] | two tile buffers per warp */
-    const size_t table = (size_t)4 << a.m.prob_bits, per_warp = 2 * rans_buf_bytes(a.m.words_cap);
+    /* one CTA per SM: slot table | (GEMV) code-pair table | x (BF16) [rows of this pass][k_pad] |
+     * two tile buffers per warp */
+    const size_t table = ((size_t)4 << a.m.prob_bits) + (gemv ? 1024 : 0), per_warp = 2 * rans_buf_bytes(a.m.words_cap);
     const int64_t kp = W->hdr.k_pad, K = W->hdr.k_cols;
     const size_t xrow = gemv ? (size_t)2 * kp : 0;
     if (table + xrow + 4 * per_warp > d->smem_optin) return EC_ERR_UNSUPPORTED;
