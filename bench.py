@@ -50,13 +50,13 @@ def peaks():
 
 
 def kernel_hash() -> str:
-    """First 16 hex digits of the SHA-256 of the kernel source without its E8 decode
-    sections (the text between each "E8 decode: begin" / "E8 decode: end" marker pair),
-    which hold only the E8 kernel and its launcher: the Huffman kernels' counters stay
-    valid while the E8 code changes."""
+    """First 16 hex digits of the SHA-256 of the kernel source without the sections
+    that the batch-1 Huffman GEMV never runs (the text between each "<tag>: begin" /
+    "<tag>: end" marker pair: the E8, rANS, FP8, exponent-codec, tensor-core and
+    prefill code): the fused GEMV's counters stay valid while only that code changes."""
     with open(KERNEL_SRC, "rb") as f:
         src = f.read()
-    src = re.sub(rb"/\* ---- E8 decode: begin ---- \*/.*?/\* ---- E8 decode: end ---- \*/\n", b"", src, flags=re.S)
+    src = re.sub(rb"/\* ---- ([A-Za-z0-9 ]+): begin ---- \*/.*?/\* ---- \1: end ---- \*/\n", b"", src, flags=re.S)
     return hashlib.sha256(src).hexdigest()[:16]
 
 

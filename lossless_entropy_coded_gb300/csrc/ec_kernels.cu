@@ -1046,6 +1046,7 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
     }
 }
 
+/* ---- not in the Huffman GEMV: begin ---- */
 /* ========================================= Huffman tensor-core GEMV (tcgen05) */
 /*
  * Small batches (MINE section 5: fused kernels for batch > 1 as the next step)
@@ -1719,6 +1720,7 @@ __global__ void gemm_reduce_kernel(const float* __restrict__ part, int ksplit, i
     }
 }
 
+/* ---- not in the Huffman GEMV: end ---- */
 /* ====================================================== Huffman decode kernel */
 /* Each CTA owns a contiguous range of the launch's tiles; it walks the range one
  * matrix segment at a time, with that matrix's pair table in shared memory.
@@ -1842,6 +1844,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) huff_decode_kernel(const
     }
 }
 
+/* ---- not in the Huffman GEMV: begin ---- */
 /* x [batch, K] into shared rows of k_pad entries in the per-128-column permuted
  * order above (zero past K). */
 __device__ __forceinline__ void stage_x_perm(uint16_t* xs, const uint16_t* __restrict__ x, int batch, int64_t K,
@@ -2477,6 +2480,7 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) exp_kernel(const __
     }
 }
 
+/* ---- not in the Huffman GEMV: end ---- */
 /* ======================================================== BF16 GEMV comparator */
 constexpr int kRowsPerWarp = 4;
 
@@ -3053,6 +3057,7 @@ int launch_huff_gemv(const HuffGemvArgs& a, bool lng, size_t smem, int grid, int
     return launch_huff_gemv_b<16, kPart>(a, lng, smem, grid, block, s);
 }
 
+/* ---- not in the Huffman GEMV: begin ---- */
 template <bool G, int B>
 int launch_rans_b(const RansArgs& a, size_t smem, int grid, int block, cudaStream_t s) {
     auto kern = a.m.tuple == 2 ? rans_kernel<G, B, true> : rans_kernel<G, B, false>;
@@ -3068,6 +3073,7 @@ int launch_rans(bool gemv, const RansArgs& a, size_t smem, int grid, int block, 
     if (a.batch <= 8) return launch_rans_b<true, 8>(a, smem, grid, block, s);
     return launch_rans_b<true, 16>(a, smem, grid, block, s);
 }
+/* ---- not in the Huffman GEMV: end ---- */
 
 /* Batch rows whose copy of x (elem bytes per value) fits in `budget` bytes of shared memory. */
 int rows_per_pass(int64_t k_pad, int batch, size_t budget, int elem = 4) {
@@ -3172,6 +3178,7 @@ bool use_mma(const ec_matrix* const* Ws, int count, int batch) {
     return mma;
 }
 
+/* ---- not in the Huffman GEMV: begin ---- */
 int huff_mma(const ec_matrix* const* Ws, int count, const uint16_t* x, float* const* ys, int batch, cudaStream_t s,
              DeviceInfo* d) {
     HuffMmaArgs a{};
@@ -3233,6 +3240,7 @@ int huff_mma(const ec_matrix* const* Ws, int count, const uint16_t* x, float* co
     }
     return EC_OK;
 }
+/* ---- not in the Huffman GEMV: end ---- */
 
 int huff_gemv(const ec_matrix* const* Ws, int count, const uint16_t* x, float* const* ys, int batch,
               cudaStream_t s, int dev, DeviceInfo* d) {
@@ -3291,6 +3299,7 @@ int huff_gemv(const ec_matrix* const* Ws, int count, const uint16_t* x, float* c
     return EC_OK;
 }
 
+/* ---- not in the Huffman GEMV: begin ---- */
 int rans_run(const ec_matrix* W, const uint16_t* x, float* y, uint16_t* out, int batch, cudaStream_t s,
              DeviceInfo* d) {
     RansArgs a{};
@@ -3440,6 +3449,7 @@ int exp_run(const ec_matrix* W, const uint16_t* x, float* y, uint16_t* out, int 
     }
     return EC_OK;
 }
+/* ---- not in the Huffman GEMV: end ---- */
 
 /* ---- E8 decode: begin ---- */
 /* E8 decode: one CTA per SM, the 17 tables in shared memory, two tile buffers per warp. */
@@ -3560,6 +3570,7 @@ int static_device(int dev, StaticDevice** out) {
 }
 
 
+/* ---- not in the Huffman GEMV: begin ---- */
 /* ------------------------------------------------------------ prefill GEMM */
 /* The Huffman decode kernel over a.total_tiles tiles (a.m, a.count, a.sub_words set). */
 int launch_huff_decode(HuffDecodeArgs& a, int code_bytes, bool lng, cudaStream_t stream, DeviceInfo* d) {
@@ -3736,6 +3747,7 @@ int plan_prefill(const ec_matrix* W, int batch, size_t work_bytes, const DeviceI
     }
 }
 
+/* ---- not in the Huffman GEMV: end ---- */
 }  // namespace
 
 /* ================================================================ C ABI */
@@ -3833,6 +3845,7 @@ extern "C" int ec_decode_batch(const ec_matrix* const* Ws, uint16_t* const* outs
     return launch_huff_decode(a, code_bytes, lng, stream, d);
 }
 
+/* ---- not in the Huffman GEMV: begin ---- */
 extern "C" int ec_gemm_work_bytes(const ec_matrix* W, int batch, size_t* bytes) {
     if (!W || !bytes || batch < 1) return EC_ERR_INVALID_ARG;
     int dev = 0;
@@ -4056,6 +4069,7 @@ extern "C" int ec_bf16_gemm(const uint16_t* w, int64_t n_rows, int64_t k_cols, c
     return gemm_run(w, n_rows, k_cols, k_cols, x, k_cols, batch, y, n_rows, 0, (float*)work, work ? work_bytes : 0,
                     stream, d);
 }
+/* ---- not in the Huffman GEMV: end ---- */
 
 extern "C" int ec_decode(const ec_matrix* W, uint16_t* out, cudaStream_t stream) {
     return ec_decode_batch(&W, &out, 1, stream);
