@@ -397,6 +397,15 @@ def extras(torch, ec, stream, device):
     g2 = capture(torch, lambda: ec.decode(W, dw), stream)
     out["w1024_decode_us"] = round(t_loop(g2.replay, 200), 2)
     out["w1024_bpw"] = round(W.stats()["bits_per_weight"], 3)
+    # the same matrix with codewords up to 24 bits (the limit the workload states):
+    # window records carry what the 12-bit pair window cannot
+    W24 = ec.encode_bf16(w, max_code_len=24, device=device)
+    g3 = capture(torch, lambda: ec.gemv(W24, x, y), stream)
+    out["w1024_maxlen24_gemv_us"] = round(t_loop(g3.replay, 200), 2)
+    g4 = capture(torch, lambda: ec.decode(W24, dw), stream)
+    out["w1024_maxlen24_decode_us"] = round(t_loop(g4.replay, 200), 2)
+    out["w1024_maxlen24_bpw"] = round(W24.stats()["bits_per_weight"], 3)
+    out["w1024_maxlen24_longest_code"] = int(W24.code_lengths().max())
 
     # rANS 4-bit tiles, both shapes, one code per symbol and pair symbols (rotate 8
     # copies to stay out of L2)

@@ -79,7 +79,7 @@ def test_round_trip_config1_and_oracle_agrees(ec):
     assert W.stats()["max_code_len"] == int(O.DF11(w, max_len=12).lengths.max())
 
 
-@pytest.mark.parametrize("max_len", [24, 12, 9])
+@pytest.mark.parametrize("max_len", [24, 16, 12, 9])
 def test_long_codes_and_length_limit(ec, max_len):
     w = fib_weights()
     W = ec.encode_bf16(w, max_code_len=max_len)
@@ -266,3 +266,20 @@ def test_misaligned_device_pointers_are_rejected(ec):
     out = torch.zeros(32 * 1024 + 8, dtype=torch.int16, device="cuda")
     assert lib.ec_decode(W.handle, out.data_ptr() + 2, None) == _ec.EC_ERR_INVALID_ARG
     assert ec.status() == 0
+
+
+@pytest.mark.parametrize("batch", [1, 3])
+def test_gemv_group_of_more_matrices_than_one_launch_holds(ec, batch):
+    """Groups above three matrices run as several launches of at most three (the fused
+    kernel keeps its pair tables in a fixed shared-memory block): every output against
+    the oracle."""
+    shapes = [(256, 1024), (64, 1024), (96, 1024), (128, 1024), (33, 1024), (300, 1024), (7, 1024)]
+    ws = [synth.llama_bf16(2350 + i, *sh) for i, sh in enumerate(shapes)]
+    Ws = [ec.encode_bf16(w) for w in ws]
+    x = synth.make_x(2350, batch, 1024)
+    ys = [torch.full((batch, sh[0]), float("nan"), dtype=torch.float32, device="cuda") for sh in shapes]
+    ec.gemv_group(Ws, torch.from_numpy(x.view(np.int16)).cuda(), ys, batch=batch)
+    assert ec.status() == 0
+    for i, (w, y) in enumerate(zip(ws, ys)):
+        y_ref, a_ref = O.gemv_bf16(w, x)
+        check_gemv(y.cpu().numpy().astype(np.float64), y_ref, a_ref, f"group member {i} b={batch}")
