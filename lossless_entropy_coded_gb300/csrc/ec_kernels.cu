@@ -831,8 +831,12 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
     const uint32_t bufs = smem_u32(wbase), buf_bytes = (uint32_t)tile_buf_bytes(a.code_bytes);
     const uint32_t xs_s = smem_u32(xs), xs_lane = xs_s + 16u * lane, tabs_s = smem_u32(tabs); /* x of the lane's 8 columns */
 
+    /* Warps are numbered CTA-fastest (warp w of CTA c is gw = w * grid + c) and take tiles
+     * gw, gw + nw, ...: the tiles of one CTA lie spread over the whole launch, so every
+     * CTA gets about the same number of code bytes even when a partial last round or
+     * regions of longer codewords would load some CTAs more than others. */
     const int nwarp = blockDim.x >> 5;
-    const int64_t gw = (int64_t)blockIdx.x * nwarp + warp, nw = (int64_t)gridDim.x * nwarp;
+    const int64_t gw = (int64_t)warp * gridDim.x + blockIdx.x, nw = (int64_t)gridDim.x * nwarp;
     const uint32_t mbars = bufs + 2 * buf_bytes;
     if (lane == 0) {
         mbar_init(mbars);
