@@ -35,6 +35,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -287,7 +288,7 @@ constexpr uint32_t kPairTabBytes = 4u * EC_PAIR_WORDS;
 constexpr uint32_t kSignMant = 0x807F807Fu;    /* sign and mantissa bits of two BF16 */
 constexpr int kSubSmemTables = 8;             /* hierarchical sub-tables staged in shared memory per launch */
 
-__host__ __device__ constexpr int huff_max_warps(int b) { return b <= 1 ? 32 : (b <= 4 ? 24 : 16); }
+__host__ __device__ constexpr int huff_max_warps(int b) { return b <= 1 ? 28 : (b <= 4 ? 24 : 16); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
@@ -321,6 +322,12 @@ __device__ __forceinline__ void tc_ld4(uint32_t taddr, uint32_t (&v)[4]) {
                  : "r"(taddr)
                  : "memory");
 }
+__device__ __forceinline__ void tc_ld8(uint32_t taddr, uint32_t (&v)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr)
+                 : "memory");
+}
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tc_st4(uint32_t taddr, const uint4& v) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
@@ -332,6 +339,10 @@ __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sy
  * so that no use of it can be scheduled before the data is there. */
 __device__ __forceinline__ void tc_wait_ld_into(uint32_t (&v)[4]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3])::"memory");
+}
+__device__ __forceinline__ void tc_wait_ld_into(uint32_t (&v)[8]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7])::"memory");
 }
 
 /*
@@ -346,7 +357,10 @@ __device__ __forceinline__ void tc_wait_ld_into(uint32_t (&v)[4]) {
  * shift reads) and bit 5 matter.  An entry's bits 0..3 hold its advance and bits
  * 4..6 are 0, so bit 5 of P flips exactly when S crosses into the next word; then
  * lo takes hi, hi takes nx (the word after hi, loaded one crossing ahead so that
- * the next lookup never waits for a load) and nx the word at wa.
+ * the next lookup never waits for a load) and nx the word at wa.  Hierarchical
+ * launches, whose long codewords may cross several words, make that move at every
+ * step (lane_adv); the others look past lo at most once per two steps and move
+ * the window after every second step (pair_first, pair_second, lane_rebase).
  */
 struct Lane {
     uint32_t P, lo, hi, nx, wa;
@@ -361,7 +375,14 @@ __device__ __forceinline__ void lane_seek(Lane& s, uint32_t area, uint32_t A) {
     s.hi = lds32(a + 4);
     s.nx = lds32(a + 8);
     s.wa = a + 12;
-    s.P = (uint32_t)S;
+    s.P = (uint32_t)S & 31u;
+}
+
+/* Pair-table entry of the window held in v (the next 12 stream bits at bits 2..13). */
+__device__ __forceinline__ uint32_t pair_addr(uint32_t tab, uint32_t v) { return tab + (v & 0x3FFCu); }
+/* Stage the 4096-entry pair table src into shared memory at dst. */
+__device__ __forceinline__ void stage_pair_table(uint32_t* dst, const uint32_t* src) {
+    for (int i = threadIdx.x; i < EC_PAIR_WORDS / 4; i += blockDim.x) ((uint4*)dst)[i] = __ldg((const uint4*)src + i);
 }
 
 /* Advance by the low bits of `e` (an entry, or a length below 32). */
@@ -379,6 +400,40 @@ __device__ __forceinline__ void lane_adv(Lane& s, uint32_t e) {
         : "r"(pn), "r"(s.P)
         : "memory");
     s.P = pn;
+}
+
+/* Two steps without a data-dependent move on the lookup chain (non-hierarchical
+ * launches).  At the start of a pair of steps (P & 32) = 0: the next codeword
+ * starts at bit P mod 32 of lo.  Advances are at most 15 bits, so the second
+ * step starts below bit 47 of lo, hi, nx and reads hi, nx when it is past lo;
+ * after it, lane_rebase moves the window on by a word when the reader has left lo.
+ * The chain from one lookup to the next is then shift, mask, add, load and the
+ * advance (plus a select every second step) instead of also testing for and
+ * making the move at every step. */
+__device__ __forceinline__ uint32_t pair_first(Lane& s, uint32_t tab) {
+    const uint32_t e = lds32(pair_addr(tab, __funnelshift_r(s.lo, s.hi, s.P)));
+    s.P += e;
+    return e;
+}
+__device__ __forceinline__ uint32_t pair_second(Lane& s, uint32_t tab) {
+    const uint32_t v = (s.P & 32u) ? __funnelshift_r(s.hi, s.nx, s.P) : __funnelshift_r(s.lo, s.hi, s.P);
+    const uint32_t e = lds32(pair_addr(tab, v));
+    s.P += e;
+    return e;
+}
+__device__ __forceinline__ void lane_rebase(Lane& s) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t.reg .b32 t;\n\t"
+        "and.b32 t, %4, 32;\n\t"
+        "setp.ne.u32 q, t, 0;\n\t"
+        "@q mov.b32 %0, %1;\n\t"
+        "@q mov.b32 %1, %2;\n\t"
+        "@q ld.shared.u32 %2, [%3];\n\t"
+        "@q add.u32 %3, %3, 4;\n\t}"
+        : "+r"(s.lo), "+r"(s.hi), "+r"(s.nx), "+r"(s.wa)
+        : "r"(s.P)
+        : "memory");
+    s.P &= ~32u;
 }
 
 /* Area bit of the lane's next codeword. */
@@ -430,7 +485,7 @@ __device__ __forceinline__ uint32_t pair_open(Lane& s, uint32_t e, uint32_t tab,
         e0 = r.x;
         lane_adv(s, r.y);
     }
-    const uint32_t f = lds32(tab + (__funnelshift_r(s.lo, s.hi, s.P) & 0x3FFCu));
+    const uint32_t f = lds32(pair_addr(tab, __funnelshift_r(s.lo, s.hi, s.P)));
     uint32_t e1 = (f >> 7) & 0xFFu, l1 = (f >> EC_PAIR_FIRST_SHIFT) & 15u;
     if (l1 == 0) {
         const uint2 r = long_codeword(__funnelshift_r(s.lo, s.hi, s.P) >> 2, f, h);
@@ -447,7 +502,7 @@ __device__ __forceinline__ uint32_t pair_open(Lane& s, uint32_t e, uint32_t tab,
  * table load and the advance, with no branch on the data. */
 template <bool kHier>
 __device__ __forceinline__ uint32_t pair_step(Lane& s, uint32_t tab, const HierCtx& h) {
-    const uint32_t e = lds32(tab + (__funnelshift_r(s.lo, s.hi, s.P) & 0x3FFCu));
+    const uint32_t e = lds32(pair_addr(tab, __funnelshift_r(s.lo, s.hi, s.P)));
     lane_adv(s, e);
     if (kHier && __builtin_expect((int32_t)e < 0, 0)) return pair_open(s, e, tab, h);
     return e;
@@ -465,6 +520,19 @@ __device__ __forceinline__ uint32_t merge_sm(uint32_t r, uint32_t e) {
 template <bool kHier>
 __device__ __forceinline__ void decode8(Lane& s, uint32_t tab, const HierCtx& h, uint32_t r0, uint32_t r1,
                                         uint32_t (&w)[4]) {
+    if (!kHier) {
+        const uint32_t e0 = pair_first(s, tab);
+        const uint32_t e1 = pair_second(s, tab);
+        lane_rebase(s);
+        w[0] = merge_sm(r0, e0);
+        w[1] = merge_sm(__funnelshift_r(r0, r0, 8), e1);
+        const uint32_t e2 = pair_first(s, tab);
+        const uint32_t e3 = pair_second(s, tab);
+        lane_rebase(s);
+        w[2] = merge_sm(r1, e2);
+        w[3] = merge_sm(__funnelshift_r(r1, r1, 8), e3);
+        return;
+    }
     const uint32_t e0 = pair_step<kHier>(s, tab, h);
     const uint32_t e1 = pair_step<kHier>(s, tab, h);
     w[0] = merge_sm(r0, e0);
@@ -850,10 +918,7 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
         first = tile_ref(a, gw, tile_offsets(a, gw));
         prefetch_code(bufs, mbars, first, lane, a.code_bytes);
     }
-    for (int k = 0; k < a.count; ++k) {
-        const uint4* src = (const uint4*)a.m[k].table;
-        for (int i = threadIdx.x; i < EC_PAIR_WORDS / 4; i += blockDim.x) tabs[k * (EC_PAIR_WORDS / 4) + i] = __ldg(src + i);
-    }
+    for (int k = 0; k < a.count; ++k) stage_pair_table((uint32_t*)(tabs + k * (EC_PAIR_WORDS / 4)), a.m[k].table);
     if (kHier) stage_sub_tables(a, subs);
     if (kTx && warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tslot), "r"(a.tx_cols)
@@ -893,8 +958,11 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
      * at use for wide ones (whose registers go to the accumulators) */
     constexpr bool kAhead = B <= 4;
     uint4 xv[kAhead ? B : 1];
-    uint32_t xt[4] = {0u, 0u, 0u, 0u}; /* kTx: x of the next 8 symbols, loading from TMEM */
-    uint32_t xcol = 0, xend = 0;       /* kTx: its TMEM address; the end of the tile's layout */
+    /* kTx: x of the current 16 symbols (one decode block), loading from TMEM; the load
+     * of the next block's is issued when a block's second half is done, whether or not
+     * the tile has one (the allocation has 8 columns to spare) */
+    uint32_t xt[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    uint32_t xcol = 0; /* kTx: its TMEM address */
     uint32_t row = 0, t_cur = 0;
     uint32_t jc = 0; /* first column / 32 of the current 8 symbols' 256-column block */
     const HuffMat* Mp = &a.m[0];
@@ -911,9 +979,11 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
      * code area, all but those beyond the buffer's room), then reduce across the warp. */
     auto flush = [&](uint32_t r, uint32_t cb, const TileRef& tile) {
         const HuffMat& M = *Mp;
-        const uint32_t seg_end = (r - row0 + 1) * kp - col0;    /* tile positions of rows <= r */
-        const uint32_t seg_begin = r == row0 ? 0u : seg_end - kp; /* ... of rows < r */
-        const uint32_t col_base = col0 - (r - row0) * kp;         /* column = col_base + position */
+        /* (with x in tensor memory every tile lies inside its row: r = row0, and every
+         * record of the tile belongs to it) */
+        const uint32_t seg_end = kTx ? ~0u : (r - row0 + 1) * kp - col0;    /* tile positions of rows <= r */
+        const uint32_t seg_begin = kTx || r == row0 ? 0u : seg_end - kp;    /* ... of rows < r */
+        const uint32_t col_base = kTx ? col0 : col0 - (r - row0) * kp;      /* column = col_base + position */
         const TileRecs tr = tile_recs(cb, tile.area, a.code_bytes);
         for (uint32_t j = (uint32_t)lane; j < tr.staged; j += 32) {
             const uint32_t e = lds32(cb + 64 + tr.code + 4 * j), q = e & 0xFFFu;
@@ -991,8 +1061,8 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
             if (!kTx) jc = (uint32_t)col0 / 32;
             if (kTx) {
                 xcol = tx + (col0 / a.tx_T) * (uint32_t)a.tx_layout_cols;
-                xend = xcol + (uint32_t)a.tx_layout_cols;
-                tc_ld4(xcol, xt);
+                tc_wait_ld_into(xt); /* the previous tile's last (unused) load */
+                tc_ld8(xcol, xt);
             } else if (kAhead) {
                 load_x(jc);
             }
@@ -1009,11 +1079,11 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
             }
         },
         [&](const uint32_t (&w)[4], int h) {
-            if (kTx) tc_wait_ld_into(xt);
+            if (kTx && h == 0) tc_wait_ld_into(xt);
 #pragma unroll
             for (int b = 0; b < B; ++b) {
                 if (B > 1 && b >= batch) break;
-                const uint4 x4 = kTx ? make_uint4(xt[0], xt[1], xt[2], xt[3])
+                const uint4 x4 = kTx ? make_uint4(xt[4 * h % 8], xt[(4 * h + 1) % 8], xt[(4 * h + 2) % 8], xt[(4 * h + 3) % 8])
                                      : kAhead ? xv[b] : lds128(xs_lane + 64 * jc + (uint32_t)(b * xs_row_bytes(kp)));
                 if (B == 1) {
                     fma2x_bf16(w[0], x4.x, acc[b][0], acc[b][1 % kAcc]);
@@ -1029,8 +1099,10 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
             }
             if (!kTx) jc += 8;
             if (kTx) { /* the next 8 symbols' x, if the tile has them (one load in flight at a time) */
-                xcol += 4;
-                if (xcol < xend) tc_ld4(xcol, xt);
+                if (h == 1) {
+                    xcol += 8;
+                    tc_ld8(xcol, xt);
+                }
             } else if (kAhead) {
                 /* rows start on block boundaries: only a second half can be followed by
                  * a new row */
@@ -1040,6 +1112,7 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
         [&](const TileRef& tile, uint32_t cb) { flush(row, cb, tile); });
     }
     if (kTx) { /* every warp is done with tensor memory */
+        tc_wait_ld(); /* the load past the warp's last block */
         tc_fence_before();
         __syncthreads();
         if (warp == 0) {
@@ -1263,11 +1336,8 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
     uint32_t region = 0; /* this warp's tile in the current pool */
     bool fits = true;    /* the next item's tile found room */
     if (d >= 0) cur = stage(ci, 0, region);
-    for (int k = 0; k < a.count; ++k) {
-        const uint4* src = (const uint4*)a.m[k].table;
-        uint4* dst = (uint4*)(smem + (tabs_s - smem_u32(smem)) + (size_t)k * kPairTabBytes);
-        for (int i = threadIdx.x; i < EC_PAIR_WORDS / 4; i += blockDim.x) dst[i] = __ldg(src + i);
-    }
+    for (int k = 0; k < a.count; ++k)
+        stage_pair_table((uint32_t*)(smem + (tabs_s - smem_u32(smem)) + (size_t)k * kPairTabBytes), a.m[k].table);
     if (kHier) stage_sub_tables(a, subs);
     if (warp == 0) { /* all 512 TMEM columns: 2 items x 8 accumulator tiles of 32 columns */
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(tslot) : "memory");
@@ -1780,8 +1850,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) huff_decode_kernel(const
             prefetch_code(bufs, mbars, first, lane, a.code_bytes);
         }
         __syncthreads();
-        const uint4* src = (const uint4*)M.table;
-        for (int i = threadIdx.x; i < EC_PAIR_WORDS / 4; i += blockDim.x) tab[i] = __ldg(src + i);
+        stage_pair_table((uint32_t*)tab, M.table);
         /* this matrix's sub-tables, when they were sized to fit (sub_smem == 0) */
         HuffMat Ms = M;
         if (kHier && M.sub_smem >= 0 && 256 * M.n_sub <= a.sub_words) {
@@ -3110,27 +3179,40 @@ int plan_huff_gemv(const DeviceInfo& d, int count, int code_bytes, int64_t kp, i
     if (tables + pl->xrow + 4 * per_warp > d.smem_optin) return EC_ERR_UNSUPPORTED;
     const int cap = huff_max_warps(batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : batch <= 8 ? 8 : 16);
     const int wmax = (int)std::min<size_t>(cap, (d.smem_optin - tables - pl->xrow) / per_warp);
-    /* Each warp takes every (grid * warps)-th tile, so a pass lasts ceil(tiles /
-     * (sms * w)) rounds of one tile per warp.  Below about 24 warps an SM is
-     * latency-bound and a round takes the same time whatever w; above, it is
-     * issue-bound and a round takes time in proportion to w.  Batch rows whose x
-     * does not fit next to the warps' buffers take further passes, each decoding
-     * the matrices again.  Pick the w with the fewest passes * rounds * max(w, 24),
-     * the larger on ties. */
-    constexpr int kKnee = 24;
-    int best = wmax, best_rows = 1;
-    int64_t best_cost = INT64_MAX;
-    for (int w = wmax; w >= 1; --w) {
+    /* Each warp takes every (grid * warps)-th tile, grid = min(SMs, tiles / w): an
+     * SM runs tiles / grid tiles in rounds of w warps, the last round with what is
+     * left.  A round takes time in proportion to its busy warps, but no less than
+     * with 16 (below that the warps' decode chains leave the SM idle).  Batch rows
+     * whose x does not fit next to the warps' buffers take further passes, each
+     * decoding the matrices again.  Cost = passes * sum over rounds of max(busy,
+     * 16); among the w within 1 % of the cheapest take the one with the largest
+     * grid, then the largest w. */
+    constexpr double kFloor = 16.0;
+    double cost[33] = {};
+    int rows_of[33] = {};
+    int64_t grid_of[33] = {};
+    double best_cost = 1e300;
+    for (int w = 1; w <= wmax; ++w) {
         const size_t fixed = tables + (size_t)w * per_warp;
         const int rows = (int)std::min<size_t>(std::min(batch, kFmaMaxRows), (d.smem_optin - fixed) / pl->xrow);
-        const int64_t passes = (batch + rows - 1) / rows, slots = (int64_t)d.sms * w;
-        const int64_t cost = passes * ((total_tiles + slots - 1) / slots) * std::max(w, kKnee);
-        if (cost < best_cost) {
-            best_cost = cost;
-            best = w;
-            best_rows = rows;
-        }
+        const int64_t passes = (batch + rows - 1) / rows;
+        const int64_t g = std::max<int64_t>(1, std::min<int64_t>(d.sms, (total_tiles + w - 1) / w));
+        const double per_sm = (double)total_tiles / (double)g; /* tiles (warp rounds) each SM runs */
+        const int64_t rounds = (int64_t)std::ceil(per_sm / w - 1e-9);
+        const double last = per_sm - (double)(rounds - 1) * w; /* warps busy in the last round */
+        cost[w] = (double)passes * ((double)(rounds - 1) * std::max<double>(w, kFloor) + std::max(last, kFloor));
+        rows_of[w] = rows;
+        grid_of[w] = g;
+        best_cost = std::min(best_cost, cost[w]);
     }
+    int best = wmax, best_rows = rows_of[wmax];
+    int64_t best_grid = -1;
+    for (int w = wmax; w >= 1; --w)
+        if (cost[w] <= 1.01 * best_cost && grid_of[w] > best_grid) {
+            best = w;
+            best_rows = rows_of[w];
+            best_grid = grid_of[w];
+        }
     pl->warps = best;
     pl->fixed = tables + (size_t)pl->warps * per_warp;
     pl->per_pass = best_rows;
@@ -3284,7 +3366,7 @@ int huff_gemv(const ec_matrix* const* Ws, int count, const uint16_t* x, float* c
         for (int k = 0; k < count && ok; ++k) ok = Ws[k]->hdr.steps == Ws[0]->hdr.steps;
         const int64_t used = ok ? (kp / T) * (T / 64) : 0;
         int cols = 32;
-        while (cols < used) cols *= 2;
+        while (cols < used + 8) cols *= 2; /* + 8: the load past a tile's last block */
         if (ok && used > 0 && cols <= 512) {
             a.tx_cols = cols;
             a.tx_layout_cols = (int)(T / 64);
