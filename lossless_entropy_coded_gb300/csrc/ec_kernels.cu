@@ -631,18 +631,22 @@ struct TileRef {
 };
 
 template <class Args>
-__device__ __forceinline__ uint2 tile_offsets(const Args& a, int64_t g) {
-    const HuffMat& M = a.m[owner(a, g)];
+__device__ __forceinline__ uint2 tile_offsets_of(const Args& a, int64_t g, int mi) {
+    const HuffMat& M = a.m[mi];
     const int64_t t = g - M.tile_begin;
     return make_uint2(ldg_early(M.tile_off + t), ldg_early(M.tile_off + t + 1));
+}
+template <class Args>
+__device__ __forceinline__ uint2 tile_offsets(const Args& a, int64_t g) {
+    return tile_offsets_of(a, g, owner(a, g));
 }
 
 /* Resolve combined tile g from its record offsets (16-byte units); a record whose
  * extent is inconsistent gets area 0. */
 template <class Args>
-__device__ __forceinline__ TileRef tile_ref(const Args& a, int64_t g, uint2 off) {
+__device__ __forceinline__ TileRef tile_ref_of(const Args& a, int64_t g, uint2 off, int mi) {
     TileRef r;
-    r.mi = owner(a, g);
+    r.mi = mi;
     const HuffMat& M = a.m[r.mi];
     r.t = (uint32_t)(g - M.tile_begin);
     r.S = r.t == M.n_tiles - 1 ? M.last_steps : M.steps;
@@ -652,6 +656,10 @@ __device__ __forceinline__ TileRef tile_ref(const Args& a, int64_t g, uint2 off)
     r.rec = M.records + (size_t)(ok ? off.x : 0u) * 16;
     r.area = ok ? area : 0;
     return r;
+}
+template <class Args>
+__device__ __forceinline__ TileRef tile_ref(const Args& a, int64_t g, uint2 off) {
+    return tile_ref_of(a, g, off, owner(a, g));
 }
 
 /* mbarrier and bulk-copy helpers (one arrival per phase: the issuing lane's). */
@@ -765,7 +773,7 @@ __device__ __forceinline__ const uint32_t* far_records(const TileRef& r, uint32_
  * already be in flight (prefetch_code).  For every tile with a sound record:
  * begin(tile) once; then, for each block of 16 symbols of the lane, block(buf,
  * tile) and two calls half(w, h) for its two 8-symbol halves h = 0, 1 in order (w =
- * four words [w(i+1) | w(i)]); then end(tile, buf).  buf is the tile's shared
+ * four words [w(i+1) | w(i)]); then end(tile, buf, recs).  buf is the tile's shared
  * buffer: lane starts, the code area, then its window records (tile_recs).  Rows start on block boundaries (k_pad is
  * a multiple of 16 * 32 positions).  The raw bytes of block b + 2 are loaded right
  * after block b is decoded, into the ring slot it frees; blocks 0 and 1 of the
@@ -775,7 +783,8 @@ __device__ __forceinline__ void huff_walk(const Args& a, uint32_t g0, uint32_t s
                                           uint32_t bufs, uint32_t buf_bytes, uint32_t& ph, int lane,
                                           CtxOf&& ctx_of, Begin&& begin, Block&& block, Half&& half, End&& end) {
     const uint32_t mbars = bufs + 2 * buf_bytes;
-    uint2 off_next = g0 + stride < g_end ? tile_offsets(a, g0 + stride) : make_uint2(0u, 0u);
+    int mi_next = g0 + stride < g_end ? owner(a, g0 + stride) : 0; /* matrix of the next tile */
+    uint2 off_next = g0 + stride < g_end ? tile_offsets_of(a, g0 + stride, mi_next) : make_uint2(0u, 0u);
     uint4 rr[2] = {};
     bool raw_ready = false, raw_swap = false;
     uint32_t cb = bufs; /* buffer of the current tile */
@@ -789,9 +798,12 @@ __device__ __forceinline__ void huff_walk(const Args& a, uint32_t g0, uint32_t s
         const bool has_next = g + stride < g_end;
         TileRef nxt{};
         if (has_next) {
-            nxt = tile_ref(a, g + stride, off_next);
+            nxt = tile_ref_of(a, g + stride, off_next, mi_next);
             prefetch_code(nb_buf, mbars + 8 * (bi ^ 1u), nxt, lane, a.code_bytes);
-            if (g + 2 * stride < g_end) off_next = tile_offsets(a, g + 2 * stride);
+            if (g + 2 * stride < g_end) {
+                mi_next = owner(a, g + 2 * stride);
+                off_next = tile_offsets_of(a, g + 2 * stride, mi_next);
+            }
         }
         const TileRecs tr = tile_recs(cb, cur.area, a.code_bytes);
         if (tr.n < 0) {
@@ -851,7 +863,7 @@ __device__ __forceinline__ void huff_walk(const Args& a, uint32_t g0, uint32_t s
         const uint32_t p = lane_pos(s, area), pmax = 8u * cbytes;
         const bool bad = lane < 31 ? (p > 8u * s1 || p + 8u <= 8u * s1) : (p + 64u > pmax);
         if (__any_sync(kFull, bad) && lane == 0) flag_corrupt(a.status);
-        end(cur, cb);
+        end(cur, cb, tr);
         cur = nxt;
         cb = nb_buf;
     }
@@ -977,14 +989,13 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
     /* Row r of the current tile (buffer cb) is complete: fold in its window records
      * (each adds (w - w_coded) * x, both products exact; they came with the tile's
      * code area, all but those beyond the buffer's room), then reduce across the warp. */
-    auto flush = [&](uint32_t r, uint32_t cb, const TileRef& tile) {
+    auto flush = [&](uint32_t r, uint32_t cb, const TileRef& tile, const TileRecs& tr) {
         const HuffMat& M = *Mp;
         /* (with x in tensor memory every tile lies inside its row: r = row0, and every
          * record of the tile belongs to it) */
         const uint32_t seg_end = kTx ? ~0u : (r - row0 + 1) * kp - col0;    /* tile positions of rows <= r */
         const uint32_t seg_begin = kTx || r == row0 ? 0u : seg_end - kp;    /* ... of rows < r */
         const uint32_t col_base = kTx ? col0 : col0 - (r - row0) * kp;      /* column = col_base + position */
-        const TileRecs tr = tile_recs(cb, tile.area, a.code_bytes);
         for (uint32_t j = (uint32_t)lane; j < tr.staged; j += 32) {
             const uint32_t e = lds32(cb + 64 + tr.code + 4 * j), q = e & 0xFFFu;
             if (q >= seg_begin && q < seg_end) {
@@ -1060,7 +1071,7 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
             row = row0; /* advanced by the block hook as rows end inside the tile */
             if (!kTx) jc = (uint32_t)col0 / 32;
             if (kTx) {
-                xcol = tx + (col0 / a.tx_T) * (uint32_t)a.tx_layout_cols;
+                xcol = tx + col0 / 64u; /* (col0 / T) layouts of T / 64 columns; col0 is a multiple of T */
                 tc_wait_ld_into(xt); /* the previous tile's last (unused) load */
                 tc_ld8(xcol, xt);
             } else if (kAhead) {
@@ -1073,7 +1084,7 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
         },
         [&](uint32_t cb, const TileRef& tile) {
             if (!kTx && jc >= jrow) { /* (with x in TMEM tiles lie inside rows) */
-                flush(row, cb, tile);
+                flush(row, cb, tile, tile_recs(cb, tile.area, a.code_bytes));
                 jc -= jrow;
                 ++row;
             }
@@ -1109,7 +1120,7 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
                 load_x(h == 1 && jc >= jrow ? jc - jrow : jc);
             }
         },
-        [&](const TileRef& tile, uint32_t cb) { flush(row, cb, tile); });
+        [&](const TileRef& tile, uint32_t cb, const TileRecs& tr) { flush(row, cb, tile, tr); });
     }
     if (kTx) { /* every warp is done with tensor memory */
         tc_wait_ld(); /* the load past the warp's last block */
@@ -1903,10 +1914,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) huff_decode_kernel(const
                     }
                     col0 += 256;
                 },
-                [&](const TileRef& r, uint32_t cb) {
+                [&](const TileRef& r, uint32_t cb, const TileRecs& tr) {
                     /* window records: the true weight over the coded one (stored above by
                      * some lane of this warp) */
-                    const TileRecs tr = tile_recs(cb, r.area, a.code_bytes);
                     if (tr.n > 0) {
                         __syncwarp();
                         decode_records(cb + 64 + tr.code, tr.staged, far_records(r, tr.code), (uint32_t)tr.n, M,
