@@ -76,13 +76,16 @@ typedef struct ec_matrix ec_matrix; /* opaque: host descriptor + one device blob
  *                the code is textbook Huffman when it fits, otherwise the
  *                optimal length-limited code (package-merge).
  *  tile_steps    symbols per lane in one tile of 32 lanes: a multiple of 16 up
- *                to 128, or 0 (the default) to choose by size: 128 (4096-weight
+ *                to 256; 0 (the default) to choose by size: 128 (4096-weight
  *                tiles, 0.125 bit per weight of lane offsets) for matrices of at
  *                least 4 M padded weights, 64 from 2 M, else 32, so that a matrix
  *                has about 1024 tiles or more to spread over the SMs, then lowered
  *                in steps of 16 until 32 * tile_steps divides the padded row (for
  *                K = 14336: 112), so that no tile crosses a row; only such
- *                matrices take the tensor-core GEMV (ec_gemv).
+ *                matrices take the tensor-core GEMV (ec_gemv), when the code
+ *                areas of 31 rows of a tile column fit its staging pools.  Tiles
+ *                of up to 256 steps carry fewer lane offsets (0.0625 bit per
+ *                weight at 256), but the batch-1 GEMV runs fastest on 128.
  *  hierarchical  0 (default): the decoder reads two codewords per lookup of a
  *                12-bit window and never branches on the data.  Where a lane's two
  *                consecutive codewords overflow the window (about 0.6 % of pairs

@@ -54,12 +54,13 @@
  * of a 12-bit window.  Wherever the two codewords of a lane's pair (symbols 2m,
  * 2m + 1) would not both fit in 12 bits, the encoder writes the codeword of the
  * shortest-coded exponent (header field huff_fill) in place of one (or both) and
- * lists the weight in a record of the tile: u32 position in the tile (12 bits) |
- * (sign << 7 | mantissa) << 12 | true exponent << 20, ascending positions, so a
+ * lists the weight in a record of the tile: u32 position in the tile (13 bits) |
+ * (sign << 7 | mantissa) << 13 | true exponent << 21, ascending positions, so a
  * record alone gives both the true and the coded weight (MINE section 4,
  * "Escapes", applied to exponent pairs).  The records follow the code area in the
  * tile record, so the copy that stages the code area brings them along (up to the
- * decoder's staging room).  Huffman tiles hold at most 4096 positions.  Without window records every pair that overflows the window, and
+ * decoder's staging room).  Huffman tiles hold at most 8192 positions (steps <=
+ * EC_HUFF_MAX_STEPS).  Without window records every pair that overflows the window, and
  * every codeword longer than 12 bits, is decoded through the hierarchical tables.
  *
  * E8 matrices (kind 3): rows padded to k_pad (a multiple of EC_E8_ROW_ALIGN) with
@@ -80,7 +81,7 @@
 #include <stdint.h>
 
 #define EC_BLOB_MAGIC 0x31434345u /* "ECC1" */
-#define EC_BLOB_VERSION 10u
+#define EC_BLOB_VERSION 11u
 
 #define EC_L1_BITS 12            /* level-1 Huffman window */
 #define EC_SUB_BITS 8            /* bits per sub-table level */
@@ -129,6 +130,10 @@
 #define EC_PAIR_OPEN 0x80000000u   /* pair not complete */
 #define EC_PAIR_FIELDS 0xFF8FFF8Fu /* every bit a valid entry may set */
 #define EC_HUFF_WINDOW_REC 1       /* ec_blob_header.huff_flags: window records in use */
+#define EC_HUFF_MAX_STEPS 256      /* symbols per lane in a Huffman tile */
+#define EC_HREC_POS_MASK 0x1FFFu   /* window record: position in the tile */
+#define EC_HREC_SM_SHIFT 13        /* window record: sign << 7 | mantissa */
+#define EC_HREC_EXP_SHIFT 21       /* window record: true exponent */
 
 /* Huffman sub-table entry (u32), see above. */
 #define EC_ENT_PTR 0x80000000u

@@ -452,7 +452,7 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
     int steps = params ? params->tile_steps : 0;
     const int hier_req = params ? params->hierarchical : 0;
     if (max_len < 1 || max_len > EC_MAX_CODE_LEN) return EC_ERR_INVALID_ARG;
-    if (steps < 0 || steps > 128 || steps % 16) return EC_ERR_INVALID_ARG;
+    if (steps < 0 || steps > EC_HUFF_MAX_STEPS || steps % 16) return EC_ERR_INVALID_ARG;
     if (hier_req != 0 && hier_req != 1) return EC_ERR_INVALID_ARG;
     int64_t nk = 0, k_pad = round_up(k_cols, EC_HUFF_ROW_ALIGN), n_pad = 0, tmp = 0;
     if (k_cols > INT64_MAX - EC_HUFF_ROW_ALIGN) return EC_ERR_OVERFLOW;
@@ -522,7 +522,7 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
 
         /* A lane's exponents in symbol order (lane l owns tile positions 256 (i / 8) +
          * 8 l + i % 8), after window-record substitution; recs gets the records
-         * (position in the tile | sign and mantissa << 12 | true exponent << 20). */
+         * (position in the tile | sign and mantissa << 13 | true exponent << 21). */
         auto lane_exponents = [&](const uint16_t* v, int64_t S, int l, uint8_t* e, std::vector<uint32_t>* recs) {
             for (int64_t i = 0; i < S; ++i) e[i] = (uint8_t)((v[256 * (i >> 3) + 8 * l + (i & 7)] >> 7) & 0xFF);
             if (records)
@@ -530,7 +530,7 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
                     if (recs) {
                         const uint32_t q = (uint32_t)(256 * (i >> 3) + 8 * l + (i & 7)), wq = v[q];
                         const uint32_t sm = ((wq >> 8) & 0x80u) | (wq & 0x7Fu);
-                        recs->push_back(q | (sm << 12) | ((uint32_t)true_e << 20));
+                        recs->push_back(q | (sm << EC_HREC_SM_SHIFT) | ((uint32_t)true_e << EC_HREC_EXP_SHIFT));
                     }
                 });
         };
@@ -670,7 +670,8 @@ extern "C" int ec_encode_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols,
                 }
                 /* lane 0 always starts at byte 0: its slot holds the record count */
                 start[0] = (uint16_t)recs.size();
-                std::sort(recs.begin(), recs.end(), [](uint32_t x, uint32_t y) { return (x & 0xFFF) < (y & 0xFFF); });
+                std::sort(recs.begin(), recs.end(),
+                          [](uint32_t x, uint32_t y) { return (x & EC_HREC_POS_MASK) < (y & EC_HREC_POS_MASK); });
                 std::memcpy(recs_at, recs.data(), 4 * recs.size());
             }
         });
@@ -1599,7 +1600,7 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
     const int64_t align = huff ? EC_HUFF_ROW_ALIGN : e8 ? EC_E8_ROW_ALIGN : EC_RANS_ROW_ALIGN;
     if (h.k_pad != round_up(h.k_cols, align)) return EC_ERR_CORRUPT;
     if (e8 ? (h.k_cols % 8 || h.steps < 1 || h.steps > 32)
-           : huff ? (h.steps < 16 || h.steps > 128 || h.steps % 16) : (h.steps < 1 || (32 * h.steps) % align))
+           : huff ? (h.steps < 16 || h.steps > EC_HUFF_MAX_STEPS || h.steps % 16) : (h.steps < 1 || (32 * h.steps) % align))
         return EC_ERR_CORRUPT;
     int64_t n_pad = 0; /* symbols, or for E8 vectors of 8 weights */
     if (!mul_ok(h.n_rows, e8 ? h.k_pad / 8 : h.k_pad, &n_pad)) return EC_ERR_CORRUPT;
@@ -1617,7 +1618,8 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
             h.max_code_area > h.max_code_bytes)
             return EC_ERR_CORRUPT;
         if (h.window_code_bytes < 0 || h.n_escapes < 0 || (!hrec && h.n_escapes != 0)) return EC_ERR_CORRUPT;
-        if (hrec && (32 * (int64_t)h.steps > 4096 || h.huff_fill < 0 || h.huff_fill > 255)) return EC_ERR_CORRUPT;
+        if (hrec && (32 * (int64_t)h.steps > (int64_t)EC_HREC_POS_MASK + 1 || h.huff_fill < 0 || h.huff_fill > 255))
+            return EC_ERR_CORRUPT;
     } else if (e8) {
         if (h.prob_bits < 9 || h.prob_bits > 12 || h.max_words < 0 ||
             h.table_words != (4 * EC_E8_TABLES * EC_E8_ALPHA + ((int64_t)EC_E8_TABLES << h.prob_bits)) / 4)
@@ -1676,8 +1678,9 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
             for (int l = 1; l < 32; ++l)
                 if (start[l] > code || (l > 1 && start[l] < start[l - 1])) return EC_ERR_CORRUPT;
             const uint32_t* rr = (const uint32_t*)(tr + 64 + EC_RAW_BYTES(n_t / 32) + code);
-            for (int64_t i = 0; i < nrec; ++i) /* 12-bit positions inside the tile, ascending */
-                if ((rr[i] >> 28) || (int64_t)(rr[i] & 0xFFFu) >= n_t || (i && (rr[i] & 0xFFFu) <= (rr[i - 1] & 0xFFFu)))
+            for (int64_t i = 0; i < nrec; ++i) /* 13-bit positions inside the tile, ascending */
+                if ((rr[i] >> (EC_HREC_EXP_SHIFT + 8)) || (int64_t)(rr[i] & EC_HREC_POS_MASK) >= n_t ||
+                    (i && (rr[i] & EC_HREC_POS_MASK) <= (rr[i - 1] & EC_HREC_POS_MASK)))
                     return EC_ERR_CORRUPT;
             n_hrec += nrec;
         } else {

@@ -543,11 +543,13 @@ __device__ __forceinline__ void decode8(Lane& s, uint32_t tab, const HierCtx& h,
     w[3] = merge_sm(__funnelshift_r(r1, r1, 8), e3);
 }
 
-/* A window record (12-bit tile position | sign and mantissa << 12 | exponent << 20):
+/* A window record (13-bit tile position | sign and mantissa << 13 | exponent << 21):
  * the BF16 weight with exponent `expo` (the record's own, or the coded one). */
 __device__ __forceinline__ uint32_t rec_weight(uint32_t r, uint32_t expo) {
-    return ((r >> 4) & 0x8000u) | (expo << 7) | ((r >> 12) & 0x7Fu);
+    return ((r >> (EC_HREC_SM_SHIFT + 7 - 15)) & 0x8000u) | (expo << 7) | ((r >> EC_HREC_SM_SHIFT) & 0x7Fu);
 }
+__device__ __forceinline__ uint32_t rec_pos(uint32_t r) { return r & EC_HREC_POS_MASK; }
+__device__ __forceinline__ uint32_t rec_exp(uint32_t r) { return r >> EC_HREC_EXP_SHIFT; }
 
 /* acc += w0 * x0 + w1 * x1 for BF16 pairs w = [w1|w0], x = [x1|x0]; the products are
  * exact and the sums are FP32 (round to nearest). */
@@ -877,10 +879,10 @@ __device__ __forceinline__ float far_records_dot(const uint32_t* far, uint32_t f
                                               uint32_t col_base, uint32_t xrow, uint32_t fill, int lane) {
     float d = 0.f;
     for (uint32_t j = from + (uint32_t)lane; j < n; j += 32) {
-        const uint32_t e = ldg_early(far + j), q = e & 0xFFFu;
+        const uint32_t e = ldg_early(far + j), q = rec_pos(e);
         if (q >= lo && q < hi) {
             const uint32_t xv1 = lds16(xrow + 2u * (col_base + q));
-            d = fma1_bf16(rec_weight(e, e >> 20), xv1, d);
+            d = fma1_bf16(rec_weight(e, rec_exp(e)), xv1, d);
             d = fma1_bf16(rec_weight(e, fill) ^ 0x8000u, xv1, d);
         }
     }
@@ -997,10 +999,10 @@ __global__ void __launch_bounds__(huff_max_warps(B) * 32, 1) huff_gemv_kernel(co
         const uint32_t seg_begin = kTx || r == row0 ? 0u : seg_end - kp;    /* ... of rows < r */
         const uint32_t col_base = kTx ? col0 : col0 - (r - row0) * kp;      /* column = col_base + position */
         for (uint32_t j = (uint32_t)lane; j < tr.staged; j += 32) {
-            const uint32_t e = lds32(cb + 64 + tr.code + 4 * j), q = e & 0xFFFu;
+            const uint32_t e = lds32(cb + 64 + tr.code + 4 * j), q = rec_pos(e);
             if (q >= seg_begin && q < seg_end) {
                 const uint32_t col = col_base + q;
-                const uint32_t wt = rec_weight(e, e >> 20);
+                const uint32_t wt = rec_weight(e, rec_exp(e));
                 const uint32_t wf = rec_weight(e, (uint32_t)M.fill) ^ 0x8000u; /* minus the coded weight */
 #pragma unroll
                 for (int b = 0; b < B; ++b) {
@@ -1531,13 +1533,13 @@ __global__ void __launch_bounds__(kMaxHW * 32, 1) huff_mma_kernel(const __grid_c
                     while (rc.x < rc.y) {
                         const uint32_t idx = rc.x + (uint32_t)lane;
                         const uint32_t e = idx < rc.y ? lds32(cb + 64 + cbytes + 4 * idx) : 0xFFFFFFFFu;
-                        const uint32_t q = e & 0xFFFu;
+                        const uint32_t q = rec_pos(e);
                         const bool in = idx < rc.y && q < 256u * (uint32_t)(ch + 1);
                         if (in) {
                             const uint32_t lr = (q >> 3) & 31u;
                             const uint32_t at = opb + (lr >> 3) * kMmaAtomBytes + (((lr & 7u) ^ (uint32_t)(d & 7)) << 4) +
                                                 4096u + (uint32_t)d * 128u + 2u * (q & 7u);
-                            const uint32_t wt = rec_weight(e, e >> 20);
+                            const uint32_t wt = rec_weight(e, rec_exp(e));
                             asm volatile("st.shared.u16 [%0], %1;" ::"r"(at), "h"((unsigned short)wt) : "memory");
                         }
                         const uint32_t n = (uint32_t)__popc(__ballot_sync(kFull, in));
@@ -1819,9 +1821,9 @@ __global__ void gemm_reduce_kernel(const float* __restrict__ part, int ksplit, i
 __device__ __forceinline__ void decode_records(uint32_t recs, uint32_t staged, const uint32_t* far, uint32_t nrec,
                                             const HuffMat& M, int64_t start, int lane) {
     for (uint32_t j = (uint32_t)lane; j < nrec; j += 32) {
-        const uint32_t e = j < staged ? lds32(recs + 4 * j) : __ldg(far + j), q = e & 0xFFFu;
+        const uint32_t e = j < staged ? lds32(recs + 4 * j) : __ldg(far + j), q = rec_pos(e);
         const int64_t f = start + q, rr = f / M.k_pad, cc = f - rr * M.k_pad;
-        if (cc < M.k_cols) M.out[(rr - M.out_row0) * M.out_ld + cc] = (uint16_t)rec_weight(e, e >> 20);
+        if (cc < M.k_cols) M.out[(rr - M.out_row0) * M.out_ld + cc] = (uint16_t)rec_weight(e, rec_exp(e));
     }
 }
 
@@ -3266,12 +3268,29 @@ int encode_x_map(CUtensorMap* map, const uint16_t* x, int64_t K, int rows) {
     return r == CUDA_SUCCESS ? EC_OK : EC_ERR_CUDA;
 }
 
+/* Whether the tensor-core kernel's fixed shared memory (two chunk buffers, the pair
+ * tables, the staged sub-tables and two pools of one item's code areas) fits the
+ * 227 KB a block may have on sm_103a (the same sums as huff_mma makes). */
+bool mma_fits(const ec_matrix* const* Ws, int count) {
+    int used = 0;
+    int64_t window = 0;
+    for (int k = 0; k < count; ++k) {
+        const int n = Ws[k]->hdr.huff_sub_tables;
+        if (n > 0 && used + n <= kSubSmemTables) used += n;
+        window = std::max<int64_t>(window, Ws[k]->hdr.window_code_bytes);
+    }
+    const size_t fixed = mma_fixed_bytes(2) + (size_t)count * kPairTabBytes + 4 * 256 * (size_t)used +
+                         2 * (size_t)((window + 15) & ~int64_t(15));
+    return fixed <= 232448;
+}
+
 /* Huffman GEMVs from mma_min_batch() on, on matrices whose tiles lie inside rows and
- * rows of x that TMA can address (16-byte stride), take the tensor-core kernel. */
+ * rows of x that TMA can address (16-byte stride), take the tensor-core kernel when
+ * its buffers fit (not for the widest tiles of long rows). */
 bool use_mma(const ec_matrix* const* Ws, int count, int batch) {
     bool mma = batch >= mma_min_batch() && Ws[0]->hdr.k_cols % 8 == 0;
     for (int k = 0; k < count && mma; ++k) mma = mma_layout(Ws[k]);
-    return mma;
+    return mma && mma_fits(Ws, count);
 }
 
 /* ---- not in the Huffman GEMV: begin ---- */

@@ -156,16 +156,16 @@ def lane_starts(dev, rec):
 
 def tile_records(h, dev, t, with_sm=False):
     """Window records of tile t: (position, true exponent, coded exponent[, sign/mantissa byte])
-    from 12-bit position | sign and mantissa << 12 | exponent << 20."""
+    from 13-bit position | sign and mantissa << 13 | exponent << 21."""
     rec, S, raw_bytes, nrec, _, area_end = tile_layout(h, dev, t)
     assert nrec == 0 or h["huff_flags"] & 1
     er = np.frombuffer(dev, np.uint32, nrec, area_end)
     out = []
     for i in range(nrec):
         r = int(er[i])
-        assert r >> 28 == 0
-        rec = (r & 0xFFF, (r >> 20) & 0xFF, h["huff_fill"])
-        out.append(rec + ((r >> 12) & 0xFF,) if with_sm else rec)
+        assert r >> 29 == 0
+        rec = (r & 0x1FFF, (r >> 21) & 0xFF, h["huff_fill"])
+        out.append(rec + ((r >> 13) & 0xFF,) if with_sm else rec)
     return out
 
 
@@ -272,12 +272,14 @@ def walk_pair_table(blob: bytes):
 
 
 @pytest.mark.parametrize("hier", [False, True])
-@pytest.mark.parametrize("case", ["llama", "fib24", "fib12", "one_symbol", "all_patterns"])
+@pytest.mark.parametrize("case", ["llama", "fib24", "fib12", "fib12_256", "one_symbol", "all_patterns"])
 def test_pair_table_walk_decodes_exponents(ec, case, hier):
     if case == "llama":
         w = synth.llama_bf16(2010, 24, 2048)
         W = ec.encode_bf16(w, device=-1, hierarchical=hier)
     elif case.startswith("fib"):
+        steps = 256 if case.endswith("_256") else 0  # 8192-position tiles: records past position 4095
+        case = case[:5]
         fib = [1, 1]
         while len(fib) < 30:
             fib.append(fib[-1] + fib[-2])
@@ -285,7 +287,10 @@ def test_pair_table_walk_decodes_exponents(ec, case, hier):
         rng = np.random.default_rng(1)
         rng.shuffle(e)
         w = ((e.astype(np.uint16) << 7) | (np.arange(e.size) % 128).astype(np.uint16)).reshape(-1, 4096)[:8]
-        W = ec.encode_bf16(w, max_code_len=int(case[3:]), device=-1, hierarchical=hier)
+        W = ec.encode_bf16(w, max_code_len=int(case[3:]), tile_steps=steps, device=-1, hierarchical=hier)
+        if steps and not hier:
+            h0, d0 = parse(W.serialize())
+            assert max(q for t in range(h0["n_tiles"]) for q, *_ in tile_records(h0, d0, t)) >= 4096
         # L=24: codewords longer than the window reach the sub-tables (or, with window
         # records, are coded as the shortest codeword and recorded);
         # L=12: the longest codeword fills the window exactly
@@ -344,7 +349,8 @@ def test_window_records_bound(ec, hier):
     assert 8 * 4 * h["n_escapes"] / w.size < 0.2  # records cost well under 0.2 bit per weight
 
 
-@pytest.mark.parametrize("shape,steps", [((7, 13), 128), ((3, 300), 32), ((40, 1024), 64), ((2, 4097), 128)])
+@pytest.mark.parametrize("shape,steps", [((7, 13), 128), ((3, 300), 32), ((40, 1024), 64), ((2, 4097), 128),
+                                         ((6, 8192), 256), ((5, 14336), 224), ((3, 5000), 240)])
 def test_huffman_blob_reads_back(ec, shape, steps):
     w = synth.llama_bf16(2007, *shape)
     W = ec.encode_bf16(w, tile_steps=steps, device=-1)
@@ -531,7 +537,8 @@ def test_deserialize_rejects_structural_corruption(ec, kind):
         assert e.value.code == -5, name
 
 
-@pytest.mark.parametrize("shape,steps", [((300, 4096), 128), ((70, 14336), 0), ((40, 1000), 64), ((5, 300), 16)])
+@pytest.mark.parametrize("shape,steps", [((300, 4096), 128), ((70, 14336), 0), ((40, 1000), 64), ((5, 300), 16),
+                                         ((40, 14336), 224)])
 def test_huffman_window_size_matches_tiles(ec, shape, steps):
     """The header's largest 31-row window of one tile column (64 bytes of lane
     starts plus the code area per tile), recomputed from the tile offsets."""
@@ -563,7 +570,7 @@ def test_gemv_path_dispatch(ec):
     assert ec.gemv_path(Wodd, 16) == "cuda_cores"
     Wx = ec.encode_bf16(synth.llama_bf16(3402, 8, 14336), tile_steps=128, device=-1)  # tiles cross rows
     assert ec.gemv_path(Wx, 16) == "cuda_cores"
-    Wy = ec.encode_bf16(synth.llama_bf16(3403, 8, 14336), device=-1)  # automatic tiles: 112 steps, inside rows
+    Wy = ec.encode_bf16(synth.llama_bf16(3403, 8, 14336), device=-1)  # automatic tiles: 32 steps, inside rows
     assert ec.gemv_path(Wy, 16) == "tensor_cores"
     assert ec.gemv_path([Wy, Wx], 16) == "cuda_cores"  # one matrix without the layout: the whole group
     R = ec.encode_rans(*synth.make_rans_case(0, 8, 4096), device=-1)
@@ -897,3 +904,4 @@ def test_validator_survives_random_corruption(ec, kind):
             ec.deserialize(bytes(x), device=-1)
         except ec.EcError as e:
             assert e.code == -5
+

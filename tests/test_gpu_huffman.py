@@ -62,7 +62,7 @@ def test_all_65536_patterns_round_trip(ec):
 
 
 @pytest.mark.parametrize("shape", [(1, 1), (7, 13), (1, 4096), (4096, 1), (3, 300), (5, 1000), (33, 2049)])
-@pytest.mark.parametrize("steps", [32, 128])
+@pytest.mark.parametrize("steps", [32, 128, 256])
 def test_round_trip_ragged_shapes(ec, shape, steps):
     w = synth.llama_bf16(2100 + shape[0], *shape)
     W = ec.encode_bf16(w, tile_steps=steps)
@@ -98,6 +98,21 @@ def test_gemv_parity(ec, shape, batch):
     W = ec.encode_bf16(w)
     y_ref, a_ref = O.gemv_bf16(w, x)
     check_gemv(gemv_gpu(ec, W, x, shape[0]), y_ref, a_ref, f"{shape} b={batch}")
+
+
+@pytest.mark.parametrize("shape,steps", [((48, 8192), 256), ((40, 14336), 224), ((33, 4096), 256), ((17, 5000), 240)])
+@pytest.mark.parametrize("batch", [1, 3, 16])
+def test_gemv_parity_large_tiles(ec, shape, steps, batch):
+    """Tiles of up to 8192 weights: inside rows (x from tensor memory at batch 1), two
+    rows per tile, and tiles that cross rows anywhere; window records past position
+    4095 fold into their rows."""
+    w = synth.llama_bf16(2250 + steps, *shape)
+    x = synth.make_x(2250, batch, shape[1])
+    W = ec.encode_bf16(w, tile_steps=steps, max_code_len=10)  # a short window: many records
+    assert W.stats()["n_records"] > 0
+    y_ref, a_ref = O.gemv_bf16(w, x)
+    check_gemv(gemv_gpu(ec, W, x, shape[0]), y_ref, a_ref, f"{shape} steps={steps} b={batch}")
+    assert np.array_equal(decode_gpu(ec, W, *shape), w)
 
 
 def test_gemv_group_matches_individual(ec):
