@@ -641,7 +641,7 @@ def aggregate_ranks(torch, dist, us_local: float, world: int, device: str):
 
 
 # ------------------------------------------------------------------ main
-PROFILE_CASES = ("gemm", "bf16_gemm", "exp", "rans_pair", "decode", "fp8_t32")
+PROFILE_CASES = ("gemm", "bf16_gemm", "exp", "rans_pair", "decode", "fp8_t32", "e8", "mma")
 
 
 def profile_case(name: str, batch: int) -> None:
@@ -650,7 +650,9 @@ def profile_case(name: str, batch: int) -> None:
     8B stack at `batch`; bf16_gemm: the tcgen05 GEMM on layer 0's gate matrix
     uncompressed; exp: the rANS exponent codec's GEMV on layer 0's gate matrix; rans_pair:
     the 4-bit pair-symbol GEMV on 14336 x 4096; decode: ec_decode_batch of layer 0;
-    fp8_t32: the FP8 GEMV with a 32-code table on 14336 x 4096."""
+    fp8_t32: the FP8 GEMV with a 32-code table on 14336 x 4096; e8: the E8 decode to
+    BF16 of 14336 x 4096; mma: the tensor-core GEMV of layer 0's gate/up group at
+    `batch` (6..64)."""
     import torch
     import lossless_entropy_coded_gb300 as ec
     import synth
@@ -684,6 +686,18 @@ def profile_case(name: str, batch: int) -> None:
         Ws = [ec.encode_bf16(synth.make_weights(s), device=0) for s in specs]
         outs = [torch.empty((s.n_rows, s.k_cols), dtype=torch.int16, device=dev) for s in specs]
         run = lambda: ec.decode_batch(Ws, outs)
+    elif name == "e8":
+        q2, r8, s8 = synth.make_e8_case(7500, 14336, 4096)
+        W = ec.encode_e8(q2, r8, s8, device=0)
+        out = torch.empty((14336, 4096), dtype=torch.int16, device=dev)
+        run = lambda: ec.decode_as(W, out, "bf16")
+    elif name == "mma":
+        gu = [s for s in specs if s.name.split(".")[1] in ("gate", "up")]
+        Ws = [ec.encode_bf16(synth.make_weights(s), device=0) for s in gu]
+        x = xs_of(gu[0].k_cols)
+        ys = [torch.empty((batch, s.n_rows), device=dev) for s in gu]
+        assert ec.gemv_path(Ws, batch) == "tensor_cores"
+        run = lambda: ec.gemv_group(Ws, x, ys, batch=batch)
     else:
         codes, r = synth.make_fp8_case(8000, 14336, 4096)
         W = ec.encode_fp8(codes, r, top_t=32, device=0)
