@@ -117,12 +117,21 @@ typedef struct {
  *  codes_per_symbol  1 (default; 0 means 1): one 4-bit code per rANS symbol;
  *                    2: a symbol is the pair of a lane's consecutive codes (MINE's
  *                    k-tuple symbols), 256 symbols, half the decode steps, at
- *                    about 0.01 bit per code over single codes with b = 12 */
+ *                    about 0.01 bit per code over single codes with b = 12
+ *  values            what a 4-bit code means: EC_RANS_VALUES_INT4 (default, 0): a
+ *                    signed integer, codes_host in [-8, 7] (int2 and int3 codes are
+ *                    the subranges [-2, 1] and [-4, 3]); EC_RANS_VALUES_FP4_E2M1: an
+ *                    FP4 E2M1 pattern (OCP Microscaling: sign, 2 exponent bits of bias
+ *                    1, 1 mantissa bit), codes_host in [0, 15]; the weight is the
+ *                    code's value times its group's FP16 scale (MINE, "Data Types") */
+#define EC_RANS_VALUES_INT4 0
+#define EC_RANS_VALUES_FP4_E2M1 1
 typedef struct {
     int32_t prob_bits;
     int32_t tile_syms;
     int32_t group;
     int32_t codes_per_symbol;
+    int32_t values;
 } ec_rans_params;
 
 /* E8 lattice codec parameters (NULL = defaults).
@@ -209,9 +218,10 @@ typedef struct {
 int ec_encode_bf16(const uint16_t* w_host, int64_t n_rows, int64_t k_cols, const ec_huff_params* params,
                    int device, ec_matrix** out);
 
-/* Encode 4-bit codes [n_rows, k_cols] (int8 values in [-8, 7], host) with FP16 scales
+/* Encode 4-bit codes [n_rows, k_cols] (int8 host values: in [-8, 7], or FP4 E2M1
+ * patterns in [0, 15] with params->values = EC_RANS_VALUES_FP4_E2M1) with FP16 scales
  * [n_rows, ceil(k_cols / group)] (host, bit patterns) as rANS tiles and upload them.
- * The represented weight is w = code * scale (exact in FP32). */
+ * The represented weight is w = value(code) * scale (exact in FP32). */
 int ec_encode_rans(const int8_t* codes_host, const uint16_t* scales_f16_host, int64_t n_rows, int64_t k_cols,
                    const ec_rans_params* params, int device, ec_matrix** out);
 

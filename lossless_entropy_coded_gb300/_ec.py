@@ -51,7 +51,10 @@ class HuffParams(ctypes.Structure):
 
 class RansParams(ctypes.Structure):
     _fields_ = [("prob_bits", ctypes.c_int32), ("tile_syms", ctypes.c_int32), ("group", ctypes.c_int32),
-                ("codes_per_symbol", ctypes.c_int32)]
+                ("codes_per_symbol", ctypes.c_int32), ("values", ctypes.c_int32)]
+
+
+_RANS_VALUES = {"int4": 0, "fp4": 1}  # EC_RANS_VALUES_INT4, EC_RANS_VALUES_FP4_E2M1
 
 
 class E8Params(ctypes.Structure):
@@ -207,13 +210,14 @@ def encode_bf16(w, max_code_len: int = 12, tile_steps: int = 0, device: int = 0,
 
 
 def encode_rans(codes, scales_f16, prob_bits: int = 12, tile_syms: int = 4096, group: int = 128,
-                device: int = 0, codes_per_symbol: int = 1) -> Matrix:
-    """rANS-encode host int8 codes [N, K] in [-8, 7] with FP16 scales [N, ceil(K/group)]
+                device: int = 0, codes_per_symbol: int = 1, values: str = "int4") -> Matrix:
+    """rANS-encode host int8 codes [N, K] with FP16 scales [N, ceil(K/group)]: values
+    "int4" takes signed codes in [-8, 7], "fp4" FP4 E2M1 patterns in [0, 15]
     (codes_per_symbol 2: one symbol per pair of a lane's consecutive codes)."""
     n, k = int(codes.shape[0]), int(codes.shape[1])
     pc, kc = _host_ptr(codes)
     ps, ks = _host_ptr(scales_f16)
-    prm = RansParams(prob_bits, tile_syms, group, codes_per_symbol)
+    prm = RansParams(prob_bits, tile_syms, group, codes_per_symbol, _RANS_VALUES[values])
     h = ctypes.c_void_p()
     _check(lib.ec_encode_rans(pc, ps, n, k, ctypes.byref(prm), device, ctypes.byref(h)), "ec_encode_rans")
     return Matrix(h.value, n, k, EC_KIND_RANS_INT4, device)

@@ -199,7 +199,9 @@ typedef struct {
     int32_t huff_sub_tables;          /* Huffman: hierarchical sub-tables after the pair table */
     int32_t huff_fill;                /* Huffman with window records: the exponent coded in place of a recorded one */
     int32_t max_code_area;            /* Huffman: largest code area of any tile (records excluded) */
-    uint8_t pad[256 - 4 * 4 - 8 * 10 - 4 * 8 - 8 * 3 - 4 * 4];
+    int32_t rans_values;              /* rANS 4-bit codes: EC_RANS_VALUES_INT4 (code + 8 in a symbol) or
+                                       * EC_RANS_VALUES_FP4_E2M1 (the symbol is the E2M1 pattern) */
+    uint8_t pad[256 - 4 * 4 - 8 * 10 - 4 * 8 - 8 * 3 - 4 * 5];
 } ec_blob_header;
 
 #endif /* EC_FORMAT_H_ */

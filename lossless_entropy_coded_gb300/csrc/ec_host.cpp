@@ -704,6 +704,8 @@ extern "C" int ec_encode_rans(const int8_t* codes, const uint16_t* scales, int64
     const int T = params ? params->tile_syms : 4096;
     const int group = params ? params->group : 128;
     const int k = params && params->codes_per_symbol ? params->codes_per_symbol : 1;
+    const int values = params ? params->values : EC_RANS_VALUES_INT4;
+    if (values != EC_RANS_VALUES_INT4 && values != EC_RANS_VALUES_FP4_E2M1) return EC_ERR_INVALID_ARG;
     if ((b_req != 0 && (b_req < 9 || b_req > 15)) || T < 32 || T % EC_RANS_ROW_ALIGN || T > 65536)
         return EC_ERR_INVALID_ARG;
     if (k != 1 && k != 2) return EC_ERR_INVALID_ARG;
@@ -719,8 +721,20 @@ extern "C" int ec_encode_rans(const int8_t* codes, const uint16_t* scales, int64
 
     return guarded([&]() -> int {
         const int64_t K = k_cols;
+        /* FP4 E2M1 patterns 0..15 are coded as the 4-bit codes c - 8: the stream and
+         * tables are the integer codec's, the header says how the decoder reads them */
+        std::vector<int8_t> shifted;
+        const int8_t* cv = codes;
+        if (values == EC_RANS_VALUES_FP4_E2M1) {
+            shifted.resize((size_t)nk);
+            for (int64_t i = 0; i < nk; ++i) {
+                if (codes[i] < 0 || codes[i] > 15) return EC_ERR_INVALID_ARG;
+                shifted[(size_t)i] = (int8_t)(codes[i] - 8);
+            }
+            cv = shifted.data();
+        }
         for (int64_t i = 0; i < nk; ++i)
-            if (codes[i] < -8 || codes[i] > 7) return EC_ERR_INVALID_ARG;
+            if (cv[i] < -8 || cv[i] > 7) return EC_ERR_INVALID_ARG;
         ec_matrix* m = new_matrix();
         if (!m) return EC_ERR_OOM;
         const int nsym = k == 1 ? 16 : 256;
@@ -730,7 +744,7 @@ extern "C" int ec_encode_rans(const int8_t* codes, const uint16_t* scales, int64
             return k == 1 ? v[32 * j + l] + 8 : 16 * (v[64 * j + l] + 8) + (v[64 * j + 32 + l] + 8);
         };
         if (k == 1) {
-            for (int64_t i = 0; i < nk; ++i) m->counts[codes[i] + 8]++;
+            for (int64_t i = 0; i < nk; ++i) m->counts[cv[i] + 8]++;
             m->counts[8] += (uint64_t)(n_rows * (KP - K));
         } else { /* histogram of the pair symbols over the padded tile layout */
             std::vector<std::array<uint64_t, 256>> part(host_threads());
@@ -743,7 +757,7 @@ extern "C" int ec_encode_rans(const int8_t* codes, const uint16_t* scales, int64
                     std::vector<int8_t> v(T);
                     for (int64_t t = lo; t < hi; ++t) {
                         const int64_t base = t * T, n_t = std::min<int64_t>(T, n_pad - base), S = n_t / 32;
-                        gather_padded(codes, K, KP, base, n_t, v.data());
+                        gather_padded(cv, K, KP, base, n_t, v.data());
                         for (int64_t j = 0; j < S / 2; ++j)
                             for (int l = 0; l < 32; ++l) hcount[symbol(v.data(), j, l)]++;
                     }
@@ -776,7 +790,7 @@ extern "C" int ec_encode_rans(const int8_t* codes, const uint16_t* scales, int64
             std::vector<int8_t> v(T);
             for (int64_t t = lo; t < hi; ++t) {
                 const int64_t base = t * T, n_t = std::min<int64_t>(T, n_pad - base), S = n_t / 32;
-                gather_padded(codes, K, KP, base, n_t, v.data());
+                gather_padded(cv, K, KP, base, n_t, v.data());
                 uint64_t x[32];
                 for (int l = 0; l < 32; ++l) x[l] = 1u << 16;
                 stack.clear();
@@ -826,6 +840,7 @@ extern "C" int ec_encode_rans(const int8_t* codes, const uint16_t* scales, int64
         h.prob_bits = b;
         h.max_words = (int32_t)max_words;
         h.rans_tuple = k;
+        h.rans_values = values;
 
         std::vector<uint8_t> blob((size_t)h.blob_bytes, 0);
         std::memcpy(blob.data(), &h, sizeof h);
@@ -1595,6 +1610,7 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
         h.kind != EC_KIND_RANS_FP8 && h.kind != EC_KIND_RANS_EXP)
         return EC_ERR_CORRUPT;
     if (h.n_rows < 0 || h.k_cols < 0 || h.k_cols > INT64_MAX / 2) return EC_ERR_CORRUPT;
+    if (h.kind != EC_KIND_RANS_INT4 && h.rans_values != 0) return EC_ERR_CORRUPT;
     const bool huff = h.kind == EC_KIND_HUFFMAN_BF16, e8 = h.kind == EC_KIND_E8, fp8 = h.kind == EC_KIND_RANS_FP8,
                ex = h.kind == EC_KIND_RANS_EXP;
     const int64_t align = huff ? EC_HUFF_ROW_ALIGN : e8 ? EC_E8_ROW_ALIGN : EC_RANS_ROW_ALIGN;
@@ -1639,6 +1655,7 @@ int validate_blob(const uint8_t* b, int64_t bytes) {
             return EC_ERR_CORRUPT;
         if (h.rans_tuple != 1 && h.rans_tuple != 2) return EC_ERR_CORRUPT;
         if (h.rans_tuple == 2 && h.prob_bits > 12) return EC_ERR_CORRUPT;
+        if (h.rans_values != EC_RANS_VALUES_INT4 && h.rans_values != EC_RANS_VALUES_FP4_E2M1) return EC_ERR_CORRUPT;
     }
     if (!mul_ok(h.table_words, 4, &t4) || !add_ok(h.table_off, t4, &end)) return EC_ERR_CORRUPT;
     if (!huff) { /* rANS: FP16 group scales; E8 and FP8: FP32 row scales; exponents: sign / mantissa bytes */

@@ -138,6 +138,7 @@ struct RansMat {
     int32_t last_steps;         /* symbols per lane of the last tile */
     uint32_t rec16;             /* records region size in 16-byte units */
     int32_t tuple;              /* codes per symbol: 1 or 2 */
+    int32_t values;             /* EC_RANS_VALUES_*: a 4-bit symbol s is the integer s - 8, or an FP4 E2M1 pattern */
 };
 
 struct RansArgs {
@@ -1945,6 +1946,17 @@ __device__ __forceinline__ void stage_x_perm(uint16_t* xs, const uint16_t* __res
 /* x'-index of column c (the permutation above). */
 __device__ __forceinline__ uint32_t x_perm_index(uint32_t c) { return (c & ~127u) + 4u * (c & 31u) + ((c >> 5) & 3u); }
 
+/* The FP32 value of 4-bit symbol s (bits 0..3): the integer s - 8, or with fp4 the
+ * FP4 E2M1 pattern s: bit 3 the sign, bits 1..2 the exponent field e (bias 1), bit
+ * 0 the mantissa m; e = 0 gives m * 0.5, otherwise (1 + m / 2) * 2^(e - 1), i.e. the
+ * FP32 pattern with biased exponent 126 + e and mantissa m << 22. */
+__device__ __forceinline__ float code_value(uint32_t s, bool fp4) {
+    if (!fp4) return __int_as_float(0x4B000000 | s) - 8388616.0f; /* (2^23 + s) - (2^23 + 8) */
+    const uint32_t e = (s >> 1) & 3u, m = s & 1u;
+    const uint32_t mag = e ? ((126u + e) << 23) | (m << 22) : (m ? 0x3F000000u : 0u);
+    return __uint_as_float(mag | ((s & 8u) << 28));
+}
+
 /* ============================================================ rANS kernels */
 /*
  * One warp per 4096-symbol tile (EntroPack, independent rANS tiles): lane l holds
@@ -2028,10 +2040,11 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) rans_kernel(const _
     const int64_t gw = (int64_t)blockIdx.x * nwarp + warp, nw = (int64_t)gridDim.x * nwarp;
     RansTile cur{};
     float sc = 0.f; /* lane g: scale of group g of the current tile */
-    if (kGemv) /* entry i: [bf16(c1) | bf16(c0)], c0 = (i >> 4) - 8 (the earlier step), c1 = (i & 15) - 8 */
+    if (kGemv) /* entry i: [bf16(v1) | bf16(v0)], v0 the value of symbol i >> 4 (the earlier step), v1 of i & 15 */
         for (int i = threadIdx.x; i < 256; i += blockDim.x) {
-            const uint32_t c0 = __bfloat16_as_ushort(__int2bfloat16_rn((i >> 4) - 8));
-            const uint32_t c1 = __bfloat16_as_ushort(__int2bfloat16_rn((i & 15) - 8));
+            const bool fp4 = M.values == EC_RANS_VALUES_FP4_E2M1;
+            const uint32_t c0 = __bfloat16_as_ushort(__float2bfloat16_rn(code_value((uint32_t)i >> 4, fp4)));
+            const uint32_t c1 = __bfloat16_as_ushort(__float2bfloat16_rn(code_value((uint32_t)i & 15u, fp4)));
             asm volatile("st.shared.u32 [%0], %1;" ::"r"(lut_s + 4u * (uint32_t)i), "r"(c0 | (c1 << 16)) : "memory");
         }
     if (gw < M.n_tiles) {
@@ -2164,13 +2177,13 @@ __global__ void __launch_bounds__(rans_max_warps(B) * 32, 1) rans_kernel(const _
                     const uint32_t v = lds16_if(need, wbase + 2 * idx, 0u);
                     x = need ? x * 65536u + v : x; /* v < 2^16 and x < 2^16: the shift-or as one multiply-add */
                     wp += __popc(bal);
-                    /* a code + 8 in the low 4 bits: (float)code = (2^23 + code + 8) - (2^23 + 8).  Pairs:
-                     * the lane's earlier step in bits 4..7, the later one in bits 0..3 */
+                    /* a symbol in the low 4 bits (pairs: the lane's earlier step in bits 4..7, the
+                     * later one in bits 0..3), its value exact in FP32 */
                     const int nc = kPair ? 2 : 1;
 #pragma unroll
                     for (int q = 0; q < nc; ++q) {
                         const uint32_t nib = kPair ? (q == 0 ? (e >> 4) & 15u : e & 15u) : e & 15u;
-                        const float cf = __int_as_float(0x4B000000 | nib) - 8388616.0f;
+                        const float cf = code_value(nib, M.values == EC_RANS_VALUES_FP4_E2M1);
                         const uint32_t c = col + 32 * (nc * s + q);
                         if (c < K) M.out[row * K + c] = __bfloat16_as_ushort(__float2bfloat16_rn(cf * scale));
                     }
@@ -2998,6 +3011,7 @@ RansMat rans_desc(const ec_matrix* W) {
     m.last_steps = h.n_tiles > 0 ? (int32_t)((h.n_rows * h.k_pad - (h.n_tiles - 1) * T) / 32) : 0;
     m.rec16 = (uint32_t)(m.records_bytes / 16);
     m.tuple = h.rans_tuple;
+    m.values = h.rans_values;
     return m;
 }
 

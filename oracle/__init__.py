@@ -25,6 +25,9 @@ Functions and the passages they follow (page titles and sections):
                                 EntroPack sec. 3.7 and appendix B.1 (FP8 / INT8 output); the OCP
                                 FP8 E4M3 format
   gemv_bf16 / gemv_rans         y = W x with FP64 accumulation
+  e2m1_value                    the OCP Microscaling FP4 E2M1 format (MINE "Data Types" names
+                                FP4 among the k-tuple types); rans_dequant_bf16 / gemv_rans
+                                take values="fp4" for 4-bit codes that are E2M1 patterns
 
 Every function is pinned by tests in tests/test_oracle_*.py against the pages'
 worked examples, closed forms, invariants or brute force.
@@ -98,6 +101,9 @@ def _L():
         "orc_rans_offsets": ([vp], vp),
         "orc_rans_payload_mut": ([vp], vp),
         "orc_rans_dequant_bf16": ([vp, vp, i64, i64, i32, vp], None),
+        "orc_rans_dequant_bf16_v": ([vp, vp, i64, i64, i32, i32, vp], None),
+        "orc_gemv_rans_v": ([vp, vp, i64, i64, i32, i32, vp, i32, vp, i64, vp, vp], None),
+        "orc_e2m1_value": ([i32], ctypes.c_double),
         "orc_gemv_bf16": ([vp, i64, i64, vp, i32, vp, i64, vp, vp], None),
         "orc_gemv_rans": ([vp, vp, i64, i64, i32, vp, i32, vp, i64, vp, vp], None),
         "orc_e8_fields": ([vp, vp], i32),
@@ -704,12 +710,21 @@ def gemv_fp8(codes: np.ndarray, row_scales: np.ndarray, x: np.ndarray, rows=None
     return y, a
 
 
-def rans_dequant_bf16(codes: np.ndarray, scales: np.ndarray, group: int = 128) -> np.ndarray:
+_VALUES = {"int4": 0, "fp4": 1}
+
+
+def e2m1_value(code: int) -> float:
+    """The FP4 E2M1 value of a 4-bit pattern (OCP Microscaling definition)."""
+    return float(_L().orc_e2m1_value(int(code)))
+
+
+def rans_dequant_bf16(codes: np.ndarray, scales: np.ndarray, group: int = 128, values: str = "int4") -> np.ndarray:
+    """BF16 of value(code) * scale: values "int4" (codes in [-8, 7]) or "fp4" (E2M1 patterns 0..15)."""
     c = np.ascontiguousarray(codes, dtype=np.int8)
     s = np.ascontiguousarray(scales, dtype=np.uint16)
     n, k = c.shape
     out = np.zeros((n, k), dtype=np.uint16)
-    _L().orc_rans_dequant_bf16(_p(c), _p(s), n, k, group, _p(out))
+    _L().orc_rans_dequant_bf16_v(_p(c), _p(s), n, k, group, _VALUES[values], _p(out))
     return out
 
 
@@ -735,7 +750,8 @@ def gemv_bf16(w: np.ndarray, x: np.ndarray, rows=None):
     return y, a
 
 
-def gemv_rans(codes: np.ndarray, scales: np.ndarray, x: np.ndarray, group: int = 128, rows=None):
+def gemv_rans(codes: np.ndarray, scales: np.ndarray, x: np.ndarray, group: int = 128, rows=None,
+              values: str = "int4"):
     c = np.ascontiguousarray(codes, dtype=np.int8)
     s = np.ascontiguousarray(scales, dtype=np.uint16)
     x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.uint16)
@@ -745,6 +761,6 @@ def gemv_rans(codes: np.ndarray, scales: np.ndarray, x: np.ndarray, group: int =
     nr = nsel if r is not None else n
     y = np.zeros((batch, nr), dtype=np.float64)
     a = np.zeros((batch, nr), dtype=np.float64)
-    _L().orc_gemv_rans(_p(c), _p(s), n, k, group, _p(x), batch, _p(r) if r is not None else None, nsel,
-                       _p(y), _p(a))
+    _L().orc_gemv_rans_v(_p(c), _p(s), n, k, group, _VALUES[values], _p(x), batch, _p(r) if r is not None else None,
+                         nsel, _p(y), _p(a))
     return y, a

@@ -803,19 +803,38 @@ const uint32_t* orc_rans_states(const orc_rans* r) { return r->states; }
 const uint32_t* orc_rans_offsets(const orc_rans* r) { return r->offsets; }
 uint16_t* orc_rans_payload_mut(orc_rans* r) { return r->payload; }
 
-/* Dequantised weight w = code * scale in FP32 (exact: a 4-bit integer times an
- * 11-bit significand), scale from group floor(j / group) of row i. */
-static float rans_weight(int8_t code, const uint16_t* scales, int64_t i, int64_t j, int64_t k_cols, int group) {
+/* FP4 E2M1 (the OCP Microscaling formats' 4-bit float; MINE lists FP4 among the
+ * k-tuple data types, "Data Types", without fixing its value set): bit 3 the sign,
+ * bits 1..2 the exponent field e with bias 1, bit 0 the mantissa bit m; e = 0 is
+ * subnormal, m * 2^-1; otherwise (1 + m / 2) * 2^(e - 1).  No infinities or NaN. */
+double orc_e2m1_value(int code) {
+    const int sign = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+    const double mag = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -mag : mag;
+}
+
+/* Dequantised weight w = value(code) * scale in FP32 (exact: a 4-bit integer, or an
+ * E2M1 value of 2 significant bits, times an 11-bit significand), scale from group
+ * floor(j / group) of row i.  values 0: the code is a signed integer in [-8, 7];
+ * values 1: the code is an FP4 E2M1 pattern in [0, 15]. */
+static float rans_weight(int8_t code, const uint16_t* scales, int64_t i, int64_t j, int64_t k_cols, int group,
+                         int values) {
     const int64_t groups = (k_cols + group - 1) / group;
-    return (float)code * orc_f16_to_f32(scales[i * groups + j / group]);
+    const float v = values ? (float)orc_e2m1_value(code) : (float)code;
+    return v * orc_f16_to_f32(scales[i * groups + j / group]);
 }
 
 /* BF16 (RNE) of the dequantised weights, the dense output of a decode. */
-void orc_rans_dequant_bf16(const int8_t* codes, const uint16_t* scales, int64_t n_rows, int64_t k_cols,
-                           int group, uint16_t* out) {
+void orc_rans_dequant_bf16_v(const int8_t* codes, const uint16_t* scales, int64_t n_rows, int64_t k_cols,
+                             int group, int values, uint16_t* out) {
     for (int64_t i = 0; i < n_rows; ++i)
         for (int64_t j = 0; j < k_cols; ++j)
-            out[i * k_cols + j] = orc_f32_to_bf16_rne(rans_weight(codes[i * k_cols + j], scales, i, j, k_cols, group));
+            out[i * k_cols + j] =
+                orc_f32_to_bf16_rne(rans_weight(codes[i * k_cols + j], scales, i, j, k_cols, group, values));
+}
+void orc_rans_dequant_bf16(const int8_t* codes, const uint16_t* scales, int64_t n_rows, int64_t k_cols,
+                           int group, uint16_t* out) {
+    orc_rans_dequant_bf16_v(codes, scales, n_rows, k_cols, group, 0, out);
 }
 
 /* ===========================================================================
@@ -841,15 +860,16 @@ void orc_gemv_bf16(const uint16_t* w, int64_t n_rows, int64_t k_cols, const uint
     }
 }
 
-void orc_gemv_rans(const int8_t* codes, const uint16_t* scales, int64_t n_rows, int64_t k_cols, int group,
-                   const uint16_t* x, int batch, const int64_t* rows, int64_t n_sel, double* y, double* a) {
+void orc_gemv_rans_v(const int8_t* codes, const uint16_t* scales, int64_t n_rows, int64_t k_cols, int group,
+                     int values, const uint16_t* x, int batch, const int64_t* rows, int64_t n_sel, double* y,
+                     double* a) {
     const int64_t nr = rows ? n_sel : n_rows;
     for (int b = 0; b < batch; ++b) {
         for (int64_t r = 0; r < nr; ++r) {
             const int64_t i = rows ? rows[r] : r;
             double acc = 0.0, mag = 0.0;
             for (int64_t j = 0; j < k_cols; ++j) {
-                const double wv = (double)rans_weight(codes[i * k_cols + j], scales, i, j, k_cols, group);
+                const double wv = (double)rans_weight(codes[i * k_cols + j], scales, i, j, k_cols, group, values);
                 const double p = wv * orc_bf16_to_f64(x[(int64_t)b * k_cols + j]);
                 acc += p;
                 mag += fabs(p);
@@ -858,6 +878,10 @@ void orc_gemv_rans(const int8_t* codes, const uint16_t* scales, int64_t n_rows, 
             a[(int64_t)b * nr + r] = mag;
         }
     }
+}
+void orc_gemv_rans(const int8_t* codes, const uint16_t* scales, int64_t n_rows, int64_t k_cols, int group,
+                   const uint16_t* x, int batch, const int64_t* rows, int64_t n_sel, double* y, double* a) {
+    orc_gemv_rans_v(codes, scales, n_rows, k_cols, group, 0, x, batch, rows, n_sel, y, a);
 }
 
 /* ===========================================================================

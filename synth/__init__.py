@@ -179,6 +179,19 @@ def make_rans_case(shape_index: int, n_rows: int | None = None, k_cols: int | No
     return codes, scales
 
 
+def fp4_codes(seed: int, shape, std: float = 1.6) -> np.ndarray:
+    """4-bit patterns (sign << 3 | k) with k = min(|round_half_even(std * z)|, 7) and the
+    sign of z: a skewed histogram over the 16 patterns, most mass on small k (the
+    patterns are taken as FP4 E2M1 codes by the codec under test)."""
+    c = codes_i8(seed, shape, std=std, lo=-7, hi=7).astype(np.int16)
+    return (((c < 0).astype(np.int16) << 3) | np.abs(c)).astype(np.int8)
+
+
+def make_fp4_case(seed: int, n_rows: int, k_cols: int, group: int = 128):
+    """(codes, FP16 scales ~ U(0.005, 0.03) per `group` weights) of an FP4 matrix."""
+    return fp4_codes(seed, (n_rows, k_cols)), scales_f16(synth_subseed(seed, 9), (n_rows, (k_cols + group - 1) // group))
+
+
 def synth_subseed(seed: int, tag: int) -> int:
     return int(_L().synth_subseed(seed, tag))
 

@@ -83,14 +83,14 @@ def test_argument_validation(ec):
 
 
 # --------------------------------------------------------------- blob reader
-HDR = struct.Struct("<IIii" + "q" * 10 + "i" * 6 + "Ii" + "qqq" + "iiii")
+HDR = struct.Struct("<IIii" + "q" * 10 + "i" * 6 + "Ii" + "qqq" + "iiiii")
 
 
 HDR_KEYS = ["magic", "version", "kind", "steps", "n_rows", "k_cols", "k_pad", "n_tiles", "table_off",
             "table_words", "scales_off", "tile_off_off", "records_off", "blob_bytes", "max_code_bytes",
             "prob_bits", "max_words", "max_len", "rans_tuple", "window_code_bytes", "e8_scale_bits",
             "fp8_table_size", "esc_off_off", "esc_records_off", "n_escapes", "huff_flags", "huff_sub_tables",
-            "huff_fill", "max_code_area"]
+            "huff_fill", "max_code_area", "rans_values"]
 
 
 def hdr_offset(key: str) -> int:
@@ -905,3 +905,35 @@ def test_validator_survives_random_corruption(ec, kind):
         except ec.EcError as e:
             assert e.code == -5
 
+
+
+@pytest.mark.parametrize("tuple_", [1, 2])
+def test_fp4_codes_are_the_integer_stream_of_code_minus_8(ec, tuple_):
+    """values="fp4": E2M1 patterns 0..15 go through the integer codec as c - 8; the
+    header marks the reading and the stream equals the oracle's coding of c - 8."""
+    codes, scales = synth.make_fp4_case(3500, 40, 1000)
+    W = ec.encode_rans(codes, scales, device=-1, codes_per_symbol=tuple_, values="fp4")
+    h, dev = parse(W.serialize())
+    assert h["rans_values"] == 1 and h["rans_tuple"] == tuple_
+    Wi = ec.encode_rans((codes - 8).astype(np.int8), scales, device=-1, codes_per_symbol=tuple_)
+    hi, devi = parse(Wi.serialize())
+    assert hi["rans_values"] == 0
+    # tables, scales, offsets and tiles byte for byte (the integer blob's stream is
+    # the oracle's word for word: test_rans_blob_matches_oracle_stream)
+    assert dev[256:] == devi[256:]
+
+
+def test_fp4_and_int4_code_ranges_are_checked(ec):
+    sc = np.full((1, 1), 0x3C00, np.uint16)
+    with pytest.raises(ec.EcError):
+        ec.encode_rans(np.array([[16]], np.int8), sc, device=-1, values="fp4")
+    with pytest.raises(ec.EcError):
+        ec.encode_rans(np.array([[-1]], np.int8), sc, device=-1, values="fp4")
+    with pytest.raises(ec.EcError):
+        ec.encode_rans(np.array([[8]], np.int8), sc, device=-1)
+    from lossless_entropy_coded_gb300 import _ec
+    import ctypes
+    h = ctypes.c_void_p()
+    c = np.array([[1]], np.int8)
+    assert _ec.lib.ec_encode_rans(c.ctypes.data, sc.ctypes.data, 1, 1, ctypes.byref(_ec.RansParams(12, 4096, 128, 1, 2)),
+                                  -1, ctypes.byref(h)) == _ec.EC_ERR_INVALID_ARG

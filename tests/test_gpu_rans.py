@@ -129,3 +129,44 @@ def test_automatic_table_size_decodes(ec, tuple_):
     assert ec.status() == 0
     y_ref, a_ref = O.gemv_rans(codes, scales, x)
     check_gemv(y.cpu().numpy(), y_ref, a_ref, "automatic table")
+
+
+@pytest.mark.parametrize("tuple_", [1, 2])
+@pytest.mark.parametrize("shape", [(7, 13), (64, 1000), (256, 4096), (33, 14336)])
+def test_fp4_decode_and_gemv(ec, shape, tuple_):
+    """FP4 E2M1 codes (values="fp4"): decode bit-exact with the oracle's BF16 of
+    e2m1(code) * scale; GEMV at batch 1 and 4 within the GEMV tolerance."""
+    codes, scales = synth.make_fp4_case(4400 + shape[0], *shape)
+    W = ec.encode_rans(codes, scales, codes_per_symbol=tuple_, values="fp4")
+    out = torch.zeros(shape, dtype=torch.int16, device="cuda")
+    ec.decode(W, out)
+    assert ec.status() == 0
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), O.rans_dequant_bf16(codes, scales, values="fp4"))
+    for batch in (1, 4):
+        x = synth.make_x(4401, batch, shape[1])
+        y = torch.full((batch, shape[0]), float("nan"), device="cuda")
+        ec.gemv(W, dev(x.view(np.int16)), y, batch=batch)
+        assert ec.status() == 0
+        y_ref, a_ref = O.gemv_rans(codes, scales, x, values="fp4")
+        check_gemv(y.cpu().numpy(), y_ref, a_ref, f"fp4 {shape} k={tuple_} b={batch}")
+
+
+@pytest.mark.parametrize("lo,hi", [(-2, 1), (-4, 3)])
+def test_int2_and_int3_codes_through_pairs(ec, lo, hi):
+    """int2 and int3 codes are subranges of the 4-bit codec: pair symbols over them
+    decode bit-exact and multiply within tolerance."""
+    shape = (96, 4096)
+    codes = synth.codes_i8(4500 + hi, shape, std=1.0, lo=lo, hi=hi)
+    scales = synth.scales_f16(4501, (shape[0], shape[1] // 128))
+    W = ec.encode_rans(codes, scales, codes_per_symbol=2)
+    out = torch.zeros(shape, dtype=torch.int16, device="cuda")
+    ec.decode(W, out)
+    assert ec.status() == 0
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), O.rans_dequant_bf16(codes, scales))
+    x = synth.make_x(4502, 1, shape[1])
+    y = torch.full((1, shape[0]), float("nan"), device="cuda")
+    ec.gemv(W, dev(x.view(np.int16)), y, batch=1)
+    assert ec.status() == 0
+    y_ref, a_ref = O.gemv_rans(codes, scales, x)
+    check_gemv(y.cpu().numpy(), y_ref, a_ref, f"int{hi.bit_length() + 1}")
+    assert W.stats()["bits_per_weight"] < (2.6 if hi == 1 else 3.5)

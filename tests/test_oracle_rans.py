@@ -103,6 +103,37 @@ def test_dequant_bf16_matches_numpy_conversions():
     assert np.array_equal(got, want)
 
 
+# ------------------------------------------------------------------ FP4 values
+# The FP4 E2M1 value set as the OCP Microscaling specification tabulates it (the
+# magnitudes of exponent fields 0..3 with mantissa bit 0, 1), written out here, not
+# derived from the oracle's formula.
+E2M1_MAGNITUDES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_values_match_the_format_table():
+    vals = [O.e2m1_value(c) for c in range(16)]
+    assert vals[:8] == E2M1_MAGNITUDES
+    assert vals[8:] == [-m for m in E2M1_MAGNITUDES]
+    assert np.signbit(vals[8])  # pattern 8 is -0
+
+
+def test_fp4_dequant_and_gemv_match_numpy():
+    codes, scales = synth.make_fp4_case(4300, 8, 384)
+    table = np.array(E2M1_MAGNITUDES + [-m for m in E2M1_MAGNITUDES], dtype=np.float32)
+    s32 = np.repeat(scales.view(np.float16).astype(np.float32), 128, axis=1)[:, :384]
+    w = table[codes.astype(np.int64)] * s32  # exact in FP32
+    import torch
+    want = torch.from_numpy(w).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.rans_dequant_bf16(codes, scales, values="fp4"), want)
+    x = synth.make_x(4301, 3, 384)
+    xf = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    y, a = O.gemv_rans(codes, scales, x, values="fp4")
+    assert np.allclose(y, xf @ w.astype(np.float64).T, rtol=1e-12, atol=1e-12)
+    assert np.allclose(a, np.abs(xf[:, None, :] * w.astype(np.float64)[None]).sum(-1), rtol=1e-12, atol=1e-12)
+    # the integer reading of the same patterns differs (a dropped mode would not)
+    assert not np.array_equal(O.rans_dequant_bf16(codes - 8, scales), want)
+
+
 # ---------------------------------------------------------------- pair symbols
 @pytest.mark.parametrize("n", [0, 64, 4096, 4160, 3 * 4096 + 1024])
 def test_pair_round_trip_and_final_states(n):
