@@ -720,7 +720,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", choices=PROFILE_CASES, help="run one named workload untimed (for ncu) and exit")
-    ap.add_argument("--batch", type=int, default=256, help="batch rows of --case gemm / bf16_gemm")
+    ap.add_argument("--batch", type=int, default=256, help="batch rows of --case gemm / bf16_gemm / mma")
     args = ap.parse_args()
     if args.case:
         return profile_case(args.case, args.batch)
