@@ -124,6 +124,7 @@ struct HuffMmaArgs {
     int sub_words;                      /* hierarchical sub-table words staged in shared memory */
 };
 
+/* ---- not in the Huffman GEMV: begin ---- */
 struct RansMat {
     const uint8_t* records;
     const uint32_t* tile_off;
@@ -147,6 +148,7 @@ struct RansArgs {
     const uint16_t* x;
     int* status;
 };
+/* ---- not in the Huffman GEMV: end ---- */
 
 /* An FP8 matrix: rANS tiles of top-t table symbols plus per-tile correction records. */
 struct Fp8Mat {
@@ -2991,6 +2993,7 @@ HuffMat huff_desc(const ec_matrix* W) {
     return m;
 }
 
+/* ---- not in the Huffman GEMV: begin ---- */
 RansMat rans_desc(const ec_matrix* W) {
     RansMat m{};
     const ec_blob_header& h = W->hdr;
@@ -3014,6 +3017,7 @@ RansMat rans_desc(const ec_matrix* W) {
     m.values = h.rans_values;
     return m;
 }
+/* ---- not in the Huffman GEMV: end ---- */
 
 Fp8Mat fp8_desc(const ec_matrix* W) {
     Fp8Mat m{};
