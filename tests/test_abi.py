@@ -573,6 +573,11 @@ def test_gemv_path_dispatch(ec):
     Wy = ec.encode_bf16(synth.llama_bf16(3403, 8, 14336), device=-1)  # automatic tiles: 32 steps, inside rows
     assert ec.gemv_path(Wy, 16) == "tensor_cores"
     assert ec.gemv_path([Wy, Wx], 16) == "cuda_cores"  # one matrix without the layout: the whole group
+    # tiles inside rows but too wide for the tensor-core kernel's staging pools (31 rows of
+    # 8192-weight tiles): CUDA cores
+    Ww = ec.encode_bf16(synth.llama_bf16(3404, 64, 8192), tile_steps=256, device=-1)
+    assert parse(Ww.serialize())[0]["k_pad"] % (32 * 256) == 0
+    assert ec.gemv_path(Ww, 16) == "cuda_cores"
     R = ec.encode_rans(*synth.make_rans_case(0, 8, 4096), device=-1)
     assert ec.gemv_path(R, 16) == "cuda_cores"
     hs = (ctypes.c_void_p * 2)(W.handle.value, R.handle.value)
